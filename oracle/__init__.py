@@ -1,0 +1,168 @@
+"""Float64 CPU oracle of the speculative-sampling verify step.
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference legs of ``bench.py`` are the only callers.  The
+product (the CUDA library and its binding) never imports this package.
+
+The arithmetic lives in ``sv_oracle.c`` (plain C, double precision); this
+module compiles it with gcc and marshals numpy arrays through ctypes.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(HERE, "sv_oracle.c")
+LIBRARY = os.path.join(HERE, "liboracle.so")
+
+DTYPES = {"f32": 0, "bf16": 1, "f64": 2}
+SEQ_BAD_TOKEN = 1
+SEQ_BAD_VALUE = 2
+
+_lock = threading.Lock()
+
+
+def compile_library(source: str = SOURCE, out: str = LIBRARY) -> str:
+    """Compile the oracle with gcc.  FMA contraction is off so that x86 and
+    aarch64 hosts round identically."""
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
+           "-fPIC", "-shared", "-o", tmp, source, "-lm", "-lpthread"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def build() -> str:
+    return compile_library()
+
+
+def _stale(lib: str, src: str) -> bool:
+    return (not os.path.exists(lib)) or os.path.getmtime(lib) < os.path.getmtime(src)
+
+
+def _as_logits(x, dtype: str) -> np.ndarray:
+    """Raw logits as a C-contiguous numpy array of the oracle's storage type.
+    bf16 is passed as its uint16 bit pattern."""
+    if hasattr(x, "detach"):  # torch tensor
+        import torch
+        t = x.detach().to("cpu").contiguous()
+        if dtype == "bf16":
+            assert t.dtype == torch.bfloat16
+            return t.view(torch.int16).numpy().view(np.uint16)
+        x = t.numpy()
+    x = np.ascontiguousarray(x)
+    want = {"f32": np.float32, "bf16": np.uint16, "f64": np.float64}[dtype]
+    assert x.dtype == want, (x.dtype, dtype)
+    return x
+
+
+def _np(x, dt):
+    if x is None:
+        return None
+    if hasattr(x, "detach"):
+        x = x.detach().to("cpu").numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=dt))
+
+
+class Oracle:
+    """ctypes handle on one compiled oracle library."""
+
+    def __init__(self, lib_path: str | None = None):
+        if lib_path is None:
+            with _lock:
+                if _stale(LIBRARY, SOURCE):
+                    compile_library()
+            lib_path = LIBRARY
+        self.lib = ctypes.CDLL(lib_path)
+        P = ctypes.c_void_p
+        i = ctypes.c_int
+        self.lib.orc_verify.restype = i
+        self.lib.orc_verify.argtypes = [P, P, i, P, P, P, i, i, i, i, P, P,
+                                        P, P, P, P, P, P, P, i]
+        self.lib.orc_softmax_row.restype = i
+        self.lib.orc_softmax_row.argtypes = [P, i, i, ctypes.c_double, P, P, P]
+
+    def verify(self, target, draft, draft_tokens, uniforms, temperature=None,
+               greedy=False, dtype="f32", threads=1, diagnostics=True):
+        """Run the verify step on B sequences.
+
+        target: [B, N+1, V] logits, draft: [B, N, V] logits (may be None when
+        greedy), draft_tokens: [B, N] int, uniforms: [B, N+1] (float32 values
+        are widened exactly), temperature: [B] or None when greedy.
+
+        Returns a dict of numpy arrays: out_tokens [B, N+1], num_accepted [B],
+        seq_status [B] and, with diagnostics, q_at_d / p_at_d [B, N],
+        tstats [B, N+1, 2], dstats [B, N, 2], accept_margin [B, N],
+        sample_margin [B].
+        """
+        tgt = _as_logits(target, dtype)
+        B, N1, V = tgt.shape
+        N = N1 - 1
+        drf = None if draft is None else _as_logits(draft, dtype)
+        if drf is not None:
+            assert drf.shape == (B, N, V), drf.shape
+        tok = _np(draft_tokens, np.int32)
+        if tok is None:
+            tok = np.zeros((B, N), np.int32)
+        assert tok.shape == (B, N)
+        u = _np(uniforms, np.float64)
+        assert u.shape == (B, N + 1)
+        T = _np(temperature, np.float64)
+        if T is not None:
+            assert T.shape == (B,)
+        out = np.full((B, N + 1), -7, np.int32)
+        acc = np.full((B,), -7, np.int32)
+        st = np.zeros((B,), np.int32)
+        res = {"out_tokens": out, "num_accepted": acc, "seq_status": st}
+        if diagnostics:
+            res.update(
+                q_at_d=np.full((B, N), np.nan), p_at_d=np.full((B, N), np.nan),
+                tstats=np.full((B, N + 1, 2), np.nan), dstats=np.full((B, N, 2), np.nan),
+                accept_margin=np.full((B, N), np.nan), sample_margin=np.full((B,), np.nan))
+
+        def ptr(a):
+            return None if a is None else a.ctypes.data
+
+        rc = self.lib.orc_verify(
+            ptr(tgt), ptr(drf), DTYPES[dtype], ptr(tok), ptr(u), ptr(T),
+            int(bool(greedy)), B, N, V, ptr(out), ptr(acc),
+            ptr(res.get("q_at_d")), ptr(res.get("p_at_d")),
+            ptr(res.get("tstats")), ptr(res.get("dstats")),
+            ptr(res.get("accept_margin")), ptr(res.get("sample_margin")),
+            ptr(st), int(threads))
+        if rc != 0:
+            raise ValueError("oracle rejected its arguments")
+        return res
+
+    def softmax_row(self, row, T, dtype="f64"):
+        """softmax(row / T) with its normaliser (m, S)."""
+        z = _as_logits(row, dtype)
+        V = z.shape[0]
+        probs = np.empty(V, np.float64)
+        m = ctypes.c_double()
+        S = ctypes.c_double()
+        rc = self.lib.orc_softmax_row(z.ctypes.data, DTYPES[dtype], V, float(T),
+                                      probs.ctypes.data, ctypes.byref(m), ctypes.byref(S))
+        if rc != 0:
+            raise ValueError("bad softmax arguments")
+        return probs, m.value, S.value
+
+
+_default: Oracle | None = None
+
+
+def default() -> Oracle:
+    global _default
+    if _default is None:
+        _default = Oracle()
+    return _default
+
+
+def verify(*args, **kwargs):
+    return default().verify(*args, **kwargs)

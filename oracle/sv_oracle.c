@@ -1,0 +1,435 @@
+/*
+ * sv_oracle.c -- float64 CPU oracle of the speculative-sampling verify step.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the slow, plain reference that the
+ * CUDA path is checked against.  Only the tests, the smoke check and the
+ * benchmark's CPU-baseline / reference legs may load it.  It shares no code,
+ * header, table or helper with the CUDA library.
+ *
+ * What it computes (per sequence b), following
+ *   "Speculative decoding -- draft, verify, repeat" (factory.pai-world.com,
+ *    lesson 07-16), section "Core algorithm", steps 2-6, and its build
+ *    section, Step 1 (rejection step), Step 2 (residual distribution) and
+ *    Step 3 (one speculative step):
+ *
+ *   q_i = softmax(zq[b,i,:] / T)   verifier distribution, i = 0..N
+ *   p_i = softmax(zp[b,i,:] / T)   draft distribution,    i = 0..N-1
+ *   for i = 0..N-1 (left to right):
+ *       accept d_i  iff  p_i(d_i) == 0  or  u[b,i] < min(1, q_i(d_i)/p_i(d_i))
+ *   first rejection at j: sample t from normalise(max(0, q_j - p_j))
+ *   no rejection (j = N):  sample the bonus token t from q_N
+ *   emit d_0..d_{j-1}, t ;  num_accepted = j
+ *
+ * Readings taken where the pages are silent (each is listed in the design doc):
+ *   - softmax is evaluated in its max-subtracted form, with plain
+ *     left-to-right summation in double;
+ *   - temperature divides both the target and the draft logits;
+ *   - the comparison is strict (u < ratio), and p_i(d_i) == 0 accepts
+ *     (the rejection-step listing maps a zero draft probability to an
+ *     infinite ratio);
+ *   - `sample` is the inverse CDF in ascending token order against one
+ *     uniform u[b,N]: t = smallest k with u*R < C_k, C_k = r_0+...+r_k,
+ *     R = C_{V-1}; if rounding leaves no such k, t = largest k with r_k > 0;
+ *   - a residual of total mass 0 (q_j == p_j) samples from q_j instead;
+ *   - greedy sequences (greedy flag, or T <= 0): a_i = argmax_k zq[b,i,k]
+ *     with the lowest index on ties; accept d_i iff d_i == a_i; emit a_j at
+ *     the first mismatch, else the bonus a_N;
+ *   - a row is invalid if it holds a NaN or +inf logit or only -inf logits;
+ *     a temperature that is NaN, +inf or in (0, FLT_MIN) is invalid; a draft
+ *     token outside [0, V) is invalid.  An invalid sequence emits -1 in every
+ *     slot and num_accepted = -1.  Every row the method reads is checked:
+ *     all 2N+1 rows of a sampled sequence, the N+1 target rows of a greedy
+ *     one.
+ *
+ * Decision margins (reported so that tests can tell rounding-sensitive
+ * decisions apart): for an accept test with ratio < 1 the margin is
+ * |u_i - ratio|, otherwise +inf; for the final sample it is the distance
+ * from u[b,N] to the nearer edge of the chosen token's CDF interval,
+ * min(|u - C_{t-1}/R|, |u - C_t/R|).  Greedy decisions have margin +inf.
+ */
+#include <float.h>
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_F32 0
+#define ORC_BF16 1
+#define ORC_F64 2
+
+#define ORC_SEQ_BAD_TOKEN 1
+#define ORC_SEQ_BAD_VALUE 2
+
+/* One logit, upcast exactly to double.  bf16 is the top half of an IEEE
+ * binary32 word, so shifting its 16 bits up by 16 gives the same value. */
+static double orc_logit(const void *base, int dtype, size_t idx)
+{
+    if (dtype == ORC_F64)
+        return ((const double *)base)[idx];
+    if (dtype == ORC_F32)
+        return (double)((const float *)base)[idx];
+    uint32_t bits = (uint32_t)((const uint16_t *)base)[idx] << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+/* Row validity as defined above: no NaN, no +inf, at least one finite value
+ * (a row of only -inf has no distribution). */
+static int orc_row_valid(const void *base, int dtype, size_t off, int V)
+{
+    int any_finite = 0;
+    for (int k = 0; k < V; k++) {
+        double z = orc_logit(base, dtype, off + (size_t)k);
+        if (isnan(z) || z == INFINITY)
+            return 0;
+        if (z != -INFINITY)
+            any_finite = 1;
+    }
+    return any_finite;
+}
+
+/* Normaliser of softmax(z / T): m = max_k z_k and S = sum_k exp((z_k - m)/T),
+ * summed left to right.  Then softmax(z/T)_k = exp((z_k - m)/T) / S. */
+static void orc_row_normaliser(const void *base, int dtype, size_t off, int V,
+                               double T, double *m_out, double *S_out)
+{
+    double m = -INFINITY;
+    for (int k = 0; k < V; k++) {
+        double z = orc_logit(base, dtype, off + (size_t)k);
+        if (z > m)
+            m = z;
+    }
+    double S = 0.0;
+    for (int k = 0; k < V; k++) {
+        double z = orc_logit(base, dtype, off + (size_t)k);
+        S += exp((z - m) / T);
+    }
+    *m_out = m;
+    *S_out = S;
+}
+
+static double orc_prob(double z, double m, double S, double T)
+{
+    return exp((z - m) / T) / S;
+}
+
+/* argmax with the lowest index on ties, compared on the stored values. */
+static int orc_argmax(const void *base, int dtype, size_t off, int V)
+{
+    int best = 0;
+    double best_z = orc_logit(base, dtype, off);
+    for (int k = 1; k < V; k++) {
+        double z = orc_logit(base, dtype, off + (size_t)k);
+        if (z > best_z) {
+            best_z = z;
+            best = k;
+        }
+    }
+    return best;
+}
+
+/* Inverse CDF of the (unnormalised) mass r[0..V-1] against u in [0,1):
+ * t = smallest k with u*R < C_k where C_k = r_0 + ... + r_k, R = C_{V-1}.
+ * Writes the margin min(|u - C_{t-1}/R|, |u - C_t/R|). */
+static int orc_inverse_cdf(const double *r, int V, double u, double *margin)
+{
+    double R = 0.0;
+    for (int k = 0; k < V; k++)
+        R += r[k];
+    double x = u * R;
+    double C_prev = 0.0, C = 0.0;
+    int t = -1;
+    for (int k = 0; k < V; k++) {
+        C_prev = C;
+        C += r[k];
+        if (x < C) {
+            t = k;
+            break;
+        }
+    }
+    if (t < 0) {
+        /* rounding left u*R at or above the last cumulative value: take the
+         * last token that carries mass, and report the distance to 1. */
+        for (int k = V - 1; k >= 0; k--) {
+            if (r[k] > 0.0) {
+                t = k;
+                break;
+            }
+        }
+        if (t < 0)
+            t = V - 1; /* all-zero mass: cannot happen for a valid row */
+        *margin = fabs(u - 1.0);
+        return t;
+    }
+    double lo = fabs(u - C_prev / R), hi = fabs(u - C / R);
+    *margin = lo < hi ? lo : hi;
+    return t;
+}
+
+typedef struct {
+    const void *target;          /* [B, N+1, V] */
+    const void *draft;           /* [B, N, V], may be NULL when greedy != 0 */
+    int dtype;
+    const int32_t *draft_tokens; /* [B, N] */
+    const double *u;             /* [B, N+1]: 0..N-1 accept tests, N sample */
+    const double *T;             /* [B], may be NULL when greedy != 0 */
+    int greedy;
+    int B, N, V;
+    int32_t *out_tokens;   /* [B, N+1] */
+    int32_t *num_accepted; /* [B] */
+    /* optional diagnostics (NULL to skip) */
+    double *q_at_d;        /* [B, N]   q_i(d_i) */
+    double *p_at_d;        /* [B, N]   p_i(d_i) */
+    double *tstats;        /* [B, N+1, 2]  (m, S) of target rows */
+    double *dstats;        /* [B, N, 2]    (m, S) of draft rows */
+    double *accept_margin; /* [B, N]   NaN where not evaluated */
+    double *sample_margin; /* [B] */
+    int32_t *seq_status;   /* [B]  0, or ORC_SEQ_* bits */
+} orc_args;
+
+static void orc_fill_invalid(const orc_args *a, int b)
+{
+    for (int i = 0; i <= a->N; i++)
+        a->out_tokens[(size_t)b * (a->N + 1) + i] = -1;
+    a->num_accepted[b] = -1;
+}
+
+static void orc_verify_sequence(const orc_args *a, int b, double *r)
+{
+    const int N = a->N, V = a->V;
+    const size_t trow0 = (size_t)b * (N + 1); /* first target row of b */
+    const size_t drow0 = (size_t)b * N;       /* first draft row of b  */
+    int status = 0;
+
+    if (a->accept_margin)
+        for (int i = 0; i < N; i++)
+            a->accept_margin[drow0 + i] = NAN;
+    if (a->sample_margin)
+        a->sample_margin[b] = NAN;
+
+    for (int i = 0; i < N; i++) {
+        int32_t d = a->draft_tokens[drow0 + i];
+        if (d < 0 || d >= V)
+            status |= ORC_SEQ_BAD_TOKEN;
+    }
+
+    int greedy = a->greedy != 0;
+    double T = 0.0;
+    if (!greedy) {
+        T = a->T[b];
+        if (isnan(T))
+            status |= ORC_SEQ_BAD_VALUE;
+        else if (T <= 0.0)
+            greedy = 1;
+        else if (T == INFINITY || T < (double)FLT_MIN)
+            status |= ORC_SEQ_BAD_VALUE;
+    }
+
+    for (int i = 0; i <= N; i++)
+        if (!orc_row_valid(a->target, a->dtype, (trow0 + i) * (size_t)V, V))
+            status |= ORC_SEQ_BAD_VALUE;
+    if (!greedy)
+        for (int i = 0; i < N; i++)
+            if (!orc_row_valid(a->draft, a->dtype, (drow0 + i) * (size_t)V, V))
+                status |= ORC_SEQ_BAD_VALUE;
+
+    if (a->seq_status)
+        a->seq_status[b] = status;
+    if (status) {
+        orc_fill_invalid(a, b);
+        return;
+    }
+
+    int32_t *out = a->out_tokens + trow0;
+    for (int i = 0; i <= N; i++)
+        out[i] = -1;
+
+    if (greedy) {
+        int j = N;
+        for (int i = 0; i < N; i++) {
+            int ai = orc_argmax(a->target, a->dtype, (trow0 + i) * (size_t)V, V);
+            if (a->draft_tokens[drow0 + i] != ai) {
+                j = i;
+                out[i] = ai;
+                break;
+            }
+            out[i] = a->draft_tokens[drow0 + i];
+            if (a->accept_margin)
+                a->accept_margin[drow0 + i] = INFINITY;
+        }
+        if (j < N && a->accept_margin)
+            a->accept_margin[drow0 + j] = INFINITY;
+        if (j == N)
+            out[N] = orc_argmax(a->target, a->dtype, (trow0 + N) * (size_t)V, V);
+        a->num_accepted[b] = j;
+        if (a->sample_margin)
+            a->sample_margin[b] = INFINITY;
+        return;
+    }
+
+    /* Normalisers of every row the method reads. */
+    double *mq = (double *)malloc(sizeof(double) * 2 * (size_t)(N + 1));
+    double *Sq = mq + (N + 1);
+    double *mp = (double *)malloc(sizeof(double) * 2 * (size_t)(N + 1));
+    double *Sp = mp + (N + 1);
+    for (int i = 0; i <= N; i++) {
+        orc_row_normaliser(a->target, a->dtype, (trow0 + i) * (size_t)V, V, T, &mq[i], &Sq[i]);
+        if (a->tstats) {
+            a->tstats[(trow0 + i) * 2 + 0] = mq[i];
+            a->tstats[(trow0 + i) * 2 + 1] = Sq[i];
+        }
+    }
+    for (int i = 0; i < N; i++) {
+        orc_row_normaliser(a->draft, a->dtype, (drow0 + i) * (size_t)V, V, T, &mp[i], &Sp[i]);
+        if (a->dstats) {
+            a->dstats[(drow0 + i) * 2 + 0] = mp[i];
+            a->dstats[(drow0 + i) * 2 + 1] = Sp[i];
+        }
+    }
+
+    /* q_i(d_i) and p_i(d_i) at every draft position. */
+    for (int i = 0; i < N; i++) {
+        int32_t d = a->draft_tokens[drow0 + i];
+        double qd = orc_prob(orc_logit(a->target, a->dtype, (trow0 + i) * (size_t)V + d), mq[i], Sq[i], T);
+        double pd = orc_prob(orc_logit(a->draft, a->dtype, (drow0 + i) * (size_t)V + d), mp[i], Sp[i], T);
+        if (a->q_at_d)
+            a->q_at_d[drow0 + i] = qd;
+        if (a->p_at_d)
+            a->p_at_d[drow0 + i] = pd;
+    }
+
+    /* Left-to-right accept scan; stop at the first rejection j. */
+    int j = N;
+    for (int i = 0; i < N; i++) {
+        int32_t d = a->draft_tokens[drow0 + i];
+        double qd = orc_prob(orc_logit(a->target, a->dtype, (trow0 + i) * (size_t)V + d), mq[i], Sq[i], T);
+        double pd = orc_prob(orc_logit(a->draft, a->dtype, (drow0 + i) * (size_t)V + d), mp[i], Sp[i], T);
+        double ui = a->u[trow0 + i];
+        int accept;
+        double margin = INFINITY;
+        if (pd == 0.0) {
+            accept = 1;
+        } else {
+            double ratio = qd / pd;
+            double thresh = ratio < 1.0 ? ratio : 1.0;
+            accept = ui < thresh;
+            if (ratio < 1.0)
+                margin = fabs(ui - ratio);
+        }
+        if (a->accept_margin)
+            a->accept_margin[drow0 + i] = margin;
+        if (!accept) {
+            j = i;
+            break;
+        }
+        out[i] = d;
+    }
+
+    /* Mass to sample from: the residual (q_j - p_j)_+ at a rejection, q_N
+     * for the bonus token. */
+    if (j < N) {
+        size_t toff = (trow0 + j) * (size_t)V, doff = (drow0 + j) * (size_t)V;
+        double R = 0.0;
+        for (int k = 0; k < V; k++) {
+            double qk = orc_prob(orc_logit(a->target, a->dtype, toff + k), mq[j], Sq[j], T);
+            double pk = orc_prob(orc_logit(a->draft, a->dtype, doff + k), mp[j], Sp[j], T);
+            double diff = qk - pk;
+            r[k] = diff > 0.0 ? diff : 0.0;
+            R += r[k];
+        }
+        if (R == 0.0) /* q_j == p_j: the rejection had probability 0 */
+            for (int k = 0; k < V; k++)
+                r[k] = orc_prob(orc_logit(a->target, a->dtype, toff + k), mq[j], Sq[j], T);
+    } else {
+        size_t toff = (trow0 + N) * (size_t)V;
+        for (int k = 0; k < V; k++)
+            r[k] = orc_prob(orc_logit(a->target, a->dtype, toff + k), mq[N], Sq[N], T);
+    }
+    double smargin;
+    out[j] = orc_inverse_cdf(r, V, a->u[trow0 + N], &smargin);
+    if (a->sample_margin)
+        a->sample_margin[b] = smargin;
+    a->num_accepted[b] = j;
+
+    free(mq);
+    free(mp);
+}
+
+typedef struct {
+    const orc_args *a;
+    int b0, b1;
+} orc_range;
+
+static void *orc_worker(void *arg)
+{
+    orc_range *rg = (orc_range *)arg;
+    double *r = (double *)malloc(sizeof(double) * (size_t)rg->a->V);
+    for (int b = rg->b0; b < rg->b1; b++)
+        orc_verify_sequence(rg->a, b, r);
+    free(r);
+    return NULL;
+}
+
+/*
+ * Batched entry point.  Returns 0, or -1 on a bad argument.  nthreads <= 1
+ * runs on the calling thread; otherwise sequences are split into nthreads
+ * contiguous ranges, one POSIX thread each.
+ */
+int orc_verify(const void *target, const void *draft, int dtype,
+               const int32_t *draft_tokens, const double *u, const double *T,
+               int greedy, int B, int N, int V,
+               int32_t *out_tokens, int32_t *num_accepted,
+               double *q_at_d, double *p_at_d, double *tstats, double *dstats,
+               double *accept_margin, double *sample_margin,
+               int32_t *seq_status, int nthreads)
+{
+    if (B < 0 || N < 0 || V < 1 || !target || !out_tokens || !num_accepted || !u)
+        return -1;
+    if (N > 0 && !draft_tokens)
+        return -1;
+    if (!greedy && (!T || (N > 0 && !draft)))
+        return -1;
+    if (dtype != ORC_F32 && dtype != ORC_BF16 && dtype != ORC_F64)
+        return -1;
+    orc_args a = {target, draft, dtype, draft_tokens, u, T, greedy, B, N, V,
+                  out_tokens, num_accepted, q_at_d, p_at_d, tstats, dstats,
+                  accept_margin, sample_margin, seq_status};
+    if (nthreads <= 1 || B <= 1) {
+        orc_range rg = {&a, 0, B};
+        orc_worker(&rg);
+        return 0;
+    }
+    if (nthreads > B)
+        nthreads = B;
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    orc_range *rg = (orc_range *)malloc(sizeof(orc_range) * (size_t)nthreads);
+    for (int t = 0; t < nthreads; t++) {
+        rg[t].a = &a;
+        rg[t].b0 = (int)((long long)B * t / nthreads);
+        rg[t].b1 = (int)((long long)B * (t + 1) / nthreads);
+        pthread_create(&th[t], NULL, orc_worker, &rg[t]);
+    }
+    for (int t = 0; t < nthreads; t++)
+        pthread_join(th[t], NULL);
+    free(th);
+    free(rg);
+    return 0;
+}
+
+/* Softmax(z/T) of one row, for the tests that pin the normaliser against a
+ * library routine. */
+int orc_softmax_row(const void *row, int dtype, int V, double T, double *probs,
+                    double *m_out, double *S_out)
+{
+    if (V < 1 || T <= 0.0)
+        return -1;
+    double m, S;
+    orc_row_normaliser(row, dtype, 0, V, T, &m, &S);
+    for (int k = 0; k < V; k++)
+        probs[k] = orc_prob(orc_logit(row, dtype, (size_t)k), m, S, T);
+    *m_out = m;
+    *S_out = S;
+    return 0;
+}

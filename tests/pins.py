@@ -1,0 +1,476 @@
+"""Pins of the oracle: checks against what the pages and the mathematics fix.
+
+Each ``pin_*`` takes an ``oracle.Oracle`` and raises AssertionError when the
+oracle disagrees.  The same battery runs against the real oracle
+(test_oracle_pins.py) and against copies with planted mistakes
+(test_oracle_mutants.py), which must each fail at least one pin.
+"""
+from __future__ import annotations
+
+import math
+import os
+
+import numpy as np
+from scipy.special import logsumexp, softmax
+
+import lawlib
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "worked_numbers.txt")
+NEG_INF = -np.inf
+
+
+def golden():
+    vals = {}
+    with open(GOLDEN) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            key, rest = line.split("=", 1)
+            parts = rest.split(";")
+            val = float(parts[0])
+            tol = float(parts[1]) if len(parts) > 1 else 0.0
+            vals[key.strip()] = (val, tol)
+    return vals
+
+
+def _log(p):
+    p = np.asarray(p, np.float64)
+    with np.errstate(divide="ignore"):
+        return np.log(p)
+
+
+def _fixed_positions(q, p, N):
+    """Context-free case: the same q and p at every position."""
+    zq = np.stack([_log(q)] * (N + 1))
+    zp = np.stack([_log(p)] * N) if N else np.zeros((0, len(q)))
+    return zq, zp
+
+
+def _alpha(q, p):
+    return float(np.minimum(np.asarray(q), np.asarray(p)).sum())
+
+
+# ---------------------------------------------------------------------------
+# Softmax normaliser against scipy
+# ---------------------------------------------------------------------------
+
+def pin_softmax_matches_scipy(orc):
+    rng = np.random.default_rng(11)
+    for V, T, scale in [(7, 1.0, 1.0), (64, 0.7, 3.0), (257, 2.5, 5.0), (1, 1.0, 1.0)]:
+        z = rng.normal(0.0, scale, V)
+        probs, m, S = orc.softmax_row(z, T, dtype="f64")
+        want = softmax(z / T)
+        assert np.allclose(probs, want, rtol=1e-13, atol=0), (V, T)
+        # log-normaliser: m/T + log S == logsumexp(z/T)
+        assert abs(m / T + math.log(S) - logsumexp(z / T)) < 1e-12
+    # end to end: the diagnostics q(d), p(d) and (m, S) of the batched call
+    B, N, V, T = 3, 2, 40, 0.8
+    zq = rng.normal(0, 2, (B, N + 1, V))
+    zp = rng.normal(0, 2, (B, N, V))
+    d = rng.integers(0, V, (B, N)).astype(np.int32)
+    u = np.full((B, N + 1), 0.5)
+    r = orc.verify(zq, zp, d, u, np.full(B, T), dtype="f64")
+    for b in range(B):
+        for i in range(N):
+            assert abs(r["q_at_d"][b, i] - softmax(zq[b, i] / T)[d[b, i]]) < 1e-14
+            assert abs(r["p_at_d"][b, i] - softmax(zp[b, i] / T)[d[b, i]]) < 1e-14
+        for i in range(N + 1):
+            m, S = r["tstats"][b, i]
+            assert m == zq[b, i].max()
+            assert abs(m / T + math.log(S) - logsumexp(zq[b, i] / T)) < 1e-12
+
+
+# ---------------------------------------------------------------------------
+# Exact law: output distribution equals ancestral sampling from q
+# ---------------------------------------------------------------------------
+
+def _check_law(law, zq, zp, T, tol=1e-10):
+    N = zq.shape[0] - 1
+    q = lawlib.target_dists(zq, T)
+    p = lawlib.draft_dists(zp, T)
+    total = sum(law.values())
+    assert abs(total - 1.0) < tol, total
+    for s in law:
+        assert 1 <= len(s) <= N + 1
+    for k in range(N + 1):
+        # joint over (accepted prefix x of length k, next emitted token y)
+        joint = {}
+        for s, pr in law.items():
+            if len(s) >= k + 1:
+                joint.setdefault(s[:k], np.zeros(len(q[k])))[s[k]] += pr
+        for x, row in joint.items():
+            mass = row.sum()
+            # P(first k tokens are the accepted drafts x) = prod min(p_i, q_i)
+            want_mass = 1.0
+            for i in range(k):
+                want_mass *= min(p[i][x[i]], q[i][x[i]])
+            assert abs(mass - want_mass) < tol, (k, x, mass, want_mass)
+            if mass > 1e-9:
+                assert np.allclose(row / mass, q[k], atol=tol / mass, rtol=0), (k, x, row / mass, q[k])
+
+
+def pin_exact_law_small(orc):
+    """Every draft tuple, every uniform: V <= 4, N <= 2, random q_i, p_i."""
+    rng = np.random.default_rng(5)
+    cases = [(3, 2, 1.0), (4, 1, 0.7), (2, 2, 1.3), (4, 2, 1.0)]
+    for V, N, T in cases:
+        zq = rng.normal(0, 1.5, (N + 1, V))
+        zp = rng.normal(0, 1.5, (N, V))
+        law = lawlib.exact_law(orc, zq, zp, T)
+        _check_law(law, zq, zp, T)
+
+
+def pin_exact_law_with_zero_mass(orc):
+    """Tokens with zero probability on either side (-inf logits)."""
+    zq = np.array([[0.0, -np.inf, 1.0, 0.5], [0.3, 0.2, -np.inf, -np.inf], [0.0, 0.0, 0.0, 0.0]])
+    zp = np.array([[1.0, 0.0, -np.inf, 0.2], [-np.inf, 0.0, 0.0, 2.0]])
+    law = lawlib.exact_law(orc, zq, zp, 1.0)
+    _check_law(law, zq, zp, 1.0)
+    for s in law:
+        # a token the verifier gives zero mass is never emitted
+        for k, t in enumerate(s):
+            assert np.isfinite(zq[k][t]), s
+
+
+# ---------------------------------------------------------------------------
+# Worked numbers from the pages
+# ---------------------------------------------------------------------------
+
+def pin_worked_accept_probability(orc):
+    g = golden()
+    want, tol = g["accept_prob.draft0.9.verifier0.45"]
+    q = np.array([0.45, 0.55])
+    p = np.array([0.9, 0.1])
+    bb = lawlib.BlackBox(orc, _log([q, q]), _log([p]), 1.0)
+    edge = lawlib._accept_edge(bb, [0], 0)
+    assert abs(edge - want) < tol, edge
+
+
+def pin_worked_tokens_per_call(orc):
+    g = golden()
+    q, p = np.array([0.75, 0.25]), np.array([0.5, 0.5])  # alpha = 0.75
+    assert abs(_alpha(q, p) - 0.75) < 1e-15
+    zq, zp = _fixed_positions(q, p, 5)
+    law = lawlib.exact_law(orc, zq, zp)
+    e = lawlib.expected_tokens(law)
+    want, tol = g["tokens_per_call.a0.75.N5"]
+    assert abs(e - want) < tol, e
+    rounded, rtol = g["tokens_per_call.a0.75.N5.page_rounded"]
+    assert abs(e - rounded) < rtol
+
+
+def pin_worked_survival(orc):
+    g = golden()
+    q, p = np.array([0.8, 0.2]), np.array([0.5, 0.5])  # alpha = 0.7
+    N = 4
+    zq, zp = _fixed_positions(q, p, N)
+    law = lawlib.exact_law(orc, zq, zp)
+    for k in range(1, N + 1):
+        surv = sum(pr for s, pr in law.items() if len(s) - 1 >= k)
+        assert abs(surv - 0.7 ** k) < 1e-10, (k, surv)
+        want, tol = g[f"survival.a0.7.k{k}"]
+        assert abs(surv - want) < tol, (k, surv, want)
+
+
+def pin_worked_ten_drafts(orc):
+    """alpha = 0.7 and ten drafts: three or four tokens per round (page 4)."""
+    g = golden()
+    q, p = np.array([0.8, 0.2]), np.array([0.5, 0.5])
+    N = 10
+    B = 40000
+    zq, zp = _fixed_positions(q, p, N)
+    rng = np.random.default_rng(3)
+    d = (rng.random((B, N)) >= 0.5).astype(np.int32)  # d_i ~ p = (0.5, 0.5)
+    u = rng.random((B, N + 1))
+    r = orc.verify(np.broadcast_to(zq, (B,) + zq.shape).copy(),
+                   np.broadcast_to(zp, (B,) + zp.shape).copy(), d, u, np.ones(B),
+                   dtype="f64", diagnostics=False)
+    mean = float((r["num_accepted"] + 1).mean())
+    closed = (1 - 0.7 ** (N + 1)) / 0.3
+    sd = float((r["num_accepted"] + 1).std()) / math.sqrt(B)
+    assert abs(mean - closed) < 4 * sd, (mean, closed, sd)
+    assert g["emitted.a0.7.N10.low"][0] <= mean <= g["emitted.a0.7.N10.high"][0]
+
+
+def pin_worked_alpha_0_4(orc):
+    g = golden()
+    q, p = np.array([0.8, 0.2]), np.array([0.2, 0.8])  # alpha = 0.4
+    e = {}
+    for N in (3, 7):
+        zq, zp = _fixed_positions(q, p, N)
+        e[N] = lawlib.expected_tokens(lawlib.exact_law(orc, zq, zp))
+        closed = (1 - 0.4 ** (N + 1)) / 0.6
+        assert abs(e[N] - closed) < 1e-9, (N, e[N], closed)
+    assert e[7] / e[3] <= g["tokens_per_call.a0.4.N7_over_N3.max"][0]
+
+
+def pin_worked_all_accepted(orc):
+    """p == q at every draft position: all N accepted and a bonus, N + 1 tokens."""
+    g = golden()
+    rng = np.random.default_rng(8)
+    N, V, B = 5, 9, 200
+    zq = rng.normal(0, 2, (B, N + 1, V))
+    zp = zq[:, :N].copy()
+    d = rng.integers(0, V, (B, N)).astype(np.int32)
+    u = rng.random((B, N + 1))
+    u[:, 0] = np.nextafter(1.0, 0.0)  # even the largest uniform accepts
+    r = orc.verify(zq, zp, d, u, np.full(B, 0.9), dtype="f64")
+    assert (r["num_accepted"] == N).all()
+    assert ((r["out_tokens"] >= 0).sum(axis=1) == g["all_accepted.N5.tokens"][0]).all()
+    assert (r["out_tokens"][:, :N] == d).all()
+
+
+def pin_tokens_per_call_range(orc):
+    g = golden()
+    rng = np.random.default_rng(9)
+    B, N, V = 500, 4, 12
+    zq = rng.normal(0, 2, (B, N + 1, V))
+    zp = rng.normal(0, 2, (B, N, V))
+    d = rng.integers(0, V, (B, N)).astype(np.int32)
+    u = rng.random((B, N + 1))
+    r = orc.verify(zq, zp, d, u, np.full(B, 1.0), dtype="f64")
+    n_emit = (r["out_tokens"] >= 0).sum(axis=1)
+    assert (n_emit >= g["tokens_per_call.min"][0]).all()
+    assert (n_emit <= N + g["tokens_per_call.max_minus_N"][0]).all()
+    assert (n_emit == r["num_accepted"] + 1).all()
+    for b in range(B):
+        j = r["num_accepted"][b]
+        assert (r["out_tokens"][b, :j] == d[b, :j]).all()
+        assert (r["out_tokens"][b, j + 1:] == -1).all()
+
+
+# ---------------------------------------------------------------------------
+# Invariants and exact boundary semantics
+# ---------------------------------------------------------------------------
+
+def pin_disjoint_one_hot(orc):
+    """p one-hot on x, q one-hot on y != x: reject at the first position and
+    emit y (q(d) = 0 makes the ratio 0, and u < 0 never holds)."""
+    V, N = 6, 3
+    for x, y in [(0, 5), (4, 1), (2, 3)]:
+        zq = np.full((1, N + 1, V), NEG_INF)
+        zq[0, :, y] = 0.0
+        zp = np.full((1, N, V), NEG_INF)
+        zp[0, :, x] = 0.0
+        for u0 in (0.0, 0.3, np.nextafter(1.0, 0.0)):
+            u = np.array([[u0, 0.5, 0.5, 0.7]])
+            r = orc.verify(zq, zp, np.full((1, N), x, np.int32), u, np.ones(1), dtype="f64")
+            assert r["num_accepted"][0] == 0
+            assert list(r["out_tokens"][0]) == [y, -1, -1, -1]
+
+
+def pin_strict_comparison(orc):
+    """Exact ratio 0.5: u = 0.5 rejects, the next double below accepts."""
+    zq = np.zeros((1, 2, 4))                       # q = 1/4 each, exactly
+    zp = np.array([[[0.0, 0.0, NEG_INF, NEG_INF]]])  # p = (1/2, 1/2, 0, 0)
+    d = np.array([[0]], np.int32)
+    r = orc.verify(zq, zp, d, np.array([[0.5, 0.1]]), np.ones(1), dtype="f64")
+    assert r["num_accepted"][0] == 0
+    r = orc.verify(zq, zp, d, np.array([[np.nextafter(0.5, 0.0), 0.1]]), np.ones(1), dtype="f64")
+    assert r["num_accepted"][0] == 1
+
+
+def pin_inverse_cdf_edges(orc):
+    """Residual (q - p)_+ = (0, 0, 1/4, 1/4): u*R below 1/4 gives token 2,
+    exactly 1/4 gives token 3 (strict comparison with the cumulative)."""
+    zq = np.zeros((1, 2, 4))
+    zp = np.array([[[0.0, 0.0, NEG_INF, NEG_INF]]])
+    d = np.array([[0]], np.int32)
+    for uN, want in [(0.0, 2), (np.nextafter(0.5, 0.0), 2), (0.5, 3), (np.nextafter(1.0, 0.0), 3)]:
+        r = orc.verify(zq, zp, d, np.array([[0.75, uN]]), np.ones(1), dtype="f64")
+        assert r["num_accepted"][0] == 0
+        assert r["out_tokens"][0, 0] == want, (uN, r["out_tokens"][0])
+    # bonus from q_N: four equal quarters
+    for uN, want in [(0.0, 0), (0.25, 1), (np.nextafter(0.5, 0.0), 1), (0.5, 2), (0.75, 3)]:
+        r = orc.verify(zq, zp, d, np.array([[0.1, uN]]), np.ones(1), dtype="f64")
+        assert r["num_accepted"][0] == 1
+        assert r["out_tokens"][0, 1] == want, (uN, r["out_tokens"][0])
+
+
+def pin_zero_draft_probability_accepts(orc):
+    """p_i(d_i) == 0 accepts whatever the uniform (ratio taken as +inf)."""
+    zq = np.zeros((1, 2, 3))
+    zp = np.array([[[0.0, NEG_INF, 0.0]]])
+    for u0 in (0.0, 0.5, np.nextafter(1.0, 0.0)):
+        r = orc.verify(zq, zp, np.array([[1]], np.int32), np.array([[u0, 0.2]]), np.ones(1), dtype="f64")
+        assert r["num_accepted"][0] == 1, u0
+        assert r["out_tokens"][0, 0] == 1
+
+
+def pin_zero_residual_samples_q(orc):
+    """q_j == p_j and a forced rejection (u = 1): the residual has no mass and
+    the token is drawn from q_j itself."""
+    zq = np.log(np.array([[[0.1, 0.2, 0.3, 0.4]] * 2]))
+    zp = zq[:, :1].copy()
+    for uN, want in [(0.05, 0), (0.2, 1), (0.5, 2), (0.95, 3)]:
+        r = orc.verify(zq, zp, np.array([[2]], np.int32), np.array([[1.0, uN]]), np.ones(1), dtype="f64")
+        assert r["num_accepted"][0] == 0
+        assert r["out_tokens"][0, 0] == want, (uN, r["out_tokens"][0])
+
+
+def pin_accept_when_verifier_not_below(orc):
+    """q(d) >= p(d) always accepts (page 3 and page 4)."""
+    rng = np.random.default_rng(13)
+    B, N, V = 400, 3, 10
+    zq = rng.normal(0, 1.5, (B, N + 1, V))
+    zp = rng.normal(0, 1.5, (B, N, V))
+    d = rng.integers(0, V, (B, N)).astype(np.int32)
+    u = rng.random((B, N + 1))
+    r = orc.verify(zq, zp, d, u, np.full(B, 1.0), dtype="f64")
+    seen = 0
+    for b in range(B):
+        j = r["num_accepted"][b]
+        for i in range(min(j + 1, N)):
+            if r["q_at_d"][b, i] >= r["p_at_d"][b, i]:
+                assert i < j, (b, i, j)
+                seen += 1
+    assert seen > 50
+
+
+def pin_greedy_rule(orc):
+    """Greedy: accept while d_i is the argmax (lowest index on ties, as
+    numpy.argmax), emit the argmax at the first mismatch or as the bonus."""
+    rng = np.random.default_rng(17)
+    B, N, V = 300, 4, 7
+    zq = rng.integers(-2, 3, (B, N + 1, V)).astype(np.float64)  # many ties
+    a = zq.argmax(axis=2)
+    d = a[:, :N].copy().astype(np.int32)
+    flip = rng.random((B, N)) < 0.3
+    d[flip] = rng.integers(0, V, flip.sum())
+    u = rng.random((B, N + 1))
+    r = orc.verify(zq, None, d, u, None, greedy=True, dtype="f64")
+    for b in range(B):
+        j = 0
+        while j < N and d[b, j] == a[b, j]:
+            j += 1
+        assert r["num_accepted"][b] == j
+        assert list(r["out_tokens"][b, :j]) == list(d[b, :j])
+        assert r["out_tokens"][b, j] == a[b, j]
+    # per-sequence greedy through T <= 0
+    T = np.where(rng.random(B) < 0.5, 0.0, -1.0)
+    r2 = orc.verify(zq, np.zeros((B, N, V)), d, u, T, dtype="f64")
+    assert (r2["out_tokens"] == r["out_tokens"]).all()
+
+
+def pin_greedy_is_zero_temperature_limit(orc):
+    """With greedy drafts and well-separated logits, sampling at T -> 0 gives
+    the greedy output for any uniforms."""
+    rng = np.random.default_rng(19)
+    B, N, V = 200, 3, 12
+    # logits on a 0.05 grid without ties: exp(-0.05 / T) vanishes at T = 1e-4
+    zq = np.stack([np.stack([rng.permutation(V) * 0.05 for _ in range(N + 1)]) for _ in range(B)])
+    zp = np.stack([np.stack([rng.permutation(V) * 0.05 for _ in range(N)]) for _ in range(B)])
+    d = zp.argmax(axis=2).astype(np.int32)
+    same = rng.random((B, N)) < 0.6
+    zp[same] = zq[:, :N][same]  # make many drafts agree with the verifier
+    d = zp.argmax(axis=2).astype(np.int32)
+    u = rng.random((B, N + 1)) * 0.999
+    rs = orc.verify(zq, zp, d, u, np.full(B, 1e-4), dtype="f64")
+    rg = orc.verify(zq, zp, d, u, None, greedy=True, dtype="f64")
+    assert (rs["out_tokens"] == rg["out_tokens"]).all()
+    assert (rs["num_accepted"] == rg["num_accepted"]).all()
+    assert 0 < rg["num_accepted"].mean() < N
+
+
+def pin_temperature_divides(orc):
+    """softmax(z/T): temperature 2 on z equals temperature 1 on z/2."""
+    rng = np.random.default_rng(23)
+    B, N, V = 50, 2, 16
+    zq = rng.normal(0, 3, (B, N + 1, V))
+    zp = rng.normal(0, 3, (B, N, V))
+    d = rng.integers(0, V, (B, N)).astype(np.int32)
+    u = rng.random((B, N + 1))
+    r1 = orc.verify(zq, zp, d, u, np.full(B, 2.0), dtype="f64")
+    r2 = orc.verify(zq / 2.0, zp / 2.0, d, u, np.full(B, 1.0), dtype="f64")
+    assert np.allclose(r1["q_at_d"], r2["q_at_d"], rtol=1e-13)
+    assert np.allclose(r1["p_at_d"], r2["p_at_d"], rtol=1e-13)
+    assert np.allclose(r1["q_at_d"], [[softmax(zq[b, i] / 2.0)[d[b, i]] for i in range(N)] for b in range(B)],
+                       rtol=1e-13)
+
+
+def pin_invalid_inputs(orc):
+    """Out-of-range drafts and non-finite rows or temperatures give -1."""
+    rng = np.random.default_rng(29)
+    B, N, V = 8, 2, 5
+    zq = rng.normal(0, 1, (B, N + 1, V))
+    zp = rng.normal(0, 1, (B, N, V))
+    d = rng.integers(0, V, (B, N)).astype(np.int32)
+    T = np.ones(B)
+    d[0, 1] = V          # bad token
+    d[1, 0] = -1         # bad token
+    zq[2, 2, 3] = np.nan  # NaN in a target row
+    zp[3, 0, 0] = np.inf  # +inf in a draft row
+    zq[4, 1, :] = NEG_INF  # a row without mass
+    T[5] = np.nan
+    T[6] = np.inf
+    u = rng.random((B, N + 1))
+    r = orc.verify(zq, zp, d, u, T, dtype="f64")
+    for b in range(7):
+        assert r["num_accepted"][b] == -1 and (r["out_tokens"][b] == -1).all(), b
+        assert r["seq_status"][b] != 0
+    assert r["seq_status"][0] == 1 and r["seq_status"][1] == 1
+    assert r["seq_status"][2] == 2
+    assert r["num_accepted"][7] >= 0 and r["seq_status"][7] == 0
+
+
+def pin_degenerate_sizes(orc):
+    # V = 1: every distribution is the point mass on token 0
+    r = orc.verify(np.zeros((2, 4, 1)), np.zeros((2, 3, 1)), np.zeros((2, 3), np.int32),
+                   np.full((2, 4), 0.99), np.ones(2), dtype="f64")
+    assert (r["num_accepted"] == 3).all() and (r["out_tokens"] == 0).all()
+    # N = 0: only the bonus token, drawn from q_0 by inverse CDF
+    zq = np.log(np.array([[[0.5, 0.25, 0.25]]]))
+    for uN, want in [(0.1, 0), (0.6, 1), (0.8, 2)]:
+        r = orc.verify(zq, None, np.zeros((1, 0), np.int32), np.array([[uN]]), np.ones(1), dtype="f64")
+        assert r["num_accepted"][0] == 0 and r["out_tokens"][0, 0] == want
+    # B = 0
+    r = orc.verify(np.zeros((0, 3, 4)), np.zeros((0, 2, 4)), np.zeros((0, 2), np.int32),
+                   np.zeros((0, 3)), np.zeros(0), dtype="f64")
+    assert r["out_tokens"].shape == (0, 3)
+
+
+def pin_storage_types(orc):
+    """bf16 and float32 logits are widened exactly: same result as the
+    float64 copy of the same values."""
+    import torch
+    rng = np.random.default_rng(31)
+    B, N, V = 20, 3, 33
+    zq = torch.tensor(rng.normal(0, 3, (B, N + 1, V)), dtype=torch.float32)
+    zp = torch.tensor(rng.normal(0, 3, (B, N, V)), dtype=torch.float32)
+    d = rng.integers(0, V, (B, N)).astype(np.int32)
+    u = rng.random((B, N + 1)).astype(np.float32)
+    T = np.full(B, 0.8, np.float32)
+    for tdt, name in [(torch.float32, "f32"), (torch.bfloat16, "bf16")]:
+        a, b_ = zq.to(tdt), zp.to(tdt)
+        r = orc.verify(a, b_, d, u, T, dtype=name)
+        r64 = orc.verify(a.double().numpy(), b_.double().numpy(), d, u, T, dtype="f64")
+        for k in ("out_tokens", "num_accepted"):
+            assert (r[k] == r64[k]).all()
+        assert np.array_equal(r["q_at_d"], r64["q_at_d"])
+
+
+ALL_PINS = [
+    pin_softmax_matches_scipy,
+    pin_exact_law_small,
+    pin_exact_law_with_zero_mass,
+    pin_worked_accept_probability,
+    pin_worked_tokens_per_call,
+    pin_worked_survival,
+    pin_worked_ten_drafts,
+    pin_worked_alpha_0_4,
+    pin_worked_all_accepted,
+    pin_tokens_per_call_range,
+    pin_disjoint_one_hot,
+    pin_strict_comparison,
+    pin_inverse_cdf_edges,
+    pin_zero_draft_probability_accepts,
+    pin_zero_residual_samples_q,
+    pin_accept_when_verifier_not_below,
+    pin_greedy_rule,
+    pin_greedy_is_zero_temperature_limit,
+    pin_temperature_divides,
+    pin_invalid_inputs,
+    pin_degenerate_sizes,
+    pin_storage_types,
+]

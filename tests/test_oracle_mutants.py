@@ -1,0 +1,81 @@
+"""Plant plausible mistakes in copies of the oracle and check that the pins
+catch every one of them (CPU only).
+
+Each mutant is a single textual edit of sv_oracle.c (a flipped comparison, a
+wrong sign, an off-by-one index, a transposed operand ...).  The copy is
+compiled into a temporary directory; the real oracle is never touched.
+"""
+import os
+
+import pytest
+
+import oracle
+import pins
+
+MUTANTS = [
+    ("accept test not strict", "accept = ui < thresh;", "accept = ui <= thresh;"),
+    ("ratio inverted", "double ratio = qd / pd;", "double ratio = pd / qd;"),
+    ("zero draft probability rejects",
+     "if (pd == 0.0) {\n            accept = 1;", "if (pd == 0.0) {\n            accept = 0;"),
+    ("residual sign flipped", "double diff = qk - pk;", "double diff = pk - qk;"),
+    ("residual not clamped", "r[k] = diff > 0.0 ? diff : 0.0;", "r[k] = diff;"),
+    ("residual from the next position",
+     "size_t toff = (trow0 + j) * (size_t)V, doff = (drow0 + j) * (size_t)V;",
+     "size_t toff = (trow0 + j + 1) * (size_t)V, doff = (drow0 + j) * (size_t)V;"),
+    ("bonus from the last draft position",
+     "size_t toff = (trow0 + N) * (size_t)V;", "size_t toff = (trow0 + N - 1) * (size_t)V;"),
+    ("temperature multiplies",
+     "return exp((z - m) / T) / S;", "return exp((z - m) * T) / S;"),
+    ("normaliser without the max shift", "S += exp((z - m) / T);", "S += exp(z / T);"),
+    ("accept uniform off by one", "double ui = a->u[trow0 + i];", "double ui = a->u[trow0 + i + 1];"),
+    ("sample uses the first uniform",
+     "out[j] = orc_inverse_cdf(r, V, a->u[trow0 + N], &smargin);",
+     "out[j] = orc_inverse_cdf(r, V, a->u[trow0 + 0], &smargin);"),
+    ("inverse CDF not strict", "if (x < C) {", "if (x <= C) {"),
+    ("greedy ties to the highest index", "if (z > best_z) {", "if (z >= best_z) {"),
+    ("scan does not stop at the first rejection",
+     "if (!accept) {\n            j = i;\n            break;\n        }",
+     "if (!accept) {\n            j = i;\n        }"),
+    ("num_accepted counts the correction token",
+     "a->sample_margin[b] = smargin;\n    a->num_accepted[b] = j;",
+     "a->sample_margin[b] = smargin;\n    a->num_accepted[b] = j + 1;"),
+    ("draft probability read from the target row",
+     "double ui = a->u[trow0 + i];",
+     "double ui = a->u[trow0 + i]; pd = orc_prob(orc_logit(a->target, a->dtype, (trow0 + i) * (size_t)V + d), mq[i], Sq[i], T);"),
+    ("greedy emits the draft at a mismatch",
+     "j = i;\n                out[i] = ai;", "j = i;\n                out[i] = a->draft_tokens[drow0 + i];"),
+    ("R == 0 reading dropped (samples the empty residual)",
+     "if (R == 0.0) /* q_j == p_j: the rejection had probability 0 */",
+     "if (0) /* q_j == p_j: the rejection had probability 0 */"),
+    ("invalid rows not detected", "if (isnan(z) || z == INFINITY)\n            return 0;",
+     "if (0)\n            return 0;"),
+    ("bad draft tokens not detected", "if (d < 0 || d >= V)", "if (d < 0 || d > V)"),
+]
+
+
+def _mutant_source(old, new):
+    src = open(oracle.SOURCE).read()
+    assert src.count(old) == 1, f"anchor must occur exactly once: {old!r}"
+    return src.replace(old, new)
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_mutant(tmp_path, name, old, new):
+    src = tmp_path / "mutant.c"
+    src.write_text(_mutant_source(old, new))
+    lib = oracle.compile_library(str(src), str(tmp_path / "libmutant.so"))
+    orc = oracle.Oracle(lib)
+    caught = []
+    for pin in pins.ALL_PINS:
+        try:
+            pin(orc)
+        except Exception as e:  # an assertion, or a crash of the mutant's logic
+            caught.append(f"{pin.__name__}: {type(e).__name__}")
+    assert caught, f"no pin caught the mutant '{name}'"
+    print(f"{name}: caught by {len(caught)} pins, e.g. {caught[0]}")
+
+
+def test_anchors_are_unique():
+    for _, old, _ in MUTANTS:
+        _mutant_source(old, old)
+    assert os.path.exists(oracle.SOURCE)
