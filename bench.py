@@ -1,0 +1,361 @@
+"""Benchmark of the speculative-sampling verify step on GB300.
+
+One step = one verify call (one kernel launch) over the whole batch of the
+workload, inputs resident in HBM.  The default workload is the Qwen-vocabulary
+batch the roofline is reported on: B=256 sequences, N=7 drafts, V=151936,
+bf16 logits, T=0.8 (1.17 GB of logits per call, larger than L2, so no flush is
+needed between steps).
+
+Prints one JSON line.  `--impl reference` times the float64 CPU oracle on the
+host cores instead (a bounded sample of the same workload per step).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verified rows/s (B·(N+1) logit rows) and achieved HBM GB/s vs GB300 peak"
+UNIT = "rows/s"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["speculative_decoding_verification_49_gb300/csrc/spec_verify.cu",
+                  "speculative_decoding_verification_49_gb300/csrc/sv_device.cuh"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "sv_verify_kernel_traffic.txt")
+
+
+def kernel_digest() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    vals = {}
+    with open(TRAFFIC_FILE) as f:
+        for line in f:
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+    if vals.get("kernel_digest") != kernel_digest():
+        return None
+    v = vals.get(f"dram_bytes_per_launch[{workload}]")
+    return float(v) if v else None
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(self.idx)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k, v in enumerate(r[3]) if v.lower() == "active"})
+        loaded = [r for r in rows if r[2] > 0] or rows
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(r[2] for r in rows)}
+
+
+def dist_init(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        dist.init_process_group(backend=backend)
+        pg = dist
+    return world, rank, local, pg
+
+
+def workload_desc(w) -> str:
+    extra = {"headline": "T=0.8, Zipf prior (-1.1 ln rank) on odd sequences",
+             "stress": "T=1.0, 5% forced near-zero-q drafts",
+             "mixed": "T in {0,0.7,1} per sequence, sigma_q in [0.3,2]",
+             "small": "T=1.0, 10% spiky target rows",
+             "tiny": "T=1.0"}.get(w.name, "")
+    return f"{w.name}: B={w.B} N={w.N} V={w.V} {w.dtype} logits, {extra}"
+
+
+def cpu_oracle_rate(w, budget_s: float, threads: int):
+    """Time the oracle on a bounded sample of sequences; returns (rows/s,
+    sequences, seconds)."""
+    import numpy as np
+    import oracle
+    import torch
+    orc = oracle.Oracle()
+    probe = min(w.B, max(threads, 4))
+    sel = torch.arange(probe, device=w.target.device)
+    args = lambda s: (w.target[s].cpu(), w.draft[s].cpu(), w.draft_tokens[s].cpu(),
+                      w.uniforms[s].double().cpu(), w.temperature[s].double().cpu())
+    t0 = time.perf_counter()
+    orc.verify(*args(sel), dtype=w.dtype, threads=threads, diagnostics=False)
+    t_probe = time.perf_counter() - t0
+    n = int(min(w.B, max(probe, probe * budget_s / max(t_probe, 1e-6))))
+    n = max(threads, (n // threads) * threads) if n >= threads else n
+    n = min(n, w.B)
+    sel = torch.arange(n, device=w.target.device)
+    a = args(sel)
+    t0 = time.perf_counter()
+    orc.verify(*a, dtype=w.dtype, threads=threads, diagnostics=False)
+    dt = time.perf_counter() - t0
+    return n * (w.N + 1) / dt, n, dt
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import synth
+    full = synth.config(args.workload)
+    # a bounded sample of the workload: the first sequences of the same recipe
+    w = synth.make_workload(args.workload, seed=0, device="cpu", B=min(full["B"], 128))
+    threads = os.cpu_count() or 1
+    rates = []
+    n_used = 0
+    t_used = 0.0
+    for k in range(args.warmup + args.steps):
+        r, n, dt = cpu_oracle_rate(w, args.ref_budget, threads)
+        if k >= args.warmup:
+            rates.append(r)
+            n_used, t_used = n, dt
+    value = statistics.median(rates)
+    sample = (f"{n_used} of {full['B']} sequences ({n_used * (w.N + 1)} verified rows, "
+              f"{n_used * (2 * w.N + 1) * w.V * w.elt / 1e9:.3f} GB of logits) per step, {t_used:.1f} s")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * n_used * (w.N + 1) / value,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": workload_desc(w).replace(f"B={w.B}", f"B={full['B']}"), "B": full["B"],
+                   "N": w.N, "V": w.V, "sample_sequences": n_used},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+    world, rank, local, pg = dist_init(args)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import synth
+    import speculative_decoding_verification_49_gb300 as sv
+    from speculative_decoding_verification_49_gb300 import build as svbuild
+    svbuild.build()
+
+    w = synth.make_workload(args.workload, seed=rank, device=dev)
+    ctx = sv.SpecVerify(w.B, w.N, w.V, w.dtype, device=local)
+    if args.cluster:
+        ctx.set_cluster_size(args.cluster)
+    stream = torch.cuda.current_stream(dev)
+    out = torch.empty((w.B, w.N + 1), dtype=torch.int32, device=dev)
+    nacc = torch.empty((w.B,), dtype=torch.int32, device=dev)
+
+    def step():
+        ctx.run(w.target, w.draft, w.draft_tokens, w.uniforms, w.temperature, out_tokens=out,
+                num_accepted=nacc, stream=stream)
+
+    # self-check against the oracle on a few sequences (rank 0, untimed)
+    check = None
+    if rank == 0 and not args.no_check:
+        sys.path.insert(0, os.path.join(ROOT, "tests"))
+        import numpy as np
+        import parity
+        seqs = np.array(sorted({0, 1, w.B // 2, w.B - 1}))
+        rep = parity.compare(w, parity.run_gpu(ctx, w, seqs=seqs),
+                             parity.run_oracle(w, seqs=seqs, threads=os.cpu_count() or 1))
+        check = {"sequences": rep["sequences"], "exact": rep["exact"],
+                 "band_sequences": rep["band_sequences"], "q_rel_max": rep.get("q_rel_max"),
+                 "S_rel_max": rep.get("S_rel_max")}
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for _ in range(args.steps):
+            step()
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+    ms = start.elapsed_time(end)
+    if pg:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+        pg.barrier()
+    if ctx.status() != sv.SV_OK:
+        raise RuntimeError("device status set during the timed region")
+
+    ms_step = ms / args.steps
+    rows = w.verified_rows
+    value = rows * world * args.steps / (ms * 1e-3)
+    gbs = w.logit_bytes / (ms_step * 1e-3) / 1e9
+    peak, peak_kind = peaks()
+
+    # end to end through the C ABI: pinned host inputs copied in, outputs read back
+    e2e = None
+    if not args.no_e2e:
+        h = {k: getattr(w, k).cpu().pin_memory() for k in ("target", "draft", "draft_tokens", "uniforms",
+                                                           "temperature")}
+        d = {k: torch.empty_like(getattr(w, k)) for k in h}
+        ho = torch.empty((w.B, w.N + 1), dtype=torch.int32).pin_memory()
+        hn = torch.empty((w.B,), dtype=torch.int32).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in h.values())
+        d2h = ho.numel() * 4 + hn.numel() * 4
+
+        def e2e_step():
+            for k in h:
+                d[k].copy_(h[k], non_blocking=True)
+            ctx.run(d["target"], d["draft"], d["draft_tokens"], d["uniforms"], d["temperature"],
+                    out_tokens=out, num_accepted=nacc, stream=stream)
+            ho.copy_(out, non_blocking=True)
+            hn.copy_(nacc, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        if pg:
+            pg.barrier()
+        es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        k2 = max(1, min(args.steps, 20))
+        es.record(stream)
+        for _ in range(k2):
+            e2e_step()
+        ee.record(stream)
+        torch.cuda.synchronize(dev)
+        ems = es.elapsed_time(ee)
+        if pg:
+            import torch.distributed as dist
+            t = torch.tensor([ems], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": rows * world * k2 / (ems * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": k2}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        rate, n, dt = cpu_oracle_rate(w, args.cpu_budget, os.cpu_count() or 1)
+        cpu = {"value": rate, "unit": UNIT, "cores": os.cpu_count() or 1, "kind": "oracle",
+               "sample": f"{n} of {w.B} sequences of the same workload ({n * (w.N + 1)} verified rows), "
+                         f"{dt:.1f} s, float64 C oracle, one POSIX thread per core"}
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": workload_desc(w), "B": w.B, "N": w.N, "V": w.V,
+                   "logit_bytes_per_step": w.logit_bytes,
+                   "l2": "inputs larger than L2 (129 MB); no flush between steps",
+                   "cluster_size": ctx.cluster_size(w.B, w.N), "parallelism": f"replicas x{world}"},
+        "hbm_gbs": gbs,
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                     "peak_kind": f"{peak_kind} (burst copy)",
+                     "traffic": committed_traffic(w.name)},
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+        "check": check,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="headline")
+    ap.add_argument("--cluster", type=int, default=0, help="cluster size override (0 = automatic)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-check", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--ref-budget", type=float, default=8.0, help="seconds of oracle work per reference step")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,142 @@
+/*
+ * spec_verify.h -- C ABI of the GB300 speculative-sampling verify step.
+ *
+ * The operation (per sequence b, positions i = 0..N, tokens k = 0..V-1) is the
+ * verify half of one speculative step as stated in "Speculative decoding --
+ * draft, verify, repeat" (factory.pai-world.com, lesson 07-16), section
+ * "Core algorithm", steps 3-6, with its build section's Step 1 (rejection
+ * step) and Step 2 (residual distribution):
+ *
+ *   q_i = softmax(target_logits[b,i,:] / T_b)    i = 0..N     (verifier)
+ *   p_i = softmax(draft_logits[b,i,:]  / T_b)    i = 0..N-1   (draft)
+ *   scan i = 0..N-1: accept draft d_i iff p_i(d_i) == 0 or
+ *                    u[b,i] < min(1, q_i(d_i) / p_i(d_i))
+ *   first rejection j: token ~ normalise(max(0, q_j - p_j))
+ *   no rejection:      bonus token ~ q_N
+ *   emit d_0..d_{j-1} and that token; num_accepted = j.
+ *
+ * The final token is drawn by inverse CDF in ascending token order from the
+ * single uniform u[b,N]: the smallest k with u*R < r_0+...+r_k, R the total
+ * mass.  A residual of total mass 0 (q_j == p_j) draws from q_j instead.
+ * Greedy sequences (greedy != 0, or T_b <= 0): a_i = argmax_k target[b,i,k]
+ * (lowest index on ties); accept d_i iff d_i == a_i; emit a_j at the first
+ * mismatch, else a_N.  Draft logits and uniforms are then not read.
+ *
+ * All tensors are caller-owned device memory, C-contiguous, row-major.  The
+ * library never allocates or synchronises inside spec_verify_run; the run is
+ * enqueued on the caller's stream and completes asynchronously.
+ *
+ * Thread-safety: a context holds a small workspace that every run updates;
+ * use one context per stream (runs on one stream are serialised by it).
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct spec_verify_ctx spec_verify_ctx;
+
+typedef enum {
+    SV_OK = 0,
+    SV_ERR_INVALID_ARG = 1, /* NULL/misaligned pointer, B or N outside the context's limits */
+    SV_ERR_SHAPE = 2,       /* V unsupported (V*elt not a multiple of 16 bytes, or too large) */
+    SV_ERR_DTYPE = 3,       /* unknown sv_dtype */
+    SV_ERR_CUDA = 4,        /* a CUDA runtime call failed (launch, attribute, copy) */
+    SV_ERR_OOM = 5,         /* workspace allocation failed at create */
+    SV_ERR_BAD_TOKEN = 6,   /* device: some draft token was outside [0, V) */
+    SV_ERR_BAD_VALUE = 7,   /* device: NaN/+inf/all -inf logits, or NaN/+inf/subnormal temperature */
+    SV_ERR_TIMEOUT = 8      /* device: a bounded wait inside the kernel gave up */
+} sv_status;
+
+typedef enum { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
+
+/*
+ * Create a context on `device` for batches of up to max_B sequences with up
+ * to max_N draft tokens over a vocabulary of V tokens stored as `dtype`.
+ * Allocates a workspace of about 16*max_B + 4*max_B*(max_N+1) bytes (per-
+ * sequence tickets, first-rejection slots, error flags and sampled tokens)
+ * and one status word; nothing else is allocated later.
+ * Requires V >= 1 and V*sizeof(dtype) a multiple of 16 (V % 8 == 0 for bf16,
+ * V % 4 == 0 for f32).  Returns SV_ERR_SHAPE otherwise, SV_ERR_OOM if the
+ * workspace cannot be allocated, SV_ERR_CUDA if the device cannot be used.
+ * On failure *out is set to NULL.
+ */
+sv_status spec_verify_create(spec_verify_ctx **out, int device, int max_B, int max_N, int V,
+                             sv_dtype dtype);
+
+/*
+ * Enqueue one verify step on `stream` (a cudaStream_t; NULL = legacy default
+ * stream).
+ *   target_logits  device [B, N+1, V] of dtype, 16-byte aligned base
+ *   draft_logits   device [B, N, V] of dtype, 16-byte aligned base; may be
+ *                  NULL when greedy != 0 or N == 0
+ *   draft_tokens   device int32 [B, N]; may be NULL when N == 0
+ *   uniforms       device float [B, N+1]: columns 0..N-1 feed the accept
+ *                  tests, column N the residual/bonus sample; values in
+ *                  [0,1); may be NULL when greedy != 0
+ *   temperature    device float [B]; T <= 0 makes that sequence greedy;
+ *                  may be NULL when greedy != 0
+ *   greedy         nonzero: every sequence is greedy
+ *   out_tokens     device int32 [B, N+1]: emitted tokens, unused slots -1
+ *   num_accepted   device int32 [B]: accepted drafts, 0..N
+ * A sequence whose inputs are invalid (a draft token outside [0,V), a row
+ * the method reads with a NaN or +inf logit or with only -inf logits, a NaN,
+ * +inf or subnormal positive temperature) gets out_tokens = -1 in every slot
+ * and num_accepted = -1, and sets a sticky device status that
+ * spec_verify_get_status reports.  Host-side errors return a code and
+ * enqueue nothing.  B == 0 enqueues nothing and returns SV_OK.
+ */
+sv_status spec_verify_run(spec_verify_ctx *ctx, const void *target_logits, const void *draft_logits,
+                          const int32_t *draft_tokens, const float *uniforms,
+                          const float *temperature, int greedy, int B, int N,
+                          int32_t *out_tokens, int32_t *num_accepted, void *stream);
+
+/*
+ * Same as spec_verify_run, and also writes, for every position, the
+ * quantities the decisions were made from (any of these may be NULL):
+ *   q_at_draft        float [B, N]: q_i(d_i)
+ *   p_at_draft        float [B, N]: p_i(d_i)
+ *   target_row_stats  float [B, N+1, 2]: (max_k z, sum_k exp((z_k - max)/T))
+ *   draft_row_stats   float [B, N, 2]:   the same for the draft rows
+ * Greedy sequences report (max, NaN) and NaN probabilities.
+ */
+sv_status spec_verify_run_debug(spec_verify_ctx *ctx, const void *target_logits,
+                                const void *draft_logits, const int32_t *draft_tokens,
+                                const float *uniforms, const float *temperature, int greedy,
+                                int B, int N, int32_t *out_tokens, int32_t *num_accepted,
+                                void *stream, float *q_at_draft, float *p_at_draft,
+                                float *target_row_stats, float *draft_row_stats);
+
+/*
+ * Synchronise the device, read and clear the sticky device status of this
+ * context: SV_OK, or the first of SV_ERR_TIMEOUT, SV_ERR_BAD_TOKEN,
+ * SV_ERR_BAD_VALUE raised by a run since the last call.  SV_ERR_CUDA if the
+ * read fails.
+ */
+sv_status spec_verify_get_status(spec_verify_ctx *ctx);
+
+/*
+ * Cluster size used by the next runs: the number of CTAs (1..16) that share
+ * one verified position; 0 restores the automatic choice.  Returns
+ * SV_ERR_INVALID_ARG for a size the device cannot co-schedule.
+ */
+sv_status spec_verify_set_cluster_size(spec_verify_ctx *ctx, int cluster_size);
+
+/* The cluster size the next run will use for B sequences of N drafts. */
+int spec_verify_cluster_size(spec_verify_ctx *ctx, int B, int N);
+
+/* Static string naming a status code. */
+const char *spec_verify_error_string(sv_status s);
+
+/* Free the workspace and the context.  NULL is ignored. */
+void spec_verify_destroy(spec_verify_ctx *ctx);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

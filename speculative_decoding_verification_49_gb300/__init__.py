@@ -1,0 +1,207 @@
+"""GB300 speculative-sampling verify step.
+
+Python binding of ``libspecverify.so`` (the CUDA kernels behind the C ABI in
+``include/spec_verify.h``).  The functions named ``spec_verify_*`` mirror the
+C entry points one to one and take raw device pointers; ``SpecVerify`` is a
+convenience wrapper that takes torch tensors and only marshals arguments.
+Every step of the verify computation runs in the CUDA library: there is no
+Python or CPU fallback, and importing a missing library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .build import LIBRARY
+
+SV_OK = 0
+SV_ERR_INVALID_ARG = 1
+SV_ERR_SHAPE = 2
+SV_ERR_DTYPE = 3
+SV_ERR_CUDA = 4
+SV_ERR_OOM = 5
+SV_ERR_BAD_TOKEN = 6
+SV_ERR_BAD_VALUE = 7
+SV_ERR_TIMEOUT = 8
+
+SV_F32 = 0
+SV_BF16 = 1
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+
+# (name, restype, argtypes) of every exported entry point
+_SIGNATURES = [
+    ("spec_verify_create", _I, [ctypes.POINTER(_P), _I, _I, _I, _I, _I]),
+    ("spec_verify_run", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P]),
+    ("spec_verify_run_debug", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
+    ("spec_verify_get_status", _I, [_P]),
+    ("spec_verify_set_cluster_size", _I, [_P, _I]),
+    ("spec_verify_cluster_size", _I, [_P, _I, _I]),
+    ("spec_verify_error_string", ctypes.c_char_p, [_I]),
+    ("spec_verify_destroy", None, [_P]),
+]
+
+_lib = None
+
+
+class SpecVerifyError(RuntimeError):
+    def __init__(self, status: int, where: str = ""):
+        self.status = status
+        super().__init__(f"{where}: {spec_verify_error_string(status)}" if where else spec_verify_error_string(status))
+
+
+def load() -> ctypes.CDLL:
+    """Load the CUDA library; raises ImportError when it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIBRARY):
+            raise ImportError(f"{LIBRARY} is missing: build it with "
+                              "`python -m speculative_decoding_verification_49_gb300.build`")
+        lib = ctypes.CDLL(LIBRARY)
+        for name, res, args in _SIGNATURES:
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def exported_names():
+    return [s[0] for s in _SIGNATURES]
+
+
+# ---- one-to-one wrappers of the C ABI (raw pointers as Python ints) ---------
+
+def spec_verify_create(device: int, max_B: int, max_N: int, V: int, dtype: int) -> int:
+    ctx = _P()
+    st = load().spec_verify_create(ctypes.byref(ctx), device, max_B, max_N, V, dtype)
+    if st != SV_OK:
+        raise SpecVerifyError(st, "spec_verify_create")
+    return ctx.value
+
+
+def spec_verify_run(ctx, target, draft, draft_tokens, uniforms, temperature, greedy, B, N,
+                    out_tokens, num_accepted, stream) -> int:
+    return load().spec_verify_run(ctx, target, draft, draft_tokens, uniforms, temperature,
+                                  int(greedy), B, N, out_tokens, num_accepted, stream)
+
+
+def spec_verify_run_debug(ctx, target, draft, draft_tokens, uniforms, temperature, greedy, B, N,
+                          out_tokens, num_accepted, stream, q_at_draft, p_at_draft,
+                          target_row_stats, draft_row_stats) -> int:
+    return load().spec_verify_run_debug(ctx, target, draft, draft_tokens, uniforms, temperature,
+                                        int(greedy), B, N, out_tokens, num_accepted, stream,
+                                        q_at_draft, p_at_draft, target_row_stats, draft_row_stats)
+
+
+def spec_verify_get_status(ctx) -> int:
+    return load().spec_verify_get_status(ctx)
+
+
+def spec_verify_set_cluster_size(ctx, cluster_size: int) -> int:
+    return load().spec_verify_set_cluster_size(ctx, cluster_size)
+
+
+def spec_verify_cluster_size(ctx, B: int, N: int) -> int:
+    return load().spec_verify_cluster_size(ctx, B, N)
+
+
+def spec_verify_error_string(status: int) -> str:
+    return load().spec_verify_error_string(status).decode()
+
+
+def spec_verify_destroy(ctx) -> None:
+    load().spec_verify_destroy(ctx)
+
+
+# ---- torch convenience wrapper -------------------------------------------------
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+class SpecVerify:
+    """A context plus argument checks for torch tensors on one CUDA device.
+
+    ``run`` enqueues the verify step on the current torch stream (or the
+    given one) and returns (out_tokens [B, N+1] int32, num_accepted [B] int32)
+    without synchronising.
+    """
+
+    def __init__(self, max_B: int, max_N: int, V: int, dtype: str = "bf16", device: int = 0):
+        self.max_B, self.max_N, self.V, self.device = max_B, max_N, V, device
+        self.dtype = dtype
+        self.ctx = spec_verify_create(device, max_B, max_N, V, SV_BF16 if dtype == "bf16" else SV_F32)
+
+    def close(self):
+        if getattr(self, "ctx", None):
+            spec_verify_destroy(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def set_cluster_size(self, c: int):
+        st = spec_verify_set_cluster_size(self.ctx, c)
+        if st != SV_OK:
+            raise SpecVerifyError(st, "spec_verify_set_cluster_size")
+
+    def cluster_size(self, B: int, N: int) -> int:
+        return spec_verify_cluster_size(self.ctx, B, N)
+
+    def status(self) -> int:
+        return spec_verify_get_status(self.ctx)
+
+    def _check(self, target, draft, draft_tokens, uniforms, temperature, greedy):
+        import torch
+        want = torch.bfloat16 if self.dtype == "bf16" else torch.float32
+        B, N1, V = target.shape
+        N = N1 - 1
+        assert V == self.V and target.dtype == want and target.is_contiguous() and target.is_cuda
+        if draft is not None:
+            assert draft.shape == (B, N, V) and draft.dtype == want and draft.is_contiguous()
+        if draft_tokens is not None:
+            assert draft_tokens.shape == (B, N) and draft_tokens.dtype == torch.int32
+            assert draft_tokens.is_contiguous()
+        if uniforms is not None:
+            assert uniforms.shape == (B, N + 1) and uniforms.dtype == torch.float32
+            assert uniforms.is_contiguous()
+        if temperature is not None:
+            assert temperature.shape == (B,) and temperature.dtype == torch.float32
+        return B, N
+
+    def run(self, target, draft, draft_tokens, uniforms, temperature, greedy=False,
+            out_tokens=None, num_accepted=None, stream=None, debug=None):
+        import torch
+        B, N = self._check(target, draft, draft_tokens, uniforms, temperature, greedy)
+        dev = target.device
+        if out_tokens is None:
+            out_tokens = torch.empty((B, N + 1), dtype=torch.int32, device=dev)
+        if num_accepted is None:
+            num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+        s = stream if stream is not None else torch.cuda.current_stream(dev)
+        args = (self.ctx, _ptr(target), _ptr(draft), _ptr(draft_tokens), _ptr(uniforms),
+                _ptr(temperature), int(bool(greedy)), B, N, _ptr(out_tokens), _ptr(num_accepted),
+                s.cuda_stream)
+        if debug is None:
+            st = spec_verify_run(*args)
+        else:
+            st = spec_verify_run_debug(*args, _ptr(debug.get("q_at_draft")), _ptr(debug.get("p_at_draft")),
+                                       _ptr(debug.get("target_row_stats")),
+                                       _ptr(debug.get("draft_row_stats")))
+        if st != SV_OK:
+            raise SpecVerifyError(st, "spec_verify_run")
+        return out_tokens, num_accepted
+
+    def debug_buffers(self, B: int, N: int, device="cuda"):
+        import torch
+        return {
+            "q_at_draft": torch.full((B, N), float("nan"), device=device),
+            "p_at_draft": torch.full((B, N), float("nan"), device=device),
+            "target_row_stats": torch.full((B, N + 1, 2), float("nan"), device=device),
+            "draft_row_stats": torch.full((B, N, 2), float("nan"), device=device),
+        }

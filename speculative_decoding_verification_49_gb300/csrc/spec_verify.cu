@@ -1,0 +1,1200 @@
+// spec_verify.cu -- GB300 (sm_103a) speculative-sampling verify step.
+//
+// One kernel launch per call.  The unit of work is one verified position
+// (sequence b, position i): target row i and, for i < N, draft row i.  A
+// thread-block cluster of C CTAs owns one unit; CTA r of the cluster owns the
+// r-th contiguous column chunk of both rows.
+//
+// Per CTA (8 consumer warps + 1 producer warp):
+//   pass 1  the producer streams the chunk of both rows through a ring of
+//           shared-memory stages with 1-D TMA bulk copies (mbarrier
+//           complete_tx); consumers keep an online (max, sum of exp) per row,
+//           or (max, argmax) for greedy sequences, and reduce it per CTA.
+//   merge   cluster barrier; every CTA reads the C partials over distributed
+//           shared memory and merges them in rank order, so all CTAs hold the
+//           same row normalisers m, S.  The accept test of position i runs in
+//           double precision on the gathered logits:
+//             accept iff p(d) == 0 or u_i < min(1, q(d)/p(d)),
+//             q(d) = exp((zq_d - mq)/T)/Sq, p(d) = exp((zp_d - mp)/T)/Sp.
+//   pass 2  (only at a rejection, or for the bonus position i == N) the chunk
+//           is streamed again and r_k = max(0, q_k - p_k) (or q_k) is summed
+//           per tile and warp with warp-inclusive scans; chunk masses are
+//           exchanged over the cluster and the CTA whose chunk holds
+//           u_N * R locates the tile, then (pass 3) the warp, lane and
+//           element where the cumulative mass first exceeds it.
+//   ticket  the last unit of a sequence to finish assembles out_tokens and
+//           num_accepted from the per-position results (first rejection j,
+//           token at j) and resets the per-sequence workspace for the next
+//           call, so no memset is ever enqueued.
+//
+// Method: "Speculative decoding -- draft, verify, repeat"
+// (factory.pai-world.com lesson 07-16), section "Core algorithm", steps 3-6;
+// build section Step 1 (rejection step) and Step 2 (residual distribution).
+#include <cfloat>
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <cuda_runtime.h>
+
+#include "spec_verify.h"
+#include "sv_device.cuh"
+
+namespace {
+
+constexpr int kConsWarps = 8;
+constexpr int kConsThreads = kConsWarps * 32;
+constexpr int kThreads = kConsThreads + 32;  // + one producer warp
+constexpr int kProducerWarp = kConsWarps;
+constexpr int kTileVecs = kConsThreads;      // one 16-byte vector per consumer thread and row
+constexpr int kTileBytes = kTileVecs * 16;   // 4 KiB per row and stage
+constexpr int kStages = 4;
+constexpr int kRingBytes = kStages * 2 * kTileBytes;
+constexpr int kMaxTiles = 128;               // tiles per chunk (512 KiB of one row)
+constexpr int kMaxCluster = 16;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait, then give up
+
+constexpr int kNoReject = 0x7f7f7f7f;        // byte pattern 0x7f: memset-able
+constexpr int kErrBadToken = 1;
+constexpr int kErrBadValue = 2;
+constexpr int kErrTimeout = 4;
+
+enum { MODE_INVALID = 0, MODE_GREEDY = 1, MODE_SAMPLED = 2 };
+enum { RES_DIFF = 0, RES_Q = 1 };
+
+constexpr double kLog2e = 1.4426950408889634074;
+
+struct SvParams {
+    const void *target;
+    const void *draft;
+    const int32_t *tokens;
+    const float *u;
+    const float *T;
+    int32_t *out;
+    int32_t *nacc;
+    float *q_at;
+    float *p_at;
+    float *tstats;
+    float *dstats;
+    int *ws_first;   // [max_B]      first rejected position, kNoReject if none
+    int *ws_ticket;  // [max_B]      units of the sequence finished
+    int *ws_err;     // [max_B]      error bits of the sequence
+    int *ws_tok;     // [max_B*(max_N+1)] token sampled at each position
+    int *status;     // sticky error bits of the context
+    int B, N, V, greedy;
+};
+
+// Shared-memory control block (after the ring).  Fields read by peer CTAs over
+// DSMEM are written before a cluster barrier and not rewritten until the next.
+struct SmemCtl {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    int last_g[kStages];   // last ring position issued into each stage
+    int abort;
+    // partials published to the cluster
+    float pm_t, ps_t, pm_d, ps_d;
+    float gv;
+    int gi, gnan;
+    double R;
+    // values broadcast inside the CTA
+    int need_res, retry, cstar, tstar;
+    float mq, isq, mp, isp;
+    double x1, x2;
+    // reduction scratch
+    float red_m[kConsWarps], red_s[kConsWarps], red_m2[kConsWarps], red_s2[kConsWarps];
+    int red_i[kConsWarps], red_n[kConsWarps];
+    float incl[kConsThreads];
+    float wsum[kMaxTiles][kConsWarps];
+};
+
+constexpr size_t kSmemBytes = kRingBytes + sizeof(SmemCtl);
+
+template <int DT> struct Elt;
+template <> struct Elt<SV_F32> {
+    static constexpr int kPerVec = 4;  // elements per 16-byte vector
+};
+template <> struct Elt<SV_BF16> {
+    static constexpr int kPerVec = 8;
+};
+
+template <int DT>
+__device__ __forceinline__ void unpack(const uint4 v, float *z)
+{
+    if constexpr (DT == SV_BF16) {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            z[2 * k] = __uint_as_float(w[k] << 16);
+            z[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+        }
+    } else {
+        z[0] = __uint_as_float(v.x);
+        z[1] = __uint_as_float(v.y);
+        z[2] = __uint_as_float(v.z);
+        z[3] = __uint_as_float(v.w);
+    }
+}
+
+template <int DT>
+__device__ __forceinline__ double logit_at(const void *base, size_t idx)
+{
+    if constexpr (DT == SV_BF16) {
+        const unsigned short bits = __ldg(static_cast<const unsigned short *>(base) + idx);
+        return (double)__uint_as_float(static_cast<uint32_t>(bits) << 16);
+    } else {
+        return (double)__ldg(static_cast<const float *>(base) + idx);
+    }
+}
+
+// ---- online softmax normaliser: m = running max, s = sum exp2((z - m) c) ----
+struct Online {
+    float m, s;
+};
+
+template <int NE>
+__device__ __forceinline__ void online_add(Online &o, const float *z, float cf)
+{
+    float vmax = z[0];
+#pragma unroll
+    for (int k = 1; k < NE; ++k)
+        vmax = fmaxf(vmax, z[k]);
+    if (vmax > o.m) {
+        o.s *= sv::ex2((o.m - vmax) * cf);
+        o.m = vmax;
+    }
+    if (o.m != -INFINITY) {
+        float e[NE];
+#pragma unroll
+        for (int k = 0; k < NE; ++k)
+            e[k] = sv::ex2((z[k] - o.m) * cf);
+#pragma unroll
+        for (int w = 1; w < NE; w *= 2)
+#pragma unroll
+            for (int k = 0; k + w < NE; k += 2 * w)
+                e[k] += e[k + w];
+        o.s += e[0];
+    } else {
+        // only -inf (or NaN) seen so far: a NaN must still poison the sum
+#pragma unroll
+        for (int k = 0; k < NE; ++k)
+            if (z[k] != z[k])
+                o.s = NAN;
+    }
+}
+
+__device__ __forceinline__ Online online_merge(Online a, Online b, float cf)
+{
+    const float m = fmaxf(a.m, b.m);
+    const float sa = (a.m == m) ? a.s : a.s * sv::ex2((a.m - m) * cf);
+    const float sb = (b.m == m) ? b.s : b.s * sv::ex2((b.m - m) * cf);
+    return {m, sa + sb};
+}
+
+__device__ __forceinline__ Online warp_merge(Online o, float cf)
+{
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        Online p;
+        p.m = __shfl_xor_sync(0xffffffffu, o.m, off);
+        p.s = __shfl_xor_sync(0xffffffffu, o.s, off);
+        o = online_merge(o, p, cf);
+    }
+    return o;
+}
+
+// ---- greedy: max, lowest index of the max, NaN seen --------------------------
+struct ArgMax {
+    float v;
+    int i;
+    int nan;
+};
+
+template <int NE>
+__device__ __forceinline__ void argmax_add(ArgMax &a, const float *z, int col0)
+{
+    float vmax = z[0];
+    int nan = z[0] != z[0];
+#pragma unroll
+    for (int k = 1; k < NE; ++k) {
+        vmax = fmaxf(vmax, z[k]);
+        nan |= z[k] != z[k];
+    }
+    a.nan |= nan;
+    if (vmax > a.v) {
+        // first element of this vector that holds the new max (ascending columns)
+        int best = NE - 1;
+#pragma unroll
+        for (int k = NE - 1; k >= 0; --k)
+            if (z[k] == vmax)
+                best = k;
+        a.v = vmax;
+        a.i = col0 + best;
+    }
+}
+
+__device__ __forceinline__ ArgMax argmax_merge(ArgMax a, ArgMax b)
+{
+    ArgMax r = (b.v > a.v || (b.v == a.v && b.i < a.i)) ? b : a;
+    r.nan = a.nan | b.nan;
+    return r;
+}
+
+__device__ __forceinline__ ArgMax warp_argmax(ArgMax a)
+{
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        ArgMax p;
+        p.v = __shfl_xor_sync(0xffffffffu, a.v, off);
+        p.i = __shfl_xor_sync(0xffffffffu, a.i, off);
+        p.nan = __shfl_xor_sync(0xffffffffu, a.nan, off);
+        a = argmax_merge(a, p);
+    }
+    return a;
+}
+
+// ---- residual mass of one 16-byte vector --------------------------------------
+// r_k = max(0, q_k - p_k) (RES_DIFF) or q_k (RES_Q), with
+// q_k = 2^((zq_k - mq) c) / Sq.  Explicit round-to-nearest intrinsics keep the
+// result bit-identical wherever it is recomputed (pass 2 and pass 3).
+template <int DT>
+__device__ __forceinline__ void residual_vec(const uint4 vt, const uint4 vd, int res_mode, float mq,
+                                             float isq, float mp, float isp, float cf, float *r)
+{
+    constexpr int NE = Elt<DT>::kPerVec;
+    float zt[NE], zd[NE];
+    unpack<DT>(vt, zt);
+    if (res_mode == RES_DIFF)
+        unpack<DT>(vd, zd);
+#pragma unroll
+    for (int e = 0; e < NE; ++e) {
+        const float qk = __fmul_rn(sv::ex2(__fmul_rn(__fsub_rn(zt[e], mq), cf)), isq);
+        if (res_mode == RES_DIFF) {
+            const float pk = __fmul_rn(sv::ex2(__fmul_rn(__fsub_rn(zd[e], mp), cf)), isp);
+            r[e] = fmaxf(__fsub_rn(qk, pk), 0.0f);
+        } else {
+            r[e] = qk;
+        }
+    }
+}
+
+__device__ __forceinline__ float warp_incl_scan(float x, int lane)
+{
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o)
+            x = __fadd_rn(x, y);
+    }
+    return x;
+}
+
+// ---- ring producer -----------------------------------------------------------
+// Issues tiles [0, ntiles) of the chunk (or the single tile `only`) into ring
+// positions g, g+1, ...  Runs on one lane of the producer warp.
+__device__ __forceinline__ void produce(SmemCtl &ctl, unsigned char *ring, const uint4 *tsrc,
+                                        const uint4 *dsrc, int nvec_chunk, int t_begin, int t_end,
+                                        uint32_t g)
+{
+    for (int t = t_begin; t < t_end; ++t, ++g) {
+        const uint32_t s = g % kStages;
+        const uint32_t ph = (g / kStages) & 1u;
+        if (!sv::mbar_wait_bounded(&ctl.empty[s], ph ^ 1u, &ctl.abort, kWaitLimitNs)) {
+            ctl.abort = 1;
+            return;
+        }
+        const int nvec = min(kTileVecs, nvec_chunk - t * kTileVecs);
+        const uint32_t bytes = static_cast<uint32_t>(nvec) * 16u;
+        sv::mbar_arrive_expect_tx(&ctl.full[s], dsrc ? 2u * bytes : bytes);
+        unsigned char *stage = ring + s * (2 * kTileBytes);
+        sv::bulk_g2s(stage, tsrc + (size_t)t * kTileVecs, bytes, &ctl.full[s]);
+        if (dsrc)
+            sv::bulk_g2s(stage + kTileBytes, dsrc + (size_t)t * kTileVecs, bytes, &ctl.full[s]);
+        ctl.last_g[s] = static_cast<int>(g);
+    }
+}
+
+// Consumer side: wait until ring position g is filled.
+__device__ __forceinline__ bool consume_wait(SmemCtl &ctl, uint32_t g)
+{
+    const uint32_t s = g % kStages;
+    return sv::mbar_wait_bounded(&ctl.full[s], (g / kStages) & 1u, &ctl.abort, kWaitLimitNs);
+}
+
+__device__ __forceinline__ void consume_release(SmemCtl &ctl, uint32_t g, int lane)
+{
+    __syncwarp();
+    if (lane == 0)
+        sv::mbar_arrive(&ctl.empty[g % kStages]);
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 4) sv_verify_kernel(const SvParams p)
+{
+    constexpr int VE = Elt<DT>::kPerVec;
+    extern __shared__ __align__(128) unsigned char smem[];
+    unsigned char *ring = smem;
+    SmemCtl &ctl = *reinterpret_cast<SmemCtl *>(smem + kRingBytes);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t C = sv::cluster_nctarank();
+    const uint32_t rank = sv::cluster_ctarank();
+    const int N = p.N, V = p.V;
+    const int unit = blockIdx.x / C;
+    const int b = unit / (N + 1);
+    const int i = unit - b * (N + 1);
+
+    int mode;
+    float T = 0.0f;
+    if (p.greedy) {
+        mode = MODE_GREEDY;
+    } else {
+        T = p.T[b];
+        if (T != T)
+            mode = MODE_INVALID;
+        else if (T <= 0.0f)
+            mode = MODE_GREEDY;
+        else if (T == INFINITY || T < FLT_MIN)
+            mode = MODE_INVALID;
+        else
+            mode = MODE_SAMPLED;
+    }
+    const bool has_draft = (mode == MODE_SAMPLED) && (i < N);
+    const int d = (i < N) ? p.tokens[(size_t)b * N + i] : 0;
+    const bool bad_d = (i < N) && (d < 0 || d >= V);
+    const float cf = (mode == MODE_SAMPLED) ? (float)(kLog2e / (double)T) : 0.0f;
+
+    // column chunk of this CTA, in 16-byte vectors
+    const int NV = V / VE;
+    const int v0 = (int)((long long)NV * rank / C);
+    const int v1 = (int)((long long)NV * (rank + 1) / C);
+    const int nvec_chunk = v1 - v0;
+    const int ntiles = (nvec_chunk + kTileVecs - 1) / kTileVecs;
+
+    const size_t trow = (size_t)b * (N + 1) + i;
+    const size_t drow = (size_t)b * N + i;
+    const size_t row_vecs = (size_t)NV;
+    const uint4 *tsrc = static_cast<const uint4 *>(p.target) + trow * row_vecs + v0;
+    const uint4 *dsrc = has_draft ? static_cast<const uint4 *>(p.draft) + drow * row_vecs + v0 : nullptr;
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            sv::mbar_init(&ctl.full[s], 1);
+            sv::mbar_init(&ctl.empty[s], kConsWarps);
+            ctl.last_g[s] = -1;
+        }
+        ctl.abort = 0;
+        ctl.need_res = 0;
+        ctl.retry = 0;
+        ctl.cstar = -1;
+        sv::fence_mbar_init();
+    }
+    __syncthreads();
+
+    uint32_t g = 0;  // ring position, advanced identically by every thread
+
+    // ------------------------------------------------------------ pass 1
+    Online ot{-INFINITY, 0.0f}, od{-INFINITY, 0.0f};
+    ArgMax ga{-INFINITY, INT_MAX, 0};
+    if (mode != MODE_INVALID) {
+        if (warp == kProducerWarp) {
+            if (lane == 0)
+                produce(ctl, ring, tsrc, dsrc, nvec_chunk, 0, ntiles, g);
+            __syncwarp();
+        } else {
+            for (int t = 0; t < ntiles; ++t) {
+                const uint32_t gt = g + t;
+                if (consume_wait(ctl, gt)) {
+                    const int vec = t * kTileVecs + tid;
+                    if (vec < nvec_chunk) {
+                        const unsigned char *stage = ring + (gt % kStages) * (2 * kTileBytes);
+                        float z[VE];
+                        unpack<DT>(reinterpret_cast<const uint4 *>(stage)[tid], z);
+                        if (mode == MODE_GREEDY) {
+                            argmax_add<VE>(ga, z, (v0 + vec) * VE);
+                        } else {
+                            online_add<VE>(ot, z, cf);
+                            if (has_draft) {
+                                unpack<DT>(reinterpret_cast<const uint4 *>(stage + kTileBytes)[tid], z);
+                                online_add<VE>(od, z, cf);
+                            }
+                        }
+                    }
+                } else {
+                    ctl.abort = 1;
+                }
+                consume_release(ctl, gt, lane);
+            }
+        }
+        g += ntiles;
+    }
+
+    // CTA partial
+    if (warp < kConsWarps) {
+        if (mode == MODE_GREEDY) {
+            ga = warp_argmax(ga);
+            if (lane == 0) {
+                ctl.red_m[warp] = ga.v;
+                ctl.red_i[warp] = ga.i;
+                ctl.red_n[warp] = ga.nan;
+            }
+        } else if (mode == MODE_SAMPLED) {
+            ot = warp_merge(ot, cf);
+            od = warp_merge(od, cf);
+            if (lane == 0) {
+                ctl.red_m[warp] = ot.m;
+                ctl.red_s[warp] = ot.s;
+                ctl.red_m2[warp] = od.m;
+                ctl.red_s2[warp] = od.s;
+            }
+        }
+    }
+    __syncthreads();
+    if (tid == 0) {
+        if (mode == MODE_GREEDY) {
+            ArgMax a{ctl.red_m[0], ctl.red_i[0], ctl.red_n[0]};
+            for (int w = 1; w < kConsWarps; ++w)
+                a = argmax_merge(a, ArgMax{ctl.red_m[w], ctl.red_i[w], ctl.red_n[w]});
+            ctl.gv = a.v;
+            ctl.gi = a.i;
+            ctl.gnan = a.nan;
+        } else if (mode == MODE_SAMPLED) {
+            Online a{ctl.red_m[0], ctl.red_s[0]}, e{ctl.red_m2[0], ctl.red_s2[0]};
+            for (int w = 1; w < kConsWarps; ++w) {
+                a = online_merge(a, Online{ctl.red_m[w], ctl.red_s[w]}, cf);
+                e = online_merge(e, Online{ctl.red_m2[w], ctl.red_s2[w]}, cf);
+            }
+            ctl.pm_t = a.m;
+            ctl.ps_t = a.s;
+            ctl.pm_d = e.m;
+            ctl.ps_d = e.s;
+        }
+    }
+    sv::cluster_sync();  // #1: partials visible cluster-wide
+
+    // ------------------------------------------------------------ merge + decide
+    if (tid == 0) {
+        int errb = 0;
+        int need_res = 0;
+        bool reject = false;
+        int tok = -1;
+        if (bad_d)
+            errb |= kErrBadToken;
+        if (mode == MODE_INVALID) {
+            errb |= kErrBadValue;
+        } else if (mode == MODE_GREEDY) {
+            ArgMax a{-INFINITY, INT_MAX, 0};
+            for (uint32_t r = 0; r < C; ++r) {
+                ArgMax o;
+                o.v = sv::ld_dsmem_f32(sv::dsmem_addr(&ctl.gv, r));
+                o.i = sv::ld_dsmem_s32(sv::dsmem_addr(&ctl.gi, r));
+                o.nan = sv::ld_dsmem_s32(sv::dsmem_addr(&ctl.gnan, r));
+                a = argmax_merge(a, o);
+            }
+            const bool valid = !a.nan && a.v != INFINITY && a.v != -INFINITY;
+            if (!valid)
+                errb |= kErrBadValue;
+            tok = a.i;
+            if (i < N)
+                reject = (d != a.i);
+            if (rank == 0 && p.tstats) {
+                p.tstats[trow * 2 + 0] = a.v;
+                p.tstats[trow * 2 + 1] = NAN;
+            }
+            if (rank == 0 && i < N) {
+                if (p.q_at)
+                    p.q_at[drow] = NAN;
+                if (p.p_at)
+                    p.p_at[drow] = NAN;
+                if (p.dstats) {
+                    p.dstats[drow * 2 + 0] = NAN;
+                    p.dstats[drow * 2 + 1] = NAN;
+                }
+            }
+        } else {
+            // merge in rank order, in double
+            const double Td = (double)T;
+            const double cd = kLog2e / Td;
+            float mq = -INFINITY, mp = -INFINITY;
+            for (uint32_t r = 0; r < C; ++r) {
+                mq = fmaxf(mq, sv::ld_dsmem_f32(sv::dsmem_addr(&ctl.pm_t, r)));
+                if (has_draft)
+                    mp = fmaxf(mp, sv::ld_dsmem_f32(sv::dsmem_addr(&ctl.pm_d, r)));
+            }
+            double Sq = 0.0, Sp = 0.0;
+            for (uint32_t r = 0; r < C; ++r) {
+                const float m_r = sv::ld_dsmem_f32(sv::dsmem_addr(&ctl.pm_t, r));
+                const float s_r = sv::ld_dsmem_f32(sv::dsmem_addr(&ctl.ps_t, r));
+                Sq += (m_r == mq) ? (double)s_r : (double)s_r * exp2(((double)m_r - (double)mq) * cd);
+                if (has_draft) {
+                    const float n_r = sv::ld_dsmem_f32(sv::dsmem_addr(&ctl.pm_d, r));
+                    const float t_r = sv::ld_dsmem_f32(sv::dsmem_addr(&ctl.ps_d, r));
+                    Sp += (n_r == mp) ? (double)t_r : (double)t_r * exp2(((double)n_r - (double)mp) * cd);
+                }
+            }
+            bool valid = isfinite(mq) && isfinite(Sq) && Sq > 0.0;
+            if (has_draft)
+                valid = valid && isfinite(mp) && isfinite(Sp) && Sp > 0.0;
+            if (!valid) {
+                errb |= kErrBadValue;
+            } else if (i < N) {
+                if (!bad_d) {
+                    const double zq = logit_at<DT>(p.target, trow * (size_t)V + d);
+                    const double zp = logit_at<DT>(p.draft, drow * (size_t)V + d);
+                    const double qd = exp((zq - (double)mq) / Td) / Sq;
+                    const double pd = exp((zp - (double)mp) / Td) / Sp;
+                    const double ui = (double)p.u[trow];
+                    bool accept;
+                    if (pd == 0.0)
+                        accept = true;
+                    else
+                        accept = ui < fmin(1.0, qd / pd);
+                    reject = !accept;
+                    need_res = reject ? 1 : 0;
+                    if (rank == 0) {
+                        if (p.q_at)
+                            p.q_at[drow] = (float)qd;
+                        if (p.p_at)
+                            p.p_at[drow] = (float)pd;
+                    }
+                }
+            } else {
+                need_res = 1;  // bonus token from q_N
+            }
+            if (rank == 0) {
+                if (p.tstats) {
+                    p.tstats[trow * 2 + 0] = mq;
+                    p.tstats[trow * 2 + 1] = (float)Sq;
+                }
+                if (p.dstats && has_draft) {
+                    p.dstats[drow * 2 + 0] = mp;
+                    p.dstats[drow * 2 + 1] = (float)Sp;
+                }
+            }
+            ctl.mq = mq;
+            ctl.isq = (float)(1.0 / Sq);
+            ctl.mp = mp;
+            ctl.isp = has_draft ? (float)(1.0 / Sp) : 0.0f;
+        }
+        if (errb)
+            need_res = 0;
+        ctl.need_res = need_res;
+        if (rank == 0) {
+            if (errb)
+                atomicOr(&p.ws_err[b], errb);
+            if (reject && i < N)
+                atomicMin(&p.ws_first[b], i);
+            if (mode == MODE_GREEDY)
+                p.ws_tok[trow] = tok;
+        }
+    }
+    __syncthreads();
+
+    // ------------------------------------------------------------ residual / bonus
+    if (ctl.need_res) {
+        int res_mode = (i < N) ? RES_DIFF : RES_Q;  // RES_Q after a retry as well
+        const float mq = ctl.mq, isq = ctl.isq, mp = ctl.mp, isp = ctl.isp;
+        for (;;) {
+            const uint4 *dres = (res_mode == RES_DIFF) ? dsrc : nullptr;
+            if (warp == kProducerWarp) {
+                if (lane == 0)
+                    produce(ctl, ring, tsrc, dres, nvec_chunk, 0, ntiles, g);
+                __syncwarp();
+            } else {
+                for (int t = 0; t < ntiles; ++t) {
+                    const uint32_t gt = g + t;
+                    float part = 0.0f;
+                    if (consume_wait(ctl, gt)) {
+                        const int vec = t * kTileVecs + tid;
+                        if (vec < nvec_chunk) {
+                            const unsigned char *stage = ring + (gt % kStages) * (2 * kTileBytes);
+                            float r[VE];
+                            const uint4 vd = dres ? reinterpret_cast<const uint4 *>(stage + kTileBytes)[tid]
+                                                  : make_uint4(0, 0, 0, 0);
+                            residual_vec<DT>(reinterpret_cast<const uint4 *>(stage)[tid], vd, res_mode, mq,
+                                             isq, mp, isp, cf, r);
+#pragma unroll
+                            for (int e = 0; e < VE; ++e)
+                                part = __fadd_rn(part, r[e]);
+                        }
+                    } else {
+                        ctl.abort = 1;
+                    }
+                    consume_release(ctl, gt, lane);
+                    const float incl = warp_incl_scan(part, lane);
+                    if (lane == 31)
+                        ctl.wsum[t][warp] = incl;
+                }
+            }
+            g += ntiles;
+            __syncthreads();
+            if (tid == 0) {
+                double Rc = 0.0;
+                for (int t = 0; t < ntiles; ++t) {
+                    double tm = 0.0;
+                    for (int w = 0; w < kConsWarps; ++w)
+                        tm += (double)ctl.wsum[t][w];
+                    Rc += tm;
+                }
+                ctl.R = Rc;
+            }
+            sv::cluster_sync();  // #2: chunk masses visible
+            if (tid == 0) {
+                double Rtot = 0.0;
+                for (uint32_t r = 0; r < C; ++r)
+                    Rtot += sv::ld_dsmem_f64(sv::dsmem_addr(&ctl.R, r));
+                if (Rtot == 0.0 && res_mode == RES_DIFF) {
+                    ctl.retry = 1;  // q_j == p_j: draw from q_j instead
+                } else {
+                    ctl.retry = 0;
+                    const double x = (double)p.u[(size_t)b * (N + 1) + N] * Rtot;
+                    double cum = 0.0;
+                    int cstar = -1;
+                    double x1 = 0.0;
+                    for (uint32_t r = 0; r < C; ++r) {
+                        const double Rr = sv::ld_dsmem_f64(sv::dsmem_addr(&ctl.R, r));
+                        if (x < cum + Rr) {
+                            cstar = (int)r;
+                            x1 = x - cum;
+                            break;
+                        }
+                        cum += Rr;
+                    }
+                    if (cstar < 0) {  // rounding: take the last chunk that has mass
+                        for (int r = (int)C - 1; r >= 0; --r) {
+                            const double Rr = sv::ld_dsmem_f64(sv::dsmem_addr(&ctl.R, (uint32_t)r));
+                            if (Rr > 0.0) {
+                                cstar = r;
+                                x1 = INFINITY;
+                                break;
+                            }
+                        }
+                        if (cstar < 0)
+                            cstar = (int)C - 1, x1 = INFINITY;
+                    }
+                    ctl.cstar = cstar;
+                    ctl.x1 = x1;
+                }
+            }
+            __syncthreads();
+            if (!ctl.retry)
+                break;
+            res_mode = RES_Q;
+            sv::cluster_sync();  // #2b: peers are done reading ctl.R
+        }
+
+        if ((int)rank == ctl.cstar) {
+            if (tid == 0) {
+                // tile of the chunk where the cumulative mass first exceeds x1
+                const double x1 = ctl.x1;
+                double cum = 0.0;
+                int tstar = -1;
+                double x2 = 0.0;
+                for (int t = 0; t < ntiles; ++t) {
+                    double tm = 0.0;
+                    for (int w = 0; w < kConsWarps; ++w)
+                        tm += (double)ctl.wsum[t][w];
+                    if (x1 < cum + tm) {
+                        tstar = t;
+                        x2 = x1 - cum;
+                        break;
+                    }
+                    cum += tm;
+                }
+                if (tstar < 0) {
+                    for (int t = ntiles - 1; t >= 0 && tstar < 0; --t) {
+                        double tm = 0.0;
+                        for (int w = 0; w < kConsWarps; ++w)
+                            tm += (double)ctl.wsum[t][w];
+                        if (tm > 0.0)
+                            tstar = t;
+                    }
+                    if (tstar < 0)
+                        tstar = ntiles - 1;
+                    x2 = INFINITY;
+                }
+                ctl.tstar = tstar;
+                ctl.x2 = x2;
+            }
+            __syncthreads();
+            const int tstar = ctl.tstar;
+            // pass 3: reload tile t*, redo its warp scans, find the element
+            const uint4 *dres = (res_mode == RES_DIFF) ? dsrc : nullptr;
+            if (warp == kProducerWarp) {
+                if (lane == 0)
+                    produce(ctl, ring, tsrc, dres, nvec_chunk, tstar, tstar + 1, g);
+                __syncwarp();
+            } else {
+                float part = 0.0f;
+                if (consume_wait(ctl, g)) {
+                    const int vec = tstar * kTileVecs + tid;
+                    if (vec < nvec_chunk) {
+                        const unsigned char *stage = ring + (g % kStages) * (2 * kTileBytes);
+                        float r[VE];
+                        const uint4 vd = dres ? reinterpret_cast<const uint4 *>(stage + kTileBytes)[tid]
+                                              : make_uint4(0, 0, 0, 0);
+                        residual_vec<DT>(reinterpret_cast<const uint4 *>(stage)[tid], vd, res_mode, mq,
+                                         isq, mp, isp, cf, r);
+#pragma unroll
+                        for (int e = 0; e < VE; ++e)
+                            part = __fadd_rn(part, r[e]);
+                    }
+                } else {
+                    ctl.abort = 1;
+                }
+                ctl.incl[tid] = warp_incl_scan(part, lane);
+            }
+            __syncthreads();
+            if (tid == 0) {
+                const double x2 = ctl.x2;
+                const int nvec_t = min(kTileVecs, nvec_chunk - tstar * kTileVecs);
+                int tsel = -1;
+                double xl = 0.0;
+                if (x2 != INFINITY) {
+                    double cum = 0.0;
+                    for (int w = 0; w < kConsWarps && tsel < 0; ++w) {
+                        const double ws = (double)ctl.incl[w * 32 + 31];
+                        if (x2 < cum + ws) {
+                            const double xw = x2 - cum;
+                            for (int l = 0; l < 32; ++l) {
+                                if (xw < (double)ctl.incl[w * 32 + l]) {
+                                    tsel = w * 32 + l;
+                                    xl = xw - (l > 0 ? (double)ctl.incl[w * 32 + l - 1] : 0.0);
+                                    break;
+                                }
+                            }
+                            if (tsel < 0)
+                                break;
+                        }
+                        cum += ws;
+                    }
+                }
+                int token = -1;
+                const unsigned char *stage = ring + (g % kStages) * (2 * kTileBytes);
+                auto thread_r = [&](int th, float *r) {
+                    const uint4 vd = dres ? reinterpret_cast<const uint4 *>(stage + kTileBytes)[th]
+                                          : make_uint4(0, 0, 0, 0);
+                    residual_vec<DT>(reinterpret_cast<const uint4 *>(stage)[th], vd, res_mode, mq, isq, mp,
+                                     isp, cf, r);
+                };
+                if (tsel >= 0 && tsel < nvec_t) {
+                    float r[VE];
+                    thread_r(tsel, r);
+                    float acc = 0.0f;
+                    for (int e = 0; e < VE; ++e) {
+                        acc = __fadd_rn(acc, r[e]);
+                        if (xl < (double)acc) {
+                            token = (v0 + tstar * kTileVecs + tsel) * VE + e;
+                            break;
+                        }
+                    }
+                }
+                if (token < 0) {
+                    // rounding left the target at or past the tile's total:
+                    // the last element of the tile that carries mass
+                    for (int th = nvec_t - 1; th >= 0 && token < 0; --th) {
+                        float r[VE];
+                        thread_r(th, r);
+                        for (int e = VE - 1; e >= 0; --e)
+                            if (r[e] > 0.0f) {
+                                token = (v0 + tstar * kTileVecs + th) * VE + e;
+                                break;
+                            }
+                    }
+                    if (token < 0)
+                        token = (v0 + tstar * kTileVecs + nvec_t) * VE - 1;
+                }
+                p.ws_tok[trow] = token;
+                __threadfence();
+            }
+            g += 1;
+        }
+    }
+
+    if (tid == 0 && ctl.abort) {
+        atomicOr(&p.ws_err[b], kErrTimeout);
+        __threadfence();
+    }
+    sv::cluster_sync();  // #3: no peer reads this CTA's shared memory any more
+
+    // ------------------------------------------------------------ per-sequence ticket
+    if (rank == 0 && tid == 0) {
+        __threadfence();
+        const int prev = atomicAdd(&p.ws_ticket[b], 1);
+        if (prev == N) {
+            __threadfence();
+            int j = __ldcg(&p.ws_first[b]);
+            if (j > N)
+                j = N;
+            const int err = __ldcg(&p.ws_err[b]);
+            int32_t *out = p.out + (size_t)b * (N + 1);
+            if (err) {
+                for (int k = 0; k <= N; ++k)
+                    out[k] = -1;
+                p.nacc[b] = -1;
+                atomicOr(p.status, err);
+            } else {
+                for (int k = 0; k < j; ++k)
+                    out[k] = p.tokens[(size_t)b * N + k];
+                out[j] = __ldcg(&p.ws_tok[(size_t)b * (N + 1) + j]);
+                for (int k = j + 1; k <= N; ++k)
+                    out[k] = -1;
+                p.nacc[b] = j;
+            }
+            p.ws_first[b] = kNoReject;
+            p.ws_err[b] = 0;
+            p.ws_ticket[b] = 0;
+        }
+    }
+
+    // never leave with a bulk copy still writing into this CTA's shared memory
+    if (tid == 0 && ctl.abort) {
+        for (int s = 0; s < kStages; ++s) {
+            const int lg = ctl.last_g[s];
+            if (lg >= 0) {
+                int never = 0;
+                sv::mbar_wait_bounded(&ctl.full[s], ((uint32_t)lg / kStages) & 1u, &never, kWaitLimitNs / 4);
+            }
+        }
+    }
+}
+
+} // namespace
+
+// =============================================================================
+// host side
+// =============================================================================
+
+struct spec_verify_ctx {
+    int device;
+    int max_B, max_N, V;
+    sv_dtype dtype;
+    int num_sms;
+    int cluster_override;
+    int max_active_clusters[kMaxCluster + 1];  // 0 = cannot co-schedule
+    void *ws;
+    int *ws_first, *ws_ticket, *ws_err, *ws_tok, *status;
+};
+
+namespace {
+
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = false;
+    explicit DeviceGuard(int dev)
+    {
+        if (cudaGetDevice(&prev) != cudaSuccess)
+            return;
+        ok = (prev == dev) || (cudaSetDevice(dev) == cudaSuccess);
+    }
+    ~DeviceGuard()
+    {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev)
+            cudaSetDevice(prev);
+    }
+};
+
+int elt_bytes(sv_dtype dt) { return dt == SV_BF16 ? 2 : 4; }
+
+template <int DT> cudaError_t set_attrs()
+{
+    cudaError_t e = cudaFuncSetAttribute(sv_verify_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemBytes);
+    if (e != cudaSuccess)
+        return e;
+    return cudaFuncSetAttribute(sv_verify_kernel<DT>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+}
+
+template <int DT> int active_clusters(int C)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(C * 1024);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, sv_verify_kernel<DT>, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+int auto_cluster(const spec_verify_ctx *c, int B, int N)
+{
+    const int elt = elt_bytes(c->dtype);
+    const long long row_bytes = (long long)c->V * elt;
+    const int nv = (int)(row_bytes / 16);
+    const long long units = (long long)B * (N + 1);
+    // about 64 KiB of each row per CTA, at least two CTAs per SM in total,
+    // at most kMaxTiles tiles per chunk, at least one vector per CTA
+    int C = (int)((row_bytes + 65535) / 65536);
+    const long long par = (2LL * c->num_sms + units - 1) / (units > 0 ? units : 1);
+    if (par > C)
+        C = (int)(par < 8 ? par : 8);
+    const int cmin = (nv + kMaxTiles * kTileVecs - 1) / (kMaxTiles * kTileVecs);
+    if (C < cmin)
+        C = cmin;
+    if (C > 8 && cmin <= 8)
+        C = 8;
+    if (C > nv)
+        C = nv;
+    if (C < 1)
+        C = 1;
+    while (C > 1 && c->max_active_clusters[C] == 0)
+        --C;
+    return C;
+}
+
+int pick_cluster(const spec_verify_ctx *c, int B, int N)
+{
+    if (c->cluster_override > 0)
+        return c->cluster_override;
+    return auto_cluster(c, B, N);
+}
+
+sv_status run_impl(spec_verify_ctx *ctx, const void *target, const void *draft, const int32_t *tokens,
+                   const float *u, const float *T, int greedy, int B, int N, int32_t *out,
+                   int32_t *nacc, void *stream, float *q_at, float *p_at, float *tstats, float *dstats)
+{
+    if (!ctx)
+        return SV_ERR_INVALID_ARG;
+    if (B < 0 || B > ctx->max_B || N < 0 || N > ctx->max_N)
+        return SV_ERR_INVALID_ARG;
+    if (B == 0)
+        return SV_OK;
+    if (!target || !out || !nacc)
+        return SV_ERR_INVALID_ARG;
+    if (N > 0 && !tokens)
+        return SV_ERR_INVALID_ARG;
+    if (!greedy && (!T || !u || (N > 0 && !draft)))
+        return SV_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(target) & 15u) || (draft && (reinterpret_cast<uintptr_t>(draft) & 15u)))
+        return SV_ERR_INVALID_ARG;
+    const int C = pick_cluster(ctx, B, N);
+    const int nv = ctx->V * elt_bytes(ctx->dtype) / 16;
+    if ((nv + C - 1) / C > kMaxTiles * kTileVecs)
+        return SV_ERR_SHAPE;
+    const long long units = (long long)B * (N + 1);
+    if (units * C > INT_MAX)
+        return SV_ERR_INVALID_ARG;
+
+    DeviceGuard guard(ctx->device);
+    if (!guard.ok)
+        return SV_ERR_CUDA;
+
+    SvParams prm;
+    prm.target = target;
+    prm.draft = greedy ? nullptr : draft;
+    prm.tokens = tokens;
+    prm.u = u;
+    prm.T = T;
+    prm.out = out;
+    prm.nacc = nacc;
+    prm.q_at = q_at;
+    prm.p_at = p_at;
+    prm.tstats = tstats;
+    prm.dstats = dstats;
+    prm.ws_first = ctx->ws_first;
+    prm.ws_ticket = ctx->ws_ticket;
+    prm.ws_err = ctx->ws_err;
+    prm.ws_tok = ctx->ws_tok;
+    prm.status = ctx->status;
+    prm.B = B;
+    prm.N = N;
+    prm.V = ctx->V;
+    prm.greedy = greedy ? 1 : 0;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(units * C));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = (ctx->dtype == SV_BF16) ? cudaLaunchKernelEx(&cfg, sv_verify_kernel<SV_BF16>, prm)
+                                            : cudaLaunchKernelEx(&cfg, sv_verify_kernel<SV_F32>, prm);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return SV_ERR_CUDA;
+    }
+    return SV_OK;
+}
+
+} // namespace
+
+extern "C" {
+
+sv_status spec_verify_create(spec_verify_ctx **out, int device, int max_B, int max_N, int V, sv_dtype dtype)
+{
+    if (!out)
+        return SV_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (dtype != SV_F32 && dtype != SV_BF16)
+        return SV_ERR_DTYPE;
+    if (max_B < 0 || max_N < 0 || device < 0)
+        return SV_ERR_INVALID_ARG;
+    if (V < 1 || ((long long)V * elt_bytes(dtype)) % 16 != 0)
+        return SV_ERR_SHAPE;
+    if ((long long)V * elt_bytes(dtype) / 16 > (long long)kMaxCluster * kMaxTiles * kTileVecs)
+        return SV_ERR_SHAPE;
+
+    DeviceGuard guard(device);
+    if (!guard.ok)
+        return SV_ERR_CUDA;
+    spec_verify_ctx *c = static_cast<spec_verify_ctx *>(calloc(1, sizeof(spec_verify_ctx)));
+    if (!c)
+        return SV_ERR_OOM;
+    c->device = device;
+    c->max_B = max_B;
+    c->max_N = max_N;
+    c->V = V;
+    c->dtype = dtype;
+    if (cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
+        free(c);
+        return SV_ERR_CUDA;
+    }
+    cudaError_t e = (dtype == SV_BF16) ? set_attrs<SV_BF16>() : set_attrs<SV_F32>();
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        free(c);
+        return SV_ERR_CUDA;
+    }
+    for (int k = 1; k <= kMaxCluster; ++k)
+        c->max_active_clusters[k] = (dtype == SV_BF16) ? active_clusters<SV_BF16>(k) : active_clusters<SV_F32>(k);
+    c->max_active_clusters[1] = c->max_active_clusters[1] > 0 ? c->max_active_clusters[1] : 1;
+
+    const size_t nb = (size_t)(max_B > 0 ? max_B : 1);
+    const size_t ntok = nb * (size_t)(max_N + 1);
+    const size_t bytes = sizeof(int) * (3 * nb + ntok + 1);
+    if (cudaMalloc(&c->ws, bytes) != cudaSuccess) {
+        cudaGetLastError();
+        free(c);
+        return SV_ERR_OOM;
+    }
+    int *w = static_cast<int *>(c->ws);
+    c->ws_first = w;
+    c->ws_ticket = w + nb;
+    c->ws_err = w + 2 * nb;
+    c->ws_tok = w + 3 * nb;
+    c->status = w + 3 * nb + ntok;
+    if (cudaMemset(c->ws, 0, bytes) != cudaSuccess || cudaMemset(c->ws_first, 0x7f, sizeof(int) * nb) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(c->ws);
+        free(c);
+        return SV_ERR_CUDA;
+    }
+    *out = c;
+    return SV_OK;
+}
+
+sv_status spec_verify_run(spec_verify_ctx *ctx, const void *target_logits, const void *draft_logits,
+                          const int32_t *draft_tokens, const float *uniforms, const float *temperature,
+                          int greedy, int B, int N, int32_t *out_tokens, int32_t *num_accepted, void *stream)
+{
+    return run_impl(ctx, target_logits, draft_logits, draft_tokens, uniforms, temperature, greedy, B, N,
+                    out_tokens, num_accepted, stream, nullptr, nullptr, nullptr, nullptr);
+}
+
+sv_status spec_verify_run_debug(spec_verify_ctx *ctx, const void *target_logits, const void *draft_logits,
+                                const int32_t *draft_tokens, const float *uniforms, const float *temperature,
+                                int greedy, int B, int N, int32_t *out_tokens, int32_t *num_accepted,
+                                void *stream, float *q_at_draft, float *p_at_draft, float *target_row_stats,
+                                float *draft_row_stats)
+{
+    return run_impl(ctx, target_logits, draft_logits, draft_tokens, uniforms, temperature, greedy, B, N,
+                    out_tokens, num_accepted, stream, q_at_draft, p_at_draft, target_row_stats,
+                    draft_row_stats);
+}
+
+sv_status spec_verify_get_status(spec_verify_ctx *ctx)
+{
+    if (!ctx)
+        return SV_ERR_INVALID_ARG;
+    DeviceGuard guard(ctx->device);
+    if (!guard.ok)
+        return SV_ERR_CUDA;
+    int bits = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpy(&bits, ctx->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return SV_ERR_CUDA;
+    }
+    if (bits) {
+        const int zero = 0;
+        if (cudaMemcpy(ctx->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) {
+            cudaGetLastError();
+            return SV_ERR_CUDA;
+        }
+    }
+    if (bits & kErrTimeout)
+        return SV_ERR_TIMEOUT;
+    if (bits & kErrBadToken)
+        return SV_ERR_BAD_TOKEN;
+    if (bits & kErrBadValue)
+        return SV_ERR_BAD_VALUE;
+    return SV_OK;
+}
+
+sv_status spec_verify_set_cluster_size(spec_verify_ctx *ctx, int cluster_size)
+{
+    if (!ctx || cluster_size < 0 || cluster_size > kMaxCluster)
+        return SV_ERR_INVALID_ARG;
+    if (cluster_size > 1 && ctx->max_active_clusters[cluster_size] == 0)
+        return SV_ERR_INVALID_ARG;
+    const int nv = ctx->V * elt_bytes(ctx->dtype) / 16;
+    if (cluster_size > nv)
+        return SV_ERR_INVALID_ARG;
+    ctx->cluster_override = cluster_size;
+    return SV_OK;
+}
+
+int spec_verify_cluster_size(spec_verify_ctx *ctx, int B, int N)
+{
+    if (!ctx)
+        return 0;
+    return pick_cluster(ctx, B, N);
+}
+
+const char *spec_verify_error_string(sv_status s)
+{
+    switch (s) {
+    case SV_OK: return "SV_OK";
+    case SV_ERR_INVALID_ARG: return "SV_ERR_INVALID_ARG: bad pointer, alignment, batch or draft count";
+    case SV_ERR_SHAPE: return "SV_ERR_SHAPE: unsupported vocabulary size";
+    case SV_ERR_DTYPE: return "SV_ERR_DTYPE: unknown logit dtype";
+    case SV_ERR_CUDA: return "SV_ERR_CUDA: a CUDA runtime call failed";
+    case SV_ERR_OOM: return "SV_ERR_OOM: workspace allocation failed";
+    case SV_ERR_BAD_TOKEN: return "SV_ERR_BAD_TOKEN: a draft token was outside [0, V)";
+    case SV_ERR_BAD_VALUE: return "SV_ERR_BAD_VALUE: non-finite logits or temperature";
+    case SV_ERR_TIMEOUT: return "SV_ERR_TIMEOUT: a bounded wait in the kernel gave up";
+    }
+    return "unknown sv_status";
+}
+
+void spec_verify_destroy(spec_verify_ctx *ctx)
+{
+    if (!ctx)
+        return;
+    {
+        DeviceGuard guard(ctx->device);
+        cudaFree(ctx->ws);
+    }
+    free(ctx);
+}
+
+} // extern "C"

@@ -1,0 +1,95 @@
+"""GPU-vs-oracle comparison used by the -m gpu tests, the smoke check and the
+benchmark's self-check.
+
+Decision rule: tokens and accept counts must match the float64 oracle
+exactly, except in sequences where one of the oracle's decisions had a margin
+below BAND (|u - ratio| for an accept test, the distance of u to the chosen
+token's CDF edge for the final sample).  Those are counted and must stay
+below 1e-4 of all decisions.  Normalised probabilities (q(d), p(d)) and the
+normaliser S must agree to 1e-5 relative for float32 logits and 2e-3 for
+bf16 logits.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+
+BAND = 1e-6
+PROB_RTOL = {"f32": 1e-5, "bf16": 2e-3}
+
+
+def run_gpu(ctx, w, debug=True, greedy=None, seqs=None):
+    greedy = w.greedy if greedy is None else greedy
+    dbg = ctx.debug_buffers(w.B, w.N, device=w.target.device) if debug else None
+    out, nacc = ctx.run(w.target, None if greedy else w.draft, w.draft_tokens,
+                        None if greedy else w.uniforms, None if greedy else w.temperature,
+                        greedy=greedy, debug=dbg)
+    torch.cuda.synchronize()
+    res = {"out_tokens": out.cpu().numpy(), "num_accepted": nacc.cpu().numpy()}
+    if dbg:
+        res.update({k: v.cpu().numpy() for k, v in dbg.items()})
+    if seqs is not None:
+        res = {k: v[seqs] for k, v in res.items()}
+    return res
+
+
+def run_oracle(w, seqs=None, threads=8, greedy=None):
+    greedy = w.greedy if greedy is None else greedy
+    sel = (lambda t: t) if seqs is None else (lambda t: t[torch.as_tensor(seqs, device=t.device)])
+    return oracle.verify(sel(w.target), None if greedy else sel(w.draft), sel(w.draft_tokens),
+                         sel(w.uniforms).double(), None if greedy else sel(w.temperature).double(),
+                         greedy=greedy, dtype=w.dtype, threads=threads)
+
+
+def compare(w, gpu, orc, check_probs=True):
+    """Returns a report dict; raises AssertionError on a mismatch outside the
+    margin band or a probability outside tolerance."""
+    out_g, acc_g = gpu["out_tokens"], gpu["num_accepted"]
+    out_o, acc_o = orc["out_tokens"], orc["num_accepted"]
+    B = out_o.shape[0]
+    am, sm = orc["accept_margin"], orc["sample_margin"]
+    decisions = int(np.isfinite(am).sum() + np.isinf(am).sum() + (~np.isnan(sm)).sum())
+    band_dec = int((am < BAND).sum() + (sm < BAND).sum())
+    in_band = (np.nan_to_num(am, nan=np.inf) < BAND).any(axis=1) | (np.nan_to_num(sm, nan=np.inf) < BAND)
+    same = (out_g == out_o).all(axis=1) & (acc_g == acc_o)
+    bad = np.nonzero(~same & ~in_band)[0]
+    assert bad.size == 0, (
+        f"{bad.size} sequences differ outside the margin band, first b={bad[0]}: "
+        f"gpu {out_g[bad[0]].tolist()}/{acc_g[bad[0]]} oracle {out_o[bad[0]].tolist()}/{acc_o[bad[0]]} "
+        f"margins {am[bad[0]].tolist()} {sm[bad[0]]}")
+    rep = {"sequences": B, "exact": int(same.sum()), "band_sequences": int(in_band.sum()),
+           "band_mismatch": int((~same & in_band).sum()), "decisions": decisions,
+           "band_decisions": band_dec}
+    if check_probs and "q_at_draft" in gpu:
+        tol = PROB_RTOL[w.dtype]
+        ok = (orc["seq_status"] == 0)[:, None] & np.isfinite(orc["q_at_d"])
+        qrel = np.abs(gpu["q_at_draft"] - orc["q_at_d"]) / np.maximum(orc["q_at_d"], 1e-300)
+        prel = np.abs(gpu["p_at_draft"] - orc["p_at_d"]) / np.maximum(orc["p_at_d"], 1e-300)
+        # probabilities below float32's normal range are compared absolutely
+        tiny_q = orc["q_at_d"] < 1e-30
+        tiny_p = orc["p_at_d"] < 1e-30
+        qrel = np.where(tiny_q, np.abs(gpu["q_at_draft"] - orc["q_at_d"]) / 1e-30, qrel)
+        prel = np.where(tiny_p, np.abs(gpu["p_at_draft"] - orc["p_at_d"]) / 1e-30, prel)
+        q_max = float(np.max(qrel[ok], initial=0.0))
+        p_max = float(np.max(prel[ok], initial=0.0))
+        assert q_max <= tol, f"q(d) relative error {q_max:.3g} > {tol}"
+        assert p_max <= tol, f"p(d) relative error {p_max:.3g} > {tol}"
+        ts_ok = (orc["seq_status"] == 0)[:, None] & np.isfinite(orc["tstats"][..., 1])
+        m_diff = np.abs(gpu["target_row_stats"][..., 0] - orc["tstats"][..., 0])[ts_ok]
+        assert (m_diff == 0).all(), "row max differs"
+        s_rel = (np.abs(gpu["target_row_stats"][..., 1] - orc["tstats"][..., 1]) / orc["tstats"][..., 1])[ts_ok]
+        s_max = float(np.max(s_rel, initial=0.0))
+        assert s_max <= tol, f"S relative error {s_max:.3g} > {tol}"
+        ds_ok = (orc["seq_status"] == 0)[:, None] & np.isfinite(orc["dstats"][..., 1])
+        d_rel = (np.abs(gpu["draft_row_stats"][..., 1] - orc["dstats"][..., 1]) / orc["dstats"][..., 1])[ds_ok]
+        d_max = float(np.max(d_rel, initial=0.0))
+        assert d_max <= tol, f"draft S relative error {d_max:.3g} > {tol}"
+        # accept-test ratio error, where both sides evaluated it
+        ratio_o = orc["q_at_d"] / np.where(orc["p_at_d"] > 0, orc["p_at_d"], np.nan)
+        ratio_g = gpu["q_at_draft"].astype(np.float64) / np.where(gpu["p_at_draft"] > 0, gpu["p_at_draft"], np.nan)
+        rr = np.abs(np.minimum(ratio_g, 1.0) - np.minimum(ratio_o, 1.0))[ok]
+        rep.update(q_rel_max=q_max, p_rel_max=p_max, S_rel_max=max(s_max, d_max),
+                   ratio_abs_max=float(np.nanmax(rr, initial=0.0)))
+    return rep

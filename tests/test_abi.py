@@ -1,0 +1,68 @@
+"""The C-ABI library builds, loads and exports every declared entry point.
+Host-side argument checks that return before any CUDA call are exercised
+too; nothing here launches a kernel (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import speculative_decoding_verification_49_gb300 as sv
+from speculative_decoding_verification_49_gb300 import build as svbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "spec_verify.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b(spec_verify_\w+)\s*\(", text)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    svbuild.build()
+    return sv.load()
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for want in ("spec_verify_create", "spec_verify_run", "spec_verify_destroy",
+                 "spec_verify_run_debug", "spec_verify_get_status", "spec_verify_error_string"):
+        assert want in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert sorted(sv.exported_names()) == declared_functions()
+
+
+def test_error_strings(lib):
+    for code in range(9):
+        s = sv.spec_verify_error_string(code)
+        assert s.startswith("SV_")
+    assert "unknown" in sv.spec_verify_error_string(99)
+
+
+def test_host_validation_without_gpu(lib):
+    ctx = ctypes.c_void_p(123)
+    # unsupported vocabulary: 1001 bf16 logits are not a whole number of 16-byte vectors
+    assert lib.spec_verify_create(ctypes.byref(ctx), 0, 4, 3, 1001, sv.SV_BF16) == sv.SV_ERR_SHAPE
+    assert ctx.value is None
+    assert lib.spec_verify_create(ctypes.byref(ctx), 0, 4, 3, 1002, sv.SV_F32) == sv.SV_ERR_SHAPE
+    assert lib.spec_verify_create(ctypes.byref(ctx), 0, 4, 3, 0, sv.SV_F32) == sv.SV_ERR_SHAPE
+    assert lib.spec_verify_create(ctypes.byref(ctx), 0, 4, 3, 1024, 7) == sv.SV_ERR_DTYPE
+    assert lib.spec_verify_create(ctypes.byref(ctx), 0, -1, 3, 1024, sv.SV_F32) == sv.SV_ERR_INVALID_ARG
+    assert lib.spec_verify_create(None, 0, 4, 3, 1024, sv.SV_F32) == sv.SV_ERR_INVALID_ARG
+    # a NULL context is rejected before anything is enqueued
+    assert sv.spec_verify_run(None, 16, 16, 16, 16, 16, 0, 1, 1, 16, 16, None) == sv.SV_ERR_INVALID_ARG
+    assert sv.spec_verify_get_status(None) == sv.SV_ERR_INVALID_ARG
+    assert sv.spec_verify_set_cluster_size(None, 2) == sv.SV_ERR_INVALID_ARG
+    sv.spec_verify_destroy(None)
+
+
+def test_library_is_built_for_sm_103a():
+    assert "arch=compute_103a,code=sm_103a" in svbuild.NVCC_FLAGS

@@ -1,0 +1,193 @@
+"""CUDA path against the float64 oracle (needs a GB300).
+
+Every call goes through the C ABI (ctypes binding of libspecverify.so).  The
+five workloads run at full size; where the oracle would take too long, it
+checks a sample of the sequences of the full-size launch.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import parity
+import synth
+import speculative_decoding_verification_49_gb300 as sv
+
+pytestmark = pytest.mark.gpu
+
+THREADS = max(1, min(16, os.cpu_count() or 1))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from speculative_decoding_verification_49_gb300 import build
+    build.build()
+    assert torch.cuda.is_available()
+
+
+def _ctx(w, **kw):
+    return sv.SpecVerify(w.B, w.N, w.V, w.dtype, **kw)
+
+
+def _check(w, seqs=None, ctx=None, greedy=None):
+    ctx = ctx or _ctx(w)
+    gpu = parity.run_gpu(ctx, w, greedy=greedy, seqs=seqs)
+    orc = parity.run_oracle(w, seqs=seqs, threads=THREADS, greedy=greedy)
+    rep = parity.compare(w, gpu, orc, check_probs=not (greedy or w.greedy))
+    print(w.name, rep)
+    assert rep["band_decisions"] <= max(1, 1e-4 * rep["decisions"]) or rep["band_mismatch"] == 0
+    assert ctx.status() == sv.SV_OK
+    return rep
+
+
+@pytest.mark.parametrize("name,seed,overrides", [
+    ("tiny", 0, {}),
+    ("tiny", 1, {}),
+    ("small", 0, {}),
+    ("small", 1, {}),
+    ("mixed", 0, {}),
+    ("headline", 0, {"B": 12}),
+    ("stress", 0, {"B": 48}),
+])
+def test_parity_full_oracle(name, seed, overrides):
+    w = synth.make_workload(name, seed=seed, device="cuda", **overrides)
+    _check(w)
+
+
+@pytest.mark.parametrize("name,nsample", [("headline", 24), ("stress", 24)])
+def test_parity_full_size_sampled(name, nsample):
+    """The full-size launch the benchmark times; the oracle checks a spread
+    of its sequences one by one."""
+    w = synth.make_workload(name, seed=0, device="cuda")
+    rng = np.random.default_rng(1)
+    seqs = np.sort(rng.choice(w.B, size=nsample, replace=False))
+    seqs[0], seqs[-1] = 0, w.B - 1
+    _check(w, seqs=seqs)
+
+
+def test_parity_all_greedy_without_draft_logits():
+    w = synth.make_workload("mixed", seed=2, device="cuda", B=16)
+    rep = _check(w, greedy=True)
+    assert rep["exact"] == rep["sequences"]
+
+
+def test_greedy_ties_take_the_lowest_index():
+    g = torch.Generator(device="cuda").manual_seed(5)
+    B, N, V = 6, 3, 4096
+    target = torch.randint(-3, 2, (B, N + 1, V), generator=g, device="cuda").to(torch.bfloat16)
+    target[:, :, V - 1] = 1.0  # ties with the first max almost everywhere
+    a = target.float().argmax(dim=-1)
+    tokens = a[:, :N].to(torch.int32).clone()
+    tokens[1, 1] = (tokens[1, 1] + 1) % V
+    T = torch.zeros(B, device="cuda")
+    u = torch.rand((B, N + 1), generator=g, device="cuda")
+    w = synth.Workload("ties", B, N, V, "bf16", target.contiguous(), torch.zeros((B, N, V), dtype=torch.bfloat16,
+                       device="cuda"), tokens, u, T)
+    rep = _check(w)
+    assert rep["exact"] == B
+
+
+@pytest.mark.parametrize("N", [0, 1, 2])
+def test_small_N(N):
+    w = synth.make_workload("small", seed=3, device="cuda", B=5, N=N)
+    _check(w)
+
+
+@pytest.mark.parametrize("V,dtype", [(8, "bf16"), (4, "f32"), (16, "f32"), (1000, "f32"), (4104, "bf16"),
+                                     (65544, "bf16"), (262144, "bf16")])
+def test_ragged_and_extreme_vocabularies(V, dtype):
+    w = synth.make_workload("small", seed=4, device="cuda", B=3, N=3, V=V, dtype=dtype)
+    _check(w)
+
+
+@pytest.mark.parametrize("C", [1, 2, 3, 4, 5, 7, 8])
+def test_every_cluster_size_matches_the_oracle(C):
+    w = synth.make_workload("headline", seed=5, device="cuda", B=6)
+    ctx = _ctx(w)
+    ctx.set_cluster_size(C)
+    assert ctx.cluster_size(w.B, w.N) == C
+    _check(w, ctx=ctx)
+
+
+def test_masked_vocabulary_rows():
+    w = synth.make_workload("small", seed=6, device="cuda", B=6)
+    g = torch.Generator(device="cuda").manual_seed(6)
+    keep = torch.rand((w.B, w.N + 1, w.V), generator=g, device="cuda") < 0.1
+    w.target = torch.where(keep, w.target, torch.full_like(w.target, float("-inf")))
+    w.draft = torch.where(keep[:, :w.N], w.draft, torch.full_like(w.draft, float("-inf")))
+    # drafts must have draft mass: re-pick them among kept tokens
+    w.draft_tokens = torch.argmax(w.draft.float(), dim=-1).to(torch.int32)
+    # a whole leading chunk of -inf in one row
+    w.target[0, 0, : w.V // 2] = float("-inf")
+    _check(w)
+
+
+def test_identical_draft_accepts_everything():
+    """p == q: the ratio is exactly 1, every draft is accepted, bonus emitted."""
+    w = synth.make_workload("headline", seed=7, device="cuda", B=8)
+    w.draft = w.target[:, : w.N].clone()
+    w.uniforms[:, : w.N] = 0.99999994  # largest float32 below 1
+    ctx = _ctx(w)
+    gpu = parity.run_gpu(ctx, w)
+    assert (gpu["num_accepted"] == w.N).all()
+    assert (gpu["out_tokens"][:, : w.N] == w.draft_tokens.cpu().numpy()).all()
+    _check(w, ctx=ctx)
+
+
+def test_disjoint_one_hot_rejects_first():
+    B, N, V = 4, 3, 2048
+    target = torch.full((B, N + 1, V), float("-inf"), device="cuda")
+    draft = torch.full((B, N, V), float("-inf"), device="cuda")
+    y, x = 1234, 77
+    target[:, :, y] = 0.0
+    draft[:, :, x] = 0.0
+    tokens = torch.full((B, N), x, dtype=torch.int32, device="cuda")
+    u = torch.rand((B, N + 1), device="cuda")
+    w = synth.Workload("onehot", B, N, V, "f32", target, draft, tokens, u, torch.ones(B, device="cuda"))
+    gpu = parity.run_gpu(_ctx(w), w)
+    assert (gpu["num_accepted"] == 0).all()
+    assert (gpu["out_tokens"][:, 0] == y).all() and (gpu["out_tokens"][:, 1:] == -1).all()
+
+
+def test_invalid_inputs_give_minus_one_and_status():
+    w = synth.make_workload("small", seed=8, device="cuda", B=6)
+    w.draft_tokens[0, 1] = w.V           # bad token
+    w.target[1, 2, 5] = float("nan")     # NaN logit
+    w.draft[2, 0, :] = float("-inf")     # draft row without mass
+    w.temperature[3] = float("nan")      # bad temperature
+    ctx = _ctx(w)
+    gpu = parity.run_gpu(ctx, w, debug=False)
+    for b in range(4):
+        assert gpu["num_accepted"][b] == -1 and (gpu["out_tokens"][b] == -1).all()
+    assert (gpu["num_accepted"][4:] >= 0).all()
+    st = ctx.status()
+    assert st in (sv.SV_ERR_BAD_TOKEN, sv.SV_ERR_BAD_VALUE)
+    assert ctx.status() == sv.SV_OK  # read-and-clear
+    orc = parity.run_oracle(w)
+    assert (orc["out_tokens"] == gpu["out_tokens"]).all()
+
+
+def test_repeated_calls_reuse_the_workspace():
+    ctx = sv.SpecVerify(64, 7, 151936, "bf16")
+    for seed, B in [(10, 5), (11, 7), (12, 3), (13, 7)]:
+        w = synth.make_workload("headline", seed=seed, device="cuda", B=B)
+        _check(w, ctx=ctx)
+
+
+def test_host_errors():
+    w = synth.make_workload("small", seed=9, device="cuda", B=2)
+    ctx = _ctx(w)
+    out = torch.empty((w.B, w.N + 1), dtype=torch.int32, device="cuda")
+    acc = torch.empty((w.B,), dtype=torch.int32, device="cuda")
+    base = (ctx.ctx, w.target.data_ptr(), w.draft.data_ptr(), w.draft_tokens.data_ptr(),
+            w.uniforms.data_ptr(), w.temperature.data_ptr(), 0)
+    tail = (out.data_ptr(), acc.data_ptr(), None)
+    assert sv.spec_verify_run(*base, w.B + 1, w.N, *tail) == sv.SV_ERR_INVALID_ARG
+    assert sv.spec_verify_run(*base, w.B, w.N + 1, *tail) == sv.SV_ERR_INVALID_ARG
+    mis = (ctx.ctx, w.target.data_ptr() + 2) + base[2:]
+    assert sv.spec_verify_run(*mis, w.B, w.N, *tail) == sv.SV_ERR_INVALID_ARG
+    assert sv.spec_verify_run(*base, 0, w.N, *tail) == sv.SV_OK
+    assert sv.spec_verify_run(ctx.ctx, w.target.data_ptr(), None, w.draft_tokens.data_ptr(),
+                              w.uniforms.data_ptr(), w.temperature.data_ptr(), 0, w.B, w.N,
+                              *tail) == sv.SV_ERR_INVALID_ARG
