@@ -209,7 +209,8 @@ def run_ours(args):
     from speculative_decoding_verification_49_gb300 import build as svbuild
     svbuild.build()
 
-    w = synth.make_workload(args.workload, seed=rank, device=dev)
+    over = {"B": args.batch} if args.batch else {}
+    w = synth.make_workload(args.workload, seed=rank, device=dev, **over)
     ctx = sv.SpecVerify(w.B, w.N, w.V, w.dtype, device=local)
     if args.cluster:
         ctx.set_cluster_size(args.cluster)
@@ -342,6 +343,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="headline")
+    ap.add_argument("--batch", type=int, default=0, help="override B (profiling of a smaller case)")
     ap.add_argument("--cluster", type=int, default=0, help="cluster size override (0 = automatic)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
