@@ -49,7 +49,8 @@ typedef enum {
     SV_ERR_OOM = 5,         /* workspace allocation failed at create */
     SV_ERR_BAD_TOKEN = 6,   /* device: some draft token was outside [0, V) */
     SV_ERR_BAD_VALUE = 7,   /* device: NaN/+inf/all -inf logits, or NaN/+inf/subnormal temperature */
-    SV_ERR_TIMEOUT = 8      /* device: a bounded wait inside the kernel gave up */
+    SV_ERR_TIMEOUT = 8,     /* device: a bounded wait inside the kernel gave up */
+    SV_ERR_TOO_LARGE = 9    /* spec_verify_run_noalloc: batch beyond its fixed scratch */
 } sv_status;
 
 typedef enum { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
@@ -134,6 +135,38 @@ const char *spec_verify_error_string(sv_status s);
 
 /* Free the workspace and the context.  NULL is ignored. */
 void spec_verify_destroy(spec_verify_ctx *ctx);
+
+/*
+ * Allocation-free variant of spec_verify_run (the pages have no counterpart:
+ * this is a deployment convenience, not part of the method).
+ *
+ * Some callers must not allocate device memory once they are running: an
+ * inference engine that reserved all free memory for its KV cache at start-up,
+ * a plug-in whose host framework owns every allocation, or a decode loop that
+ * cannot afford the implicit device synchronisation and possible failure of a
+ * cudaMalloc.  This entry point needs no context and allocates nothing: its
+ * scratch is a fixed array of about 156 KiB compiled into the library, which
+ * every GPU that loads the library holds until the process exits.
+ *
+ * Arguments are those of spec_verify_run, with the vocabulary size V and the
+ * logit dtype given per call; it runs on the current device.  Limits: B <= 2048
+ * and B*(N+1) <= 32768, else SV_ERR_TOO_LARGE and nothing is enqueued.
+ * Invalid sequences are reported through out_tokens = -1 and
+ * num_accepted = -1 only (there is no status word to query).
+ *
+ * The first call on a device does a one-time, synchronous set-up (it looks up
+ * the scratch address, clears it and sets kernel attributes); make that first
+ * call before any stream capture.  Every later call enqueues four small
+ * memsets of the scratch slots it uses and the kernel, on `stream`, and
+ * nothing else.  All calls on a device share the one scratch array: calls
+ * that can overlap on the GPU (different streams without ordering between
+ * them, or several host threads) race and corrupt each other's results.
+ */
+sv_status spec_verify_run_noalloc(const void *target_logits, const void *draft_logits,
+                                  const int32_t *draft_tokens, const float *uniforms,
+                                  const float *temperature, int greedy, int B, int N, int V,
+                                  sv_dtype dtype, int32_t *out_tokens, int32_t *num_accepted,
+                                  void *stream);
 
 #ifdef __cplusplus
 }

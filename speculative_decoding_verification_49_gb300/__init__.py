@@ -23,6 +23,7 @@ SV_ERR_OOM = 5
 SV_ERR_BAD_TOKEN = 6
 SV_ERR_BAD_VALUE = 7
 SV_ERR_TIMEOUT = 8
+SV_ERR_TOO_LARGE = 9
 
 SV_F32 = 0
 SV_BF16 = 1
@@ -40,6 +41,7 @@ _SIGNATURES = [
     ("spec_verify_cluster_size", _I, [_P, _I, _I]),
     ("spec_verify_error_string", ctypes.c_char_p, [_I]),
     ("spec_verify_destroy", None, [_P]),
+    ("spec_verify_run_noalloc", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
 ]
 
 _lib = None
@@ -113,6 +115,15 @@ def spec_verify_error_string(status: int) -> str:
 
 def spec_verify_destroy(ctx) -> None:
     load().spec_verify_destroy(ctx)
+
+
+def spec_verify_run_noalloc(target, draft, draft_tokens, uniforms, temperature, greedy, B, N, V, dtype,
+                            out_tokens, num_accepted, stream) -> int:
+    """Context-free variant that allocates nothing: scratch is a fixed array
+    inside the library (B <= 2048, B*(N+1) <= 32768), shared by every call on
+    the device, so calls must not overlap on the GPU."""
+    return load().spec_verify_run_noalloc(target, draft, draft_tokens, uniforms, temperature,
+                                          int(greedy), B, N, V, dtype, out_tokens, num_accepted, stream)
 
 
 # ---- torch convenience wrapper -------------------------------------------------

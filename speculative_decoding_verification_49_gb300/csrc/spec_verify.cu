@@ -38,6 +38,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <cuda_runtime.h>
+#include <mutex>
 
 #include "spec_verify.h"
 #include "sv_device.cuh"
@@ -1182,6 +1183,9 @@ const char *spec_verify_error_string(sv_status s)
     case SV_ERR_BAD_TOKEN: return "SV_ERR_BAD_TOKEN: a draft token was outside [0, V)";
     case SV_ERR_BAD_VALUE: return "SV_ERR_BAD_VALUE: non-finite logits or temperature";
     case SV_ERR_TIMEOUT: return "SV_ERR_TIMEOUT: a bounded wait in the kernel gave up";
+    case SV_ERR_TOO_LARGE:
+        return "SV_ERR_TOO_LARGE: batch exceeds the fixed scratch of spec_verify_run_noalloc "
+               "(B <= 2048, B*(N+1) <= 32768)";
     }
     return "unknown sv_status";
 }
@@ -1198,3 +1202,136 @@ void spec_verify_destroy(spec_verify_ctx *ctx)
 }
 
 } // extern "C"
+
+// =============================================================================
+// entry point for callers that cannot allocate device memory
+// =============================================================================
+//
+// spec_verify_run_noalloc runs the same kernel as spec_verify_run, but its
+// scratch (per-sequence tickets, first-rejection slots, error flags, sampled
+// tokens and a status word) lives in the file-scope array below instead of a
+// context workspace.  The array is part of the module image: every GPU that
+// loads this library holds it until the process exits, and nothing is ever
+// allocated for it.  Host code only sees a stand-in symbol for it, so the
+// device address is looked up once per device with cudaGetSymbolAddress.
+
+namespace {
+constexpr int kNoAllocMaxB = 2048;        // sequences per call
+constexpr int kNoAllocMaxUnits = 32768;   // B*(N+1) verified positions per call
+constexpr int kNoAllocInts = 3 * kNoAllocMaxB + kNoAllocMaxUnits + 1;  // about 156 KiB
+constexpr int kNoAllocMaxDevices = 64;
+} // namespace
+
+static __device__ __align__(256) int g_sv_noalloc_scratch[kNoAllocInts];
+
+namespace {
+
+struct NoAllocDevice {
+    bool ready;
+    int *scratch;     // device address of g_sv_noalloc_scratch on this device
+    int num_sms;
+    int clusters_bf16[kMaxCluster + 1];
+    int clusters_f32[kMaxCluster + 1];
+};
+
+std::mutex g_noalloc_mutex;
+NoAllocDevice g_noalloc[kNoAllocMaxDevices];
+
+// One-time set-up on `device` (which the caller has made current): resolve
+// the scratch address, put it in its idle state, set the kernel attributes and
+// record how many clusters of each size fit.  Synchronous.
+sv_status noalloc_setup(int device, NoAllocDevice &nd)
+{
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_sv_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
+        cudaGetLastError();
+        return SV_ERR_CUDA;
+    }
+    int *w = static_cast<int *>(ptr);
+    if (cudaMemset(w, 0, sizeof(int) * kNoAllocInts) != cudaSuccess ||
+        cudaMemset(w, 0x7f, sizeof(int) * kNoAllocMaxB) != cudaSuccess ||
+        cudaDeviceGetAttribute(&nd.num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+        set_attrs<SV_BF16>() != cudaSuccess || set_attrs<SV_F32>() != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        return SV_ERR_CUDA;
+    }
+    for (int k = 1; k <= kMaxCluster; ++k) {
+        nd.clusters_bf16[k] = active_clusters<SV_BF16>(k);
+        nd.clusters_f32[k] = active_clusters<SV_F32>(k);
+    }
+    nd.clusters_bf16[1] = nd.clusters_bf16[1] > 0 ? nd.clusters_bf16[1] : 1;
+    nd.clusters_f32[1] = nd.clusters_f32[1] > 0 ? nd.clusters_f32[1] : 1;
+    nd.scratch = w;
+    nd.ready = true;
+    return SV_OK;
+}
+
+} // namespace
+
+extern "C" sv_status spec_verify_run_noalloc(const void *target_logits, const void *draft_logits,
+                                            const int32_t *draft_tokens, const float *uniforms,
+                                            const float *temperature, int greedy, int B, int N, int V,
+                                            sv_dtype dtype, int32_t *out_tokens, int32_t *num_accepted,
+                                            void *stream)
+{
+    if (dtype != SV_F32 && dtype != SV_BF16)
+        return SV_ERR_DTYPE;
+    if (B < 0 || N < 0)
+        return SV_ERR_INVALID_ARG;
+    if (V < 1 || ((long long)V * elt_bytes(dtype)) % 16 != 0 ||
+        (long long)V * elt_bytes(dtype) / 16 > (long long)kMaxCluster * kMaxTiles * kTileVecs)
+        return SV_ERR_SHAPE;
+    if (B > kNoAllocMaxB || (long long)B * (N + 1) > kNoAllocMaxUnits)
+        return SV_ERR_TOO_LARGE;
+    if (B == 0)
+        return SV_OK;
+
+    int device = -1;
+    if (cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= kNoAllocMaxDevices) {
+        cudaGetLastError();
+        return SV_ERR_CUDA;
+    }
+    NoAllocDevice *nd = &g_noalloc[device];
+    {
+        std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+        if (!nd->ready) {
+            const sv_status st = noalloc_setup(device, *nd);
+            if (st != SV_OK)
+                return st;
+        }
+    }
+
+    // A context on the stack that points into the static scratch.
+    spec_verify_ctx c;
+    memset(&c, 0, sizeof c);
+    c.device = device;
+    c.max_B = kNoAllocMaxB;
+    c.max_N = kNoAllocMaxUnits;
+    c.V = V;
+    c.dtype = dtype;
+    c.num_sms = nd->num_sms;
+    memcpy(c.max_active_clusters, dtype == SV_BF16 ? nd->clusters_bf16 : nd->clusters_f32,
+           sizeof c.max_active_clusters);
+    int *w = nd->scratch;
+    c.ws = w;
+    c.ws_first = w;
+    c.ws_ticket = w + kNoAllocMaxB;
+    c.ws_err = w + 2 * kNoAllocMaxB;
+    c.ws_tok = w + 3 * kNoAllocMaxB;
+    c.status = w + 3 * kNoAllocMaxB + kNoAllocMaxUnits;
+
+    // The scratch keeps whatever the previous call left in it: put the slots
+    // this call uses into their starting state first (on the same stream, so
+    // calls issued in stream order never see each other's values).
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(c.ws_first, 0x7f, sizeof(int) * B, st) != cudaSuccess ||
+        cudaMemsetAsync(c.ws_ticket, 0, sizeof(int) * B, st) != cudaSuccess ||
+        cudaMemsetAsync(c.ws_err, 0, sizeof(int) * B, st) != cudaSuccess ||
+        cudaMemsetAsync(c.status, 0, sizeof(int), st) != cudaSuccess) {
+        cudaGetLastError();
+        return SV_ERR_CUDA;
+    }
+    return run_impl(&c, target_logits, draft_logits, draft_tokens, uniforms, temperature, greedy, B, N,
+                    out_tokens, num_accepted, stream, nullptr, nullptr, nullptr, nullptr);
+}

@@ -41,7 +41,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_error_strings(lib):
-    for code in range(9):
+    for code in range(10):
         s = sv.spec_verify_error_string(code)
         assert s.startswith("SV_")
     assert "unknown" in sv.spec_verify_error_string(99)
