@@ -49,11 +49,13 @@ constexpr int kConsWarps = 8;
 constexpr int kConsThreads = kConsWarps * 32;
 constexpr int kThreads = kConsThreads + 32;  // + one producer warp
 constexpr int kProducerWarp = kConsWarps;
-constexpr int kTileVecs = kConsThreads;      // one 16-byte vector per consumer thread and row
-constexpr int kTileBytes = kTileVecs * 16;   // 4 KiB per row and stage
-constexpr int kStages = 4;
+constexpr int kVPT = 2;                      // 16-byte vectors per consumer thread, row and stage
+constexpr int kSliceVecs = kConsThreads;     // one vector per consumer thread: the scan unit
+constexpr int kTileVecs = kVPT * kSliceVecs; // vectors per row and stage
+constexpr int kTileBytes = kTileVecs * 16;
+constexpr int kStages = 3;
 constexpr int kRingBytes = kStages * 2 * kTileBytes;
-constexpr int kMaxTiles = 128;               // tiles per chunk (512 KiB of one row)
+constexpr int kMaxSlices = 128;              // slices per chunk (512 KiB of one row)
 constexpr int kMaxCluster = 16;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait, then give up
 
@@ -94,20 +96,22 @@ struct SmemCtl {
     uint64_t empty[kStages];
     int last_g[kStages];   // last ring position issued into each stage
     int abort;
-    // partials published to the cluster
-    float pm_t, ps_t, pm_d, ps_d;
-    float gv;
+    // published to the cluster
+    float pm_t, ps_t, pm_d, ps_d;  // sampled partials (target, draft)
+    float gv;                      // greedy partial
     int gi, gnan;
-    double R;
+    float Rc;                      // residual mass of this CTA's chunk
+    int go;                        // rank 0: this position samples its token
     // values broadcast inside the CTA
-    int need_res, retry, cstar, tstar;
-    float mq, isq, mp, isp;
-    double x1, x2;
+    int need_res, reject, errb, tok, go_all, retry, cstar, tstar;
+    float cf, mq, isq, mp, isp;
+    float x1, x2;
     // reduction scratch
     float red_m[kConsWarps], red_s[kConsWarps], red_m2[kConsWarps], red_s2[kConsWarps];
     int red_i[kConsWarps], red_n[kConsWarps];
     float incl[kConsThreads];
-    float wsum[kMaxTiles][kConsWarps];
+    float wsum[kMaxSlices][kConsWarps];  // per slice and warp: residual mass
+    float tcum[kMaxSlices];              // inclusive prefix of slice masses
 };
 
 constexpr size_t kSmemBytes = kRingBytes + sizeof(SmemCtl);
@@ -139,13 +143,13 @@ __device__ __forceinline__ void unpack(const uint4 v, float *z)
 }
 
 template <int DT>
-__device__ __forceinline__ double logit_at(const void *base, size_t idx)
+__device__ __forceinline__ float logit_at(const void *base, size_t idx)
 {
     if constexpr (DT == SV_BF16) {
         const unsigned short bits = __ldg(static_cast<const unsigned short *>(base) + idx);
-        return (double)__uint_as_float(static_cast<uint32_t>(bits) << 16);
+        return __uint_as_float(static_cast<uint32_t>(bits) << 16);
     } else {
-        return (double)__ldg(static_cast<const float *>(base) + idx);
+        return __ldg(static_cast<const float *>(base) + idx);
     }
 }
 
@@ -205,6 +209,75 @@ __device__ __forceinline__ Online warp_merge(Online o, float cf)
     return o;
 }
 
+// Packed form of online_add for one 16-byte vector: the max over the vector
+// is taken on bf16x2 words (exact), the exponent arguments (z - m) * c and the
+// sums run on f32x2 pairs, and the thread keeps two partial sums (s, s2).
+// The arguments are rounded exactly as in online_add.
+struct Online2 {
+    float m;
+    unsigned long long s;  // (even, odd) partial sums
+};
+
+__device__ __forceinline__ float lo_bf16(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float hi_bf16(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+template <int DT>
+__device__ __forceinline__ void online_add2(Online2 &o, const uint4 v, float cf)
+{
+    float vmax;
+    unsigned long long z[4];
+    constexpr int NP = (DT == SV_BF16) ? 4 : 2;  // f32x2 pairs per vector
+    if constexpr (DT == SV_BF16) {
+        const uint32_t mx = sv::bmax2(sv::bmax2(v.x, v.y), sv::bmax2(v.z, v.w));
+        vmax = fmaxf(lo_bf16(mx), hi_bf16(mx));
+        z[0] = sv::pack2(lo_bf16(v.x), hi_bf16(v.x));
+        z[1] = sv::pack2(lo_bf16(v.y), hi_bf16(v.y));
+        z[2] = sv::pack2(lo_bf16(v.z), hi_bf16(v.z));
+        z[3] = sv::pack2(lo_bf16(v.w), hi_bf16(v.w));
+    } else {
+        const float x = __uint_as_float(v.x), y = __uint_as_float(v.y);
+        const float zz = __uint_as_float(v.z), w = __uint_as_float(v.w);
+        vmax = fmaxf(fmaxf(x, y), fmaxf(zz, w));
+        z[0] = sv::pack2(x, y);
+        z[1] = sv::pack2(zz, w);
+    }
+    if (vmax > o.m) {
+        const float r = sv::ex2((o.m - vmax) * cf);
+        o.s = sv::mul2(o.s, sv::pack2(r, r));
+        o.m = vmax;
+    }
+    if (o.m != -INFINITY) {
+        const unsigned long long M = sv::pack2(o.m, o.m), Cf = sv::pack2(cf, cf);
+        unsigned long long e[NP];
+#pragma unroll
+        for (int k = 0; k < NP; ++k) {
+            float a0, a1;
+            sv::unpack2(sv::mul2(sv::sub2(z[k], M), Cf), a0, a1);
+            e[k] = sv::pack2(sv::ex2(a0), sv::ex2(a1));
+        }
+        if constexpr (NP == 4)
+            o.s = sv::add2(o.s, sv::add2(sv::add2(e[0], e[1]), sv::add2(e[2], e[3])));
+        else
+            o.s = sv::add2(o.s, sv::add2(e[0], e[1]));
+    } else {
+        // only -inf (or NaN) seen so far: a NaN must still poison the sum
+#pragma unroll
+        for (int k = 0; k < NP; ++k) {
+            float a0, a1;
+            sv::unpack2(z[k], a0, a1);
+            if (a0 != a0 || a1 != a1)
+                o.s = sv::pack2(NAN, NAN);
+        }
+    }
+}
+
+__device__ __forceinline__ Online online_fold(const Online2 &o)
+{
+    float a, b;
+    sv::unpack2(o.s, a, b);
+    return {o.m, a + b};
+}
+
 // ---- greedy: max, lowest index of the max, NaN seen --------------------------
 struct ArgMax {
     float v;
@@ -225,6 +298,41 @@ __device__ __forceinline__ void argmax_add(ArgMax &a, const float *z, int col0)
     a.nan |= nan;
     if (vmax > a.v) {
         // first element of this vector that holds the new max (ascending columns)
+        int best = NE - 1;
+#pragma unroll
+        for (int k = NE - 1; k >= 0; --k)
+            if (z[k] == vmax)
+                best = k;
+        a.v = vmax;
+        a.i = col0 + best;
+    }
+}
+
+// Packed form of argmax_add for one 16-byte vector: the vector max (and a
+// NaN test) on bf16x2 words / pairs of floats, the index only when the max
+// improves.
+template <int DT>
+__device__ __forceinline__ void argmax_add2(ArgMax &a, const uint4 v, int col0)
+{
+    constexpr int NE = Elt<DT>::kPerVec;
+    float vmax;
+    int nan;
+    if constexpr (DT == SV_BF16) {
+        const uint32_t mx = sv::bmax2(sv::bmax2(v.x, v.y), sv::bmax2(v.z, v.w));
+        const uint32_t mn = sv::bmax2_nan(sv::bmax2_nan(v.x, v.y), sv::bmax2_nan(v.z, v.w));
+        vmax = fmaxf(lo_bf16(mx), hi_bf16(mx));
+        nan = mx != mn;
+    } else {
+        const float x = __uint_as_float(v.x), y = __uint_as_float(v.y);
+        const float zz = __uint_as_float(v.z), w = __uint_as_float(v.w);
+        vmax = fmaxf(fmaxf(x, y), fmaxf(zz, w));
+        const float vn = sv::fmax_nan(sv::fmax_nan(x, y), sv::fmax_nan(zz, w));
+        nan = vn != vn;
+    }
+    a.nan |= nan;
+    if (vmax > a.v) {
+        float z[NE];
+        unpack<DT>(v, z);
         int best = NE - 1;
 #pragma unroll
         for (int k = NE - 1; k >= 0; --k)
@@ -342,9 +450,12 @@ __global__ void __launch_bounds__(kThreads, 4) sv_verify_kernel(const SvParams p
     const uint32_t C = sv::cluster_nctarank();
     const uint32_t rank = sv::cluster_ctarank();
     const int N = p.N, V = p.V;
+    // Units are ordered position-major (all sequences at position 0, then 1,
+    // ...), so when position i is decided the earlier positions of the same
+    // sequence have usually been decided already.
     const int unit = blockIdx.x / C;
-    const int b = unit / (N + 1);
-    const int i = unit - b * (N + 1);
+    const int i = unit / p.B;
+    const int b = unit - i * p.B;
 
     int mode;
     float T = 0.0f;
@@ -364,14 +475,14 @@ __global__ void __launch_bounds__(kThreads, 4) sv_verify_kernel(const SvParams p
     const bool has_draft = (mode == MODE_SAMPLED) && (i < N);
     const int d = (i < N) ? p.tokens[(size_t)b * N + i] : 0;
     const bool bad_d = (i < N) && (d < 0 || d >= V);
-    const float cf = (mode == MODE_SAMPLED) ? (float)(kLog2e / (double)T) : 0.0f;
 
     // column chunk of this CTA, in 16-byte vectors
     const int NV = V / VE;
     const int v0 = (int)((long long)NV * rank / C);
     const int v1 = (int)((long long)NV * (rank + 1) / C);
     const int nvec_chunk = v1 - v0;
-    const int ntiles = (nvec_chunk + kTileVecs - 1) / kTileVecs;
+    const int ntiles = (nvec_chunk + kTileVecs - 1) / kTileVecs;    // ring tiles
+    const int nslices = (nvec_chunk + kSliceVecs - 1) / kSliceVecs; // scan slices
 
     const size_t trow = (size_t)b * (N + 1) + i;
     const size_t drow = (size_t)b * N + i;
@@ -389,14 +500,17 @@ __global__ void __launch_bounds__(kThreads, 4) sv_verify_kernel(const SvParams p
         ctl.need_res = 0;
         ctl.retry = 0;
         ctl.cstar = -1;
+        // log2(e)/T, rounded once from double
+        ctl.cf = (mode == MODE_SAMPLED) ? (float)(kLog2e / (double)T) : 0.0f;
         sv::fence_mbar_init();
     }
     __syncthreads();
+    const float cf = ctl.cf;
 
     uint32_t g = 0;  // ring position, advanced identically by every thread
 
     // ------------------------------------------------------------ pass 1
-    Online ot{-INFINITY, 0.0f}, od{-INFINITY, 0.0f};
+    Online2 ot2{-INFINITY, 0ull}, od2{-INFINITY, 0ull};  // 0ull = (+0.0f, +0.0f)
     ArgMax ga{-INFINITY, INT_MAX, 0};
     if (mode != MODE_INVALID) {
         if (warp == kProducerWarp) {
@@ -407,18 +521,19 @@ __global__ void __launch_bounds__(kThreads, 4) sv_verify_kernel(const SvParams p
             for (int t = 0; t < ntiles; ++t) {
                 const uint32_t gt = g + t;
                 if (consume_wait(ctl, gt)) {
-                    const int vec = t * kTileVecs + tid;
-                    if (vec < nvec_chunk) {
-                        const unsigned char *stage = ring + (gt % kStages) * (2 * kTileBytes);
-                        float z[VE];
-                        unpack<DT>(reinterpret_cast<const uint4 *>(stage)[tid], z);
-                        if (mode == MODE_GREEDY) {
-                            argmax_add<VE>(ga, z, (v0 + vec) * VE);
-                        } else {
-                            online_add<VE>(ot, z, cf);
-                            if (has_draft) {
-                                unpack<DT>(reinterpret_cast<const uint4 *>(stage + kTileBytes)[tid], z);
-                                online_add<VE>(od, z, cf);
+                    const unsigned char *stage = ring + (gt % kStages) * (2 * kTileBytes);
+#pragma unroll
+                    for (int k = 0; k < kVPT; ++k) {
+                        const int sv_ = k * kSliceVecs + tid;  // vector within the stage
+                        const int vec = t * kTileVecs + sv_;
+                        if (vec < nvec_chunk) {
+                            const uint4 vt = reinterpret_cast<const uint4 *>(stage)[sv_];
+                            if (mode == MODE_GREEDY) {
+                                argmax_add2<DT>(ga, vt, (v0 + vec) * VE);
+                            } else {
+                                online_add2<DT>(ot2, vt, cf);
+                                if (has_draft)
+                                    online_add2<DT>(od2, reinterpret_cast<const uint4 *>(stage + kTileBytes)[sv_], cf);
                             }
                         }
                     }
@@ -432,6 +547,7 @@ __global__ void __launch_bounds__(kThreads, 4) sv_verify_kernel(const SvParams p
     }
 
     // CTA partial
+    Online ot = online_fold(ot2), od = online_fold(od2);
     if (warp < kConsWarps) {
         if (mode == MODE_GREEDY) {
             ga = warp_argmax(ga);
@@ -475,128 +591,157 @@ __global__ void __launch_bounds__(kThreads, 4) sv_verify_kernel(const SvParams p
     sv::cluster_sync();  // #1: partials visible cluster-wide
 
     // ------------------------------------------------------------ merge + decide
-    if (tid == 0) {
-        int errb = 0;
-        int need_res = 0;
-        bool reject = false;
-        int tok = -1;
-        if (bad_d)
-            errb |= kErrBadToken;
-        if (mode == MODE_INVALID) {
-            errb |= kErrBadValue;
-        } else if (mode == MODE_GREEDY) {
+    // Warp 0 merges the C partials (lane r reads CTA r over DSMEM) with a
+    // butterfly whose result is the same in every lane and every CTA of the
+    // cluster; lane 0 then decides position i.
+    if (warp == 0) {
+        int errb = bad_d ? kErrBadToken : 0;
+        int need_res = 0, reject = 0, tok = -1;
+        if (mode == MODE_GREEDY) {
             ArgMax a{-INFINITY, INT_MAX, 0};
-            for (uint32_t r = 0; r < C; ++r) {
-                ArgMax o;
-                o.v = sv::ld_dsmem_f32(sv::dsmem_addr(&ctl.gv, r));
-                o.i = sv::ld_dsmem_s32(sv::dsmem_addr(&ctl.gi, r));
-                o.nan = sv::ld_dsmem_s32(sv::dsmem_addr(&ctl.gnan, r));
-                a = argmax_merge(a, o);
+            if (lane < (int)C) {
+                a.v = sv::ld_dsmem_f32(sv::dsmem_addr(&ctl.gv, lane));
+                a.i = sv::ld_dsmem_s32(sv::dsmem_addr(&ctl.gi, lane));
+                a.nan = sv::ld_dsmem_s32(sv::dsmem_addr(&ctl.gnan, lane));
             }
-            const bool valid = !a.nan && a.v != INFINITY && a.v != -INFINITY;
-            if (!valid)
-                errb |= kErrBadValue;
-            tok = a.i;
-            if (i < N)
-                reject = (d != a.i);
-            if (rank == 0 && p.tstats) {
-                p.tstats[trow * 2 + 0] = a.v;
-                p.tstats[trow * 2 + 1] = NAN;
-            }
-            if (rank == 0 && i < N) {
-                if (p.q_at)
-                    p.q_at[drow] = NAN;
-                if (p.p_at)
-                    p.p_at[drow] = NAN;
-                if (p.dstats) {
-                    p.dstats[drow * 2 + 0] = NAN;
-                    p.dstats[drow * 2 + 1] = NAN;
+            a = warp_argmax(a);
+            if (lane == 0) {
+                if (a.nan || a.v == INFINITY || a.v == -INFINITY)
+                    errb |= kErrBadValue;
+                tok = a.i;
+                reject = (i < N) && (d != a.i);
+                if (rank == 0 && p.tstats) {
+                    p.tstats[trow * 2 + 0] = a.v;
+                    p.tstats[trow * 2 + 1] = NAN;
                 }
-            }
-        } else {
-            // merge in rank order, in double
-            const double Td = (double)T;
-            const double cd = kLog2e / Td;
-            float mq = -INFINITY, mp = -INFINITY;
-            for (uint32_t r = 0; r < C; ++r) {
-                mq = fmaxf(mq, sv::ld_dsmem_f32(sv::dsmem_addr(&ctl.pm_t, r)));
-                if (has_draft)
-                    mp = fmaxf(mp, sv::ld_dsmem_f32(sv::dsmem_addr(&ctl.pm_d, r)));
-            }
-            double Sq = 0.0, Sp = 0.0;
-            for (uint32_t r = 0; r < C; ++r) {
-                const float m_r = sv::ld_dsmem_f32(sv::dsmem_addr(&ctl.pm_t, r));
-                const float s_r = sv::ld_dsmem_f32(sv::dsmem_addr(&ctl.ps_t, r));
-                Sq += (m_r == mq) ? (double)s_r : (double)s_r * exp2(((double)m_r - (double)mq) * cd);
-                if (has_draft) {
-                    const float n_r = sv::ld_dsmem_f32(sv::dsmem_addr(&ctl.pm_d, r));
-                    const float t_r = sv::ld_dsmem_f32(sv::dsmem_addr(&ctl.ps_d, r));
-                    Sp += (n_r == mp) ? (double)t_r : (double)t_r * exp2(((double)n_r - (double)mp) * cd);
-                }
-            }
-            bool valid = isfinite(mq) && isfinite(Sq) && Sq > 0.0;
-            if (has_draft)
-                valid = valid && isfinite(mp) && isfinite(Sp) && Sp > 0.0;
-            if (!valid) {
-                errb |= kErrBadValue;
-            } else if (i < N) {
-                if (!bad_d) {
-                    const double zq = logit_at<DT>(p.target, trow * (size_t)V + d);
-                    const double zp = logit_at<DT>(p.draft, drow * (size_t)V + d);
-                    const double qd = exp((zq - (double)mq) / Td) / Sq;
-                    const double pd = exp((zp - (double)mp) / Td) / Sp;
-                    const double ui = (double)p.u[trow];
-                    bool accept;
-                    if (pd == 0.0)
-                        accept = true;
-                    else
-                        accept = ui < fmin(1.0, qd / pd);
-                    reject = !accept;
-                    need_res = reject ? 1 : 0;
-                    if (rank == 0) {
-                        if (p.q_at)
-                            p.q_at[drow] = (float)qd;
-                        if (p.p_at)
-                            p.p_at[drow] = (float)pd;
+                if (rank == 0 && i < N) {
+                    if (p.q_at)
+                        p.q_at[drow] = NAN;
+                    if (p.p_at)
+                        p.p_at[drow] = NAN;
+                    if (p.dstats) {
+                        p.dstats[drow * 2 + 0] = NAN;
+                        p.dstats[drow * 2 + 1] = NAN;
                     }
                 }
-            } else {
-                need_res = 1;  // bonus token from q_N
             }
-            if (rank == 0) {
-                if (p.tstats) {
-                    p.tstats[trow * 2 + 0] = mq;
-                    p.tstats[trow * 2 + 1] = (float)Sq;
-                }
-                if (p.dstats && has_draft) {
-                    p.dstats[drow * 2 + 0] = mp;
-                    p.dstats[drow * 2 + 1] = (float)Sp;
+        } else if (mode == MODE_SAMPLED) {
+            Online t{-INFINITY, 0.0f}, e{-INFINITY, 0.0f};
+            if (lane < (int)C) {
+                t.m = sv::ld_dsmem_f32(sv::dsmem_addr(&ctl.pm_t, lane));
+                t.s = sv::ld_dsmem_f32(sv::dsmem_addr(&ctl.ps_t, lane));
+                if (has_draft) {
+                    e.m = sv::ld_dsmem_f32(sv::dsmem_addr(&ctl.pm_d, lane));
+                    e.s = sv::ld_dsmem_f32(sv::dsmem_addr(&ctl.ps_d, lane));
                 }
             }
-            ctl.mq = mq;
-            ctl.isq = (float)(1.0 / Sq);
-            ctl.mp = mp;
-            ctl.isp = has_draft ? (float)(1.0 / Sp) : 0.0f;
+            t = warp_merge(t, cf);
+            e = warp_merge(e, cf);
+            if (lane == 0) {
+                const float mq = t.m, Sq = t.s, mp = e.m, Sp = e.s;
+                bool valid = isfinite(mq) && isfinite(Sq) && Sq > 0.0f;
+                if (has_draft)
+                    valid = valid && isfinite(mp) && isfinite(Sp) && Sp > 0.0f;
+                if (!valid) {
+                    errb |= kErrBadValue;
+                } else if (i < N) {
+                    if (!bad_d) {
+                        // accept iff p(d) == 0 or u < min(1, q(d)/p(d)), with
+                        // q(d)/p(d) = 2^L * Sp/Sq, L = ((zq-mq) - (zp-mp)) log2(e)/T
+                        const float zq = logit_at<DT>(p.target, trow * (size_t)V + d);
+                        const float zp = logit_at<DT>(p.draft, drow * (size_t)V + d);
+                        const double ui = (double)p.u[trow];
+                        const double invT = 1.0 / (double)T;
+                        const double xq = ((double)zq - (double)mq) * invT;
+                        const double xp = ((double)zp - (double)mp) * invT;
+                        bool accept;
+                        if (zp == -INFINITY) {
+                            accept = true;  // p(d) = 0
+                        } else if (zq == -INFINITY) {
+                            accept = false;  // q(d) = 0 and u < 0 never holds
+                        } else if (xq < -700.0 || xp < -700.0) {
+                            // near double underflow: evaluate q(d), p(d) as the definition does
+                            const double qd = exp(xq) / (double)Sq, pd = exp(xp) / (double)Sp;
+                            accept = (pd == 0.0) || (ui < fmin(1.0, qd / pd));
+                        } else {
+                            const double L = (xq - xp) * kLog2e;
+                            const double n = floor(L);
+                            const float frac = (float)(L - n);
+                            const double ratio = ldexp((double)(sv::ex2(frac) * (Sp / Sq)), (int)n);
+                            accept = ui < fmin(1.0, ratio);
+                        }
+                        reject = !accept;
+                        need_res = reject;
+                        if (rank == 0) {
+                            if (p.q_at)
+                                p.q_at[drow] = (float)(exp(xq) / (double)Sq);
+                            if (p.p_at)
+                                p.p_at[drow] = (float)(exp(xp) / (double)Sp);
+                        }
+                    }
+                } else {
+                    need_res = 1;  // bonus token from q_N
+                }
+                if (rank == 0) {
+                    if (p.tstats) {
+                        p.tstats[trow * 2 + 0] = mq;
+                        p.tstats[trow * 2 + 1] = Sq;
+                    }
+                    if (p.dstats && has_draft) {
+                        p.dstats[drow * 2 + 0] = mp;
+                        p.dstats[drow * 2 + 1] = Sp;
+                    }
+                }
+                ctl.mq = mq;
+                ctl.isq = 1.0f / Sq;
+                ctl.mp = mp;
+                ctl.isp = has_draft ? 1.0f / Sp : 0.0f;
+            }
+        } else {
+            errb |= kErrBadValue;
         }
-        if (errb)
-            need_res = 0;
-        ctl.need_res = need_res;
-        if (rank == 0) {
+        if (lane == 0) {
             if (errb)
-                atomicOr(&p.ws_err[b], errb);
-            if (reject && i < N)
-                atomicMin(&p.ws_first[b], i);
-            if (mode == MODE_GREEDY)
-                p.ws_tok[trow] = tok;
+                need_res = 0;
+            ctl.errb = errb;
+            ctl.need_res = need_res;
+            ctl.reject = reject;
+            ctl.tok = tok;
         }
     }
     __syncthreads();
 
+    // Rank 0 records the outcome for the sequence.  A rejecting (or bonus)
+    // position learns whether an earlier position has already rejected: if so
+    // its sample can never be emitted and is skipped.
+    if (rank == 0 && tid == 0) {
+        if (ctl.errb)
+            atomicOr(&p.ws_err[b], ctl.errb);
+        int prior = kNoReject;
+        if (ctl.reject)
+            prior = atomicMin(&p.ws_first[b], i);
+        else if (ctl.need_res)
+            prior = atomicAdd(&p.ws_first[b], 0);
+        if (mode == MODE_GREEDY)
+            p.ws_tok[trow] = ctl.tok;
+        ctl.go = (ctl.need_res && prior > i) ? 1 : 0;
+    }
+    int go = 0;
+    if (ctl.need_res) {      // same value in every CTA of the cluster
+        sv::cluster_sync();  // #1b: rank 0's verdict visible
+        if (tid == 0)
+            ctl.go_all = sv::ld_dsmem_s32(sv::dsmem_addr(&ctl.go, 0));
+        __syncthreads();
+        go = ctl.go_all;
+    }
+
     // ------------------------------------------------------------ residual / bonus
-    if (ctl.need_res) {
+    if (go) {
         int res_mode = (i < N) ? RES_DIFF : RES_Q;  // RES_Q after a retry as well
         const float mq = ctl.mq, isq = ctl.isq, mp = ctl.mp, isp = ctl.isp;
+        const float uN = p.u[(size_t)b * (N + 1) + N];
         for (;;) {
+            // pass 2: residual mass per tile and warp
             const uint4 *dres = (res_mode == RES_DIFF) ? dsrc : nullptr;
             if (warp == kProducerWarp) {
                 if (lane == 0)
@@ -605,122 +750,130 @@ __global__ void __launch_bounds__(kThreads, 4) sv_verify_kernel(const SvParams p
             } else {
                 for (int t = 0; t < ntiles; ++t) {
                     const uint32_t gt = g + t;
-                    float part = 0.0f;
-                    if (consume_wait(ctl, gt)) {
-                        const int vec = t * kTileVecs + tid;
-                        if (vec < nvec_chunk) {
-                            const unsigned char *stage = ring + (gt % kStages) * (2 * kTileBytes);
+                    float part[kVPT];
+                    const bool ok = consume_wait(ctl, gt);
+                    if (!ok)
+                        ctl.abort = 1;
+                    const unsigned char *stage = ring + (gt % kStages) * (2 * kTileBytes);
+#pragma unroll
+                    for (int k = 0; k < kVPT; ++k) {
+                        part[k] = 0.0f;
+                        const int sv_ = k * kSliceVecs + tid;
+                        const int vec = t * kTileVecs + sv_;
+                        if (ok && vec < nvec_chunk) {
                             float r[VE];
-                            const uint4 vd = dres ? reinterpret_cast<const uint4 *>(stage + kTileBytes)[tid]
+                            const uint4 vd = dres ? reinterpret_cast<const uint4 *>(stage + kTileBytes)[sv_]
                                                   : make_uint4(0, 0, 0, 0);
-                            residual_vec<DT>(reinterpret_cast<const uint4 *>(stage)[tid], vd, res_mode, mq,
+                            residual_vec<DT>(reinterpret_cast<const uint4 *>(stage)[sv_], vd, res_mode, mq,
                                              isq, mp, isp, cf, r);
 #pragma unroll
                             for (int e = 0; e < VE; ++e)
-                                part = __fadd_rn(part, r[e]);
+                                part[k] = __fadd_rn(part[k], r[e]);
                         }
-                    } else {
-                        ctl.abort = 1;
                     }
                     consume_release(ctl, gt, lane);
-                    const float incl = warp_incl_scan(part, lane);
-                    if (lane == 31)
-                        ctl.wsum[t][warp] = incl;
+#pragma unroll
+                    for (int k = 0; k < kVPT; ++k) {
+                        const int sl = t * kVPT + k;
+                        const float incl = warp_incl_scan(part[k], lane);
+                        if (lane == 31 && sl < nslices)
+                            ctl.wsum[sl][warp] = incl;
+                    }
                 }
             }
             g += ntiles;
             __syncthreads();
-            if (tid == 0) {
-                double Rc = 0.0;
-                for (int t = 0; t < ntiles; ++t) {
-                    double tm = 0.0;
-                    for (int w = 0; w < kConsWarps; ++w)
-                        tm += (double)ctl.wsum[t][w];
-                    Rc += tm;
+            if (warp == 0) {
+                // slice masses and their inclusive prefix over the chunk
+                float carry = 0.0f;
+                for (int t0 = 0; t0 < nslices; t0 += 32) {
+                    const int t = t0 + lane;
+                    float tm = 0.0f;
+                    if (t < nslices)
+#pragma unroll
+                        for (int w = 0; w < kConsWarps; ++w)
+                            tm = __fadd_rn(tm, ctl.wsum[t][w]);
+                    const float inc = __fadd_rn(warp_incl_scan(tm, lane), carry);
+                    if (t < nslices)
+                        ctl.tcum[t] = inc;
+                    carry = __shfl_sync(0xffffffffu, inc, 31);
                 }
-                ctl.R = Rc;
+                if (lane == 0)
+                    ctl.Rc = carry;
             }
             sv::cluster_sync();  // #2: chunk masses visible
-            if (tid == 0) {
-                double Rtot = 0.0;
-                for (uint32_t r = 0; r < C; ++r)
-                    Rtot += sv::ld_dsmem_f64(sv::dsmem_addr(&ctl.R, r));
-                if (Rtot == 0.0 && res_mode == RES_DIFF) {
-                    ctl.retry = 1;  // q_j == p_j: draw from q_j instead
-                } else {
-                    ctl.retry = 0;
-                    const double x = (double)p.u[(size_t)b * (N + 1) + N] * Rtot;
-                    double cum = 0.0;
-                    int cstar = -1;
-                    double x1 = 0.0;
-                    for (uint32_t r = 0; r < C; ++r) {
-                        const double Rr = sv::ld_dsmem_f64(sv::dsmem_addr(&ctl.R, r));
-                        if (x < cum + Rr) {
-                            cstar = (int)r;
-                            x1 = x - cum;
-                            break;
-                        }
-                        cum += Rr;
-                    }
-                    if (cstar < 0) {  // rounding: take the last chunk that has mass
-                        for (int r = (int)C - 1; r >= 0; --r) {
-                            const double Rr = sv::ld_dsmem_f64(sv::dsmem_addr(&ctl.R, (uint32_t)r));
-                            if (Rr > 0.0) {
-                                cstar = r;
-                                x1 = INFINITY;
-                                break;
-                            }
-                        }
-                        if (cstar < 0)
-                            cstar = (int)C - 1, x1 = INFINITY;
-                    }
-                    ctl.cstar = cstar;
+            if (warp == 0) {
+                // chunk c* whose cumulative mass first exceeds u_N * R
+                const float Rr = (lane < (int)C) ? sv::ld_dsmem_f32(sv::dsmem_addr(&ctl.Rc, lane)) : 0.0f;
+                const float cum = warp_incl_scan(Rr, lane);
+                const float Rt = __shfl_sync(0xffffffffu, cum, 31);
+                const float x = __fmul_rn(uN, Rt);
+                const unsigned hit = __ballot_sync(0xffffffffu, lane < (int)C && x < cum);
+                int cs;
+                float x1;
+                if (hit) {
+                    cs = __ffs(hit) - 1;
+                    const float prev = __shfl_sync(0xffffffffu, cum, cs > 0 ? cs - 1 : 0);
+                    x1 = __fsub_rn(x, cs > 0 ? prev : 0.0f);
+                } else {  // rounding: the last chunk that has mass
+                    const unsigned pos = __ballot_sync(0xffffffffu, lane < (int)C && Rr > 0.0f);
+                    cs = pos ? 31 - __clz(pos) : (int)C - 1;
+                    x1 = INFINITY;
+                }
+                if (lane == 0) {
+                    ctl.retry = (Rt == 0.0f && res_mode == RES_DIFF) ? 1 : 0;
+                    ctl.cstar = cs;
                     ctl.x1 = x1;
                 }
             }
             __syncthreads();
             if (!ctl.retry)
                 break;
-            res_mode = RES_Q;
-            sv::cluster_sync();  // #2b: peers are done reading ctl.R
+            res_mode = RES_Q;    // q_j == p_j: draw from q_j instead
+            sv::cluster_sync();  // #2b: peers are done reading ctl.Rc
         }
 
         if ((int)rank == ctl.cstar) {
-            if (tid == 0) {
-                // tile of the chunk where the cumulative mass first exceeds x1
-                const double x1 = ctl.x1;
-                double cum = 0.0;
-                int tstar = -1;
-                double x2 = 0.0;
-                for (int t = 0; t < ntiles; ++t) {
-                    double tm = 0.0;
-                    for (int w = 0; w < kConsWarps; ++w)
-                        tm += (double)ctl.wsum[t][w];
-                    if (x1 < cum + tm) {
-                        tstar = t;
-                        x2 = x1 - cum;
-                        break;
+            if (warp == 0) {
+                // slice s* of the chunk, and the target relative to its start
+                const float x1 = ctl.x1;
+                int ts = -1;
+                float x2 = INFINITY;
+                if (x1 != INFINITY) {
+                    for (int t0 = 0; t0 < nslices && ts < 0; t0 += 32) {
+                        const int t = t0 + lane;
+                        const unsigned m = __ballot_sync(0xffffffffu, t < nslices && x1 < ctl.tcum[t]);
+                        if (m)
+                            ts = t0 + __ffs(m) - 1;
                     }
-                    cum += tm;
+                    if (ts >= 0)
+                        x2 = __fsub_rn(x1, ts > 0 ? ctl.tcum[ts - 1] : 0.0f);
                 }
-                if (tstar < 0) {
-                    for (int t = ntiles - 1; t >= 0 && tstar < 0; --t) {
-                        double tm = 0.0;
-                        for (int w = 0; w < kConsWarps; ++w)
-                            tm += (double)ctl.wsum[t][w];
-                        if (tm > 0.0)
-                            tstar = t;
+                if (ts < 0) {  // rounding: the last slice that has mass
+                    for (int t0 = ((nslices - 1) / 32) * 32; t0 >= 0 && ts < 0; t0 -= 32) {
+                        const int t = t0 + lane;
+                        float tm = 0.0f;
+                        if (t < nslices)
+                            for (int w = 0; w < kConsWarps; ++w)
+                                tm += ctl.wsum[t][w];
+                        const unsigned m = __ballot_sync(0xffffffffu, tm > 0.0f);
+                        if (m)
+                            ts = t0 + 31 - __clz(m);
                     }
-                    if (tstar < 0)
-                        tstar = ntiles - 1;
+                    if (ts < 0)
+                        ts = nslices - 1;
                     x2 = INFINITY;
                 }
-                ctl.tstar = tstar;
-                ctl.x2 = x2;
+                if (lane == 0) {
+                    ctl.tstar = ts;
+                    ctl.x2 = x2;
+                }
             }
             __syncthreads();
-            const int tstar = ctl.tstar;
-            // pass 3: reload tile t*, redo its warp scans, find the element
+            const int sstar = ctl.tstar;              // slice
+            const int tstar = sstar / kVPT;           // ring tile holding it
+            const int kstar = sstar - tstar * kVPT;   // its place in the stage
+            // pass 3: reload the tile of slice s*, redo its warp scans, find the element
             const uint4 *dres = (res_mode == RES_DIFF) ? dsrc : nullptr;
             if (warp == kProducerWarp) {
                 if (lane == 0)
@@ -729,14 +882,15 @@ __global__ void __launch_bounds__(kThreads, 4) sv_verify_kernel(const SvParams p
             } else {
                 float part = 0.0f;
                 if (consume_wait(ctl, g)) {
-                    const int vec = tstar * kTileVecs + tid;
+                    const int vec = sstar * kSliceVecs + tid;
                     if (vec < nvec_chunk) {
                         const unsigned char *stage = ring + (g % kStages) * (2 * kTileBytes);
+                        const int sv_ = kstar * kSliceVecs + tid;
                         float r[VE];
-                        const uint4 vd = dres ? reinterpret_cast<const uint4 *>(stage + kTileBytes)[tid]
+                        const uint4 vd = dres ? reinterpret_cast<const uint4 *>(stage + kTileBytes)[sv_]
                                               : make_uint4(0, 0, 0, 0);
-                        residual_vec<DT>(reinterpret_cast<const uint4 *>(stage)[tid], vd, res_mode, mq,
-                                         isq, mp, isp, cf, r);
+                        residual_vec<DT>(reinterpret_cast<const uint4 *>(stage)[sv_], vd, res_mode, mq, isq,
+                                         mp, isp, cf, r);
 #pragma unroll
                         for (int e = 0; e < VE; ++e)
                             part = __fadd_rn(part, r[e]);
@@ -747,67 +901,67 @@ __global__ void __launch_bounds__(kThreads, 4) sv_verify_kernel(const SvParams p
                 ctl.incl[tid] = warp_incl_scan(part, lane);
             }
             __syncthreads();
-            if (tid == 0) {
-                const double x2 = ctl.x2;
-                const int nvec_t = min(kTileVecs, nvec_chunk - tstar * kTileVecs);
-                int tsel = -1;
-                double xl = 0.0;
-                if (x2 != INFINITY) {
-                    double cum = 0.0;
-                    for (int w = 0; w < kConsWarps && tsel < 0; ++w) {
-                        const double ws = (double)ctl.incl[w * 32 + 31];
-                        if (x2 < cum + ws) {
-                            const double xw = x2 - cum;
-                            for (int l = 0; l < 32; ++l) {
-                                if (xw < (double)ctl.incl[w * 32 + l]) {
-                                    tsel = w * 32 + l;
-                                    xl = xw - (l > 0 ? (double)ctl.incl[w * 32 + l - 1] : 0.0);
+            if (warp == 0) {
+                const int nvec_t = min(kSliceVecs, nvec_chunk - sstar * kSliceVecs);
+                const float x2 = ctl.x2;
+                const float wt = (lane < kConsWarps) ? ctl.incl[lane * 32 + 31] : 0.0f;
+                const float wc = warp_incl_scan(wt, lane);
+                int sel = -1;
+                float xl = 0.0f;
+                const unsigned mw = __ballot_sync(0xffffffffu, lane < kConsWarps && x2 < wc);
+                if (mw) {
+                    const int ws = __ffs(mw) - 1;
+                    const float wprev = __shfl_sync(0xffffffffu, wc, ws > 0 ? ws - 1 : 0);
+                    const float xw = __fsub_rn(x2, ws > 0 ? wprev : 0.0f);
+                    const float li = ctl.incl[ws * 32 + lane];
+                    const unsigned ml = __ballot_sync(0xffffffffu, xw < li);
+                    if (ml) {
+                        const int ls = __ffs(ml) - 1;
+                        const float lprev = __shfl_sync(0xffffffffu, li, ls > 0 ? ls - 1 : 0);
+                        sel = ws * 32 + ls;
+                        xl = __fsub_rn(xw, ls > 0 ? lprev : 0.0f);
+                    }
+                }
+                if (lane == 0) {
+                    const unsigned char *stage = ring + (g % kStages) * (2 * kTileBytes);
+                    auto thread_r = [&](int th, float *r) {
+                        const int sv_ = kstar * kSliceVecs + th;
+                        const uint4 vd = dres ? reinterpret_cast<const uint4 *>(stage + kTileBytes)[sv_]
+                                              : make_uint4(0, 0, 0, 0);
+                        residual_vec<DT>(reinterpret_cast<const uint4 *>(stage)[sv_], vd, res_mode, mq, isq, mp,
+                                         isp, cf, r);
+                    };
+                    int token = -1;
+                    if (sel >= 0 && sel < nvec_t) {
+                        float r[VE];
+                        thread_r(sel, r);
+                        float acc = 0.0f;
+                        for (int e = 0; e < VE; ++e) {
+                            acc = __fadd_rn(acc, r[e]);
+                            if (xl < acc) {
+                                token = (v0 + sstar * kSliceVecs + sel) * VE + e;
+                                break;
+                            }
+                        }
+                    }
+                    if (token < 0) {
+                        // rounding left the target at or past the total: the
+                        // last element of the tile that carries mass
+                        for (int th = nvec_t - 1; th >= 0 && token < 0; --th) {
+                            float r[VE];
+                            thread_r(th, r);
+                            for (int e = VE - 1; e >= 0; --e)
+                                if (r[e] > 0.0f) {
+                                    token = (v0 + sstar * kSliceVecs + th) * VE + e;
                                     break;
                                 }
-                            }
-                            if (tsel < 0)
-                                break;
                         }
-                        cum += ws;
+                        if (token < 0)
+                            token = (v0 + sstar * kSliceVecs + nvec_t) * VE - 1;
                     }
+                    p.ws_tok[trow] = token;
+                    __threadfence();
                 }
-                int token = -1;
-                const unsigned char *stage = ring + (g % kStages) * (2 * kTileBytes);
-                auto thread_r = [&](int th, float *r) {
-                    const uint4 vd = dres ? reinterpret_cast<const uint4 *>(stage + kTileBytes)[th]
-                                          : make_uint4(0, 0, 0, 0);
-                    residual_vec<DT>(reinterpret_cast<const uint4 *>(stage)[th], vd, res_mode, mq, isq, mp,
-                                     isp, cf, r);
-                };
-                if (tsel >= 0 && tsel < nvec_t) {
-                    float r[VE];
-                    thread_r(tsel, r);
-                    float acc = 0.0f;
-                    for (int e = 0; e < VE; ++e) {
-                        acc = __fadd_rn(acc, r[e]);
-                        if (xl < (double)acc) {
-                            token = (v0 + tstar * kTileVecs + tsel) * VE + e;
-                            break;
-                        }
-                    }
-                }
-                if (token < 0) {
-                    // rounding left the target at or past the tile's total:
-                    // the last element of the tile that carries mass
-                    for (int th = nvec_t - 1; th >= 0 && token < 0; --th) {
-                        float r[VE];
-                        thread_r(th, r);
-                        for (int e = VE - 1; e >= 0; --e)
-                            if (r[e] > 0.0f) {
-                                token = (v0 + tstar * kTileVecs + th) * VE + e;
-                                break;
-                            }
-                    }
-                    if (token < 0)
-                        token = (v0 + tstar * kTileVecs + nvec_t) * VE - 1;
-                }
-                p.ws_tok[trow] = token;
-                __threadfence();
             }
             g += 1;
         }
@@ -936,12 +1090,12 @@ int auto_cluster(const spec_verify_ctx *c, int B, int N)
     const int nv = (int)(row_bytes / 16);
     const long long units = (long long)B * (N + 1);
     // about 64 KiB of each row per CTA, at least two CTAs per SM in total,
-    // at most kMaxTiles tiles per chunk, at least one vector per CTA
+    // at most kMaxSlices slices per chunk, at least one vector per CTA
     int C = (int)((row_bytes + 65535) / 65536);
     const long long par = (2LL * c->num_sms + units - 1) / (units > 0 ? units : 1);
     if (par > C)
         C = (int)(par < 8 ? par : 8);
-    const int cmin = (nv + kMaxTiles * kTileVecs - 1) / (kMaxTiles * kTileVecs);
+    const int cmin = (nv + kMaxSlices * kSliceVecs - 1) / (kMaxSlices * kSliceVecs);
     if (C < cmin)
         C = cmin;
     if (C > 8 && cmin <= 8)
@@ -982,7 +1136,7 @@ sv_status run_impl(spec_verify_ctx *ctx, const void *target, const void *draft, 
         return SV_ERR_INVALID_ARG;
     const int C = pick_cluster(ctx, B, N);
     const int nv = ctx->V * elt_bytes(ctx->dtype) / 16;
-    if ((nv + C - 1) / C > kMaxTiles * kTileVecs)
+    if ((nv + C - 1) / C > kMaxSlices * kSliceVecs)
         return SV_ERR_SHAPE;
     const long long units = (long long)B * (N + 1);
     if (units * C > INT_MAX)
@@ -1050,7 +1204,7 @@ sv_status spec_verify_create(spec_verify_ctx **out, int device, int max_B, int m
         return SV_ERR_INVALID_ARG;
     if (V < 1 || ((long long)V * elt_bytes(dtype)) % 16 != 0)
         return SV_ERR_SHAPE;
-    if ((long long)V * elt_bytes(dtype) / 16 > (long long)kMaxCluster * kMaxTiles * kTileVecs)
+    if ((long long)V * elt_bytes(dtype) / 16 > (long long)kMaxCluster * kMaxSlices * kSliceVecs)
         return SV_ERR_SHAPE;
 
     DeviceGuard guard(device);
@@ -1280,7 +1434,7 @@ extern "C" sv_status spec_verify_run_noalloc(const void *target_logits, const vo
     if (B < 0 || N < 0)
         return SV_ERR_INVALID_ARG;
     if (V < 1 || ((long long)V * elt_bytes(dtype)) % 16 != 0 ||
-        (long long)V * elt_bytes(dtype) / 16 > (long long)kMaxCluster * kMaxTiles * kTileVecs)
+        (long long)V * elt_bytes(dtype) / 16 > (long long)kMaxCluster * kMaxSlices * kSliceVecs)
         return SV_ERR_SHAPE;
     if (B > kNoAllocMaxB || (long long)B * (N + 1) > kNoAllocMaxUnits)
         return SV_ERR_TOO_LARGE;
