@@ -42,6 +42,9 @@ _SIGNATURES = [
     ("spec_verify_error_string", ctypes.c_char_p, [_I]),
     ("spec_verify_destroy", None, [_P]),
     ("spec_verify_run_noalloc", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
+    ("spec_verify_profile", _I, [_P, _I]),
+    ("spec_verify_profile_read", _I, [_P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double),
+                                      ctypes.POINTER(_I)]),
 ]
 
 _lib = None
@@ -120,10 +123,21 @@ def spec_verify_destroy(ctx) -> None:
 def spec_verify_run_noalloc(target, draft, draft_tokens, uniforms, temperature, greedy, B, N, V, dtype,
                             out_tokens, num_accepted, stream) -> int:
     """Context-free variant that allocates nothing: scratch is a fixed array
-    inside the library (B <= 2048, B*(N+1) <= 32768), shared by every call on
+    inside the library (B <= 2048, B*(N+1) <= 16384), shared by every call on
     the device, so calls must not overlap on the GPU."""
     return load().spec_verify_run_noalloc(target, draft, draft_tokens, uniforms, temperature,
                                           int(greedy), B, N, V, dtype, out_tokens, num_accepted, stream)
+
+
+def spec_verify_profile(ctx, enable: bool) -> int:
+    return load().spec_verify_profile(ctx, int(bool(enable)))
+
+
+def spec_verify_profile_read(ctx):
+    """(status, ms_rows, ms_sample, runs) summed over the profiled runs."""
+    a, b, n = ctypes.c_double(), ctypes.c_double(), _I()
+    st = load().spec_verify_profile_read(ctx, ctypes.byref(a), ctypes.byref(b), ctypes.byref(n))
+    return st, a.value, b.value, n.value
 
 
 # ---- torch convenience wrapper -------------------------------------------------
@@ -166,6 +180,18 @@ class SpecVerify:
 
     def status(self) -> int:
         return spec_verify_get_status(self.ctx)
+
+    def profile(self, enable: bool):
+        st = spec_verify_profile(self.ctx, enable)
+        if st != SV_OK:
+            raise SpecVerifyError(st, "spec_verify_profile")
+
+    def profile_read(self):
+        """(ms in the row kernel, ms in the sampling kernel, runs)."""
+        st, a, b, n = spec_verify_profile_read(self.ctx)
+        if st != SV_OK:
+            raise SpecVerifyError(st, "spec_verify_profile_read")
+        return a, b, n
 
     def _check(self, target, draft, draft_tokens, uniforms, temperature, greedy):
         import torch

@@ -1,31 +1,26 @@
 // spec_verify.cu -- GB300 (sm_103a) speculative-sampling verify step.
 //
-// One kernel launch per call.  The unit of work is one verified position
-// (sequence b, position i): target row i and, for i < N, draft row i.  A
-// thread-block cluster of C CTAs owns one unit; CTA r of the cluster owns the
-// r-th contiguous column chunk of both rows.
+// Two kernel launches per call.
 //
-// Per CTA (8 consumer warps + 1 producer warp):
-//   pass 1  the producer streams the chunk of both rows through a ring of
-//           shared-memory stages with 1-D TMA bulk copies (mbarrier
-//           complete_tx); consumers keep an online (max, sum of exp) per row,
-//           or (max, argmax) for greedy sequences, and reduce it per CTA.
-//   merge   cluster barrier; every CTA reads the C partials over distributed
-//           shared memory and merges them in rank order, so all CTAs hold the
-//           same row normalisers m, S.  The accept test of position i runs in
-//           double precision on the gathered logits:
-//             accept iff p(d) == 0 or u_i < min(1, q(d)/p(d)),
-//             q(d) = exp((zq_d - mq)/T)/Sq, p(d) = exp((zp_d - mp)/T)/Sp.
-//   pass 2  (only at a rejection, or for the bonus position i == N) the chunk
-//           is streamed again and r_k = max(0, q_k - p_k) (or q_k) is summed
-//           per tile and warp with warp-inclusive scans; chunk masses are
-//           exchanged over the cluster and the CTA whose chunk holds
-//           u_N * R locates the tile, then (pass 3) the warp, lane and
-//           element where the cumulative mass first exceeds it.
-//   ticket  the last unit of a sequence to finish assembles out_tokens and
-//           num_accepted from the per-position results (first rejection j,
-//           token at j) and resets the per-sequence workspace for the next
-//           call, so no memset is ever enqueued.
+// Kernel A (sv_rows_kernel): one verified position (sequence b, position i)
+// per thread-block cluster of C CTAs; CTA r owns the r-th contiguous column
+// chunk of target row i and, for i < N, draft row i.  Per CTA (8 consumer
+// warps + 1 producer warp) the producer streams the chunk through a ring of
+// shared-memory stages with 1-D TMA bulk copies (mbarrier complete_tx) and the
+// consumers keep an online (max, sum of exp) per row, or (max, argmax) for
+// greedy sequences.  The partials are merged over distributed shared memory,
+// and position i is decided from the two gathered logits:
+//     accept iff p(d) == 0 or u_i < min(1, q(d)/p(d)),
+//     q(d) = exp((zq_d - mq)/T)/Sq, p(d) = exp((zp_d - mp)/T)/Sp.
+// A rejection lowers the sequence's first-rejection slot (atomicMin); the row
+// statistics (mq, Sq, mp, Sp) go to the workspace.
+//
+// Kernel B (sv_sample_kernel): one cluster per sequence.  It reads the first
+// rejection j (N if none) and samples the emitted token at j from
+// normalise(max(0, q_j - p_j)) (or the bonus token from q_N) by inverse CDF,
+// writes out_tokens and num_accepted, and resets the workspace for the next
+// call, so no memset is ever enqueued.  Only one row pair per sequence is
+// read a second time.
 //
 // Method: "Speculative decoding -- draft, verify, repeat"
 // (factory.pai-world.com lesson 07-16), section "Core algorithm", steps 3-6;
@@ -57,6 +52,7 @@ constexpr int kStages = 3;
 constexpr int kRingBytes = kStages * 2 * kTileBytes;
 constexpr int kMaxSlices = 128;              // slices per chunk (512 KiB of one row)
 constexpr int kMaxCluster = 16;
+constexpr int kProfRuns = 4096;  // runs whose kernel times one profiling session keeps
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait, then give up
 
 constexpr int kNoReject = 0x7f7f7f7f;        // byte pattern 0x7f: memset-able
@@ -81,40 +77,49 @@ struct SvParams {
     float *p_at;
     float *tstats;
     float *dstats;
-    int *ws_first;   // [max_B]      first rejected position, kNoReject if none
-    int *ws_ticket;  // [max_B]      units of the sequence finished
-    int *ws_err;     // [max_B]      error bits of the sequence
-    int *ws_tok;     // [max_B*(max_N+1)] token sampled at each position
-    int *status;     // sticky error bits of the context
+    int *ws_first;    // [max_B] first rejected position, kNoReject if none
+    int *ws_err;      // [max_B] error bits of the sequence
+    int *ws_tok;      // [max_B*(max_N+1)] greedy argmax of each position
+    float *ws_stats;  // [max_B*(max_N+1)][4] (mq, Sq, mp, Sp) of each position
+    int *status;      // sticky error bits of the context
     int B, N, V, greedy;
 };
 
-// Shared-memory control block (after the ring).  Fields read by peer CTAs over
-// DSMEM are written before a cluster barrier and not rewritten until the next.
-struct SmemCtl {
+// Producer/consumer ring state in shared memory.
+struct Ring {
     uint64_t full[kStages];
     uint64_t empty[kStages];
-    int last_g[kStages];   // last ring position issued into each stage
+    int last_g[kStages];  // last ring position issued into each stage
     int abort;
-    // published to the cluster
+};
+
+// Shared-memory control blocks (after the ring).  Fields read by peer CTAs
+// over DSMEM are written before a cluster barrier and not rewritten after it.
+struct CtlA {
+    Ring ring;
+    float cf;                      // log2(e) / T
     float pm_t, ps_t, pm_d, ps_d;  // sampled partials (target, draft)
     float gv;                      // greedy partial
     int gi, gnan;
-    float Rc;                      // residual mass of this CTA's chunk
-    int go;                        // rank 0: this position samples its token
-    // values broadcast inside the CTA
-    int need_res, reject, errb, tok, go_all, retry, cstar, tstar;
-    float cf, mq, isq, mp, isp;
-    float x1, x2;
-    // reduction scratch
+    float zq_d, zp_d, u_i;         // the decision's inputs
     float red_m[kConsWarps], red_s[kConsWarps], red_m2[kConsWarps], red_s2[kConsWarps];
     int red_i[kConsWarps], red_n[kConsWarps];
+};
+
+struct CtlB {
+    Ring ring;
+    float cf;
+    float Rc;  // residual mass of this CTA's chunk (published)
+    int ab;    // this CTA gave up a wait (published)
+    int retry, cstar, tstar, any_abort;
+    float x1, x2;
     float incl[kConsThreads];
     float wsum[kMaxSlices][kConsWarps];  // per slice and warp: residual mass
     float tcum[kMaxSlices];              // inclusive prefix of slice masses
 };
 
-constexpr size_t kSmemBytes = kRingBytes + sizeof(SmemCtl);
+constexpr size_t kSmemA = kRingBytes + sizeof(CtlA);
+constexpr size_t kSmemB = kRingBytes + sizeof(CtlB);
 
 template <int DT> struct Elt;
 template <> struct Elt<SV_F32> {
@@ -365,8 +370,10 @@ __device__ __forceinline__ ArgMax warp_argmax(ArgMax a)
 
 // ---- residual mass of one 16-byte vector --------------------------------------
 // r_k = max(0, q_k - p_k) (RES_DIFF) or q_k (RES_Q), with
-// q_k = 2^((zq_k - mq) c) / Sq.  Explicit round-to-nearest intrinsics keep the
-// result bit-identical wherever it is recomputed (pass 2 and pass 3).
+// q_k = 2^((zq_k - mq) c) / Sq.  Target and draft element k travel as one
+// f32x2 pair.  Every operation rounds to nearest and nothing is contracted,
+// so the result is bit-identical wherever it is recomputed (pass 2 and
+// pass 3).
 template <int DT>
 __device__ __forceinline__ void residual_vec(const uint4 vt, const uint4 vd, int res_mode, float mq,
                                              float isq, float mp, float isp, float cf, float *r)
@@ -374,16 +381,24 @@ __device__ __forceinline__ void residual_vec(const uint4 vt, const uint4 vd, int
     constexpr int NE = Elt<DT>::kPerVec;
     float zt[NE], zd[NE];
     unpack<DT>(vt, zt);
-    if (res_mode == RES_DIFF)
+    const unsigned long long Cf = sv::pack2(cf, cf);
+    if (res_mode == RES_DIFF) {
         unpack<DT>(vd, zd);
+        const unsigned long long M = sv::pack2(mq, mp), IS = sv::pack2(isq, isp);
 #pragma unroll
-    for (int e = 0; e < NE; ++e) {
-        const float qk = __fmul_rn(sv::ex2(__fmul_rn(__fsub_rn(zt[e], mq), cf)), isq);
-        if (res_mode == RES_DIFF) {
-            const float pk = __fmul_rn(sv::ex2(__fmul_rn(__fsub_rn(zd[e], mp), cf)), isp);
+        for (int e = 0; e < NE; ++e) {
+            float a0, a1, qk, pk;
+            sv::unpack2(sv::mul2(sv::sub2(sv::pack2(zt[e], zd[e]), M), Cf), a0, a1);
+            sv::unpack2(sv::mul2(sv::pack2(sv::ex2(a0), sv::ex2(a1)), IS), qk, pk);
             r[e] = fmaxf(__fsub_rn(qk, pk), 0.0f);
-        } else {
-            r[e] = qk;
+        }
+    } else {
+        const unsigned long long M = sv::pack2(mq, mq), IS = sv::pack2(isq, isq);
+#pragma unroll
+        for (int e = 0; e < NE; e += 2) {
+            float a0, a1;
+            sv::unpack2(sv::mul2(sv::sub2(sv::pack2(zt[e], zt[e + 1]), M), Cf), a0, a1);
+            sv::unpack2(sv::mul2(sv::pack2(sv::ex2(a0), sv::ex2(a1)), IS), r[e], r[e + 1]);
         }
     }
 }
@@ -399,137 +414,173 @@ __device__ __forceinline__ float warp_incl_scan(float x, int lane)
     return x;
 }
 
-// ---- ring producer -----------------------------------------------------------
-// Issues tiles [0, ntiles) of the chunk (or the single tile `only`) into ring
-// positions g, g+1, ...  Runs on one lane of the producer warp.
-__device__ __forceinline__ void produce(SmemCtl &ctl, unsigned char *ring, const uint4 *tsrc,
-                                        const uint4 *dsrc, int nvec_chunk, int t_begin, int t_end,
-                                        uint32_t g)
+// ---- ring of shared-memory stages fed by TMA bulk copies --------------------
+// Issues ring tiles [t_begin, t_end) of the chunk into ring positions g, g+1,
+// ...  Runs on one lane of the producer warp.
+__device__ __forceinline__ void produce(Ring &rg, unsigned char *ring, const uint4 *tsrc, const uint4 *dsrc,
+                                        int nvec_chunk, int t_begin, int t_end, uint32_t g)
 {
     for (int t = t_begin; t < t_end; ++t, ++g) {
         const uint32_t s = g % kStages;
         const uint32_t ph = (g / kStages) & 1u;
-        if (!sv::mbar_wait_bounded(&ctl.empty[s], ph ^ 1u, &ctl.abort, kWaitLimitNs)) {
-            ctl.abort = 1;
+        if (!sv::mbar_wait_bounded(&rg.empty[s], ph ^ 1u, &rg.abort, kWaitLimitNs)) {
+            rg.abort = 1;
             return;
         }
         const int nvec = min(kTileVecs, nvec_chunk - t * kTileVecs);
         const uint32_t bytes = static_cast<uint32_t>(nvec) * 16u;
-        sv::mbar_arrive_expect_tx(&ctl.full[s], dsrc ? 2u * bytes : bytes);
+        sv::mbar_arrive_expect_tx(&rg.full[s], dsrc ? 2u * bytes : bytes);
         unsigned char *stage = ring + s * (2 * kTileBytes);
-        sv::bulk_g2s(stage, tsrc + (size_t)t * kTileVecs, bytes, &ctl.full[s]);
+        sv::bulk_g2s(stage, tsrc + (size_t)t * kTileVecs, bytes, &rg.full[s]);
         if (dsrc)
-            sv::bulk_g2s(stage + kTileBytes, dsrc + (size_t)t * kTileVecs, bytes, &ctl.full[s]);
-        ctl.last_g[s] = static_cast<int>(g);
+            sv::bulk_g2s(stage + kTileBytes, dsrc + (size_t)t * kTileVecs, bytes, &rg.full[s]);
+        rg.last_g[s] = static_cast<int>(g);
     }
 }
 
 // Consumer side: wait until ring position g is filled.
-__device__ __forceinline__ bool consume_wait(SmemCtl &ctl, uint32_t g)
+__device__ __forceinline__ bool consume_wait(Ring &rg, uint32_t g)
 {
     const uint32_t s = g % kStages;
-    return sv::mbar_wait_bounded(&ctl.full[s], (g / kStages) & 1u, &ctl.abort, kWaitLimitNs);
+    return sv::mbar_wait_bounded(&rg.full[s], (g / kStages) & 1u, &rg.abort, kWaitLimitNs);
 }
 
-__device__ __forceinline__ void consume_release(SmemCtl &ctl, uint32_t g, int lane)
+__device__ __forceinline__ void consume_release(Ring &rg, uint32_t g, int lane)
 {
     __syncwarp();
     if (lane == 0)
-        sv::mbar_arrive(&ctl.empty[g % kStages]);
+        sv::mbar_arrive(&rg.empty[g % kStages]);
 }
 
+// Called by thread 0 before the first __syncthreads of a kernel.
+__device__ __forceinline__ void ring_init(Ring &rg)
+{
+    for (int s = 0; s < kStages; ++s) {
+        sv::mbar_init(&rg.full[s], 1);
+        sv::mbar_init(&rg.empty[s], kConsWarps);
+        rg.last_g[s] = -1;
+    }
+    rg.abort = 0;
+    sv::fence_mbar_init();
+}
+
+// After an abort: never leave with a bulk copy still writing into this CTA's
+// shared memory (bounded wait on the last copy issued into each stage).
+__device__ __forceinline__ void ring_drain(Ring &rg)
+{
+    for (int s = 0; s < kStages; ++s) {
+        const int lg = rg.last_g[s];
+        if (lg >= 0) {
+            int never = 0;
+            sv::mbar_wait_bounded(&rg.full[s], ((uint32_t)lg / kStages) & 1u, &never, kWaitLimitNs / 4);
+        }
+    }
+}
+
+__device__ __forceinline__ int sequence_mode(const SvParams &p, int b, float &T)
+{
+    T = 0.0f;
+    if (p.greedy)
+        return MODE_GREEDY;
+    T = p.T[b];
+    if (T != T)
+        return MODE_INVALID;
+    if (T <= 0.0f)
+        return MODE_GREEDY;
+    if (T == INFINITY || T < FLT_MIN)
+        return MODE_INVALID;
+    return MODE_SAMPLED;
+}
+
+// Column chunk of CTA `rank` of `C`, in 16-byte vectors.
+struct Chunk {
+    int v0, nvec, ntiles, nslices;
+};
+
+__device__ __forceinline__ Chunk chunk_of(int NV, uint32_t rank, uint32_t C)
+{
+    Chunk c;
+    c.v0 = (int)((long long)NV * rank / C);
+    const int v1 = (int)((long long)NV * (rank + 1) / C);
+    c.nvec = v1 - c.v0;
+    c.ntiles = (c.nvec + kTileVecs - 1) / kTileVecs;
+    c.nslices = (c.nvec + kSliceVecs - 1) / kSliceVecs;
+    return c;
+}
+
+// =============================================================================
+// Kernel A: row normalisers and accept decisions, one cluster per position
+// =============================================================================
+//
+// Positions are taken in descending order (all sequences at position N, then
+// N-1, ..., then 0) so that position 0, where most first rejections happen,
+// is read last and is still in L2 when kernel B samples there.
 template <int DT>
-__global__ void __launch_bounds__(kThreads, 4) sv_verify_kernel(const SvParams p)
+__global__ void __launch_bounds__(kThreads, 4) sv_rows_kernel(const SvParams p)
 {
     constexpr int VE = Elt<DT>::kPerVec;
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char *ring = smem;
-    SmemCtl &ctl = *reinterpret_cast<SmemCtl *>(smem + kRingBytes);
+    CtlA &ctl = *reinterpret_cast<CtlA *>(smem + kRingBytes);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t C = sv::cluster_nctarank();
     const uint32_t rank = sv::cluster_ctarank();
     const int N = p.N, V = p.V;
-    // Units are ordered position-major (all sequences at position 0, then 1,
-    // ...), so when position i is decided the earlier positions of the same
-    // sequence have usually been decided already.
     const int unit = blockIdx.x / C;
-    const int i = unit / p.B;
-    const int b = unit - i * p.B;
+    const int pos = unit / p.B;
+    const int i = N - pos;
+    const int b = unit - pos * p.B;
 
-    int mode;
-    float T = 0.0f;
-    if (p.greedy) {
-        mode = MODE_GREEDY;
-    } else {
-        T = p.T[b];
-        if (T != T)
-            mode = MODE_INVALID;
-        else if (T <= 0.0f)
-            mode = MODE_GREEDY;
-        else if (T == INFINITY || T < FLT_MIN)
-            mode = MODE_INVALID;
-        else
-            mode = MODE_SAMPLED;
-    }
+    float T;
+    const int mode = sequence_mode(p, b, T);
     const bool has_draft = (mode == MODE_SAMPLED) && (i < N);
     const int d = (i < N) ? p.tokens[(size_t)b * N + i] : 0;
     const bool bad_d = (i < N) && (d < 0 || d >= V);
 
-    // column chunk of this CTA, in 16-byte vectors
-    const int NV = V / VE;
-    const int v0 = (int)((long long)NV * rank / C);
-    const int v1 = (int)((long long)NV * (rank + 1) / C);
-    const int nvec_chunk = v1 - v0;
-    const int ntiles = (nvec_chunk + kTileVecs - 1) / kTileVecs;    // ring tiles
-    const int nslices = (nvec_chunk + kSliceVecs - 1) / kSliceVecs; // scan slices
-
+    const Chunk ch = chunk_of(V / VE, rank, C);
     const size_t trow = (size_t)b * (N + 1) + i;
     const size_t drow = (size_t)b * N + i;
-    const size_t row_vecs = (size_t)NV;
-    const uint4 *tsrc = static_cast<const uint4 *>(p.target) + trow * row_vecs + v0;
-    const uint4 *dsrc = has_draft ? static_cast<const uint4 *>(p.draft) + drow * row_vecs + v0 : nullptr;
+    const size_t row_vecs = (size_t)(V / VE);
+    const uint4 *tsrc = static_cast<const uint4 *>(p.target) + trow * row_vecs + ch.v0;
+    const uint4 *dsrc = has_draft ? static_cast<const uint4 *>(p.draft) + drow * row_vecs + ch.v0 : nullptr;
 
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            sv::mbar_init(&ctl.full[s], 1);
-            sv::mbar_init(&ctl.empty[s], kConsWarps);
-            ctl.last_g[s] = -1;
-        }
-        ctl.abort = 0;
-        ctl.need_res = 0;
-        ctl.retry = 0;
-        ctl.cstar = -1;
-        // log2(e)/T, rounded once from double
-        ctl.cf = (mode == MODE_SAMPLED) ? (float)(kLog2e / (double)T) : 0.0f;
-        sv::fence_mbar_init();
+        ring_init(ctl.ring);
+        ctl.cf = (mode == MODE_SAMPLED) ? (float)(kLog2e / (double)T) : 0.0f;  // log2(e)/T
+    }
+    // The decision's inputs are loaded by an idle lane of the producer warp at
+    // the start and parked in shared memory after pass 1.
+    const bool prefetcher = rank == 0 && tid == 32 * kProducerWarp + 1;
+    float pre_zq = 0.0f, pre_zp = 0.0f, pre_u = 0.0f;
+    if (prefetcher && mode == MODE_SAMPLED && i < N && !bad_d) {
+        pre_zq = logit_at<DT>(p.target, trow * (size_t)V + d);
+        pre_zp = logit_at<DT>(p.draft, drow * (size_t)V + d);
+        pre_u = p.u[trow];
     }
     __syncthreads();
     const float cf = ctl.cf;
 
-    uint32_t g = 0;  // ring position, advanced identically by every thread
-
-    // ------------------------------------------------------------ pass 1
+    // ---- pass 1: stream the chunk of both rows once
     Online2 ot2{-INFINITY, 0ull}, od2{-INFINITY, 0ull};  // 0ull = (+0.0f, +0.0f)
     ArgMax ga{-INFINITY, INT_MAX, 0};
     if (mode != MODE_INVALID) {
         if (warp == kProducerWarp) {
             if (lane == 0)
-                produce(ctl, ring, tsrc, dsrc, nvec_chunk, 0, ntiles, g);
+                produce(ctl.ring, ring, tsrc, dsrc, ch.nvec, 0, ch.ntiles, 0);
             __syncwarp();
         } else {
-            for (int t = 0; t < ntiles; ++t) {
-                const uint32_t gt = g + t;
-                if (consume_wait(ctl, gt)) {
-                    const unsigned char *stage = ring + (gt % kStages) * (2 * kTileBytes);
+            for (int t = 0; t < ch.ntiles; ++t) {
+                if (consume_wait(ctl.ring, t)) {
+                    const unsigned char *stage = ring + (t % kStages) * (2 * kTileBytes);
 #pragma unroll
                     for (int k = 0; k < kVPT; ++k) {
                         const int sv_ = k * kSliceVecs + tid;  // vector within the stage
                         const int vec = t * kTileVecs + sv_;
-                        if (vec < nvec_chunk) {
+                        if (vec < ch.nvec) {
                             const uint4 vt = reinterpret_cast<const uint4 *>(stage)[sv_];
                             if (mode == MODE_GREEDY) {
-                                argmax_add2<DT>(ga, vt, (v0 + vec) * VE);
+                                argmax_add2<DT>(ga, vt, (ch.v0 + vec) * VE);
                             } else {
                                 online_add2<DT>(ot2, vt, cf);
                                 if (has_draft)
@@ -538,15 +589,20 @@ __global__ void __launch_bounds__(kThreads, 4) sv_verify_kernel(const SvParams p
                         }
                     }
                 } else {
-                    ctl.abort = 1;
+                    ctl.ring.abort = 1;
                 }
-                consume_release(ctl, gt, lane);
+                consume_release(ctl.ring, t, lane);
             }
         }
-        g += ntiles;
     }
 
-    // CTA partial
+    if (prefetcher) {
+        ctl.zq_d = pre_zq;
+        ctl.zp_d = pre_zp;
+        ctl.u_i = pre_u;
+    }
+
+    // ---- CTA partial
     Online ot = online_fold(ot2), od = online_fold(od2);
     if (warp < kConsWarps) {
         if (mode == MODE_GREEDY) {
@@ -588,15 +644,15 @@ __global__ void __launch_bounds__(kThreads, 4) sv_verify_kernel(const SvParams p
             ctl.ps_d = e.s;
         }
     }
-    sv::cluster_sync();  // #1: partials visible cluster-wide
+    if (C > 1)
+        sv::cluster_sync();  // partials visible cluster-wide
+    else
+        __syncthreads();
 
-    // ------------------------------------------------------------ merge + decide
-    // Warp 0 merges the C partials (lane r reads CTA r over DSMEM) with a
-    // butterfly whose result is the same in every lane and every CTA of the
-    // cluster; lane 0 then decides position i.
-    if (warp == 0) {
-        int errb = bad_d ? kErrBadToken : 0;
-        int need_res = 0, reject = 0, tok = -1;
+    // ---- merge over the cluster and decide (rank 0 only: the others are done)
+    // Warp 0 merges the C partials (lane r reads CTA r over DSMEM); lane 0
+    // decides position i and records the outcome for kernel B.
+    if (rank == 0 && warp == 0) {
         if (mode == MODE_GREEDY) {
             ArgMax a{-INFINITY, INT_MAX, 0};
             if (lane < (int)C) {
@@ -606,15 +662,19 @@ __global__ void __launch_bounds__(kThreads, 4) sv_verify_kernel(const SvParams p
             }
             a = warp_argmax(a);
             if (lane == 0) {
+                int errb = bad_d ? kErrBadToken : 0;
                 if (a.nan || a.v == INFINITY || a.v == -INFINITY)
                     errb |= kErrBadValue;
-                tok = a.i;
-                reject = (i < N) && (d != a.i);
-                if (rank == 0 && p.tstats) {
+                p.ws_tok[trow] = a.i;
+                if (i < N && d != a.i)
+                    atomicMin(&p.ws_first[b], i);
+                if (errb)
+                    atomicOr(&p.ws_err[b], errb);
+                if (p.tstats) {
                     p.tstats[trow * 2 + 0] = a.v;
                     p.tstats[trow * 2 + 1] = NAN;
                 }
-                if (rank == 0 && i < N) {
+                if (i < N) {
                     if (p.q_at)
                         p.q_at[drow] = NAN;
                     if (p.p_at)
@@ -638,358 +698,124 @@ __global__ void __launch_bounds__(kThreads, 4) sv_verify_kernel(const SvParams p
             t = warp_merge(t, cf);
             e = warp_merge(e, cf);
             if (lane == 0) {
+                int errb = bad_d ? kErrBadToken : 0;
                 const float mq = t.m, Sq = t.s, mp = e.m, Sp = e.s;
                 bool valid = isfinite(mq) && isfinite(Sq) && Sq > 0.0f;
                 if (has_draft)
                     valid = valid && isfinite(mp) && isfinite(Sp) && Sp > 0.0f;
                 if (!valid) {
                     errb |= kErrBadValue;
-                } else if (i < N) {
-                    if (!bad_d) {
-                        // accept iff p(d) == 0 or u < min(1, q(d)/p(d)), with
-                        // q(d)/p(d) = 2^L * Sp/Sq, L = ((zq-mq) - (zp-mp)) log2(e)/T
-                        const float zq = logit_at<DT>(p.target, trow * (size_t)V + d);
-                        const float zp = logit_at<DT>(p.draft, drow * (size_t)V + d);
-                        const double ui = (double)p.u[trow];
-                        const double invT = 1.0 / (double)T;
-                        const double xq = ((double)zq - (double)mq) * invT;
-                        const double xp = ((double)zp - (double)mp) * invT;
-                        bool accept;
-                        if (zp == -INFINITY) {
-                            accept = true;  // p(d) = 0
-                        } else if (zq == -INFINITY) {
-                            accept = false;  // q(d) = 0 and u < 0 never holds
-                        } else if (xq < -700.0 || xp < -700.0) {
-                            // near double underflow: evaluate q(d), p(d) as the definition does
-                            const double qd = exp(xq) / (double)Sq, pd = exp(xp) / (double)Sp;
-                            accept = (pd == 0.0) || (ui < fmin(1.0, qd / pd));
-                        } else {
-                            const double L = (xq - xp) * kLog2e;
-                            const double n = floor(L);
-                            const float frac = (float)(L - n);
-                            const double ratio = ldexp((double)(sv::ex2(frac) * (Sp / Sq)), (int)n);
-                            accept = ui < fmin(1.0, ratio);
-                        }
-                        reject = !accept;
-                        need_res = reject;
-                        if (rank == 0) {
-                            if (p.q_at)
-                                p.q_at[drow] = (float)(exp(xq) / (double)Sq);
-                            if (p.p_at)
-                                p.p_at[drow] = (float)(exp(xp) / (double)Sp);
-                        }
+                } else if (i < N && !bad_d) {
+                    // accept iff p(d) == 0 or u < min(1, q(d)/p(d)), with
+                    // q(d)/p(d) = 2^L * Sp/Sq, L = ((zq-mq) - (zp-mp)) log2(e)/T
+                    const float zq = ctl.zq_d, zp = ctl.zp_d;
+                    const double ui = (double)ctl.u_i;
+                    const double invT = 1.0 / (double)T;
+                    const double xq = ((double)zq - (double)mq) * invT;
+                    const double xp = ((double)zp - (double)mp) * invT;
+                    bool accept;
+                    if (zp == -INFINITY) {
+                        accept = true;  // p(d) = 0
+                    } else if (zq == -INFINITY) {
+                        accept = false;  // q(d) = 0 and u < 0 never holds
+                    } else if (xq < -700.0 || xp < -700.0) {
+                        // near double underflow: evaluate q(d), p(d) as the definition does
+                        const double qd = exp(xq) / (double)Sq, pd = exp(xp) / (double)Sp;
+                        accept = (pd == 0.0) || (ui < fmin(1.0, qd / pd));
+                    } else {
+                        const double L = (xq - xp) * kLog2e;
+                        const double n = floor(L);
+                        const float frac = (float)(L - n);
+                        const double ratio = ldexp((double)(sv::ex2(frac) * (Sp / Sq)), (int)n);
+                        accept = ui < fmin(1.0, ratio);
                     }
-                } else {
-                    need_res = 1;  // bonus token from q_N
+                    if (!accept)
+                        atomicMin(&p.ws_first[b], i);
+                    if (p.q_at)
+                        p.q_at[drow] = (float)(exp(xq) / (double)Sq);
+                    if (p.p_at)
+                        p.p_at[drow] = (float)(exp(xp) / (double)Sp);
                 }
-                if (rank == 0) {
-                    if (p.tstats) {
-                        p.tstats[trow * 2 + 0] = mq;
-                        p.tstats[trow * 2 + 1] = Sq;
-                    }
-                    if (p.dstats && has_draft) {
-                        p.dstats[drow * 2 + 0] = mp;
-                        p.dstats[drow * 2 + 1] = Sp;
-                    }
+                float *st = p.ws_stats + trow * 4;
+                st[0] = mq;
+                st[1] = Sq;
+                st[2] = mp;
+                st[3] = Sp;
+                if (errb)
+                    atomicOr(&p.ws_err[b], errb);
+                if (p.tstats) {
+                    p.tstats[trow * 2 + 0] = mq;
+                    p.tstats[trow * 2 + 1] = Sq;
                 }
-                ctl.mq = mq;
-                ctl.isq = 1.0f / Sq;
-                ctl.mp = mp;
-                ctl.isp = has_draft ? 1.0f / Sp : 0.0f;
+                if (p.dstats && has_draft) {
+                    p.dstats[drow * 2 + 0] = mp;
+                    p.dstats[drow * 2 + 1] = Sp;
+                }
             }
-        } else {
-            errb |= kErrBadValue;
-        }
-        if (lane == 0) {
-            if (errb)
-                need_res = 0;
-            ctl.errb = errb;
-            ctl.need_res = need_res;
-            ctl.reject = reject;
-            ctl.tok = tok;
+        } else if (lane == 0) {
+            atomicOr(&p.ws_err[b], kErrBadValue | (bad_d ? kErrBadToken : 0));
         }
     }
-    __syncthreads();
-
-    // Rank 0 records the outcome for the sequence.  A rejecting (or bonus)
-    // position learns whether an earlier position has already rejected: if so
-    // its sample can never be emitted and is skipped.
-    if (rank == 0 && tid == 0) {
-        if (ctl.errb)
-            atomicOr(&p.ws_err[b], ctl.errb);
-        int prior = kNoReject;
-        if (ctl.reject)
-            prior = atomicMin(&p.ws_first[b], i);
-        else if (ctl.need_res)
-            prior = atomicAdd(&p.ws_first[b], 0);
-        if (mode == MODE_GREEDY)
-            p.ws_tok[trow] = ctl.tok;
-        ctl.go = (ctl.need_res && prior > i) ? 1 : 0;
-    }
-    int go = 0;
-    if (ctl.need_res) {      // same value in every CTA of the cluster
-        sv::cluster_sync();  // #1b: rank 0's verdict visible
-        if (tid == 0)
-            ctl.go_all = sv::ld_dsmem_s32(sv::dsmem_addr(&ctl.go, 0));
-        __syncthreads();
-        go = ctl.go_all;
-    }
-
-    // ------------------------------------------------------------ residual / bonus
-    if (go) {
-        int res_mode = (i < N) ? RES_DIFF : RES_Q;  // RES_Q after a retry as well
-        const float mq = ctl.mq, isq = ctl.isq, mp = ctl.mp, isp = ctl.isp;
-        const float uN = p.u[(size_t)b * (N + 1) + N];
-        for (;;) {
-            // pass 2: residual mass per tile and warp
-            const uint4 *dres = (res_mode == RES_DIFF) ? dsrc : nullptr;
-            if (warp == kProducerWarp) {
-                if (lane == 0)
-                    produce(ctl, ring, tsrc, dres, nvec_chunk, 0, ntiles, g);
-                __syncwarp();
-            } else {
-                for (int t = 0; t < ntiles; ++t) {
-                    const uint32_t gt = g + t;
-                    float part[kVPT];
-                    const bool ok = consume_wait(ctl, gt);
-                    if (!ok)
-                        ctl.abort = 1;
-                    const unsigned char *stage = ring + (gt % kStages) * (2 * kTileBytes);
-#pragma unroll
-                    for (int k = 0; k < kVPT; ++k) {
-                        part[k] = 0.0f;
-                        const int sv_ = k * kSliceVecs + tid;
-                        const int vec = t * kTileVecs + sv_;
-                        if (ok && vec < nvec_chunk) {
-                            float r[VE];
-                            const uint4 vd = dres ? reinterpret_cast<const uint4 *>(stage + kTileBytes)[sv_]
-                                                  : make_uint4(0, 0, 0, 0);
-                            residual_vec<DT>(reinterpret_cast<const uint4 *>(stage)[sv_], vd, res_mode, mq,
-                                             isq, mp, isp, cf, r);
-#pragma unroll
-                            for (int e = 0; e < VE; ++e)
-                                part[k] = __fadd_rn(part[k], r[e]);
-                        }
-                    }
-                    consume_release(ctl, gt, lane);
-#pragma unroll
-                    for (int k = 0; k < kVPT; ++k) {
-                        const int sl = t * kVPT + k;
-                        const float incl = warp_incl_scan(part[k], lane);
-                        if (lane == 31 && sl < nslices)
-                            ctl.wsum[sl][warp] = incl;
-                    }
-                }
-            }
-            g += ntiles;
-            __syncthreads();
-            if (warp == 0) {
-                // slice masses and their inclusive prefix over the chunk
-                float carry = 0.0f;
-                for (int t0 = 0; t0 < nslices; t0 += 32) {
-                    const int t = t0 + lane;
-                    float tm = 0.0f;
-                    if (t < nslices)
-#pragma unroll
-                        for (int w = 0; w < kConsWarps; ++w)
-                            tm = __fadd_rn(tm, ctl.wsum[t][w]);
-                    const float inc = __fadd_rn(warp_incl_scan(tm, lane), carry);
-                    if (t < nslices)
-                        ctl.tcum[t] = inc;
-                    carry = __shfl_sync(0xffffffffu, inc, 31);
-                }
-                if (lane == 0)
-                    ctl.Rc = carry;
-            }
-            sv::cluster_sync();  // #2: chunk masses visible
-            if (warp == 0) {
-                // chunk c* whose cumulative mass first exceeds u_N * R
-                const float Rr = (lane < (int)C) ? sv::ld_dsmem_f32(sv::dsmem_addr(&ctl.Rc, lane)) : 0.0f;
-                const float cum = warp_incl_scan(Rr, lane);
-                const float Rt = __shfl_sync(0xffffffffu, cum, 31);
-                const float x = __fmul_rn(uN, Rt);
-                const unsigned hit = __ballot_sync(0xffffffffu, lane < (int)C && x < cum);
-                int cs;
-                float x1;
-                if (hit) {
-                    cs = __ffs(hit) - 1;
-                    const float prev = __shfl_sync(0xffffffffu, cum, cs > 0 ? cs - 1 : 0);
-                    x1 = __fsub_rn(x, cs > 0 ? prev : 0.0f);
-                } else {  // rounding: the last chunk that has mass
-                    const unsigned pos = __ballot_sync(0xffffffffu, lane < (int)C && Rr > 0.0f);
-                    cs = pos ? 31 - __clz(pos) : (int)C - 1;
-                    x1 = INFINITY;
-                }
-                if (lane == 0) {
-                    ctl.retry = (Rt == 0.0f && res_mode == RES_DIFF) ? 1 : 0;
-                    ctl.cstar = cs;
-                    ctl.x1 = x1;
-                }
-            }
-            __syncthreads();
-            if (!ctl.retry)
-                break;
-            res_mode = RES_Q;    // q_j == p_j: draw from q_j instead
-            sv::cluster_sync();  // #2b: peers are done reading ctl.Rc
-        }
-
-        if ((int)rank == ctl.cstar) {
-            if (warp == 0) {
-                // slice s* of the chunk, and the target relative to its start
-                const float x1 = ctl.x1;
-                int ts = -1;
-                float x2 = INFINITY;
-                if (x1 != INFINITY) {
-                    for (int t0 = 0; t0 < nslices && ts < 0; t0 += 32) {
-                        const int t = t0 + lane;
-                        const unsigned m = __ballot_sync(0xffffffffu, t < nslices && x1 < ctl.tcum[t]);
-                        if (m)
-                            ts = t0 + __ffs(m) - 1;
-                    }
-                    if (ts >= 0)
-                        x2 = __fsub_rn(x1, ts > 0 ? ctl.tcum[ts - 1] : 0.0f);
-                }
-                if (ts < 0) {  // rounding: the last slice that has mass
-                    for (int t0 = ((nslices - 1) / 32) * 32; t0 >= 0 && ts < 0; t0 -= 32) {
-                        const int t = t0 + lane;
-                        float tm = 0.0f;
-                        if (t < nslices)
-                            for (int w = 0; w < kConsWarps; ++w)
-                                tm += ctl.wsum[t][w];
-                        const unsigned m = __ballot_sync(0xffffffffu, tm > 0.0f);
-                        if (m)
-                            ts = t0 + 31 - __clz(m);
-                    }
-                    if (ts < 0)
-                        ts = nslices - 1;
-                    x2 = INFINITY;
-                }
-                if (lane == 0) {
-                    ctl.tstar = ts;
-                    ctl.x2 = x2;
-                }
-            }
-            __syncthreads();
-            const int sstar = ctl.tstar;              // slice
-            const int tstar = sstar / kVPT;           // ring tile holding it
-            const int kstar = sstar - tstar * kVPT;   // its place in the stage
-            // pass 3: reload the tile of slice s*, redo its warp scans, find the element
-            const uint4 *dres = (res_mode == RES_DIFF) ? dsrc : nullptr;
-            if (warp == kProducerWarp) {
-                if (lane == 0)
-                    produce(ctl, ring, tsrc, dres, nvec_chunk, tstar, tstar + 1, g);
-                __syncwarp();
-            } else {
-                float part = 0.0f;
-                if (consume_wait(ctl, g)) {
-                    const int vec = sstar * kSliceVecs + tid;
-                    if (vec < nvec_chunk) {
-                        const unsigned char *stage = ring + (g % kStages) * (2 * kTileBytes);
-                        const int sv_ = kstar * kSliceVecs + tid;
-                        float r[VE];
-                        const uint4 vd = dres ? reinterpret_cast<const uint4 *>(stage + kTileBytes)[sv_]
-                                              : make_uint4(0, 0, 0, 0);
-                        residual_vec<DT>(reinterpret_cast<const uint4 *>(stage)[sv_], vd, res_mode, mq, isq,
-                                         mp, isp, cf, r);
-#pragma unroll
-                        for (int e = 0; e < VE; ++e)
-                            part = __fadd_rn(part, r[e]);
-                    }
-                } else {
-                    ctl.abort = 1;
-                }
-                ctl.incl[tid] = warp_incl_scan(part, lane);
-            }
-            __syncthreads();
-            if (warp == 0) {
-                const int nvec_t = min(kSliceVecs, nvec_chunk - sstar * kSliceVecs);
-                const float x2 = ctl.x2;
-                const float wt = (lane < kConsWarps) ? ctl.incl[lane * 32 + 31] : 0.0f;
-                const float wc = warp_incl_scan(wt, lane);
-                int sel = -1;
-                float xl = 0.0f;
-                const unsigned mw = __ballot_sync(0xffffffffu, lane < kConsWarps && x2 < wc);
-                if (mw) {
-                    const int ws = __ffs(mw) - 1;
-                    const float wprev = __shfl_sync(0xffffffffu, wc, ws > 0 ? ws - 1 : 0);
-                    const float xw = __fsub_rn(x2, ws > 0 ? wprev : 0.0f);
-                    const float li = ctl.incl[ws * 32 + lane];
-                    const unsigned ml = __ballot_sync(0xffffffffu, xw < li);
-                    if (ml) {
-                        const int ls = __ffs(ml) - 1;
-                        const float lprev = __shfl_sync(0xffffffffu, li, ls > 0 ? ls - 1 : 0);
-                        sel = ws * 32 + ls;
-                        xl = __fsub_rn(xw, ls > 0 ? lprev : 0.0f);
-                    }
-                }
-                if (lane == 0) {
-                    const unsigned char *stage = ring + (g % kStages) * (2 * kTileBytes);
-                    auto thread_r = [&](int th, float *r) {
-                        const int sv_ = kstar * kSliceVecs + th;
-                        const uint4 vd = dres ? reinterpret_cast<const uint4 *>(stage + kTileBytes)[sv_]
-                                              : make_uint4(0, 0, 0, 0);
-                        residual_vec<DT>(reinterpret_cast<const uint4 *>(stage)[sv_], vd, res_mode, mq, isq, mp,
-                                         isp, cf, r);
-                    };
-                    int token = -1;
-                    if (sel >= 0 && sel < nvec_t) {
-                        float r[VE];
-                        thread_r(sel, r);
-                        float acc = 0.0f;
-                        for (int e = 0; e < VE; ++e) {
-                            acc = __fadd_rn(acc, r[e]);
-                            if (xl < acc) {
-                                token = (v0 + sstar * kSliceVecs + sel) * VE + e;
-                                break;
-                            }
-                        }
-                    }
-                    if (token < 0) {
-                        // rounding left the target at or past the total: the
-                        // last element of the tile that carries mass
-                        for (int th = nvec_t - 1; th >= 0 && token < 0; --th) {
-                            float r[VE];
-                            thread_r(th, r);
-                            for (int e = VE - 1; e >= 0; --e)
-                                if (r[e] > 0.0f) {
-                                    token = (v0 + sstar * kSliceVecs + th) * VE + e;
-                                    break;
-                                }
-                        }
-                        if (token < 0)
-                            token = (v0 + sstar * kSliceVecs + nvec_t) * VE - 1;
-                    }
-                    p.ws_tok[trow] = token;
-                    __threadfence();
-                }
-            }
-            g += 1;
-        }
-    }
-
-    if (tid == 0 && ctl.abort) {
+    if (tid == 0 && ctl.ring.abort)
         atomicOr(&p.ws_err[b], kErrTimeout);
-        __threadfence();
-    }
-    sv::cluster_sync();  // #3: no peer reads this CTA's shared memory any more
+    if (C > 1)
+        sv::cluster_sync();  // no peer reads this CTA's shared memory any more
+    if (tid == 0 && ctl.ring.abort)
+        ring_drain(ctl.ring);
+}
 
-    // ------------------------------------------------------------ per-sequence ticket
-    if (rank == 0 && tid == 0) {
-        __threadfence();
-        const int prev = atomicAdd(&p.ws_ticket[b], 1);
-        if (prev == N) {
-            __threadfence();
-            int j = __ldcg(&p.ws_first[b]);
-            if (j > N)
-                j = N;
-            const int err = __ldcg(&p.ws_err[b]);
-            int32_t *out = p.out + (size_t)b * (N + 1);
+// =============================================================================
+// Kernel B: the emitted token of each sequence, one cluster per sequence
+// =============================================================================
+//
+// j = first rejected position (N if none).  Sampled sequences draw the token
+// at j from (q_j - p_j)+ (or from q_N) by inverse CDF; the cluster splits the
+// row pair into C column chunks, each CTA sums its residual mass per slice
+// of 256 vectors with warp scans, the chunk masses are exchanged over DSMEM,
+// and the CTA whose chunk holds u_N * R finds the element.  Every r_k is
+// computed by the same rounded expression in both passes, so the pass that
+// picks the slice and the pass that picks the element agree.
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 4) sv_sample_kernel(const SvParams p)
+{
+    constexpr int VE = Elt<DT>::kPerVec;
+    extern __shared__ __align__(128) unsigned char smem[];
+    unsigned char *ring = smem;
+    CtlB &ctl = *reinterpret_cast<CtlB *>(smem + kRingBytes);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t C = sv::cluster_nctarank();
+    const uint32_t rank = sv::cluster_ctarank();
+    const int N = p.N, V = p.V;
+    const int b = blockIdx.x / C;
+
+    float T;
+    const int mode = sequence_mode(p, b, T);
+    // kernel A's results: launched as a dependent grid, this waits for them
+    sv::grid_dependency_wait();
+    int j = __ldcg(&p.ws_first[b]);
+    j = j > N ? N : j;
+    const int err = __ldcg(&p.ws_err[b]);
+    if (tid == 0) {
+        ring_init(ctl.ring);
+        ctl.cf = (mode == MODE_SAMPLED) ? (float)(kLog2e / (double)T) : 0.0f;
+    }
+    // every CTA has read j and err before the workspace is reset below
+    if (C > 1)
+        sv::cluster_sync();
+    else
+        __syncthreads();
+    const float cf = ctl.cf;
+    int32_t *out = p.out + (size_t)b * (N + 1);
+
+    if (err || mode != MODE_SAMPLED) {
+        if (rank == 0 && tid == 0) {
             if (err) {
                 for (int k = 0; k <= N; ++k)
                     out[k] = -1;
                 p.nacc[b] = -1;
                 atomicOr(p.status, err);
-            } else {
+            } else {  // greedy: the argmax at j
                 for (int k = 0; k < j; ++k)
                     out[k] = p.tokens[(size_t)b * N + k];
                 out[j] = __ldcg(&p.ws_tok[(size_t)b * (N + 1) + j]);
@@ -999,20 +825,284 @@ __global__ void __launch_bounds__(kThreads, 4) sv_verify_kernel(const SvParams p
             }
             p.ws_first[b] = kNoReject;
             p.ws_err[b] = 0;
-            p.ws_ticket[b] = 0;
         }
+        return;
     }
 
-    // never leave with a bulk copy still writing into this CTA's shared memory
-    if (tid == 0 && ctl.abort) {
-        for (int s = 0; s < kStages; ++s) {
-            const int lg = ctl.last_g[s];
-            if (lg >= 0) {
-                int never = 0;
-                sv::mbar_wait_bounded(&ctl.full[s], ((uint32_t)lg / kStages) & 1u, &never, kWaitLimitNs / 4);
+    const size_t trow = (size_t)b * (N + 1) + j;
+    const size_t drow = (size_t)b * N + j;
+    const Chunk ch = chunk_of(V / VE, rank, C);
+    const size_t row_vecs = (size_t)(V / VE);
+    const uint4 *tsrc = static_cast<const uint4 *>(p.target) + trow * row_vecs + ch.v0;
+    const uint4 *dsrc = (j < N) ? static_cast<const uint4 *>(p.draft) + drow * row_vecs + ch.v0 : nullptr;
+    const float *st = p.ws_stats + trow * 4;
+    const float mq = __ldcg(st + 0), Sq = __ldcg(st + 1);
+    const float mp = (j < N) ? __ldcg(st + 2) : 0.0f, Sp = (j < N) ? __ldcg(st + 3) : 1.0f;
+    const float isq = 1.0f / Sq, isp = (j < N) ? 1.0f / Sp : 0.0f;
+    const float uN = p.u[(size_t)b * (N + 1) + N];
+
+    int res_mode = (j < N) ? RES_DIFF : RES_Q;  // RES_Q after a retry as well
+    uint32_t g = 0;                              // ring position
+    int any_abort = 0;
+    for (;;) {
+        // ---- pass 2: residual mass per slice and warp
+        const uint4 *dres = (res_mode == RES_DIFF) ? dsrc : nullptr;
+        if (warp == kProducerWarp) {
+            if (lane == 0)
+                produce(ctl.ring, ring, tsrc, dres, ch.nvec, 0, ch.ntiles, g);
+            __syncwarp();
+        } else {
+            for (int t = 0; t < ch.ntiles; ++t) {
+                const uint32_t gt = g + t;
+                float part[kVPT];
+                const bool ok = consume_wait(ctl.ring, gt);
+                if (!ok)
+                    ctl.ring.abort = 1;
+                const unsigned char *stage = ring + (gt % kStages) * (2 * kTileBytes);
+#pragma unroll
+                for (int k = 0; k < kVPT; ++k) {
+                    part[k] = 0.0f;
+                    const int sv_ = k * kSliceVecs + tid;
+                    const int vec = t * kTileVecs + sv_;
+                    if (ok && vec < ch.nvec) {
+                        float r[VE];
+                        const uint4 vd = dres ? reinterpret_cast<const uint4 *>(stage + kTileBytes)[sv_]
+                                              : make_uint4(0, 0, 0, 0);
+                        residual_vec<DT>(reinterpret_cast<const uint4 *>(stage)[sv_], vd, res_mode, mq, isq, mp,
+                                         isp, cf, r);
+#pragma unroll
+                        for (int e = 0; e < VE; ++e)
+                            part[k] = __fadd_rn(part[k], r[e]);
+                    }
+                }
+                consume_release(ctl.ring, gt, lane);
+#pragma unroll
+                for (int k = 0; k < kVPT; ++k) {
+                    const int sl = t * kVPT + k;
+                    const float incl = warp_incl_scan(part[k], lane);
+                    if (lane == 31 && sl < ch.nslices)
+                        ctl.wsum[sl][warp] = incl;
+                }
+            }
+        }
+        g += ch.ntiles;
+        __syncthreads();
+        if (warp == 0) {
+            // slice masses and their inclusive prefix over the chunk
+            float carry = 0.0f;
+            for (int t0 = 0; t0 < ch.nslices; t0 += 32) {
+                const int t = t0 + lane;
+                float tm = 0.0f;
+                if (t < ch.nslices)
+#pragma unroll
+                    for (int w = 0; w < kConsWarps; ++w)
+                        tm = __fadd_rn(tm, ctl.wsum[t][w]);
+                const float inc = __fadd_rn(warp_incl_scan(tm, lane), carry);
+                if (t < ch.nslices)
+                    ctl.tcum[t] = inc;
+                carry = __shfl_sync(0xffffffffu, inc, 31);
+            }
+            if (lane == 0) {
+                ctl.Rc = carry;
+                ctl.ab = ctl.ring.abort;
+            }
+        }
+        if (C > 1)
+            sv::cluster_sync();  // chunk masses visible
+        else
+            __syncthreads();
+        if (warp == 0) {
+            // chunk c* whose cumulative mass first exceeds u_N * R
+            float Rr = 0.0f;
+            int ab = 0;
+            if (lane < (int)C) {
+                Rr = sv::ld_dsmem_f32(sv::dsmem_addr(&ctl.Rc, lane));
+                ab = sv::ld_dsmem_s32(sv::dsmem_addr(&ctl.ab, lane));
+            }
+            const float cum = warp_incl_scan(Rr, lane);
+            const float Rt = __shfl_sync(0xffffffffu, cum, 31);
+            const float x = __fmul_rn(uN, Rt);
+            const unsigned hit = __ballot_sync(0xffffffffu, lane < (int)C && x < cum);
+            int cs;
+            float x1;
+            if (hit) {
+                cs = __ffs(hit) - 1;
+                const float prev = __shfl_sync(0xffffffffu, cum, cs > 0 ? cs - 1 : 0);
+                x1 = __fsub_rn(x, cs > 0 ? prev : 0.0f);
+            } else {  // rounding: the last chunk that has mass
+                const unsigned pos = __ballot_sync(0xffffffffu, lane < (int)C && Rr > 0.0f);
+                cs = pos ? 31 - __clz(pos) : (int)C - 1;
+                x1 = INFINITY;
+            }
+            const unsigned abm = __ballot_sync(0xffffffffu, ab != 0);
+            if (lane == 0) {
+                ctl.retry = (Rt == 0.0f && res_mode == RES_DIFF) ? 1 : 0;
+                ctl.cstar = cs;
+                ctl.x1 = x1;
+                ctl.any_abort = abm != 0;
+            }
+        }
+        __syncthreads();
+        any_abort = ctl.any_abort;
+        if (!ctl.retry)
+            break;
+        res_mode = RES_Q;  // q_j == p_j: draw from q_j instead
+        if (C > 1)
+            sv::cluster_sync();  // peers are done reading ctl.Rc
+        else
+            __syncthreads();
+    }
+
+    if ((int)rank == ctl.cstar) {
+        if (warp == 0) {
+            // slice s* of the chunk, and the target relative to its start
+            const float x1 = ctl.x1;
+            int ts = -1;
+            float x2 = INFINITY;
+            if (x1 != INFINITY) {
+                for (int t0 = 0; t0 < ch.nslices && ts < 0; t0 += 32) {
+                    const int t = t0 + lane;
+                    const unsigned m = __ballot_sync(0xffffffffu, t < ch.nslices && x1 < ctl.tcum[t]);
+                    if (m)
+                        ts = t0 + __ffs(m) - 1;
+                }
+                if (ts >= 0)
+                    x2 = __fsub_rn(x1, ts > 0 ? ctl.tcum[ts - 1] : 0.0f);
+            }
+            if (ts < 0) {  // rounding: the last slice that has mass
+                for (int t0 = ((ch.nslices - 1) / 32) * 32; t0 >= 0 && ts < 0; t0 -= 32) {
+                    const int t = t0 + lane;
+                    float tm = 0.0f;
+                    if (t < ch.nslices)
+                        for (int w = 0; w < kConsWarps; ++w)
+                            tm += ctl.wsum[t][w];
+                    const unsigned m = __ballot_sync(0xffffffffu, tm > 0.0f);
+                    if (m)
+                        ts = t0 + 31 - __clz(m);
+                }
+                if (ts < 0)
+                    ts = ch.nslices - 1;
+                x2 = INFINITY;
+            }
+            if (lane == 0) {
+                ctl.tstar = ts;
+                ctl.x2 = x2;
+            }
+        }
+        __syncthreads();
+        const int sstar = ctl.tstar;              // slice
+        const int tstar = sstar / kVPT;           // ring tile holding it
+        const int kstar = sstar - tstar * kVPT;   // its place in the stage
+        // ---- pass 3: reload the tile of slice s*, redo its warp scans, find the element
+        const uint4 *dres = (res_mode == RES_DIFF) ? dsrc : nullptr;
+        if (warp == kProducerWarp) {
+            if (lane == 0)
+                produce(ctl.ring, ring, tsrc, dres, ch.nvec, tstar, tstar + 1, g);
+            __syncwarp();
+        } else {
+            float part = 0.0f;
+            if (consume_wait(ctl.ring, g)) {
+                const int vec = sstar * kSliceVecs + tid;
+                if (vec < ch.nvec) {
+                    const unsigned char *stage = ring + (g % kStages) * (2 * kTileBytes);
+                    const int sv_ = kstar * kSliceVecs + tid;
+                    float r[VE];
+                    const uint4 vd = dres ? reinterpret_cast<const uint4 *>(stage + kTileBytes)[sv_]
+                                          : make_uint4(0, 0, 0, 0);
+                    residual_vec<DT>(reinterpret_cast<const uint4 *>(stage)[sv_], vd, res_mode, mq, isq, mp, isp,
+                                     cf, r);
+#pragma unroll
+                    for (int e = 0; e < VE; ++e)
+                        part = __fadd_rn(part, r[e]);
+                }
+            } else {
+                ctl.ring.abort = 1;
+            }
+            ctl.incl[tid] = warp_incl_scan(part, lane);
+        }
+        __syncthreads();
+        if (warp == 0) {
+            const int nvec_t = min(kSliceVecs, ch.nvec - sstar * kSliceVecs);
+            const float x2 = ctl.x2;
+            const float wt = (lane < kConsWarps) ? ctl.incl[lane * 32 + 31] : 0.0f;
+            const float wc = warp_incl_scan(wt, lane);
+            int sel = -1;
+            float xl = 0.0f;
+            const unsigned mw = __ballot_sync(0xffffffffu, lane < kConsWarps && x2 < wc);
+            if (mw) {
+                const int ws = __ffs(mw) - 1;
+                const float wprev = __shfl_sync(0xffffffffu, wc, ws > 0 ? ws - 1 : 0);
+                const float xw = __fsub_rn(x2, ws > 0 ? wprev : 0.0f);
+                const float li = ctl.incl[ws * 32 + lane];
+                const unsigned ml = __ballot_sync(0xffffffffu, xw < li);
+                if (ml) {
+                    const int ls = __ffs(ml) - 1;
+                    const float lprev = __shfl_sync(0xffffffffu, li, ls > 0 ? ls - 1 : 0);
+                    sel = ws * 32 + ls;
+                    xl = __fsub_rn(xw, ls > 0 ? lprev : 0.0f);
+                }
+            }
+            if (lane == 0) {
+                const unsigned char *stage = ring + (g % kStages) * (2 * kTileBytes);
+                auto thread_r = [&](int th, float *r) {
+                    const int sv_ = kstar * kSliceVecs + th;
+                    const uint4 vd = dres ? reinterpret_cast<const uint4 *>(stage + kTileBytes)[sv_]
+                                          : make_uint4(0, 0, 0, 0);
+                    residual_vec<DT>(reinterpret_cast<const uint4 *>(stage)[sv_], vd, res_mode, mq, isq, mp, isp,
+                                     cf, r);
+                };
+                int token = -1;
+                if (sel >= 0 && sel < nvec_t) {
+                    float r[VE];
+                    thread_r(sel, r);
+                    float acc = 0.0f;
+                    for (int e = 0; e < VE; ++e) {
+                        acc = __fadd_rn(acc, r[e]);
+                        if (xl < acc) {
+                            token = (ch.v0 + sstar * kSliceVecs + sel) * VE + e;
+                            break;
+                        }
+                    }
+                }
+                if (token < 0) {
+                    // rounding left the target at or past the total: the
+                    // last element of the slice that carries mass
+                    for (int th = nvec_t - 1; th >= 0 && token < 0; --th) {
+                        float r[VE];
+                        thread_r(th, r);
+                        for (int e = VE - 1; e >= 0; --e)
+                            if (r[e] > 0.0f) {
+                                token = (ch.v0 + sstar * kSliceVecs + th) * VE + e;
+                                break;
+                            }
+                    }
+                    if (token < 0)
+                        token = (ch.v0 + sstar * kSliceVecs + nvec_t) * VE - 1;
+                }
+                // the sequence's outputs, and its workspace back to idle
+                if (any_abort || ctl.ring.abort) {
+                    for (int k = 0; k <= N; ++k)
+                        out[k] = -1;
+                    p.nacc[b] = -1;
+                    atomicOr(p.status, kErrTimeout);
+                } else {
+                    for (int k = 0; k < j; ++k)
+                        out[k] = p.tokens[(size_t)b * N + k];
+                    out[j] = token;
+                    for (int k = j + 1; k <= N; ++k)
+                        out[k] = -1;
+                    p.nacc[b] = j;
+                }
+                p.ws_first[b] = kNoReject;
+                p.ws_err[b] = 0;
             }
         }
     }
+
+    if (C > 1)
+        sv::cluster_sync();  // no peer reads this CTA's shared memory any more
+    if (tid == 0 && ctl.ring.abort)
+        ring_drain(ctl.ring);
 }
 
 } // namespace
@@ -1026,10 +1116,15 @@ struct spec_verify_ctx {
     int max_B, max_N, V;
     sv_dtype dtype;
     int num_sms;
-    int cluster_override;
-    int max_active_clusters[kMaxCluster + 1];  // 0 = cannot co-schedule
+    int cluster_override;                // kernel A cluster size, 0 = automatic
+    int clusters_a[kMaxCluster + 1];     // co-resident clusters of kernel A per size, 0 = none
+    int clusters_b[kMaxCluster + 1];     // the same for kernel B
     void *ws;
-    int *ws_first, *ws_ticket, *ws_err, *ws_tok, *status;
+    int *ws_first, *ws_err, *ws_tok, *status;
+    float *ws_stats;
+    // profiling: events before kernel A, between the kernels and after kernel B
+    int prof_on, prof_runs;
+    cudaEvent_t *prof_ev;  // [kProfRuns][3]
 };
 
 namespace {
@@ -1053,49 +1148,75 @@ struct DeviceGuard {
 
 int elt_bytes(sv_dtype dt) { return dt == SV_BF16 ? 2 : 4; }
 
-template <int DT> cudaError_t set_attrs()
+template <typename K> cudaError_t set_kernel_attrs(K kernel, size_t smem)
 {
-    cudaError_t e = cudaFuncSetAttribute(sv_verify_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
-    return cudaFuncSetAttribute(sv_verify_kernel<DT>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
 }
 
-template <int DT> int active_clusters(int C)
+template <int DT> cudaError_t set_attrs()
+{
+    cudaError_t e = set_kernel_attrs(sv_rows_kernel<DT>, kSmemA);
+    if (e != cudaSuccess)
+        return e;
+    return set_kernel_attrs(sv_sample_kernel<DT>, kSmemB);
+}
+
+// attr must hold two entries; `dependent` lets the launch overlap the tail of
+// the previous kernel on the stream (the kernel waits for it on the device).
+cudaLaunchConfig_t launch_config(unsigned grid, int C, size_t smem, cudaStream_t stream,
+                                 cudaLaunchAttribute *attr, bool dependent = false)
 {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(C * 1024);
+    cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cudaLaunchAttribute attr[1];
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = C;
+    attr[0].val.clusterDim.x = (unsigned)C;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (dependent) {
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.numAttrs = 2;
+    }
+    return cfg;
+}
+
+template <typename K> int active_clusters(K kernel, int C, size_t smem)
+{
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = launch_config((unsigned)(C * 1024), C, smem, nullptr, attr);
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, sv_verify_kernel<DT>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
     return n;
 }
 
-int auto_cluster(const spec_verify_ctx *c, int B, int N)
+// Co-resident cluster counts for every size, both kernels.
+template <int DT> void query_clusters(int *a, int *b)
 {
-    const int elt = elt_bytes(c->dtype);
-    const long long row_bytes = (long long)c->V * elt;
-    const int nv = (int)(row_bytes / 16);
-    const long long units = (long long)B * (N + 1);
-    // about 64 KiB of each row per CTA, at least two CTAs per SM in total,
-    // at most kMaxSlices slices per chunk, at least one vector per CTA
-    int C = (int)((row_bytes + 65535) / 65536);
-    const long long par = (2LL * c->num_sms + units - 1) / (units > 0 ? units : 1);
-    if (par > C)
-        C = (int)(par < 8 ? par : 8);
-    const int cmin = (nv + kMaxSlices * kSliceVecs - 1) / (kMaxSlices * kSliceVecs);
+    for (int k = 1; k <= kMaxCluster; ++k) {
+        a[k] = active_clusters(sv_rows_kernel<DT>, k, kSmemA);
+        b[k] = active_clusters(sv_sample_kernel<DT>, k, kSmemB);
+    }
+    a[1] = a[1] > 0 ? a[1] : 1;
+    b[1] = b[1] > 0 ? b[1] : 1;
+}
+
+// Smallest cluster that keeps each chunk within kMaxSlices slices.
+int min_cluster(int nv) { return (nv + kMaxSlices * kSliceVecs - 1) / (kMaxSlices * kSliceVecs); }
+
+int clamp_cluster(int C, int nv, const int *fits)
+{
+    const int cmin = min_cluster(nv);
     if (C < cmin)
         C = cmin;
     if (C > 8 && cmin <= 8)
@@ -1104,16 +1225,35 @@ int auto_cluster(const spec_verify_ctx *c, int B, int N)
         C = nv;
     if (C < 1)
         C = 1;
-    while (C > 1 && c->max_active_clusters[C] == 0)
+    while (C > 1 && C > cmin && fits[C] == 0)
         --C;
     return C;
 }
 
-int pick_cluster(const spec_verify_ctx *c, int B, int N)
+// Kernel A: one CTA per position once there are about two waves of positions
+// (four CTAs per SM), else split the rows over a cluster for parallelism.
+int cluster_a(const spec_verify_ctx *c, int B, int N)
 {
     if (c->cluster_override > 0)
         return c->cluster_override;
-    return auto_cluster(c, B, N);
+    const int nv = c->V * elt_bytes(c->dtype) / 16;
+    const long long units = (long long)B * (N + 1);
+    const long long want = 8LL * c->num_sms;
+    const int C = (int)((want + units - 1) / (units > 0 ? units : 1));
+    return clamp_cluster(C < 8 ? C : 8, nv, c->clusters_a);
+}
+
+// Kernel B: at most two CTAs per sequence (fewer, longer streams measured
+// faster than more, shorter ones), more when a chunk would be too large.
+int cluster_b(const spec_verify_ctx *c, int B)
+{
+    const long long row_bytes = (long long)c->V * elt_bytes(c->dtype);
+    const int nv = (int)(row_bytes / 16);
+    long long C = (row_bytes + 32767) / 32768;
+    const long long par = (2LL * c->num_sms + B - 1) / (B > 0 ? B : 1);
+    if (par > C)
+        C = par;
+    return clamp_cluster((int)(C < 2 ? C : 2), nv, c->clusters_b);
 }
 
 sv_status run_impl(spec_verify_ctx *ctx, const void *target, const void *draft, const int32_t *tokens,
@@ -1134,12 +1274,13 @@ sv_status run_impl(spec_verify_ctx *ctx, const void *target, const void *draft, 
         return SV_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(target) & 15u) || (draft && (reinterpret_cast<uintptr_t>(draft) & 15u)))
         return SV_ERR_INVALID_ARG;
-    const int C = pick_cluster(ctx, B, N);
+    const int CA = cluster_a(ctx, B, N);
+    const int CB = cluster_b(ctx, B);
     const int nv = ctx->V * elt_bytes(ctx->dtype) / 16;
-    if ((nv + C - 1) / C > kMaxSlices * kSliceVecs)
+    if ((nv + CA - 1) / CA > kMaxSlices * kSliceVecs || (nv + CB - 1) / CB > kMaxSlices * kSliceVecs)
         return SV_ERR_SHAPE;
     const long long units = (long long)B * (N + 1);
-    if (units * C > INT_MAX)
+    if (units * CA > INT_MAX || (long long)B * CB > INT_MAX)
         return SV_ERR_INVALID_ARG;
 
     DeviceGuard guard(ctx->device);
@@ -1159,29 +1300,35 @@ sv_status run_impl(spec_verify_ctx *ctx, const void *target, const void *draft, 
     prm.tstats = tstats;
     prm.dstats = dstats;
     prm.ws_first = ctx->ws_first;
-    prm.ws_ticket = ctx->ws_ticket;
     prm.ws_err = ctx->ws_err;
     prm.ws_tok = ctx->ws_tok;
+    prm.ws_stats = ctx->ws_stats;
     prm.status = ctx->status;
     prm.B = B;
     prm.N = N;
     prm.V = ctx->V;
     prm.greedy = greedy ? 1 : 0;
 
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(units * C));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cfg.stream = static_cast<cudaStream_t>(stream);
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)C;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cudaError_t e = (ctx->dtype == SV_BF16) ? cudaLaunchKernelEx(&cfg, sv_verify_kernel<SV_BF16>, prm)
-                                            : cudaLaunchKernelEx(&cfg, sv_verify_kernel<SV_F32>, prm);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaEvent_t *ev = nullptr;
+    if (ctx->prof_on && ctx->prof_runs < kProfRuns)
+        ev = ctx->prof_ev + 3 * ctx->prof_runs++;
+    if (ev)
+        cudaEventRecord(ev[0], st);
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = launch_config((unsigned)(units * CA), CA, kSmemA, st, attr);
+    cudaError_t e = (ctx->dtype == SV_BF16) ? cudaLaunchKernelEx(&cfg, sv_rows_kernel<SV_BF16>, prm)
+                                            : cudaLaunchKernelEx(&cfg, sv_rows_kernel<SV_F32>, prm);
+    if (e == cudaSuccess) {
+        if (ev)
+            cudaEventRecord(ev[1], st);
+        // dependent launch only when nothing is recorded between the kernels
+        cfg = launch_config((unsigned)(B * CB), CB, kSmemB, st, attr, /*dependent=*/ev == nullptr);
+        e = (ctx->dtype == SV_BF16) ? cudaLaunchKernelEx(&cfg, sv_sample_kernel<SV_BF16>, prm)
+                                    : cudaLaunchKernelEx(&cfg, sv_sample_kernel<SV_F32>, prm);
+        if (ev && e == cudaSuccess)
+            cudaEventRecord(ev[2], st);
+    }
     if (e != cudaSuccess) {
         cudaGetLastError();
         return SV_ERR_CUDA;
@@ -1228,13 +1375,15 @@ sv_status spec_verify_create(spec_verify_ctx **out, int device, int max_B, int m
         free(c);
         return SV_ERR_CUDA;
     }
-    for (int k = 1; k <= kMaxCluster; ++k)
-        c->max_active_clusters[k] = (dtype == SV_BF16) ? active_clusters<SV_BF16>(k) : active_clusters<SV_F32>(k);
-    c->max_active_clusters[1] = c->max_active_clusters[1] > 0 ? c->max_active_clusters[1] : 1;
+    if (dtype == SV_BF16)
+        query_clusters<SV_BF16>(c->clusters_a, c->clusters_b);
+    else
+        query_clusters<SV_F32>(c->clusters_a, c->clusters_b);
 
+    // workspace: first[nb] err[nb] tok[ntok] stats[4*ntok] status
     const size_t nb = (size_t)(max_B > 0 ? max_B : 1);
     const size_t ntok = nb * (size_t)(max_N + 1);
-    const size_t bytes = sizeof(int) * (3 * nb + ntok + 1);
+    const size_t bytes = sizeof(int) * (2 * nb + 5 * ntok + 1);
     if (cudaMalloc(&c->ws, bytes) != cudaSuccess) {
         cudaGetLastError();
         free(c);
@@ -1242,10 +1391,10 @@ sv_status spec_verify_create(spec_verify_ctx **out, int device, int max_B, int m
     }
     int *w = static_cast<int *>(c->ws);
     c->ws_first = w;
-    c->ws_ticket = w + nb;
-    c->ws_err = w + 2 * nb;
-    c->ws_tok = w + 3 * nb;
-    c->status = w + 3 * nb + ntok;
+    c->ws_err = w + nb;
+    c->ws_tok = w + 2 * nb;
+    c->ws_stats = reinterpret_cast<float *>(w + 2 * nb + ntok);
+    c->status = w + 2 * nb + 5 * ntok;
     if (cudaMemset(c->ws, 0, bytes) != cudaSuccess || cudaMemset(c->ws_first, 0x7f, sizeof(int) * nb) != cudaSuccess ||
         cudaDeviceSynchronize() != cudaSuccess) {
         cudaGetLastError();
@@ -1309,7 +1458,7 @@ sv_status spec_verify_set_cluster_size(spec_verify_ctx *ctx, int cluster_size)
 {
     if (!ctx || cluster_size < 0 || cluster_size > kMaxCluster)
         return SV_ERR_INVALID_ARG;
-    if (cluster_size > 1 && ctx->max_active_clusters[cluster_size] == 0)
+    if (cluster_size > 1 && ctx->clusters_a[cluster_size] == 0)
         return SV_ERR_INVALID_ARG;
     const int nv = ctx->V * elt_bytes(ctx->dtype) / 16;
     if (cluster_size > nv)
@@ -1322,7 +1471,7 @@ int spec_verify_cluster_size(spec_verify_ctx *ctx, int B, int N)
 {
     if (!ctx)
         return 0;
-    return pick_cluster(ctx, B, N);
+    return cluster_a(ctx, B, N);
 }
 
 const char *spec_verify_error_string(sv_status s)
@@ -1339,9 +1488,81 @@ const char *spec_verify_error_string(sv_status s)
     case SV_ERR_TIMEOUT: return "SV_ERR_TIMEOUT: a bounded wait in the kernel gave up";
     case SV_ERR_TOO_LARGE:
         return "SV_ERR_TOO_LARGE: batch exceeds the fixed scratch of spec_verify_run_noalloc "
-               "(B <= 2048, B*(N+1) <= 32768)";
+               "(B <= 2048, B*(N+1) <= 16384)";
     }
     return "unknown sv_status";
+}
+
+namespace {
+void prof_free(spec_verify_ctx *ctx)
+{
+    if (ctx->prof_ev) {
+        for (int k = 0; k < 3 * kProfRuns; ++k)
+            cudaEventDestroy(ctx->prof_ev[k]);
+        free(ctx->prof_ev);
+        ctx->prof_ev = nullptr;
+    }
+    ctx->prof_on = 0;
+    ctx->prof_runs = 0;
+}
+} // namespace
+
+sv_status spec_verify_profile(spec_verify_ctx *ctx, int enable)
+{
+    if (!ctx)
+        return SV_ERR_INVALID_ARG;
+    DeviceGuard guard(ctx->device);
+    if (!guard.ok)
+        return SV_ERR_CUDA;
+    if (!enable) {
+        prof_free(ctx);
+        return SV_OK;
+    }
+    if (!ctx->prof_ev) {
+        ctx->prof_ev = static_cast<cudaEvent_t *>(calloc(3 * kProfRuns, sizeof(cudaEvent_t)));
+        if (!ctx->prof_ev)
+            return SV_ERR_OOM;
+        for (int k = 0; k < 3 * kProfRuns; ++k)
+            if (cudaEventCreate(&ctx->prof_ev[k]) != cudaSuccess) {
+                cudaGetLastError();
+                for (int m = 0; m < k; ++m)
+                    cudaEventDestroy(ctx->prof_ev[m]);
+                free(ctx->prof_ev);
+                ctx->prof_ev = nullptr;
+                return SV_ERR_CUDA;
+            }
+    }
+    ctx->prof_on = 1;
+    ctx->prof_runs = 0;
+    return SV_OK;
+}
+
+sv_status spec_verify_profile_read(spec_verify_ctx *ctx, double *ms_rows, double *ms_sample, int *runs)
+{
+    if (!ctx || !ctx->prof_ev)
+        return SV_ERR_INVALID_ARG;
+    DeviceGuard guard(ctx->device);
+    if (!guard.ok)
+        return SV_ERR_CUDA;
+    double a = 0.0, b = 0.0;
+    for (int k = 0; k < ctx->prof_runs; ++k) {
+        cudaEvent_t *ev = ctx->prof_ev + 3 * k;
+        float t1 = 0.0f, t2 = 0.0f;
+        if (cudaEventSynchronize(ev[2]) != cudaSuccess || cudaEventElapsedTime(&t1, ev[0], ev[1]) != cudaSuccess ||
+            cudaEventElapsedTime(&t2, ev[1], ev[2]) != cudaSuccess) {
+            cudaGetLastError();
+            return SV_ERR_CUDA;
+        }
+        a += t1;
+        b += t2;
+    }
+    if (ms_rows)
+        *ms_rows = a;
+    if (ms_sample)
+        *ms_sample = b;
+    if (runs)
+        *runs = ctx->prof_runs;
+    return SV_OK;
 }
 
 void spec_verify_destroy(spec_verify_ctx *ctx)
@@ -1350,6 +1571,7 @@ void spec_verify_destroy(spec_verify_ctx *ctx)
         return;
     {
         DeviceGuard guard(ctx->device);
+        prof_free(ctx);
         cudaFree(ctx->ws);
     }
     free(ctx);
@@ -1371,8 +1593,8 @@ void spec_verify_destroy(spec_verify_ctx *ctx)
 
 namespace {
 constexpr int kNoAllocMaxB = 2048;        // sequences per call
-constexpr int kNoAllocMaxUnits = 32768;   // B*(N+1) verified positions per call
-constexpr int kNoAllocInts = 3 * kNoAllocMaxB + kNoAllocMaxUnits + 1;  // about 156 KiB
+constexpr int kNoAllocMaxUnits = 16384;   // B*(N+1) verified positions per call
+constexpr int kNoAllocInts = 2 * kNoAllocMaxB + 5 * kNoAllocMaxUnits + 1;  // about 336 KiB
 constexpr int kNoAllocMaxDevices = 64;
 } // namespace
 
@@ -1384,8 +1606,8 @@ struct NoAllocDevice {
     bool ready;
     int *scratch;     // device address of g_sv_noalloc_scratch on this device
     int num_sms;
-    int clusters_bf16[kMaxCluster + 1];
-    int clusters_f32[kMaxCluster + 1];
+    int clusters_bf16[2][kMaxCluster + 1];  // kernels A, B
+    int clusters_f32[2][kMaxCluster + 1];
 };
 
 std::mutex g_noalloc_mutex;
@@ -1410,12 +1632,8 @@ sv_status noalloc_setup(int device, NoAllocDevice &nd)
         cudaGetLastError();
         return SV_ERR_CUDA;
     }
-    for (int k = 1; k <= kMaxCluster; ++k) {
-        nd.clusters_bf16[k] = active_clusters<SV_BF16>(k);
-        nd.clusters_f32[k] = active_clusters<SV_F32>(k);
-    }
-    nd.clusters_bf16[1] = nd.clusters_bf16[1] > 0 ? nd.clusters_bf16[1] : 1;
-    nd.clusters_f32[1] = nd.clusters_f32[1] > 0 ? nd.clusters_f32[1] : 1;
+    query_clusters<SV_BF16>(nd.clusters_bf16[0], nd.clusters_bf16[1]);
+    query_clusters<SV_F32>(nd.clusters_f32[0], nd.clusters_f32[1]);
     nd.scratch = w;
     nd.ready = true;
     return SV_OK;
@@ -1465,22 +1683,21 @@ extern "C" sv_status spec_verify_run_noalloc(const void *target_logits, const vo
     c.V = V;
     c.dtype = dtype;
     c.num_sms = nd->num_sms;
-    memcpy(c.max_active_clusters, dtype == SV_BF16 ? nd->clusters_bf16 : nd->clusters_f32,
-           sizeof c.max_active_clusters);
+    memcpy(c.clusters_a, dtype == SV_BF16 ? nd->clusters_bf16[0] : nd->clusters_f32[0], sizeof c.clusters_a);
+    memcpy(c.clusters_b, dtype == SV_BF16 ? nd->clusters_bf16[1] : nd->clusters_f32[1], sizeof c.clusters_b);
     int *w = nd->scratch;
     c.ws = w;
     c.ws_first = w;
-    c.ws_ticket = w + kNoAllocMaxB;
-    c.ws_err = w + 2 * kNoAllocMaxB;
-    c.ws_tok = w + 3 * kNoAllocMaxB;
-    c.status = w + 3 * kNoAllocMaxB + kNoAllocMaxUnits;
+    c.ws_err = w + kNoAllocMaxB;
+    c.ws_tok = w + 2 * kNoAllocMaxB;
+    c.ws_stats = reinterpret_cast<float *>(w + 2 * kNoAllocMaxB + kNoAllocMaxUnits);
+    c.status = w + 2 * kNoAllocMaxB + 5 * kNoAllocMaxUnits;
 
     // The scratch keeps whatever the previous call left in it: put the slots
     // this call uses into their starting state first (on the same stream, so
     // calls issued in stream order never see each other's values).
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(c.ws_first, 0x7f, sizeof(int) * B, st) != cudaSuccess ||
-        cudaMemsetAsync(c.ws_ticket, 0, sizeof(int) * B, st) != cudaSuccess ||
         cudaMemsetAsync(c.ws_err, 0, sizeof(int) * B, st) != cudaSuccess ||
         cudaMemsetAsync(c.status, 0, sizeof(int), st) != cudaSuccess) {
         cudaGetLastError();

@@ -90,6 +90,14 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+// ---- programmatic dependent launch -------------------------------------------
+// Blocks until the grids this one depends on have completed and their memory
+// is visible (a no-op when the launch had no such dependency).
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---- thread-block cluster --------------------------------------------------
 __device__ __forceinline__ uint32_t cluster_ctarank()
 {

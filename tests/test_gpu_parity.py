@@ -191,3 +191,17 @@ def test_host_errors():
     assert sv.spec_verify_run(ctx.ctx, w.target.data_ptr(), None, w.draft_tokens.data_ptr(),
                               w.uniforms.data_ptr(), w.temperature.data_ptr(), 0, w.B, w.N,
                               *tail) == sv.SV_ERR_INVALID_ARG
+
+
+def test_profiling_hook_times_both_kernels():
+    w = synth.make_workload("headline", seed=14, device="cuda", B=8)
+    ctx = _ctx(w)
+    ctx.profile(True)
+    for _ in range(3):
+        ctx.run(w.target, w.draft, w.draft_tokens, w.uniforms, w.temperature)
+    ms_rows, ms_sample, n = ctx.profile_read()
+    assert n == 3 and ms_rows > 0.0 and ms_sample > 0.0
+    ctx.profile(False)
+    with pytest.raises(sv.SpecVerifyError):
+        ctx.profile_read()
+    _check(w, ctx=ctx)  # profiling left the results alone
