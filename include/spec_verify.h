@@ -23,7 +23,7 @@
  * mismatch, else a_N.  Draft logits and uniforms are then not read.
  *
  * All tensors are caller-owned device memory, C-contiguous, row-major.  The
- * library never allocates or synchronises inside spec_verify_run; the run (two
+ * library never allocates or synchronises inside spec_verify_run; the run (three
  * kernel launches) is enqueued on the caller's stream and completes
  * asynchronously.
  *
@@ -59,9 +59,10 @@ typedef enum { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
 /*
  * Create a context on `device` for batches of up to max_B sequences with up
  * to max_N draft tokens over a vocabulary of V tokens stored as `dtype`.
- * Allocates a workspace of about 8*max_B + 20*max_B*(max_N+1) bytes (per-
- * sequence first-rejection slots and error flags; per-position argmax and
- * row statistics) and one status word; nothing else is allocated later.
+ * Allocates a workspace of about 8*max_B + 20*max_B*(max_N+1) +
+ * 32*max_B*ceil(V*elt/4 KiB) bytes (per-sequence first-rejection slots and
+ * error flags; per-position argmax and row statistics; per-slice residual
+ * masses) and one status word; nothing else is allocated later.
  * Requires V >= 1 and V*sizeof(dtype) a multiple of 16 (V % 8 == 0 for bf16,
  * V % 4 == 0 for f32).  Returns SV_ERR_SHAPE otherwise, SV_ERR_OOM if the
  * workspace cannot be allocated, SV_ERR_CUDA if the device cannot be used.
@@ -137,12 +138,12 @@ const char *spec_verify_error_string(sv_status s);
 
 /*
  * Kernel timing for benchmarks.  While enabled, every run records CUDA events
- * before its first kernel (row normalisers and accept tests), between the two
- * kernels and after the second (sampling and output), up to 4096 runs;
- * enabling again restarts the count.  The run then launches its second
- * kernel without overlapping the first.  spec_verify_profile_read waits for
- * the recorded runs and returns the summed device time of each kernel in
- * milliseconds and the number of runs.  Disabling frees the events.
+ * before its first kernel (row normalisers and accept tests), after it, and
+ * after the last (sampling and output), up to 4096 runs; enabling again
+ * restarts the count.  The sampling kernels then start only after the first
+ * kernel has finished.  spec_verify_profile_read waits for the recorded runs
+ * and returns the summed device time of the two parts in milliseconds and the
+ * number of runs.  Disabling frees the events.
  */
 sv_status spec_verify_profile(spec_verify_ctx *ctx, int enable);
 sv_status spec_verify_profile_read(spec_verify_ctx *ctx, double *ms_rows, double *ms_sample, int *runs);
@@ -159,19 +160,19 @@ void spec_verify_destroy(spec_verify_ctx *ctx);
  * a plug-in whose host framework owns every allocation, or a decode loop that
  * cannot afford the implicit device synchronisation and possible failure of a
  * cudaMalloc.  This entry point needs no context and allocates nothing: its
- * scratch is a fixed array of about 336 KiB compiled into the library, which
+ * scratch is a fixed array of about 848 KiB compiled into the library, which
  * every GPU that loads the library holds until the process exits.
  *
  * Arguments are those of spec_verify_run, with the vocabulary size V and the
- * logit dtype given per call; it runs on the current device.  Limits: B <= 2048
- * and B*(N+1) <= 16384, else SV_ERR_TOO_LARGE and nothing is enqueued.
+ * logit dtype given per call; it runs on the current device.  Limits: B <= 2048,
+ * B*(N+1) <= 16384 and B*ceil(V*elt/4 KiB) <= 16384, else SV_ERR_TOO_LARGE and nothing is enqueued.
  * Invalid sequences are reported through out_tokens = -1 and
  * num_accepted = -1 only (there is no status word to query).
  *
  * The first call on a device does a one-time, synchronous set-up (it looks up
  * the scratch address, clears it and sets kernel attributes); make that first
  * call before any stream capture.  Every later call enqueues three small
- * memsets of the scratch slots it uses and the two kernels, on `stream`, and
+ * memsets of the scratch slots it uses and the three kernels, on `stream`, and
  * nothing else.  All calls on a device share the one scratch array: calls
  * that can overlap on the GPU (different streams without ordering between
  * them, or several host threads) race and corrupt each other's results.

@@ -123,7 +123,8 @@ def spec_verify_destroy(ctx) -> None:
 def spec_verify_run_noalloc(target, draft, draft_tokens, uniforms, temperature, greedy, B, N, V, dtype,
                             out_tokens, num_accepted, stream) -> int:
     """Context-free variant that allocates nothing: scratch is a fixed array
-    inside the library (B <= 2048, B*(N+1) <= 16384), shared by every call on
+    inside the library (B <= 2048, B*(N+1) <= 16384,
+    B*ceil(V*elt/4KiB) <= 16384), shared by every call on
     the device, so calls must not overlap on the GPU."""
     return load().spec_verify_run_noalloc(target, draft, draft_tokens, uniforms, temperature,
                                           int(greedy), B, N, V, dtype, out_tokens, num_accepted, stream)

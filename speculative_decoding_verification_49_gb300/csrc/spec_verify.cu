@@ -1,6 +1,6 @@
 // spec_verify.cu -- GB300 (sm_103a) speculative-sampling verify step.
 //
-// Two kernel launches per call.
+// Three kernel launches per call.
 //
 // Kernel A (sv_rows_kernel): one verified position (sequence b, position i)
 // per thread-block cluster of C CTAs; CTA r owns the r-th contiguous column
@@ -15,12 +15,13 @@
 // A rejection lowers the sequence's first-rejection slot (atomicMin); the row
 // statistics (mq, Sq, mp, Sp) go to the workspace.
 //
-// Kernel B (sv_sample_kernel): one cluster per sequence.  It reads the first
-// rejection j (N if none) and samples the emitted token at j from
-// normalise(max(0, q_j - p_j)) (or the bonus token from q_N) by inverse CDF,
-// writes out_tokens and num_accepted, and resets the workspace for the next
-// call, so no memset is ever enqueued.  Only one row pair per sequence is
-// read a second time.
+// Kernels B (sv_mass_kernel) and C (sv_pick_kernel) sample the emitted token
+// at the first rejection j (N if none) from normalise(max(0, q_j - p_j)) (or
+// the bonus token from q_N) by inverse CDF: B sums the residual mass of every
+// slice of those row pairs with a balanced persistent grid, C finds the slice,
+// the thread and the element, writes out_tokens and num_accepted, and resets
+// the workspace for the next call, so no memset is ever enqueued.  Only one
+// row pair per sequence is read a second time.
 //
 // Method: "Speculative decoding -- draft, verify, repeat"
 // (factory.pai-world.com lesson 07-16), section "Core algorithm", steps 3-6;
@@ -48,8 +49,8 @@ constexpr int kVPT = 2;                      // 16-byte vectors per consumer thr
 constexpr int kSliceVecs = kConsThreads;     // one vector per consumer thread: the scan unit
 constexpr int kTileVecs = kVPT * kSliceVecs; // vectors per row and stage
 constexpr int kTileBytes = kTileVecs * 16;
-constexpr int kStages = 3;
-constexpr int kRingBytes = kStages * 2 * kTileBytes;
+constexpr int kStagesA = 3;                  // ring depth of the row kernel
+__host__ __device__ constexpr int ring_bytes(int stages) { return stages * 2 * kTileBytes; }
 constexpr int kMaxSlices = 128;              // slices per chunk (512 KiB of one row)
 constexpr int kMaxCluster = 16;
 constexpr int kProfRuns = 4096;  // runs whose kernel times one profiling session keeps
@@ -81,22 +82,24 @@ struct SvParams {
     int *ws_err;      // [max_B] error bits of the sequence
     int *ws_tok;      // [max_B*(max_N+1)] greedy argmax of each position
     float *ws_stats;  // [max_B*(max_N+1)][4] (mq, Sq, mp, Sp) of each position
+    float *ws_slice;  // [max_B*slices][8] residual mass of each warp's share of a slice
     int *status;      // sticky error bits of the context
     int B, N, V, greedy;
 };
 
 // Producer/consumer ring state in shared memory.
-struct Ring {
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
-    int last_g[kStages];  // last ring position issued into each stage
+template <int S> struct Ring {
+    static constexpr int kStages = S;
+    uint64_t full[S];
+    uint64_t empty[S];
+    int last_g[S];  // last ring position issued into each stage
     int abort;
 };
 
 // Shared-memory control blocks (after the ring).  Fields read by peer CTAs
 // over DSMEM are written before a cluster barrier and not rewritten after it.
 struct CtlA {
-    Ring ring;
+    Ring<kStagesA> ring;
     float cf;                      // log2(e) / T
     float pm_t, ps_t, pm_d, ps_d;  // sampled partials (target, draft)
     float gv;                      // greedy partial
@@ -106,20 +109,7 @@ struct CtlA {
     int red_i[kConsWarps], red_n[kConsWarps];
 };
 
-struct CtlB {
-    Ring ring;
-    float cf;
-    float Rc;  // residual mass of this CTA's chunk (published)
-    int ab;    // this CTA gave up a wait (published)
-    int retry, cstar, tstar, any_abort;
-    float x1, x2;
-    float incl[kConsThreads];
-    float wsum[kMaxSlices][kConsWarps];  // per slice and warp: residual mass
-    float tcum[kMaxSlices];              // inclusive prefix of slice masses
-};
-
-constexpr size_t kSmemA = kRingBytes + sizeof(CtlA);
-constexpr size_t kSmemB = kRingBytes + sizeof(CtlB);
+constexpr size_t kSmemA = ring_bytes(kStagesA) + sizeof(CtlA);
 
 template <int DT> struct Elt;
 template <> struct Elt<SV_F32> {
@@ -417,9 +407,11 @@ __device__ __forceinline__ float warp_incl_scan(float x, int lane)
 // ---- ring of shared-memory stages fed by TMA bulk copies --------------------
 // Issues ring tiles [t_begin, t_end) of the chunk into ring positions g, g+1,
 // ...  Runs on one lane of the producer warp.
-__device__ __forceinline__ void produce(Ring &rg, unsigned char *ring, const uint4 *tsrc, const uint4 *dsrc,
+template <typename RingT>
+__device__ __forceinline__ void produce(RingT &rg, unsigned char *ring, const uint4 *tsrc, const uint4 *dsrc,
                                         int nvec_chunk, int t_begin, int t_end, uint32_t g)
 {
+    constexpr int kStages = RingT::kStages;
     for (int t = t_begin; t < t_end; ++t, ++g) {
         const uint32_t s = g % kStages;
         const uint32_t ph = (g / kStages) & 1u;
@@ -439,23 +431,27 @@ __device__ __forceinline__ void produce(Ring &rg, unsigned char *ring, const uin
 }
 
 // Consumer side: wait until ring position g is filled.
-__device__ __forceinline__ bool consume_wait(Ring &rg, uint32_t g)
+template <typename RingT>
+__device__ __forceinline__ bool consume_wait(RingT &rg, uint32_t g)
 {
+    constexpr int kStages = RingT::kStages;
     const uint32_t s = g % kStages;
     return sv::mbar_wait_bounded(&rg.full[s], (g / kStages) & 1u, &rg.abort, kWaitLimitNs);
 }
 
-__device__ __forceinline__ void consume_release(Ring &rg, uint32_t g, int lane)
+template <typename RingT>
+__device__ __forceinline__ void consume_release(RingT &rg, uint32_t g, int lane)
 {
     __syncwarp();
     if (lane == 0)
-        sv::mbar_arrive(&rg.empty[g % kStages]);
+        sv::mbar_arrive(&rg.empty[g % RingT::kStages]);
 }
 
 // Called by thread 0 before the first __syncthreads of a kernel.
-__device__ __forceinline__ void ring_init(Ring &rg)
+template <typename RingT>
+__device__ __forceinline__ void ring_init(RingT &rg)
 {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < RingT::kStages; ++s) {
         sv::mbar_init(&rg.full[s], 1);
         sv::mbar_init(&rg.empty[s], kConsWarps);
         rg.last_g[s] = -1;
@@ -466,13 +462,14 @@ __device__ __forceinline__ void ring_init(Ring &rg)
 
 // After an abort: never leave with a bulk copy still writing into this CTA's
 // shared memory (bounded wait on the last copy issued into each stage).
-__device__ __forceinline__ void ring_drain(Ring &rg)
+template <typename RingT>
+__device__ __forceinline__ void ring_drain(RingT &rg)
 {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < RingT::kStages; ++s) {
         const int lg = rg.last_g[s];
         if (lg >= 0) {
             int never = 0;
-            sv::mbar_wait_bounded(&rg.full[s], ((uint32_t)lg / kStages) & 1u, &never, kWaitLimitNs / 4);
+            sv::mbar_wait_bounded(&rg.full[s], ((uint32_t)lg / RingT::kStages) & 1u, &never, kWaitLimitNs / 4);
         }
     }
 }
@@ -521,7 +518,8 @@ __global__ void __launch_bounds__(kThreads, 4) sv_rows_kernel(const SvParams p)
     constexpr int VE = Elt<DT>::kPerVec;
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char *ring = smem;
-    CtlA &ctl = *reinterpret_cast<CtlA *>(smem + kRingBytes);
+    constexpr int kStages = kStagesA;
+    CtlA &ctl = *reinterpret_cast<CtlA *>(smem + ring_bytes(kStages));
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t C = sv::cluster_nctarank();
@@ -765,51 +763,249 @@ __global__ void __launch_bounds__(kThreads, 4) sv_rows_kernel(const SvParams p)
 }
 
 // =============================================================================
-// Kernel B: the emitted token of each sequence, one cluster per sequence
+// Kernels B and C: the emitted token of each sequence
 // =============================================================================
 //
 // j = first rejected position (N if none).  Sampled sequences draw the token
-// at j from (q_j - p_j)+ (or from q_N) by inverse CDF; the cluster splits the
-// row pair into C column chunks, each CTA sums its residual mass per slice
-// of 256 vectors with warp scans, the chunk masses are exchanged over DSMEM,
-// and the CTA whose chunk holds u_N * R finds the element.  Every r_k is
-// computed by the same rounded expression in both passes, so the pass that
-// picks the slice and the pass that picks the element agree.
-template <int DT>
-__global__ void __launch_bounds__(kThreads, 4) sv_sample_kernel(const SvParams p)
+// at j from normalise(max(0, q_j - p_j)) (or the bonus token from q_N) by
+// inverse CDF in ascending token order.
+//
+// Kernel B (sv_mass_kernel) sums the residual mass of every slice of 256
+// 16-byte vectors of those row pairs.  Its grid is a fixed number of CTAs;
+// each takes an equal contiguous share of all ring tiles of all sampled
+// sequences and streams them through its TMA ring, so the work is balanced
+// to one tile.  Thread t takes vector t of a slice; a slice's mass is the sum
+// of its 8 warp totals (warp-inclusive scans), added in warp order.
+//
+// Kernel C (sv_pick_kernel), one CTA per sequence, finds the slice where the
+// cumulative mass first exceeds u_N * R, recomputes that slice with the same
+// rounded arithmetic (so its warp totals equal kernel B's), finds the warp,
+// lane and element, writes out_tokens / num_accepted and returns the
+// workspace slots to their idle state.
+
+constexpr int kPickThreads = kSliceVecs;  // one vector of a slice per thread
+
+// Ring of the mass kernel: kVPTM slices per tile, kStagesM stages.
+constexpr int kVPTM = 2;
+constexpr int kStagesM = 3;
+constexpr int kTileVecsM = kVPTM * kSliceVecs;
+constexpr int kTileBytesM = kTileVecsM * 16;
+constexpr int kRingBytesM = kStagesM * 2 * kTileBytesM;
+
+// Per-stage description of the tile the producer put there.
+struct TileMeta {
+    int b;         // sequence, or -1: no more tiles
+    int slice;     // first slice of the tile within the sequence's row
+    int res_mode;
+    float mq, isq, mp, isp, cf;
+};
+
+struct CtlM {
+    Ring<kStagesM> ring;
+    TileMeta meta[kStagesM];
+};
+
+constexpr size_t kSmemM = kRingBytesM + sizeof(CtlM);
+
+// Residual-mode parameters of sequence b, or false when b is not sampled.
+struct SeqSample {
+    int j, res_mode;
+    float mq, isq, mp, isp, cf, uN;
+};
+
+__device__ __forceinline__ bool sequence_sample(const SvParams &p, int b, SeqSample &s)
 {
-    constexpr int VE = Elt<DT>::kPerVec;
-    extern __shared__ __align__(128) unsigned char smem[];
-    unsigned char *ring = smem;
-    CtlB &ctl = *reinterpret_cast<CtlB *>(smem + kRingBytes);
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const uint32_t C = sv::cluster_nctarank();
-    const uint32_t rank = sv::cluster_ctarank();
-    const int N = p.N, V = p.V;
-    const int b = blockIdx.x / C;
-
     float T;
     const int mode = sequence_mode(p, b, T);
-    // kernel A's results: launched as a dependent grid, this waits for them
-    sv::grid_dependency_wait();
     int j = __ldcg(&p.ws_first[b]);
-    j = j > N ? N : j;
+    j = j > p.N ? p.N : j;
     const int err = __ldcg(&p.ws_err[b]);
-    if (tid == 0) {
-        ring_init(ctl.ring);
-        ctl.cf = (mode == MODE_SAMPLED) ? (float)(kLog2e / (double)T) : 0.0f;
-    }
-    // every CTA has read j and err before the workspace is reset below
-    if (C > 1)
-        sv::cluster_sync();
-    else
-        __syncthreads();
-    const float cf = ctl.cf;
-    int32_t *out = p.out + (size_t)b * (N + 1);
+    s.j = j;
+    if (err || mode != MODE_SAMPLED)
+        return false;
+    const float *st = p.ws_stats + ((size_t)b * (p.N + 1) + j) * 4;
+    s.res_mode = (j < p.N) ? RES_DIFF : RES_Q;
+    s.mq = __ldcg(st + 0);
+    s.isq = 1.0f / __ldcg(st + 1);
+    s.mp = (j < p.N) ? __ldcg(st + 2) : 0.0f;
+    s.isp = (j < p.N) ? 1.0f / __ldcg(st + 3) : 0.0f;
+    s.cf = (float)(kLog2e / (double)T);
+    s.uN = p.u[(size_t)b * (p.N + 1) + p.N];
+    return true;
+}
 
-    if (err || mode != MODE_SAMPLED) {
-        if (rank == 0 && tid == 0) {
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 4) sv_mass_kernel(const SvParams p)
+{
+    constexpr int VE = Elt<DT>::kPerVec;
+    constexpr int kStages = kStagesM;
+    extern __shared__ __align__(128) unsigned char smem[];
+    unsigned char *ring = smem;
+    CtlM &ctl = *reinterpret_cast<CtlM *>(smem + kRingBytesM);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int N = p.N;
+    const int NV = p.V / VE;
+    const int T = (NV + kTileVecsM - 1) / kTileVecsM;  // ring tiles per row
+    const int S = (NV + kSliceVecs - 1) / kSliceVecs;  // slices per row
+    const long long total = (long long)p.B * T;
+    const long long t_begin = total * blockIdx.x / gridDim.x;
+    const long long t_end = total * (blockIdx.x + 1) / gridDim.x;
+
+    if (tid == 0)
+        ring_init(ctl.ring);
+    sv::grid_dependency_wait();  // kernel A's results
+    __syncthreads();
+
+    if (warp == kProducerWarp) {
+        if (lane == 0) {
+            uint32_t g = 0;
+            int cur_b = -1;
+            bool cur_ok = false;
+            SeqSample sq{};
+            for (long long tt = t_begin; tt < t_end && !ctl.ring.abort; ++tt) {
+                const int b = (int)(tt / T);
+                const int t = (int)(tt - (long long)b * T);
+                if (b != cur_b) {
+                    cur_b = b;
+                    cur_ok = sequence_sample(p, b, sq);
+                }
+                if (!cur_ok)
+                    continue;
+                const uint32_t s = g % kStages;
+                if (!sv::mbar_wait_bounded(&ctl.ring.empty[s], ((g / kStages) & 1u) ^ 1u, &ctl.ring.abort,
+                                           kWaitLimitNs)) {
+                    ctl.ring.abort = 1;
+                    break;
+                }
+                TileMeta &m = ctl.meta[s];
+                m.b = b;
+                m.slice = t * kVPTM;
+                m.res_mode = sq.res_mode;
+                m.mq = sq.mq;
+                m.isq = sq.isq;
+                m.mp = sq.mp;
+                m.isp = sq.isp;
+                m.cf = sq.cf;
+                const size_t trow = (size_t)b * (N + 1) + sq.j;
+                const uint4 *tsrc = static_cast<const uint4 *>(p.target) + trow * (size_t)NV;
+                const uint4 *dsrc = (sq.res_mode == RES_DIFF)
+                                        ? static_cast<const uint4 *>(p.draft) + ((size_t)b * N + sq.j) * (size_t)NV
+                                        : nullptr;
+                const int nvec = min(kTileVecsM, NV - t * kTileVecsM);
+                const uint32_t bytes = static_cast<uint32_t>(nvec) * 16u;
+                sv::mbar_arrive_expect_tx(&ctl.ring.full[s], dsrc ? 2u * bytes : bytes);
+                unsigned char *stage = ring + s * (2 * kTileBytesM);
+                sv::bulk_g2s(stage, tsrc + (size_t)t * kTileVecsM, bytes, &ctl.ring.full[s]);
+                if (dsrc)
+                    sv::bulk_g2s(stage + kTileBytesM, dsrc + (size_t)t * kTileVecsM, bytes, &ctl.ring.full[s]);
+                ctl.ring.last_g[s] = static_cast<int>(g);
+                ++g;
+            }
+            // end marker (no bytes): consumers stop at it
+            const uint32_t s = g % kStages;
+            if (!ctl.ring.abort &&
+                sv::mbar_wait_bounded(&ctl.ring.empty[s], ((g / kStages) & 1u) ^ 1u, &ctl.ring.abort, kWaitLimitNs)) {
+                ctl.meta[s].b = -1;
+                sv::mbar_arrive_expect_tx(&ctl.ring.full[s], 0);
+            } else {
+                ctl.ring.abort = 1;
+            }
+        }
+        __syncwarp();
+    } else {
+        for (uint32_t g = 0;; ++g) {
+            const uint32_t s = g % kStages;
+            if (!consume_wait(ctl.ring, g)) {
+                ctl.ring.abort = 1;
+                break;
+            }
+            const TileMeta m = ctl.meta[s];
+            if (m.b < 0)
+                break;
+            const unsigned char *stage = ring + s * (2 * kTileBytesM);
+#pragma unroll
+            for (int k = 0; k < kVPTM; ++k) {
+                const int sv_ = k * kSliceVecs + tid;
+                const int vec = m.slice * kSliceVecs + sv_;
+                float part = 0.0f;
+                if (vec < NV) {
+                    float r[VE];
+                    const uint4 vd = (m.res_mode == RES_DIFF) ? reinterpret_cast<const uint4 *>(stage + kTileBytesM)[sv_]
+                                                              : make_uint4(0, 0, 0, 0);
+                    residual_vec<DT>(reinterpret_cast<const uint4 *>(stage)[sv_], vd, m.res_mode, m.mq, m.isq, m.mp,
+                                     m.isp, m.cf, r);
+#pragma unroll
+                    for (int e = 0; e < VE; ++e)
+                        part = __fadd_rn(part, r[e]);
+                }
+                const float incl = warp_incl_scan(part, lane);
+                const int sl = m.slice + k;
+                if (lane == 31 && sl < S)
+                    p.ws_slice[((size_t)m.b * S + sl) * kConsWarps + warp] = incl;  // this warp's share
+            }
+            consume_release(ctl.ring, g, lane);
+        }
+    }
+    if (tid == 0 && ctl.ring.abort) {
+        atomicOr(p.status, kErrTimeout);
+        ring_drain(ctl.ring);
+    }
+}
+
+// Mass of one slice of the residual at thread granularity: thread t's share
+// (vector t of the slice) and its warp-inclusive prefix; identical to the
+// arithmetic of sv_mass_kernel.
+template <int DT>
+__device__ __forceinline__ float slice_thread_mass(const uint4 *tsrc, const uint4 *dsrc, int slice, int NV, int tid,
+                                                   const SeqSample &s, float *r)
+{
+    constexpr int VE = Elt<DT>::kPerVec;
+    const int vec = slice * kSliceVecs + tid;
+    float part = 0.0f;
+    if (vec < NV) {
+        const uint4 vd = (s.res_mode == RES_DIFF) ? __ldcg(dsrc + vec) : make_uint4(0, 0, 0, 0);
+        residual_vec<DT>(__ldcg(tsrc + vec), vd, s.res_mode, s.mq, s.isq, s.mp, s.isp, s.cf, r);
+#pragma unroll
+        for (int e = 0; e < VE; ++e)
+            part = __fadd_rn(part, r[e]);
+    } else {
+#pragma unroll
+        for (int e = 0; e < VE; ++e)
+            r[e] = 0.0f;
+    }
+    return part;
+}
+
+constexpr int kMaxRowSlices = kMaxCluster * kMaxSlices;  // slices of the longest supported row
+
+struct PickShared {
+    float slice[kMaxRowSlices];  // the sequence's slice masses
+    float incl[kPickThreads];
+    float wtot[kConsWarps];
+    int sstar, retry, token;
+    float x1;
+};
+
+template <int DT>
+__global__ void __launch_bounds__(kPickThreads) sv_pick_kernel(const SvParams p)
+{
+    constexpr int VE = Elt<DT>::kPerVec;
+    __shared__ PickShared sh;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int b = blockIdx.x;
+    const int N = p.N;
+    const int NV = p.V / VE;
+    const int S = (NV + kSliceVecs - 1) / kSliceVecs;
+
+    sv::grid_dependency_wait();  // kernel B's slice masses
+    SeqSample sq{};
+    const bool sampled = sequence_sample(p, b, sq);
+    const int j = sq.j;
+    int32_t *out = p.out + (size_t)b * (N + 1);
+    if (!sampled) {
+        if (tid == 0) {
+            const int err = __ldcg(&p.ws_err[b]);
             if (err) {
                 for (int k = 0; k <= N; ++k)
                     out[k] = -1;
@@ -830,279 +1026,180 @@ __global__ void __launch_bounds__(kThreads, 4) sv_sample_kernel(const SvParams p
     }
 
     const size_t trow = (size_t)b * (N + 1) + j;
-    const size_t drow = (size_t)b * N + j;
-    const Chunk ch = chunk_of(V / VE, rank, C);
-    const size_t row_vecs = (size_t)(V / VE);
-    const uint4 *tsrc = static_cast<const uint4 *>(p.target) + trow * row_vecs + ch.v0;
-    const uint4 *dsrc = (j < N) ? static_cast<const uint4 *>(p.draft) + drow * row_vecs + ch.v0 : nullptr;
-    const float *st = p.ws_stats + trow * 4;
-    const float mq = __ldcg(st + 0), Sq = __ldcg(st + 1);
-    const float mp = (j < N) ? __ldcg(st + 2) : 0.0f, Sp = (j < N) ? __ldcg(st + 3) : 1.0f;
-    const float isq = 1.0f / Sq, isp = (j < N) ? 1.0f / Sp : 0.0f;
-    const float uN = p.u[(size_t)b * (N + 1) + N];
+    const uint4 *tsrc = static_cast<const uint4 *>(p.target) + trow * (size_t)NV;
+    const uint4 *dsrc = (j < N) ? static_cast<const uint4 *>(p.draft) + ((size_t)b * N + j) * (size_t)NV : nullptr;
+    const float *shares = p.ws_slice + (size_t)b * S * kConsWarps;
+    float r[VE];
+    for (int sl = tid; sl < S; sl += kPickThreads) {
+        // a slice's mass: its 8 warp shares added in warp order
+        const float4 a = __ldcg(reinterpret_cast<const float4 *>(shares + (size_t)sl * kConsWarps));
+        const float4 c = __ldcg(reinterpret_cast<const float4 *>(shares + (size_t)sl * kConsWarps + 4));
+        float tot = 0.0f;
+        tot = __fadd_rn(tot, a.x);
+        tot = __fadd_rn(tot, a.y);
+        tot = __fadd_rn(tot, a.z);
+        tot = __fadd_rn(tot, a.w);
+        tot = __fadd_rn(tot, c.x);
+        tot = __fadd_rn(tot, c.y);
+        tot = __fadd_rn(tot, c.z);
+        tot = __fadd_rn(tot, c.w);
+        sh.slice[sl] = tot;
+    }
+    __syncthreads();
 
-    int res_mode = (j < N) ? RES_DIFF : RES_Q;  // RES_Q after a retry as well
-    uint32_t g = 0;                              // ring position
-    int any_abort = 0;
-    for (;;) {
-        // ---- pass 2: residual mass per slice and warp
-        const uint4 *dres = (res_mode == RES_DIFF) ? dsrc : nullptr;
-        if (warp == kProducerWarp) {
-            if (lane == 0)
-                produce(ctl.ring, ring, tsrc, dres, ch.nvec, 0, ch.ntiles, g);
-            __syncwarp();
-        } else {
-            for (int t = 0; t < ch.ntiles; ++t) {
-                const uint32_t gt = g + t;
-                float part[kVPT];
-                const bool ok = consume_wait(ctl.ring, gt);
-                if (!ok)
-                    ctl.ring.abort = 1;
-                const unsigned char *stage = ring + (gt % kStages) * (2 * kTileBytes);
-#pragma unroll
-                for (int k = 0; k < kVPT; ++k) {
-                    part[k] = 0.0f;
-                    const int sv_ = k * kSliceVecs + tid;
-                    const int vec = t * kTileVecs + sv_;
-                    if (ok && vec < ch.nvec) {
-                        float r[VE];
-                        const uint4 vd = dres ? reinterpret_cast<const uint4 *>(stage + kTileBytes)[sv_]
-                                              : make_uint4(0, 0, 0, 0);
-                        residual_vec<DT>(reinterpret_cast<const uint4 *>(stage)[sv_], vd, res_mode, mq, isq, mp,
-                                         isp, cf, r);
-#pragma unroll
-                        for (int e = 0; e < VE; ++e)
-                            part[k] = __fadd_rn(part[k], r[e]);
-                    }
-                }
-                consume_release(ctl.ring, gt, lane);
-#pragma unroll
-                for (int k = 0; k < kVPT; ++k) {
-                    const int sl = t * kVPT + k;
-                    const float incl = warp_incl_scan(part[k], lane);
-                    if (lane == 31 && sl < ch.nslices)
-                        ctl.wsum[sl][warp] = incl;
-                }
-            }
-        }
-        g += ch.ntiles;
-        __syncthreads();
-        if (warp == 0) {
-            // slice masses and their inclusive prefix over the chunk
-            float carry = 0.0f;
-            for (int t0 = 0; t0 < ch.nslices; t0 += 32) {
-                const int t = t0 + lane;
-                float tm = 0.0f;
-                if (t < ch.nslices)
-#pragma unroll
+    for (int attempt = 0; attempt < 2; ++attempt) {
+        if (attempt == 1) {
+            // q_j == p_j: the residual has no mass; draw from q_j instead
+            sq.res_mode = RES_Q;
+            for (int sl = 0; sl < S; ++sl) {
+                const float part = slice_thread_mass<DT>(tsrc, nullptr, sl, NV, tid, sq, r);
+                const float incl = warp_incl_scan(part, lane);
+                if (lane == 31)
+                    sh.wtot[warp] = incl;
+                __syncthreads();
+                if (tid == 0) {
+                    float tot = 0.0f;
                     for (int w = 0; w < kConsWarps; ++w)
-                        tm = __fadd_rn(tm, ctl.wsum[t][w]);
-                const float inc = __fadd_rn(warp_incl_scan(tm, lane), carry);
-                if (t < ch.nslices)
-                    ctl.tcum[t] = inc;
-                carry = __shfl_sync(0xffffffffu, inc, 31);
-            }
-            if (lane == 0) {
-                ctl.Rc = carry;
-                ctl.ab = ctl.ring.abort;
+                        tot = __fadd_rn(tot, sh.wtot[w]);
+                    sh.slice[sl] = tot;
+                }
+                __syncthreads();
             }
         }
-        if (C > 1)
-            sv::cluster_sync();  // chunk masses visible
-        else
-            __syncthreads();
+        // slice s* whose cumulative mass first exceeds u_N * R (warp 0)
         if (warp == 0) {
-            // chunk c* whose cumulative mass first exceeds u_N * R
-            float Rr = 0.0f;
-            int ab = 0;
-            if (lane < (int)C) {
-                Rr = sv::ld_dsmem_f32(sv::dsmem_addr(&ctl.Rc, lane));
-                ab = sv::ld_dsmem_s32(sv::dsmem_addr(&ctl.ab, lane));
+            float carry = 0.0f;
+            for (int c0 = 0; c0 < S; c0 += 32) {
+                const int c = c0 + lane;
+                const float m = (c < S) ? sh.slice[c] : 0.0f;
+                carry = __shfl_sync(0xffffffffu, __fadd_rn(warp_incl_scan(m, lane), carry), 31);
             }
-            const float cum = warp_incl_scan(Rr, lane);
-            const float Rt = __shfl_sync(0xffffffffu, cum, 31);
-            const float x = __fmul_rn(uN, Rt);
-            const unsigned hit = __ballot_sync(0xffffffffu, lane < (int)C && x < cum);
-            int cs;
-            float x1;
-            if (hit) {
-                cs = __ffs(hit) - 1;
-                const float prev = __shfl_sync(0xffffffffu, cum, cs > 0 ? cs - 1 : 0);
-                x1 = __fsub_rn(x, cs > 0 ? prev : 0.0f);
-            } else {  // rounding: the last chunk that has mass
-                const unsigned pos = __ballot_sync(0xffffffffu, lane < (int)C && Rr > 0.0f);
-                cs = pos ? 31 - __clz(pos) : (int)C - 1;
+            const float Rt = carry;
+            const float x = __fmul_rn(sq.uN, Rt);
+            int cs = -1;
+            float x1 = INFINITY, run = 0.0f;
+            for (int c0 = 0; c0 < S && cs < 0; c0 += 32) {
+                const int c = c0 + lane;
+                const float m = (c < S) ? sh.slice[c] : 0.0f;
+                const float inc = __fadd_rn(warp_incl_scan(m, lane), run);
+                const unsigned hit = __ballot_sync(0xffffffffu, c < S && x < inc);
+                if (hit) {
+                    const int l = __ffs(hit) - 1;
+                    const float prev = __shfl_sync(0xffffffffu, inc, l > 0 ? l - 1 : 0);
+                    cs = c0 + l;
+                    x1 = __fsub_rn(x, l > 0 ? prev : run);
+                }
+                run = __shfl_sync(0xffffffffu, inc, 31);
+            }
+            if (cs < 0) {  // rounding: the last slice that has mass
+                for (int c0 = ((S - 1) / 32) * 32; c0 >= 0 && cs < 0; c0 -= 32) {
+                    const int c = c0 + lane;
+                    const unsigned m = __ballot_sync(0xffffffffu, c < S && sh.slice[c] > 0.0f);
+                    if (m)
+                        cs = c0 + 31 - __clz(m);
+                }
+                if (cs < 0)
+                    cs = S - 1;
                 x1 = INFINITY;
             }
-            const unsigned abm = __ballot_sync(0xffffffffu, ab != 0);
             if (lane == 0) {
-                ctl.retry = (Rt == 0.0f && res_mode == RES_DIFF) ? 1 : 0;
-                ctl.cstar = cs;
-                ctl.x1 = x1;
-                ctl.any_abort = abm != 0;
+                sh.retry = (Rt == 0.0f && sq.res_mode == RES_DIFF) ? 1 : 0;
+                sh.sstar = cs;
+                sh.x1 = x1;
             }
         }
         __syncthreads();
-        any_abort = ctl.any_abort;
-        if (!ctl.retry)
+        if (!sh.retry)
             break;
-        res_mode = RES_Q;  // q_j == p_j: draw from q_j instead
-        if (C > 1)
-            sv::cluster_sync();  // peers are done reading ctl.Rc
-        else
-            __syncthreads();
+        __syncthreads();
     }
 
-    if ((int)rank == ctl.cstar) {
-        if (warp == 0) {
-            // slice s* of the chunk, and the target relative to its start
-            const float x1 = ctl.x1;
-            int ts = -1;
-            float x2 = INFINITY;
-            if (x1 != INFINITY) {
-                for (int t0 = 0; t0 < ch.nslices && ts < 0; t0 += 32) {
-                    const int t = t0 + lane;
-                    const unsigned m = __ballot_sync(0xffffffffu, t < ch.nslices && x1 < ctl.tcum[t]);
-                    if (m)
-                        ts = t0 + __ffs(m) - 1;
-                }
-                if (ts >= 0)
-                    x2 = __fsub_rn(x1, ts > 0 ? ctl.tcum[ts - 1] : 0.0f);
+    // recompute slice s*: warp totals equal kernel B's, then warp, lane, element
+    const int ss = sh.sstar;
+    const float part = slice_thread_mass<DT>(tsrc, dsrc, ss, NV, tid, sq, r);
+    const float incl = warp_incl_scan(part, lane);
+    sh.incl[tid] = incl;
+    __syncthreads();
+    // thread that owns the target: broadcast its element values through r
+    const float x1 = sh.x1;
+    int sel = -1;
+    float xl = 0.0f;
+    if (warp == 0 && x1 != INFINITY) {
+        const float wt = (lane < kConsWarps) ? sh.incl[lane * 32 + 31] : 0.0f;
+        float wc = 0.0f;  // warp totals added in warp order, as kernel B does
+        float wprev = 0.0f;
+        int ws = -1;
+        for (int w = 0; w < kConsWarps; ++w) {
+            const float wtw = __shfl_sync(0xffffffffu, wt, w);
+            const float next = __fadd_rn(wc, wtw);
+            if (ws < 0 && x1 < next) {
+                ws = w;
+                wprev = wc;
             }
-            if (ts < 0) {  // rounding: the last slice that has mass
-                for (int t0 = ((ch.nslices - 1) / 32) * 32; t0 >= 0 && ts < 0; t0 -= 32) {
-                    const int t = t0 + lane;
-                    float tm = 0.0f;
-                    if (t < ch.nslices)
-                        for (int w = 0; w < kConsWarps; ++w)
-                            tm += ctl.wsum[t][w];
-                    const unsigned m = __ballot_sync(0xffffffffu, tm > 0.0f);
-                    if (m)
-                        ts = t0 + 31 - __clz(m);
-                }
-                if (ts < 0)
-                    ts = ch.nslices - 1;
-                x2 = INFINITY;
-            }
-            if (lane == 0) {
-                ctl.tstar = ts;
-                ctl.x2 = x2;
+            wc = next;
+        }
+        if (ws >= 0) {
+            const float xw = __fsub_rn(x1, wprev);
+            const float li = sh.incl[ws * 32 + lane];
+            const unsigned ml = __ballot_sync(0xffffffffu, xw < li);
+            if (ml) {
+                const int ls = __ffs(ml) - 1;
+                const float lprev = __shfl_sync(0xffffffffu, li, ls > 0 ? ls - 1 : 0);
+                sel = ws * 32 + ls;
+                xl = __fsub_rn(xw, ls > 0 ? lprev : 0.0f);
             }
         }
-        __syncthreads();
-        const int sstar = ctl.tstar;              // slice
-        const int tstar = sstar / kVPT;           // ring tile holding it
-        const int kstar = sstar - tstar * kVPT;   // its place in the stage
-        // ---- pass 3: reload the tile of slice s*, redo its warp scans, find the element
-        const uint4 *dres = (res_mode == RES_DIFF) ? dsrc : nullptr;
-        if (warp == kProducerWarp) {
-            if (lane == 0)
-                produce(ctl.ring, ring, tsrc, dres, ch.nvec, tstar, tstar + 1, g);
-            __syncwarp();
-        } else {
-            float part = 0.0f;
-            if (consume_wait(ctl.ring, g)) {
-                const int vec = sstar * kSliceVecs + tid;
-                if (vec < ch.nvec) {
-                    const unsigned char *stage = ring + (g % kStages) * (2 * kTileBytes);
-                    const int sv_ = kstar * kSliceVecs + tid;
-                    float r[VE];
-                    const uint4 vd = dres ? reinterpret_cast<const uint4 *>(stage + kTileBytes)[sv_]
-                                          : make_uint4(0, 0, 0, 0);
-                    residual_vec<DT>(reinterpret_cast<const uint4 *>(stage)[sv_], vd, res_mode, mq, isq, mp, isp,
-                                     cf, r);
-#pragma unroll
-                    for (int e = 0; e < VE; ++e)
-                        part = __fadd_rn(part, r[e]);
-                }
-            } else {
-                ctl.ring.abort = 1;
-            }
-            ctl.incl[tid] = warp_incl_scan(part, lane);
-        }
-        __syncthreads();
-        if (warp == 0) {
-            const int nvec_t = min(kSliceVecs, ch.nvec - sstar * kSliceVecs);
-            const float x2 = ctl.x2;
-            const float wt = (lane < kConsWarps) ? ctl.incl[lane * 32 + 31] : 0.0f;
-            const float wc = warp_incl_scan(wt, lane);
-            int sel = -1;
-            float xl = 0.0f;
-            const unsigned mw = __ballot_sync(0xffffffffu, lane < kConsWarps && x2 < wc);
-            if (mw) {
-                const int ws = __ffs(mw) - 1;
-                const float wprev = __shfl_sync(0xffffffffu, wc, ws > 0 ? ws - 1 : 0);
-                const float xw = __fsub_rn(x2, ws > 0 ? wprev : 0.0f);
-                const float li = ctl.incl[ws * 32 + lane];
-                const unsigned ml = __ballot_sync(0xffffffffu, xw < li);
-                if (ml) {
-                    const int ls = __ffs(ml) - 1;
-                    const float lprev = __shfl_sync(0xffffffffu, li, ls > 0 ? ls - 1 : 0);
-                    sel = ws * 32 + ls;
-                    xl = __fsub_rn(xw, ls > 0 ? lprev : 0.0f);
-                }
-            }
-            if (lane == 0) {
-                const unsigned char *stage = ring + (g % kStages) * (2 * kTileBytes);
-                auto thread_r = [&](int th, float *r) {
-                    const int sv_ = kstar * kSliceVecs + th;
-                    const uint4 vd = dres ? reinterpret_cast<const uint4 *>(stage + kTileBytes)[sv_]
-                                          : make_uint4(0, 0, 0, 0);
-                    residual_vec<DT>(reinterpret_cast<const uint4 *>(stage)[sv_], vd, res_mode, mq, isq, mp, isp,
-                                     cf, r);
-                };
-                int token = -1;
-                if (sel >= 0 && sel < nvec_t) {
-                    float r[VE];
-                    thread_r(sel, r);
-                    float acc = 0.0f;
-                    for (int e = 0; e < VE; ++e) {
-                        acc = __fadd_rn(acc, r[e]);
-                        if (xl < acc) {
-                            token = (ch.v0 + sstar * kSliceVecs + sel) * VE + e;
-                            break;
-                        }
-                    }
-                }
-                if (token < 0) {
-                    // rounding left the target at or past the total: the
-                    // last element of the slice that carries mass
-                    for (int th = nvec_t - 1; th >= 0 && token < 0; --th) {
-                        float r[VE];
-                        thread_r(th, r);
-                        for (int e = VE - 1; e >= 0; --e)
-                            if (r[e] > 0.0f) {
-                                token = (ch.v0 + sstar * kSliceVecs + th) * VE + e;
-                                break;
-                            }
-                    }
-                    if (token < 0)
-                        token = (ch.v0 + sstar * kSliceVecs + nvec_t) * VE - 1;
-                }
-                // the sequence's outputs, and its workspace back to idle
-                if (any_abort || ctl.ring.abort) {
-                    for (int k = 0; k <= N; ++k)
-                        out[k] = -1;
-                    p.nacc[b] = -1;
-                    atomicOr(p.status, kErrTimeout);
-                } else {
-                    for (int k = 0; k < j; ++k)
-                        out[k] = p.tokens[(size_t)b * N + k];
-                    out[j] = token;
-                    for (int k = j + 1; k <= N; ++k)
-                        out[k] = -1;
-                    p.nacc[b] = j;
-                }
-                p.ws_first[b] = kNoReject;
-                p.ws_err[b] = 0;
-            }
+        if (lane == 0) {
+            sh.sstar = sel;  // reused: the selected thread
+            sh.x1 = xl;
         }
     }
-
-    if (C > 1)
-        sv::cluster_sync();  // no peer reads this CTA's shared memory any more
-    if (tid == 0 && ctl.ring.abort)
-        ring_drain(ctl.ring);
+    __syncthreads();
+    sel = sh.sstar;
+    xl = sh.x1;
+    if (tid == (sel >= 0 ? sel : 0)) {
+        int token = -1;
+        if (sel >= 0) {
+            float acc = 0.0f;
+            for (int e = 0; e < VE; ++e) {
+                acc = __fadd_rn(acc, r[e]);
+                if (xl < acc) {
+                    token = (ss * kSliceVecs + tid) * VE + e;
+                    break;
+                }
+            }
+        }
+        sh.token = token;  // -1 if rounding left it unset
+    }
+    __syncthreads();
+    if (sh.token < 0) {
+        // rounding: the last element of slice s* that carries mass
+        if (tid == 0)
+            sh.sstar = -1;
+        __syncthreads();
+        int mine = -1;
+        for (int e = VE - 1; e >= 0; --e)
+            if (r[e] > 0.0f) {
+                mine = (ss * kSliceVecs + tid) * VE + e;
+                break;
+            }
+        if (mine >= 0)
+            atomicMax(&sh.sstar, mine);
+        __syncthreads();
+        if (tid == 0)
+            sh.token = sh.sstar >= 0 ? sh.sstar : min(NV, (ss + 1) * kSliceVecs) * VE - 1;
+        __syncthreads();
+    }
+    if (tid == 0) {
+        for (int k = 0; k < j; ++k)
+            out[k] = p.tokens[(size_t)b * N + k];
+        out[j] = sh.token;
+        for (int k = j + 1; k <= N; ++k)
+            out[k] = -1;
+        p.nacc[b] = j;
+        p.ws_first[b] = kNoReject;
+        p.ws_err[b] = 0;
+    }
 }
 
 } // namespace
@@ -1118,10 +1215,10 @@ struct spec_verify_ctx {
     int num_sms;
     int cluster_override;                // kernel A cluster size, 0 = automatic
     int clusters_a[kMaxCluster + 1];     // co-resident clusters of kernel A per size, 0 = none
-    int clusters_b[kMaxCluster + 1];     // the same for kernel B
     void *ws;
+    int mass_ctas;                       // resident CTAs of the mass kernel (all SMs)
     int *ws_first, *ws_err, *ws_tok, *status;
-    float *ws_stats;
+    float *ws_stats, *ws_slice;
     // profiling: events before kernel A, between the kernels and after kernel B
     int prof_on, prof_runs;
     cudaEvent_t *prof_ev;  // [kProfRuns][3]
@@ -1158,10 +1255,28 @@ template <typename K> cudaError_t set_kernel_attrs(K kernel, size_t smem)
 
 template <int DT> cudaError_t set_attrs()
 {
-    cudaError_t e = set_kernel_attrs(sv_rows_kernel<DT>, kSmemA);
+    const cudaError_t e = set_kernel_attrs(sv_rows_kernel<DT>, kSmemA);
     if (e != cudaSuccess)
         return e;
-    return set_kernel_attrs(sv_sample_kernel<DT>, kSmemB);
+    return cudaFuncSetAttribute(sv_mass_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemM);
+}
+
+// Resident CTAs of the mass kernel on the whole device.
+template <int DT> int mass_ctas(int num_sms)
+{
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, sv_mass_kernel<DT>, kThreads, kSmemM) != cudaSuccess) {
+        cudaGetLastError();
+        n = 1;
+    }
+    return (n > 0 ? n : 1) * num_sms;
+}
+
+// Slices of 256 vectors per row.
+int residual_slices(int V, sv_dtype dt)
+{
+    const int nv = V * (dt == SV_BF16 ? 2 : 4) / 16;
+    return (nv + kSliceVecs - 1) / kSliceVecs;
 }
 
 // attr must hold two entries; `dependent` lets the launch overlap the tail of
@@ -1200,15 +1315,12 @@ template <typename K> int active_clusters(K kernel, int C, size_t smem)
     return n;
 }
 
-// Co-resident cluster counts for every size, both kernels.
-template <int DT> void query_clusters(int *a, int *b)
+// Co-resident clusters of kernel A for every cluster size.
+template <int DT> void query_clusters(int *a)
 {
-    for (int k = 1; k <= kMaxCluster; ++k) {
+    for (int k = 1; k <= kMaxCluster; ++k)
         a[k] = active_clusters(sv_rows_kernel<DT>, k, kSmemA);
-        b[k] = active_clusters(sv_sample_kernel<DT>, k, kSmemB);
-    }
     a[1] = a[1] > 0 ? a[1] : 1;
-    b[1] = b[1] > 0 ? b[1] : 1;
 }
 
 // Smallest cluster that keeps each chunk within kMaxSlices slices.
@@ -1243,19 +1355,6 @@ int cluster_a(const spec_verify_ctx *c, int B, int N)
     return clamp_cluster(C < 8 ? C : 8, nv, c->clusters_a);
 }
 
-// Kernel B: at most two CTAs per sequence (fewer, longer streams measured
-// faster than more, shorter ones), more when a chunk would be too large.
-int cluster_b(const spec_verify_ctx *c, int B)
-{
-    const long long row_bytes = (long long)c->V * elt_bytes(c->dtype);
-    const int nv = (int)(row_bytes / 16);
-    long long C = (row_bytes + 32767) / 32768;
-    const long long par = (2LL * c->num_sms + B - 1) / (B > 0 ? B : 1);
-    if (par > C)
-        C = par;
-    return clamp_cluster((int)(C < 2 ? C : 2), nv, c->clusters_b);
-}
-
 sv_status run_impl(spec_verify_ctx *ctx, const void *target, const void *draft, const int32_t *tokens,
                    const float *u, const float *T, int greedy, int B, int N, int32_t *out,
                    int32_t *nacc, void *stream, float *q_at, float *p_at, float *tstats, float *dstats)
@@ -1275,14 +1374,17 @@ sv_status run_impl(spec_verify_ctx *ctx, const void *target, const void *draft, 
     if ((reinterpret_cast<uintptr_t>(target) & 15u) || (draft && (reinterpret_cast<uintptr_t>(draft) & 15u)))
         return SV_ERR_INVALID_ARG;
     const int CA = cluster_a(ctx, B, N);
-    const int CB = cluster_b(ctx, B);
     const int nv = ctx->V * elt_bytes(ctx->dtype) / 16;
-    if ((nv + CA - 1) / CA > kMaxSlices * kSliceVecs || (nv + CB - 1) / CB > kMaxSlices * kSliceVecs)
+    if ((nv + CA - 1) / CA > kMaxSlices * kSliceVecs)
         return SV_ERR_SHAPE;
     const long long units = (long long)B * (N + 1);
-    if (units * CA > INT_MAX || (long long)B * CB > INT_MAX)
+    if (units * CA > INT_MAX)
         return SV_ERR_INVALID_ARG;
+    const long long tiles = (long long)B * ((nv + kTileVecsM - 1) / kTileVecsM);
+    const int grid_m = (int)(tiles < ctx->mass_ctas ? tiles : ctx->mass_ctas);
 
+    if (reinterpret_cast<uintptr_t>(ctx->ws_slice) & 15u)  // kernel C reads it as float4
+        return SV_ERR_CUDA;
     DeviceGuard guard(ctx->device);
     if (!guard.ok)
         return SV_ERR_CUDA;
@@ -1303,6 +1405,7 @@ sv_status run_impl(spec_verify_ctx *ctx, const void *target, const void *draft, 
     prm.ws_err = ctx->ws_err;
     prm.ws_tok = ctx->ws_tok;
     prm.ws_stats = ctx->ws_stats;
+    prm.ws_slice = ctx->ws_slice;
     prm.status = ctx->status;
     prm.B = B;
     prm.N = N;
@@ -1322,10 +1425,30 @@ sv_status run_impl(spec_verify_ctx *ctx, const void *target, const void *draft, 
     if (e == cudaSuccess) {
         if (ev)
             cudaEventRecord(ev[1], st);
-        // dependent launch only when nothing is recorded between the kernels
-        cfg = launch_config((unsigned)(B * CB), CB, kSmemB, st, attr, /*dependent=*/ev == nullptr);
-        e = (ctx->dtype == SV_BF16) ? cudaLaunchKernelEx(&cfg, sv_sample_kernel<SV_BF16>, prm)
-                                    : cudaLaunchKernelEx(&cfg, sv_sample_kernel<SV_F32>, prm);
+        // B and C are dependent launches (their start overlaps the previous
+        // kernel's tail), except between the profiling events
+        cudaLaunchAttribute pdl[1];
+        pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        pdl[0].val.programmaticStreamSerializationAllowed = 1;
+        cudaLaunchConfig_t cfgm = {};
+        cfgm.gridDim = dim3((unsigned)(grid_m > 0 ? grid_m : 1));
+        cfgm.blockDim = dim3(kThreads);
+        cfgm.dynamicSmemBytes = kSmemM;
+        cfgm.stream = st;
+        cfgm.attrs = pdl;
+        cfgm.numAttrs = ev == nullptr ? 1 : 0;
+        e = (ctx->dtype == SV_BF16) ? cudaLaunchKernelEx(&cfgm, sv_mass_kernel<SV_BF16>, prm)
+                                    : cudaLaunchKernelEx(&cfgm, sv_mass_kernel<SV_F32>, prm);
+        if (e == cudaSuccess) {
+            cudaLaunchConfig_t cfgp = {};
+            cfgp.gridDim = dim3((unsigned)B);
+            cfgp.blockDim = dim3(kPickThreads);
+            cfgp.stream = st;
+            cfgp.attrs = pdl;
+            cfgp.numAttrs = 1;
+            e = (ctx->dtype == SV_BF16) ? cudaLaunchKernelEx(&cfgp, sv_pick_kernel<SV_BF16>, prm)
+                                        : cudaLaunchKernelEx(&cfgp, sv_pick_kernel<SV_F32>, prm);
+        }
         if (ev && e == cudaSuccess)
             cudaEventRecord(ev[2], st);
     }
@@ -1376,14 +1499,19 @@ sv_status spec_verify_create(spec_verify_ctx **out, int device, int max_B, int m
         return SV_ERR_CUDA;
     }
     if (dtype == SV_BF16)
-        query_clusters<SV_BF16>(c->clusters_a, c->clusters_b);
+        query_clusters<SV_BF16>(c->clusters_a);
     else
-        query_clusters<SV_F32>(c->clusters_a, c->clusters_b);
+        query_clusters<SV_F32>(c->clusters_a);
 
-    // workspace: first[nb] err[nb] tok[ntok] stats[4*ntok] status
+    c->mass_ctas = (dtype == SV_BF16) ? mass_ctas<SV_BF16>(c->num_sms) : mass_ctas<SV_F32>(c->num_sms);
+
+    // workspace: first[nb] err[nb] tok[ntok] stats[4*ntok] | slice[nb*S*8] status;
+    // the slice shares start on a 256-byte boundary (kernel C reads them as float4)
     const size_t nb = (size_t)(max_B > 0 ? max_B : 1);
     const size_t ntok = nb * (size_t)(max_N + 1);
-    const size_t bytes = sizeof(int) * (2 * nb + 5 * ntok + 1);
+    const size_t nslice = nb * (size_t)residual_slices(V, dtype) * kConsWarps;
+    const size_t slice_off = (2 * nb + 5 * ntok + 63) / 64 * 64;
+    const size_t bytes = sizeof(int) * (slice_off + nslice + 1);
     if (cudaMalloc(&c->ws, bytes) != cudaSuccess) {
         cudaGetLastError();
         free(c);
@@ -1394,7 +1522,8 @@ sv_status spec_verify_create(spec_verify_ctx **out, int device, int max_B, int m
     c->ws_err = w + nb;
     c->ws_tok = w + 2 * nb;
     c->ws_stats = reinterpret_cast<float *>(w + 2 * nb + ntok);
-    c->status = w + 2 * nb + 5 * ntok;
+    c->ws_slice = reinterpret_cast<float *>(w + slice_off);
+    c->status = w + slice_off + nslice;
     if (cudaMemset(c->ws, 0, bytes) != cudaSuccess || cudaMemset(c->ws_first, 0x7f, sizeof(int) * nb) != cudaSuccess ||
         cudaDeviceSynchronize() != cudaSuccess) {
         cudaGetLastError();
@@ -1488,7 +1617,7 @@ const char *spec_verify_error_string(sv_status s)
     case SV_ERR_TIMEOUT: return "SV_ERR_TIMEOUT: a bounded wait in the kernel gave up";
     case SV_ERR_TOO_LARGE:
         return "SV_ERR_TOO_LARGE: batch exceeds the fixed scratch of spec_verify_run_noalloc "
-               "(B <= 2048, B*(N+1) <= 16384)";
+               "(B <= 2048, B*(N+1) <= 16384, B*ceil(V*elt/4KiB) <= 16384)";
     }
     return "unknown sv_status";
 }
@@ -1594,7 +1723,10 @@ void spec_verify_destroy(spec_verify_ctx *ctx)
 namespace {
 constexpr int kNoAllocMaxB = 2048;        // sequences per call
 constexpr int kNoAllocMaxUnits = 16384;   // B*(N+1) verified positions per call
-constexpr int kNoAllocInts = 2 * kNoAllocMaxB + 5 * kNoAllocMaxUnits + 1;  // about 336 KiB
+constexpr int kNoAllocMaxSlices = 16384;  // B*ceil(V*elt/4 KiB) residual slices per call
+constexpr int kNoAllocSliceOff = 2 * kNoAllocMaxB + 5 * kNoAllocMaxUnits;  // a multiple of 64 ints
+static_assert(kNoAllocSliceOff % 64 == 0, "slice shares must start on a 256-byte boundary");
+constexpr int kNoAllocInts = kNoAllocSliceOff + 8 * kNoAllocMaxSlices + 1;  // about 848 KiB
 constexpr int kNoAllocMaxDevices = 64;
 } // namespace
 
@@ -1606,8 +1738,9 @@ struct NoAllocDevice {
     bool ready;
     int *scratch;     // device address of g_sv_noalloc_scratch on this device
     int num_sms;
-    int clusters_bf16[2][kMaxCluster + 1];  // kernels A, B
-    int clusters_f32[2][kMaxCluster + 1];
+    int mass_bf16, mass_f32;
+    int clusters_bf16[kMaxCluster + 1];  // co-resident clusters of the row kernel per size
+    int clusters_f32[kMaxCluster + 1];
 };
 
 std::mutex g_noalloc_mutex;
@@ -1632,8 +1765,10 @@ sv_status noalloc_setup(int device, NoAllocDevice &nd)
         cudaGetLastError();
         return SV_ERR_CUDA;
     }
-    query_clusters<SV_BF16>(nd.clusters_bf16[0], nd.clusters_bf16[1]);
-    query_clusters<SV_F32>(nd.clusters_f32[0], nd.clusters_f32[1]);
+    query_clusters<SV_BF16>(nd.clusters_bf16);
+    query_clusters<SV_F32>(nd.clusters_f32);
+    nd.mass_bf16 = mass_ctas<SV_BF16>(nd.num_sms);
+    nd.mass_f32 = mass_ctas<SV_F32>(nd.num_sms);
     nd.scratch = w;
     nd.ready = true;
     return SV_OK;
@@ -1654,7 +1789,8 @@ extern "C" sv_status spec_verify_run_noalloc(const void *target_logits, const vo
     if (V < 1 || ((long long)V * elt_bytes(dtype)) % 16 != 0 ||
         (long long)V * elt_bytes(dtype) / 16 > (long long)kMaxCluster * kMaxSlices * kSliceVecs)
         return SV_ERR_SHAPE;
-    if (B > kNoAllocMaxB || (long long)B * (N + 1) > kNoAllocMaxUnits)
+    if (B > kNoAllocMaxB || (long long)B * (N + 1) > kNoAllocMaxUnits ||
+        (long long)B * residual_slices(V, dtype) > kNoAllocMaxSlices)
         return SV_ERR_TOO_LARGE;
     if (B == 0)
         return SV_OK;
@@ -1683,15 +1819,16 @@ extern "C" sv_status spec_verify_run_noalloc(const void *target_logits, const vo
     c.V = V;
     c.dtype = dtype;
     c.num_sms = nd->num_sms;
-    memcpy(c.clusters_a, dtype == SV_BF16 ? nd->clusters_bf16[0] : nd->clusters_f32[0], sizeof c.clusters_a);
-    memcpy(c.clusters_b, dtype == SV_BF16 ? nd->clusters_bf16[1] : nd->clusters_f32[1], sizeof c.clusters_b);
+    memcpy(c.clusters_a, dtype == SV_BF16 ? nd->clusters_bf16 : nd->clusters_f32, sizeof c.clusters_a);
+    c.mass_ctas = dtype == SV_BF16 ? nd->mass_bf16 : nd->mass_f32;
     int *w = nd->scratch;
     c.ws = w;
     c.ws_first = w;
     c.ws_err = w + kNoAllocMaxB;
     c.ws_tok = w + 2 * kNoAllocMaxB;
     c.ws_stats = reinterpret_cast<float *>(w + 2 * kNoAllocMaxB + kNoAllocMaxUnits);
-    c.status = w + 2 * kNoAllocMaxB + 5 * kNoAllocMaxUnits;
+    c.ws_slice = reinterpret_cast<float *>(w + kNoAllocSliceOff);
+    c.status = w + kNoAllocSliceOff + 8 * kNoAllocMaxSlices;
 
     // The scratch keeps whatever the previous call left in it: put the slots
     // this call uses into their starting state first (on the same stream, so
