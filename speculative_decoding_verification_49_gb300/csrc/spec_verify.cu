@@ -813,7 +813,8 @@ struct SeqSample {
     float mq, isq, mp, isp, cf, uN;
 };
 
-__device__ __forceinline__ bool sequence_sample(const SvParams &p, int b, SeqSample &s)
+// cf (log2(e)/T, one double division) is left to the caller when with_cf is false.
+__device__ __forceinline__ bool sequence_sample(const SvParams &p, int b, SeqSample &s, bool with_cf = true)
 {
     float T;
     const int mode = sequence_mode(p, b, T);
@@ -829,7 +830,7 @@ __device__ __forceinline__ bool sequence_sample(const SvParams &p, int b, SeqSam
     s.isq = 1.0f / __ldcg(st + 1);
     s.mp = (j < p.N) ? __ldcg(st + 2) : 0.0f;
     s.isp = (j < p.N) ? 1.0f / __ldcg(st + 3) : 0.0f;
-    s.cf = (float)(kLog2e / (double)T);
+    s.cf = with_cf ? (float)(kLog2e / (double)T) : T;
     s.uN = p.u[(size_t)b * (p.N + 1) + p.N];
     return true;
 }
@@ -1000,7 +1001,11 @@ __global__ void __launch_bounds__(kPickThreads) sv_pick_kernel(const SvParams p)
 
     sv::grid_dependency_wait();  // kernel B's slice masses
     SeqSample sq{};
-    const bool sampled = sequence_sample(p, b, sq);
+    const bool sampled = sequence_sample(p, b, sq, /*with_cf=*/false);  // sq.cf holds T
+    if (tid == 0)
+        sh.x1 = sampled ? (float)(kLog2e / (double)sq.cf) : 0.0f;  // log2(e)/T, once
+    __syncthreads();
+    sq.cf = sh.x1;
     const int j = sq.j;
     int32_t *out = p.out + (size_t)b * (N + 1);
     if (!sampled) {
