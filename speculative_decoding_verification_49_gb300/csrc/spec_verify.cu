@@ -360,35 +360,46 @@ __device__ __forceinline__ ArgMax warp_argmax(ArgMax a)
 
 // ---- residual mass of one 16-byte vector --------------------------------------
 // r_k = max(0, q_k - p_k) (RES_DIFF) or q_k (RES_Q), with
-// q_k = 2^((zq_k - mq) c) / Sq.  Target and draft element k travel as one
-// f32x2 pair.  Every operation rounds to nearest and nothing is contracted,
-// so the result is bit-identical wherever it is recomputed (pass 2 and
-// pass 3).
+// q_k = 2^((zq_k - mq) c) / Sq.  Adjacent elements k, k+1 travel as one f32x2
+// pair (they come out of one bf16x2 word, or two neighbouring floats).  Every
+// operation rounds to nearest and nothing is contracted, so the result is
+// bit-identical wherever it is recomputed (kernels B and C).
 template <int DT>
 __device__ __forceinline__ void residual_vec(const uint4 vt, const uint4 vd, int res_mode, float mq,
                                              float isq, float mp, float isp, float cf, float *r)
 {
     constexpr int NE = Elt<DT>::kPerVec;
-    float zt[NE], zd[NE];
-    unpack<DT>(vt, zt);
-    const unsigned long long Cf = sv::pack2(cf, cf);
-    if (res_mode == RES_DIFF) {
-        unpack<DT>(vd, zd);
-        const unsigned long long M = sv::pack2(mq, mp), IS = sv::pack2(isq, isp);
+    constexpr int NP = NE / 2;
+    unsigned long long zt[NP], zd[NP];
+    const uint32_t wt[4] = {vt.x, vt.y, vt.z, vt.w};
+    const uint32_t wd[4] = {vd.x, vd.y, vd.z, vd.w};
 #pragma unroll
-        for (int e = 0; e < NE; ++e) {
-            float a0, a1, qk, pk;
-            sv::unpack2(sv::mul2(sv::sub2(sv::pack2(zt[e], zd[e]), M), Cf), a0, a1);
-            sv::unpack2(sv::mul2(sv::pack2(sv::ex2(a0), sv::ex2(a1)), IS), qk, pk);
-            r[e] = fmaxf(__fsub_rn(qk, pk), 0.0f);
+    for (int k = 0; k < NP; ++k) {
+        if constexpr (DT == SV_BF16) {
+            zt[k] = sv::pack2(__uint_as_float(wt[k] << 16), __uint_as_float(wt[k] & 0xffff0000u));
+            zd[k] = sv::pack2(__uint_as_float(wd[k] << 16), __uint_as_float(wd[k] & 0xffff0000u));
+        } else {
+            zt[k] = sv::pack2(__uint_as_float(wt[2 * k]), __uint_as_float(wt[2 * k + 1]));
+            zd[k] = sv::pack2(__uint_as_float(wd[2 * k]), __uint_as_float(wd[2 * k + 1]));
         }
-    } else {
-        const unsigned long long M = sv::pack2(mq, mq), IS = sv::pack2(isq, isq);
+    }
+    const unsigned long long Cf = sv::pack2(cf, cf);
+    const unsigned long long Mq = sv::pack2(mq, mq), Iq = sv::pack2(isq, isq);
 #pragma unroll
-        for (int e = 0; e < NE; e += 2) {
-            float a0, a1;
-            sv::unpack2(sv::mul2(sv::sub2(sv::pack2(zt[e], zt[e + 1]), M), Cf), a0, a1);
-            sv::unpack2(sv::mul2(sv::pack2(sv::ex2(a0), sv::ex2(a1)), IS), r[e], r[e + 1]);
+    for (int k = 0; k < NP; ++k) {
+        float a0, a1;
+        sv::unpack2(sv::mul2(sv::sub2(zt[k], Mq), Cf), a0, a1);
+        const unsigned long long q = sv::mul2(sv::pack2(sv::ex2(a0), sv::ex2(a1)), Iq);
+        if (res_mode == RES_DIFF) {
+            const unsigned long long Mp = sv::pack2(mp, mp), Ip = sv::pack2(isp, isp);
+            sv::unpack2(sv::mul2(sv::sub2(zd[k], Mp), Cf), a0, a1);
+            const unsigned long long pk = sv::mul2(sv::pack2(sv::ex2(a0), sv::ex2(a1)), Ip);
+            float d0, d1;
+            sv::unpack2(sv::sub2(q, pk), d0, d1);
+            r[2 * k] = fmaxf(d0, 0.0f);
+            r[2 * k + 1] = fmaxf(d1, 0.0f);
+        } else {
+            sv::unpack2(q, r[2 * k], r[2 * k + 1]);
         }
     }
 }
