@@ -130,6 +130,23 @@ def dist_init(args):
     return world, rank, local, pg
 
 
+def max_over_ranks(ms: float, pg, device) -> float:
+    """The slowest rank's time: every rank ran the same number of steps on its
+    own replica, so the job finishes when the slowest one does."""
+    if pg is None:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_step: int, world: int, steps: int, ms: float) -> float:
+    """Whole-job throughput: units every rank processed, over the slowest time."""
+    return units_per_step * world * steps / (ms * 1e-3)
+
+
 def workload_desc(w) -> str:
     extra = {"headline": "T=0.8, Zipf prior (-1.1 ln rank) on odd sequences",
              "stress": "T=1.0, 5% forced near-zero-q drafts",
@@ -266,19 +283,15 @@ def run_ours(args):
             step()
         end.record(stream)
         torch.cuda.synchronize(dev)
-    ms = start.elapsed_time(end)
+    ms = max_over_ranks(start.elapsed_time(end), pg, dev)
     if pg:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
         pg.barrier()
     if ctx.status() != sv.SV_OK:
         raise RuntimeError("device status set during the timed region")
 
     ms_step = ms / args.steps
     rows = w.verified_rows
-    value = rows * world * args.steps / (ms * 1e-3)
+    value = job_rate(rows, world, args.steps, ms)
     gbs = w.logit_bytes / (ms_step * 1e-3) / 1e9
     peak, peak_kind = peaks()
 
@@ -330,13 +343,8 @@ def run_ours(args):
             e2e_step()
         ee.record(stream)
         torch.cuda.synchronize(dev)
-        ems = es.elapsed_time(ee)
-        if pg:
-            import torch.distributed as dist
-            t = torch.tensor([ems], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
-        e2e = {"value": rows * world * k2 / (ems * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        ems = max_over_ranks(es.elapsed_time(ee), pg, dev)
+        e2e = {"value": job_rate(rows, world, k2, ems), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": k2}
 
     cpu = None
