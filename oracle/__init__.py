@@ -87,6 +87,8 @@ class Oracle:
                                         P, P, P, P, P, P, P, i]
         self.lib.orc_softmax_row.restype = i
         self.lib.orc_softmax_row.argtypes = [P, i, i, ctypes.c_double, P, P, P]
+        self.lib.orc_kv_commit.restype = i
+        self.lib.orc_kv_commit.argtypes = [P, P, P, P, i, i, i, i, ctypes.c_size_t]
 
     def verify(self, target, draft, draft_tokens, uniforms, temperature=None,
                greedy=False, dtype="f32", threads=1, diagnostics=True):
@@ -154,6 +156,24 @@ class Oracle:
         return probs, m.value, S.value
 
 
+    def kv_commit(self, scratch, cache, cache_len, num_accepted):
+        """Append each sequence's accepted draft KV rows to its cache.
+
+        scratch: uint8 [P, B, N, row_bytes], cache: uint8 [P, B, max_len,
+        row_bytes], cache_len: int [B], num_accepted: int [B].  Works on
+        copies; returns (cache, cache_len, status bits)."""
+        s = np.ascontiguousarray(_np(scratch, np.uint8))
+        c = np.array(_np(cache, np.uint8), copy=True, order="C")
+        ln = np.array(_np(cache_len, np.int32), copy=True)
+        a = _np(num_accepted, np.int32)
+        P, B, N, row = s.shape
+        assert c.shape[:2] == (P, B) and c.shape[3] == row, (c.shape, s.shape)
+        assert ln.shape == (B,) and a.shape == (B,)
+        st = self.lib.orc_kv_commit(s.ctypes.data, c.ctypes.data, ln.ctypes.data, a.ctypes.data,
+                                    P, B, N, c.shape[2], row)
+        return c, ln, int(st)
+
+
 _default: Oracle | None = None
 
 
@@ -166,3 +186,7 @@ def default() -> Oracle:
 
 def verify(*args, **kwargs):
     return default().verify(*args, **kwargs)
+
+
+def kv_commit(*args, **kwargs):
+    return default().kv_commit(*args, **kwargs)

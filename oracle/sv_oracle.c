@@ -433,3 +433,53 @@ int orc_softmax_row(const void *row, int dtype, int V, double T, double *probs,
     *S_out = S;
     return 0;
 }
+
+/*
+ * KV-cache commit after a verify step, following the same lesson's section
+ * "KV cache dance": the verifier's forward over the N drafts writes their N
+ * KV entries into a scratch buffer; once the verify step has fixed how many
+ * drafts were accepted, the first num_accepted of those entries are appended
+ * to the cache and the rest are dropped (the rollback).  Exercise 4 of the
+ * lesson states the check: a 10-token prefix, 5 drafts, a rejection at the
+ * third draft, and the cache then reads prefix + the first 2 drafts.
+ *
+ * Layout (bytes, row-major): scratch [P][B][N][row_bytes], cache
+ * [P][B][max_len][row_bytes]; P planes (for example K and V of every layer)
+ * share one length per sequence, cache_len[b].  Per sequence b:
+ *   a = num_accepted[b]
+ *   a < 0 (an invalid verify):          nothing is committed
+ *   a > N:                              nothing; status |= 2
+ *   cache_len[b] < 0 or
+ *   cache_len[b] + a > max_len:         nothing; status |= 1
+ *   otherwise, for every plane p and k < a:
+ *       cache[p][b][cache_len[b] + k] = scratch[p][b][k];  cache_len[b] += a
+ * Returns the status bits.
+ */
+int orc_kv_commit(const unsigned char *scratch, unsigned char *cache, int32_t *cache_len,
+                  const int32_t *num_accepted, int P, int B, int N, int max_len,
+                  size_t row_bytes)
+{
+    int status = 0;
+    for (int b = 0; b < B; ++b) {
+        const int a = num_accepted[b];
+        if (a < 0)
+            continue;
+        if (a > N) {
+            status |= 2;
+            continue;
+        }
+        const int len = cache_len[b];
+        if (len < 0 || (long long)len + a > max_len) {
+            status |= 1;
+            continue;
+        }
+        for (int p = 0; p < P; ++p)
+            for (int k = 0; k < a; ++k) {
+                const size_t src = (((size_t)p * B + b) * N + k) * row_bytes;
+                const size_t dst = (((size_t)p * B + b) * max_len + len + k) * row_bytes;
+                memcpy(cache + dst, scratch + src, row_bytes);
+            }
+        cache_len[b] = len + a;
+    }
+    return status;
+}

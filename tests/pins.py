@@ -450,6 +450,137 @@ def pin_storage_types(orc):
         assert np.array_equal(r["q_at_d"], r64["q_at_d"])
 
 
+# ---- KV-cache commit / rollback ---------------------------------------------
+
+def _kv_row(plane, pos, tok, row_bytes):
+    """Bytes that identify (plane, position, token): a stand-in KV entry."""
+    r = (np.arange(row_bytes, dtype=np.int64) * 7 + plane * 31 + pos * 13 + tok * 3) % 251
+    r[:4] = (plane, pos, tok & 0xFF, (tok >> 8) & 0xFF)
+    return r.astype(np.uint8)
+
+
+def _kv_state(tokens_per_seq, P, max_len, row_bytes, fill=0xEE):
+    cache = np.full((P, len(tokens_per_seq), max_len, row_bytes), fill, np.uint8)
+    for b, toks in enumerate(tokens_per_seq):
+        for p in range(P):
+            for pos, t in enumerate(toks):
+                cache[p, b, pos] = _kv_row(p, pos, t, row_bytes)
+    return cache
+
+
+def _kv_scratch(drafts_per_seq, starts, P, N, row_bytes):
+    s = np.zeros((P, len(drafts_per_seq), N, row_bytes), np.uint8)
+    for b, (ds, L) in enumerate(zip(drafts_per_seq, starts)):
+        for p in range(P):
+            for k, t in enumerate(ds):
+                s[p, b, k] = _kv_row(p, L + k, t, row_bytes)
+    return s
+
+
+def _rejection_at(orc, N, reject_1based, V=8):
+    """num_accepted from the verify oracle for drafts whose first
+    reject_1based - 1 positions have p == q (ratio 1: always accepted) and
+    whose next position has disjoint one-hot p and q (ratio 0: always
+    rejected), whatever the uniforms."""
+    rng = np.random.default_rng(0)
+    zq = rng.normal(0, 1, (1, N + 1, V))
+    zp = zq[:, :N].copy()
+    j = reject_1based - 1
+    zq[0, j] = NEG_INF
+    zq[0, j, 1] = 0.0
+    zp[0, j] = NEG_INF
+    zp[0, j, 2] = 0.0
+    d = np.zeros((1, N), np.int32)
+    for i in range(N):
+        d[0, i] = int(np.argmax(zp[0, i]))
+    u = np.full((1, N + 1), 0.999, np.float32)
+    r = orc.verify(zq, zp, d, u, np.ones(1), dtype="f64")
+    return int(r["num_accepted"][0]), d[0]
+
+
+def pin_kv_exercise_rollback(orc):
+    """The lesson's rollback exercise: prefix 10, 5 drafts, rejection at the
+    third draft; the cache then reads prefix + the first 2 drafts."""
+    g = golden()
+    L0 = int(g["kv_rollback.prefix"][0])
+    N = int(g["kv_rollback.drafts"][0])
+    rej = int(g["kv_rollback.rejected_draft_1based"][0])
+    want_acc = int(g["kv_rollback.accepted"][0])
+    acc, _ = _rejection_at(orc, N, rej)
+    assert acc == want_acc, (acc, want_acc)
+    P, row, max_len = 4, 32, 24
+    rng = np.random.default_rng(1)
+    prefixes = [list(rng.integers(0, 50000, L0)) for _ in range(3)]
+    drafts = [list(rng.integers(0, 50000, N)) for _ in range(3)]
+    cache = _kv_state(prefixes, P, max_len, row)
+    scratch = _kv_scratch(drafts, [L0] * 3, P, N, row)
+    nacc = np.array([acc, N, 0], np.int32)
+    c2, ln, st = orc.kv_commit(scratch, cache, np.full(3, L0, np.int32), nacc)
+    assert st == 0
+    assert list(ln) == [L0 + acc, L0 + N, L0]
+    for b in range(3):
+        seq = prefixes[b] + drafts[b][: nacc[b]]
+        assert np.array_equal(c2[:, b, : ln[b]], _kv_state([seq], P, ln[b], row)[:, 0])
+        # the rolled-back drafts never reach the cache
+        assert (c2[:, b, ln[b]:] == 0xEE).all()
+    # next iteration: three more entries land right after the committed ones
+    more = [list(rng.integers(0, 50000, N)) for _ in range(3)]
+    scratch2 = _kv_scratch(more, list(ln), P, N, row)
+    c3, ln3, st = orc.kv_commit(scratch2, c2, ln, np.array([3, 1, 5], np.int32))
+    assert st == 0 and list(ln3) == [L0 + acc + 3, L0 + N + 1, L0 + 5]
+    for b, k in enumerate([3, 1, 5]):
+        seq = prefixes[b] + drafts[b][: nacc[b]] + more[b][:k]
+        assert np.array_equal(c3[:, b, : ln3[b]], _kv_state([seq], P, ln3[b], row)[:, 0])
+
+
+def pin_kv_bad_counts_and_overflow(orc):
+    P, B, N, row, max_len = 2, 6, 4, 16, 12
+    rng = np.random.default_rng(2)
+    cache = rng.integers(0, 256, (P, B, max_len, row), dtype=np.uint8)
+    scratch = rng.integers(0, 256, (P, B, N, row), dtype=np.uint8)
+    lens = np.array([3, 3, 10, 8, -1, 5], np.int32)
+    nacc = np.array([-1, N + 1, 3, 4, 0, 2], np.int32)
+    c2, ln, st = orc.kv_commit(scratch, cache, lens, nacc)
+    assert st == (1 | 2), st
+    # -1: an invalid verify commits nothing and is not an error here
+    # N+1: a count the verify cannot produce; 10+3 > 12: overflow; -1 length: bad
+    for b in (0, 1, 2, 4):
+        assert ln[b] == lens[b] and np.array_equal(c2[:, b], cache[:, b])
+    # exactly filling the cache is fine; the others still commit
+    assert ln[3] == 12 and np.array_equal(c2[:, 3, 8:12], scratch[:, 3, :4])
+    assert ln[5] == 7 and np.array_equal(c2[:, 5, 5:7], scratch[:, 5, :2])
+    assert np.array_equal(c2[:, 5, :5], cache[:, 5, :5]) and np.array_equal(c2[:, 5, 7:], cache[:, 5, 7:])
+    _, _, st = orc.kv_commit(scratch[:, :1], cache[:, :1], np.array([0], np.int32), np.array([N], np.int32))
+    assert st == 0
+
+
+def pin_kv_planes_and_sequences_stay_apart(orc):
+    """Every plane gets its own rows at the sequence's shared length; nothing
+    outside [len, len + a) moves (random bytes, several layouts)."""
+    rng = np.random.default_rng(3)
+    for P, B, N, row, max_len in [(1, 1, 1, 16, 1), (3, 5, 7, 48, 20), (6, 2, 3, 1024, 9)]:
+        cache = rng.integers(0, 256, (P, B, max_len, row), dtype=np.uint8)
+        scratch = rng.integers(0, 256, (P, B, N, row), dtype=np.uint8)
+        nacc = rng.integers(0, N + 1, B).astype(np.int32)
+        lens = np.array([rng.integers(0, max_len - a + 1) for a in nacc], np.int32)
+        c2, ln, st = orc.kv_commit(scratch, cache, lens, nacc)
+        assert st == 0 and np.array_equal(ln, lens + nacc)
+        for p in range(P):
+            for b in range(B):
+                L, a = lens[b], nacc[b]
+                assert np.array_equal(c2[p, b, L:L + a], scratch[p, b, :a])
+                assert np.array_equal(c2[p, b, :L], cache[p, b, :L])
+                assert np.array_equal(c2[p, b, L + a:], cache[p, b, L + a:])
+    # no sequences, no drafts
+    c2, ln, st = orc.kv_commit(np.zeros((2, 0, 3, 16), np.uint8), np.zeros((2, 0, 4, 16), np.uint8),
+                               np.zeros(0, np.int32), np.zeros(0, np.int32))
+    assert st == 0 and ln.size == 0
+    cache = rng.integers(0, 256, (2, 2, 4, 16), dtype=np.uint8)
+    c2, ln, st = orc.kv_commit(np.zeros((2, 2, 0, 16), np.uint8), cache, np.array([1, 4], np.int32),
+                               np.zeros(2, np.int32))
+    assert st == 0 and list(ln) == [1, 4] and np.array_equal(c2, cache)
+
+
 ALL_PINS = [
     pin_softmax_matches_scipy,
     pin_exact_law_small,
@@ -473,4 +604,7 @@ ALL_PINS = [
     pin_invalid_inputs,
     pin_degenerate_sizes,
     pin_storage_types,
+    pin_kv_exercise_rollback,
+    pin_kv_bad_counts_and_overflow,
+    pin_kv_planes_and_sequences_stay_apart,
 ]

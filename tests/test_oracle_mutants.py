@@ -50,6 +50,15 @@ MUTANTS = [
     ("invalid rows not detected", "if (isnan(z) || z == INFINITY)\n            return 0;",
      "if (0)\n            return 0;"),
     ("bad draft tokens not detected", "if (d < 0 || d >= V)", "if (d < 0 || d > V)"),
+    ("kv commits one row too many", "for (int k = 0; k < a; ++k) {", "for (int k = 0; k <= a && k < N; ++k) {"),
+    ("kv destination ignores the cache length",
+     "* max_len + len + k) * row_bytes;", "* max_len + k) * row_bytes;"),
+    ("kv length not advanced", "cache_len[b] = len + a;", "cache_len[b] = len;"),
+    ("kv overflow check off by one", "(long long)len + a > max_len", "(long long)len + a >= max_len"),
+    ("kv plane and sequence transposed in the scratch",
+     "src = (((size_t)p * B + b) * N + k) * row_bytes;", "src = (((size_t)b * P + p) * N + k) * row_bytes;"),
+    ("kv bad count not reported", "if (a > N) {", "if (a > N + 1) {"),
+    ("kv invalid verify commits", "if (a < 0)\n            continue;", "if (a < -1)\n            continue;"),
 ]
 
 
