@@ -231,6 +231,49 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# KV layout of the commit measurement: a 7B-class model with grouped-query
+# attention, 28 layers x {K, V} planes, 4 KV heads x 128 bf16 per token entry
+KV_PLANES, KV_HEADS, KV_DIM, KV_MAX_LEN = 56, 4, 128, 2048
+
+
+def measure_kv_commit(sv, torch, dev, stream, nacc, N, reps=50):
+    """Times spec_verify_kv_commit for the batch's accepted counts: L2 is
+    flushed (a 256 MiB write) and the lengths restored before each call; each
+    call is bracketed by CUDA events on the launching stream."""
+    B = nacc.shape[0]
+    gen = torch.Generator(device=dev).manual_seed(11)
+    scratch = torch.randn((KV_PLANES, B, N, KV_HEADS, KV_DIM), generator=gen, device=dev).to(torch.bfloat16)
+    cache = torch.empty((KV_PLANES, B, KV_MAX_LEN, KV_HEADS, KV_DIM), dtype=torch.bfloat16, device=dev)
+    lens0 = torch.randint(0, KV_MAX_LEN - N + 1, (B,), generator=gen, device=dev, dtype=torch.int32)
+    lens = lens0.clone()
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    row_bytes = KV_HEADS * KV_DIM * 2
+    a = nacc.cpu().clamp(min=0)
+    moved = 2 * int(a.sum()) * KV_PLANES * row_bytes  # each committed row read once, written once
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for k in range(reps + 3):
+        lens.copy_(lens0)
+        flush.zero_()
+        if k >= 3:
+            evs[k - 3][0].record(stream)
+        sv.kv_commit(scratch, cache, lens, nacc, status=status, stream=stream)
+        if k >= 3:
+            evs[k - 3][1].record(stream)
+    torch.cuda.synchronize(dev)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"kv commit status {int(status.item())}")
+    us = statistics.median(1e3 * e0.elapsed_time(e1) for e0, e1 in evs)
+    gbs = moved / (us * 1e-6) / 1e9
+    peak, peak_kind = peaks()
+    del cache, scratch, flush
+    return {"us_per_call": us, "bytes_moved": moved, "gbs": gbs, "frac": gbs / peak,
+            "peak": peak, "peak_kind": f"{peak_kind} (burst copy)", "launches_per_call": 2,
+            "layout": f"{KV_PLANES} planes (28 layers x K,V) x B={B} x N={N} scratch rows -> cache of "
+                      f"{KV_MAX_LEN} positions, {row_bytes} B rows ({KV_HEADS} KV heads x {KV_DIM} bf16)",
+            "accepted_rows": int(a.sum()), "timing": f"median of {reps} calls, L2 flushed before each"}
+
+
 def run_ours(args):
     import torch
     world, rank, local, pg = dist_init(args)
@@ -308,8 +351,10 @@ def run_ours(args):
     kernels = {
         "sv_rows_kernel": {"us_per_launch": rows_us, "share": ms_rows / (ms_rows + ms_sample),
                            "algorithmic_bytes": w.logit_bytes, "gbs": rows_gbs},
-        "sv_sample_kernel": {"us_per_launch": sample_us, "share": ms_sample / (ms_rows + ms_sample),
-                             "note": "re-reads one row pair per sequence (not counted in the metric)"},
+        "sv_mass_kernel+sv_pick_kernel": {
+            "us_per_launch": sample_us, "share": ms_sample / (ms_rows + ms_sample),
+            "note": "residual sampling; re-reads the rejected row pair of each sampled sequence "
+                    "(not counted in the metric)"},
     }
 
     # end to end through the C ABI: pinned host inputs copied in, outputs read back
@@ -347,6 +392,21 @@ def run_ours(args):
         e2e = {"value": job_rate(rows, world, k2, ems), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": k2}
 
+    # acceptance telemetry kept by the library over every run so far
+    counts = ctx.acceptance_counts()
+    runs = sum(counts)
+    acc = None
+    if runs:
+        mean = sum(k * c for k, c in enumerate(counts[: w.N + 1])) / runs
+        acc = {"runs_x_sequences": runs, "invalid": counts[w.N + 1], "mean_accepted": mean,
+               "mean_tokens_per_call": mean + 1,
+               "position_accept_rate": [sum(counts[i + 1: w.N + 1]) / max(1, sum(counts[i: w.N + 1]))
+                                        for i in range(w.N)]}
+
+    kv = None
+    if not args.no_kv:
+        kv = measure_kv_commit(sv, torch, dev, stream, nacc, w.N)
+
     cpu = None
     if rank == 0 and not args.no_cpu:
         rate, n, dt = cpu_oracle_rate(w, args.cpu_budget, os.cpu_count() or 1)
@@ -370,9 +430,11 @@ def run_ours(args):
                      "unit": "GB/s", "frac": rows_gbs / peak, "peak_kind": f"{peak_kind} (burst copy)",
                      "traffic": committed_traffic(w.name), "step_gbs": gbs, "step_frac": gbs / peak},
         "kernels": kernels,
+        "acceptance": acc,
+        "kv_commit": kv,
         "e2e": e2e,
         "cpu_baseline": cpu,
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": 3 * args.steps,  # rows, mass and pick kernels per verify call
         "clocks": clk.summary(),
         "check": check,
     }
@@ -393,6 +455,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-check", action="store_true")
+    ap.add_argument("--no-kv", action="store_true", help="skip the KV-cache commit measurement")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-budget", type=float, default=8.0, help="seconds of oracle work per reference step")
     args = ap.parse_args()

@@ -59,10 +59,11 @@ typedef enum { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
 /*
  * Create a context on `device` for batches of up to max_B sequences with up
  * to max_N draft tokens over a vocabulary of V tokens stored as `dtype`.
- * Allocates a workspace of about 8*max_B + 20*max_B*(max_N+1) +
+ * Allocates a workspace of about 8*(max_N+2) + 8*max_B + 20*max_B*(max_N+1) +
  * 32*max_B*ceil(V*elt/4 KiB) bytes (per-sequence first-rejection slots and
  * error flags; per-position argmax and row statistics; per-slice residual
- * masses) and one status word; nothing else is allocated later.
+ * masses, the acceptance counters) and one status word; nothing else is
+ * allocated later.
  * Requires V >= 1 and V*sizeof(dtype) a multiple of 16 (V % 8 == 0 for bf16,
  * V % 4 == 0 for f32).  Returns SV_ERR_SHAPE otherwise, SV_ERR_OOM if the
  * workspace cannot be allocated, SV_ERR_CUDA if the device cannot be used.
@@ -121,6 +122,16 @@ sv_status spec_verify_run_debug(spec_verify_ctx *ctx, const void *target_logits,
  * read fails.
  */
 sv_status spec_verify_get_status(spec_verify_ctx *ctx);
+
+/*
+ * Acceptance telemetry (how many drafts each verify accepted, the quantity
+ * the pages tell users to watch: mean accepted length and acceptance rate).
+ * Every run adds each sequence to counts[k], k = its num_accepted (0..N), or
+ * to counts[max_N + 1] when it was invalid.  Copies the max_N + 2 counters
+ * into `counts` (ncounts >= max_N + 2; further entries are zeroed), after
+ * synchronising the device; reset != 0 then clears them.
+ */
+sv_status spec_verify_acceptance_counts(spec_verify_ctx *ctx, uint64_t *counts, int ncounts, int reset);
 
 /*
  * Cluster size used by the next runs: the number of CTAs (1..16) that share
@@ -182,6 +193,47 @@ sv_status spec_verify_run_noalloc(const void *target_logits, const void *draft_l
                                   const float *temperature, int greedy, int B, int N, int V,
                                   sv_dtype dtype, int32_t *out_tokens, int32_t *num_accepted,
                                   void *stream);
+
+/*
+ * KV-cache commit and rollback after a verify step: "Speculative decoding --
+ * draft, verify, repeat" (factory.pai-world.com, lesson 07-16), section "KV
+ * cache dance" and its exercise 4.  The verifier's forward over the N drafts
+ * wrote their KV entries to a scratch buffer; this appends each sequence's
+ * first num_accepted[b] entries to its cache and advances cache_len[b], so
+ * the next iteration reads the prefix plus the accepted drafts.  The rejected
+ * entries are never copied (the rollback).
+ *
+ * Layout (device memory, caller-owned, byte rows of any content):
+ *   scratch   [planes][B][N][row_bytes]        may be NULL when N == 0
+ *   cache     [planes][B][max_len][row_bytes]  rows cache_len[b] .. + a - 1 written
+ *   cache_len int32 [B], read and advanced in place
+ *   num_accepted int32 [B], as written by spec_verify_run (-1 = invalid sequence)
+ * A plane is any slab that shares the sequence's length, e.g. the K or the V
+ * half of one layer; row_bytes is one token's entry in one plane.
+ *
+ * Per sequence: num_accepted < 0 commits nothing; num_accepted > N commits
+ * nothing and sets SV_KV_BAD_COUNT; cache_len < 0 or cache_len + num_accepted
+ * > max_len commits nothing and sets SV_KV_OVERFLOW.  The bits are OR-ed into
+ * *status (device int32, may be NULL); the caller clears it.  SV_KV_TIMEOUT
+ * reports a copy that did not finish within 2 s (nothing is stored then).
+ *
+ * Host errors: SV_ERR_INVALID_ARG for negative sizes, planes < 1,
+ * row_bytes == 0 or not a multiple of 16, a NULL pointer that is needed, or
+ * scratch / cache not 16-byte aligned; SV_ERR_TOO_LARGE when the byte offsets
+ * would pass 2^62; SV_ERR_CUDA when a launch fails.  Asynchronous on
+ * `stream` (cudaStream_t, NULL = legacy default stream), on the current
+ * device; allocates nothing; two kernel launches (one when N == 0), ordered
+ * after the work already on the stream.
+ */
+enum {
+    SV_KV_OVERFLOW = 1,   /* cache_len + num_accepted > max_len, or cache_len < 0 */
+    SV_KV_BAD_COUNT = 2,  /* num_accepted > N */
+    SV_KV_TIMEOUT = 4     /* a staging copy did not complete */
+};
+
+sv_status spec_verify_kv_commit(const void *scratch, void *cache, int32_t *cache_len,
+                                const int32_t *num_accepted, int32_t *status, int planes, int B,
+                                int N, int max_len, size_t row_bytes, void *stream);
 
 #ifdef __cplusplus
 }

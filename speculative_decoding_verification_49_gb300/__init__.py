@@ -10,6 +10,7 @@ Python or CPU fallback, and importing a missing library raises.
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 
 from .build import LIBRARY
@@ -43,9 +44,15 @@ _SIGNATURES = [
     ("spec_verify_destroy", None, [_P]),
     ("spec_verify_run_noalloc", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
     ("spec_verify_profile", _I, [_P, _I]),
+    ("spec_verify_acceptance_counts", _I, [_P, ctypes.POINTER(ctypes.c_uint64), _I, _I]),
     ("spec_verify_profile_read", _I, [_P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double),
                                       ctypes.POINTER(_I)]),
+    ("spec_verify_kv_commit", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, ctypes.c_size_t, _P]),
 ]
+
+SV_KV_OVERFLOW = 1
+SV_KV_BAD_COUNT = 2
+SV_KV_TIMEOUT = 4
 
 _lib = None
 
@@ -130,6 +137,14 @@ def spec_verify_run_noalloc(target, draft, draft_tokens, uniforms, temperature, 
                                           int(greedy), B, N, V, dtype, out_tokens, num_accepted, stream)
 
 
+def spec_verify_acceptance_counts(ctx, ncounts: int, reset: bool = False):
+    """(status, counts): counts[k] sequences that accepted k drafts, the last
+    entry invalid sequences."""
+    arr = (ctypes.c_uint64 * ncounts)()
+    st = load().spec_verify_acceptance_counts(ctx, arr, ncounts, int(bool(reset)))
+    return st, list(arr)
+
+
 def spec_verify_profile(ctx, enable: bool) -> int:
     return load().spec_verify_profile(ctx, int(bool(enable)))
 
@@ -139,6 +154,14 @@ def spec_verify_profile_read(ctx):
     a, b, n = ctypes.c_double(), ctypes.c_double(), _I()
     st = load().spec_verify_profile_read(ctx, ctypes.byref(a), ctypes.byref(b), ctypes.byref(n))
     return st, a.value, b.value, n.value
+
+
+def spec_verify_kv_commit(scratch, cache, cache_len, num_accepted, status, planes, B, N, max_len, row_bytes,
+                          stream) -> int:
+    """Append each sequence's first num_accepted scratch KV rows to its cache
+    and advance cache_len (device pointers; asynchronous on stream)."""
+    return load().spec_verify_kv_commit(scratch, cache, cache_len, num_accepted, status, planes, B, N,
+                                        max_len, row_bytes, stream)
 
 
 # ---- torch convenience wrapper -------------------------------------------------
@@ -181,6 +204,14 @@ class SpecVerify:
 
     def status(self) -> int:
         return spec_verify_get_status(self.ctx)
+
+    def acceptance_counts(self, reset: bool = False):
+        """counts[k] = sequences that accepted k drafts (k = 0..max_N) since the
+        last reset; counts[max_N + 1] = invalid sequences."""
+        st, counts = spec_verify_acceptance_counts(self.ctx, self.max_N + 2, reset)
+        if st != SV_OK:
+            raise SpecVerifyError(st, "spec_verify_acceptance_counts")
+        return counts
 
     def profile(self, enable: bool):
         st = spec_verify_profile(self.ctx, enable)
@@ -243,3 +274,30 @@ class SpecVerify:
             "target_row_stats": torch.full((B, N + 1, 2), float("nan"), device=device),
             "draft_row_stats": torch.full((B, N, 2), float("nan"), device=device),
         }
+
+
+def kv_commit(scratch, cache, cache_len, num_accepted, status=None, stream=None):
+    """Torch front end of spec_verify_kv_commit.
+
+    scratch [P, B, N, *row] and cache [P, B, max_len, *row] are contiguous
+    CUDA tensors of one dtype (a row is one token's entry in one plane, e.g.
+    [kv_heads, head_dim]); cache_len and num_accepted are int32 [B]; status is
+    an optional int32 [1] that collects SV_KV_* bits.  Enqueues on the
+    current torch stream (or ``stream``) and does not synchronise."""
+    import torch
+    if scratch.dtype != cache.dtype or scratch.shape[:2] != cache.shape[:2] or scratch.shape[3:] != cache.shape[3:]:
+        raise ValueError(f"scratch {tuple(scratch.shape)} and cache {tuple(cache.shape)} do not match")
+    for name, t in (("scratch", scratch), ("cache", cache)):
+        if not t.is_cuda or not t.is_contiguous() or t.dim() < 3:
+            raise ValueError(f"{name} must be a contiguous CUDA tensor [P, B, rows, ...]")
+    P, B, N = scratch.shape[:3]
+    max_len = cache.shape[2]
+    for name, t in (("cache_len", cache_len), ("num_accepted", num_accepted)):
+        if t.dtype != torch.int32 or t.shape != (B,) or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous int32 CUDA tensor of shape ({B},)")
+    row_bytes = math.prod(cache.shape[3:]) * cache.element_size()
+    s = stream if stream is not None else torch.cuda.current_stream(cache.device)
+    st = spec_verify_kv_commit(_ptr(scratch) if N else None, _ptr(cache), _ptr(cache_len), _ptr(num_accepted),
+                               _ptr(status), P, B, N, max_len, row_bytes, s.cuda_stream)
+    if st != SV_OK:
+        raise SpecVerifyError(st, "spec_verify_kv_commit")

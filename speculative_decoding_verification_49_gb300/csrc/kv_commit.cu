@@ -1,0 +1,219 @@
+// kv_commit.cu -- KV-cache commit/rollback after a verify step, for sm_103a.
+//
+// "Speculative decoding -- draft, verify, repeat" (factory.pai-world.com,
+// lesson 07-16), section "KV cache dance": the verifier's forward over the N
+// drafts writes their N KV entries into a scratch buffer; once the verify step
+// has fixed num_accepted, the first num_accepted entries are appended to the
+// cache and the others are dropped.  The lesson's exercise 4 states the check
+// (prefix + the accepted drafts is what the next iteration reads).
+//
+// The work is a plain byte copy: per (plane, sequence) segment, the first
+// a*row_bytes bytes of its scratch rows go to the cache at row cache_len[b].
+// Two kernels, both stream-ordered after whatever produced num_accepted:
+//   sv_kv_copy_kernel  one warp per CTA; each lane owns one segment (or, for
+//                      segments longer than a chunk, lane 0 owns one chunk of
+//                      one segment) and moves it with a TMA bulk load into
+//                      shared memory and a TMA bulk store out of it;
+//   sv_kv_len_kernel   advances cache_len and reports bad counts / overflow.
+// The length update needs its own launch: every copying CTA reads cache_len.
+#include <climits>
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "spec_verify.h"
+#include "sv_device.cuh"
+
+namespace {
+
+using namespace sv;
+
+constexpr int kKvThreads = 32;
+constexpr uint32_t kKvChunk = 32u * 1024u;     // staging bytes per CTA (dynamic shared memory)
+constexpr uint64_t kKvWaitNs = 2000000000ull;  // give up on a bulk load after 2 s
+constexpr int kKvLenThreads = 256;
+
+struct KvParams {
+    const unsigned char *scratch;  // [P][B][N][row_bytes]
+    unsigned char *cache;          // [P][B][max_len][row_bytes]
+    int32_t *cache_len;            // [B]
+    const int32_t *nacc;           // [B]
+    int32_t *status;               // error bits, may be null
+    int P, B, N, max_len;
+    unsigned long long row_bytes;
+    unsigned long long seg_bytes;  // N * row_bytes: one sequence's scratch rows in one plane
+    int group;                     // segments per CTA (1 when a segment spans several chunks)
+    int nchunk;                    // chunks per segment (1 when group > 1)
+};
+
+// Rows of a sequence to commit, and the error bits its counts raise.
+__device__ __forceinline__ int kv_rows(int a, int len, int N, int max_len, int &bits)
+{
+    bits = 0;
+    if (a < 0)  // the verify step flagged the sequence invalid: nothing to commit
+        return 0;
+    if (a > N) {
+        bits = SV_KV_BAD_COUNT;
+        return 0;
+    }
+    if (len < 0 || (long long)len + a > max_len) {
+        bits = SV_KV_OVERFLOW;
+        return 0;
+    }
+    return a;
+}
+
+__global__ void __launch_bounds__(kKvThreads) sv_kv_copy_kernel(KvParams k)
+{
+    extern __shared__ __align__(128) unsigned char kv_stage[];
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int no_abort;
+
+    grid_dependency_wait();
+    const int lane = threadIdx.x;
+    const long long unit = blockIdx.x;
+    const long long seg = (unit / k.nchunk) * k.group + lane;
+    const unsigned long long off = (unsigned long long)(unit % k.nchunk) * kKvChunk;
+    const long long nseg = (long long)k.P * k.B;
+
+    uint32_t bytes = 0;
+    const unsigned char *src = nullptr;
+    unsigned char *dst = nullptr;
+    if (lane < k.group && seg < nseg) {
+        const int b = (int)(seg % k.B);
+        const int len = __ldg(&k.cache_len[b]);
+        int bits;
+        const int rows = kv_rows(__ldg(&k.nacc[b]), len, k.N, k.max_len, bits);
+        const unsigned long long total = (unsigned long long)rows * k.row_bytes;
+        if (total > off) {
+            const unsigned long long n = total - off;
+            bytes = (uint32_t)(n < kKvChunk ? n : kKvChunk);
+            src = k.scratch + (unsigned long long)seg * k.seg_bytes + off;
+            dst = k.cache + ((unsigned long long)seg * k.max_len + len) * k.row_bytes + off;
+        }
+    }
+    const uint32_t total = __reduce_add_sync(0xffffffffu, bytes);
+    if (total == 0)
+        return;
+
+    if (lane == 0) {
+        no_abort = 0;
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(&bar, total);
+    }
+    __syncwarp();
+    unsigned char *slot = kv_stage + (k.group > 1 ? (size_t)lane * k.seg_bytes : 0);
+    if (bytes)
+        bulk_g2s(slot, src, bytes, &bar);
+    if (!mbar_wait_bounded(&bar, 0, &no_abort, kKvWaitNs)) {
+        if (k.status)
+            atomicOr(k.status, SV_KV_TIMEOUT);
+        mbar_wait_bounded(&bar, 0, &no_abort, kKvWaitNs);  // let the loads in flight land
+        return;
+    }
+    if (bytes) {
+        bulk_s2g(dst, slot, bytes);
+        bulk_commit();
+        bulk_wait_read_all();  // the stage must outlive the store's reads
+    }
+}
+
+__global__ void __launch_bounds__(kKvLenThreads) sv_kv_len_kernel(KvParams k)
+{
+    grid_dependency_wait();  // every copy of this commit has read cache_len
+    const int b = blockIdx.x * kKvLenThreads + threadIdx.x;
+    if (b >= k.B)
+        return;
+    const int len = k.cache_len[b];
+    int bits;
+    const int rows = kv_rows(k.nacc[b], len, k.N, k.max_len, bits);
+    if (bits) {
+        if (k.status)
+            atomicOr(k.status, bits);
+        return;
+    }
+    k.cache_len[b] = len + rows;
+}
+
+cudaLaunchConfig_t kv_launch(unsigned grid, unsigned block, size_t smem, cudaStream_t stream,
+                             cudaLaunchAttribute *attr)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
+}
+
+bool aligned16(const void *p)
+{
+    return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+} // namespace
+
+extern "C" sv_status spec_verify_kv_commit(const void *scratch, void *cache, int32_t *cache_len,
+                                           const int32_t *num_accepted, int32_t *status, int planes,
+                                           int B, int N, int max_len, size_t row_bytes, void *stream)
+{
+    if (B < 0 || N < 0 || planes < 1 || max_len < 0 || row_bytes == 0 || row_bytes % 16 != 0)
+        return SV_ERR_INVALID_ARG;
+    if (B == 0)
+        return SV_OK;
+    if (!cache_len || !num_accepted || (N > 0 && (!scratch || !cache)))
+        return SV_ERR_INVALID_ARG;
+    if (!aligned16(scratch) || !aligned16(cache))
+        return SV_ERR_INVALID_ARG;
+    // every byte offset the kernels form must fit in 62 bits
+    const unsigned long long rows_max = (unsigned long long)(max_len > N ? max_len : N);
+    const unsigned long long segs = (unsigned long long)planes * (unsigned long long)B;
+    if (rows_max > 0 && row_bytes > (1ull << 62) / rows_max / segs)
+        return SV_ERR_TOO_LARGE;
+
+    KvParams k;
+    k.scratch = static_cast<const unsigned char *>(scratch);
+    k.cache = static_cast<unsigned char *>(cache);
+    k.cache_len = cache_len;
+    k.nacc = num_accepted;
+    k.status = status;
+    k.P = planes;
+    k.B = B;
+    k.N = N;
+    k.max_len = max_len;
+    k.row_bytes = row_bytes;
+    k.seg_bytes = (unsigned long long)N * row_bytes;
+    if (k.seg_bytes <= kKvChunk && k.seg_bytes > 0) {
+        const unsigned long long g = kKvChunk / k.seg_bytes;
+        k.group = (int)(g < (unsigned long long)kKvThreads ? g : kKvThreads);
+        k.nchunk = 1;
+    } else {
+        k.group = 1;
+        k.nchunk = (int)((k.seg_bytes + kKvChunk - 1) / kKvChunk);  // < 2^31 by the check above
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    if (N > 0 && max_len > 0) {
+        const unsigned long long units = (segs + k.group - 1) / k.group * (unsigned long long)k.nchunk;
+        if (units > (unsigned long long)INT_MAX)
+            return SV_ERR_TOO_LARGE;
+        cudaLaunchConfig_t cfg = kv_launch((unsigned)units, kKvThreads, kKvChunk, st, attr);
+        if (cudaLaunchKernelEx(&cfg, sv_kv_copy_kernel, k) != cudaSuccess) {
+            cudaGetLastError();
+            return SV_ERR_CUDA;
+        }
+    }
+    cudaLaunchConfig_t cfg = kv_launch((unsigned)((B + kKvLenThreads - 1) / kKvLenThreads), kKvLenThreads, 0, st,
+                                       attr);
+    if (cudaLaunchKernelEx(&cfg, sv_kv_len_kernel, k) != cudaSuccess) {
+        cudaGetLastError();
+        return SV_ERR_CUDA;
+    }
+    return SV_OK;
+}

@@ -84,6 +84,8 @@ struct SvParams {
     float *ws_stats;  // [max_B*(max_N+1)][4] (mq, Sq, mp, Sp) of each position
     float *ws_slice;  // [max_B*slices][8] residual mass of each warp's share of a slice
     int *status;      // sticky error bits of the context
+    unsigned long long *hist;          // [N+1] sequences by accepted drafts (may be NULL)
+    unsigned long long *hist_invalid;  // sequences that were invalid
     int B, N, V, greedy;
 };
 
@@ -1027,6 +1029,8 @@ __global__ void __launch_bounds__(kPickThreads) sv_pick_kernel(const SvParams p)
                     out[k] = -1;
                 p.nacc[b] = -1;
                 atomicOr(p.status, err);
+                if (p.hist)
+                    atomicAdd(p.hist_invalid, 1ull);
             } else {  // greedy: the argmax at j
                 for (int k = 0; k < j; ++k)
                     out[k] = p.tokens[(size_t)b * N + k];
@@ -1034,6 +1038,8 @@ __global__ void __launch_bounds__(kPickThreads) sv_pick_kernel(const SvParams p)
                 for (int k = j + 1; k <= N; ++k)
                     out[k] = -1;
                 p.nacc[b] = j;
+                if (p.hist)
+                    atomicAdd(&p.hist[j], 1ull);
             }
             p.ws_first[b] = kNoReject;
             p.ws_err[b] = 0;
@@ -1213,6 +1219,8 @@ __global__ void __launch_bounds__(kPickThreads) sv_pick_kernel(const SvParams p)
         for (int k = j + 1; k <= N; ++k)
             out[k] = -1;
         p.nacc[b] = j;
+        if (p.hist)
+            atomicAdd(&p.hist[j], 1ull);
         p.ws_first[b] = kNoReject;
         p.ws_err[b] = 0;
     }
@@ -1235,6 +1243,7 @@ struct spec_verify_ctx {
     int mass_ctas;                       // resident CTAs of the mass kernel (all SMs)
     int *ws_first, *ws_err, *ws_tok, *status;
     float *ws_stats, *ws_slice;
+    unsigned long long *hist;  // [max_N + 2]: accepted-draft histogram, then invalid
     // profiling: events before kernel A, between the kernels and after kernel B
     int prof_on, prof_runs;
     cudaEvent_t *prof_ev;  // [kProfRuns][3]
@@ -1422,6 +1431,8 @@ sv_status run_impl(spec_verify_ctx *ctx, const void *target, const void *draft, 
     prm.ws_tok = ctx->ws_tok;
     prm.ws_stats = ctx->ws_stats;
     prm.ws_slice = ctx->ws_slice;
+    prm.hist = ctx->hist;
+    prm.hist_invalid = ctx->hist ? ctx->hist + ctx->max_N + 1 : nullptr;
     prm.status = ctx->status;
     prm.B = B;
     prm.N = N;
@@ -1521,25 +1532,27 @@ sv_status spec_verify_create(spec_verify_ctx **out, int device, int max_B, int m
 
     c->mass_ctas = (dtype == SV_BF16) ? mass_ctas<SV_BF16>(c->num_sms) : mass_ctas<SV_F32>(c->num_sms);
 
-    // workspace: first[nb] err[nb] tok[ntok] stats[4*ntok] | slice[nb*S*8] status;
+    // workspace: hist[max_N+2] (u64) | first[nb] err[nb] tok[ntok] stats[4*ntok] | slice[nb*S*8] status;
     // the slice shares start on a 256-byte boundary (kernel C reads them as float4)
     const size_t nb = (size_t)(max_B > 0 ? max_B : 1);
     const size_t ntok = nb * (size_t)(max_N + 1);
     const size_t nslice = nb * (size_t)residual_slices(V, dtype) * kConsWarps;
-    const size_t slice_off = (2 * nb + 5 * ntok + 63) / 64 * 64;
+    const size_t hist_ints = ((size_t)(max_N + 2) * 2 + 63) / 64 * 64;
+    const size_t slice_off = (hist_ints + 2 * nb + 5 * ntok + 63) / 64 * 64;
     const size_t bytes = sizeof(int) * (slice_off + nslice + 1);
     if (cudaMalloc(&c->ws, bytes) != cudaSuccess) {
         cudaGetLastError();
         free(c);
         return SV_ERR_OOM;
     }
-    int *w = static_cast<int *>(c->ws);
+    c->hist = static_cast<unsigned long long *>(c->ws);
+    int *w = static_cast<int *>(c->ws) + hist_ints;
     c->ws_first = w;
     c->ws_err = w + nb;
     c->ws_tok = w + 2 * nb;
     c->ws_stats = reinterpret_cast<float *>(w + 2 * nb + ntok);
-    c->ws_slice = reinterpret_cast<float *>(w + slice_off);
-    c->status = w + slice_off + nslice;
+    c->ws_slice = reinterpret_cast<float *>(static_cast<int *>(c->ws) + slice_off);
+    c->status = static_cast<int *>(c->ws) + slice_off + nslice;
     if (cudaMemset(c->ws, 0, bytes) != cudaSuccess || cudaMemset(c->ws_first, 0x7f, sizeof(int) * nb) != cudaSuccess ||
         cudaDeviceSynchronize() != cudaSuccess) {
         cudaGetLastError();
@@ -1596,6 +1609,25 @@ sv_status spec_verify_get_status(spec_verify_ctx *ctx)
         return SV_ERR_BAD_TOKEN;
     if (bits & kErrBadValue)
         return SV_ERR_BAD_VALUE;
+    return SV_OK;
+}
+
+sv_status spec_verify_acceptance_counts(spec_verify_ctx *ctx, uint64_t *counts, int ncounts, int reset)
+{
+    if (!ctx || !counts || ncounts < ctx->max_N + 2)
+        return SV_ERR_INVALID_ARG;
+    DeviceGuard guard(ctx->device);
+    if (!guard.ok)
+        return SV_ERR_CUDA;
+    const size_t bytes = sizeof(unsigned long long) * (size_t)(ctx->max_N + 2);
+    if (cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpy(counts, ctx->hist, bytes, cudaMemcpyDeviceToHost) != cudaSuccess ||
+        (reset && cudaMemset(ctx->hist, 0, bytes) != cudaSuccess) || (reset && cudaDeviceSynchronize() != cudaSuccess)) {
+        cudaGetLastError();
+        return SV_ERR_CUDA;
+    }
+    for (int k = ctx->max_N + 2; k < ncounts; ++k)
+        counts[k] = 0;
     return SV_OK;
 }
 

@@ -61,7 +61,26 @@ def test_host_validation_without_gpu(lib):
     assert sv.spec_verify_run(None, 16, 16, 16, 16, 16, 0, 1, 1, 16, 16, None) == sv.SV_ERR_INVALID_ARG
     assert sv.spec_verify_get_status(None) == sv.SV_ERR_INVALID_ARG
     assert sv.spec_verify_set_cluster_size(None, 2) == sv.SV_ERR_INVALID_ARG
+    st, _ = sv.spec_verify_acceptance_counts(None, 8)
+    assert st == sv.SV_ERR_INVALID_ARG
     sv.spec_verify_destroy(None)
+
+
+def test_kv_commit_host_validation_without_gpu(lib):
+    kv = sv.spec_verify_kv_commit
+    ok = (256, 512, 1024, 2048, None)  # scratch, cache, cache_len, num_accepted, status
+    assert kv(*ok, 2, 4, 5, 16, 0, None) == sv.SV_ERR_INVALID_ARG      # row_bytes 0
+    assert kv(*ok, 2, 4, 5, 16, 24, None) == sv.SV_ERR_INVALID_ARG     # not a multiple of 16
+    assert kv(*ok, 0, 4, 5, 16, 32, None) == sv.SV_ERR_INVALID_ARG     # no planes
+    assert kv(*ok, 2, -1, 5, 16, 32, None) == sv.SV_ERR_INVALID_ARG
+    assert kv(*ok, 2, 4, -1, 16, 32, None) == sv.SV_ERR_INVALID_ARG
+    assert kv(*ok, 2, 4, 5, -1, 32, None) == sv.SV_ERR_INVALID_ARG
+    assert kv(264, 512, 1024, 2048, None, 2, 4, 5, 16, 32, None) == sv.SV_ERR_INVALID_ARG  # misaligned
+    assert kv(256, 520, 1024, 2048, None, 2, 4, 5, 16, 32, None) == sv.SV_ERR_INVALID_ARG
+    assert kv(None, 512, 1024, 2048, None, 2, 4, 5, 16, 32, None) == sv.SV_ERR_INVALID_ARG
+    assert kv(256, 512, None, 2048, None, 2, 4, 5, 16, 32, None) == sv.SV_ERR_INVALID_ARG
+    assert kv(*ok, 1 << 20, 1 << 20, 5, 1 << 20, 1 << 20, None) == sv.SV_ERR_TOO_LARGE
+    assert kv(*ok, 2, 0, 5, 16, 32, None) == sv.SV_OK                  # no sequences: nothing to do
 
 
 def test_library_is_built_for_sm_103a():

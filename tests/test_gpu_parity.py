@@ -205,3 +205,26 @@ def test_profiling_hook_times_both_kernels():
     with pytest.raises(sv.SpecVerifyError):
         ctx.profile_read()
     _check(w, ctx=ctx)  # profiling left the results alone
+
+
+def test_acceptance_counts_match_the_oracle_histogram():
+    """The counters kernel C keeps equal the histogram of the oracle's
+    num_accepted over every run since the last reset (invalid sequences in
+    the last slot)."""
+    ctx = sv.SpecVerify(16, 5, 32000, "bf16")
+    assert ctx.acceptance_counts() == [0] * 7
+    want = np.zeros(7, dtype=np.int64)
+    for seed, B in [(20, 16), (21, 9)]:
+        w = synth.make_workload("small", seed=seed, device="cuda", B=B)
+        if seed == 21:
+            w.draft_tokens[3, 0] = -2  # one invalid sequence
+        parity.run_gpu(ctx, w, debug=False)
+        orc = parity.run_oracle(w, threads=THREADS)
+        for a in orc["num_accepted"]:
+            want[a if a >= 0 else 6] += 1
+    ctx.status()
+    got = ctx.acceptance_counts(reset=True)
+    assert sum(got) == 25 and got[6] == 1
+    # a sampled decision inside the margin band may move one sequence
+    assert np.abs(np.array(got) - want).sum() <= 2
+    assert ctx.acceptance_counts() == [0] * 7
