@@ -214,8 +214,7 @@ sv_status spec_verify_run_noalloc(const void *target_logits, const void *draft_l
  * Per sequence: num_accepted < 0 commits nothing; num_accepted > N commits
  * nothing and sets SV_KV_BAD_COUNT; cache_len < 0 or cache_len + num_accepted
  * > max_len commits nothing and sets SV_KV_OVERFLOW.  The bits are OR-ed into
- * *status (device int32, may be NULL); the caller clears it.  SV_KV_TIMEOUT
- * reports a copy that did not finish within 2 s (nothing is stored then).
+ * *status (device int32, may be NULL); the caller clears it.
  *
  * Host errors: SV_ERR_INVALID_ARG for negative sizes, planes < 1,
  * row_bytes == 0 or not a multiple of 16, a NULL pointer that is needed, or
@@ -227,8 +226,7 @@ sv_status spec_verify_run_noalloc(const void *target_logits, const void *draft_l
  */
 enum {
     SV_KV_OVERFLOW = 1,   /* cache_len + num_accepted > max_len, or cache_len < 0 */
-    SV_KV_BAD_COUNT = 2,  /* num_accepted > N */
-    SV_KV_TIMEOUT = 4     /* a staging copy did not complete */
+    SV_KV_BAD_COUNT = 2   /* num_accepted > N */
 };
 
 sv_status spec_verify_kv_commit(const void *scratch, void *cache, int32_t *cache_len,

@@ -52,7 +52,6 @@ _SIGNATURES = [
 
 SV_KV_OVERFLOW = 1
 SV_KV_BAD_COUNT = 2
-SV_KV_TIMEOUT = 4
 
 _lib = None
 

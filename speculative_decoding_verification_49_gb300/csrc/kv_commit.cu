@@ -10,12 +10,18 @@
 // The work is a plain byte copy: per (plane, sequence) segment, the first
 // a*row_bytes bytes of its scratch rows go to the cache at row cache_len[b].
 // Two kernels, both stream-ordered after whatever produced num_accepted:
-//   sv_kv_copy_kernel  one warp per CTA; each lane owns one segment (or, for
-//                      segments longer than a chunk, lane 0 owns one chunk of
-//                      one segment) and moves it with a TMA bulk load into
-//                      shared memory and a TMA bulk store out of it;
+//   sv_kv_copy_kernel  one warp per 4 KiB unit of a segment's scratch rows;
+//                      the warp moves the accepted part of its unit with
+//                      coalesced 16-byte loads and stores, four per lane in
+//                      flight (a warp whose unit holds no accepted row exits
+//                      at once);
 //   sv_kv_len_kernel   advances cache_len and reports bad counts / overflow.
-// The length update needs its own launch: every copying CTA reads cache_len.
+// The length update needs its own launch: every copying warp reads cache_len.
+// The copy is HBM-bound on the accepted bytes (each read once, written once).
+// A sequence typically accepts one or two of its N rows, so the segments are
+// small: the copy is done in registers, since a shared-memory (TMA) stage
+// would have to be sized for all N rows; measured, the TMA-staged copy, a
+// persistent grid and larger units were no faster.
 #include <climits>
 #include <cstddef>
 #include <cstdint>
@@ -29,9 +35,9 @@ namespace {
 
 using namespace sv;
 
-constexpr int kKvThreads = 32;
-constexpr uint32_t kKvChunk = 32u * 1024u;     // staging bytes per CTA (dynamic shared memory)
-constexpr uint64_t kKvWaitNs = 2000000000ull;  // give up on a bulk load after 2 s
+constexpr int kKvWarps = 4;                 // warps per CTA of the copy kernel
+constexpr uint32_t kKvUnit = 4096u;         // bytes of a segment one warp owns
+constexpr int kKvUnroll = 4;                // 16-byte vectors per lane in flight
 constexpr int kKvLenThreads = 256;
 
 struct KvParams {
@@ -43,8 +49,7 @@ struct KvParams {
     int P, B, N, max_len;
     unsigned long long row_bytes;
     unsigned long long seg_bytes;  // N * row_bytes: one sequence's scratch rows in one plane
-    int group;                     // segments per CTA (1 when a segment spans several chunks)
-    int nchunk;                    // chunks per segment (1 when group > 1)
+    int nunit;                     // units per segment
 };
 
 // Rows of a sequence to commit, and the error bits its counts raise.
@@ -64,59 +69,37 @@ __device__ __forceinline__ int kv_rows(int a, int len, int N, int max_len, int &
     return a;
 }
 
-__global__ void __launch_bounds__(kKvThreads) sv_kv_copy_kernel(KvParams k)
+__global__ void __launch_bounds__(kKvWarps * 32) sv_kv_copy_kernel(KvParams k)
 {
-    extern __shared__ __align__(128) unsigned char kv_stage[];
-    __shared__ __align__(8) uint64_t bar;
-    __shared__ int no_abort;
-
     grid_dependency_wait();
-    const int lane = threadIdx.x;
-    const long long unit = blockIdx.x;
-    const long long seg = (unit / k.nchunk) * k.group + lane;
-    const unsigned long long off = (unsigned long long)(unit % k.nchunk) * kKvChunk;
-    const long long nseg = (long long)k.P * k.B;
-
-    uint32_t bytes = 0;
-    const unsigned char *src = nullptr;
-    unsigned char *dst = nullptr;
-    if (lane < k.group && seg < nseg) {
-        const int b = (int)(seg % k.B);
-        const int len = __ldg(&k.cache_len[b]);
-        int bits;
-        const int rows = kv_rows(__ldg(&k.nacc[b]), len, k.N, k.max_len, bits);
-        const unsigned long long total = (unsigned long long)rows * k.row_bytes;
-        if (total > off) {
-            const unsigned long long n = total - off;
-            bytes = (uint32_t)(n < kKvChunk ? n : kKvChunk);
-            src = k.scratch + (unsigned long long)seg * k.seg_bytes + off;
-            dst = k.cache + ((unsigned long long)seg * k.max_len + len) * k.row_bytes + off;
-        }
-    }
-    const uint32_t total = __reduce_add_sync(0xffffffffu, bytes);
-    if (total == 0)
+    const int warp = threadIdx.x >> 5;
+    const unsigned lane = threadIdx.x & 31u;
+    const long long unit = (long long)blockIdx.x * kKvWarps + warp;
+    const long long seg = unit / k.nunit;
+    if (seg >= (long long)k.P * k.B)
         return;
-
-    if (lane == 0) {
-        no_abort = 0;
-        mbar_init(&bar, 1);
-        fence_mbar_init();
-        mbar_arrive_expect_tx(&bar, total);
-    }
-    __syncwarp();
-    unsigned char *slot = kv_stage + (k.group > 1 ? (size_t)lane * k.seg_bytes : 0);
-    if (bytes)
-        bulk_g2s(slot, src, bytes, &bar);
-    if (!mbar_wait_bounded(&bar, 0, &no_abort, kKvWaitNs)) {
-        if (k.status)
-            atomicOr(k.status, SV_KV_TIMEOUT);
-        mbar_wait_bounded(&bar, 0, &no_abort, kKvWaitNs);  // let the loads in flight land
+    const unsigned long long off = (unsigned long long)(unit % k.nunit) * kKvUnit;
+    const int b = (int)(seg % k.B);
+    const int len = __ldg(&k.cache_len[b]);
+    int bits;
+    const int rows = kv_rows(__ldg(&k.nacc[b]), len, k.N, k.max_len, bits);
+    const unsigned long long total = (unsigned long long)rows * k.row_bytes;
+    if (total <= off)
         return;
-    }
-    if (bytes) {
-        bulk_s2g(dst, slot, bytes);
-        bulk_commit();
-        bulk_wait_read_all();  // the stage must outlive the store's reads
+    const unsigned long long left = total - off;
+    const unsigned n = (unsigned)((left < kKvUnit ? left : kKvUnit) / 16);  // 16-byte vectors
+    const int4 *src = reinterpret_cast<const int4 *>(k.scratch + (unsigned long long)seg * k.seg_bytes + off);
+    int4 *dst = reinterpret_cast<int4 *>(k.cache + ((unsigned long long)seg * k.max_len + len) * k.row_bytes + off);
+    for (unsigned v = lane; v < n; v += 32u * kKvUnroll) {
+        int4 r[kKvUnroll];
+#pragma unroll
+        for (int u = 0; u < kKvUnroll; ++u)
+            if (v + 32u * u < n)
+                r[u] = __ldcs(src + v + 32u * u);  // read once: evict first
+#pragma unroll
+        for (int u = 0; u < kKvUnroll; ++u)
+            if (v + 32u * u < n)
+                dst[v + 32u * u] = r[u];
     }
 }
 
@@ -189,21 +172,18 @@ extern "C" sv_status spec_verify_kv_commit(const void *scratch, void *cache, int
     k.max_len = max_len;
     k.row_bytes = row_bytes;
     k.seg_bytes = (unsigned long long)N * row_bytes;
-    if (k.seg_bytes <= kKvChunk && k.seg_bytes > 0) {
-        const unsigned long long g = kKvChunk / k.seg_bytes;
-        k.group = (int)(g < (unsigned long long)kKvThreads ? g : kKvThreads);
-        k.nchunk = 1;
-    } else {
-        k.group = 1;
-        k.nchunk = (int)((k.seg_bytes + kKvChunk - 1) / kKvChunk);  // < 2^31 by the check above
-    }
+    const unsigned long long nunit = (k.seg_bytes + kKvUnit - 1) / kKvUnit;
+    if (nunit > (unsigned long long)INT_MAX)
+        return SV_ERR_TOO_LARGE;
+    k.nunit = (int)nunit;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaLaunchAttribute attr[1];
     if (N > 0 && max_len > 0) {
-        const unsigned long long units = (segs + k.group - 1) / k.group * (unsigned long long)k.nchunk;
-        if (units > (unsigned long long)INT_MAX)
+        const unsigned long long warps = segs * (unsigned long long)k.nunit;
+        const unsigned long long ctas = (warps + kKvWarps - 1) / kKvWarps;
+        if (ctas > (unsigned long long)INT_MAX)
             return SV_ERR_TOO_LARGE;
-        cudaLaunchConfig_t cfg = kv_launch((unsigned)units, kKvThreads, kKvChunk, st, attr);
+        cudaLaunchConfig_t cfg = kv_launch((unsigned)ctas, kKvWarps * 32, 0, st, attr);
         if (cudaLaunchKernelEx(&cfg, sv_kv_copy_kernel, k) != cudaSuccess) {
             cudaGetLastError();
             return SV_ERR_CUDA;

@@ -90,28 +90,6 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
-// ---- TMA: 1-D bulk copy this CTA's shared memory -> global --------------------
-// dst, src 16-byte aligned, bytes a multiple of 16; tracked by the issuing
-// thread's bulk-async group (commit, then wait before the source is reused).
-__device__ __forceinline__ void bulk_s2g(void *dst, const void *src, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
-                 "r"(smem_u32(src)), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit()
-{
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-
-// Waits until the committed bulk stores of this thread have read their shared
-// memory source (their global writes may still be in flight).
-__device__ __forceinline__ void bulk_wait_read_all()
-{
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-
 // ---- programmatic dependent launch -------------------------------------------
 // Blocks until the grids this one depends on have completed and their memory
 // is visible (a no-op when the launch had no such dependency).
