@@ -10,18 +10,21 @@
 // The work is a plain byte copy: per (plane, sequence) segment, the first
 // a*row_bytes bytes of its scratch rows go to the cache at row cache_len[b].
 // Two kernels, both stream-ordered after whatever produced num_accepted:
-//   sv_kv_copy_kernel  one warp per 4 KiB unit of a segment's scratch rows;
-//                      the warp moves the accepted part of its unit with
-//                      coalesced 16-byte loads and stores, four per lane in
-//                      flight (a warp whose unit holds no accepted row exits
-//                      at once);
+//   sv_kv_copy_kernel  one warp per 4 KiB unit of a segment's scratch rows
+//                      (grid: x = plane and unit, y = sequence, so the index
+//                      arithmetic stays in 32 bits); the warp moves the
+//                      accepted part of its unit with coalesced 16-byte loads
+//                      and stores, four per lane in flight (a warp whose unit
+//                      holds no accepted row exits at once);
 //   sv_kv_len_kernel   advances cache_len and reports bad counts / overflow.
 // The length update needs its own launch: every copying warp reads cache_len.
 // The copy is HBM-bound on the accepted bytes (each read once, written once).
-// A sequence typically accepts one or two of its N rows, so the segments are
-// small: the copy is done in registers, since a shared-memory (TMA) stage
-// would have to be sized for all N rows; measured, the TMA-staged copy, a
-// persistent grid and larger units were no faster.
+// A sequence typically accepts one or two of its N rows, so the work is small
+// and most units are empty.  Measured alternatives that were no faster on
+// such a commit: a TMA-staged copy (bulk load into shared memory, bulk store
+// out; the stage must be sized for all N rows), a persistent grid, one CTA
+// per (sequence, split) striping all planes, larger or smaller units, and
+// deeper unrolling.
 #include <climits>
 #include <cstddef>
 #include <cstdint>
@@ -39,6 +42,7 @@ constexpr int kKvWarps = 4;                 // warps per CTA of the copy kernel
 constexpr uint32_t kKvUnit = 4096u;         // bytes of a segment one warp owns
 constexpr int kKvUnroll = 4;                // 16-byte vectors per lane in flight
 constexpr int kKvLenThreads = 256;
+constexpr int kKvMaxGridY = 65535;          // sequences per launch row; larger batches loop
 
 struct KvParams {
     const unsigned char *scratch;  // [P][B][N][row_bytes]
@@ -72,34 +76,37 @@ __device__ __forceinline__ int kv_rows(int a, int len, int N, int max_len, int &
 __global__ void __launch_bounds__(kKvWarps * 32) sv_kv_copy_kernel(KvParams k)
 {
     grid_dependency_wait();
-    const int warp = threadIdx.x >> 5;
+    // blockIdx.y walks the sequences, blockIdx.x the (plane, unit) pairs of one
+    // sequence; every warp of a CTA serves the same sequence
     const unsigned lane = threadIdx.x & 31u;
-    const long long unit = (long long)blockIdx.x * kKvWarps + warp;
-    const long long seg = unit / k.nunit;
-    if (seg >= (long long)k.P * k.B)
+    const unsigned u = blockIdx.x * kKvWarps + (threadIdx.x >> 5);
+    if (u >= (unsigned)k.P * (unsigned)k.nunit)
         return;
-    const unsigned long long off = (unsigned long long)(unit % k.nunit) * kKvUnit;
-    const int b = (int)(seg % k.B);
-    const int len = __ldg(&k.cache_len[b]);
-    int bits;
-    const int rows = kv_rows(__ldg(&k.nacc[b]), len, k.N, k.max_len, bits);
-    const unsigned long long total = (unsigned long long)rows * k.row_bytes;
-    if (total <= off)
-        return;
-    const unsigned long long left = total - off;
-    const unsigned n = (unsigned)((left < kKvUnit ? left : kKvUnit) / 16);  // 16-byte vectors
-    const int4 *src = reinterpret_cast<const int4 *>(k.scratch + (unsigned long long)seg * k.seg_bytes + off);
-    int4 *dst = reinterpret_cast<int4 *>(k.cache + ((unsigned long long)seg * k.max_len + len) * k.row_bytes + off);
-    for (unsigned v = lane; v < n; v += 32u * kKvUnroll) {
-        int4 r[kKvUnroll];
+    const unsigned p = k.nunit == 1 ? u : u / (unsigned)k.nunit;
+    const unsigned long long off = (unsigned long long)(u - p * (unsigned)k.nunit) * kKvUnit;
+    for (int b = blockIdx.y; b < k.B; b += gridDim.y) {
+        const int len = __ldg(&k.cache_len[b]);
+        int bits;
+        const unsigned long long total =
+            (unsigned long long)kv_rows(__ldg(&k.nacc[b]), len, k.N, k.max_len, bits) * k.row_bytes;
+        if (total <= off)
+            continue;
+        const unsigned long long left = total - off;
+        const unsigned n = (unsigned)((left < kKvUnit ? left : kKvUnit) / 16);  // 16-byte vectors
+        const unsigned long long seg = (unsigned long long)p * k.B + b;
+        const int4 *src = reinterpret_cast<const int4 *>(k.scratch + seg * k.seg_bytes + off);
+        int4 *dst = reinterpret_cast<int4 *>(k.cache + (seg * k.max_len + len) * k.row_bytes + off);
+        for (unsigned v = lane; v < n; v += 32u * kKvUnroll) {
+            int4 x[kKvUnroll];
 #pragma unroll
-        for (int u = 0; u < kKvUnroll; ++u)
-            if (v + 32u * u < n)
-                r[u] = __ldcs(src + v + 32u * u);  // read once: evict first
+            for (int j = 0; j < kKvUnroll; ++j)
+                if (v + 32u * j < n)
+                    x[j] = __ldcs(src + v + 32u * j);  // read once: evict first
 #pragma unroll
-        for (int u = 0; u < kKvUnroll; ++u)
-            if (v + 32u * u < n)
-                dst[v + 32u * u] = r[u];
+            for (int j = 0; j < kKvUnroll; ++j)
+                if (v + 32u * j < n)
+                    dst[v + 32u * j] = x[j];
+        }
     }
 }
 
@@ -179,11 +186,12 @@ extern "C" sv_status spec_verify_kv_commit(const void *scratch, void *cache, int
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaLaunchAttribute attr[1];
     if (N > 0 && max_len > 0) {
-        const unsigned long long warps = segs * (unsigned long long)k.nunit;
-        const unsigned long long ctas = (warps + kKvWarps - 1) / kKvWarps;
-        if (ctas > (unsigned long long)INT_MAX)
+        const unsigned long long per_seq = (unsigned long long)planes * k.nunit;  // warps per sequence
+        if (per_seq > (unsigned long long)UINT_MAX - kKvWarps)
             return SV_ERR_TOO_LARGE;
-        cudaLaunchConfig_t cfg = kv_launch((unsigned)ctas, kKvWarps * 32, 0, st, attr);
+        cudaLaunchConfig_t cfg = kv_launch((unsigned)((per_seq + kKvWarps - 1) / kKvWarps), kKvWarps * 32, 0, st,
+                                           attr);
+        cfg.gridDim.y = (unsigned)(B < kKvMaxGridY ? B : kKvMaxGridY);
         if (cudaLaunchKernelEx(&cfg, sv_kv_copy_kernel, k) != cudaSuccess) {
             cudaGetLastError();
             return SV_ERR_CUDA;
