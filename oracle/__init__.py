@@ -87,6 +87,8 @@ class Oracle:
                                         P, P, P, P, P, P, P, i]
         self.lib.orc_softmax_row.restype = i
         self.lib.orc_softmax_row.argtypes = [P, i, i, ctypes.c_double, P, P, P]
+        self.lib.orc_tree_verify.restype = i
+        self.lib.orc_tree_verify.argtypes = [P, P, i, P, P, P, P, i, i, i, i, P, P, P, P, P, P, P, P, i]
         self.lib.orc_kv_commit.restype = i
         self.lib.orc_kv_commit.argtypes = [P, P, P, P, i, i, i, i, ctypes.c_size_t]
 
@@ -156,6 +158,50 @@ class Oracle:
         return probs, m.value, S.value
 
 
+    def tree_verify(self, target, draft, parent, tokens, uniforms, temperature=None,
+                    greedy=False, dtype="f32", threads=1, diagnostics=True):
+        """Verify B candidate trees of M+1 nodes (node 0 = the committed context).
+
+        target, draft: [B, M+1, V] logits per node (draft rows of leaves are
+        not read; draft may be None when greedy); parent: [B, M+1] or [M+1]
+        int (parent[0] = -1, parent[n] < n); tokens: [B, M+1] int (entry 0
+        unused); uniforms: [B, M+1] (entry n >= 1 the accept test of node n,
+        entry 0 the final sample); temperature: [B] or None when greedy.
+
+        Returns out_tokens, path_nodes [B, M+1], num_accepted, seq_status [B]
+        and, with diagnostics, tstats / dstats [B, M+1, 2] (visited nodes),
+        accept_margin [B, M+1] (NaN = not tested), sample_margin [B]."""
+        tgt = _as_logits(target, dtype)
+        B, M1, V = tgt.shape
+        M = M1 - 1
+        drf = None if draft is None else _as_logits(draft, dtype)
+        if drf is not None:
+            assert drf.shape == (B, M + 1, V), drf.shape
+        par = _np(parent, np.int32)
+        if par.ndim == 1:
+            par = np.ascontiguousarray(np.broadcast_to(par, (B, M + 1)))
+        tok = _np(tokens, np.int32)
+        u = _np(uniforms, np.float64)
+        T = _np(temperature, np.float64)
+        assert par.shape == (B, M + 1) and tok.shape == (B, M + 1) and u.shape == (B, M + 1)
+        res = {"out_tokens": np.full((B, M + 1), -7, np.int32), "path_nodes": np.full((B, M + 1), -7, np.int32),
+               "num_accepted": np.full((B,), -7, np.int32), "seq_status": np.zeros((B,), np.int32)}
+        if diagnostics:
+            res.update(tstats=np.full((B, M + 1, 2), np.nan), dstats=np.full((B, M + 1, 2), np.nan),
+                       accept_margin=np.full((B, M + 1), np.nan), sample_margin=np.full((B,), np.nan))
+
+        def ptr(a):
+            return None if a is None else a.ctypes.data
+
+        rc = self.lib.orc_tree_verify(
+            ptr(tgt), ptr(drf), DTYPES[dtype], ptr(par), ptr(tok), ptr(u), ptr(T), int(bool(greedy)),
+            B, M, V, ptr(res["out_tokens"]), ptr(res["path_nodes"]), ptr(res["num_accepted"]),
+            ptr(res.get("tstats")), ptr(res.get("dstats")), ptr(res.get("accept_margin")),
+            ptr(res.get("sample_margin")), ptr(res["seq_status"]), int(threads))
+        if rc != 0:
+            raise ValueError("oracle rejected its arguments")
+        return res
+
     def kv_commit(self, scratch, cache, cache_len, num_accepted):
         """Append each sequence's accepted draft KV rows to its cache.
 
@@ -190,3 +236,7 @@ def verify(*args, **kwargs):
 
 def kv_commit(*args, **kwargs):
     return default().kv_commit(*args, **kwargs)
+
+
+def tree_verify(*args, **kwargs):
+    return default().tree_verify(*args, **kwargs)

@@ -483,3 +483,260 @@ int orc_kv_commit(const unsigned char *scratch, unsigned char *cache, int32_t *c
     }
     return status;
 }
+
+/*
+ * Tree verification.  The pages name candidate trees (the lesson's "Medusa"
+ * section: candidates from every head verified in one forward with tree
+ * attention; its "EAGLE" section and the reading list: EAGLE-2's dynamic draft
+ * trees) and require that the output keep the verifier's distribution
+ * ("A friend writes first and the teacher grades", section "The guarantee that
+ * the answer does not change"), but give no rule for a node with several
+ * candidates.  The plainest rule that keeps the guarantee, taken here: the
+ * children of a node are independent draws from the draft distribution at
+ * that node, and they are tried in ascending node order with the same accept
+ * test, each rejection replacing the current verifier distribution by the
+ * normalised residual (current - draft)+; an accepted child becomes the new
+ * node; when every child is rejected, the token is drawn from the last
+ * residual; a leaf draws the bonus token from its verifier distribution.
+ * A tree whose nodes form one chain is exactly the chain verify above.
+ *
+ * Per sequence b, nodes n = 0..M (node 0 = the committed context):
+ *   parent[b][n]: -1 for n = 0, in [0, n) otherwise (siblings in index order)
+ *   tokens[b][n]: the draft token of node n (n >= 1)
+ *   target row n: logits of the verifier after node n's path, q_n = softmax(./T)
+ *   draft row n:  logits of the draft at node n, p_n = softmax(./T), from which
+ *                 n's children were drawn (read only for nodes with children)
+ *   u[b][n], n >= 1: the accept test of node n;  u[b][0]: the final sample
+ * Walk: n = 0, r = q_0.  For each child c of n in order: x = tokens[c];
+ *   accept iff p_n(x) == 0 or u[c] < min(1, r(x)/p_n(x)); on accept the path
+ *   gains c, n = c, r = q_c and the walk goes on; on reject
+ *   r <- (r - p_n)+ / sum (r - p_n)+, or r unchanged if that sum is 0.
+ *   No child accepted (or none at all): t = inverse CDF of r at u[b][0].
+ * Outputs: out_tokens = the path's tokens then t, -1 after; path_nodes = the
+ * path's node ids, -1 after; num_accepted = path length.  Greedy sequences:
+ * accept the first child whose token is argmax q_n; emit argmax q_n at the
+ * end.  Invalid sequences (as in the chain verify, plus a parent array that
+ * breaks the rules above: status bit 4) emit -1 everywhere.
+ */
+#define ORC_SEQ_BAD_TREE 4
+
+typedef struct {
+    const void *target, *draft;
+    int dtype;
+    const int32_t *parent, *tokens;
+    const double *u, *T;
+    int greedy, B, M, V;
+    int32_t *out_tokens, *path_nodes, *num_accepted;
+    double *tstats, *dstats, *accept_margin, *sample_margin;
+    int32_t *seq_status;
+} orc_tree_args;
+
+static void orc_tree_sequence(const orc_tree_args *a, int b, double *r, double *p)
+{
+    const int M = a->M, V = a->V;
+    const size_t row0 = (size_t)b * (M + 1); /* node n of b is row row0 + n */
+    const int32_t *par = a->parent + row0;
+    const int32_t *tok = a->tokens + row0;
+    int32_t *out = a->out_tokens + row0, *path = a->path_nodes + row0;
+    int status = 0;
+
+    for (int n = 0; n <= M; n++) {
+        out[n] = -1;
+        path[n] = -1;
+        if (a->accept_margin)
+            a->accept_margin[row0 + n] = NAN;
+    }
+    if (a->sample_margin)
+        a->sample_margin[b] = NAN;
+
+    if (par[0] != -1)
+        status |= ORC_SEQ_BAD_TREE;
+    for (int n = 1; n <= M; n++) {
+        if (par[n] < 0 || par[n] >= n)
+            status |= ORC_SEQ_BAD_TREE;
+        if (tok[n] < 0 || tok[n] >= V)
+            status |= ORC_SEQ_BAD_TOKEN;
+    }
+    int greedy = a->greedy != 0;
+    double T = 0.0;
+    if (!greedy) {
+        T = a->T[b];
+        if (isnan(T))
+            status |= ORC_SEQ_BAD_VALUE;
+        else if (T <= 0.0)
+            greedy = 1;
+        else if (T == INFINITY || T < (double)FLT_MIN)
+            status |= ORC_SEQ_BAD_VALUE;
+    }
+    for (int n = 0; n <= M; n++) {
+        if (!orc_row_valid(a->target, a->dtype, (row0 + n) * (size_t)V, V))
+            status |= ORC_SEQ_BAD_VALUE;
+        int has_child = 0;
+        for (int c = n + 1; c <= M; c++)
+            if (par[c] == n)
+                has_child = 1;
+        if (!greedy && has_child && !(status & ORC_SEQ_BAD_TREE) &&
+            !orc_row_valid(a->draft, a->dtype, (row0 + n) * (size_t)V, V))
+            status |= ORC_SEQ_BAD_VALUE;
+    }
+    if (a->seq_status)
+        a->seq_status[b] = status;
+    if (status) {
+        a->num_accepted[b] = -1;
+        return;
+    }
+
+    int n = 0, depth = 0;
+    if (greedy) {
+        for (;;) {
+            int an = orc_argmax(a->target, a->dtype, (row0 + n) * (size_t)V, V);
+            int next = -1;
+            for (int c = n + 1; c <= M && next < 0; c++) {
+                if (par[c] != n)
+                    continue;
+                if (a->accept_margin)
+                    a->accept_margin[row0 + c] = INFINITY;
+                if (tok[c] == an)
+                    next = c;
+            }
+            if (next < 0) {
+                out[depth] = an;
+                break;
+            }
+            out[depth] = tok[next];
+            path[depth] = next;
+            depth++;
+            n = next;
+        }
+        a->num_accepted[b] = depth;
+        if (a->sample_margin)
+            a->sample_margin[b] = INFINITY;
+        return;
+    }
+
+    for (;;) {
+        double mq, Sq;
+        orc_row_normaliser(a->target, a->dtype, (row0 + n) * (size_t)V, V, T, &mq, &Sq);
+        if (a->tstats) {
+            a->tstats[(row0 + n) * 2 + 0] = mq;
+            a->tstats[(row0 + n) * 2 + 1] = Sq;
+        }
+        for (int k = 0; k < V; k++)
+            r[k] = orc_prob(orc_logit(a->target, a->dtype, (row0 + n) * (size_t)V + k), mq, Sq, T);
+        int has_child = 0;
+        for (int c = n + 1; c <= M; c++)
+            if (par[c] == n)
+                has_child = 1;
+        if (has_child) {
+            double mp, Sp;
+            orc_row_normaliser(a->draft, a->dtype, (row0 + n) * (size_t)V, V, T, &mp, &Sp);
+            if (a->dstats) {
+                a->dstats[(row0 + n) * 2 + 0] = mp;
+                a->dstats[(row0 + n) * 2 + 1] = Sp;
+            }
+            for (int k = 0; k < V; k++)
+                p[k] = orc_prob(orc_logit(a->draft, a->dtype, (row0 + n) * (size_t)V + k), mp, Sp, T);
+        }
+        int next = -1;
+        for (int c = n + 1; c <= M && next < 0; c++) {
+            if (par[c] != n)
+                continue;
+            const int x = tok[c];
+            int accept;
+            double margin = INFINITY;
+            if (p[x] == 0.0) {
+                accept = 1;
+            } else {
+                double ratio = r[x] / p[x];
+                double thresh = ratio < 1.0 ? ratio : 1.0;
+                accept = a->u[row0 + c] < thresh;
+                if (ratio < 1.0)
+                    margin = fabs(a->u[row0 + c] - ratio);
+            }
+            if (a->accept_margin)
+                a->accept_margin[row0 + c] = margin;
+            if (accept) {
+                next = c;
+                break;
+            }
+            /* rejected: the next sibling is tested against the residual */
+            double R = 0.0;
+            for (int k = 0; k < V; k++) {
+                double diff = r[k] - p[k];
+                R += diff > 0.0 ? diff : 0.0;
+            }
+            if (R > 0.0)
+                for (int k = 0; k < V; k++) {
+                    double diff = r[k] - p[k];
+                    r[k] = (diff > 0.0 ? diff : 0.0) / R;
+                }
+        }
+        if (next < 0) {
+            double smargin;
+            out[depth] = orc_inverse_cdf(r, V, a->u[row0], &smargin);
+            if (a->sample_margin)
+                a->sample_margin[b] = smargin;
+            break;
+        }
+        out[depth] = tok[next];
+        path[depth] = next;
+        depth++;
+        n = next;
+    }
+    a->num_accepted[b] = depth;
+}
+
+typedef struct {
+    const orc_tree_args *a;
+    int b0, b1;
+} orc_tree_range;
+
+static void *orc_tree_worker(void *arg)
+{
+    orc_tree_range *rg = (orc_tree_range *)arg;
+    double *r = (double *)malloc(sizeof(double) * 2 * (size_t)rg->a->V);
+    for (int b = rg->b0; b < rg->b1; b++)
+        orc_tree_sequence(rg->a, b, r, r + rg->a->V);
+    free(r);
+    return NULL;
+}
+
+/* Batched tree verification; returns 0, or -1 on a bad argument. */
+int orc_tree_verify(const void *target, const void *draft, int dtype, const int32_t *parent,
+                    const int32_t *tokens, const double *u, const double *T, int greedy,
+                    int B, int M, int V, int32_t *out_tokens, int32_t *path_nodes,
+                    int32_t *num_accepted, double *tstats, double *dstats,
+                    double *accept_margin, double *sample_margin, int32_t *seq_status,
+                    int nthreads)
+{
+    if (B < 0 || M < 0 || V < 1 || !target || !parent || !tokens || !u || !out_tokens ||
+        !path_nodes || !num_accepted)
+        return -1;
+    if (!greedy && (!T || (M > 0 && !draft)))
+        return -1;
+    if (dtype != ORC_F32 && dtype != ORC_BF16 && dtype != ORC_F64)
+        return -1;
+    orc_tree_args a = {target, draft, dtype, parent, tokens, u, T, greedy, B, M, V,
+                       out_tokens, path_nodes, num_accepted, tstats, dstats,
+                       accept_margin, sample_margin, seq_status};
+    if (nthreads <= 1 || B <= 1) {
+        orc_tree_range rg = {&a, 0, B};
+        orc_tree_worker(&rg);
+        return 0;
+    }
+    if (nthreads > B)
+        nthreads = B;
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    orc_tree_range *rg = (orc_tree_range *)malloc(sizeof(orc_tree_range) * (size_t)nthreads);
+    for (int t = 0; t < nthreads; t++) {
+        rg[t].a = &a;
+        rg[t].b0 = (int)((long long)B * t / nthreads);
+        rg[t].b1 = (int)((long long)B * (t + 1) / nthreads);
+        pthread_create(&th[t], NULL, orc_tree_worker, &rg[t]);
+    }
+    for (int t = 0; t < nthreads; t++)
+        pthread_join(th[t], NULL);
+    free(th);
+    free(rg);
+    return 0;
+}

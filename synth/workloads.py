@@ -172,6 +172,145 @@ def make_workload(name: str, seed: int = 0, device="cpu", chunk_rows: int = 4096
                     draft_tokens=tokens, uniforms=uniforms, temperature=T)
 
 
+# ---- candidate trees ---------------------------------------------------------
+#
+# Tree recipe (per sequence b, node n = 0..M, node 0 = the committed context):
+#   base[b,n,:] ~ N(0, sigma_p^2)              (the draft's logits at node n)
+#   draft[b,n,:] = base[b,n,:];  target[b,n,:] = base[b,n,:] + N(0, sigma_q^2)
+# then the twists, then rounding to the storage dtype.  The children of node n
+# are independent Gumbel-max draws from softmax(draft[b,n,:]/T) (argmax for
+# T <= 0).  Topologies: "eagle16" is a fixed 16-node tree shaped like the
+# static trees of Medusa / EAGLE (wide at the root, narrowing with depth);
+# "random" gives every sequence its own tree, parent[n] uniform in
+# [max(0, n-3), n-1] (dynamic trees, as in EAGLE-2).  Uniforms: one per node
+# (column n >= 1: the accept test of node n; column 0: the final sample).
+EAGLE16_PARENT = [-1, 0, 0, 0, 0, 1, 1, 1, 2, 2, 3, 5, 5, 6, 8, 11]
+
+TREE_CONFIGS = {
+    "tree_small": dict(B=6, M=10, V=4096, dtype="f32", T=1.0, sigma_p=2.0, sigma_q=1.0, topology="random"),
+    "tree_mixed": dict(B=16, M=20, V=32000, dtype="bf16", T=(0.0, 0.7, 1.0), sigma_p=3.0, sigma_q=(0.3, 2.0),
+                       topology="random", spike_frac=0.10, spike=8.0),
+    "tree": dict(B=64, M=15, V=151936, dtype="bf16", T=0.8, sigma_p=3.0, sigma_q=1.0, zipf=1.1,
+                 topology="eagle16"),
+}
+
+
+@dataclasses.dataclass
+class TreeWorkload:
+    name: str
+    B: int
+    M: int
+    V: int
+    dtype: str
+    target: torch.Tensor       # [B, M+1, V]
+    draft: torch.Tensor        # [B, M+1, V] (rows of leaves are not read)
+    parent: torch.Tensor       # [B, M+1] int32
+    tokens: torch.Tensor       # [B, M+1] int32 (column 0 unused)
+    uniforms: torch.Tensor     # [B, M+1] float32
+    temperature: torch.Tensor  # [B] float32
+    greedy: bool = False
+
+    @property
+    def elt(self) -> int:
+        return 2 if self.dtype == "bf16" else 4
+
+    def internal(self):
+        """[B, M+1] bool: nodes with at least one child."""
+        has = torch.zeros((self.B, self.M + 1), dtype=torch.bool, device=self.parent.device)
+        if self.M > 0:
+            has.scatter_(1, self.parent[:, 1:].long().clamp(min=0), True)
+        return has
+
+    @property
+    def logit_bytes(self) -> int:
+        """Rows the verify reads: every target row, the draft rows of internal
+        nodes (of sampled sequences)."""
+        sampled = self.temperature > 0 if not self.greedy else torch.zeros_like(self.temperature, dtype=torch.bool)
+        draft_rows = int((self.internal() & sampled.view(-1, 1)).sum())
+        return (self.B * (self.M + 1) + draft_rows) * self.V * self.elt
+
+
+def tree_config(name: str, **overrides) -> dict:
+    c = dict(TREE_CONFIGS[name])
+    c.update(overrides)
+    c["name"] = name
+    return c
+
+
+def make_tree_workload(name: str, seed: int = 0, device="cpu", **overrides) -> TreeWorkload:
+    c = tree_config(name, **overrides)
+    B, M, V = c["B"], c["M"], c["V"]
+    dev = torch.device(device)
+    g = torch.Generator(device=dev)
+    g.manual_seed(int(seed) + 7919)
+    tdt = _torch_dtype(c["dtype"])
+
+    T_spec = c["T"]
+    if isinstance(T_spec, tuple):
+        pick = torch.randint(0, len(T_spec), (B,), generator=g, device=dev)
+        T = torch.tensor(T_spec, dtype=torch.float32, device=dev)[pick]
+    else:
+        T = torch.full((B,), float(T_spec), dtype=torch.float32, device=dev)
+    sq_spec = c["sigma_q"]
+    if isinstance(sq_spec, tuple):
+        lo, hi = sq_spec
+        sigma_q = lo + (hi - lo) * torch.rand((B,), generator=g, device=dev)
+    else:
+        sigma_q = torch.full((B,), float(sq_spec), device=dev)
+
+    if c["topology"] == "eagle16":
+        assert M == len(EAGLE16_PARENT) - 1
+        parent = torch.tensor(EAGLE16_PARENT, dtype=torch.int32, device=dev).repeat(B, 1)
+    else:
+        parent = torch.full((B, M + 1), -1, dtype=torch.int32, device=dev)
+        for n in range(1, M + 1):
+            lo = max(0, n - 3)
+            parent[:, n] = torch.randint(lo, n, (B,), generator=g, device=dev).to(torch.int32)
+
+    target = torch.empty((B, M + 1, V), dtype=tdt, device=dev)
+    draft = torch.empty((B, M + 1, V), dtype=tdt, device=dev)
+    zipf_bias = None
+    if c.get("zipf"):
+        rank = torch.arange(1, V + 1, device=dev, dtype=torch.float32)
+        zipf_bias = -float(c["zipf"]) * torch.log(rank)
+    per = max(1, 4096 // (M + 1))
+    for b0 in range(0, B, per):
+        b1 = min(B, b0 + per)
+        nb = b1 - b0
+        base = torch.randn((nb, M + 1, V), generator=g, device=dev) * c["sigma_p"]
+        zq = base + torch.randn((nb, M + 1, V), generator=g, device=dev) * sigma_q[b0:b1].view(nb, 1, 1)
+        if zipf_bias is not None:
+            odd = (torch.arange(b0, b1, device=dev) % 2 == 1).view(nb, 1, 1)
+            base = torch.where(odd, base + zipf_bias, base)
+            zq = torch.where(odd, zq + zipf_bias, zq)
+        target[b0:b1] = zq.to(tdt)
+        draft[b0:b1] = base.to(tdt)
+        del base, zq
+
+    if c.get("spike_frac"):
+        rows = torch.rand((B, M + 1), generator=g, device=dev) < c["spike_frac"]
+        tok = torch.randint(0, V, (B, M + 1), generator=g, device=dev)
+        idx = rows.nonzero(as_tuple=False)
+        if idx.numel():
+            bb, nn = idx[:, 0], idx[:, 1]
+            kk = tok[bb, nn]
+            target[bb, nn, kk] = (target[bb, nn, kk].float() + float(c["spike"])).to(tdt)
+
+    # children: independent Gumbel-max draws from their parent's draft row
+    tokens = torch.zeros((B, M + 1), dtype=torch.int32, device=dev)
+    for n in range(1, M + 1):
+        par = parent[:, n].long()
+        z = draft[torch.arange(B, device=dev), par].float()
+        Tb = T.view(-1, 1)
+        gumbel = -torch.log(torch.empty_like(z).exponential_(generator=g))
+        sampled = torch.argmax(z / torch.where(Tb > 0, Tb, torch.ones_like(Tb)) + gumbel, dim=-1)
+        greedy = torch.argmax(z, dim=-1)
+        tokens[:, n] = torch.where(T > 0, sampled, greedy).to(torch.int32)
+    uniforms = torch.rand((B, M + 1), generator=g, device=dev, dtype=torch.float32)
+    return TreeWorkload(name=name, B=B, M=M, V=V, dtype=c["dtype"], target=target, draft=draft, parent=parent,
+                        tokens=tokens, uniforms=uniforms, temperature=T)
+
+
 def describe(name: str) -> str:
     c = config(name)
     B, N, V = c["B"], c["N"], c["V"]
@@ -180,4 +319,5 @@ def describe(name: str) -> str:
     return f"{name}: B={B} N={N} V={V} {c['dtype']} ({gb:.3f} GB of logits)"
 
 
-__all__ = ["CONFIGS", "Workload", "config", "make_workload", "describe"]
+__all__ = ["CONFIGS", "Workload", "config", "make_workload", "describe", "TREE_CONFIGS", "TreeWorkload",
+           "tree_config", "make_tree_workload", "EAGLE16_PARENT"]

@@ -14,9 +14,11 @@ import numpy as np
 from scipy.special import logsumexp, softmax
 
 import lawlib
+import treelaw
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "worked_numbers.txt")
 NEG_INF = -np.inf
+ONE_MINUS = np.nextafter(1.0, 0.0)
 
 
 def golden():
@@ -581,6 +583,157 @@ def pin_kv_planes_and_sequences_stay_apart(orc):
     assert st == 0 and list(ln) == [1, 4] and np.array_equal(c2, cache)
 
 
+# ---- tree verification ---------------------------------------------------------
+
+def _prefix_model(seed, V, scale=1.5, mask=False):
+    """Logits after every token prefix, drawn once per prefix (a stand-in for a
+    language model); with mask, one token per prefix gets -inf."""
+    cache = {}
+
+    def f(prefix):
+        key = tuple(int(t) for t in prefix)
+        if key not in cache:
+            g = np.random.default_rng([seed, len(key)] + [t + 1 for t in key])
+            z = g.normal(0.0, scale, V)
+            if mask:
+                z[g.integers(V)] = NEG_INF
+            cache[key] = z
+        return cache[key]
+    return f
+
+
+def pin_tree_exact_law(orc):
+    """Children drawn independently from their parent's draft distribution,
+    every assignment and every uniform: the emitted sequence is distributed as
+    ancestral sampling from the verifier, prefix by prefix."""
+    cases = [([-1, 0, 0, 1, 1], 3, 1.0, False), ([-1, 0, 0, 0], 3, 0.8, False),
+             ([-1, 0, 1, 1, 0], 2, 1.3, False), ([-1, 0, 0, 1], 3, 1.0, True)]
+    for i, (parent, V, T, mask) in enumerate(cases):
+        mq, mp = _prefix_model(100 + i, V, mask=mask), _prefix_model(200 + i, V, mask=mask)
+        law = treelaw.exact_tree_law(orc, parent, V, mq, mp, T)
+        treelaw.check_ancestral(law, mq, T)
+        depth = max(len(s) for s in law)
+        assert depth >= 2, law  # some draft is accepted with positive probability
+
+
+def pin_tree_chain_is_the_chain_verify(orc):
+    """A tree whose nodes form one chain gives the chain verify's outputs
+    (uniforms mapped: node n+1 <- u[n], the final sample <- u[N]); the draft
+    row of the last node (a leaf) is not read."""
+    rng = np.random.default_rng(31)
+    B, N, V, T = 60, 4, 6, 0.9
+    zq = rng.normal(0, 1.2, (B, N + 1, V))
+    zp = rng.normal(0, 1.2, (B, N, V))
+    d = rng.integers(0, V, (B, N)).astype(np.int32)
+    u = rng.random((B, N + 1))
+    parent = np.arange(-1, N, dtype=np.int32)
+    tok = np.concatenate([np.zeros((B, 1), np.int32), d], axis=1)
+    ut = np.concatenate([u[:, N:], u[:, :N]], axis=1)
+    zpt = np.concatenate([zp, np.full((B, 1, V), np.nan)], axis=1)
+    for greedy in (False, True):
+        c = orc.verify(zq, None if greedy else zp, d, u, None if greedy else np.full(B, T), greedy=greedy, dtype="f64")
+        t = orc.tree_verify(zq, None if greedy else zpt, parent, tok, ut, None if greedy else np.full(B, T),
+                            greedy=greedy, dtype="f64")
+        assert (t["seq_status"] == 0).all()
+        sure = (c["sample_margin"] > 1e-12) | greedy
+        assert sure.sum() >= B - 2
+        assert np.array_equal(c["num_accepted"], t["num_accepted"])
+        assert np.array_equal(c["out_tokens"][sure], t["out_tokens"][sure])
+        for b in range(B):
+            a = c["num_accepted"][b]
+            assert list(t["path_nodes"][b][:a]) == list(range(1, a + 1)) and (t["path_nodes"][b][a:] == -1).all()
+            if not greedy:
+                np.testing.assert_allclose(t["accept_margin"][b, 1:a + 2][: min(a + 1, N)],
+                                           c["accept_margin"][b, : min(a + 1, N)], rtol=1e-12)
+
+
+def pin_tree_worked_siblings(orc):
+    """Two children at the root, q_0 = (1/2, 1/2), p_0 = (0.9, 0.1), V = 2.
+    The first child (token 0) passes with probability (1/2)/0.9 = 5/9.  After
+    its rejection the residual is (0, 1): a second child with token 0 has
+    ratio 0 and always fails (the token is then 1), one with token 1 has ratio
+    10 and always passes."""
+    zq = np.log(np.array([[0.5, 0.5], [0.5, 0.5], [0.5, 0.5]]))[None]
+    zp = np.log(np.array([[0.9, 0.1], [0.5, 0.5], [0.5, 0.5]]))[None]
+    parent = [-1, 0, 0]
+    for toks, u1, want_path, want_first in [((0, 0), 0.6, [], 1), ((0, 1), 0.6, [2], 1), ((0, 1), 0.5, [1], 0),
+                                            ((0, 0), 0.5, [1], 0)]:
+        r = orc.tree_verify(zq, zp, parent, np.array([[0, *toks]]), np.array([[0.3, u1, 0.99]]), np.ones(1),
+                            dtype="f64")
+        path = list(r["path_nodes"][0][: r["num_accepted"][0]])
+        assert path == want_path, (toks, u1, path)
+        assert r["out_tokens"][0][0] == want_first
+        assert abs(r["accept_margin"][0][1] - abs(u1 - 5.0 / 9.0)) < 1e-15
+        if toks == (0, 0) and u1 > 5.0 / 9.0:
+            assert abs(r["accept_margin"][0][2] - 0.99) < 1e-15  # |u - 0|
+            assert r["sample_margin"][0] > 0.3 - 1e-15  # the residual is all on token 1
+        if toks == (0, 1) and u1 > 5.0 / 9.0:
+            assert r["accept_margin"][0][2] == np.inf
+    # a child whose token the draft gives probability 0 is accepted (ratio +inf),
+    # as in the chain verify, whatever its uniform
+    zp0 = np.array([[[0.0, -np.inf], [0.0, 0.0], [0.0, 0.0]]])
+    for u1 in (0.0, 0.5, ONE_MINUS):
+        r = orc.tree_verify(zq, zp0, parent, np.array([[0, 1, 0]]), np.array([[0.3, u1, 0.5]]), np.ones(1),
+                            dtype="f64")
+        assert list(r["path_nodes"][0][:1]) == [1] and r["accept_margin"][0][1] == np.inf
+
+
+def pin_tree_greedy_rule(orc):
+    """Greedy: accept the first child (in index order) whose token is the
+    verifier's argmax at its parent; emit the argmax where no child matches."""
+    V = 6
+    zq = np.zeros((1, 6, V))
+    zq[0, 0, 3] = 2.0  # root argmax 3
+    zq[0, 2, 4] = 1.0  # node 2 argmax 4
+    zq[0, 5, 1] = 3.0  # node 5 argmax 1
+    zq[0, 3, 0] = 9.0  # node 3 (never reached) argmax 0
+    parent = [-1, 0, 0, 0, 2, 2]
+    tok = np.array([[0, 1, 3, 3, 2, 4]])
+    for greedy, T in [(True, None), (False, np.zeros(1))]:
+        r = orc.tree_verify(zq, None if greedy else np.zeros_like(zq), parent, tok, np.full((1, 6), 0.5), T,
+                            greedy=greedy, dtype="f64")
+        assert list(r["path_nodes"][0][:2]) == [2, 5] and r["num_accepted"][0] == 2
+        assert list(r["out_tokens"][0][:3]) == [3, 4, 1] and (r["out_tokens"][0][3:] == -1).all()
+    # ties go to the lowest index, as in the chain verify
+    zq2 = np.zeros((1, 2, V))
+    r = orc.tree_verify(zq2, None, [-1, 0], np.array([[0, 0]]), np.zeros((1, 2)), None, greedy=True, dtype="f64")
+    assert r["num_accepted"][0] == 1 and list(r["out_tokens"][0]) == [0, 0]
+
+
+def pin_tree_invalid_inputs(orc):
+    V, M = 5, 3
+    rng = np.random.default_rng(41)
+    good_parent = np.array([-1, 0, 0, 1], np.int32)
+    base = dict(zq=rng.normal(0, 1, (1, M + 1, V)), zp=rng.normal(0, 1, (1, M + 1, V)),
+                parent=good_parent, tok=np.array([[0, 1, 2, 3]], np.int32), T=np.ones(1))
+
+    def run(**kw):
+        a = {**base, **kw}
+        return orc.tree_verify(a["zq"], a["zp"], a["parent"], a["tok"], np.full((1, M + 1), 0.4), a["T"], dtype="f64")
+
+    assert run()["seq_status"][0] == 0
+    for bad_parent in ([0, 0, 0, 1], [-1, 0, 2, 1], [-1, 0, 0, -1], [-1, 0, 0, 4]):
+        r = run(parent=np.array(bad_parent, np.int32))
+        assert r["seq_status"][0] & 4 and r["num_accepted"][0] == -1 and (r["out_tokens"] == -1).all()
+    assert run(tok=np.array([[0, 1, V, 3]], np.int32))["seq_status"][0] == 1
+    zp = base["zp"].copy()
+    zp[0, 1, 2] = np.nan  # node 1 has a child: its draft row is read
+    assert run(zp=zp)["seq_status"][0] == 2
+    zp = base["zp"].copy()
+    zp[0, 3, :] = np.nan  # leaves' draft rows are not read
+    zp[0, 2, :] = np.nan
+    assert run(zp=zp)["seq_status"][0] == 0
+    zq = base["zq"].copy()
+    zq[0, 2, 0] = np.inf  # every verifier row is read
+    assert run(zq=zq)["seq_status"][0] == 2
+    assert run(T=np.array([np.nan]))["seq_status"][0] == 2
+    # a root alone: the bonus token from q_0
+    r = orc.tree_verify(base["zq"][:, :1], base["zp"][:, :1], [-1], np.zeros((1, 1), np.int32),
+                        np.array([[0.25]]), np.ones(1), dtype="f64")
+    q0 = softmax(base["zq"][0, 0])
+    assert r["num_accepted"][0] == 0 and r["out_tokens"][0][0] == int(np.searchsorted(np.cumsum(q0), 0.25, side="right"))
+
+
 ALL_PINS = [
     pin_softmax_matches_scipy,
     pin_exact_law_small,
@@ -607,4 +760,9 @@ ALL_PINS = [
     pin_kv_exercise_rollback,
     pin_kv_bad_counts_and_overflow,
     pin_kv_planes_and_sequences_stay_apart,
+    pin_tree_exact_law,
+    pin_tree_chain_is_the_chain_verify,
+    pin_tree_worked_siblings,
+    pin_tree_greedy_rule,
+    pin_tree_invalid_inputs,
 ]

@@ -59,6 +59,25 @@ MUTANTS = [
      "src = (((size_t)p * B + b) * N + k) * row_bytes;", "src = (((size_t)b * P + p) * N + k) * row_bytes;"),
     ("kv bad count not reported", "if (a > N) {", "if (a > N + 1) {"),
     ("kv invalid verify commits", "if (a < 0)\n            continue;", "if (a < -1)\n            continue;"),
+    ("tree: sibling residual skipped", "if (R > 0.0)\n                for (int k = 0; k < V; k++) {",
+     "if (0)\n                for (int k = 0; k < V; k++) {"),
+    ("tree: residual not normalised", "r[k] = (diff > 0.0 ? diff : 0.0) / R;", "r[k] = (diff > 0.0 ? diff : 0.0);"),
+    ("tree: siblings tried in reverse order",
+     "for (int c = n + 1; c <= M && next < 0; c++) {\n            if (par[c] != n)\n                continue;\n            const int x",
+     "for (int c = M; c > n && next < 0; c--) {\n            if (par[c] != n)\n                continue;\n            const int x"),
+    ("tree: final sample reuses the first child's uniform",
+     "out[depth] = orc_inverse_cdf(r, V, a->u[row0], &smargin);",
+     "out[depth] = orc_inverse_cdf(r, V, a->u[row0 + (M > 0)], &smargin);"),
+    ("tree: a node may be its own parent", "if (par[n] < 0 || par[n] >= n)", "if (par[n] < 0 || par[n] > n)"),
+    ("tree: leaves' draft rows validated", "if (!greedy && has_child && !(status & ORC_SEQ_BAD_TREE) &&",
+     "if (!greedy && !(status & ORC_SEQ_BAD_TREE) &&"),
+    ("tree: zero draft probability rejects", "if (p[x] == 0.0) {\n                accept = 1;",
+     "if (p[x] == 0.0) {\n                accept = 0;"),
+    ("tree: greedy takes the last matching child",
+     "for (int c = n + 1; c <= M && next < 0; c++) {\n                if (par[c] != n)",
+     "for (int c = n + 1; c <= M; c++) {\n                if (par[c] != n)"),
+    ("tree: bonus from the parent's row at a leaf", "r[k] = orc_prob(orc_logit(a->target, a->dtype, (row0 + n) * (size_t)V + k), mq, Sq, T);",
+     "r[k] = orc_prob(orc_logit(a->target, a->dtype, (row0 + (n ? par[n] : 0)) * (size_t)V + k), mq, Sq, T);"),
 ]
 
 
