@@ -51,7 +51,8 @@ typedef enum {
     SV_ERR_BAD_TOKEN = 6,   /* device: some draft token was outside [0, V) */
     SV_ERR_BAD_VALUE = 7,   /* device: NaN/+inf/all -inf logits, or NaN/+inf/subnormal temperature */
     SV_ERR_TIMEOUT = 8,     /* device: a bounded wait inside the kernel gave up */
-    SV_ERR_TOO_LARGE = 9    /* spec_verify_run_noalloc: batch beyond its fixed scratch */
+    SV_ERR_TOO_LARGE = 9,   /* spec_verify_run_noalloc: batch beyond its fixed scratch */
+    SV_ERR_BAD_TREE = 10    /* device: a parent array broke parent[0] = -1, 0 <= parent[n] < n */
 } sv_status;
 
 typedef enum { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
@@ -122,6 +123,51 @@ sv_status spec_verify_run_debug(spec_verify_ctx *ctx, const void *target_logits,
  * read fails.
  */
 sv_status spec_verify_get_status(spec_verify_ctx *ctx);
+
+/*
+ * Tree verification: B candidate trees of M+1 nodes each, node 0 being the
+ * committed context (the pages name candidate trees: "Speculative decoding --
+ * draft, verify, repeat", sections on Medusa, with its tree attention, and on
+ * EAGLE, with EAGLE-2's dynamic draft trees; they state no rule for a node
+ * with several candidates, so this follows the plainest one that keeps the
+ * output distributed as the verifier's: the children of a node are taken to
+ * be independent draws from the draft distribution at that node and are tried
+ * in index order, each rejection replacing the current verifier distribution
+ * by the normalised residual max(0, r - p) / sum max(0, r - p); an accepted
+ * child becomes the current node; when no child passes, the token is drawn
+ * from the last residual (from q of the node at a leaf).  A tree whose nodes
+ * form one chain gives exactly spec_verify_run's result.
+ *
+ * Arguments (device memory, caller-owned, contiguous; per sequence b, node n):
+ *   target_logits [B, M+1, V]  verifier logits after node n's path
+ *   draft_logits  [B, M+1, V]  draft logits at node n (the distribution its
+ *                              children were drawn from); rows of leaves are
+ *                              not read; may be NULL when greedy or M == 0
+ *   parent        int32 [B, M+1]  parent[b][0] = -1, 0 <= parent[b][n] < n
+ *   draft_tokens  int32 [B, M+1]  the token of node n (entry 0 unused)
+ *   uniforms      float [B, M+1]  entry n >= 1: the accept test of node n;
+ *                                 entry 0: the final sample
+ *   temperature   float [B]; T <= 0 (or greedy != 0) selects greedy: accept
+ *                 the first child whose token is the verifier's argmax
+ *                 (lowest index on ties), emit the argmax where none is
+ *   out_tokens    int32 [B, M+1]  the accepted path's tokens, then the drawn
+ *                                 token, then -1
+ *   path_nodes    int32 [B, M+1]  the accepted path's node ids, then -1
+ *   num_accepted  int32 [B]       path length (-1 for an invalid sequence)
+ *   target_row_stats, draft_row_stats  float [B, M+1, 2] (m, S) per node, or
+ *                 NULL; written for every node (draft: nodes with children)
+ * Requires B <= max_B, M <= max_N of the context, M + 1 <= 1024 and
+ * V*elt <= 2 MiB.  Invalid sequences (a bad token, a bad parent array, a row
+ * with NaN/+inf or only -inf among those read, a bad temperature) emit -1
+ * everywhere and set the context's status (SV_ERR_BAD_TREE for the parent
+ * array).  Two launches on `stream`; nothing is allocated.  The acceptance
+ * counters count path lengths.
+ */
+sv_status spec_verify_tree_run(spec_verify_ctx *ctx, const void *target_logits, const void *draft_logits,
+                               const int32_t *parent, const int32_t *draft_tokens, const float *uniforms,
+                               const float *temperature, int greedy, int B, int M, int32_t *out_tokens,
+                               int32_t *path_nodes, int32_t *num_accepted, float *target_row_stats,
+                               float *draft_row_stats, void *stream);
 
 /*
  * Acceptance telemetry (how many drafts each verify accepted, the quantity

@@ -25,6 +25,7 @@ SV_ERR_BAD_TOKEN = 6
 SV_ERR_BAD_VALUE = 7
 SV_ERR_TIMEOUT = 8
 SV_ERR_TOO_LARGE = 9
+SV_ERR_BAD_TREE = 10
 
 SV_F32 = 0
 SV_BF16 = 1
@@ -48,6 +49,7 @@ _SIGNATURES = [
     ("spec_verify_profile_read", _I, [_P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double),
                                       ctypes.POINTER(_I)]),
     ("spec_verify_kv_commit", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, ctypes.c_size_t, _P]),
+    ("spec_verify_tree_run", _I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
 ]
 
 SV_KV_OVERFLOW = 1
@@ -153,6 +155,14 @@ def spec_verify_profile_read(ctx):
     a, b, n = ctypes.c_double(), ctypes.c_double(), _I()
     st = load().spec_verify_profile_read(ctx, ctypes.byref(a), ctypes.byref(b), ctypes.byref(n))
     return st, a.value, b.value, n.value
+
+
+def spec_verify_tree_run(ctx, target, draft, parent, draft_tokens, uniforms, temperature, greedy, B, M,
+                         out_tokens, path_nodes, num_accepted, target_row_stats, draft_row_stats, stream) -> int:
+    """Verify B candidate trees of M+1 nodes (device pointers; asynchronous)."""
+    return load().spec_verify_tree_run(ctx, target, draft, parent, draft_tokens, uniforms, temperature,
+                                       int(greedy), B, M, out_tokens, path_nodes, num_accepted,
+                                       target_row_stats, draft_row_stats, stream)
 
 
 def spec_verify_kv_commit(scratch, cache, cache_len, num_accepted, status, planes, B, N, max_len, row_bytes,
@@ -264,6 +274,40 @@ class SpecVerify:
         if st != SV_OK:
             raise SpecVerifyError(st, "spec_verify_run")
         return out_tokens, num_accepted
+
+    def tree_run(self, target, draft, parent, tokens, uniforms, temperature, greedy=False, out_tokens=None,
+                 path_nodes=None, num_accepted=None, stream=None, stats=None):
+        """Tree verification; returns (out_tokens [B, M+1], path_nodes [B, M+1],
+        num_accepted [B]) without synchronising.  ``stats`` may hold
+        "target_row_stats" / "draft_row_stats" float32 [B, M+1, 2] tensors."""
+        import torch
+        B, M1, V = target.shape
+        M = M1 - 1
+        want = torch.bfloat16 if self.dtype == "bf16" else torch.float32
+        if target.dtype != want or V != self.V or not target.is_contiguous():
+            raise ValueError("target logits must be contiguous [B, M+1, V] of the context's dtype")
+        if draft is not None and (draft.shape != target.shape or draft.dtype != want or not draft.is_contiguous()):
+            raise ValueError("draft logits must match the target's shape and dtype")
+        for name, t, dt in (("parent", parent, torch.int32), ("tokens", tokens, torch.int32),
+                            ("uniforms", uniforms, torch.float32)):
+            if t is not None and (t.shape != (B, M + 1) or t.dtype != dt or not t.is_contiguous()):
+                raise ValueError(f"{name} must be contiguous {dt} of shape ({B}, {M + 1})")
+        dev = target.device
+        if out_tokens is None:
+            out_tokens = torch.empty((B, M + 1), dtype=torch.int32, device=dev)
+        if path_nodes is None:
+            path_nodes = torch.empty((B, M + 1), dtype=torch.int32, device=dev)
+        if num_accepted is None:
+            num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+        s = stream if stream is not None else torch.cuda.current_stream(dev)
+        stats = stats or {}
+        st = spec_verify_tree_run(self.ctx, _ptr(target), _ptr(draft), _ptr(parent), _ptr(tokens), _ptr(uniforms),
+                                  _ptr(temperature), greedy, B, M, _ptr(out_tokens), _ptr(path_nodes),
+                                  _ptr(num_accepted), _ptr(stats.get("target_row_stats")),
+                                  _ptr(stats.get("draft_row_stats")), s.cuda_stream)
+        if st != SV_OK:
+            raise SpecVerifyError(st, "spec_verify_tree_run")
+        return out_tokens, path_nodes, num_accepted
 
     def debug_buffers(self, B: int, N: int, device="cuda"):
         import torch

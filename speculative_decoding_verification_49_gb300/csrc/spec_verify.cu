@@ -60,6 +60,7 @@ constexpr int kNoReject = 0x7f7f7f7f;        // byte pattern 0x7f: memset-able
 constexpr int kErrBadToken = 1;
 constexpr int kErrBadValue = 2;
 constexpr int kErrTimeout = 4;
+constexpr int kErrBadTree = 8;
 
 enum { MODE_INVALID = 0, MODE_GREEDY = 1, MODE_SAMPLED = 2 };
 enum { RES_DIFF = 0, RES_Q = 1 };
@@ -86,6 +87,9 @@ struct SvParams {
     int *status;      // sticky error bits of the context
     unsigned long long *hist;          // [N+1] sequences by accepted drafts (may be NULL)
     unsigned long long *hist_invalid;  // sequences that were invalid
+    // tree verification (N is then the node count M; rows are per node)
+    const int32_t *parent;  // [B][M+1]
+    int32_t *path;          // [B][M+1] accepted node ids
     int B, N, V, greedy;
 };
 
@@ -107,6 +111,7 @@ struct CtlA {
     float gv;                      // greedy partial
     int gi, gnan;
     float zq_d, zp_d, u_i;         // the decision's inputs
+    int has_child;                 // tree: the node has children (its draft row is read)
     float red_m[kConsWarps], red_s[kConsWarps], red_m2[kConsWarps], red_s2[kConsWarps];
     int red_i[kConsWarps], red_n[kConsWarps];
 };
@@ -525,7 +530,7 @@ __device__ __forceinline__ Chunk chunk_of(int NV, uint32_t rank, uint32_t C)
 // Positions are taken in descending order (all sequences at position N, then
 // N-1, ..., then 0) so that position 0, where most first rejections happen,
 // is read last and is still in L2 when kernel B samples there.
-template <int DT>
+template <int DT, bool TREE>
 __global__ void __launch_bounds__(kThreads, 4) sv_rows_kernel(const SvParams p)
 {
     constexpr int VE = Elt<DT>::kPerVec;
@@ -545,24 +550,45 @@ __global__ void __launch_bounds__(kThreads, 4) sv_rows_kernel(const SvParams p)
 
     float T;
     const int mode = sequence_mode(p, b, T);
-    const bool has_draft = (mode == MODE_SAMPLED) && (i < N);
-    const int d = (i < N) ? p.tokens[(size_t)b * N + i] : 0;
-    const bool bad_d = (i < N) && (d < 0 || d >= V);
+    const size_t trow = (size_t)b * (N + 1) + i;
+    const size_t drow = TREE ? trow : (size_t)b * N + i;
+    int d = 0;
+    bool bad_d = false, bad_tree = false;
+    if constexpr (TREE) {
+        // node i: its token (i >= 1) and its parent must be valid
+        if (i > 0) {
+            d = p.tokens[trow];
+            bad_d = d < 0 || d >= V;
+        }
+        const int par = p.parent[trow];
+        bad_tree = (i == 0) ? (par != -1) : (par < 0 || par >= i);
+    } else {
+        d = (i < N) ? p.tokens[(size_t)b * N + i] : 0;
+        bad_d = (i < N) && (d < 0 || d >= V);
+    }
 
     const Chunk ch = chunk_of(V / VE, rank, C);
-    const size_t trow = (size_t)b * (N + 1) + i;
-    const size_t drow = (size_t)b * N + i;
     const size_t row_vecs = (size_t)(V / VE);
     const uint4 *tsrc = static_cast<const uint4 *>(p.target) + trow * row_vecs + ch.v0;
-    const uint4 *dsrc = has_draft ? static_cast<const uint4 *>(p.draft) + drow * row_vecs + ch.v0 : nullptr;
 
     if (tid == 0) {
         ring_init(ctl.ring);
         ctl.cf = (mode == MODE_SAMPLED) ? (float)(kLog2e / (double)T) : 0.0f;  // log2(e)/T
     }
+    if constexpr (TREE) {
+        // a node's draft row is read only when the node has children
+        if (warp == kProducerWarp) {
+            bool any = false;
+            for (int c = i + 1 + lane; c <= N; c += 32)
+                any |= p.parent[(size_t)b * (N + 1) + c] == i;
+            any = __any_sync(0xffffffffu, any);
+            if (lane == 0)
+                ctl.has_child = any ? 1 : 0;
+        }
+    }
     // The decision's inputs are loaded by an idle lane of the producer warp at
     // the start and parked in shared memory after pass 1.
-    const bool prefetcher = rank == 0 && tid == 32 * kProducerWarp + 1;
+    const bool prefetcher = !TREE && rank == 0 && tid == 32 * kProducerWarp + 1;
     float pre_zq = 0.0f, pre_zp = 0.0f, pre_u = 0.0f;
     if (prefetcher && mode == MODE_SAMPLED && i < N && !bad_d) {
         pre_zq = logit_at<DT>(p.target, trow * (size_t)V + d);
@@ -571,6 +597,8 @@ __global__ void __launch_bounds__(kThreads, 4) sv_rows_kernel(const SvParams p)
     }
     __syncthreads();
     const float cf = ctl.cf;
+    const bool has_draft = (mode == MODE_SAMPLED) && (TREE ? ctl.has_child != 0 : i < N);
+    const uint4 *dsrc = has_draft ? static_cast<const uint4 *>(p.draft) + drow * row_vecs + ch.v0 : nullptr;
 
     // ---- pass 1: stream the chunk of both rows once
     Online2 ot2{-INFINITY, 0ull}, od2{-INFINITY, 0ull};  // 0ull = (+0.0f, +0.0f)
@@ -673,11 +701,11 @@ __global__ void __launch_bounds__(kThreads, 4) sv_rows_kernel(const SvParams p)
             }
             a = warp_argmax(a);
             if (lane == 0) {
-                int errb = bad_d ? kErrBadToken : 0;
+                int errb = (bad_d ? kErrBadToken : 0) | (bad_tree ? kErrBadTree : 0);
                 if (a.nan || a.v == INFINITY || a.v == -INFINITY)
                     errb |= kErrBadValue;
                 p.ws_tok[trow] = a.i;
-                if (i < N && d != a.i)
+                if (!TREE && i < N && d != a.i)
                     atomicMin(&p.ws_first[b], i);
                 if (errb)
                     atomicOr(&p.ws_err[b], errb);
@@ -685,7 +713,7 @@ __global__ void __launch_bounds__(kThreads, 4) sv_rows_kernel(const SvParams p)
                     p.tstats[trow * 2 + 0] = a.v;
                     p.tstats[trow * 2 + 1] = NAN;
                 }
-                if (i < N) {
+                if (!TREE && i < N) {
                     if (p.q_at)
                         p.q_at[drow] = NAN;
                     if (p.p_at)
@@ -709,14 +737,14 @@ __global__ void __launch_bounds__(kThreads, 4) sv_rows_kernel(const SvParams p)
             t = warp_merge(t, cf);
             e = warp_merge(e, cf);
             if (lane == 0) {
-                int errb = bad_d ? kErrBadToken : 0;
+                int errb = (bad_d ? kErrBadToken : 0) | (bad_tree ? kErrBadTree : 0);
                 const float mq = t.m, Sq = t.s, mp = e.m, Sp = e.s;
                 bool valid = isfinite(mq) && isfinite(Sq) && Sq > 0.0f;
                 if (has_draft)
                     valid = valid && isfinite(mp) && isfinite(Sp) && Sp > 0.0f;
                 if (!valid) {
                     errb |= kErrBadValue;
-                } else if (i < N && !bad_d) {
+                } else if (!TREE && i < N && !bad_d) {
                     // accept iff p(d) == 0 or u < min(1, q(d)/p(d)), with
                     // q(d)/p(d) = 2^L * Sp/Sq, L = ((zq-mq) - (zp-mp)) log2(e)/T
                     const float zq = ctl.zq_d, zp = ctl.zp_d;
@@ -764,7 +792,7 @@ __global__ void __launch_bounds__(kThreads, 4) sv_rows_kernel(const SvParams p)
                 }
             }
         } else if (lane == 0) {
-            atomicOr(&p.ws_err[b], kErrBadValue | (bad_d ? kErrBadToken : 0));
+            atomicOr(&p.ws_err[b], kErrBadValue | (bad_d ? kErrBadToken : 0) | (bad_tree ? kErrBadTree : 0));
         }
     }
     if (tid == 0 && ctl.ring.abort)
@@ -1226,6 +1254,484 @@ __global__ void __launch_bounds__(kPickThreads) sv_pick_kernel(const SvParams p)
     }
 }
 
+// =============================================================================
+// Tree verification: the walk (kernel W), one CTA per sequence
+// =============================================================================
+//
+// Kernel A (TREE) has left, per node, the row statistics (mq, Sq, mp, Sp), or
+// the argmax for greedy sequences, and the error bits.  The walk starts at the
+// root; at node n it tries n's children in index order.  With r_0 = q_n and
+// r_{k+1} = (r_k - p_n)+ / R_{k+1}, R_{k+1} = sum (r_k - p_n)+, child c (the
+// (k+1)-th tried) passes iff p_n(x) == 0 or u_c < min(1, r_k(x) / p_n(x)),
+// x = its token.  A pass moves the walk to c; a rejection costs one pass over
+// the row pair of n through the TMA ring, which yields the slice masses of
+// (r_k - p_n)+ and so R_{k+1} (when it is 0, r_k stays).  When no child
+// passes, the token is drawn from r_k by inverse CDF at u[0]: the slice masses
+// of the last rejection pass are r_k's up to the factor R_k, otherwise one
+// more pass computes them.  The element arithmetic is explicitly rounded and
+// identical in every pass and in the recomputation of the chosen slice.
+
+constexpr int kStagesW = 8;                 // ring depth of the walk: 128 KiB of row pairs in flight
+constexpr int kMaxTreeNodes = 1024;         // nodes per tree (root included)
+constexpr int kMaxWalkSlices = 512;         // slices of one row: V*elt <= 2 MiB
+
+struct CtlW {
+    Ring<kStagesW> ring;
+    float shares[kMaxWalkSlices * kConsWarps];  // warp shares of every slice of the current pass
+    float slice[kMaxWalkSlices];                // slice masses
+    float invR[kMaxTreeNodes];                  // 1/R_1 .. 1/R_k of the current node
+    float incl[kConsThreads];
+    int kids[kMaxTreeNodes];
+    int nkids, accept, sstar, token;
+    float Rt, x1, cf;
+};
+
+constexpr size_t kSmemW = ring_bytes(kStagesW) + sizeof(CtlW);
+
+// r_k (diff = false) or (r_k - p)+ (diff = true) for the VE elements of one
+// 16-byte vector; pairs of adjacent elements travel as one f32x2.
+template <int DT>
+__device__ __forceinline__ void tree_vec(const uint4 vt, const uint4 vd, bool diff, int k, const float *invR,
+                                         float mq, float isq, float mp, float isp, float cf, float *r)
+{
+    constexpr int NE = Elt<DT>::kPerVec;
+    constexpr int NP = NE / 2;
+    const uint32_t wt[4] = {vt.x, vt.y, vt.z, vt.w};
+    const uint32_t wd[4] = {vd.x, vd.y, vd.z, vd.w};
+    const unsigned long long Cf = sv::pack2(cf, cf);
+    const unsigned long long Mq = sv::pack2(mq, mq), Iq = sv::pack2(isq, isq);
+    const unsigned long long Mp = sv::pack2(mp, mp), Ip = sv::pack2(isp, isp);
+    const bool need_p = diff || k > 0;
+#pragma unroll
+    for (int e = 0; e < NP; ++e) {
+        unsigned long long zt, zd;
+        if constexpr (DT == SV_BF16) {
+            zt = sv::pack2(__uint_as_float(wt[e] << 16), __uint_as_float(wt[e] & 0xffff0000u));
+            zd = sv::pack2(__uint_as_float(wd[e] << 16), __uint_as_float(wd[e] & 0xffff0000u));
+        } else {
+            zt = sv::pack2(__uint_as_float(wt[2 * e]), __uint_as_float(wt[2 * e + 1]));
+            zd = sv::pack2(__uint_as_float(wd[2 * e]), __uint_as_float(wd[2 * e + 1]));
+        }
+        float a0, a1;
+        sv::unpack2(sv::mul2(sv::sub2(zt, Mq), Cf), a0, a1);
+        unsigned long long x = sv::mul2(sv::pack2(sv::ex2(a0), sv::ex2(a1)), Iq);
+        unsigned long long pk = 0ull;
+        if (need_p) {
+            sv::unpack2(sv::mul2(sv::sub2(zd, Mp), Cf), a0, a1);
+            pk = sv::mul2(sv::pack2(sv::ex2(a0), sv::ex2(a1)), Ip);
+        }
+        for (int j = 0; j < k; ++j) {
+            float d0, d1;
+            sv::unpack2(sv::sub2(x, pk), d0, d1);
+            const float ir = invR[j];
+            x = sv::mul2(sv::pack2(fmaxf(d0, 0.0f), fmaxf(d1, 0.0f)), sv::pack2(ir, ir));
+        }
+        if (diff) {
+            float d0, d1;
+            sv::unpack2(sv::sub2(x, pk), d0, d1);
+            r[2 * e] = fmaxf(d0, 0.0f);
+            r[2 * e + 1] = fmaxf(d1, 0.0f);
+        } else {
+            sv::unpack2(x, r[2 * e], r[2 * e + 1]);
+        }
+    }
+}
+
+// The same arithmetic for one element: r_k(x) and p(x).
+__device__ __forceinline__ void tree_elem(float zq, float zp, int k, const float *invR, float mq, float isq,
+                                          float mp, float isp, float cf, float &rk, float &px)
+{
+    float x = __fmul_rn(sv::ex2(__fmul_rn(__fsub_rn(zq, mq), cf)), isq);
+    px = __fmul_rn(sv::ex2(__fmul_rn(__fsub_rn(zp, mp), cf)), isp);
+    for (int j = 0; j < k; ++j)
+        x = __fmul_rn(fmaxf(__fsub_rn(x, px), 0.0f), invR[j]);
+    rk = x;
+}
+
+// Chain test at the first child: u < min(1, q(x)/p(x)) in the log domain, as
+// kernel A decides it.
+__device__ __forceinline__ bool first_child_test(float zq, float zp, float mq, float Sq, float mp, float Sp, float T,
+                                                 double u)
+{
+    if (zp == -INFINITY)
+        return true;  // p(x) = 0
+    if (zq == -INFINITY)
+        return false;  // q(x) = 0 and u < 0 never holds
+    const double invT = 1.0 / (double)T;
+    const double xq = ((double)zq - (double)mq) * invT;
+    const double xp = ((double)zp - (double)mp) * invT;
+    if (xq < -700.0 || xp < -700.0) {
+        const double qd = exp(xq) / (double)Sq, pd = exp(xp) / (double)Sp;
+        return (pd == 0.0) || (u < fmin(1.0, qd / pd));
+    }
+    const double L = (xq - xp) * kLog2e;
+    const double fl = floor(L);
+    const float frac = (float)(L - fl);
+    const double ratio = ldexp((double)(sv::ex2(frac) * (Sp / Sq)), (int)fl);
+    return u < fmin(1.0, ratio);
+}
+
+// One pass over the row pair of a node: the slice masses of r_k (diff false)
+// or (r_k - p)+ (diff true) into w.slice, their total into w.Rt.  Every thread
+// of the CTA calls it; g is the ring position, advanced by the pass.
+template <int DT>
+__device__ void walk_mass_pass(CtlW &w, unsigned char *ring, uint32_t &g, const uint4 *tsrc, const uint4 *dsrc,
+                               int NV, bool diff, int k, float mq, float isq, float mp, float isp, float cf)
+{
+    constexpr int VE = Elt<DT>::kPerVec;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int NT = (NV + kTileVecs - 1) / kTileVecs;
+    const int S = (NV + kSliceVecs - 1) / kSliceVecs;
+    if (warp == kProducerWarp) {
+        if (lane == 0)
+            produce(w.ring, ring, tsrc, dsrc, NV, 0, NT, g);
+        __syncwarp();
+    } else {
+        for (int t = 0; t < NT; ++t) {
+            const uint32_t gt = g + (uint32_t)t;
+            if (consume_wait(w.ring, gt)) {
+                const unsigned char *stage = ring + (gt % kStagesW) * (2 * kTileBytes);
+#pragma unroll
+                for (int q = 0; q < kVPT; ++q) {
+                    const int sv_ = q * kSliceVecs + tid;
+                    const int vec = t * kTileVecs + sv_;
+                    float part = 0.0f;
+                    if (vec < NV) {
+                        float r[VE];
+                        const uint4 vd = dsrc ? reinterpret_cast<const uint4 *>(stage + kTileBytes)[sv_]
+                                              : make_uint4(0, 0, 0, 0);
+                        tree_vec<DT>(reinterpret_cast<const uint4 *>(stage)[sv_], vd, diff, k, w.invR, mq, isq, mp,
+                                     isp, cf, r);
+#pragma unroll
+                        for (int e = 0; e < VE; ++e)
+                            part = __fadd_rn(part, r[e]);
+                    }
+                    const float incl = warp_incl_scan(part, lane);
+                    const int sl = t * kVPT + q;
+                    if (lane == 31 && sl < S)
+                        w.shares[sl * kConsWarps + warp] = incl;
+                }
+            } else {
+                w.ring.abort = 1;
+            }
+            consume_release(w.ring, gt, lane);
+        }
+    }
+    g += (uint32_t)NT;
+    __syncthreads();
+    for (int sl = tid; sl < S; sl += kThreads) {
+        float tot = 0.0f;
+        for (int q = 0; q < kConsWarps; ++q)
+            tot = __fadd_rn(tot, w.shares[sl * kConsWarps + q]);
+        w.slice[sl] = tot;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        float carry = 0.0f;
+        for (int c0 = 0; c0 < S; c0 += 32) {
+            const int c = c0 + lane;
+            const float m = (c < S) ? w.slice[c] : 0.0f;
+            carry = __shfl_sync(0xffffffffu, __fadd_rn(warp_incl_scan(m, lane), carry), 31);
+        }
+        if (lane == 0)
+            w.Rt = carry;
+    }
+    __syncthreads();
+}
+
+// Inverse CDF over the slice masses in w.slice (total w.Rt) at u: the slice,
+// then (recomputing that slice with the pass's arithmetic) the warp, lane and
+// element.  Every thread calls it; returns the token.
+template <int DT>
+__device__ int walk_pick(CtlW &w, const uint4 *tsrc, const uint4 *dsrc, int NV, bool diff, int k, float mq, float isq,
+                         float mp, float isp, float cf, float u)
+{
+    constexpr int VE = Elt<DT>::kPerVec;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int S = (NV + kSliceVecs - 1) / kSliceVecs;
+    if (warp == 0) {
+        const float x = __fmul_rn(u, w.Rt);
+        int cs = -1;
+        float x1 = INFINITY, run = 0.0f;
+        for (int c0 = 0; c0 < S && cs < 0; c0 += 32) {
+            const int c = c0 + lane;
+            const float m = (c < S) ? w.slice[c] : 0.0f;
+            const float inc = __fadd_rn(warp_incl_scan(m, lane), run);
+            const unsigned hit = __ballot_sync(0xffffffffu, c < S && x < inc);
+            if (hit) {
+                const int l = __ffs(hit) - 1;
+                const float prev = __shfl_sync(0xffffffffu, inc, l > 0 ? l - 1 : 0);
+                cs = c0 + l;
+                x1 = __fsub_rn(x, l > 0 ? prev : run);
+            }
+            run = __shfl_sync(0xffffffffu, inc, 31);
+        }
+        if (cs < 0) {  // rounding: the last slice that has mass
+            for (int c0 = ((S - 1) / 32) * 32; c0 >= 0 && cs < 0; c0 -= 32) {
+                const int c = c0 + lane;
+                const unsigned m = __ballot_sync(0xffffffffu, c < S && w.slice[c] > 0.0f);
+                if (m)
+                    cs = c0 + 31 - __clz(m);
+            }
+            if (cs < 0)
+                cs = S - 1;
+            x1 = INFINITY;
+        }
+        if (lane == 0) {
+            w.sstar = cs;
+            w.x1 = x1;
+        }
+    }
+    __syncthreads();
+    const int ss = w.sstar;
+    float r[VE];
+#pragma unroll
+    for (int e = 0; e < VE; ++e)
+        r[e] = 0.0f;
+    if (warp < kConsWarps) {
+        const int vec = ss * kSliceVecs + tid;
+        float part = 0.0f;
+        if (vec < NV) {
+            const uint4 vd = dsrc ? __ldcg(dsrc + vec) : make_uint4(0, 0, 0, 0);
+            tree_vec<DT>(__ldcg(tsrc + vec), vd, diff, k, w.invR, mq, isq, mp, isp, cf, r);
+#pragma unroll
+            for (int e = 0; e < VE; ++e)
+                part = __fadd_rn(part, r[e]);
+        }
+        w.incl[tid] = warp_incl_scan(part, lane);
+    }
+    __syncthreads();
+    const float x1 = w.x1;
+    if (warp == 0) {
+        int sel = -1;
+        float xl = 0.0f;
+        if (x1 != INFINITY) {
+            const float wt = (lane < kConsWarps) ? w.incl[lane * 32 + 31] : 0.0f;
+            float wc = 0.0f, wprev = 0.0f;
+            int ws = -1;
+            for (int q = 0; q < kConsWarps; ++q) {
+                const float wtw = __shfl_sync(0xffffffffu, wt, q);
+                const float next = __fadd_rn(wc, wtw);
+                if (ws < 0 && x1 < next) {
+                    ws = q;
+                    wprev = wc;
+                }
+                wc = next;
+            }
+            if (ws >= 0) {
+                const float xw = __fsub_rn(x1, wprev);
+                const float li = w.incl[ws * 32 + lane];
+                const unsigned ml = __ballot_sync(0xffffffffu, xw < li);
+                if (ml) {
+                    const int ls = __ffs(ml) - 1;
+                    const float lprev = __shfl_sync(0xffffffffu, li, ls > 0 ? ls - 1 : 0);
+                    sel = ws * 32 + ls;
+                    xl = __fsub_rn(xw, ls > 0 ? lprev : 0.0f);
+                }
+            }
+        }
+        if (lane == 0) {
+            w.sstar = sel;  // reused: the selected thread
+            w.x1 = xl;
+            w.token = -1;
+        }
+    }
+    __syncthreads();
+    const int sel = w.sstar;
+    if (sel >= 0 && tid == sel) {
+        float acc = 0.0f;
+        for (int e = 0; e < VE; ++e) {
+            acc = __fadd_rn(acc, r[e]);
+            if (w.x1 < acc) {
+                w.token = (ss * kSliceVecs + tid) * VE + e;
+                break;
+            }
+        }
+    }
+    __syncthreads();
+    if (w.token < 0) {
+        // rounding: the last element of slice s* that carries mass
+        if (tid == 0)
+            w.sstar = -1;
+        __syncthreads();
+        if (warp < kConsWarps) {
+            for (int e = VE - 1; e >= 0; --e)
+                if (r[e] > 0.0f) {
+                    atomicMax(&w.sstar, (ss * kSliceVecs + tid) * VE + e);
+                    break;
+                }
+        }
+        __syncthreads();
+        if (tid == 0)
+            w.token = w.sstar >= 0 ? w.sstar : min(NV, (ss + 1) * kSliceVecs) * VE - 1;
+        __syncthreads();
+    }
+    return w.token;
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 1) sv_tree_walk_kernel(const SvParams p)
+{
+    constexpr int VE = Elt<DT>::kPerVec;
+    extern __shared__ __align__(128) unsigned char smem[];
+    unsigned char *ring = smem;
+    CtlW &w = *reinterpret_cast<CtlW *>(smem + ring_bytes(kStagesW));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int b = blockIdx.x, M = p.N, V = p.V, NV = V / VE;
+    const size_t row0 = (size_t)b * (M + 1);
+    const int32_t *par = p.parent + row0;
+    const int32_t *tok = p.tokens + row0;
+    int32_t *out = p.out + row0;
+    int32_t *path = p.path + row0;
+
+    float T;
+    const int mode = sequence_mode(p, b, T);
+    if (tid == 0) {
+        ring_init(w.ring);
+        w.cf = (mode == MODE_SAMPLED) ? (float)(kLog2e / (double)T) : 0.0f;
+    }
+    sv::grid_dependency_wait();  // kernel A's statistics
+    __syncthreads();
+    const int err = __ldcg(&p.ws_err[b]);
+    if (err || mode == MODE_INVALID) {
+        if (tid == 0) {
+            for (int q = 0; q <= M; ++q) {
+                out[q] = -1;
+                path[q] = -1;
+            }
+            p.nacc[b] = -1;
+            atomicOr(p.status, err ? err : kErrBadValue);
+            if (p.hist)
+                atomicAdd(p.hist_invalid, 1ull);
+            p.ws_err[b] = 0;
+        }
+        return;
+    }
+    int depth = 0;
+    if (mode == MODE_GREEDY) {
+        if (tid == 0) {
+            int n = 0;
+            for (;;) {
+                const int an = __ldcg(&p.ws_tok[row0 + n]);
+                int next = -1;
+                for (int c = n + 1; c <= M && next < 0; ++c)
+                    if (par[c] == n && tok[c] == an)
+                        next = c;
+                if (next < 0) {
+                    out[depth] = an;
+                    break;
+                }
+                out[depth] = tok[next];
+                path[depth] = next;
+                ++depth;
+                n = next;
+            }
+        }
+    } else {
+        const float cf = w.cf;
+        const float u0 = p.u[row0];
+        uint32_t g = 0;
+        int n = 0;
+        for (;;) {
+            const float *st = p.ws_stats + (row0 + n) * 4;
+            const float mq = __ldcg(st + 0), Sq = __ldcg(st + 1), mp = __ldcg(st + 2), Sp = __ldcg(st + 3);
+            const float isq = 1.0f / Sq;
+            const uint4 *tsrc = static_cast<const uint4 *>(p.target) + (row0 + n) * (size_t)NV;
+            const uint4 *dsrc = static_cast<const uint4 *>(p.draft) + (row0 + n) * (size_t)NV;
+            // children of n, in index order
+            if (warp == 0) {
+                int cnt = 0;
+                for (int c0 = n + 1; c0 <= M; c0 += 32) {
+                    const int c = c0 + lane;
+                    const bool is = c <= M && par[c] == n;
+                    const unsigned m = __ballot_sync(0xffffffffu, is);
+                    if (is)
+                        w.kids[cnt + __popc(m & ((1u << lane) - 1u))] = c;
+                    cnt += __popc(m);
+                }
+                if (lane == 0)
+                    w.nkids = cnt;
+            }
+            __syncthreads();
+            const int nk = w.nkids;
+            const float isp = nk ? 1.0f / Sp : 0.0f;
+            int k = 0, accepted = -1;
+            bool masses_ready = false;  // w.slice holds r_k's masses up to a factor
+            for (int ci = 0; ci < nk; ++ci) {
+                const int c = w.kids[ci];
+                if (tid == 0) {
+                    const int x = tok[c];
+                    const float zq = logit_at<DT>(p.target, (row0 + n) * (size_t)V + x);
+                    const float zp = logit_at<DT>(p.draft, (row0 + n) * (size_t)V + x);
+                    const double uc = (double)p.u[row0 + c];
+                    bool acc;
+                    if (k == 0) {
+                        acc = first_child_test(zq, zp, mq, Sq, mp, Sp, T, uc);
+                    } else {
+                        float rk, px;
+                        tree_elem(zq, zp, k, w.invR, mq, isq, mp, isp, cf, rk, px);
+                        acc = (zp == -INFINITY) || (px == 0.0f) || (uc < fmin(1.0, (double)rk / (double)px));
+                    }
+                    w.accept = acc ? 1 : 0;
+                }
+                __syncthreads();
+                if (w.accept) {
+                    accepted = c;
+                    break;
+                }
+                walk_mass_pass<DT>(w, ring, g, tsrc, dsrc, NV, /*diff=*/true, k, mq, isq, mp, isp, cf);
+                if (w.Rt > 0.0f) {
+                    if (tid == 0)
+                        w.invR[k] = __frcp_rn(w.Rt);
+                    ++k;
+                    masses_ready = true;
+                } else {
+                    masses_ready = false;  // the residual is empty: r_k stays
+                }
+                __syncthreads();
+            }
+            if (accepted >= 0) {
+                if (tid == 0) {
+                    out[depth] = tok[accepted];
+                    path[depth] = accepted;
+                }
+                ++depth;
+                n = accepted;
+                __syncthreads();
+                continue;
+            }
+            // the token: from r_k
+            bool diff = false;
+            int kk = k;
+            if (masses_ready) {
+                diff = true;  // the last pass: (r_{k-1} - p)+ = R_k r_k
+                kk = k - 1;
+            } else {
+                walk_mass_pass<DT>(w, ring, g, tsrc, nk ? dsrc : nullptr, NV, false, k, mq, isq, mp, isp, cf);
+            }
+            const int t = walk_pick<DT>(w, tsrc, (diff || kk > 0) ? dsrc : nullptr, NV, diff, kk, mq, isq, mp, isp,
+                                        cf, u0);
+            if (tid == 0)
+                out[depth] = t;
+            break;
+        }
+    }
+    if (tid == 0) {
+        for (int q = depth + 1; q <= M; ++q)
+            out[q] = -1;
+        for (int q = depth; q <= M; ++q)
+            path[q] = -1;
+        p.nacc[b] = depth;
+        if (p.hist)
+            atomicAdd(&p.hist[depth], 1ull);
+        p.ws_err[b] = 0;
+        if (w.ring.abort) {
+            atomicOr(p.status, kErrTimeout);
+            ring_drain(w.ring);
+        }
+    }
+}
+
 } // namespace
 
 // =============================================================================
@@ -1239,6 +1745,7 @@ struct spec_verify_ctx {
     int num_sms;
     int cluster_override;                // kernel A cluster size, 0 = automatic
     int clusters_a[kMaxCluster + 1];     // co-resident clusters of kernel A per size, 0 = none
+    int clusters_tree[kMaxCluster + 1];  // the same for kernel A over tree nodes
     void *ws;
     int mass_ctas;                       // resident CTAs of the mass kernel (all SMs)
     int *ws_first, *ws_err, *ws_tok, *status;
@@ -1280,10 +1787,14 @@ template <typename K> cudaError_t set_kernel_attrs(K kernel, size_t smem)
 
 template <int DT> cudaError_t set_attrs()
 {
-    const cudaError_t e = set_kernel_attrs(sv_rows_kernel<DT>, kSmemA);
-    if (e != cudaSuccess)
-        return e;
-    return cudaFuncSetAttribute(sv_mass_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemM);
+    cudaError_t e = set_kernel_attrs(sv_rows_kernel<DT, false>, kSmemA);
+    if (e == cudaSuccess)
+        e = set_kernel_attrs(sv_rows_kernel<DT, true>, kSmemA);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(sv_mass_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemM);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(sv_tree_walk_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemW);
+    return e;
 }
 
 // Resident CTAs of the mass kernel on the whole device.
@@ -1341,10 +1852,10 @@ template <typename K> int active_clusters(K kernel, int C, size_t smem)
 }
 
 // Co-resident clusters of kernel A for every cluster size.
-template <int DT> void query_clusters(int *a)
+template <int DT, bool TREE = false> void query_clusters(int *a)
 {
     for (int k = 1; k <= kMaxCluster; ++k)
-        a[k] = active_clusters(sv_rows_kernel<DT>, k, kSmemA);
+        a[k] = active_clusters(sv_rows_kernel<DT, TREE>, k, kSmemA);
     a[1] = a[1] > 0 ? a[1] : 1;
 }
 
@@ -1369,7 +1880,7 @@ int clamp_cluster(int C, int nv, const int *fits)
 
 // Kernel A: one CTA per position once there are about two waves of positions
 // (four CTAs per SM), else split the rows over a cluster for parallelism.
-int cluster_a(const spec_verify_ctx *c, int B, int N)
+int cluster_a(const spec_verify_ctx *c, int B, int N, bool tree = false)
 {
     if (c->cluster_override > 0)
         return c->cluster_override;
@@ -1377,7 +1888,7 @@ int cluster_a(const spec_verify_ctx *c, int B, int N)
     const long long units = (long long)B * (N + 1);
     const long long want = 8LL * c->num_sms;
     const int C = (int)((want + units - 1) / (units > 0 ? units : 1));
-    return clamp_cluster(C < 8 ? C : 8, nv, c->clusters_a);
+    return clamp_cluster(C < 8 ? C : 8, nv, tree ? c->clusters_tree : c->clusters_a);
 }
 
 sv_status run_impl(spec_verify_ctx *ctx, const void *target, const void *draft, const int32_t *tokens,
@@ -1434,6 +1945,8 @@ sv_status run_impl(spec_verify_ctx *ctx, const void *target, const void *draft, 
     prm.hist = ctx->hist;
     prm.hist_invalid = ctx->hist ? ctx->hist + ctx->max_N + 1 : nullptr;
     prm.status = ctx->status;
+    prm.parent = nullptr;
+    prm.path = nullptr;
     prm.B = B;
     prm.N = N;
     prm.V = ctx->V;
@@ -1447,8 +1960,8 @@ sv_status run_impl(spec_verify_ctx *ctx, const void *target, const void *draft, 
         cudaEventRecord(ev[0], st);
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = launch_config((unsigned)(units * CA), CA, kSmemA, st, attr);
-    cudaError_t e = (ctx->dtype == SV_BF16) ? cudaLaunchKernelEx(&cfg, sv_rows_kernel<SV_BF16>, prm)
-                                            : cudaLaunchKernelEx(&cfg, sv_rows_kernel<SV_F32>, prm);
+    cudaError_t e = (ctx->dtype == SV_BF16) ? cudaLaunchKernelEx(&cfg, sv_rows_kernel<SV_BF16, false>, prm)
+                                            : cudaLaunchKernelEx(&cfg, sv_rows_kernel<SV_F32, false>, prm);
     if (e == cudaSuccess) {
         if (ev)
             cudaEventRecord(ev[1], st);
@@ -1478,6 +1991,87 @@ sv_status run_impl(spec_verify_ctx *ctx, const void *target, const void *draft, 
         }
         if (ev && e == cudaSuccess)
             cudaEventRecord(ev[2], st);
+    }
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return SV_ERR_CUDA;
+    }
+    return SV_OK;
+}
+
+sv_status tree_run_impl(spec_verify_ctx *ctx, const void *target, const void *draft, const int32_t *parent,
+                        const int32_t *tokens, const float *u, const float *T, int greedy, int B, int M,
+                        int32_t *out, int32_t *path, int32_t *nacc, float *tstats, float *dstats, void *stream)
+{
+    if (!ctx)
+        return SV_ERR_INVALID_ARG;
+    if (B < 0 || B > ctx->max_B || M < 0 || M > ctx->max_N || M + 1 > kMaxTreeNodes)
+        return SV_ERR_INVALID_ARG;
+    if (B == 0)
+        return SV_OK;
+    if (!target || !parent || !tokens || !out || !path || !nacc)
+        return SV_ERR_INVALID_ARG;
+    if (!greedy && (!T || !u || (M > 0 && !draft)))
+        return SV_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(target) & 15u) || (draft && (reinterpret_cast<uintptr_t>(draft) & 15u)))
+        return SV_ERR_INVALID_ARG;
+    const int nv = ctx->V * elt_bytes(ctx->dtype) / 16;
+    if ((nv + kSliceVecs - 1) / kSliceVecs > kMaxWalkSlices)
+        return SV_ERR_SHAPE;
+    const int CA = cluster_a(ctx, B, M, /*tree=*/true);
+    if ((nv + CA - 1) / CA > kMaxSlices * kSliceVecs)
+        return SV_ERR_SHAPE;
+    const long long units = (long long)B * (M + 1);
+    if (units * CA > INT_MAX)
+        return SV_ERR_INVALID_ARG;
+    DeviceGuard guard(ctx->device);
+    if (!guard.ok)
+        return SV_ERR_CUDA;
+
+    SvParams prm;
+    memset(&prm, 0, sizeof prm);
+    prm.target = target;
+    prm.draft = greedy ? nullptr : draft;
+    prm.tokens = tokens;
+    prm.u = u;
+    prm.T = T;
+    prm.out = out;
+    prm.nacc = nacc;
+    prm.tstats = tstats;
+    prm.dstats = dstats;
+    prm.ws_first = ctx->ws_first;
+    prm.ws_err = ctx->ws_err;
+    prm.ws_tok = ctx->ws_tok;
+    prm.ws_stats = ctx->ws_stats;
+    prm.ws_slice = ctx->ws_slice;
+    prm.hist = ctx->hist;
+    prm.hist_invalid = ctx->hist ? ctx->hist + ctx->max_N + 1 : nullptr;
+    prm.status = ctx->status;
+    prm.parent = parent;
+    prm.path = path;
+    prm.B = B;
+    prm.N = M;
+    prm.V = ctx->V;
+    prm.greedy = greedy ? 1 : 0;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = launch_config((unsigned)(units * CA), CA, kSmemA, st, attr);
+    cudaError_t e = (ctx->dtype == SV_BF16) ? cudaLaunchKernelEx(&cfg, sv_rows_kernel<SV_BF16, true>, prm)
+                                            : cudaLaunchKernelEx(&cfg, sv_rows_kernel<SV_F32, true>, prm);
+    if (e == cudaSuccess) {
+        cudaLaunchAttribute pdl[1];
+        pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        pdl[0].val.programmaticStreamSerializationAllowed = 1;
+        cudaLaunchConfig_t cfgw = {};
+        cfgw.gridDim = dim3((unsigned)B);
+        cfgw.blockDim = dim3(kThreads);
+        cfgw.dynamicSmemBytes = kSmemW;
+        cfgw.stream = st;
+        cfgw.attrs = pdl;
+        cfgw.numAttrs = 1;
+        e = (ctx->dtype == SV_BF16) ? cudaLaunchKernelEx(&cfgw, sv_tree_walk_kernel<SV_BF16>, prm)
+                                    : cudaLaunchKernelEx(&cfgw, sv_tree_walk_kernel<SV_F32>, prm);
     }
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -1525,10 +2119,13 @@ sv_status spec_verify_create(spec_verify_ctx **out, int device, int max_B, int m
         free(c);
         return SV_ERR_CUDA;
     }
-    if (dtype == SV_BF16)
+    if (dtype == SV_BF16) {
         query_clusters<SV_BF16>(c->clusters_a);
-    else
+        query_clusters<SV_BF16, true>(c->clusters_tree);
+    } else {
         query_clusters<SV_F32>(c->clusters_a);
+        query_clusters<SV_F32, true>(c->clusters_tree);
+    }
 
     c->mass_ctas = (dtype == SV_BF16) ? mass_ctas<SV_BF16>(c->num_sms) : mass_ctas<SV_F32>(c->num_sms);
 
@@ -1583,6 +2180,16 @@ sv_status spec_verify_run_debug(spec_verify_ctx *ctx, const void *target_logits,
                     draft_row_stats);
 }
 
+sv_status spec_verify_tree_run(spec_verify_ctx *ctx, const void *target_logits, const void *draft_logits,
+                               const int32_t *parent, const int32_t *draft_tokens, const float *uniforms,
+                               const float *temperature, int greedy, int B, int M, int32_t *out_tokens,
+                               int32_t *path_nodes, int32_t *num_accepted, float *target_row_stats,
+                               float *draft_row_stats, void *stream)
+{
+    return tree_run_impl(ctx, target_logits, draft_logits, parent, draft_tokens, uniforms, temperature, greedy, B,
+                         M, out_tokens, path_nodes, num_accepted, target_row_stats, draft_row_stats, stream);
+}
+
 sv_status spec_verify_get_status(spec_verify_ctx *ctx)
 {
     if (!ctx)
@@ -1605,6 +2212,8 @@ sv_status spec_verify_get_status(spec_verify_ctx *ctx)
     }
     if (bits & kErrTimeout)
         return SV_ERR_TIMEOUT;
+    if (bits & kErrBadTree)
+        return SV_ERR_BAD_TREE;
     if (bits & kErrBadToken)
         return SV_ERR_BAD_TOKEN;
     if (bits & kErrBadValue)
@@ -1663,6 +2272,7 @@ const char *spec_verify_error_string(sv_status s)
     case SV_ERR_BAD_TOKEN: return "SV_ERR_BAD_TOKEN: a draft token was outside [0, V)";
     case SV_ERR_BAD_VALUE: return "SV_ERR_BAD_VALUE: non-finite logits or temperature";
     case SV_ERR_TIMEOUT: return "SV_ERR_TIMEOUT: a bounded wait in the kernel gave up";
+    case SV_ERR_BAD_TREE: return "SV_ERR_BAD_TREE: a parent array broke parent[0] = -1, 0 <= parent[n] < n";
     case SV_ERR_TOO_LARGE:
         return "SV_ERR_TOO_LARGE: batch exceeds the fixed scratch of spec_verify_run_noalloc "
                "(B <= 2048, B*(N+1) <= 16384, B*ceil(V*elt/4KiB) <= 16384)";

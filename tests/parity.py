@@ -93,3 +93,88 @@ def compare(w, gpu, orc, check_probs=True):
         rep.update(q_rel_max=q_max, p_rel_max=p_max, S_rel_max=max(s_max, d_max),
                    ratio_abs_max=float(np.nanmax(rr, initial=0.0)))
     return rep
+
+
+# ---- tree verification ----------------------------------------------------------
+
+# Band of a tree decision taken against a residual (a sibling after k >= 1
+# rejections, or a token drawn from such a residual): r_k is rebuilt from
+# float32 probabilities through k subtractions and normalisations, and the
+# subtraction r - p loses relative precision where r and p are close, so these
+# decisions are compared outside a wider band, scaled by k.
+TREE_BAND_PER_STEP = 1e-4
+
+
+def run_gpu_tree(ctx, w, greedy=None, seqs=None, stats=True):
+    greedy = w.greedy if greedy is None else greedy
+    st = None
+    if stats:
+        st = {k: torch.full((w.B, w.M + 1, 2), float("nan"), device=w.target.device)
+              for k in ("target_row_stats", "draft_row_stats")}
+    out, path, nacc = ctx.tree_run(w.target, None if greedy else w.draft, w.parent, w.tokens,
+                                   None if greedy else w.uniforms, None if greedy else w.temperature,
+                                   greedy=greedy, stats=st)
+    torch.cuda.synchronize()
+    res = {"out_tokens": out.cpu().numpy(), "path_nodes": path.cpu().numpy(), "num_accepted": nacc.cpu().numpy()}
+    if st:
+        res.update({k: v.cpu().numpy() for k, v in st.items()})
+    if seqs is not None:
+        res = {k: v[seqs] for k, v in res.items()}
+    return res
+
+
+def run_oracle_tree(w, seqs=None, threads=8, greedy=None):
+    greedy = w.greedy if greedy is None else greedy
+    sel = (lambda t: t) if seqs is None else (lambda t: t[torch.as_tensor(seqs, device=t.device)])
+    return oracle.tree_verify(sel(w.target), None if greedy else sel(w.draft), sel(w.parent), sel(w.tokens),
+                              sel(w.uniforms).double(), None if greedy else sel(w.temperature).double(),
+                              greedy=greedy, dtype=w.dtype, threads=threads)
+
+
+def _sibling_steps(parent, margin):
+    """Per tested node: how many siblings were rejected before it (k)."""
+    k = np.zeros(margin.shape, np.int64)
+    for b in range(margin.shape[0]):
+        seen = {}
+        for c in range(1, margin.shape[1]):
+            if not np.isnan(margin[b, c]):
+                p = int(parent[b, c])
+                k[b, c] = seen.get(p, 0)
+                seen[p] = k[b, c] + 1
+    return k
+
+
+def compare_tree(w, gpu, orc, seqs=None, check_stats=True):
+    """Report dict; AssertionError on a mismatch outside the margin bands or a
+    normaliser outside tolerance."""
+    parent = w.parent.cpu().numpy() if seqs is None else w.parent.cpu().numpy()[seqs]
+    am, sm = orc["accept_margin"], orc["sample_margin"]
+    k = _sibling_steps(parent, am)
+    band = np.where(k == 0, BAND, TREE_BAND_PER_STEP * np.maximum(k, 1))
+    in_band_acc = (np.nan_to_num(am, nan=np.inf) < band).any(axis=1)
+    # the final draw comes from a residual when the last tested node was rejected
+    kmax = np.where(np.isnan(am), -1, k).max(axis=1, initial=-1)
+    sband = np.where(kmax >= 0, TREE_BAND_PER_STEP * (kmax + 1), BAND)
+    in_band = in_band_acc | (np.nan_to_num(sm, nan=np.inf) < sband)
+    same = ((gpu["out_tokens"] == orc["out_tokens"]).all(axis=1) & (gpu["path_nodes"] == orc["path_nodes"]).all(axis=1)
+            & (gpu["num_accepted"] == orc["num_accepted"]))
+    bad = np.nonzero(~same & ~in_band)[0]
+    assert bad.size == 0, (
+        f"{bad.size} trees differ outside the margin band, first b={bad[0]}: gpu {gpu['out_tokens'][bad[0]].tolist()} "
+        f"{gpu['path_nodes'][bad[0]].tolist()} oracle {orc['out_tokens'][bad[0]].tolist()} "
+        f"{orc['path_nodes'][bad[0]].tolist()} margins {am[bad[0]].tolist()} {sm[bad[0]]}")
+    tested = int((~np.isnan(am)).sum())
+    rep = {"sequences": int(len(same)), "exact": int(same.sum()), "band_sequences": int(in_band.sum()),
+           "band_mismatch": int((~same & in_band).sum()), "tests": tested,
+           "sibling_tests": int(((k > 0) & ~np.isnan(am)).sum())}
+    if check_stats and "target_row_stats" in gpu:
+        tol = PROB_RTOL[w.dtype]
+        ok = (orc["seq_status"] == 0)[:, None] & np.isfinite(orc["tstats"][..., 1])
+        assert (gpu["target_row_stats"][..., 0][ok] == orc["tstats"][..., 0][ok]).all(), "row max differs"
+        s_rel = (np.abs(gpu["target_row_stats"][..., 1] - orc["tstats"][..., 1]) / orc["tstats"][..., 1])[ok]
+        okd = (orc["seq_status"] == 0)[:, None] & np.isfinite(orc["dstats"][..., 1])
+        d_rel = (np.abs(gpu["draft_row_stats"][..., 1] - orc["dstats"][..., 1]) / orc["dstats"][..., 1])[okd]
+        s_max = float(max(np.max(s_rel, initial=0.0), np.max(d_rel, initial=0.0)))
+        assert s_max <= tol, f"S relative error {s_max:.3g} > {tol}"
+        rep["S_rel_max"] = s_max
+    return rep

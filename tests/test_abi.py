@@ -41,7 +41,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_error_strings(lib):
-    for code in range(10):
+    for code in range(11):
         s = sv.spec_verify_error_string(code)
         assert s.startswith("SV_")
     assert "unknown" in sv.spec_verify_error_string(99)
@@ -64,6 +64,12 @@ def test_host_validation_without_gpu(lib):
     st, _ = sv.spec_verify_acceptance_counts(None, 8)
     assert st == sv.SV_ERR_INVALID_ARG
     sv.spec_verify_destroy(None)
+
+
+def test_tree_run_host_validation_without_gpu(lib):
+    tr = sv.spec_verify_tree_run
+    args = (16, 16, 16, 16, 16, 16, 0, 2, 3, 16, 16, 16, None, None, None)
+    assert tr(None, *args) == sv.SV_ERR_INVALID_ARG  # no context: rejected before any CUDA call
 
 
 def test_kv_commit_host_validation_without_gpu(lib):
