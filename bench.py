@@ -280,6 +280,62 @@ def measure_kv_commit(sv, torch, dev, stream, nacc, N, max_len=KV_MAX_LEN, reps=
             "accepted_rows": int(a.sum()), "timing": f"mean of {reps} calls, L2 flushed (256 MiB write, then 256 MiB read) before each"}
 
 
+def measure_tree(sv, torch, dev, stream, rank, steps=200, warmup=5, cpu=True):
+    """Times spec_verify_tree_run on the 64-tree batch (16-node trees shaped
+    like static Medusa/EAGLE trees, V = 151936 bf16).  Its 467 MB of logits
+    exceed L2, so calls run back to back between two CUDA events."""
+    import synth
+    w = synth.make_tree_workload("tree", seed=rank, device=dev)
+    ctx = sv.SpecVerify(w.B, w.M, w.V, w.dtype, device=dev.index or 0)
+    out = torch.empty((w.B, w.M + 1), dtype=torch.int32, device=dev)
+    path = torch.empty_like(out)
+    nacc = torch.empty((w.B,), dtype=torch.int32, device=dev)
+
+    def call():
+        ctx.tree_run(w.target, w.draft, w.parent, w.tokens, w.uniforms, w.temperature, out_tokens=out,
+                     path_nodes=path, num_accepted=nacc, stream=stream)
+
+    for _ in range(warmup):
+        call()
+    ctx.acceptance_counts(reset=True)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    if ctx.status() != sv.SV_OK:
+        raise RuntimeError("device status set during the tree measurement")
+    us = 1e3 * e0.elapsed_time(e1) / steps
+    counts = ctx.acceptance_counts()
+    mean_path = sum(k * c for k, c in enumerate(counts[: w.M + 1])) / max(1, sum(counts[: w.M + 1]))
+    peak, peak_kind = peaks()
+    gbs = w.logit_bytes / (us * 1e-6) / 1e9
+    res = {"workload": f"tree: B={w.B} trees of M+1={w.M + 1} nodes (fixed 16-node topology), V={w.V} {w.dtype}, "
+                       f"T=0.8, Zipf prior on odd trees",
+           "us_per_call": us, "nodes_per_s": w.B * (w.M + 1) / (us * 1e-6), "logit_bytes": w.logit_bytes,
+           "gbs": gbs, "frac": gbs / peak, "peak": peak, "peak_kind": f"{peak_kind} (burst copy)",
+           "mean_path_length": mean_path, "launches_per_call": 2, "steps": steps,
+           "note": "bytes count every verifier row and the draft rows of nodes with children; the walk's "
+                   "re-reads of rejected row pairs are not counted"}
+    if cpu:
+        import numpy as np
+        import oracle
+        args = [t.cpu() for t in (w.target, w.draft, w.parent, w.tokens)] + \
+            [w.uniforms.double().cpu(), w.temperature.double().cpu()]
+        done, t0 = 0, time.perf_counter()
+        while time.perf_counter() - t0 < 3.0:  # the whole batch, repeated for about 3 s
+            oracle.tree_verify(*args, dtype=w.dtype, threads=os.cpu_count() or 1, diagnostics=False)
+            done += w.B
+        dt = time.perf_counter() - t0
+        res["cpu_baseline"] = {"value": done * (w.M + 1) / dt, "unit": "tree nodes/s", "cores": os.cpu_count() or 1,
+                               "kind": "oracle",
+                               "sample": f"{done} tree verifications ({done // w.B} passes over the batch) in {dt:.1f} s"}
+    ctx.close()
+    return res
+
+
 def run_ours(args):
     import torch
     world, rank, local, pg = dist_init(args)
@@ -412,6 +468,9 @@ def run_ours(args):
     kv = None
     if not args.no_kv:
         kv = measure_kv_commit(sv, torch, dev, stream, nacc, w.N, max_len=args.kv_max_len)
+    tree = None
+    if not args.no_tree:
+        tree = measure_tree(sv, torch, dev, stream, rank, cpu=(rank == 0 and not args.no_cpu))
 
     cpu = None
     if rank == 0 and not args.no_cpu:
@@ -438,6 +497,7 @@ def run_ours(args):
         "kernels": kernels,
         "acceptance": acc,
         "kv_commit": kv,
+        "tree": tree,
         "e2e": e2e,
         "cpu_baseline": cpu,
         "gpu_launches": 3 * args.steps,  # rows, mass and pick kernels per verify call
@@ -462,6 +522,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-check", action="store_true")
     ap.add_argument("--no-kv", action="store_true", help="skip the KV-cache commit measurement")
+    ap.add_argument("--no-tree", action="store_true", help="skip the tree-verification measurement")
     ap.add_argument("--kv-max-len", type=int, default=KV_MAX_LEN,
                     help="cache positions of the KV-commit measurement (the copy does not depend on it)")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")

@@ -1270,8 +1270,16 @@ __global__ void __launch_bounds__(kPickThreads) sv_pick_kernel(const SvParams p)
 // of the last rejection pass are r_k's up to the factor R_k, otherwise one
 // more pass computes them.  The element arithmetic is explicitly rounded and
 // identical in every pass and in the recomputation of the chosen slice.
+// A pass is bound by the arithmetic of one SM (two exp2 per element pair plus
+// the residual chain), so the CTA has several groups of 8 consumer warps; the
+// group that consumes a tile maps thread t to vector t of each slice, exactly
+// as the recomputation does.
 
 constexpr int kStagesW = 8;                 // ring depth of the walk: 128 KiB of row pairs in flight
+constexpr int kWalkGroups = 3;              // consumer groups of 8 warps; group g takes ring tiles g, g+3, ...
+constexpr int kWalkThreads = kWalkGroups * kConsThreads + 32;  // + the producer warp
+constexpr int kWalkProducerWarp = kWalkGroups * kConsWarps;
+static_assert(kWalkThreads <= 1024, "a CTA holds at most 1024 threads");
 constexpr int kMaxTreeNodes = 1024;         // nodes per tree (root included)
 constexpr int kMaxWalkSlices = 512;         // slices of one row: V*elt <= 2 MiB
 
@@ -1382,18 +1390,19 @@ __device__ void walk_mass_pass(CtlW &w, unsigned char *ring, uint32_t &g, const 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int NT = (NV + kTileVecs - 1) / kTileVecs;
     const int S = (NV + kSliceVecs - 1) / kSliceVecs;
-    if (warp == kProducerWarp) {
+    if (warp == kWalkProducerWarp) {
         if (lane == 0)
             produce(w.ring, ring, tsrc, dsrc, NV, 0, NT, g);
         __syncwarp();
     } else {
-        for (int t = 0; t < NT; ++t) {
+        const int grp = warp / kConsWarps, lt = tid - grp * kConsThreads, lw = warp - grp * kConsWarps;
+        for (int t = grp; t < NT; t += kWalkGroups) {
             const uint32_t gt = g + (uint32_t)t;
             if (consume_wait(w.ring, gt)) {
                 const unsigned char *stage = ring + (gt % kStagesW) * (2 * kTileBytes);
 #pragma unroll
                 for (int q = 0; q < kVPT; ++q) {
-                    const int sv_ = q * kSliceVecs + tid;
+                    const int sv_ = q * kSliceVecs + lt;
                     const int vec = t * kTileVecs + sv_;
                     float part = 0.0f;
                     if (vec < NV) {
@@ -1409,7 +1418,7 @@ __device__ void walk_mass_pass(CtlW &w, unsigned char *ring, uint32_t &g, const 
                     const float incl = warp_incl_scan(part, lane);
                     const int sl = t * kVPT + q;
                     if (lane == 31 && sl < S)
-                        w.shares[sl * kConsWarps + warp] = incl;
+                        w.shares[sl * kConsWarps + lw] = incl;
                 }
             } else {
                 w.ring.abort = 1;
@@ -1419,7 +1428,7 @@ __device__ void walk_mass_pass(CtlW &w, unsigned char *ring, uint32_t &g, const 
     }
     g += (uint32_t)NT;
     __syncthreads();
-    for (int sl = tid; sl < S; sl += kThreads) {
+    for (int sl = tid; sl < S; sl += kWalkThreads) {
         float tot = 0.0f;
         for (int q = 0; q < kConsWarps; ++q)
             tot = __fadd_rn(tot, w.shares[sl * kConsWarps + q]);
@@ -1570,7 +1579,7 @@ __device__ int walk_pick(CtlW &w, const uint4 *tsrc, const uint4 *dsrc, int NV, 
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kThreads, 1) sv_tree_walk_kernel(const SvParams p)
+__global__ void __launch_bounds__(kWalkThreads, 1) sv_tree_walk_kernel(const SvParams p)
 {
     constexpr int VE = Elt<DT>::kPerVec;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -2065,7 +2074,7 @@ sv_status tree_run_impl(spec_verify_ctx *ctx, const void *target, const void *dr
         pdl[0].val.programmaticStreamSerializationAllowed = 1;
         cudaLaunchConfig_t cfgw = {};
         cfgw.gridDim = dim3((unsigned)B);
-        cfgw.blockDim = dim3(kThreads);
+        cfgw.blockDim = dim3(kWalkThreads);
         cfgw.dynamicSmemBytes = kSmemW;
         cfgw.stream = st;
         cfgw.attrs = pdl;
