@@ -170,6 +170,19 @@ sv_status spec_verify_tree_run(spec_verify_ctx *ctx, const void *target_logits, 
                                float *draft_row_stats, void *stream);
 
 /*
+ * The LM-head product on the tensor cores: logits[r][v] = sum_k hidden[r][k] *
+ * weight[v][k], bf16 inputs, f32 accumulation ("Speculative decoding -- draft,
+ * verify, repeat", section "Core algorithm": the verifier's forward ends in
+ * this product; so does the draft's).  hidden: device [M, K] bf16 row-major,
+ * weight: device [V, K] bf16 row-major (each row a vocabulary entry), logits:
+ * device [M, V] f32.  K must be a multiple of 8 and both inputs 16-byte
+ * aligned, else SV_ERR_INVALID_ARG; SV_ERR_CUDA if the TMA descriptors cannot
+ * be built or the launch fails.  Asynchronous on `stream`, current device.
+ */
+sv_status spec_verify_lm_head_logits(const void *hidden, const void *weight, int M, int V, int K, float *logits,
+                                     void *stream);
+
+/*
  * Acceptance telemetry (how many drafts each verify accepted, the quantity
  * the pages tell users to watch: mean accepted length and acceptance rate).
  * Every run adds each sequence to counts[k], k = its num_accepted (0..N), or

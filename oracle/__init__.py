@@ -240,3 +240,11 @@ def kv_commit(*args, **kwargs):
 
 def tree_verify(*args, **kwargs):
     return default().tree_verify(*args, **kwargs)
+
+
+def lm_head_logits(hidden, weight):
+    """logits[r, v] = sum_k hidden[r, k] * weight[v, k] in float64 (the plain
+    definition of the LM-head product; bf16 inputs widen exactly)."""
+    h = np.asarray(hidden.float().cpu().numpy() if hasattr(hidden, "float") else hidden, dtype=np.float64)
+    w = np.asarray(weight.float().cpu().numpy() if hasattr(weight, "float") else weight, dtype=np.float64)
+    return h @ w.T

@@ -50,6 +50,7 @@ _SIGNATURES = [
                                       ctypes.POINTER(_I)]),
     ("spec_verify_kv_commit", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, ctypes.c_size_t, _P]),
     ("spec_verify_tree_run", _I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
+    ("spec_verify_lm_head_logits", _I, [_P, _P, _I, _I, _I, _P, _P]),
 ]
 
 SV_KV_OVERFLOW = 1
@@ -344,3 +345,21 @@ def kv_commit(scratch, cache, cache_len, num_accepted, status=None, stream=None)
                                _ptr(status), P, B, N, max_len, row_bytes, s.cuda_stream)
     if st != SV_OK:
         raise SpecVerifyError(st, "spec_verify_kv_commit")
+
+
+def lm_head_logits(hidden, weight, out=None, stream=None):
+    """logits = hidden @ weight.T on the tensor cores (bf16 in, f32 out);
+    hidden [M, K] and weight [V, K] contiguous bf16 CUDA tensors."""
+    import torch
+    if hidden.dtype != torch.bfloat16 or weight.dtype != torch.bfloat16 or hidden.dim() != 2 or weight.dim() != 2 \
+            or hidden.shape[1] != weight.shape[1] or not hidden.is_contiguous() or not weight.is_contiguous():
+        raise ValueError("hidden [M, K] and weight [V, K] must be contiguous bf16")
+    M, K = hidden.shape
+    V = weight.shape[0]
+    if out is None:
+        out = torch.empty((M, V), dtype=torch.float32, device=hidden.device)
+    s = stream if stream is not None else torch.cuda.current_stream(hidden.device)
+    st = load().spec_verify_lm_head_logits(_ptr(hidden), _ptr(weight), M, V, K, _ptr(out), s.cuda_stream)
+    if st != SV_OK:
+        raise SpecVerifyError(st, "spec_verify_lm_head_logits")
+    return out

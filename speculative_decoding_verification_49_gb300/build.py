@@ -7,8 +7,9 @@ import sys
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
-SOURCES = [os.path.join(HERE, "csrc", "spec_verify.cu"), os.path.join(HERE, "csrc", "kv_commit.cu")]
-DEPENDS = SOURCES + [os.path.join(HERE, "csrc", "sv_device.cuh"),
+SOURCES = [os.path.join(HERE, "csrc", "spec_verify.cu"), os.path.join(HERE, "csrc", "kv_commit.cu"),
+           os.path.join(HERE, "csrc", "lmhead.cu")]
+DEPENDS = SOURCES + [os.path.join(HERE, "csrc", "sv_device.cuh"), os.path.join(HERE, "csrc", "sv_tc.cuh"),
                      os.path.join(ROOT, "include", "spec_verify.h")]
 LIBRARY = os.path.join(HERE, "libspecverify.so")
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",

@@ -1,0 +1,244 @@
+// lmhead.cu -- the verifier's LM-head GEMM on the tcgen05 tensor cores of
+// sm_103a: logits[r, v] = sum_k hidden[r, k] * weight[v, k] (bf16 in, f32
+// accumulated in tensor memory).
+//
+// "Speculative decoding -- draft, verify, repeat" (factory.pai-world.com,
+// lesson 07-16), section "Core algorithm": the verifier scores the N drafts
+// in one forward pass, whose last step is this product of the final hidden
+// states with the LM head; the draft model ends in the same product.
+//
+// One CTA computes a 128 x 256 tile: warp 0 streams 128 x 64 tiles of the
+// hidden states and 256 x 64 tiles of the weight with 2-D TMA copies (128-byte
+// swizzle) into a 4-stage shared-memory ring; one thread of warp 1 issues
+// tcgen05.mma (M = 128, N = 256, K = 16, four per 64-wide stage) into a
+// 128 x 256 f32 accumulator in tensor memory and frees each stage with
+// tcgen05.commit; warps 4-7 read the accumulator back (tcgen05.ld, one TMEM
+// lane = one row per thread) and run the epilogue.  Every mbarrier wait is
+// bounded (2 s); a CTA that gives up sets the status word, lets its copies
+// and MMAs land and frees its tensor memory.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <climits>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "spec_verify.h"
+#include "sv_tc.cuh"
+
+namespace {
+
+constexpr int kBM = 128;  // tile rows (TMEM lanes)
+constexpr int kBN = 256;  // tile columns (TMEM columns)
+constexpr int kBK = 64;   // K per stage: one 128-byte swizzle row of bf16
+constexpr int kStagesG = 4;
+constexpr int kTileA = kBM * kBK * 2;
+constexpr int kTileB = kBN * kBK * 2;
+constexpr int kStageBytes = kTileA + kTileB;
+constexpr int kGemmThreads = 256;
+constexpr uint32_t kTmemCols = 256;
+constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr int kErrTimeout = 4;
+
+struct GemmCtl {
+    uint64_t full[kStagesG];
+    uint64_t empty[kStagesG];
+    uint64_t accum;
+    int last_kb[kStagesG];  // last k-block issued into each stage
+    uint32_t tmem_base;
+    int abort;
+};
+
+constexpr size_t kSmemG = 1024 + (size_t)kStagesG * kStageBytes + sizeof(GemmCtl);
+
+struct LmParams {
+    int M, N, K;
+    float *logits;  // [M, N] f32
+    int *status;    // error bits, may be null
+};
+
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    sv_lmhead_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, LmParams p)
+{
+    extern __shared__ unsigned char smem_raw[];
+    // 128-byte-swizzled tiles want 1024-byte alignment
+    unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    GemmCtl &ctl = *reinterpret_cast<GemmCtl *>(smem + (size_t)kStagesG * kStageBytes);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.x * kBM, n0 = blockIdx.y * kBN;
+    const int nk = (p.K + kBK - 1) / kBK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStagesG; ++s) {
+            sv::mbar_init(&ctl.full[s], 1);
+            sv::mbar_init(&ctl.empty[s], 1);
+            ctl.last_kb[s] = -1;
+        }
+        sv::mbar_init(&ctl.accum, 1);
+        ctl.abort = 0;
+        sv::fence_mbar_init();
+    }
+    if (warp == 2) {
+        sv::tmem_alloc(&ctl.tmem_base, kTmemCols);
+        sv::tmem_relinquish();
+    }
+    sv::tc_fence_before();
+    __syncthreads();
+    sv::tc_fence_after();
+    const uint32_t tmem = ctl.tmem_base;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            sv::tma_prefetch_desc(&tmA);
+            sv::tma_prefetch_desc(&tmB);
+            for (int kb = 0; kb < nk; ++kb) {
+                const int s = kb % kStagesG;
+                const uint32_t ph = (uint32_t)(kb / kStagesG) & 1u;
+                if (!sv::mbar_wait_bounded(&ctl.empty[s], ph ^ 1u, &ctl.abort, kWaitNs)) {
+                    ctl.abort = 1;
+                    break;
+                }
+                unsigned char *a = smem + (size_t)s * kStageBytes;
+                sv::mbar_arrive_expect_tx(&ctl.full[s], kStageBytes);
+                sv::tma_load_2d(a, &tmA, kb * kBK, m0, &ctl.full[s]);
+                sv::tma_load_2d(a + kTileA, &tmB, kb * kBK, n0, &ctl.full[s]);
+                ctl.last_kb[s] = kb;
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = sv::idesc_bf16_f32(kBM, kBN);
+            for (int kb = 0; kb < nk; ++kb) {
+                const int s = kb % kStagesG;
+                const uint32_t ph = (uint32_t)(kb / kStagesG) & 1u;
+                if (!sv::mbar_wait_bounded(&ctl.full[s], ph, &ctl.abort, kWaitNs)) {
+                    ctl.abort = 1;
+                    break;
+                }
+                sv::tc_fence_after();
+                const unsigned char *a = smem + (size_t)s * kStageBytes;
+                const uint64_t da = sv::smem_desc_k128(a), db = sv::smem_desc_k128(a + kTileA);
+#pragma unroll
+                for (int kk = 0; kk < kBK / 16; ++kk)  // K = 16 per MMA: 32 bytes along the swizzled row
+                    sv::tc_mma_bf16(tmem, da + 2u * kk, db + 2u * kk, idesc, (kb | kk) != 0);
+                sv::tc_commit(&ctl.empty[s]);  // the stage is free once these MMAs have read it
+            }
+            sv::tc_commit(&ctl.accum);  // the accumulator is complete
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        int never = 0;
+        const bool ok = sv::mbar_wait_bounded(&ctl.accum, 0, &never, kWaitNs);
+        sv::tc_fence_after();
+        const int q = warp - 4;  // TMEM lanes 32q .. 32q+31
+        const int row = m0 + 32 * q + lane;
+        if (__all_sync(0xffffffffu, ok && !ctl.abort)) {  // tcgen05.ld is warp-collective
+            for (int c0 = 0; c0 < kBN; c0 += 32) {
+                float v[32];
+                sv::tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0, v);
+                if (row < p.M && p.logits) {
+                    float *dst = p.logits + (size_t)row * p.N + n0 + c0;
+                    for (int i = 0; i < 32; ++i)
+                        if (n0 + c0 + i < p.N)
+                            dst[i] = v[i];
+                }
+            }
+        } else if (lane == 0 && p.status) {
+            atomicOr(p.status, kErrTimeout);
+        }
+        __syncwarp();
+    }
+    sv::tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x == 0 && ctl.abort) {
+        // let every copy issued into this CTA's shared memory land before it exits
+        for (int s = 0; s < kStagesG; ++s)
+            if (ctl.last_kb[s] >= 0) {
+                int never = 0;
+                sv::mbar_wait_bounded(&ctl.full[s], (uint32_t)(ctl.last_kb[s] / kStagesG) & 1u, &never, kWaitNs / 4);
+            }
+        if (p.status)
+            atomicOr(p.status, kErrTimeout);
+    }
+    if (warp == 2)
+        sv::tmem_dealloc(tmem, kTmemCols);
+}
+
+// ---- host side -----------------------------------------------------------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static std::atomic<EncodeTiledFn> fn{nullptr};
+    EncodeTiledFn f = fn.load();
+    if (!f) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        f = reinterpret_cast<EncodeTiledFn>(ptr);
+        fn.store(f);
+    }
+    return f;
+}
+
+// Row-major bf16 matrix [rows, K] as a TMA map with boxes of box_rows x 64.
+bool make_map(CUtensorMap *m, const void *base, int rows, int K, int box_rows)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc)
+        return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+std::once_flag g_attr_once;
+cudaError_t g_attr_err = cudaSuccess;
+
+} // namespace
+
+extern "C" sv_status spec_verify_lm_head_logits(const void *hidden, const void *weight, int M, int V, int K,
+                                                float *logits, void *stream)
+{
+    if (M < 0 || V < 0 || K < 1 || K % 8 != 0)
+        return SV_ERR_INVALID_ARG;
+    if (M == 0 || V == 0)
+        return SV_OK;
+    if (!hidden || !weight || !logits || (reinterpret_cast<uintptr_t>(hidden) & 15u) ||
+        (reinterpret_cast<uintptr_t>(weight) & 15u))
+        return SV_ERR_INVALID_ARG;
+    std::call_once(g_attr_once, [] {
+        g_attr_err = cudaFuncSetAttribute(sv_lmhead_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemG);
+    });
+    if (g_attr_err != cudaSuccess)
+        return SV_ERR_CUDA;
+    CUtensorMap ta, tb;
+    if (!make_map(&ta, hidden, M, K, kBM) || !make_map(&tb, weight, V, K, kBN))
+        return SV_ERR_CUDA;
+    LmParams p;
+    p.M = M;
+    p.N = V;
+    p.K = K;
+    p.logits = logits;
+    p.status = nullptr;
+    const dim3 grid((unsigned)((M + kBM - 1) / kBM), (unsigned)((V + kBN - 1) / kBN));
+    sv_lmhead_kernel<<<grid, kGemmThreads, kSmemG, static_cast<cudaStream_t>(stream)>>>(ta, tb, p);
+    if (cudaGetLastError() != cudaSuccess)
+        return SV_ERR_CUDA;
+    return SV_OK;
+}

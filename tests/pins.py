@@ -734,6 +734,26 @@ def pin_tree_invalid_inputs(orc):
     assert r["num_accepted"][0] == 0 and r["out_tokens"][0][0] == int(np.searchsorted(np.cumsum(q0), 0.25, side="right"))
 
 
+# ---- the LM-head product ----------------------------------------------------------
+
+def pin_lm_head_definition(orc):
+    """logits[r, v] = sum_k hidden[r, k] weight[v, k]: an identity weight
+    returns the hidden states, a one-hot hidden row selects a weight column,
+    and a tiny case equals the sum written out."""
+    import oracle
+    rng = np.random.default_rng(51)
+    h = rng.normal(size=(3, 4))
+    assert np.array_equal(oracle.lm_head_logits(h, np.eye(4)), h)
+    w = rng.normal(size=(5, 4))
+    e = np.zeros((1, 4))
+    e[0, 2] = 1.0
+    assert np.array_equal(oracle.lm_head_logits(e, w)[0], w[:, 2])
+    got = oracle.lm_head_logits(h, w)
+    for r in range(3):
+        for v in range(5):
+            assert abs(got[r, v] - sum(h[r, k] * w[v, k] for k in range(4))) < 1e-12
+
+
 ALL_PINS = [
     pin_softmax_matches_scipy,
     pin_exact_law_small,
@@ -765,4 +785,5 @@ ALL_PINS = [
     pin_tree_worked_siblings,
     pin_tree_greedy_rule,
     pin_tree_invalid_inputs,
+    pin_lm_head_definition,
 ]

@@ -1,0 +1,51 @@
+"""The tensor-core LM-head product against its float64 definition (needs a GB300)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import speculative_decoding_verification_49_gb300 as sv
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from speculative_decoding_verification_49_gb300 import build
+    build.build()
+    assert torch.cuda.is_available()
+
+
+def _case(M, V, K, seed):
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    h = (torch.randn((M, K), generator=g) * 0.5).to(torch.bfloat16)
+    w = (torch.randn((V, K), generator=g) * 0.05).to(torch.bfloat16)
+    return h, w
+
+
+def _bound(h, w):
+    # f32 accumulation of K products: |error| <= K * 2^-23 * sum_k |h_k w_k| (generous)
+    return (h.abs().double() @ w.abs().double().T).numpy() * h.shape[1] * 2.0 ** -23 + 1e-30
+
+
+@pytest.mark.parametrize("M,V,K", [(128, 256, 64), (300, 1000, 72), (1, 17, 8), (257, 2304, 896),
+                                   (130, 4099, 3584)])
+def test_lm_head_logits_match_the_definition(M, V, K):
+    h, w = _case(M, V, K, seed=M + V + K)
+    got = sv.lm_head_logits(h.cuda(), w.cuda()).cpu().double().numpy()
+    want = oracle.lm_head_logits(h, w)
+    err = np.abs(got - want)
+    assert (err <= _bound(h, w)).all(), float((err / _bound(h, w)).max())
+
+
+def test_lm_head_logits_sampled_at_vocabulary_size():
+    """A Qwen-sized head (V = 151936, K = 3584) for 256 rows; 16 rows checked."""
+    M, V, K = 256, 151936, 3584
+    g = torch.Generator(device="cuda").manual_seed(1)
+    h = (torch.randn((M, K), generator=g, device="cuda") * 0.5).to(torch.bfloat16)
+    w = (torch.randn((V, K), generator=g, device="cuda") * 0.05).to(torch.bfloat16)
+    got = sv.lm_head_logits(h, w)
+    rows = torch.tensor([0, 1, 63, 64, 127, 128, 200, 255, 5, 77, 99, 150, 180, 222, 240, 254])
+    want = oracle.lm_head_logits(h[rows].cpu(), w.cpu())
+    err = np.abs(got[rows.cuda()].cpu().double().numpy() - want)
+    assert (err <= _bound(h[rows].cpu(), w.cpu())).all()
