@@ -183,6 +183,36 @@ sv_status spec_verify_lm_head_logits(const void *hidden, const void *weight, int
                                      void *stream);
 
 /*
+ * The verify step fused into the LM-head products: the inputs are the final
+ * hidden states and the LM-head weights of both models instead of logits
+ * (the verifier's forward and the draft's both end in this product: "Speculative
+ * decoding -- draft, verify, repeat", section "Core algorithm").  The logits
+ * are computed on the tensor cores and reduced in the product's epilogue to
+ * the row statistics the method needs (max, sum of exp((z - max)/T), or the
+ * argmax for greedy sequences, and the logit at each draft token), so they
+ * never reach HBM; only the row pair at each sampled sequence's first
+ * rejection is recomputed, as float32 logits, to draw the token.  The result
+ * equals spec_verify_run on the float32 logits hidden @ weight^T.
+ *
+ *   target_hidden [B*(N+1), Kt] bf16, row b*(N+1)+i for position i
+ *   target_weight [V, Kt] bf16 (row v: vocabulary entry v)
+ *   draft_hidden  [B*N, Kd] bf16, draft_weight [V, Kd] bf16 (NULL when greedy)
+ *   the other arguments as spec_verify_run; target_row_stats [B, N+1, 2] and
+ *   draft_row_stats [B, N, 2] (m, S) may be NULL.
+ * Requires a context created with SV_F32 (SV_ERR_DTYPE otherwise; its V is the
+ * vocabulary size), Kt and Kd multiples of 8, 16-byte aligned inputs.  The
+ * first call (and a call with larger Kt or Kd) allocates its scratch
+ * (cudaMalloc, about 8*(2*max_N+1)*max_B*ceil(V/256) + 8*max_B*V +
+ * 2*max_B*(Kt+Kd) bytes) and therefore synchronises; later calls enqueue nine
+ * launches on `stream` and allocate nothing.
+ */
+sv_status spec_verify_run_fused(spec_verify_ctx *ctx, const void *target_hidden, const void *target_weight,
+                                int Kt, const void *draft_hidden, const void *draft_weight, int Kd,
+                                const int32_t *draft_tokens, const float *uniforms, const float *temperature,
+                                int greedy, int B, int N, int32_t *out_tokens, int32_t *num_accepted,
+                                float *target_row_stats, float *draft_row_stats, void *stream);
+
+/*
  * Acceptance telemetry (how many drafts each verify accepted, the quantity
  * the pages tell users to watch: mean accepted length and acceptance rate).
  * Every run adds each sequence to counts[k], k = its num_accepted (0..N), or

@@ -51,6 +51,7 @@ _SIGNATURES = [
     ("spec_verify_kv_commit", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, ctypes.c_size_t, _P]),
     ("spec_verify_tree_run", _I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
     ("spec_verify_lm_head_logits", _I, [_P, _P, _I, _I, _I, _P, _P]),
+    ("spec_verify_run_fused", _I, [_P, _P, _P, _I, _P, _P, _I, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P]),
 ]
 
 SV_KV_OVERFLOW = 1
@@ -309,6 +310,35 @@ class SpecVerify:
         if st != SV_OK:
             raise SpecVerifyError(st, "spec_verify_tree_run")
         return out_tokens, path_nodes, num_accepted
+
+    def run_fused(self, target_hidden, target_weight, draft_hidden, draft_weight, draft_tokens, uniforms,
+                  temperature, greedy=False, out_tokens=None, num_accepted=None, stream=None, stats=None):
+        """The verify step fused into the LM-head products (context dtype
+        "f32"): hidden states [rows, K] and weights [V, K] in bf16; returns
+        (out_tokens, num_accepted) without synchronising."""
+        import torch
+        Kt = target_hidden.shape[1]
+        N = draft_tokens.shape[1]
+        B = target_hidden.shape[0] // (N + 1)
+        Kd = draft_hidden.shape[1] if draft_hidden is not None else 0
+        for t in (target_hidden, target_weight, draft_hidden, draft_weight):
+            if t is not None and (t.dtype != torch.bfloat16 or not t.is_contiguous()):
+                raise ValueError("hidden states and weights must be contiguous bf16")
+        dev = target_hidden.device
+        if out_tokens is None:
+            out_tokens = torch.empty((B, N + 1), dtype=torch.int32, device=dev)
+        if num_accepted is None:
+            num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+        s = stream if stream is not None else torch.cuda.current_stream(dev)
+        stats = stats or {}
+        st = load().spec_verify_run_fused(
+            self.ctx, _ptr(target_hidden), _ptr(target_weight), Kt, _ptr(draft_hidden), _ptr(draft_weight), Kd,
+            _ptr(draft_tokens), _ptr(uniforms), _ptr(temperature), int(bool(greedy)), B, N, _ptr(out_tokens),
+            _ptr(num_accepted), _ptr(stats.get("target_row_stats")), _ptr(stats.get("draft_row_stats")),
+            s.cuda_stream)
+        if st != SV_OK:
+            raise SpecVerifyError(st, "spec_verify_run_fused")
+        return out_tokens, num_accepted
 
     def debug_buffers(self, B: int, N: int, device="cuda"):
         import torch

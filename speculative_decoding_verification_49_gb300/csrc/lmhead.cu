@@ -13,18 +13,24 @@
 // tcgen05.mma (M = 128, N = 256, K = 16, four per 64-wide stage) into a
 // 128 x 256 f32 accumulator in tensor memory and frees each stage with
 // tcgen05.commit; warps 4-7 read the accumulator back (tcgen05.ld, one TMEM
-// lane = one row per thread) and run the epilogue.  Every mbarrier wait is
+// lane = one row per thread) and run the epilogue: either the logits go out
+// as f32, or (the fused verify path) only each row's statistics over the
+// tile do -- max and sum of exp2((z - max) * log2(e)/T), or max and argmax
+// for greedy rows, and the logit at the row's draft token -- so the logits
+// never reach HBM.  Every mbarrier wait is
 // bounded (2 s); a CTA that gives up sets the status word, lets its copies
 // and MMAs land and frees its tensor memory.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cfloat>
 #include <climits>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
 
+#include "lmhead.h"
 #include "spec_verify.h"
 #include "sv_tc.cuh"
 
@@ -53,12 +59,72 @@ struct GemmCtl {
 
 constexpr size_t kSmemG = 1024 + (size_t)kStagesG * kStageBytes + sizeof(GemmCtl);
 
+constexpr double kLog2e = 1.4426950408889634074;
+
 struct LmParams {
     int M, N, K;
-    float *logits;  // [M, N] f32
+    float *logits;  // [M, N] f32 (logits epilogue)
     int *status;    // error bits, may be null
+    svlm::StatsArgs st;  // statistics epilogue
 };
 
+// The statistics of one row over one tile (32 columns per tcgen05.ld).  A
+// thread whose row is past M still issues the warp-collective loads but
+// writes nothing.
+__device__ __forceinline__ void row_stats(uint32_t taddr, int n0, const LmParams &p, int row_in)
+{
+    const svlm::StatsArgs &a = p.st;
+    const bool valid = row_in < p.M;
+    const int row = valid ? row_in : 0;
+    const int b = row / a.rows_per_seq;
+    const int i = row - b * a.rows_per_seq;
+    float T = a.greedy || !a.T ? 0.0f : a.T[b];
+    const bool sampled = T > 0.0f && T != INFINITY && T >= FLT_MIN;  // NaN compares false
+    const float cf = sampled ? (float)(kLog2e / (double)T) : 0.0f;
+    const int d = (i < a.N) ? a.tokens[(size_t)b * a.N + i] : -1;
+    const int dl = d - n0;  // the draft token's column in this tile, if in range
+    float m = -INFINITY;
+    int arg = INT_MAX;
+    for (int c0 = 0; c0 < kBN; c0 += 32) {
+        float v[32];
+        sv::tmem_ld32(taddr + (uint32_t)c0, v);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+            const int c = c0 + k;
+            if (n0 + c < p.N) {
+                if (v[k] > m) {
+                    m = v[k];
+                    arg = n0 + c;
+                }
+                if (c == dl && valid)
+                    a.zgat[row] = v[k];
+            }
+        }
+    }
+    float s = 0.0f;
+    // tcgen05.ld is warp-collective and the rows of one warp may belong to
+    // greedy and sampled sequences alike: the whole warp loads, the sampled
+    // rows accumulate
+    if (__any_sync(0xffffffffu, sampled)) {
+        for (int c0 = 0; c0 < kBN; c0 += 32) {
+            float v[32];
+            sv::tmem_ld32(taddr + (uint32_t)c0, v);
+            if (sampled) {
+#pragma unroll
+                for (int k = 0; k < 32; ++k)
+                    if (n0 + c0 + k < p.N)
+                        s = __fadd_rn(s, sv::ex2(__fmul_rn(__fsub_rn(v[k], m), cf)));
+            }
+        }
+    }
+    if (valid) {
+        float *out = a.part + ((size_t)row * ((p.N + kBN - 1) / kBN) + n0 / kBN) * 2;
+        out[0] = m;
+        out[1] = sampled ? s : __int_as_float(arg);
+    }
+}
+
+template <bool STATS>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     sv_lmhead_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, LmParams p)
 {
@@ -136,14 +202,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int q = warp - 4;  // TMEM lanes 32q .. 32q+31
         const int row = m0 + 32 * q + lane;
         if (__all_sync(0xffffffffu, ok && !ctl.abort)) {  // tcgen05.ld is warp-collective
-            for (int c0 = 0; c0 < kBN; c0 += 32) {
-                float v[32];
-                sv::tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0, v);
-                if (row < p.M && p.logits) {
-                    float *dst = p.logits + (size_t)row * p.N + n0 + c0;
-                    for (int i = 0; i < 32; ++i)
-                        if (n0 + c0 + i < p.N)
-                            dst[i] = v[i];
+            const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16);
+            if constexpr (STATS) {
+                row_stats(taddr, n0, p, row);
+            } else {
+                for (int c0 = 0; c0 < kBN; c0 += 32) {
+                    float v[32];
+                    sv::tmem_ld32(taddr + (uint32_t)c0, v);
+                    if (row < p.M) {
+                        float *dst = p.logits + (size_t)row * p.N + n0 + c0;
+                        for (int i = 0; i < 32; ++i)
+                            if (n0 + c0 + i < p.N)
+                                dst[i] = v[i];
+                    }
                 }
             }
         } else if (lane == 0 && p.status) {
@@ -210,35 +281,68 @@ bool make_map(CUtensorMap *m, const void *base, int rows, int K, int box_rows)
 std::once_flag g_attr_once;
 cudaError_t g_attr_err = cudaSuccess;
 
-} // namespace
-
-extern "C" sv_status spec_verify_lm_head_logits(const void *hidden, const void *weight, int M, int V, int K,
-                                                float *logits, void *stream)
+template <bool STATS>
+sv_status launch(const void *hidden, const void *weight, int M, int V, int K, const LmParams &p, cudaStream_t st)
 {
     if (M < 0 || V < 0 || K < 1 || K % 8 != 0)
         return SV_ERR_INVALID_ARG;
     if (M == 0 || V == 0)
         return SV_OK;
-    if (!hidden || !weight || !logits || (reinterpret_cast<uintptr_t>(hidden) & 15u) ||
-        (reinterpret_cast<uintptr_t>(weight) & 15u))
+    if (!hidden || !weight || (reinterpret_cast<uintptr_t>(hidden) & 15u) || (reinterpret_cast<uintptr_t>(weight) & 15u))
         return SV_ERR_INVALID_ARG;
     std::call_once(g_attr_once, [] {
-        g_attr_err = cudaFuncSetAttribute(sv_lmhead_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemG);
+        g_attr_err = cudaFuncSetAttribute(sv_lmhead_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)kSmemG);
+        if (g_attr_err == cudaSuccess)
+            g_attr_err = cudaFuncSetAttribute(sv_lmhead_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              (int)kSmemG);
     });
     if (g_attr_err != cudaSuccess)
         return SV_ERR_CUDA;
     CUtensorMap ta, tb;
     if (!make_map(&ta, hidden, M, K, kBM) || !make_map(&tb, weight, V, K, kBN))
         return SV_ERR_CUDA;
-    LmParams p;
+    const dim3 grid((unsigned)((M + kBM - 1) / kBM), (unsigned)((V + kBN - 1) / kBN));
+    sv_lmhead_kernel<STATS><<<grid, kGemmThreads, kSmemG, st>>>(ta, tb, p);
+    if (cudaGetLastError() != cudaSuccess)
+        return SV_ERR_CUDA;
+    return SV_OK;
+}
+
+} // namespace
+
+namespace svlm {
+
+sv_status launch_logits(const void *hidden, const void *weight, int M, int V, int K, float *logits,
+                        cudaStream_t stream)
+{
+    if (M > 0 && V > 0 && !logits)
+        return SV_ERR_INVALID_ARG;
+    LmParams p{};
     p.M = M;
     p.N = V;
     p.K = K;
     p.logits = logits;
-    p.status = nullptr;
-    const dim3 grid((unsigned)((M + kBM - 1) / kBM), (unsigned)((V + kBN - 1) / kBN));
-    sv_lmhead_kernel<<<grid, kGemmThreads, kSmemG, static_cast<cudaStream_t>(stream)>>>(ta, tb, p);
-    if (cudaGetLastError() != cudaSuccess)
-        return SV_ERR_CUDA;
-    return SV_OK;
+    return launch<false>(hidden, weight, M, V, K, p, stream);
+}
+
+sv_status launch_stats(const void *hidden, const void *weight, int M, int V, int K, const StatsArgs &a,
+                       cudaStream_t stream)
+{
+    if (M > 0 && V > 0 && (!a.part || !a.zgat || a.rows_per_seq < 1 || (a.N > 0 && !a.tokens)))
+        return SV_ERR_INVALID_ARG;
+    LmParams p{};
+    p.M = M;
+    p.N = V;
+    p.K = K;
+    p.st = a;
+    return launch<true>(hidden, weight, M, V, K, p, stream);
+}
+
+} // namespace svlm
+
+extern "C" sv_status spec_verify_lm_head_logits(const void *hidden, const void *weight, int M, int V, int K,
+                                                float *logits, void *stream)
+{
+    return svlm::launch_logits(hidden, weight, M, V, K, logits, static_cast<cudaStream_t>(stream));
 }

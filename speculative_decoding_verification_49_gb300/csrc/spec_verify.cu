@@ -37,6 +37,7 @@
 #include <mutex>
 
 #include "spec_verify.h"
+#include "lmhead.h"
 #include "sv_device.cuh"
 
 namespace {
@@ -90,8 +91,22 @@ struct SvParams {
     // tree verification (N is then the node count M; rows are per node)
     const int32_t *parent;  // [B][M+1]
     int32_t *path;          // [B][M+1] accepted node ids
+    // fused LM-head path: the sampling kernels read row b of compact
+    // [B, V] buffers instead of the verify inputs' rows (b, j)
+    int sample_compact;
     int B, N, V, greedy;
 };
+
+// Rows the sampling kernels read for sequence b stopping at position j.
+__device__ __forceinline__ size_t sample_trow(const SvParams &p, int b, int j)
+{
+    return p.sample_compact ? (size_t)b : (size_t)b * (p.N + 1) + j;
+}
+
+__device__ __forceinline__ size_t sample_drow(const SvParams &p, int b, int j)
+{
+    return p.sample_compact ? (size_t)b : (size_t)b * p.N + j;
+}
 
 // Producer/consumer ring state in shared memory.
 template <int S> struct Ring {
@@ -886,7 +901,6 @@ __global__ void __launch_bounds__(kThreads, 4) sv_mass_kernel(const SvParams p)
     CtlM &ctl = *reinterpret_cast<CtlM *>(smem + kRingBytesM);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int N = p.N;
     const int NV = p.V / VE;
     const int T = (NV + kTileVecsM - 1) / kTileVecsM;  // ring tiles per row
     const int S = (NV + kSliceVecs - 1) / kSliceVecs;  // slices per row
@@ -929,10 +943,9 @@ __global__ void __launch_bounds__(kThreads, 4) sv_mass_kernel(const SvParams p)
                 m.mp = sq.mp;
                 m.isp = sq.isp;
                 m.cf = sq.cf;
-                const size_t trow = (size_t)b * (N + 1) + sq.j;
-                const uint4 *tsrc = static_cast<const uint4 *>(p.target) + trow * (size_t)NV;
+                const uint4 *tsrc = static_cast<const uint4 *>(p.target) + sample_trow(p, b, sq.j) * (size_t)NV;
                 const uint4 *dsrc = (sq.res_mode == RES_DIFF)
-                                        ? static_cast<const uint4 *>(p.draft) + ((size_t)b * N + sq.j) * (size_t)NV
+                                        ? static_cast<const uint4 *>(p.draft) + sample_drow(p, b, sq.j) * (size_t)NV
                                         : nullptr;
                 const int nvec = min(kTileVecsM, NV - t * kTileVecsM);
                 const uint32_t bytes = static_cast<uint32_t>(nvec) * 16u;
@@ -1075,9 +1088,8 @@ __global__ void __launch_bounds__(kPickThreads) sv_pick_kernel(const SvParams p)
         return;
     }
 
-    const size_t trow = (size_t)b * (N + 1) + j;
-    const uint4 *tsrc = static_cast<const uint4 *>(p.target) + trow * (size_t)NV;
-    const uint4 *dsrc = (j < N) ? static_cast<const uint4 *>(p.draft) + ((size_t)b * N + j) * (size_t)NV : nullptr;
+    const uint4 *tsrc = static_cast<const uint4 *>(p.target) + sample_trow(p, b, j) * (size_t)NV;
+    const uint4 *dsrc = (j < N) ? static_cast<const uint4 *>(p.draft) + sample_drow(p, b, j) * (size_t)NV : nullptr;
     const float *shares = p.ws_slice + (size_t)b * S * kConsWarps;
     float r[VE];
     for (int sl = tid; sl < S; sl += kPickThreads) {
@@ -1741,6 +1753,131 @@ __global__ void __launch_bounds__(kWalkThreads, 1) sv_tree_walk_kernel(const SvP
     }
 }
 
+// =============================================================================
+// Fused LM-head path: decisions from the GEMM epilogue's tile statistics
+// =============================================================================
+//
+// The tensor-core product of the hidden states with the LM head leaves, per
+// row and 256-column tile, (m, s) or (max, argmax), and the logit at the
+// row's draft token (lmhead.cu).  One warp per position merges the tiles of
+// the target row and of the draft row in tile order, then decides position i
+// exactly as kernel A does.  A gather kernel then copies, per sequence, the
+// hidden states of the rows at the first rejection j; their logits are
+// recomputed on the tensor cores into compact [B, V] buffers, which kernels B
+// and C sample from.
+
+struct FusedArgs {
+    const float *part_t, *part_d;  // [rows, tiles, 2]
+    const float *zgat_t, *zgat_d;  // [rows]
+    int tiles;
+    const unsigned char *hid_t, *hid_d;  // hidden states, rows of row_bytes_t / row_bytes_d
+    unsigned char *hc_t, *hc_d;          // [B] gathered rows
+    int row_bytes_t, row_bytes_d;
+};
+
+__device__ __forceinline__ void merge_tiles(const float *part, int tiles, bool sampled, float cf, int lane, float &m,
+                                            float &s, int &arg)
+{
+    if (sampled) {
+        Online o{-INFINITY, 0.0f};
+        for (int t = lane; t < tiles; t += 32)
+            o = online_merge(o, Online{part[2 * t], part[2 * t + 1]}, cf);
+        o = warp_merge(o, cf);
+        m = o.m;
+        s = o.s;
+        arg = 0;
+    } else {
+        ArgMax a{-INFINITY, INT_MAX, 0};
+        for (int t = lane; t < tiles; t += 32)
+            a = argmax_merge(a, ArgMax{part[2 * t], __float_as_int(part[2 * t + 1]), 0});
+        a = warp_argmax(a);
+        m = a.v;
+        s = 0.0f;
+        arg = a.i;
+    }
+}
+
+__global__ void __launch_bounds__(256) sv_fused_decide_kernel(const SvParams p, const FusedArgs f)
+{
+    sv::grid_dependency_wait();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int unit = blockIdx.x * 8 + warp;
+    const int N = p.N;
+    if (unit >= p.B * (N + 1))
+        return;
+    const int b = unit / (N + 1), i = unit - b * (N + 1);
+    float T;
+    const int mode = sequence_mode(p, b, T);
+    if (mode == MODE_INVALID) {
+        if (lane == 0)
+            atomicOr(&p.ws_err[b], kErrBadValue);
+        return;
+    }
+    const bool sampled = mode == MODE_SAMPLED;
+    const float cf = sampled ? (float)(kLog2e / (double)T) : 0.0f;
+    const size_t trow = (size_t)b * (N + 1) + i, drow = (size_t)b * N + i;
+    float mq, Sq, mp = -INFINITY, Sp = 0.0f;
+    int aq, ap;
+    merge_tiles(f.part_t + trow * f.tiles * 2, f.tiles, sampled, cf, lane, mq, Sq, aq);
+    if (sampled && i < N)
+        merge_tiles(f.part_d + drow * f.tiles * 2, f.tiles, true, cf, lane, mp, Sp, ap);
+    if (lane != 0)
+        return;
+    const int d = (i < N) ? p.tokens[drow] : 0;
+    const bool bad_d = (i < N) && (d < 0 || d >= p.V);
+    int errb = bad_d ? kErrBadToken : 0;
+    if (!isfinite(mq) || (sampled && !(isfinite(Sq) && Sq > 0.0f)) ||
+        (sampled && i < N && !(isfinite(mp) && isfinite(Sp) && Sp > 0.0f)))
+        errb |= kErrBadValue;
+    if (!sampled) {
+        p.ws_tok[trow] = aq;
+        if (i < N && d != aq)
+            atomicMin(&p.ws_first[b], i);
+        if (p.tstats) {
+            p.tstats[trow * 2 + 0] = mq;
+            p.tstats[trow * 2 + 1] = NAN;
+        }
+    } else {
+        if (!errb && i < N &&
+            !first_child_test(__ldcg(&f.zgat_t[trow]), __ldcg(&f.zgat_d[drow]), mq, Sq, mp, Sp, T, (double)p.u[trow]))
+            atomicMin(&p.ws_first[b], i);
+        float *st = p.ws_stats + trow * 4;
+        st[0] = mq;
+        st[1] = Sq;
+        st[2] = mp;
+        st[3] = Sp;
+        if (p.tstats) {
+            p.tstats[trow * 2 + 0] = mq;
+            p.tstats[trow * 2 + 1] = Sq;
+        }
+        if (p.dstats && i < N) {
+            p.dstats[drow * 2 + 0] = mp;
+            p.dstats[drow * 2 + 1] = Sp;
+        }
+    }
+    if (errb)
+        atomicOr(&p.ws_err[b], errb);
+}
+
+// Hidden states of row pair j of every sequence into the compact buffers.
+__global__ void __launch_bounds__(256) sv_fused_gather_kernel(const SvParams p, const FusedArgs f)
+{
+    sv::grid_dependency_wait();
+    const int b = blockIdx.x, N = p.N;
+    int j = __ldcg(&p.ws_first[b]);
+    j = j > N ? N : j;
+    const uint4 *src = reinterpret_cast<const uint4 *>(f.hid_t + ((size_t)b * (N + 1) + j) * f.row_bytes_t);
+    uint4 *dst = reinterpret_cast<uint4 *>(f.hc_t + (size_t)b * f.row_bytes_t);
+    for (int v = threadIdx.x; v < f.row_bytes_t / 16; v += blockDim.x)
+        dst[v] = __ldg(src + v);
+    if (j < N && f.hid_d) {
+        const uint4 *sd = reinterpret_cast<const uint4 *>(f.hid_d + ((size_t)b * N + j) * f.row_bytes_d);
+        uint4 *dd = reinterpret_cast<uint4 *>(f.hc_d + (size_t)b * f.row_bytes_d);
+        for (int v = threadIdx.x; v < f.row_bytes_d / 16; v += blockDim.x)
+            dd[v] = __ldg(sd + v);
+    }
+}
+
 } // namespace
 
 // =============================================================================
@@ -1760,6 +1897,11 @@ struct spec_verify_ctx {
     int *ws_first, *ws_err, *ws_tok, *status;
     float *ws_stats, *ws_slice;
     unsigned long long *hist;  // [max_N + 2]: accepted-draft histogram, then invalid
+    // fused LM-head path: scratch allocated on its first call (and when K grows)
+    void *fz;
+    int fz_Kt, fz_Kd;
+    float *fz_part_t, *fz_part_d, *fz_zgat_t, *fz_zgat_d, *fz_lt, *fz_ld;
+    unsigned char *fz_hc_t, *fz_hc_d;
     // profiling: events before kernel A, between the kernels and after kernel B
     int prof_on, prof_runs;
     cudaEvent_t *prof_ev;  // [kProfRuns][3]
@@ -1956,6 +2098,7 @@ sv_status run_impl(spec_verify_ctx *ctx, const void *target, const void *draft, 
     prm.status = ctx->status;
     prm.parent = nullptr;
     prm.path = nullptr;
+    prm.sample_compact = 0;
     prm.B = B;
     prm.N = N;
     prm.V = ctx->V;
@@ -2089,6 +2232,141 @@ sv_status tree_run_impl(spec_verify_ctx *ctx, const void *target, const void *dr
     return SV_OK;
 }
 
+// Scratch of the fused path, sized for the context's limits and the widest
+// hidden states seen so far.
+sv_status fused_scratch(spec_verify_ctx *ctx, int Kt, int Kd)
+{
+    if (ctx->fz && Kt <= ctx->fz_Kt && Kd <= ctx->fz_Kd)
+        return SV_OK;
+    Kt = Kt > ctx->fz_Kt ? Kt : ctx->fz_Kt;
+    Kd = Kd > ctx->fz_Kd ? Kd : ctx->fz_Kd;
+    const size_t nb = (size_t)(ctx->max_B > 0 ? ctx->max_B : 1);
+    const size_t rows_t = nb * (size_t)(ctx->max_N + 1), rows_d = nb * (size_t)(ctx->max_N > 0 ? ctx->max_N : 1);
+    const size_t tiles = (size_t)svlm::tiles(ctx->V);
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    const size_t o_pt = 0, o_pd = o_pt + up(rows_t * tiles * 8), o_zt = o_pd + up(rows_d * tiles * 8);
+    const size_t o_zd = o_zt + up(rows_t * 4), o_lt = o_zd + up(rows_d * 4), o_ld = o_lt + up(nb * ctx->V * 4);
+    const size_t o_ht = o_ld + up(nb * ctx->V * 4), o_hd = o_ht + up(nb * (size_t)Kt * 2);
+    const size_t bytes = o_hd + up(nb * (size_t)(Kd > 0 ? Kd : 8) * 2);
+    cudaFree(ctx->fz);
+    ctx->fz = nullptr;
+    if (cudaMalloc(&ctx->fz, bytes) != cudaSuccess) {
+        cudaGetLastError();
+        ctx->fz = nullptr;
+        return SV_ERR_OOM;
+    }
+    unsigned char *z = static_cast<unsigned char *>(ctx->fz);
+    ctx->fz_part_t = reinterpret_cast<float *>(z + o_pt);
+    ctx->fz_part_d = reinterpret_cast<float *>(z + o_pd);
+    ctx->fz_zgat_t = reinterpret_cast<float *>(z + o_zt);
+    ctx->fz_zgat_d = reinterpret_cast<float *>(z + o_zd);
+    ctx->fz_lt = reinterpret_cast<float *>(z + o_lt);
+    ctx->fz_ld = reinterpret_cast<float *>(z + o_ld);
+    ctx->fz_hc_t = z + o_ht;
+    ctx->fz_hc_d = z + o_hd;
+    ctx->fz_Kt = Kt;
+    ctx->fz_Kd = Kd;
+    return SV_OK;
+}
+
+sv_status fused_run_impl(spec_verify_ctx *ctx, const void *ht, const void *wt, int Kt, const void *hd, const void *wd,
+                         int Kd, const int32_t *tokens, const float *u, const float *T, int greedy, int B, int N,
+                         int32_t *out, int32_t *nacc, float *tstats, float *dstats, void *stream)
+{
+    if (!ctx)
+        return SV_ERR_INVALID_ARG;
+    if (ctx->dtype != SV_F32)
+        return SV_ERR_DTYPE;  // the recomputed logits are float32
+    if (B < 0 || B > ctx->max_B || N < 0 || N > ctx->max_N || Kt < 8 || Kt % 8 != 0)
+        return SV_ERR_INVALID_ARG;
+    if (B == 0)
+        return SV_OK;
+    const bool need_draft = !greedy && N > 0;
+    if (!ht || !wt || !out || !nacc || (N > 0 && !tokens) || (!greedy && (!T || !u)))
+        return SV_ERR_INVALID_ARG;
+    if (need_draft && (!hd || !wd || Kd < 8 || Kd % 8 != 0))
+        return SV_ERR_INVALID_ARG;
+    for (const void *q : {ht, wt, hd, wd})
+        if (reinterpret_cast<uintptr_t>(q) & 15u)
+            return SV_ERR_INVALID_ARG;
+    DeviceGuard guard(ctx->device);
+    if (!guard.ok)
+        return SV_ERR_CUDA;
+    sv_status r = fused_scratch(ctx, Kt, need_draft ? Kd : 8);
+    if (r != SV_OK)
+        return r;
+    const int V = ctx->V;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    // 1. tile statistics of every verifier row and every draft row
+    svlm::StatsArgs a{tokens, greedy ? nullptr : T, greedy ? 1 : 0, N, N + 1, ctx->fz_part_t, ctx->fz_zgat_t};
+    if ((r = svlm::launch_stats(ht, wt, B * (N + 1), V, Kt, a, st)) != SV_OK)
+        return r;
+    if (need_draft) {
+        svlm::StatsArgs ad{tokens, T, 0, N, N, ctx->fz_part_d, ctx->fz_zgat_d};
+        if ((r = svlm::launch_stats(hd, wd, B * N, V, Kd, ad, st)) != SV_OK)
+            return r;
+    }
+
+    SvParams prm;
+    memset(&prm, 0, sizeof prm);
+    prm.target = ctx->fz_lt;
+    prm.draft = ctx->fz_ld;
+    prm.tokens = tokens;
+    prm.u = u;
+    prm.T = T;
+    prm.out = out;
+    prm.nacc = nacc;
+    prm.tstats = tstats;
+    prm.dstats = dstats;
+    prm.ws_first = ctx->ws_first;
+    prm.ws_err = ctx->ws_err;
+    prm.ws_tok = ctx->ws_tok;
+    prm.ws_stats = ctx->ws_stats;
+    prm.ws_slice = ctx->ws_slice;
+    prm.hist = ctx->hist;
+    prm.hist_invalid = ctx->hist ? ctx->hist + ctx->max_N + 1 : nullptr;
+    prm.status = ctx->status;
+    prm.sample_compact = 1;
+    prm.B = B;
+    prm.N = N;
+    prm.V = V;
+    prm.greedy = greedy ? 1 : 0;
+    FusedArgs f;
+    f.part_t = ctx->fz_part_t;
+    f.part_d = ctx->fz_part_d;
+    f.zgat_t = ctx->fz_zgat_t;
+    f.zgat_d = ctx->fz_zgat_d;
+    f.tiles = svlm::tiles(V);
+    f.hid_t = static_cast<const unsigned char *>(ht);
+    f.hid_d = need_draft ? static_cast<const unsigned char *>(hd) : nullptr;
+    f.hc_t = ctx->fz_hc_t;
+    f.hc_d = ctx->fz_hc_d;
+    f.row_bytes_t = Kt * 2;
+    f.row_bytes_d = need_draft ? Kd * 2 : 0;
+
+    // 2. decisions; 3. the hidden rows at the first rejection
+    const long long units = (long long)B * (N + 1);
+    sv_fused_decide_kernel<<<(unsigned)((units + 7) / 8), 256, 0, st>>>(prm, f);
+    sv_fused_gather_kernel<<<(unsigned)B, 256, 0, st>>>(prm, f);
+    if (cudaGetLastError() != cudaSuccess)
+        return SV_ERR_CUDA;
+    // 4. their logits, recomputed on the tensor cores
+    if ((r = svlm::launch_logits(ctx->fz_hc_t, wt, B, V, Kt, ctx->fz_lt, st)) != SV_OK)
+        return r;
+    if (need_draft && (r = svlm::launch_logits(ctx->fz_hc_d, wd, B, V, Kd, ctx->fz_ld, st)) != SV_OK)
+        return r;
+    // 5. residual masses and the token, as in spec_verify_run
+    const int nv = V * 4 / 16;
+    const long long tiles_m = (long long)B * ((nv + kTileVecsM - 1) / kTileVecsM);
+    const int grid_m = (int)(tiles_m < ctx->mass_ctas ? tiles_m : ctx->mass_ctas);
+    sv_mass_kernel<SV_F32><<<(unsigned)(grid_m > 0 ? grid_m : 1), kThreads, kSmemM, st>>>(prm);
+    sv_pick_kernel<SV_F32><<<(unsigned)B, kPickThreads, 0, st>>>(prm);
+    if (cudaGetLastError() != cudaSuccess)
+        return SV_ERR_CUDA;
+    return SV_OK;
+}
+
 } // namespace
 
 extern "C" {
@@ -2197,6 +2475,17 @@ sv_status spec_verify_tree_run(spec_verify_ctx *ctx, const void *target_logits, 
 {
     return tree_run_impl(ctx, target_logits, draft_logits, parent, draft_tokens, uniforms, temperature, greedy, B,
                          M, out_tokens, path_nodes, num_accepted, target_row_stats, draft_row_stats, stream);
+}
+
+sv_status spec_verify_run_fused(spec_verify_ctx *ctx, const void *target_hidden, const void *target_weight,
+                                int Kt, const void *draft_hidden, const void *draft_weight, int Kd,
+                                const int32_t *draft_tokens, const float *uniforms, const float *temperature,
+                                int greedy, int B, int N, int32_t *out_tokens, int32_t *num_accepted,
+                                float *target_row_stats, float *draft_row_stats, void *stream)
+{
+    return fused_run_impl(ctx, target_hidden, target_weight, Kt, draft_hidden, draft_weight, Kd, draft_tokens,
+                          uniforms, temperature, greedy, B, N, out_tokens, num_accepted, target_row_stats,
+                          draft_row_stats, stream);
 }
 
 sv_status spec_verify_get_status(spec_verify_ctx *ctx)
@@ -2369,6 +2658,7 @@ void spec_verify_destroy(spec_verify_ctx *ctx)
         DeviceGuard guard(ctx->device);
         prof_free(ctx);
         cudaFree(ctx->ws);
+        cudaFree(ctx->fz);
     }
     free(ctx);
 }

@@ -311,6 +311,80 @@ def make_tree_workload(name: str, seed: int = 0, device="cpu", **overrides) -> T
                         tokens=tokens, uniforms=uniforms, temperature=T)
 
 
+# ---- hidden states and LM heads (the fused path) ---------------------------------
+#
+# Recipe: verifier weight W_t [V, Kt] ~ N(0, (sigma_z^2 / Kt)), hidden states
+# h_t [B*(N+1), Kt] ~ N(0, 1), so the verifier logits h_t W_t^T have standard
+# deviation ~ sigma_z.  The draft model reads the first Kd features:
+# W_d = W_t[:, :Kd] * sqrt(Kt / Kd) and h_d[b*N+i] = h_t[b*(N+1)+i, :Kd] +
+# N(0, rho^2), so draft and verifier logits correlate (about sqrt(Kd/Kt)).
+# Draft tokens: Gumbel-max draws from the draft's own logits at temperature T
+# (argmax at T <= 0); uniforms U[0, 1).  All tensors bf16 except the uniforms.
+FUSED_CONFIGS = {
+    "fused_small": dict(B=8, N=3, V=4096, Kt=256, Kd=128, T=1.0, sigma_z=3.0, rho=0.3),
+    "fused_mixed": dict(B=16, N=4, V=32000, Kt=512, Kd=256, T=(0.0, 0.7, 1.0), sigma_z=3.0, rho=0.5),
+    "fused": dict(B=256, N=7, V=151936, Kt=3584, Kd=896, T=0.8, sigma_z=3.0, rho=0.3),
+}
+
+
+@dataclasses.dataclass
+class FusedWorkload:
+    name: str
+    B: int
+    N: int
+    V: int
+    Kt: int
+    Kd: int
+    target_hidden: torch.Tensor   # [B*(N+1), Kt] bf16
+    target_weight: torch.Tensor   # [V, Kt] bf16
+    draft_hidden: torch.Tensor    # [B*N, Kd] bf16
+    draft_weight: torch.Tensor    # [V, Kd] bf16
+    draft_tokens: torch.Tensor    # [B, N] int32
+    uniforms: torch.Tensor        # [B, N+1] float32
+    temperature: torch.Tensor     # [B] float32
+    greedy: bool = False
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.V * (self.B * (self.N + 1) * self.Kt + self.B * self.N * self.Kd)
+
+
+def make_fused_workload(name: str, seed: int = 0, device="cpu", **overrides) -> FusedWorkload:
+    c = dict(FUSED_CONFIGS[name])
+    c.update(overrides)
+    B, N, V, Kt, Kd = c["B"], c["N"], c["V"], c["Kt"], c["Kd"]
+    dev = torch.device(device)
+    g = torch.Generator(device=dev)
+    g.manual_seed(int(seed) + 104729)
+    T_spec = c["T"]
+    if isinstance(T_spec, tuple):
+        pick = torch.randint(0, len(T_spec), (B,), generator=g, device=dev)
+        T = torch.tensor(T_spec, dtype=torch.float32, device=dev)[pick]
+    else:
+        T = torch.full((B,), float(T_spec), dtype=torch.float32, device=dev)
+    wt = torch.empty((V, Kt), dtype=torch.bfloat16, device=dev)
+    step = 8192
+    for v0 in range(0, V, step):
+        v1 = min(V, v0 + step)
+        wt[v0:v1] = (torch.randn((v1 - v0, Kt), generator=g, device=dev) * (c["sigma_z"] / Kt ** 0.5)).to(torch.bfloat16)
+    wd = (wt[:, :Kd].float() * (Kt / Kd) ** 0.5).to(torch.bfloat16).contiguous()
+    ht = torch.randn((B, N + 1, Kt), generator=g, device=dev)
+    hd = ht[:, :N, :Kd] + torch.randn((B, N, Kd), generator=g, device=dev) * c["rho"]
+    ht = ht.reshape(B * (N + 1), Kt).to(torch.bfloat16).contiguous()
+    hd = hd.reshape(B * N, Kd).to(torch.bfloat16).contiguous()
+    tokens = torch.empty((B, N), dtype=torch.int32, device=dev)
+    for b0 in range(0, B, 32):
+        b1 = min(B, b0 + 32)
+        zd = (hd[b0 * N:b1 * N].float() @ wd.float().T).view(b1 - b0, N, V)  # the draft's logits, to draw its tokens
+        Tb = T[b0:b1].view(-1, 1, 1)
+        gumbel = -torch.log(torch.empty_like(zd).exponential_(generator=g))
+        sampled = torch.argmax(zd / torch.where(Tb > 0, Tb, torch.ones_like(Tb)) + gumbel, dim=-1)
+        tokens[b0:b1] = torch.where(Tb.view(-1, 1) > 0, sampled, torch.argmax(zd, dim=-1)).to(torch.int32)
+        del zd, gumbel
+    uniforms = torch.rand((B, N + 1), generator=g, device=dev, dtype=torch.float32)
+    return FusedWorkload(name, B, N, V, Kt, Kd, ht, wt, hd, wd, tokens, uniforms, T)
+
+
 def describe(name: str) -> str:
     c = config(name)
     B, N, V = c["B"], c["N"], c["V"]
@@ -320,4 +394,5 @@ def describe(name: str) -> str:
 
 
 __all__ = ["CONFIGS", "Workload", "config", "make_workload", "describe", "TREE_CONFIGS", "TreeWorkload",
-           "tree_config", "make_tree_workload", "EAGLE16_PARENT"]
+           "tree_config", "make_tree_workload", "EAGLE16_PARENT", "FUSED_CONFIGS", "FusedWorkload",
+           "make_fused_workload"]

@@ -178,3 +178,72 @@ def compare_tree(w, gpu, orc, seqs=None, check_stats=True):
         assert s_max <= tol, f"S relative error {s_max:.3g} > {tol}"
         rep["S_rel_max"] = s_max
     return rep
+
+
+# ---- the fused LM-head path ----------------------------------------------------------
+
+# The fused path decides on float32 logits accumulated on the tensor cores from
+# bf16 products (|dz| up to a few 1e-6 at these sizes); the oracle on the
+# float64 products.  Decisions whose margin is within this band may differ.
+FUSED_BAND = 1e-4
+
+
+def run_gpu_fused(ctx, w, greedy=None, seqs=None):
+    greedy = w.greedy if greedy is None else greedy
+    st = {"target_row_stats": torch.full((w.B, w.N + 1, 2), float("nan"), device=w.target_hidden.device),
+          "draft_row_stats": torch.full((w.B, w.N, 2), float("nan"), device=w.target_hidden.device)}
+    out, nacc = ctx.run_fused(w.target_hidden, w.target_weight, None if greedy else w.draft_hidden,
+                              None if greedy else w.draft_weight, w.draft_tokens,
+                              None if greedy else w.uniforms, None if greedy else w.temperature,
+                              greedy=greedy, stats=st)
+    torch.cuda.synchronize()
+    res = {"out_tokens": out.cpu().numpy(), "num_accepted": nacc.cpu().numpy()}
+    res.update({k: v.cpu().numpy() for k, v in st.items()})
+    if seqs is not None:
+        res = {k: v[seqs] for k, v in res.items()}
+    return res
+
+
+def run_oracle_fused(w, seqs=None, threads=8, greedy=None):
+    """Float64 logits (the plain product) of the selected sequences, then the
+    verify oracle on them."""
+    greedy = w.greedy if greedy is None else greedy
+    B, N = w.B, w.N
+    sel = np.arange(B) if seqs is None else np.asarray(seqs)
+    rt = (sel[:, None] * (N + 1) + np.arange(N + 1)[None, :]).ravel()
+    rd = (sel[:, None] * N + np.arange(N)[None, :]).ravel()
+    th = w.target_hidden[torch.as_tensor(rt, device=w.target_hidden.device)]
+    zt = oracle.lm_head_logits(th, w.target_weight).reshape(len(sel), N + 1, w.V)
+    zd = None
+    if not greedy and N > 0:
+        dh = w.draft_hidden[torch.as_tensor(rd, device=w.draft_hidden.device)]
+        zd = oracle.lm_head_logits(dh, w.draft_weight).reshape(len(sel), N, w.V)
+    idx = torch.as_tensor(sel, device=w.draft_tokens.device)
+    res = oracle.verify(zt, zd, w.draft_tokens[idx], w.uniforms[idx].double(),
+                        None if greedy else w.temperature[idx].double(), greedy=greedy, dtype="f64", threads=threads)
+    # greedy decisions: the gap between the two largest logits of each verifier row
+    top2 = np.sort(zt, axis=-1)[..., -2:]
+    res["top2_gap"] = top2[..., 1] - top2[..., 0]
+    return res
+
+
+def compare_fused(w, gpu, orc, greedy=False):
+    am, sm = orc["accept_margin"], orc["sample_margin"]
+    in_band = (np.nan_to_num(am, nan=np.inf) < FUSED_BAND).any(axis=1) | (np.nan_to_num(sm, nan=np.inf) < FUSED_BAND)
+    greedy_rows = (orc["tstats"][..., 1] != orc["tstats"][..., 1]).all(axis=1) if not greedy else np.ones(len(am), bool)
+    in_band |= greedy_rows & (orc["top2_gap"] < FUSED_BAND).any(axis=1)
+    same = (gpu["out_tokens"] == orc["out_tokens"]).all(axis=1) & (gpu["num_accepted"] == orc["num_accepted"])
+    bad = np.nonzero(~same & ~in_band)[0]
+    assert bad.size == 0, (f"{bad.size} sequences differ outside the band, first {bad[0]}: gpu "
+                           f"{gpu['out_tokens'][bad[0]].tolist()} oracle {orc['out_tokens'][bad[0]].tolist()} "
+                           f"margins {am[bad[0]].tolist()} {sm[bad[0]]}")
+    ok = (orc["seq_status"] == 0)[:, None] & np.isfinite(orc["tstats"][..., 1])
+    m_err = float(np.max(np.abs(gpu["target_row_stats"][..., 0] - orc["tstats"][..., 0])[ok], initial=0.0))
+    s_rel = float(np.max((np.abs(gpu["target_row_stats"][..., 1] - orc["tstats"][..., 1]) / orc["tstats"][..., 1])[ok],
+                         initial=0.0))
+    okd = (orc["seq_status"] == 0)[:, None] & np.isfinite(orc["dstats"][..., 1])
+    d_rel = float(np.max((np.abs(gpu["draft_row_stats"][..., 1] - orc["dstats"][..., 1]) / orc["dstats"][..., 1])[okd],
+                         initial=0.0))
+    assert m_err < 1e-3 and s_rel < 1e-3 and d_rel < 1e-3, (m_err, s_rel, d_rel)
+    return {"sequences": int(len(same)), "exact": int(same.sum()), "band_sequences": int(in_band.sum()),
+            "band_mismatch": int((~same & in_band).sum()), "m_abs_max": m_err, "S_rel_max": max(s_rel, d_rel)}
