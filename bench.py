@@ -67,6 +67,17 @@ def peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def tensor_peak():
+    """Dense bf16 tensor throughput: the measured cuBLAS burst figure, else the fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        if "bf16_tflops" in d:
+            return float(d["bf16_tflops"]), "measured (cuBLAS bf16 burst)"
+    return 1900.0, "fallback"
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
 
@@ -337,6 +348,64 @@ def measure_tree(sv, torch, dev, stream, rank, steps=200, warmup=5, cpu=True):
     return res
 
 
+def measure_fused(sv, torch, dev, stream, rank, steps=20, warmup=3, batch=0):
+    """Times spec_verify_run_fused on the 256-sequence, 7-draft batch with
+    Qwen-sized heads (V = 151936; verifier K = 3584, draft K = 896) against
+    the unfused pipeline: cuBLAS (torch.matmul) writes bf16 logits, then
+    spec_verify_run verifies them.  The hidden states and weights (1.4 GB)
+    exceed L2; calls run back to back between two CUDA events."""
+    import synth
+    w = synth.make_fused_workload("fused", seed=rank, device=dev, **({"B": batch} if batch else {}))
+    ctx = sv.SpecVerify(w.B, w.N, w.V, "f32", device=dev.index or 0)
+    ctx_b = sv.SpecVerify(w.B, w.N, w.V, "bf16", device=dev.index or 0)
+    out = torch.empty((w.B, w.N + 1), dtype=torch.int32, device=dev)
+    nacc = torch.empty((w.B,), dtype=torch.int32, device=dev)
+    zt = torch.empty((w.B * (w.N + 1), w.V), dtype=torch.bfloat16, device=dev)
+    zd = torch.empty((w.B * w.N, w.V), dtype=torch.bfloat16, device=dev)
+
+    def fused():
+        ctx.run_fused(w.target_hidden, w.target_weight, w.draft_hidden, w.draft_weight, w.draft_tokens, w.uniforms,
+                      w.temperature, out_tokens=out, num_accepted=nacc, stream=stream)
+
+    def unfused():
+        torch.matmul(w.target_hidden, w.target_weight.T, out=zt)
+        torch.matmul(w.draft_hidden, w.draft_weight.T, out=zd)
+        ctx_b.run(zt.view(w.B, w.N + 1, w.V), zd.view(w.B, w.N, w.V), w.draft_tokens, w.uniforms, w.temperature,
+                  out_tokens=out, num_accepted=nacc, stream=stream)
+
+    def gemm_only():
+        torch.matmul(w.target_hidden, w.target_weight.T, out=zt)
+        torch.matmul(w.draft_hidden, w.draft_weight.T, out=zd)
+
+    res = {}
+    for name, fn in (("fused", fused), ("cublas_then_verify", unfused), ("cublas_gemms_alone", gemm_only)):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        res[name] = 1e3 * e0.elapsed_time(e1) / steps
+    if ctx.status() != sv.SV_OK or ctx_b.status() != sv.SV_OK:
+        raise RuntimeError("device status set during the fused measurement")
+    tc_peak, tc_kind = tensor_peak()
+    tflops = w.flops / (res["fused"] * 1e-6) / 1e12
+    ctx.close()
+    ctx_b.close()
+    return {"workload": f"fused: B={w.B} N={w.N} V={w.V}, verifier K={w.Kt}, draft K={w.Kd}, bf16 hidden states and "
+                        f"heads, T=0.8",
+            "us_per_call": res["fused"], "verified_rows_per_s": w.B * (w.N + 1) / (res["fused"] * 1e-6),
+            "unfused_us_per_call": res["cublas_then_verify"], "cublas_gemms_us": res["cublas_gemms_alone"],
+            "speedup_vs_unfused": res["cublas_then_verify"] / res["fused"],
+            "roofline": {"bound": "tensor", "achieved": tflops, "peak": tc_peak, "unit": "TFLOP/s",
+                         "frac": tflops / tc_peak, "flops_per_call": w.flops,
+                         "peak_kind": tc_kind},
+            "launches_per_call": 9, "steps": steps}
+
+
 def run_ours(args):
     import torch
     world, rank, local, pg = dist_init(args)
@@ -498,6 +567,9 @@ def run_ours(args):
     kv = None
     if not args.no_kv:
         kv = measure_kv_commit(sv, torch, dev, stream, nacc, w.N, max_len=args.kv_max_len)
+    fused = None
+    if not args.no_fused:
+        fused = measure_fused(sv, torch, dev, stream, rank, batch=args.fused_batch)
     tree = None
     if not args.no_tree:
         tree = measure_tree(sv, torch, dev, stream, rank, cpu=(rank == 0 and not args.no_cpu))
@@ -531,6 +603,7 @@ def run_ours(args):
         "acceptance": acc,
         "kv_commit": kv,
         "tree": tree,
+        "fused_lm_head": fused,
         "e2e": e2e,
         "cpu_baseline": cpu,
         "gpu_launches": 3 * args.steps,  # rows, mass and pick kernels per verify call
@@ -556,6 +629,8 @@ def main():
     ap.add_argument("--no-check", action="store_true")
     ap.add_argument("--no-kv", action="store_true", help="skip the KV-cache commit measurement")
     ap.add_argument("--no-tree", action="store_true", help="skip the tree-verification measurement")
+    ap.add_argument("--no-fused", action="store_true", help="skip the fused LM-head measurement")
+    ap.add_argument("--fused-batch", type=int, default=0, help="override B of the fused LM-head measurement")
     ap.add_argument("--kv-max-len", type=int, default=KV_MAX_LEN,
                     help="cache positions of the KV-commit measurement (the copy does not depend on it)")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
