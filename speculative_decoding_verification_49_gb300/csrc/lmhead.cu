@@ -7,19 +7,22 @@
 // in one forward pass, whose last step is this product of the final hidden
 // states with the LM head; the draft model ends in the same product.
 //
-// One CTA computes a 128 x 256 tile: warp 0 streams 128 x 64 tiles of the
-// hidden states and 256 x 64 tiles of the weight with 2-D TMA copies (128-byte
-// swizzle) into a 4-stage shared-memory ring; one thread of warp 1 issues
-// tcgen05.mma (M = 128, N = 256, K = 16, four per 64-wide stage) into a
-// 128 x 256 f32 accumulator in tensor memory and frees each stage with
-// tcgen05.commit; warps 4-7 read the accumulator back (tcgen05.ld, one TMEM
-// lane = one row per thread) and run the epilogue: either the logits go out
-// as f32, or (the fused verify path) only each row's statistics over the
-// tile do -- max and sum of exp2((z - max) * log2(e)/T), or max and argmax
-// for greedy rows, and the logit at the row's draft token -- so the logits
-// never reach HBM.  Every mbarrier wait is
-// bounded (2 s); a CTA that gives up sets the status word, lets its copies
-// and MMAs land and frees its tensor memory.
+// A persistent grid (one CTA per SM) walks the 128 x 256 output tiles, the
+// tiles of one 256-column weight slab next to each other so that the CTAs
+// working at the same time share that slab through L2.  Warp 0 streams
+// 128 x 64 tiles of the hidden states and 256 x 64 tiles of the weight with
+// 2-D TMA copies (128-byte swizzle) into a 4-stage shared-memory ring, across
+// tile boundaries; one thread of warp 1 issues tcgen05.mma (M = 128, N = 256,
+// K = 16, four per 64-wide stage) into one of two 128 x 256 f32 accumulators
+// in tensor memory (all 512 columns) and frees each stage with
+// tcgen05.commit; warps 4-7 read a finished accumulator back (tcgen05.ld, one
+// TMEM lane = one row per thread) while the next tile accumulates into the
+// other one, and run the epilogue: either the logits go out as f32, or (the
+// fused verify path) only each row's statistics over the tile do -- max and
+// sum of exp2((z - max) * log2(e)/T), or max and argmax for greedy rows, and
+// the logit at the row's draft token -- so the logits never reach HBM.
+// Every mbarrier wait is bounded (2 s); a CTA that gives up sets the status
+// word, lets its copies land and frees its tensor memory.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -44,15 +47,16 @@ constexpr int kTileA = kBM * kBK * 2;
 constexpr int kTileB = kBN * kBK * 2;
 constexpr int kStageBytes = kTileA + kTileB;
 constexpr int kGemmThreads = 256;
-constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTmemCols = 512;  // two 128 x 256 f32 accumulators
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int kErrTimeout = 4;
 
 struct GemmCtl {
     uint64_t full[kStagesG];
     uint64_t empty[kStagesG];
-    uint64_t accum;
-    int last_kb[kStagesG];  // last k-block issued into each stage
+    uint64_t acc_full[2];   // an accumulator holds a finished tile (MMA commit)
+    uint64_t acc_empty[2];  // the epilogue has read it (one arrival per epilogue warp)
+    int last_kb[kStagesG];  // last k-block (counted over all tiles) issued into each stage
     uint32_t tmem_base;
     int abort;
 };
@@ -133,7 +137,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     GemmCtl &ctl = *reinterpret_cast<GemmCtl *>(smem + (size_t)kStagesG * kStageBytes);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.x * kBM, n0 = blockIdx.y * kBN;
+    const int Mt = (p.M + kBM - 1) / kBM;
+    const int ntile = Mt * ((p.N + kBN - 1) / kBN);
     const int nk = (p.K + kBK - 1) / kBK;
 
     if (threadIdx.x == 0) {
@@ -142,7 +147,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             sv::mbar_init(&ctl.empty[s], 1);
             ctl.last_kb[s] = -1;
         }
-        sv::mbar_init(&ctl.accum, 1);
+        for (int b = 0; b < 2; ++b) {
+            sv::mbar_init(&ctl.acc_full[b], 1);
+            sv::mbar_init(&ctl.acc_empty[b], 4);
+        }
         ctl.abort = 0;
         sv::fence_mbar_init();
     }
@@ -159,50 +167,75 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (lane == 0) {
             sv::tma_prefetch_desc(&tmA);
             sv::tma_prefetch_desc(&tmB);
-            for (int kb = 0; kb < nk; ++kb) {
-                const int s = kb % kStagesG;
-                const uint32_t ph = (uint32_t)(kb / kStagesG) & 1u;
-                if (!sv::mbar_wait_bounded(&ctl.empty[s], ph ^ 1u, &ctl.abort, kWaitNs)) {
-                    ctl.abort = 1;
-                    break;
+            uint32_t g = 0;  // k-blocks issued so far, over all tiles
+            for (int tile = blockIdx.x; tile < ntile && !ctl.abort; tile += gridDim.x) {
+                const int m0 = (tile % Mt) * kBM, n0 = (tile / Mt) * kBN;
+                for (int kb = 0; kb < nk; ++kb, ++g) {
+                    const int s = (int)(g % kStagesG);
+                    const uint32_t ph = (g / kStagesG) & 1u;
+                    if (!sv::mbar_wait_bounded(&ctl.empty[s], ph ^ 1u, &ctl.abort, kWaitNs)) {
+                        ctl.abort = 1;
+                        break;
+                    }
+                    unsigned char *a = smem + (size_t)s * kStageBytes;
+                    sv::mbar_arrive_expect_tx(&ctl.full[s], kStageBytes);
+                    sv::tma_load_2d(a, &tmA, kb * kBK, m0, &ctl.full[s]);
+                    sv::tma_load_2d(a + kTileA, &tmB, kb * kBK, n0, &ctl.full[s]);
+                    ctl.last_kb[s] = (int)g;
                 }
-                unsigned char *a = smem + (size_t)s * kStageBytes;
-                sv::mbar_arrive_expect_tx(&ctl.full[s], kStageBytes);
-                sv::tma_load_2d(a, &tmA, kb * kBK, m0, &ctl.full[s]);
-                sv::tma_load_2d(a + kTileA, &tmB, kb * kBK, n0, &ctl.full[s]);
-                ctl.last_kb[s] = kb;
             }
         }
         __syncwarp();
     } else if (warp == 1) {
         if (lane == 0) {
             constexpr uint32_t idesc = sv::idesc_bf16_f32(kBM, kBN);
-            for (int kb = 0; kb < nk; ++kb) {
-                const int s = kb % kStagesG;
-                const uint32_t ph = (uint32_t)(kb / kStagesG) & 1u;
-                if (!sv::mbar_wait_bounded(&ctl.full[s], ph, &ctl.abort, kWaitNs)) {
+            uint32_t g = 0;
+            int t = 0;
+            for (int tile = blockIdx.x; tile < ntile && !ctl.abort; tile += gridDim.x, ++t) {
+                const int buf = t & 1;
+                const uint32_t use = (uint32_t)(t >> 1);
+                // the epilogue has finished with this accumulator's previous tile
+                if (!sv::mbar_wait_bounded(&ctl.acc_empty[buf], (use & 1u) ^ 1u, &ctl.abort, kWaitNs)) {
                     ctl.abort = 1;
                     break;
                 }
                 sv::tc_fence_after();
-                const unsigned char *a = smem + (size_t)s * kStageBytes;
-                const uint64_t da = sv::smem_desc_k128(a), db = sv::smem_desc_k128(a + kTileA);
+                const uint32_t d = tmem + (uint32_t)(buf * kBN);
+                for (int kb = 0; kb < nk; ++kb, ++g) {
+                    const int s = (int)(g % kStagesG);
+                    const uint32_t ph = (g / kStagesG) & 1u;
+                    if (!sv::mbar_wait_bounded(&ctl.full[s], ph, &ctl.abort, kWaitNs)) {
+                        ctl.abort = 1;
+                        break;
+                    }
+                    sv::tc_fence_after();
+                    const unsigned char *a = smem + (size_t)s * kStageBytes;
+                    const uint64_t da = sv::smem_desc_k128(a), db = sv::smem_desc_k128(a + kTileA);
 #pragma unroll
-                for (int kk = 0; kk < kBK / 16; ++kk)  // K = 16 per MMA: 32 bytes along the swizzled row
-                    sv::tc_mma_bf16(tmem, da + 2u * kk, db + 2u * kk, idesc, (kb | kk) != 0);
-                sv::tc_commit(&ctl.empty[s]);  // the stage is free once these MMAs have read it
+                    for (int kk = 0; kk < kBK / 16; ++kk)  // K = 16 per MMA: 32 bytes along the swizzled row
+                        sv::tc_mma_bf16(d, da + 2u * kk, db + 2u * kk, idesc, (kb | kk) != 0);
+                    sv::tc_commit(&ctl.empty[s]);  // the stage is free once these MMAs have read it
+                }
+                sv::tc_commit(&ctl.acc_full[buf]);  // the tile is complete
             }
-            sv::tc_commit(&ctl.accum);  // the accumulator is complete
         }
         __syncwarp();
     } else if (warp >= 4) {
-        int never = 0;
-        const bool ok = sv::mbar_wait_bounded(&ctl.accum, 0, &never, kWaitNs);
-        sv::tc_fence_after();
         const int q = warp - 4;  // TMEM lanes 32q .. 32q+31
-        const int row = m0 + 32 * q + lane;
-        if (__all_sync(0xffffffffu, ok && !ctl.abort)) {  // tcgen05.ld is warp-collective
-            const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16);
+        int t = 0;
+        for (int tile = blockIdx.x; tile < ntile; tile += gridDim.x, ++t) {
+            const int buf = t & 1;
+            const uint32_t use = (uint32_t)(t >> 1);
+            const bool ok = sv::mbar_wait_bounded(&ctl.acc_full[buf], use & 1u, &ctl.abort, kWaitNs);
+            if (!__all_sync(0xffffffffu, ok && !ctl.abort)) {  // tcgen05.ld is warp-collective
+                if (lane == 0 && p.status)
+                    atomicOr(p.status, kErrTimeout);
+                break;
+            }
+            sv::tc_fence_after();
+            const int m0 = (tile % Mt) * kBM, n0 = (tile / Mt) * kBN;
+            const int row = m0 + 32 * q + lane;
+            const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * kBN);
             if constexpr (STATS) {
                 row_stats(taddr, n0, p, row);
             } else {
@@ -217,10 +250,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                 }
             }
-        } else if (lane == 0 && p.status) {
-            atomicOr(p.status, kErrTimeout);
+            sv::tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                sv::mbar_arrive(&ctl.acc_empty[buf]);
         }
-        __syncwarp();
     }
     sv::tc_fence_before();
     __syncthreads();
@@ -302,7 +336,13 @@ sv_status launch(const void *hidden, const void *weight, int M, int V, int K, co
     CUtensorMap ta, tb;
     if (!make_map(&ta, hidden, M, K, kBM) || !make_map(&tb, weight, V, K, kBN))
         return SV_ERR_CUDA;
-    const dim3 grid((unsigned)((M + kBM - 1) / kBM), (unsigned)((V + kBN - 1) / kBN));
+    const long long ntile = (long long)((M + kBM - 1) / kBM) * ((V + kBN - 1) / kBN);
+    if (ntile > INT_MAX)
+        return SV_ERR_INVALID_ARG;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return SV_ERR_CUDA;
+    const unsigned grid = (unsigned)(ntile < sms ? ntile : sms);  // one CTA per SM walks the tiles
     sv_lmhead_kernel<STATS><<<grid, kGemmThreads, kSmemG, st>>>(ta, tb, p);
     if (cudaGetLastError() != cudaSuccess)
         return SV_ERR_CUDA;
