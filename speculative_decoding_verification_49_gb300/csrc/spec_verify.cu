@@ -1034,11 +1034,130 @@ __device__ __forceinline__ float slice_thread_mass(const uint4 *tsrc, const uint
 
 constexpr int kMaxRowSlices = kMaxCluster * kMaxSlices;  // slices of the longest supported row
 
+// ---- inverse CDF over slice masses (kernel C and the tree walk) ---------------
+// Warp-wide: the first slice whose cumulative mass exceeds x, and x1 = x minus
+// the mass before it; when rounding leaves x at or above the total, the last
+// slice with mass and x1 = INFINITY.  Cumulative sums are warp-inclusive scans
+// in slice order.
+__device__ __forceinline__ void warp_find_slice(const float *slice, int S, float x, int lane, int &cs, float &x1)
+{
+    cs = -1;
+    x1 = INFINITY;
+    float run = 0.0f;
+    for (int c0 = 0; c0 < S && cs < 0; c0 += 32) {
+        const int c = c0 + lane;
+        const float m = (c < S) ? slice[c] : 0.0f;
+        const float inc = __fadd_rn(warp_incl_scan(m, lane), run);
+        const unsigned hit = __ballot_sync(0xffffffffu, c < S && x < inc);
+        if (hit) {
+            const int l = __ffs(hit) - 1;
+            const float prev = __shfl_sync(0xffffffffu, inc, l > 0 ? l - 1 : 0);
+            cs = c0 + l;
+            x1 = __fsub_rn(x, l > 0 ? prev : run);
+        }
+        run = __shfl_sync(0xffffffffu, inc, 31);
+    }
+    if (cs < 0) {  // rounding: the last slice that has mass
+        for (int c0 = ((S - 1) / 32) * 32; c0 >= 0 && cs < 0; c0 -= 32) {
+            const int c = c0 + lane;
+            const unsigned m = __ballot_sync(0xffffffffu, c < S && slice[c] > 0.0f);
+            if (m)
+                cs = c0 + 31 - __clz(m);
+        }
+        if (cs < 0)
+            cs = S - 1;
+        x1 = INFINITY;
+    }
+}
+
+// Element search inside slice ss, whose masses thread t holds for vector t
+// (r[VE] and their sum `part`; threads past the 256 of a slice pass zeros):
+// warp totals in warp order, then the lane, then the element where the
+// cumulative mass first exceeds x1; rounding falls back to the last element
+// with mass.  Every thread of the block calls it (it synchronises the block).
+struct PickState {
+    float incl[kConsThreads];
+    int sel, token;
+    float xl;
+};
+
+template <int VE>
+__device__ int pick_in_slice(PickState &ps, int ss, float part, const float *r, float x1, int NV)
+{
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const float incl = warp_incl_scan(part, lane);
+    if (tid < kConsThreads)
+        ps.incl[tid] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int sel = -1;
+        float xl = 0.0f;
+        if (x1 != INFINITY) {
+            const float wt = (lane < kConsWarps) ? ps.incl[lane * 32 + 31] : 0.0f;
+            float wc = 0.0f, wprev = 0.0f;
+            int ws = -1;
+            for (int w = 0; w < kConsWarps; ++w) {
+                const float wtw = __shfl_sync(0xffffffffu, wt, w);
+                const float next = __fadd_rn(wc, wtw);
+                if (ws < 0 && x1 < next) {
+                    ws = w;
+                    wprev = wc;
+                }
+                wc = next;
+            }
+            if (ws >= 0) {
+                const float xw = __fsub_rn(x1, wprev);
+                const float li = ps.incl[ws * 32 + lane];
+                const unsigned ml = __ballot_sync(0xffffffffu, xw < li);
+                if (ml) {
+                    const int ls = __ffs(ml) - 1;
+                    const float lprev = __shfl_sync(0xffffffffu, li, ls > 0 ? ls - 1 : 0);
+                    sel = ws * 32 + ls;
+                    xl = __fsub_rn(xw, ls > 0 ? lprev : 0.0f);
+                }
+            }
+        }
+        if (lane == 0) {
+            ps.sel = sel;
+            ps.xl = xl;
+            ps.token = -1;
+        }
+    }
+    __syncthreads();
+    if (ps.sel >= 0 && tid == ps.sel) {
+        float acc = 0.0f;
+        for (int e = 0; e < VE; ++e) {
+            acc = __fadd_rn(acc, r[e]);
+            if (ps.xl < acc) {
+                ps.token = (ss * kSliceVecs + tid) * VE + e;
+                break;
+            }
+        }
+    }
+    __syncthreads();
+    if (ps.token < 0) {
+        if (tid == 0)
+            ps.sel = -1;
+        __syncthreads();
+        if (tid < kConsThreads)
+            for (int e = VE - 1; e >= 0; --e)
+                if (r[e] > 0.0f) {
+                    atomicMax(&ps.sel, (ss * kSliceVecs + tid) * VE + e);
+                    break;
+                }
+        __syncthreads();
+        if (tid == 0)
+            ps.token = ps.sel >= 0 ? ps.sel : min(NV, (ss + 1) * kSliceVecs) * VE - 1;
+        __syncthreads();
+    }
+    return ps.token;
+}
+
 struct PickShared {
     float slice[kMaxRowSlices];  // the sequence's slice masses
-    float incl[kPickThreads];
     float wtot[kConsWarps];
-    int sstar, retry, token;
+    PickState ps;
+    int sstar, retry;
     float x1;
 };
 
@@ -1137,33 +1256,9 @@ __global__ void __launch_bounds__(kPickThreads) sv_pick_kernel(const SvParams p)
                 carry = __shfl_sync(0xffffffffu, __fadd_rn(warp_incl_scan(m, lane), carry), 31);
             }
             const float Rt = carry;
-            const float x = __fmul_rn(sq.uN, Rt);
-            int cs = -1;
-            float x1 = INFINITY, run = 0.0f;
-            for (int c0 = 0; c0 < S && cs < 0; c0 += 32) {
-                const int c = c0 + lane;
-                const float m = (c < S) ? sh.slice[c] : 0.0f;
-                const float inc = __fadd_rn(warp_incl_scan(m, lane), run);
-                const unsigned hit = __ballot_sync(0xffffffffu, c < S && x < inc);
-                if (hit) {
-                    const int l = __ffs(hit) - 1;
-                    const float prev = __shfl_sync(0xffffffffu, inc, l > 0 ? l - 1 : 0);
-                    cs = c0 + l;
-                    x1 = __fsub_rn(x, l > 0 ? prev : run);
-                }
-                run = __shfl_sync(0xffffffffu, inc, 31);
-            }
-            if (cs < 0) {  // rounding: the last slice that has mass
-                for (int c0 = ((S - 1) / 32) * 32; c0 >= 0 && cs < 0; c0 -= 32) {
-                    const int c = c0 + lane;
-                    const unsigned m = __ballot_sync(0xffffffffu, c < S && sh.slice[c] > 0.0f);
-                    if (m)
-                        cs = c0 + 31 - __clz(m);
-                }
-                if (cs < 0)
-                    cs = S - 1;
-                x1 = INFINITY;
-            }
+            int cs;
+            float x1;
+            warp_find_slice(sh.slice, S, __fmul_rn(sq.uN, Rt), lane, cs, x1);
             if (lane == 0) {
                 sh.retry = (Rt == 0.0f && sq.res_mode == RES_DIFF) ? 1 : 0;
                 sh.sstar = cs;
@@ -1176,86 +1271,14 @@ __global__ void __launch_bounds__(kPickThreads) sv_pick_kernel(const SvParams p)
         __syncthreads();
     }
 
-    // recompute slice s*: warp totals equal kernel B's, then warp, lane, element
+    // recompute slice s* (warp totals equal kernel B's), then warp, lane, element
     const int ss = sh.sstar;
     const float part = slice_thread_mass<DT>(tsrc, dsrc, ss, NV, tid, sq, r);
-    const float incl = warp_incl_scan(part, lane);
-    sh.incl[tid] = incl;
-    __syncthreads();
-    // thread that owns the target: broadcast its element values through r
-    const float x1 = sh.x1;
-    int sel = -1;
-    float xl = 0.0f;
-    if (warp == 0 && x1 != INFINITY) {
-        const float wt = (lane < kConsWarps) ? sh.incl[lane * 32 + 31] : 0.0f;
-        float wc = 0.0f;  // warp totals added in warp order, as kernel B does
-        float wprev = 0.0f;
-        int ws = -1;
-        for (int w = 0; w < kConsWarps; ++w) {
-            const float wtw = __shfl_sync(0xffffffffu, wt, w);
-            const float next = __fadd_rn(wc, wtw);
-            if (ws < 0 && x1 < next) {
-                ws = w;
-                wprev = wc;
-            }
-            wc = next;
-        }
-        if (ws >= 0) {
-            const float xw = __fsub_rn(x1, wprev);
-            const float li = sh.incl[ws * 32 + lane];
-            const unsigned ml = __ballot_sync(0xffffffffu, xw < li);
-            if (ml) {
-                const int ls = __ffs(ml) - 1;
-                const float lprev = __shfl_sync(0xffffffffu, li, ls > 0 ? ls - 1 : 0);
-                sel = ws * 32 + ls;
-                xl = __fsub_rn(xw, ls > 0 ? lprev : 0.0f);
-            }
-        }
-        if (lane == 0) {
-            sh.sstar = sel;  // reused: the selected thread
-            sh.x1 = xl;
-        }
-    }
-    __syncthreads();
-    sel = sh.sstar;
-    xl = sh.x1;
-    if (tid == (sel >= 0 ? sel : 0)) {
-        int token = -1;
-        if (sel >= 0) {
-            float acc = 0.0f;
-            for (int e = 0; e < VE; ++e) {
-                acc = __fadd_rn(acc, r[e]);
-                if (xl < acc) {
-                    token = (ss * kSliceVecs + tid) * VE + e;
-                    break;
-                }
-            }
-        }
-        sh.token = token;  // -1 if rounding left it unset
-    }
-    __syncthreads();
-    if (sh.token < 0) {
-        // rounding: the last element of slice s* that carries mass
-        if (tid == 0)
-            sh.sstar = -1;
-        __syncthreads();
-        int mine = -1;
-        for (int e = VE - 1; e >= 0; --e)
-            if (r[e] > 0.0f) {
-                mine = (ss * kSliceVecs + tid) * VE + e;
-                break;
-            }
-        if (mine >= 0)
-            atomicMax(&sh.sstar, mine);
-        __syncthreads();
-        if (tid == 0)
-            sh.token = sh.sstar >= 0 ? sh.sstar : min(NV, (ss + 1) * kSliceVecs) * VE - 1;
-        __syncthreads();
-    }
+    const int token = pick_in_slice<VE>(sh.ps, ss, part, r, sh.x1, NV);
     if (tid == 0) {
         for (int k = 0; k < j; ++k)
             out[k] = p.tokens[(size_t)b * N + k];
-        out[j] = sh.token;
+        out[j] = token;
         for (int k = j + 1; k <= N; ++k)
             out[k] = -1;
         p.nacc[b] = j;
@@ -1300,9 +1323,9 @@ struct CtlW {
     float shares[kMaxWalkSlices * kConsWarps];  // warp shares of every slice of the current pass
     float slice[kMaxWalkSlices];                // slice masses
     float invR[kMaxTreeNodes];                  // 1/R_1 .. 1/R_k of the current node
-    float incl[kConsThreads];
+    PickState ps;
     int kids[kMaxTreeNodes];
-    int nkids, accept, sstar, token;
+    int nkids, accept, sstar;
     float Rt, x1, cf;
 };
 
@@ -1471,33 +1494,9 @@ __device__ int walk_pick(CtlW &w, const uint4 *tsrc, const uint4 *dsrc, int NV, 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int S = (NV + kSliceVecs - 1) / kSliceVecs;
     if (warp == 0) {
-        const float x = __fmul_rn(u, w.Rt);
-        int cs = -1;
-        float x1 = INFINITY, run = 0.0f;
-        for (int c0 = 0; c0 < S && cs < 0; c0 += 32) {
-            const int c = c0 + lane;
-            const float m = (c < S) ? w.slice[c] : 0.0f;
-            const float inc = __fadd_rn(warp_incl_scan(m, lane), run);
-            const unsigned hit = __ballot_sync(0xffffffffu, c < S && x < inc);
-            if (hit) {
-                const int l = __ffs(hit) - 1;
-                const float prev = __shfl_sync(0xffffffffu, inc, l > 0 ? l - 1 : 0);
-                cs = c0 + l;
-                x1 = __fsub_rn(x, l > 0 ? prev : run);
-            }
-            run = __shfl_sync(0xffffffffu, inc, 31);
-        }
-        if (cs < 0) {  // rounding: the last slice that has mass
-            for (int c0 = ((S - 1) / 32) * 32; c0 >= 0 && cs < 0; c0 -= 32) {
-                const int c = c0 + lane;
-                const unsigned m = __ballot_sync(0xffffffffu, c < S && w.slice[c] > 0.0f);
-                if (m)
-                    cs = c0 + 31 - __clz(m);
-            }
-            if (cs < 0)
-                cs = S - 1;
-            x1 = INFINITY;
-        }
+        int cs;
+        float x1;
+        warp_find_slice(w.slice, S, __fmul_rn(u, w.Rt), lane, cs, x1);
         if (lane == 0) {
             w.sstar = cs;
             w.x1 = x1;
@@ -1509,85 +1508,16 @@ __device__ int walk_pick(CtlW &w, const uint4 *tsrc, const uint4 *dsrc, int NV, 
 #pragma unroll
     for (int e = 0; e < VE; ++e)
         r[e] = 0.0f;
-    if (warp < kConsWarps) {
-        const int vec = ss * kSliceVecs + tid;
-        float part = 0.0f;
-        if (vec < NV) {
-            const uint4 vd = dsrc ? __ldcg(dsrc + vec) : make_uint4(0, 0, 0, 0);
-            tree_vec<DT>(__ldcg(tsrc + vec), vd, diff, k, w.invR, mq, isq, mp, isp, cf, r);
+    float part = 0.0f;
+    const int vec = ss * kSliceVecs + tid;
+    if (tid < kConsThreads && vec < NV) {
+        const uint4 vd = dsrc ? __ldcg(dsrc + vec) : make_uint4(0, 0, 0, 0);
+        tree_vec<DT>(__ldcg(tsrc + vec), vd, diff, k, w.invR, mq, isq, mp, isp, cf, r);
 #pragma unroll
-            for (int e = 0; e < VE; ++e)
-                part = __fadd_rn(part, r[e]);
-        }
-        w.incl[tid] = warp_incl_scan(part, lane);
+        for (int e = 0; e < VE; ++e)
+            part = __fadd_rn(part, r[e]);
     }
-    __syncthreads();
-    const float x1 = w.x1;
-    if (warp == 0) {
-        int sel = -1;
-        float xl = 0.0f;
-        if (x1 != INFINITY) {
-            const float wt = (lane < kConsWarps) ? w.incl[lane * 32 + 31] : 0.0f;
-            float wc = 0.0f, wprev = 0.0f;
-            int ws = -1;
-            for (int q = 0; q < kConsWarps; ++q) {
-                const float wtw = __shfl_sync(0xffffffffu, wt, q);
-                const float next = __fadd_rn(wc, wtw);
-                if (ws < 0 && x1 < next) {
-                    ws = q;
-                    wprev = wc;
-                }
-                wc = next;
-            }
-            if (ws >= 0) {
-                const float xw = __fsub_rn(x1, wprev);
-                const float li = w.incl[ws * 32 + lane];
-                const unsigned ml = __ballot_sync(0xffffffffu, xw < li);
-                if (ml) {
-                    const int ls = __ffs(ml) - 1;
-                    const float lprev = __shfl_sync(0xffffffffu, li, ls > 0 ? ls - 1 : 0);
-                    sel = ws * 32 + ls;
-                    xl = __fsub_rn(xw, ls > 0 ? lprev : 0.0f);
-                }
-            }
-        }
-        if (lane == 0) {
-            w.sstar = sel;  // reused: the selected thread
-            w.x1 = xl;
-            w.token = -1;
-        }
-    }
-    __syncthreads();
-    const int sel = w.sstar;
-    if (sel >= 0 && tid == sel) {
-        float acc = 0.0f;
-        for (int e = 0; e < VE; ++e) {
-            acc = __fadd_rn(acc, r[e]);
-            if (w.x1 < acc) {
-                w.token = (ss * kSliceVecs + tid) * VE + e;
-                break;
-            }
-        }
-    }
-    __syncthreads();
-    if (w.token < 0) {
-        // rounding: the last element of slice s* that carries mass
-        if (tid == 0)
-            w.sstar = -1;
-        __syncthreads();
-        if (warp < kConsWarps) {
-            for (int e = VE - 1; e >= 0; --e)
-                if (r[e] > 0.0f) {
-                    atomicMax(&w.sstar, (ss * kSliceVecs + tid) * VE + e);
-                    break;
-                }
-        }
-        __syncthreads();
-        if (tid == 0)
-            w.token = w.sstar >= 0 ? w.sstar : min(NV, (ss + 1) * kSliceVecs) * VE - 1;
-        __syncthreads();
-    }
-    return w.token;
+    return pick_in_slice<VE>(w.ps, ss, part, r, w.x1, NV);
 }
 
 template <int DT>
