@@ -1317,6 +1317,7 @@ constexpr int kWalkProducerWarp = kWalkGroups * kConsWarps;
 static_assert(kWalkThreads <= 1024, "a CTA holds at most 1024 threads");
 constexpr int kMaxTreeNodes = 1024;         // nodes per tree (root included)
 constexpr int kMaxWalkSlices = 512;         // slices of one row: V*elt <= 2 MiB
+constexpr int kMaxWalkCluster = 4;          // CTAs (SMs) that share one tree's passes
 
 struct CtlW {
     Ring<kStagesW> ring;
@@ -1414,25 +1415,60 @@ __device__ __forceinline__ bool first_child_test(float zq, float zp, float mq, f
     return u < fmin(1.0, ratio);
 }
 
+// Ring tile of the i-th tile this CTA streams in a pass: a cluster of C CTAs
+// splits the row pair's tiles in blocks of kWalkGroups (one per consumer group).
+__device__ __forceinline__ int walk_tile(int i, uint32_t rank, uint32_t C)
+{
+    return (int)(((uint32_t)(i / kWalkGroups) * C + rank) * kWalkGroups) + i % kWalkGroups;
+}
+
 // One pass over the row pair of a node: the slice masses of r_k (diff false)
 // or (r_k - p)+ (diff true) into w.slice, their total into w.Rt.  Every thread
-// of the CTA calls it; g is the ring position, advanced by the pass.
+// of every CTA of the cluster calls it; g is this CTA's ring position,
+// advanced by the pass.  Each CTA streams its share of the tiles, writes the
+// warp shares of those slices into its own shared memory, and after a cluster
+// barrier every CTA adds up every slice (reading the peers' shares over
+// distributed shared memory) in the same order, so all of them hold the same
+// slice masses and total.
 template <int DT>
 __device__ void walk_mass_pass(CtlW &w, unsigned char *ring, uint32_t &g, const uint4 *tsrc, const uint4 *dsrc,
                                int NV, bool diff, int k, float mq, float isq, float mp, float isp, float cf)
 {
     constexpr int VE = Elt<DT>::kPerVec;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t C = sv::cluster_nctarank(), rank = sv::cluster_ctarank();
     const int NT = (NV + kTileVecs - 1) / kTileVecs;
     const int S = (NV + kSliceVecs - 1) / kSliceVecs;
+    int n_own = 0;  // tiles this CTA streams: a prefix i = 0 .. n_own-1 of its sequence
+    while (walk_tile(n_own, rank, C) < NT)
+        ++n_own;
     if (warp == kWalkProducerWarp) {
-        if (lane == 0)
-            produce(w.ring, ring, tsrc, dsrc, NV, 0, NT, g);
+        if (lane == 0) {
+            for (int i = 0; i < n_own; ++i) {
+                const uint32_t gi = g + (uint32_t)i;
+                const uint32_t st = gi % kStagesW;
+                if (!sv::mbar_wait_bounded(&w.ring.empty[st], ((gi / kStagesW) & 1u) ^ 1u, &w.ring.abort,
+                                           kWaitLimitNs)) {
+                    w.ring.abort = 1;
+                    break;
+                }
+                const int t = walk_tile(i, rank, C);
+                const int nvec = min(kTileVecs, NV - t * kTileVecs);
+                const uint32_t bytes = static_cast<uint32_t>(nvec) * 16u;
+                sv::mbar_arrive_expect_tx(&w.ring.full[st], dsrc ? 2u * bytes : bytes);
+                unsigned char *stage = ring + st * (2 * kTileBytes);
+                sv::bulk_g2s(stage, tsrc + (size_t)t * kTileVecs, bytes, &w.ring.full[st]);
+                if (dsrc)
+                    sv::bulk_g2s(stage + kTileBytes, dsrc + (size_t)t * kTileVecs, bytes, &w.ring.full[st]);
+                w.ring.last_g[st] = static_cast<int>(gi);
+            }
+        }
         __syncwarp();
     } else {
         const int grp = warp / kConsWarps, lt = tid - grp * kConsThreads, lw = warp - grp * kConsWarps;
-        for (int t = grp; t < NT; t += kWalkGroups) {
-            const uint32_t gt = g + (uint32_t)t;
+        for (int i = grp; i < n_own; i += kWalkGroups) {
+            const uint32_t gt = g + (uint32_t)i;
+            const int t = walk_tile(i, rank, C);
             if (consume_wait(w.ring, gt)) {
                 const unsigned char *stage = ring + (gt % kStagesW) * (2 * kTileBytes);
 #pragma unroll
@@ -1461,15 +1497,25 @@ __device__ void walk_mass_pass(CtlW &w, unsigned char *ring, uint32_t &g, const 
             consume_release(w.ring, gt, lane);
         }
     }
-    g += (uint32_t)NT;
-    __syncthreads();
+    g += (uint32_t)n_own;
+    if (C > 1)
+        sv::cluster_sync();  // every CTA's shares are visible cluster-wide
+    else
+        __syncthreads();
     for (int sl = tid; sl < S; sl += kWalkThreads) {
+        const uint32_t owner = (uint32_t)((sl / kVPT) / kWalkGroups) % C;
         float tot = 0.0f;
-        for (int q = 0; q < kConsWarps; ++q)
-            tot = __fadd_rn(tot, w.shares[sl * kConsWarps + q]);
+        for (int q = 0; q < kConsWarps; ++q) {
+            const float v = (owner == rank) ? w.shares[sl * kConsWarps + q]
+                                            : sv::ld_dsmem_f32(sv::dsmem_addr(&w.shares[sl * kConsWarps + q], owner));
+            tot = __fadd_rn(tot, v);
+        }
         w.slice[sl] = tot;
     }
-    __syncthreads();
+    if (C > 1)
+        sv::cluster_sync();  // no peer reads these shares any more: the next pass may overwrite them
+    else
+        __syncthreads();
     if (warp == 0) {
         float carry = 0.0f;
         for (int c0 = 0; c0 < S; c0 += 32) {
@@ -1528,7 +1574,9 @@ __global__ void __launch_bounds__(kWalkThreads, 1) sv_tree_walk_kernel(const SvP
     unsigned char *ring = smem;
     CtlW &w = *reinterpret_cast<CtlW *>(smem + ring_bytes(kStagesW));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int b = blockIdx.x, M = p.N, V = p.V, NV = V / VE;
+    const uint32_t C = sv::cluster_nctarank(), rank = sv::cluster_ctarank();
+    const int b = blockIdx.x / (int)C, M = p.N, V = p.V, NV = V / VE;
+    const bool leader = rank == 0;  // every CTA of the cluster walks the tree; the leader writes
     const size_t row0 = (size_t)b * (M + 1);
     const int32_t *par = p.parent + row0;
     const int32_t *tok = p.tokens + row0;
@@ -1545,7 +1593,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) sv_tree_walk_kernel(const SvP
     __syncthreads();
     const int err = __ldcg(&p.ws_err[b]);
     if (err || mode == MODE_INVALID) {
-        if (tid == 0) {
+        if (tid == 0 && leader) {
             for (int q = 0; q <= M; ++q) {
                 out[q] = -1;
                 path[q] = -1;
@@ -1560,6 +1608,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1) sv_tree_walk_kernel(const SvP
     }
     int depth = 0;
     if (mode == MODE_GREEDY) {
+        if (!leader)
+            return;
         if (tid == 0) {
             int n = 0;
             for (;;) {
@@ -1642,7 +1692,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) sv_tree_walk_kernel(const SvP
                 __syncthreads();
             }
             if (accepted >= 0) {
-                if (tid == 0) {
+                if (tid == 0 && leader) {
                     out[depth] = tok[accepted];
                     path[depth] = accepted;
                 }
@@ -1662,12 +1712,12 @@ __global__ void __launch_bounds__(kWalkThreads, 1) sv_tree_walk_kernel(const SvP
             }
             const int t = walk_pick<DT>(w, tsrc, (diff || kk > 0) ? dsrc : nullptr, NV, diff, kk, mq, isq, mp, isp,
                                         cf, u0);
-            if (tid == 0)
+            if (tid == 0 && leader)
                 out[depth] = t;
             break;
         }
     }
-    if (tid == 0) {
+    if (tid == 0 && leader) {
         for (int q = depth + 1; q <= M; ++q)
             out[q] = -1;
         for (int q = depth; q <= M; ++q)
@@ -1676,10 +1726,10 @@ __global__ void __launch_bounds__(kWalkThreads, 1) sv_tree_walk_kernel(const SvP
         if (p.hist)
             atomicAdd(&p.hist[depth], 1ull);
         p.ws_err[b] = 0;
-        if (w.ring.abort) {
-            atomicOr(p.status, kErrTimeout);
-            ring_drain(w.ring);
-        }
+    }
+    if (tid == 0 && w.ring.abort) {
+        atomicOr(p.status, kErrTimeout);
+        ring_drain(w.ring);
     }
 }
 
@@ -2145,13 +2195,22 @@ sv_status tree_run_impl(spec_verify_ctx *ctx, const void *target, const void *dr
         cudaLaunchAttribute pdl[1];
         pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         pdl[0].val.programmaticStreamSerializationAllowed = 1;
+        // a cluster of CW CTAs per tree splits each residual pass (one CTA per SM)
+        int CW = ctx->num_sms / B;
+        CW = CW < 1 ? 1 : CW > kMaxWalkCluster ? kMaxWalkCluster : CW;
+        cudaLaunchAttribute wattr[2];
+        wattr[0] = pdl[0];
+        wattr[1].id = cudaLaunchAttributeClusterDimension;
+        wattr[1].val.clusterDim.x = (unsigned)CW;
+        wattr[1].val.clusterDim.y = 1;
+        wattr[1].val.clusterDim.z = 1;
         cudaLaunchConfig_t cfgw = {};
-        cfgw.gridDim = dim3((unsigned)B);
+        cfgw.gridDim = dim3((unsigned)(B * CW));
         cfgw.blockDim = dim3(kWalkThreads);
         cfgw.dynamicSmemBytes = kSmemW;
         cfgw.stream = st;
-        cfgw.attrs = pdl;
-        cfgw.numAttrs = 1;
+        cfgw.attrs = wattr;
+        cfgw.numAttrs = 2;
         e = (ctx->dtype == SV_BF16) ? cudaLaunchKernelEx(&cfgw, sv_tree_walk_kernel<SV_BF16>, prm)
                                     : cudaLaunchKernelEx(&cfgw, sv_tree_walk_kernel<SV_F32>, prm);
     }
