@@ -72,6 +72,17 @@ def test_tree_run_host_validation_without_gpu(lib):
     assert tr(None, *args) == sv.SV_ERR_INVALID_ARG  # no context: rejected before any CUDA call
 
 
+def test_fused_and_lm_head_host_validation_without_gpu(lib):
+    fr = lib.spec_verify_run_fused
+    args = (16, 16, 64, 16, 16, 64, 16, 16, 16, 0, 2, 3, 16, 16, None, None, None)
+    assert fr(None, *args) == sv.SV_ERR_INVALID_ARG  # no context
+    lm = lib.spec_verify_lm_head_logits
+    assert lm(16, 16, 4, 8, 12, 16, None) == sv.SV_ERR_INVALID_ARG   # K not a multiple of 8
+    assert lm(16, 16, -1, 8, 16, 16, None) == sv.SV_ERR_INVALID_ARG  # negative rows
+    assert lm(24, 16, 4, 8, 16, 16, None) == sv.SV_ERR_INVALID_ARG   # misaligned hidden states
+    assert lm(16, 16, 0, 8, 16, 16, None) == sv.SV_OK                # nothing to do
+
+
 def test_kv_commit_host_validation_without_gpu(lib):
     kv = sv.spec_verify_kv_commit
     ok = (256, 512, 1024, 2048, None)  # scratch, cache, cache_len, num_accepted, status
