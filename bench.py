@@ -403,7 +403,7 @@ def measure_fused(sv, torch, dev, stream, rank, steps=20, warmup=3, batch=0):
             "roofline": {"bound": "tensor", "achieved": tflops, "peak": tc_peak, "unit": "TFLOP/s",
                          "frac": tflops / tc_peak, "flops_per_call": w.flops,
                          "peak_kind": tc_kind},
-            "launches_per_call": 9, "steps": steps}
+            "launches_per_call": 8, "steps": steps}
 
 
 def run_ours(args):

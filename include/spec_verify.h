@@ -25,7 +25,9 @@
  * All tensors are caller-owned device memory, C-contiguous, row-major.  The
  * library never allocates or synchronises inside spec_verify_run; the run (three
  * kernel launches) is enqueued on the caller's stream and completes
- * asynchronously.
+ * asynchronously.  Further entry points below: tree verification, the verify
+ * fused into the LM-head products, the LM-head product alone, the KV-cache
+ * commit, acceptance counters, kernel timing and an allocation-free variant.
  *
  * Thread-safety: a context holds a small workspace that every run updates;
  * use one context per stream (runs on one stream are serialised by it).
@@ -63,8 +65,9 @@ typedef enum { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
  * Allocates a workspace of about 8*(max_N+2) + 8*max_B + 20*max_B*(max_N+1) +
  * 32*max_B*ceil(V*elt/4 KiB) bytes (per-sequence first-rejection slots and
  * error flags; per-position argmax and row statistics; per-slice residual
- * masses, the acceptance counters) and one status word; nothing else is
- * allocated later.
+ * masses, the acceptance counters) and one status word.  spec_verify_run and
+ * spec_verify_tree_run allocate nothing later; spec_verify_run_fused adds its
+ * own scratch on its first call.
  * Requires V >= 1 and V*sizeof(dtype) a multiple of 16 (V % 8 == 0 for bf16,
  * V % 4 == 0 for f32).  Returns SV_ERR_SHAPE otherwise, SV_ERR_OOM if the
  * workspace cannot be allocated, SV_ERR_CUDA if the device cannot be used.
@@ -203,8 +206,9 @@ sv_status spec_verify_lm_head_logits(const void *hidden, const void *weight, int
  * vocabulary size), Kt and Kd multiples of 8, 16-byte aligned inputs.  The
  * first call (and a call with larger Kt or Kd) allocates its scratch
  * (cudaMalloc, about 8*(2*max_N+1)*max_B*ceil(V/256) + 8*max_B*V +
- * 2*max_B*(Kt+Kd) bytes) and therefore synchronises; later calls enqueue nine
- * launches on `stream` and allocate nothing.
+ * 2*max_B*(Kt+Kd) bytes) and therefore synchronises; later calls enqueue eight
+ * launches on `stream` (six when greedy: no draft products) and allocate
+ * nothing.
  */
 sv_status spec_verify_run_fused(spec_verify_ctx *ctx, const void *target_hidden, const void *target_weight,
                                 int Kt, const void *draft_hidden, const void *draft_weight, int Kd,
