@@ -567,12 +567,13 @@ def run_ours(args):
     kv = None
     if not args.no_kv:
         kv = measure_kv_commit(sv, torch, dev, stream, nacc, w.N, max_len=args.kv_max_len)
-    fused = None
-    if not args.no_fused:
-        fused = measure_fused(sv, torch, dev, stream, rank, batch=args.fused_batch)
+    # the tree walk is bound by SM arithmetic: measure it before the power-heavy GEMMs
     tree = None
     if not args.no_tree:
         tree = measure_tree(sv, torch, dev, stream, rank, cpu=(rank == 0 and not args.no_cpu))
+    fused = None
+    if not args.no_fused:
+        fused = measure_fused(sv, torch, dev, stream, rank, batch=args.fused_batch)
 
     cpu = None
     if rank == 0 and not args.no_cpu:
