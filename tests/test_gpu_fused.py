@@ -39,6 +39,14 @@ def test_fused_parity(name, seed):
     _check(w)
 
 
+@pytest.mark.parametrize("V,Kt,Kd", [(4104, 200, 72), (1000, 64, 8), (20, 520, 136)])
+def test_fused_ragged_vocabulary_and_depth(V, Kt, Kd):
+    """A last vocabulary tile shorter than 256 columns, and K not a multiple of
+    the 64-wide stage (the tensor maps fill the missing columns with zeros)."""
+    w = synth.make_fused_workload("fused_small", seed=V, device="cuda", V=V, Kt=Kt, Kd=Kd)
+    _check(w)
+
+
 def test_fused_all_greedy_without_draft_model():
     w = synth.make_fused_workload("fused_mixed", seed=1, device="cuda")
     rep, _ = _check(w, greedy=True)
