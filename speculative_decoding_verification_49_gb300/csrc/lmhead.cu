@@ -7,12 +7,16 @@
 // in one forward pass, whose last step is this product of the final hidden
 // states with the LM head; the draft model ends in the same product.
 //
-// A persistent grid (one CTA per SM) walks the 128 x 256 output tiles, the
-// tiles of one 256-column weight slab next to each other so that the CTAs
-// working at the same time share that slab through L2.  Warp 0 streams
-// 128 x 64 tiles of the hidden states and 256 x 64 tiles of the weight with
-// 2-D TMA copies (128-byte swizzle) into a 4-stage shared-memory ring, across
-// tile boundaries; one thread of warp 1 issues tcgen05.mma (M = 128, N = 256,
+// A persistent grid of CTA pairs (clusters of 2, one CTA per SM) walks the
+// output in 256 x 256 blocks: the two CTAs of a pair take the two 128-row
+// tiles of one block, and the blocks of one 256-column weight slab come next
+// to each other so that the pairs working at the same time share that slab
+// through L2.  In each CTA warp 0 streams its 128 x 64 tile of the hidden
+// states and half of the 256 x 64 weight tile with 2-D TMA copies (128-byte
+// swizzle) into a 4-stage shared-memory ring, across tile boundaries; the
+// weight half is multicast into both CTAs, so each SM stages 32 KiB per 64-wide
+// step instead of 48 KiB, and a stage is refilled only when the MMAs of both
+// CTAs have read it.  One thread of warp 1 issues tcgen05.mma (M = 128, N = 256,
 // K = 16, four per 64-wide stage) into one of two 128 x 256 f32 accumulators
 // in tensor memory (all 512 columns) and frees each stage with
 // tcgen05.commit; warps 4-7 read a finished accumulator back (tcgen05.ld, one
@@ -47,13 +51,14 @@ constexpr int kTileA = kBM * kBK * 2;
 constexpr int kTileB = kBN * kBK * 2;
 constexpr int kStageBytes = kTileA + kTileB;
 constexpr int kGemmThreads = 256;
+constexpr int kPair = 2;  // CTAs of a cluster sharing one weight tile
 constexpr uint32_t kTmemCols = 512;  // two 128 x 256 f32 accumulators
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int kErrTimeout = 4;
 
 struct GemmCtl {
     uint64_t full[kStagesG];
-    uint64_t empty[kStagesG];
+    uint64_t empty[kStagesG];  // both CTAs of the pair have read the stage (one MMA commit each)
     uint64_t acc_full[2];   // an accumulator holds a finished tile (MMA commit)
     uint64_t acc_empty[2];  // the epilogue has read it (one arrival per epilogue warp)
     int last_kb[kStagesG];  // last k-block (counted over all tiles) issued into each stage
@@ -137,14 +142,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     GemmCtl &ctl = *reinterpret_cast<GemmCtl *>(smem + (size_t)kStagesG * kStageBytes);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = sv::cluster_ctarank();
+    const int pair = blockIdx.x / kPair, npairs_grid = gridDim.x / kPair;
     const int Mt = (p.M + kBM - 1) / kBM;
-    const int ntile = Mt * ((p.N + kBN - 1) / kBN);
+    const int Mp = (Mt + kPair - 1) / kPair;  // 256-row blocks
+    const int nblock = Mp * ((p.N + kBN - 1) / kBN);
     const int nk = (p.K + kBK - 1) / kBK;
+    constexpr uint16_t kBoth = (1u << kPair) - 1u;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStagesG; ++s) {
             sv::mbar_init(&ctl.full[s], 1);
-            sv::mbar_init(&ctl.empty[s], 1);
+            sv::mbar_init(&ctl.empty[s], kPair);
             ctl.last_kb[s] = -1;
         }
         for (int b = 0; b < 2; ++b) {
@@ -159,7 +168,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         sv::tmem_relinquish();
     }
     sv::tc_fence_before();
-    __syncthreads();
+    sv::cluster_sync();  // both CTAs' barriers exist before any copy or commit reaches them
     sv::tc_fence_after();
     const uint32_t tmem = ctl.tmem_base;
 
@@ -168,8 +177,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             sv::tma_prefetch_desc(&tmA);
             sv::tma_prefetch_desc(&tmB);
             uint32_t g = 0;  // k-blocks issued so far, over all tiles
-            for (int tile = blockIdx.x; tile < ntile && !ctl.abort; tile += gridDim.x) {
-                const int m0 = (tile % Mt) * kBM, n0 = (tile / Mt) * kBN;
+            for (int blk = pair; blk < nblock && !ctl.abort; blk += npairs_grid) {
+                const int m0 = ((blk % Mp) * kPair + (int)rank) * kBM, n0 = (blk / Mp) * kBN;
                 for (int kb = 0; kb < nk; ++kb, ++g) {
                     const int s = (int)(g % kStagesG);
                     const uint32_t ph = (g / kStagesG) & 1u;
@@ -180,7 +189,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     unsigned char *a = smem + (size_t)s * kStageBytes;
                     sv::mbar_arrive_expect_tx(&ctl.full[s], kStageBytes);
                     sv::tma_load_2d(a, &tmA, kb * kBK, m0, &ctl.full[s]);
-                    sv::tma_load_2d(a + kTileA, &tmB, kb * kBK, n0, &ctl.full[s]);
+                    // this CTA's half of the weight tile, into both CTAs
+                    sv::tma_load_2d_multicast(a + kTileA + rank * (kTileB / kPair), &tmB, kb * kBK,
+                                              n0 + (int)rank * (kBN / kPair), &ctl.full[s], kBoth);
                     ctl.last_kb[s] = (int)g;
                 }
             }
@@ -191,7 +202,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             constexpr uint32_t idesc = sv::idesc_bf16_f32(kBM, kBN);
             uint32_t g = 0;
             int t = 0;
-            for (int tile = blockIdx.x; tile < ntile && !ctl.abort; tile += gridDim.x, ++t) {
+            for (int blk = pair; blk < nblock && !ctl.abort; blk += npairs_grid, ++t) {
                 const int buf = t & 1;
                 const uint32_t use = (uint32_t)(t >> 1);
                 // the epilogue has finished with this accumulator's previous tile
@@ -214,7 +225,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk)  // K = 16 per MMA: 32 bytes along the swizzled row
                         sv::tc_mma_bf16(d, da + 2u * kk, db + 2u * kk, idesc, (kb | kk) != 0);
-                    sv::tc_commit(&ctl.empty[s]);  // the stage is free once these MMAs have read it
+                    sv::tc_commit_multicast(&ctl.empty[s], kBoth);  // this CTA's MMAs have read the stage
                 }
                 sv::tc_commit(&ctl.acc_full[buf]);  // the tile is complete
             }
@@ -223,7 +234,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     } else if (warp >= 4) {
         const int q = warp - 4;  // TMEM lanes 32q .. 32q+31
         int t = 0;
-        for (int tile = blockIdx.x; tile < ntile; tile += gridDim.x, ++t) {
+        for (int blk = pair; blk < nblock; blk += npairs_grid, ++t) {
             const int buf = t & 1;
             const uint32_t use = (uint32_t)(t >> 1);
             const bool ok = sv::mbar_wait_bounded(&ctl.acc_full[buf], use & 1u, &ctl.abort, kWaitNs);
@@ -233,7 +244,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 break;
             }
             sv::tc_fence_after();
-            const int m0 = (tile % Mt) * kBM, n0 = (tile / Mt) * kBN;
+            const int m0 = ((blk % Mp) * kPair + (int)rank) * kBM, n0 = (blk / Mp) * kBN;
             const int row = m0 + 32 * q + lane;
             const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * kBN);
             if constexpr (STATS) {
@@ -268,6 +279,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (p.status)
             atomicOr(p.status, kErrTimeout);
     }
+    sv::cluster_sync();  // the peer no longer writes into this CTA's stages or barriers
     if (warp == 2)
         sv::tmem_dealloc(tmem, kTmemCols);
 }
@@ -334,18 +346,31 @@ sv_status launch(const void *hidden, const void *weight, int M, int V, int K, co
     if (g_attr_err != cudaSuccess)
         return SV_ERR_CUDA;
     CUtensorMap ta, tb;
-    if (!make_map(&ta, hidden, M, K, kBM) || !make_map(&tb, weight, V, K, kBN))
+    if (!make_map(&ta, hidden, M, K, kBM) || !make_map(&tb, weight, V, K, kBN / kPair))
         return SV_ERR_CUDA;
-    const long long ntile = (long long)((M + kBM - 1) / kBM) * ((V + kBN - 1) / kBN);
-    if (ntile > INT_MAX)
+    const long long nblock = (long long)((M + kBM * kPair - 1) / (kBM * kPair)) * ((V + kBN - 1) / kBN);
+    if (nblock > INT_MAX / kPair)
         return SV_ERR_INVALID_ARG;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return SV_ERR_CUDA;
-    const unsigned grid = (unsigned)(ntile < sms ? ntile : sms);  // one CTA per SM walks the tiles
-    sv_lmhead_kernel<STATS><<<grid, kGemmThreads, kSmemG, st>>>(ta, tb, p);
-    if (cudaGetLastError() != cudaSuccess)
+    const long long pairs = nblock < sms / kPair ? nblock : sms / kPair;  // one CTA per SM walks the blocks
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kPair;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(pairs * kPair));
+    cfg.blockDim = dim3(kGemmThreads);
+    cfg.dynamicSmemBytes = kSmemG;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, sv_lmhead_kernel<STATS>, ta, tb, p) != cudaSuccess) {
+        cudaGetLastError();
         return SV_ERR_CUDA;
+    }
     return SV_OK;
 }
 
