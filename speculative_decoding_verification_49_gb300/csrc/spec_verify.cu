@@ -1161,81 +1161,72 @@ struct PickShared {
     float x1;
 };
 
+// Outputs of a sequence that is not sampled -- invalid (-1 everywhere, the
+// status bits) or greedy (the argmax at j) -- and the reset of its slots.
+// Thread 0.
+__device__ void emit_unsampled(const SvParams &p, int b, int j)
+{
+    const int N = p.N;
+    int32_t *out = p.out + (size_t)b * (N + 1);
+    const int err = __ldcg(&p.ws_err[b]);
+    if (err) {
+        for (int k = 0; k <= N; ++k)
+            out[k] = -1;
+        p.nacc[b] = -1;
+        atomicOr(p.status, err);
+        if (p.hist)
+            atomicAdd(p.hist_invalid, 1ull);
+    } else {
+        for (int k = 0; k < j; ++k)
+            out[k] = p.tokens[(size_t)b * N + k];
+        out[j] = __ldcg(&p.ws_tok[(size_t)b * (N + 1) + j]);
+        for (int k = j + 1; k <= N; ++k)
+            out[k] = -1;
+        p.nacc[b] = j;
+        if (p.hist)
+            atomicAdd(&p.hist[j], 1ull);
+    }
+    p.ws_first[b] = kNoReject;
+    p.ws_err[b] = 0;
+}
+
+// Outputs of a sampled sequence and the reset of its slots.  Thread 0.
+__device__ void emit_sampled(const SvParams &p, int b, int j, int token)
+{
+    const int N = p.N;
+    int32_t *out = p.out + (size_t)b * (N + 1);
+    for (int k = 0; k < j; ++k)
+        out[k] = p.tokens[(size_t)b * N + k];
+    out[j] = token;
+    for (int k = j + 1; k <= N; ++k)
+        out[k] = -1;
+    p.nacc[b] = j;
+    if (p.hist)
+        atomicAdd(&p.hist[j], 1ull);
+    p.ws_first[b] = kNoReject;
+    p.ws_err[b] = 0;
+}
+
+// The token of a sampled sequence, from the slice masses of its residual in
+// sh.slice: the slice where the cumulative mass first exceeds u_N * R, then
+// (recomputing that slice with the masses' arithmetic) the warp, lane and
+// element.  A residual without mass (q_j == p_j) is replaced by q_j, whose
+// slice masses are recomputed here.  Every thread of the block calls it;
+// threads past the first 256 only take part in the barriers.
 template <int DT>
-__global__ void __launch_bounds__(kPickThreads) sv_pick_kernel(const SvParams p)
+__device__ int draw_token(PickShared &sh, SeqSample &sq, const uint4 *tsrc, const uint4 *dsrc, int NV, int S)
 {
     constexpr int VE = Elt<DT>::kPerVec;
-    __shared__ PickShared sh;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int b = blockIdx.x;
-    const int N = p.N;
-    const int NV = p.V / VE;
-    const int S = (NV + kSliceVecs - 1) / kSliceVecs;
-
-    sv::grid_dependency_wait();  // kernel B's slice masses
-    SeqSample sq{};
-    const bool sampled = sequence_sample(p, b, sq, /*with_cf=*/false);  // sq.cf holds T
-    if (tid == 0)
-        sh.x1 = sampled ? (float)(kLog2e / (double)sq.cf) : 0.0f;  // log2(e)/T, once
-    __syncthreads();
-    sq.cf = sh.x1;
-    const int j = sq.j;
-    int32_t *out = p.out + (size_t)b * (N + 1);
-    if (!sampled) {
-        if (tid == 0) {
-            const int err = __ldcg(&p.ws_err[b]);
-            if (err) {
-                for (int k = 0; k <= N; ++k)
-                    out[k] = -1;
-                p.nacc[b] = -1;
-                atomicOr(p.status, err);
-                if (p.hist)
-                    atomicAdd(p.hist_invalid, 1ull);
-            } else {  // greedy: the argmax at j
-                for (int k = 0; k < j; ++k)
-                    out[k] = p.tokens[(size_t)b * N + k];
-                out[j] = __ldcg(&p.ws_tok[(size_t)b * (N + 1) + j]);
-                for (int k = j + 1; k <= N; ++k)
-                    out[k] = -1;
-                p.nacc[b] = j;
-                if (p.hist)
-                    atomicAdd(&p.hist[j], 1ull);
-            }
-            p.ws_first[b] = kNoReject;
-            p.ws_err[b] = 0;
-        }
-        return;
-    }
-
-    const uint4 *tsrc = static_cast<const uint4 *>(p.target) + sample_trow(p, b, j) * (size_t)NV;
-    const uint4 *dsrc = (j < N) ? static_cast<const uint4 *>(p.draft) + sample_drow(p, b, j) * (size_t)NV : nullptr;
-    const float *shares = p.ws_slice + (size_t)b * S * kConsWarps;
+    const bool cons = tid < kConsThreads;
     float r[VE];
-    for (int sl = tid; sl < S; sl += kPickThreads) {
-        // a slice's mass: its 8 warp shares added in warp order
-        const float4 a = __ldcg(reinterpret_cast<const float4 *>(shares + (size_t)sl * kConsWarps));
-        const float4 c = __ldcg(reinterpret_cast<const float4 *>(shares + (size_t)sl * kConsWarps + 4));
-        float tot = 0.0f;
-        tot = __fadd_rn(tot, a.x);
-        tot = __fadd_rn(tot, a.y);
-        tot = __fadd_rn(tot, a.z);
-        tot = __fadd_rn(tot, a.w);
-        tot = __fadd_rn(tot, c.x);
-        tot = __fadd_rn(tot, c.y);
-        tot = __fadd_rn(tot, c.z);
-        tot = __fadd_rn(tot, c.w);
-        sh.slice[sl] = tot;
-    }
-    __syncthreads();
-
     for (int attempt = 0; attempt < 2; ++attempt) {
         if (attempt == 1) {
-            // q_j == p_j: the residual has no mass; draw from q_j instead
             sq.res_mode = RES_Q;
             for (int sl = 0; sl < S; ++sl) {
-                const float part = slice_thread_mass<DT>(tsrc, nullptr, sl, NV, tid, sq, r);
+                const float part = cons ? slice_thread_mass<DT>(tsrc, nullptr, sl, NV, tid, sq, r) : 0.0f;
                 const float incl = warp_incl_scan(part, lane);
-                if (lane == 31)
+                if (lane == 31 && cons)
                     sh.wtot[warp] = incl;
                 __syncthreads();
                 if (tid == 0) {
@@ -1247,7 +1238,6 @@ __global__ void __launch_bounds__(kPickThreads) sv_pick_kernel(const SvParams p)
                 __syncthreads();
             }
         }
-        // slice s* whose cumulative mass first exceeds u_N * R (warp 0)
         if (warp == 0) {
             float carry = 0.0f;
             for (int c0 = 0; c0 < S; c0 += 32) {
@@ -1270,23 +1260,65 @@ __global__ void __launch_bounds__(kPickThreads) sv_pick_kernel(const SvParams p)
             break;
         __syncthreads();
     }
-
-    // recompute slice s* (warp totals equal kernel B's), then warp, lane, element
     const int ss = sh.sstar;
-    const float part = slice_thread_mass<DT>(tsrc, dsrc, ss, NV, tid, sq, r);
-    const int token = pick_in_slice<VE>(sh.ps, ss, part, r, sh.x1, NV);
-    if (tid == 0) {
-        for (int k = 0; k < j; ++k)
-            out[k] = p.tokens[(size_t)b * N + k];
-        out[j] = token;
-        for (int k = j + 1; k <= N; ++k)
-            out[k] = -1;
-        p.nacc[b] = j;
-        if (p.hist)
-            atomicAdd(&p.hist[j], 1ull);
-        p.ws_first[b] = kNoReject;
-        p.ws_err[b] = 0;
+    float part = 0.0f;
+    if (cons) {
+        part = slice_thread_mass<DT>(tsrc, sq.res_mode == RES_DIFF ? dsrc : nullptr, ss, NV, tid, sq, r);
+    } else {
+#pragma unroll
+        for (int e = 0; e < VE; ++e)
+            r[e] = 0.0f;
     }
+    return pick_in_slice<VE>(sh.ps, ss, part, r, sh.x1, NV);
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kPickThreads) sv_pick_kernel(const SvParams p)
+{
+    constexpr int VE = Elt<DT>::kPerVec;
+    __shared__ PickShared sh;
+    const int tid = threadIdx.x;
+    const int b = blockIdx.x;
+    const int N = p.N;
+    const int NV = p.V / VE;
+    const int S = (NV + kSliceVecs - 1) / kSliceVecs;
+
+    sv::grid_dependency_wait();  // kernel B's slice masses
+    SeqSample sq{};
+    const bool sampled = sequence_sample(p, b, sq, /*with_cf=*/false);  // sq.cf holds T
+    if (tid == 0)
+        sh.x1 = sampled ? (float)(kLog2e / (double)sq.cf) : 0.0f;  // log2(e)/T, once
+    __syncthreads();
+    sq.cf = sh.x1;
+    const int j = sq.j;
+    if (!sampled) {
+        if (tid == 0)
+            emit_unsampled(p, b, j);
+        return;
+    }
+
+    const uint4 *tsrc = static_cast<const uint4 *>(p.target) + sample_trow(p, b, j) * (size_t)NV;
+    const uint4 *dsrc = (j < N) ? static_cast<const uint4 *>(p.draft) + sample_drow(p, b, j) * (size_t)NV : nullptr;
+    const float *shares = p.ws_slice + (size_t)b * S * kConsWarps;
+    for (int sl = tid; sl < S; sl += kPickThreads) {
+        // a slice's mass: its 8 warp shares added in warp order
+        const float4 a = __ldcg(reinterpret_cast<const float4 *>(shares + (size_t)sl * kConsWarps));
+        const float4 c = __ldcg(reinterpret_cast<const float4 *>(shares + (size_t)sl * kConsWarps + 4));
+        float tot = 0.0f;
+        tot = __fadd_rn(tot, a.x);
+        tot = __fadd_rn(tot, a.y);
+        tot = __fadd_rn(tot, a.z);
+        tot = __fadd_rn(tot, a.w);
+        tot = __fadd_rn(tot, c.x);
+        tot = __fadd_rn(tot, c.y);
+        tot = __fadd_rn(tot, c.z);
+        tot = __fadd_rn(tot, c.w);
+        sh.slice[sl] = tot;
+    }
+    __syncthreads();
+    const int token = draw_token<DT>(sh, sq, tsrc, dsrc, NV, S);
+    if (tid == 0)
+        emit_sampled(p, b, j, token);
 }
 
 // =============================================================================
