@@ -7,8 +7,9 @@
 // in one forward pass, whose last step is this product of the final hidden
 // states with the LM head; the draft model ends in the same product.
 //
-// A persistent grid of CTA pairs (clusters of 2, one CTA per SM) walks the
-// output in 256 x 256 blocks: the two CTAs of a pair take the two 128-row
+// A persistent grid of CTA pairs (clusters of 2, one CTA per SM; single CTAs
+// when the product has only one 128-row tile) walks the output in 256 x 256
+// blocks: the two CTAs of a pair take the two 128-row
 // tiles of one block, and the blocks of one 256-column weight slab come next
 // to each other so that the pairs working at the same time share that slab
 // through L2.  In each CTA warp 0 streams its 128 x 64 tile of the hidden
@@ -51,7 +52,7 @@ constexpr int kTileA = kBM * kBK * 2;
 constexpr int kTileB = kBN * kBK * 2;
 constexpr int kStageBytes = kTileA + kTileB;
 constexpr int kGemmThreads = 256;
-constexpr int kPair = 2;  // CTAs of a cluster sharing one weight tile
+constexpr int kMaxPair = 2;  // CTAs of a cluster sharing one weight tile (1 when there is one row tile)
 constexpr uint32_t kTmemCols = 512;  // two 128 x 256 f32 accumulators
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int kErrTimeout = 4;
@@ -143,17 +144,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     GemmCtl &ctl = *reinterpret_cast<GemmCtl *>(smem + (size_t)kStagesG * kStageBytes);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = sv::cluster_ctarank();
-    const int pair = blockIdx.x / kPair, npairs_grid = gridDim.x / kPair;
+    const int P = (int)sv::cluster_nctarank();  // CTAs sharing a weight tile: 1 or 2
+    const int pair = blockIdx.x / P, npairs_grid = gridDim.x / P;
     const int Mt = (p.M + kBM - 1) / kBM;
-    const int Mp = (Mt + kPair - 1) / kPair;  // 256-row blocks
+    const int Mp = (Mt + P - 1) / P;  // blocks of P row tiles
     const int nblock = Mp * ((p.N + kBN - 1) / kBN);
     const int nk = (p.K + kBK - 1) / kBK;
-    constexpr uint16_t kBoth = (1u << kPair) - 1u;
+    const uint16_t all = (uint16_t)((1u << P) - 1u);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStagesG; ++s) {
             sv::mbar_init(&ctl.full[s], 1);
-            sv::mbar_init(&ctl.empty[s], kPair);
+            sv::mbar_init(&ctl.empty[s], (uint32_t)P);
             ctl.last_kb[s] = -1;
         }
         for (int b = 0; b < 2; ++b) {
@@ -178,7 +180,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             sv::tma_prefetch_desc(&tmB);
             uint32_t g = 0;  // k-blocks issued so far, over all tiles
             for (int blk = pair; blk < nblock && !ctl.abort; blk += npairs_grid) {
-                const int m0 = ((blk % Mp) * kPair + (int)rank) * kBM, n0 = (blk / Mp) * kBN;
+                const int m0 = ((blk % Mp) * P + (int)rank) * kBM, n0 = (blk / Mp) * kBN;
                 for (int kb = 0; kb < nk; ++kb, ++g) {
                     const int s = (int)(g % kStagesG);
                     const uint32_t ph = (g / kStagesG) & 1u;
@@ -189,9 +191,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     unsigned char *a = smem + (size_t)s * kStageBytes;
                     sv::mbar_arrive_expect_tx(&ctl.full[s], kStageBytes);
                     sv::tma_load_2d(a, &tmA, kb * kBK, m0, &ctl.full[s]);
-                    // this CTA's half of the weight tile, into both CTAs
-                    sv::tma_load_2d_multicast(a + kTileA + rank * (kTileB / kPair), &tmB, kb * kBK,
-                                              n0 + (int)rank * (kBN / kPair), &ctl.full[s], kBoth);
+                    // this CTA's share of the weight tile, into every CTA of the cluster
+                    sv::tma_load_2d_multicast(a + kTileA + rank * (kTileB / P), &tmB, kb * kBK, n0 + (int)rank * (kBN / P),
+                                              &ctl.full[s], all);
                     ctl.last_kb[s] = (int)g;
                 }
             }
@@ -225,7 +227,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk)  // K = 16 per MMA: 32 bytes along the swizzled row
                         sv::tc_mma_bf16(d, da + 2u * kk, db + 2u * kk, idesc, (kb | kk) != 0);
-                    sv::tc_commit_multicast(&ctl.empty[s], kBoth);  // this CTA's MMAs have read the stage
+                    sv::tc_commit_multicast(&ctl.empty[s], all);  // this CTA's MMAs have read the stage
                 }
                 sv::tc_commit(&ctl.acc_full[buf]);  // the tile is complete
             }
@@ -244,7 +246,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 break;
             }
             sv::tc_fence_after();
-            const int m0 = ((blk % Mp) * kPair + (int)rank) * kBM, n0 = (blk / Mp) * kBN;
+            const int m0 = ((blk % Mp) * P + (int)rank) * kBM, n0 = (blk / Mp) * kBN;
             const int row = m0 + 32 * q + lane;
             const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * kBN);
             if constexpr (STATS) {
@@ -346,22 +348,24 @@ sv_status launch(const void *hidden, const void *weight, int M, int V, int K, co
     if (g_attr_err != cudaSuccess)
         return SV_ERR_CUDA;
     CUtensorMap ta, tb;
-    if (!make_map(&ta, hidden, M, K, kBM) || !make_map(&tb, weight, V, K, kBN / kPair))
+    // pairs of CTAs share each weight tile when there are two row tiles to pair
+    const int P = (M + kBM - 1) / kBM >= kMaxPair ? kMaxPair : 1;
+    if (!make_map(&ta, hidden, M, K, kBM) || !make_map(&tb, weight, V, K, kBN / P))
         return SV_ERR_CUDA;
-    const long long nblock = (long long)((M + kBM * kPair - 1) / (kBM * kPair)) * ((V + kBN - 1) / kBN);
-    if (nblock > INT_MAX / kPair)
+    const long long nblock = (long long)((M + kBM * P - 1) / (kBM * P)) * ((V + kBN - 1) / kBN);
+    if (nblock > INT_MAX / P)
         return SV_ERR_INVALID_ARG;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return SV_ERR_CUDA;
-    const long long pairs = nblock < sms / kPair ? nblock : sms / kPair;  // one CTA per SM walks the blocks
+    const long long pairs = nblock < sms / P ? nblock : sms / P;  // one CTA per SM walks the blocks
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kPair;
+    attr[0].val.clusterDim.x = (unsigned)P;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(pairs * kPair));
+    cfg.gridDim = dim3((unsigned)(pairs * P));
     cfg.blockDim = dim3(kGemmThreads);
     cfg.dynamicSmemBytes = kSmemG;
     cfg.stream = st;
