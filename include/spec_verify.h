@@ -252,6 +252,19 @@ const char *spec_verify_error_string(sv_status s);
 sv_status spec_verify_profile(spec_verify_ctx *ctx, int enable);
 sv_status spec_verify_profile_read(spec_verify_ctx *ctx, double *ms_rows, double *ms_sample, int *runs);
 
+/*
+ * Self-test of the library's failure detection (the pages have no
+ * counterpart).  Every wait inside the kernels is bounded: it gives up after
+ * a time limit (2 s in the verify kernels), reports SV_ERR_TIMEOUT through the
+ * status word, lets its copies in flight land and returns, so a stalled
+ * producer never hangs the GPU.  This call launches one block whose barrier
+ * wait nothing ever satisfies, with a limit of limit_us microseconds
+ * (1 .. 10^7), synchronises `stream` and sets *gave_up = 1 if the block gave
+ * up and reported it, 0 otherwise.  Returns SV_ERR_INVALID_ARG for a bad
+ * limit or a NULL gave_up, SV_ERR_CUDA if the launch or copies fail.
+ */
+sv_status spec_verify_selftest_timeout(int limit_us, int *gave_up, void *stream);
+
 /* Free the workspace and the context.  NULL is ignored. */
 void spec_verify_destroy(spec_verify_ctx *ctx);
 

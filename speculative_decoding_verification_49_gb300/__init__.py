@@ -51,6 +51,7 @@ _SIGNATURES = [
     ("spec_verify_kv_commit", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, ctypes.c_size_t, _P]),
     ("spec_verify_tree_run", _I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
     ("spec_verify_lm_head_logits", _I, [_P, _P, _I, _I, _I, _P, _P]),
+    ("spec_verify_selftest_timeout", _I, [_I, ctypes.POINTER(_I), _P]),
     ("spec_verify_run_fused", _I, [_P, _P, _P, _I, _P, _P, _I, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P]),
 ]
 
@@ -393,3 +394,15 @@ def lm_head_logits(hidden, weight, out=None, stream=None):
     if st != SV_OK:
         raise SpecVerifyError(st, "spec_verify_lm_head_logits")
     return out
+
+
+def selftest_timeout(limit_us: int = 10000, stream=None) -> bool:
+    """True when a kernel wait that nothing satisfies gave up within
+    limit_us and reported it (the library's bounded-wait failure detection)."""
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    flag = _I(0)
+    st = load().spec_verify_selftest_timeout(int(limit_us), ctypes.byref(flag), s.cuda_stream)
+    if st != SV_OK:
+        raise SpecVerifyError(st, "spec_verify_selftest_timeout")
+    return bool(flag.value)

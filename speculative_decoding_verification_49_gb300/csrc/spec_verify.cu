@@ -1890,6 +1890,28 @@ __global__ void __launch_bounds__(256) sv_fused_gather_kernel(const SvParams p, 
     }
 }
 
+// =============================================================================
+// Self-test of the bounded waits
+// =============================================================================
+//
+// Every mbarrier wait in the library gives up after a time limit and reports
+// it.  This kernel waits on a barrier that nothing ever arrives at, with the
+// same bounded wait, and records whether it gave up.
+__device__ int g_sv_timeout_probe;
+
+__global__ void sv_timeout_probe_kernel(uint64_t limit_ns)
+{
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int never;
+    if (threadIdx.x == 0) {
+        never = 0;
+        sv::mbar_init(&bar, 1);
+        sv::fence_mbar_init();
+        const bool completed = sv::mbar_wait_bounded(&bar, 0, &never, limit_ns);
+        g_sv_timeout_probe = completed ? 1 : 2;
+    }
+}
+
 } // namespace
 
 // =============================================================================
@@ -2513,6 +2535,31 @@ sv_status spec_verify_run_fused(spec_verify_ctx *ctx, const void *target_hidden,
     return fused_run_impl(ctx, target_hidden, target_weight, Kt, draft_hidden, draft_weight, Kd, draft_tokens,
                           uniforms, temperature, greedy, B, N, out_tokens, num_accepted, target_row_stats,
                           draft_row_stats, stream);
+}
+
+sv_status spec_verify_selftest_timeout(int limit_us, int *gave_up, void *stream)
+{
+    if (limit_us < 1 || limit_us > 10000000 || !gave_up)
+        return SV_ERR_INVALID_ARG;
+    *gave_up = 0;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int zero = 0;
+    int flag = 0;
+    if (cudaMemcpyToSymbolAsync(g_sv_timeout_probe, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, st) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return SV_ERR_CUDA;
+    }
+    sv_timeout_probe_kernel<<<1, 32, 0, st>>>((uint64_t)limit_us * 1000ull);
+    if (cudaGetLastError() != cudaSuccess ||
+        cudaMemcpyFromSymbolAsync(&flag, g_sv_timeout_probe, sizeof flag, 0, cudaMemcpyDeviceToHost, st) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess) {
+        cudaGetLastError();
+        return SV_ERR_CUDA;
+    }
+    *gave_up = flag == 2 ? 1 : 0;
+    return SV_OK;
 }
 
 sv_status spec_verify_get_status(spec_verify_ctx *ctx)

@@ -83,6 +83,13 @@ def test_fused_and_lm_head_host_validation_without_gpu(lib):
     assert lm(16, 16, 0, 8, 16, 16, None) == sv.SV_OK                # nothing to do
 
 
+def test_selftest_timeout_host_validation_without_gpu(lib):
+    flag = ctypes.c_int(7)
+    assert lib.spec_verify_selftest_timeout(0, ctypes.byref(flag), None) == sv.SV_ERR_INVALID_ARG
+    assert lib.spec_verify_selftest_timeout(10 ** 8, ctypes.byref(flag), None) == sv.SV_ERR_INVALID_ARG
+    assert lib.spec_verify_selftest_timeout(1000, None, None) == sv.SV_ERR_INVALID_ARG
+
+
 def test_kv_commit_host_validation_without_gpu(lib):
     kv = sv.spec_verify_kv_commit
     ok = (256, 512, 1024, 2048, None)  # scratch, cache, cache_len, num_accepted, status
@@ -102,3 +109,23 @@ def test_kv_commit_host_validation_without_gpu(lib):
 
 def test_library_is_built_for_sm_103a():
     assert "arch=compute_103a,code=sm_103a" in svbuild.NVCC_FLAGS
+
+
+def test_header_is_plain_c(tmp_path):
+    """A C99 caller of every entry point compiles against the header (gcc)."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not available")
+    here = os.path.dirname(os.path.abspath(__file__))
+    root = os.path.dirname(here)
+    src = os.path.join(here, "c", "abi_usage.c")
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-c", src,
+                        "-I", os.path.join(root, "include"), "-o", str(tmp_path / "abi_usage.o")],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    # every declared function is called by the example
+    text = open(src).read()
+    for name in declared_functions():
+        assert name + "(" in text, name

@@ -228,3 +228,16 @@ def test_acceptance_counts_match_the_oracle_histogram():
     # a sampled decision inside the margin band may move one sequence
     assert np.abs(np.array(got) - want).sum() <= 2
     assert ctx.acceptance_counts() == [0] * 7
+
+
+def test_bounded_wait_gives_up_and_reports():
+    """Failure detection without a fault: a kernel wait that nothing ever
+    satisfies gives up after its limit and reports it; the GPU and a context
+    stay usable afterwards."""
+    import time
+    t0 = time.perf_counter()
+    assert sv.selftest_timeout(20000)  # 20 ms
+    dt = time.perf_counter() - t0
+    assert 0.015 < dt < 2.0, dt
+    w = synth.make_workload("tiny", seed=11, device="cuda")
+    _check(w)
