@@ -7,27 +7,29 @@
 // in one forward pass, whose last step is this product of the final hidden
 // states with the LM head; the draft model ends in the same product.
 //
-// A persistent grid of CTA pairs (clusters of 2, one CTA per SM; single CTAs
-// when the product has only one 128-row tile) walks the output in 256 x 256
-// blocks: the two CTAs of a pair take the two 128-row
-// tiles of one block, and the blocks of one 256-column weight slab come next
-// to each other so that the pairs working at the same time share that slab
-// through L2.  In each CTA warp 0 streams its 128 x 64 tile of the hidden
-// states and half of the 256 x 64 weight tile with 2-D TMA copies (128-byte
-// swizzle) into a 4-stage shared-memory ring, across tile boundaries; the
-// weight half is multicast into both CTAs, so each SM stages 32 KiB per 64-wide
-// step instead of 48 KiB, and a stage is refilled only when the MMAs of both
-// CTAs have read it.  One thread of warp 1 issues tcgen05.mma (M = 128, N = 256,
-// K = 16, four per 64-wide stage) into one of two 128 x 256 f32 accumulators
-// in tensor memory (all 512 columns) and frees each stage with
-// tcgen05.commit; warps 4-7 read a finished accumulator back (tcgen05.ld, one
-// TMEM lane = one row per thread) while the next tile accumulates into the
-// other one, and run the epilogue: either the logits go out as f32, or (the
-// fused verify path) only each row's statistics over the tile do -- max and
-// sum of exp2((z - max) * log2(e)/T), or max and argmax for greedy rows, and
-// the logit at the row's draft token -- so the logits never reach HBM.
+// A persistent grid walks the output in blocks of 256 columns and, when the
+// product has at least two 128-row tiles, 256 rows: a cluster of two CTAs on
+// neighbouring SMs acts as one MMA unit (tcgen05 cta_group::2).  Each CTA's
+// warp 0 streams its 128 x 64 tile of the hidden states and its 128 x 64 half
+// of the weight tile with 2-D TMA copies (128-byte swizzle) into a 6-stage
+// shared-memory ring, across tile boundaries, and both CTAs' copies are
+// counted on the even CTA's barrier.  One thread of the even CTA's warp 1
+// issues tcgen05.mma with M = 256, N = 256, K = 16 (four per 64-wide stage):
+// each SM stages and reads 32 KiB per 4.2 MFLOP of its share, where one CTA
+// computing 128 x 256 alone would stage and read 48 KiB.  The commits free a
+// stage in both CTAs.  The accumulator is one of two 128 x 256 f32 halves in
+// each CTA's tensor memory (all 512 columns), so warps 4-7 of both CTAs read a
+// finished tile back (tcgen05.ld, one TMEM lane = one row per thread) while
+// the next tile accumulates into the other one.  A product with a single row
+// tile runs on single CTAs (M = 128, the whole weight tile, 4 stages).  The
+// epilogue either writes the logits as f32, or (the fused verify path) only
+// each row's statistics over the tile -- max and sum of exp2((z - max) *
+// log2(e)/T), or max and argmax for greedy rows, and the logit at the row's
+// draft token -- so the logits never reach HBM.  The blocks of one
+// 256-column weight slab come next to each other so that the units working at
+// the same time share that slab through L2.
 // Every mbarrier wait is bounded (2 s); a CTA that gives up sets the status
-// word, lets its copies land and frees its tensor memory.
+// word, lets the copies its barriers count land and frees its tensor memory.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -44,30 +46,47 @@
 
 namespace {
 
-constexpr int kBM = 128;  // tile rows (TMEM lanes)
+constexpr int kBM = 128;  // tile rows per CTA (TMEM lanes)
 constexpr int kBN = 256;  // tile columns (TMEM columns)
 constexpr int kBK = 64;   // K per stage: one 128-byte swizzle row of bf16
-constexpr int kStagesG = 4;
 constexpr int kTileA = kBM * kBK * 2;
 constexpr int kTileB = kBN * kBK * 2;
-constexpr int kStageBytes = kTileA + kTileB;
 constexpr int kGemmThreads = 256;
-constexpr int kMaxPair = 2;  // CTAs of a cluster sharing one weight tile (1 when there is one row tile)
 constexpr uint32_t kTmemCols = 512;  // two 128 x 256 f32 accumulators
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int kErrTimeout = 4;
+constexpr int kMaxStagesG = 6;
+
+// A single CTA stages its 128 x 64 hidden tile and the whole 256 x 64 weight
+// tile per step (48 KiB, 4 stages); a CTA of a pair stages its 128 hidden rows
+// and its 128-column half of the weight tile (32 KiB, 6 stages).
+template <bool PAIR> struct GemmCfg {
+    static constexpr int kStages = PAIR ? 6 : 4;
+    static constexpr int kTileBh = PAIR ? kTileB / 2 : kTileB;
+    static constexpr int kStage = kTileA + kTileBh;
+};
 
 struct GemmCtl {
-    uint64_t full[kStagesG];
-    uint64_t empty[kStagesG];  // both CTAs of the pair have read the stage (one MMA commit each)
+    uint64_t full[kMaxStagesG];     // the stage's copies have landed (a pair: both CTAs', on the even CTA's)
+    uint64_t empty[kMaxStagesG];    // the MMAs have read the stage (commit, multicast to both CTAs of a pair)
     uint64_t acc_full[2];   // an accumulator holds a finished tile (MMA commit)
-    uint64_t acc_empty[2];  // the epilogue has read it (one arrival per epilogue warp)
-    int last_kb[kStagesG];  // last k-block (counted over all tiles) issued into each stage
+    uint64_t acc_empty[2];  // the epilogue has read it (one arrival per epilogue warp, of both CTAs of a pair)
+    int last_kb[kMaxStagesG];  // last k-block (counted over all tiles) issued into each stage
     uint32_t tmem_base;
     int abort;
 };
 
-constexpr size_t kSmemG = 1024 + (size_t)kStagesG * kStageBytes + sizeof(GemmCtl);
+// Logits epilogue: each epilogue warp turns its 32 rows x 32 columns around in
+// shared memory (row stride 33: no bank conflicts) so that every store of the
+// warp writes 128 contiguous bytes of one row.
+constexpr int kEpiStride = 33;
+constexpr size_t kEpiBytes = 4 * 32 * kEpiStride * sizeof(float);
+
+template <bool PAIR> constexpr size_t smem_bytes()
+{
+    return 1024 + (size_t)GemmCfg<PAIR>::kStages * GemmCfg<PAIR>::kStage + sizeof(GemmCtl) + kEpiBytes;
+}
+static_assert(smem_bytes<true>() <= 232448 && smem_bytes<false>() <= 232448, "227 KiB of shared memory per CTA");
 
 constexpr double kLog2e = 1.4426950408889634074;
 
@@ -78,11 +97,16 @@ struct LmParams {
     svlm::StatsArgs st;  // statistics epilogue
 };
 
-// The statistics of one row over one tile (32 columns per tcgen05.ld).  A
-// thread whose row is past M still issues the warp-collective loads but
-// writes nothing.
+// The statistics of one row over one tile, in one pass over two chunks of 128
+// columns (four tcgen05.ld in flight per chunk, one wait): the chunk maximum
+// as a tree, then for sampled rows the running sum of exp2((z - max) * cf),
+// rescaled when the maximum grows, over eight independent partial sums; for
+// greedy rows the lowest column holding the maximum.  Columns past the
+// vocabulary count as -inf; NaN never becomes the maximum.  A thread whose row
+// is past M still issues the warp-collective loads but writes nothing.
 __device__ __forceinline__ void row_stats(uint32_t taddr, int n0, const LmParams &p, int row_in)
 {
+    constexpr int kChunk = 128;
     const svlm::StatsArgs &a = p.st;
     const bool valid = row_in < p.M;
     const int row = valid ? row_in : 0;
@@ -93,38 +117,66 @@ __device__ __forceinline__ void row_stats(uint32_t taddr, int n0, const LmParams
     const float cf = sampled ? (float)(kLog2e / (double)T) : 0.0f;
     const int d = (i < a.N) ? a.tokens[(size_t)b * a.N + i] : -1;
     const int dl = d - n0;  // the draft token's column in this tile, if in range
-    float m = -INFINITY;
+    float m = -INFINITY, s = 0.0f;
     int arg = INT_MAX;
-    for (int c0 = 0; c0 < kBN; c0 += 32) {
-        float v[32];
-        sv::tmem_ld32(taddr + (uint32_t)c0, v);
+#pragma unroll 1
+    for (int c0 = 0; c0 < kBN; c0 += kChunk) {
+        uint32_t r[kChunk];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-            const int c = c0 + k;
-            if (n0 + c < p.N) {
-                if (v[k] > m) {
-                    m = v[k];
-                    arg = n0 + c;
-                }
-                if (c == dl && valid)
+        for (int j = 0; j < kChunk / 32; ++j)
+            sv::tmem_ld32_nowait(taddr + (uint32_t)(c0 + 32 * j), r + 32 * j);
+        sv::tmem_wait_ld();
+        const int lim = p.N - n0 - c0;  // columns of this chunk inside the vocabulary
+        float v[kChunk];
+#pragma unroll
+        for (int k = 0; k < kChunk; ++k)
+            v[k] = (k < lim) ? __uint_as_float(r[k]) : -INFINITY;
+        if (valid && (unsigned)(dl - c0) < (unsigned)kChunk && dl - c0 < lim) {
+#pragma unroll
+            for (int k = 0; k < kChunk; ++k)
+                if (k == dl - c0)
                     a.zgat[row] = v[k];
-            }
         }
-    }
-    float s = 0.0f;
-    // tcgen05.ld is warp-collective and the rows of one warp may belong to
-    // greedy and sampled sequences alike: the whole warp loads, the sampled
-    // rows accumulate
-    if (__any_sync(0xffffffffu, sampled)) {
-        for (int c0 = 0; c0 < kBN; c0 += 32) {
-            float v[32];
-            sv::tmem_ld32(taddr + (uint32_t)c0, v);
-            if (sampled) {
+        float mx[16];
 #pragma unroll
-                for (int k = 0; k < 32; ++k)
-                    if (n0 + c0 + k < p.N)
-                        s = __fadd_rn(s, sv::ex2(__fmul_rn(__fsub_rn(v[k], m), cf)));
+        for (int k = 0; k < 16; ++k)
+            mx[k] = v[k];
+#pragma unroll
+        for (int k = 16; k < kChunk; ++k)
+            mx[k & 15] = fmaxf(mx[k & 15], v[k]);
+#pragma unroll
+        for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+            for (int k = 0; k < w; ++k)
+                mx[k] = fmaxf(mx[k], mx[k + w]);
+        const float mc = mx[0];
+        if (sampled) {
+            const float mn = fmaxf(m, mc);
+            if (mn != -INFINITY) {
+                s = __fmul_rn(s, sv::ex2(__fmul_rn(__fsub_rn(m, mn), cf)));
+                float acc[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    acc[k] = 0.0f;
+#pragma unroll
+                for (int k = 0; k < kChunk; ++k)
+                    acc[k & 7] = __fadd_rn(acc[k & 7], sv::ex2(__fmul_rn(__fsub_rn(v[k], mn), cf)));
+#pragma unroll
+                for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+                    for (int k = 0; k < w; ++k)
+                        acc[k] = __fadd_rn(acc[k], acc[k + w]);
+                s = __fadd_rn(s, acc[0]);
             }
+            m = mn;
+        } else if (mc > m) {
+            m = mc;
+            int idx = 0;
+#pragma unroll
+            for (int k = kChunk - 1; k >= 0; --k)
+                if (v[k] == mc)
+                    idx = k;
+            arg = n0 + c0 + idx;
         }
     }
     if (valid) {
@@ -134,43 +186,55 @@ __device__ __forceinline__ void row_stats(uint32_t taddr, int n0, const LmParams
     }
 }
 
-template <bool STATS>
+template <bool STATS, bool PAIR>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     sv_lmhead_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, LmParams p)
 {
+    using Cfg = GemmCfg<PAIR>;
+    constexpr int kStages = Cfg::kStages;
+    constexpr int P = PAIR ? 2 : 1;  // CTAs per MMA unit
     extern __shared__ unsigned char smem_raw[];
     // 128-byte-swizzled tiles want 1024-byte alignment
     unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    GemmCtl &ctl = *reinterpret_cast<GemmCtl *>(smem + (size_t)kStagesG * kStageBytes);
+    GemmCtl &ctl = *reinterpret_cast<GemmCtl *>(smem + (size_t)kStages * Cfg::kStage);
+    float *epi = reinterpret_cast<float *>(smem + (size_t)kStages * Cfg::kStage + sizeof(GemmCtl));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t rank = sv::cluster_ctarank();
-    const int P = (int)sv::cluster_nctarank();  // CTAs sharing a weight tile: 1 or 2
-    const int pair = blockIdx.x / P, npairs_grid = gridDim.x / P;
+    const uint32_t rank = PAIR ? sv::cluster_ctarank() : 0u;
+    const bool leader = rank == 0;  // the CTA whose thread issues the MMAs
+    const int unit = blockIdx.x / P, nunits = gridDim.x / P;
     const int Mt = (p.M + kBM - 1) / kBM;
     const int Mp = (Mt + P - 1) / P;  // blocks of P row tiles
     const int nblock = Mp * ((p.N + kBN - 1) / kBN);
     const int nk = (p.K + kBK - 1) / kBK;
-    const uint16_t all = (uint16_t)((1u << P) - 1u);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStagesG; ++s) {
-            sv::mbar_init(&ctl.full[s], 1);
-            sv::mbar_init(&ctl.empty[s], (uint32_t)P);
+        for (int s = 0; s < kStages; ++s) {
+            sv::mbar_init(&ctl.full[s], 1);  // the even CTA's expect-tx arrival
+            sv::mbar_init(&ctl.empty[s], 1);
             ctl.last_kb[s] = -1;
         }
         for (int b = 0; b < 2; ++b) {
             sv::mbar_init(&ctl.acc_full[b], 1);
-            sv::mbar_init(&ctl.acc_empty[b], 4);
+            sv::mbar_init(&ctl.acc_empty[b], 4u * P);
         }
         ctl.abort = 0;
         sv::fence_mbar_init();
     }
-    if (warp == 2) {
+    if constexpr (PAIR) {
+        sv::cluster_sync();  // the peer is running before the collective allocation
+        if (warp == 2) {
+            sv::tmem_alloc_pair(&ctl.tmem_base, kTmemCols);
+            sv::tmem_relinquish_pair();
+        }
+    } else if (warp == 2) {
         sv::tmem_alloc(&ctl.tmem_base, kTmemCols);
         sv::tmem_relinquish();
     }
     sv::tc_fence_before();
-    sv::cluster_sync();  // both CTAs' barriers exist before any copy or commit reaches them
+    if constexpr (PAIR)
+        sv::cluster_sync();  // both CTAs' barriers exist before any copy, arrival or commit reaches them
+    else
+        __syncthreads();
     sv::tc_fence_after();
     const uint32_t tmem = ctl.tmem_base;
 
@@ -179,35 +243,44 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             sv::tma_prefetch_desc(&tmA);
             sv::tma_prefetch_desc(&tmB);
             uint32_t g = 0;  // k-blocks issued so far, over all tiles
-            for (int blk = pair; blk < nblock && !ctl.abort; blk += npairs_grid) {
+            for (int blk = unit; blk < nblock && !ctl.abort; blk += nunits) {
                 const int m0 = ((blk % Mp) * P + (int)rank) * kBM, n0 = (blk / Mp) * kBN;
                 for (int kb = 0; kb < nk; ++kb, ++g) {
-                    const int s = (int)(g % kStagesG);
-                    const uint32_t ph = (g / kStagesG) & 1u;
+                    const int s = (int)(g % kStages);
+                    const uint32_t ph = (g / kStages) & 1u;
                     if (!sv::mbar_wait_bounded(&ctl.empty[s], ph ^ 1u, &ctl.abort, kWaitNs)) {
                         ctl.abort = 1;
                         break;
                     }
-                    unsigned char *a = smem + (size_t)s * kStageBytes;
-                    sv::mbar_arrive_expect_tx(&ctl.full[s], kStageBytes);
-                    sv::tma_load_2d(a, &tmA, kb * kBK, m0, &ctl.full[s]);
-                    // this CTA's share of the weight tile, into every CTA of the cluster
-                    sv::tma_load_2d_multicast(a + kTileA + rank * (kTileB / P), &tmB, kb * kBK, n0 + (int)rank * (kBN / P),
-                                              &ctl.full[s], all);
+                    unsigned char *a = smem + (size_t)s * Cfg::kStage;
+                    if constexpr (PAIR) {
+                        // this CTA's hidden rows and weight half, counted on the even CTA's barrier, which
+                        // alone posts the bytes of both CTAs (the odd CTA's may land first: the phase
+                        // cannot complete before that arrival)
+                        const uint32_t full_cl = sv::dsmem_addr(&ctl.full[s], 0);
+                        if (leader)
+                            sv::mbar_arrive_expect_tx(&ctl.full[s], 2u * Cfg::kStage);
+                        sv::tma_load_2d_pair(a, &tmA, kb * kBK, m0, full_cl);
+                        sv::tma_load_2d_pair(a + kTileA, &tmB, kb * kBK, n0 + (int)rank * (kBN / 2), full_cl);
+                    } else {
+                        sv::mbar_arrive_expect_tx(&ctl.full[s], Cfg::kStage);
+                        sv::tma_load_2d(a, &tmA, kb * kBK, m0, &ctl.full[s]);
+                        sv::tma_load_2d(a + kTileA, &tmB, kb * kBK, n0, &ctl.full[s]);
+                    }
                     ctl.last_kb[s] = (int)g;
                 }
             }
         }
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0) {
-            constexpr uint32_t idesc = sv::idesc_bf16_f32(kBM, kBN);
+        if (lane == 0 && leader) {
+            constexpr uint32_t idesc = sv::idesc_bf16_f32(kBM * P, kBN);
             uint32_t g = 0;
             int t = 0;
-            for (int blk = pair; blk < nblock && !ctl.abort; blk += npairs_grid, ++t) {
+            for (int blk = unit; blk < nblock && !ctl.abort; blk += nunits, ++t) {
                 const int buf = t & 1;
                 const uint32_t use = (uint32_t)(t >> 1);
-                // the epilogue has finished with this accumulator's previous tile
+                // the epilogue (of both CTAs) has finished with this accumulator's previous tile
                 if (!sv::mbar_wait_bounded(&ctl.acc_empty[buf], (use & 1u) ^ 1u, &ctl.abort, kWaitNs)) {
                     ctl.abort = 1;
                     break;
@@ -215,28 +288,39 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 sv::tc_fence_after();
                 const uint32_t d = tmem + (uint32_t)(buf * kBN);
                 for (int kb = 0; kb < nk; ++kb, ++g) {
-                    const int s = (int)(g % kStagesG);
-                    const uint32_t ph = (g / kStagesG) & 1u;
+                    const int s = (int)(g % kStages);
+                    const uint32_t ph = (g / kStages) & 1u;
                     if (!sv::mbar_wait_bounded(&ctl.full[s], ph, &ctl.abort, kWaitNs)) {
                         ctl.abort = 1;
                         break;
                     }
                     sv::tc_fence_after();
-                    const unsigned char *a = smem + (size_t)s * kStageBytes;
+                    const unsigned char *a = smem + (size_t)s * Cfg::kStage;
                     const uint64_t da = sv::smem_desc_k128(a), db = sv::smem_desc_k128(a + kTileA);
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk)  // K = 16 per MMA: 32 bytes along the swizzled row
-                        sv::tc_mma_bf16(d, da + 2u * kk, db + 2u * kk, idesc, (kb | kk) != 0);
-                    sv::tc_commit_multicast(&ctl.empty[s], all);  // this CTA's MMAs have read the stage
+                    for (int kk = 0; kk < kBK / 16; ++kk) {  // K = 16 per MMA: 32 bytes along the swizzled row
+                        if constexpr (PAIR)
+                            sv::tc_mma_bf16_pair(d, da + 2u * kk, db + 2u * kk, idesc, (kb | kk) != 0);
+                        else
+                            sv::tc_mma_bf16(d, da + 2u * kk, db + 2u * kk, idesc, (kb | kk) != 0);
+                    }
+                    // the stage may be refilled once these MMAs have read it
+                    if constexpr (PAIR)
+                        sv::tc_commit_pair_multicast(&ctl.empty[s], 3);
+                    else
+                        sv::tc_commit(&ctl.empty[s]);
                 }
-                sv::tc_commit(&ctl.acc_full[buf]);  // the tile is complete
+                if constexpr (PAIR)
+                    sv::tc_commit_pair_multicast(&ctl.acc_full[buf], 3);  // the tile is complete
+                else
+                    sv::tc_commit(&ctl.acc_full[buf]);
             }
         }
         __syncwarp();
     } else if (warp >= 4) {
         const int q = warp - 4;  // TMEM lanes 32q .. 32q+31
         int t = 0;
-        for (int blk = pair; blk < nblock; blk += npairs_grid, ++t) {
+        for (int blk = unit; blk < nblock; blk += nunits, ++t) {
             const int buf = t & 1;
             const uint32_t use = (uint32_t)(t >> 1);
             const bool ok = sv::mbar_wait_bounded(&ctl.acc_full[buf], use & 1u, &ctl.abort, kWaitNs);
@@ -252,38 +336,54 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             if constexpr (STATS) {
                 row_stats(taddr, n0, p, row);
             } else {
+                float *stg = epi + q * 32 * kEpiStride;
+                const int r0 = m0 + 32 * q;  // the warp's first row
                 for (int c0 = 0; c0 < kBN; c0 += 32) {
                     float v[32];
                     sv::tmem_ld32(taddr + (uint32_t)c0, v);
-                    if (row < p.M) {
-                        float *dst = p.logits + (size_t)row * p.N + n0 + c0;
-                        for (int i = 0; i < 32; ++i)
-                            if (n0 + c0 + i < p.N)
-                                dst[i] = v[i];
-                    }
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        stg[lane * kEpiStride + i] = v[i];
+                    __syncwarp();
+                    const int col = n0 + c0 + lane;
+                    const int rows = min(32, p.M - r0);
+                    if (col < p.N)
+                        for (int r = 0; r < rows; ++r)
+                            p.logits[(size_t)(r0 + r) * p.N + col] = stg[r * kEpiStride + lane];
+                    __syncwarp();
                 }
             }
             sv::tc_fence_before();
             __syncwarp();
-            if (lane == 0)
-                sv::mbar_arrive(&ctl.acc_empty[buf]);
+            if (lane == 0) {
+                if constexpr (PAIR)
+                    sv::mbar_arrive_cl(sv::dsmem_addr(&ctl.acc_empty[buf], 0));
+                else
+                    sv::mbar_arrive(&ctl.acc_empty[buf]);
+            }
         }
     }
     sv::tc_fence_before();
     __syncthreads();
     if (threadIdx.x == 0 && ctl.abort) {
-        // let every copy issued into this CTA's shared memory land before it exits
-        for (int s = 0; s < kStagesG; ++s)
-            if (ctl.last_kb[s] >= 0) {
-                int never = 0;
-                sv::mbar_wait_bounded(&ctl.full[s], (uint32_t)(ctl.last_kb[s] / kStagesG) & 1u, &never, kWaitNs / 4);
-            }
+        // let the copies this CTA's barriers count land before it exits (a pair's
+        // odd CTA counts on the even CTA's barriers, which drains them)
+        if (leader)
+            for (int s = 0; s < kStages; ++s)
+                if (ctl.last_kb[s] >= 0) {
+                    int never = 0;
+                    sv::mbar_wait_bounded(&ctl.full[s], (uint32_t)(ctl.last_kb[s] / kStages) & 1u, &never, kWaitNs / 4);
+                }
         if (p.status)
             atomicOr(p.status, kErrTimeout);
     }
-    sv::cluster_sync();  // the peer no longer writes into this CTA's stages or barriers
-    if (warp == 2)
+    if constexpr (PAIR) {
+        sv::cluster_sync();  // the peer no longer writes into this CTA's stages, barriers or tensor memory
+        if (warp == 2)
+            sv::tmem_dealloc_pair(tmem, kTmemCols);
+    } else if (warp == 2) {
         sv::tmem_dealloc(tmem, kTmemCols);
+    }
 }
 
 // ---- host side -----------------------------------------------------------------
@@ -329,6 +429,37 @@ bool make_map(CUtensorMap *m, const void *base, int rows, int K, int box_rows)
 std::once_flag g_attr_once;
 cudaError_t g_attr_err = cudaSuccess;
 
+template <bool STATS, bool PAIR> cudaError_t set_smem_attr()
+{
+    return cudaFuncSetAttribute(sv_lmhead_kernel<STATS, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)smem_bytes<PAIR>());
+}
+
+// Clusters (CTAs, or CTA pairs) of the kernel that fit on the device at once,
+// queried once per device and kind; SMs / P if the query fails.
+template <bool STATS>
+int resident_units(bool pair, int dev, int sms, const cudaLaunchConfig_t &cfg)
+{
+    constexpr int kMaxDev = 64;
+    static std::atomic<int> cache[kMaxDev][2];
+    const int P = pair ? 2 : 1;
+    if (dev < 0 || dev >= kMaxDev)
+        return sms / P;
+    int n = cache[dev][pair].load();
+    if (n <= 0) {
+        n = 0;
+        const cudaError_t e = pair ? cudaOccupancyMaxActiveClusters(&n, sv_lmhead_kernel<STATS, true>, &cfg)
+                                   : cudaOccupancyMaxActiveClusters(&n, sv_lmhead_kernel<STATS, false>, &cfg);
+        if (e != cudaSuccess || n <= 0) {
+            cudaGetLastError();
+            return sms / P;
+        }
+        n = n < sms / P ? n : sms / P;
+        cache[dev][pair].store(n);
+    }
+    return n;
+}
+
 template <bool STATS>
 sv_status launch(const void *hidden, const void *weight, int M, int V, int K, const LmParams &p, cudaStream_t st)
 {
@@ -339,17 +470,21 @@ sv_status launch(const void *hidden, const void *weight, int M, int V, int K, co
     if (!hidden || !weight || (reinterpret_cast<uintptr_t>(hidden) & 15u) || (reinterpret_cast<uintptr_t>(weight) & 15u))
         return SV_ERR_INVALID_ARG;
     std::call_once(g_attr_once, [] {
-        g_attr_err = cudaFuncSetAttribute(sv_lmhead_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          (int)kSmemG);
-        if (g_attr_err == cudaSuccess)
-            g_attr_err = cudaFuncSetAttribute(sv_lmhead_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              (int)kSmemG);
+        cudaError_t e = set_smem_attr<false, false>();
+        if (e == cudaSuccess)
+            e = set_smem_attr<false, true>();
+        if (e == cudaSuccess)
+            e = set_smem_attr<true, false>();
+        if (e == cudaSuccess)
+            e = set_smem_attr<true, true>();
+        g_attr_err = e;
     });
     if (g_attr_err != cudaSuccess)
         return SV_ERR_CUDA;
     CUtensorMap ta, tb;
-    // pairs of CTAs share each weight tile when there are two row tiles to pair
-    const int P = (M + kBM - 1) / kBM >= kMaxPair ? kMaxPair : 1;
+    // CTA pairs (one 256-row MMA) when there are two row tiles to pair
+    const bool pair = (M + kBM - 1) / kBM >= 2;
+    const int P = pair ? 2 : 1;
     if (!make_map(&ta, hidden, M, K, kBM) || !make_map(&tb, weight, V, K, kBN / P))
         return SV_ERR_CUDA;
     const long long nblock = (long long)((M + kBM * P - 1) / (kBM * P)) * ((V + kBN - 1) / kBN);
@@ -358,20 +493,25 @@ sv_status launch(const void *hidden, const void *weight, int M, int V, int K, co
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return SV_ERR_CUDA;
-    const long long pairs = nblock < sms / P ? nblock : sms / P;  // one CTA per SM walks the blocks
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)P;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(pairs * P));
+    cfg.gridDim = dim3((unsigned)((sms / P) * P));
     cfg.blockDim = dim3(kGemmThreads);
-    cfg.dynamicSmemBytes = kSmemG;
+    cfg.dynamicSmemBytes = pair ? smem_bytes<true>() : smem_bytes<false>();
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, sv_lmhead_kernel<STATS>, ta, tb, p) != cudaSuccess) {
+    // one CTA per SM walks the blocks: as many units as can be resident at once
+    const int fit = resident_units<STATS>(pair, dev, sms, cfg);
+    const long long units = nblock < fit ? nblock : fit;
+    cfg.gridDim = dim3((unsigned)(units * P));
+    const cudaError_t e = pair ? cudaLaunchKernelEx(&cfg, sv_lmhead_kernel<STATS, true>, ta, tb, p)
+                               : cudaLaunchKernelEx(&cfg, sv_lmhead_kernel<STATS, false>, ta, tb, p);
+    if (e != cudaSuccess) {
         cudaGetLastError();
         return SV_ERR_CUDA;
     }

@@ -20,19 +20,6 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, int x, 
         : "memory");
 }
 
-// The same copy multicast to the CTAs of the cluster in cta_mask: each receives
-// the box at the same shared-memory offset and its own mbarrier at `bar`'s
-// offset is signalled.
-__device__ __forceinline__ void tma_load_2d_multicast(void *dst, const void *tmap, int x, int y, uint64_t *bar,
-                                                      uint16_t cta_mask)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster "
-        "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(cta_mask)
-        : "memory");
-}
-
 __device__ __forceinline__ void tma_prefetch_desc(const void *tmap)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
@@ -80,16 +67,6 @@ __device__ __forceinline__ void tc_commit(uint64_t *bar)
                  : "memory");
 }
 
-// The same, arriving on the mbarrier at `bar`'s offset in every CTA of cta_mask.
-__device__ __forceinline__ void tc_commit_multicast(uint64_t *bar, uint16_t cta_mask)
-{
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_u32(bar)),
-        "h"(cta_mask)
-        : "memory");
-}
-
 // 32 consecutive f32 columns of this thread's TMEM lane (warp w reads lanes
 // 32*(w%4) .. +31); taddr = (lane base << 16) | column.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v)
@@ -108,6 +85,87 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v)
 #pragma unroll
     for (int i = 0; i < 32; ++i)
         v[i] = __uint_as_float(r[i]);
+}
+
+// The same load without the wait: several may be in flight; tmem_wait_ld()
+// waits for all of them before the registers are read.
+__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t *r)
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// ---- CTA pairs (cta_group::2) ---------------------------------------------------
+// Two CTAs of a cluster (ranks 2c, 2c+1) act as one MMA unit: one thread of the
+// even CTA issues M = 256 products whose A rows 0-127 and B columns 0-127 come
+// from its own shared memory and A rows 128-255 and B columns 128-255 from the
+// odd CTA's, at the same offsets; accumulator rows 0-127 land in the even CTA's
+// tensor memory, 128-255 in the odd CTA's, at the same column address.  The
+// allocation is collective: one warp of each CTA executes it.
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t *slot, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
+                 "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair()
+{
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// 2-D TMA into this CTA's shared memory, completion signalled on the mbarrier
+// at cluster address bar_cl, which may belong to the peer CTA of the pair.
+__device__ __forceinline__ void tma_load_2d_pair(void *dst, const void *tmap, int x, int y, uint32_t bar_cl)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+        "%3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar_cl)
+        : "memory");
+}
+
+// Arrive on the mbarrier at cluster address bar_cl (which may belong to a peer CTA).
+__device__ __forceinline__ void mbar_arrive_cl(uint32_t bar_cl)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cl) : "memory");
+}
+
+__device__ __forceinline__ void tc_mma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive on the mbarrier at `bar`'s offset in every CTA of cta_mask once the
+// pair MMAs this thread issued before have completed.
+__device__ __forceinline__ void tc_commit_pair_multicast(uint64_t *bar, uint16_t cta_mask)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(cta_mask)
+        : "memory");
 }
 
 // ---- descriptors -------------------------------------------------------------------

@@ -29,7 +29,7 @@ def _bound(h, w):
 
 
 @pytest.mark.parametrize("M,V,K", [(128, 256, 64), (300, 1000, 72), (1, 17, 8), (257, 2304, 896),
-                                   (130, 4099, 3584)])
+                                   (130, 4099, 3584), (520, 40000, 136)])
 def test_lm_head_logits_match_the_definition(M, V, K):
     h, w = _case(M, V, K, seed=M + V + K)
     got = sv.lm_head_logits(h.cuda(), w.cuda()).cpu().double().numpy()
