@@ -1,5 +1,6 @@
 """The verify step fused into the LM-head products, against the float64
 oracle on the float64 products (needs a GB300)."""
+import dataclasses
 import os
 
 import numpy as np
@@ -51,6 +52,39 @@ def test_fused_all_greedy_without_draft_model():
     w = synth.make_fused_workload("fused_mixed", seed=1, device="cuda")
     rep, _ = _check(w, greedy=True)
     assert rep["exact"] >= rep["sequences"] - rep["band_sequences"]
+
+
+@pytest.mark.parametrize("c1,c2", [(5, 40), (100, 200), (30, 700), (255, 256)])
+def test_fused_greedy_ties_take_the_lowest_column(c1, c2):
+    """Two vocabulary columns with identical head rows give equal logits; the
+    greedy token is the lower column (the first index of the argmax), whether
+    the twins share a 128-column chunk of the epilogue, sit in two chunks of one
+    tile, or in two tiles.  Position k's draft token is the higher twin, so a
+    kernel that took it would accept position k instead of emitting the lower
+    twin there."""
+    B, N, V, K = 8, 3, 1024, 64
+    w = synth.make_fused_workload("fused_small", seed=c1 + c2, device="cuda", B=B, N=N, V=V, Kt=K, Kd=K)
+    wt = w.target_weight.clone()
+    wt[c2] = wt[c1]
+    th = (wt[c1].float() * 40.0).to(torch.bfloat16).repeat(B * (N + 1), 1).contiguous()
+    toks = torch.full((B, N), c1, dtype=torch.int32, device="cuda")
+    want_out = np.full((B, N + 1), -1, np.int32)
+    want_nacc = np.zeros(B, np.int32)
+    for b in range(B):
+        k = b % (N + 1)  # the higher twin's position; k == N: every draft is the lower twin
+        if k < N:
+            toks[b, k] = c2
+        want_out[b, :k + 1] = c1
+        want_nacc[b] = k
+    w2 = dataclasses.replace(w, target_weight=wt, target_hidden=th, draft_tokens=toks)
+    orc = parity.run_oracle_fused(w2, threads=THREADS, greedy=True)
+    assert (orc["out_tokens"] == want_out).all() and (orc["num_accepted"] == want_nacc).all()
+    ctx = sv.SpecVerify(B, N, V, "f32")
+    out, nacc = ctx.run_fused(th, wt, None, None, toks, None, None, greedy=True)
+    torch.cuda.synchronize()
+    assert (out.cpu().numpy() == want_out).all(), out.cpu().numpy().tolist()
+    assert (nacc.cpu().numpy() == want_nacc).all()
+    assert ctx.status() == sv.SV_OK
 
 
 def test_fused_full_size_sampled():
