@@ -1355,20 +1355,30 @@ struct CtlW {
     Ring<kStagesW> ring;
     float shares[kMaxWalkSlices * kConsWarps];  // warp shares of every slice of the current pass
     float slice[kMaxWalkSlices];                // slice masses
-    float invR[kMaxTreeNodes];                  // 1/R_1 .. 1/R_k of the current node
     PickState ps;
     int kids[kMaxTreeNodes];
     int nkids, accept, sstar;
     float Rt, x1, cf;
+    // the tree, fetched once: every decision of the walk reads shared memory
+    int par[kMaxTreeNodes], tok[kMaxTreeNodes];
+    int amax[kMaxTreeNodes];                    // greedy: the argmax of each node's verifier row
+    float u[kMaxTreeNodes];
+    float zq[kMaxTreeNodes], zp[kMaxTreeNodes];  // logits at node c's token in its parent's rows
+    float st[kMaxTreeNodes * 4];                // (mq, Sq, mp, Sp) of each node
 };
 
 constexpr size_t kSmemW = ring_bytes(kStagesW) + sizeof(CtlW);
+static_assert(kSmemW <= 232448, "227 KiB of shared memory per CTA");
 
-// r_k (diff = false) or (r_k - p)+ (diff = true) for the VE elements of one
-// 16-byte vector; pairs of adjacent elements travel as one f32x2.
+// (q - c p)+ (use_p) or q for the VE elements of one 16-byte vector, with
+// q = 2^((zq - mq) cf) / Sq and p = 2^((zp - mp) cf) / Sp, each rounded, then
+// q - c p = fma(p, -c, q) (one rounding: at c = 1 exactly kernel B's q - p, so
+// a chain-shaped tree samples as the chain does).  Pairs of adjacent elements
+// travel as one f32x2; every operation rounds to nearest, so the walk's passes
+// and the recomputation of the chosen slice agree bit for bit.
 template <int DT>
-__device__ __forceinline__ void tree_vec(const uint4 vt, const uint4 vd, bool diff, int k, const float *invR,
-                                         float mq, float isq, float mp, float isp, float cf, float *r)
+__device__ __forceinline__ void tree_vec(const uint4 vt, const uint4 vd, bool use_p, float mq, float isq, float mp,
+                                         float isp, float c, float cf, float *r)
 {
     constexpr int NE = Elt<DT>::kPerVec;
     constexpr int NP = NE / 2;
@@ -1376,8 +1386,7 @@ __device__ __forceinline__ void tree_vec(const uint4 vt, const uint4 vd, bool di
     const uint32_t wd[4] = {vd.x, vd.y, vd.z, vd.w};
     const unsigned long long Cf = sv::pack2(cf, cf);
     const unsigned long long Mq = sv::pack2(mq, mq), Iq = sv::pack2(isq, isq);
-    const unsigned long long Mp = sv::pack2(mp, mp), Ip = sv::pack2(isp, isp);
-    const bool need_p = diff || k > 0;
+    const unsigned long long Mp = sv::pack2(mp, mp), Ip = sv::pack2(isp, isp), Nc = sv::pack2(-c, -c);
 #pragma unroll
     for (int e = 0; e < NP; ++e) {
         unsigned long long zt, zd;
@@ -1390,38 +1399,17 @@ __device__ __forceinline__ void tree_vec(const uint4 vt, const uint4 vd, bool di
         }
         float a0, a1;
         sv::unpack2(sv::mul2(sv::sub2(zt, Mq), Cf), a0, a1);
-        unsigned long long x = sv::mul2(sv::pack2(sv::ex2(a0), sv::ex2(a1)), Iq);
-        unsigned long long pk = 0ull;
-        if (need_p) {
+        const unsigned long long x = sv::mul2(sv::pack2(sv::ex2(a0), sv::ex2(a1)), Iq);
+        if (use_p) {
             sv::unpack2(sv::mul2(sv::sub2(zd, Mp), Cf), a0, a1);
-            pk = sv::mul2(sv::pack2(sv::ex2(a0), sv::ex2(a1)), Ip);
-        }
-        for (int j = 0; j < k; ++j) {
             float d0, d1;
-            sv::unpack2(sv::sub2(x, pk), d0, d1);
-            const float ir = invR[j];
-            x = sv::mul2(sv::pack2(fmaxf(d0, 0.0f), fmaxf(d1, 0.0f)), sv::pack2(ir, ir));
-        }
-        if (diff) {
-            float d0, d1;
-            sv::unpack2(sv::sub2(x, pk), d0, d1);
+            sv::unpack2(sv::fma2(sv::mul2(sv::pack2(sv::ex2(a0), sv::ex2(a1)), Ip), Nc, x), d0, d1);
             r[2 * e] = fmaxf(d0, 0.0f);
             r[2 * e + 1] = fmaxf(d1, 0.0f);
         } else {
             sv::unpack2(x, r[2 * e], r[2 * e + 1]);
         }
     }
-}
-
-// The same arithmetic for one element: r_k(x) and p(x).
-__device__ __forceinline__ void tree_elem(float zq, float zp, int k, const float *invR, float mq, float isq,
-                                          float mp, float isp, float cf, float &rk, float &px)
-{
-    float x = __fmul_rn(sv::ex2(__fmul_rn(__fsub_rn(zq, mq), cf)), isq);
-    px = __fmul_rn(sv::ex2(__fmul_rn(__fsub_rn(zp, mp), cf)), isp);
-    for (int j = 0; j < k; ++j)
-        x = __fmul_rn(fmaxf(__fsub_rn(x, px), 0.0f), invR[j]);
-    rk = x;
 }
 
 // Chain test at the first child: u < min(1, q(x)/p(x)) in the log domain, as
@@ -1454,8 +1442,8 @@ __device__ __forceinline__ int walk_tile(int i, uint32_t rank, uint32_t C)
     return (int)(((uint32_t)(i / kWalkGroups) * C + rank) * kWalkGroups) + i % kWalkGroups;
 }
 
-// One pass over the row pair of a node: the slice masses of r_k (diff false)
-// or (r_k - p)+ (diff true) into w.slice, their total into w.Rt.  Every thread
+// One pass over the row pair of a node: the slice masses of (q - c p)+
+// (use_p) or q into w.slice, their total into w.Rt.  Every thread
 // of every CTA of the cluster calls it; g is this CTA's ring position,
 // advanced by the pass.  Each CTA streams its share of the tiles, writes the
 // warp shares of those slices into its own shared memory, and after a cluster
@@ -1464,7 +1452,7 @@ __device__ __forceinline__ int walk_tile(int i, uint32_t rank, uint32_t C)
 // slice masses and total.
 template <int DT>
 __device__ void walk_mass_pass(CtlW &w, unsigned char *ring, uint32_t &g, const uint4 *tsrc, const uint4 *dsrc,
-                               int NV, bool diff, int k, float mq, float isq, float mp, float isp, float cf)
+                               int NV, float mq, float isq, float mp, float isp, float c, float cf)
 {
     constexpr int VE = Elt<DT>::kPerVec;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1512,8 +1500,8 @@ __device__ void walk_mass_pass(CtlW &w, unsigned char *ring, uint32_t &g, const 
                         float r[VE];
                         const uint4 vd = dsrc ? reinterpret_cast<const uint4 *>(stage + kTileBytes)[sv_]
                                               : make_uint4(0, 0, 0, 0);
-                        tree_vec<DT>(reinterpret_cast<const uint4 *>(stage)[sv_], vd, diff, k, w.invR, mq, isq, mp,
-                                     isp, cf, r);
+                        tree_vec<DT>(reinterpret_cast<const uint4 *>(stage)[sv_], vd, dsrc != nullptr, mq, isq, mp,
+                                     isp, c, cf, r);
 #pragma unroll
                         for (int e = 0; e < VE; ++e)
                             part = __fadd_rn(part, r[e]);
@@ -1562,11 +1550,12 @@ __device__ void walk_mass_pass(CtlW &w, unsigned char *ring, uint32_t &g, const 
 }
 
 // Inverse CDF over the slice masses in w.slice (total w.Rt) at u: the slice,
-// then (recomputing that slice with the pass's arithmetic) the warp, lane and
-// element.  Every thread calls it; returns the token.
+// then (recomputing that slice with the pass's arithmetic: (q - c p)+ when
+// dsrc is given, else q) the warp, lane and element.  Every thread calls it;
+// returns the token.
 template <int DT>
-__device__ int walk_pick(CtlW &w, const uint4 *tsrc, const uint4 *dsrc, int NV, bool diff, int k, float mq, float isq,
-                         float mp, float isp, float cf, float u)
+__device__ int walk_pick(CtlW &w, const uint4 *tsrc, const uint4 *dsrc, int NV, float mq, float isq, float mp,
+                         float isp, float c, float cf, float u)
 {
     constexpr int VE = Elt<DT>::kPerVec;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1590,7 +1579,7 @@ __device__ int walk_pick(CtlW &w, const uint4 *tsrc, const uint4 *dsrc, int NV, 
     const int vec = ss * kSliceVecs + tid;
     if (tid < kConsThreads && vec < NV) {
         const uint4 vd = dsrc ? __ldcg(dsrc + vec) : make_uint4(0, 0, 0, 0);
-        tree_vec<DT>(__ldcg(tsrc + vec), vd, diff, k, w.invR, mq, isq, mp, isp, cf, r);
+        tree_vec<DT>(__ldcg(tsrc + vec), vd, dsrc != nullptr, mq, isq, mp, isp, c, cf, r);
 #pragma unroll
         for (int e = 0; e < VE; ++e)
             part = __fadd_rn(part, r[e]);
@@ -1621,7 +1610,29 @@ __global__ void __launch_bounds__(kWalkThreads, 1) sv_tree_walk_kernel(const SvP
         ring_init(w.ring);
         w.cf = (mode == MODE_SAMPLED) ? (float)(kLog2e / (double)T) : 0.0f;
     }
+    // The tree's inputs (kernel A does not write them, so before the wait):
+    // topology, tokens, uniforms and, for sampled trees, the two logits each
+    // child's test reads in its parent's rows (checked indices: a bad tree or
+    // token is caught by kernel A and ends the walk below).
+    for (int c = tid; c <= M; c += kWalkThreads) {
+        const int pc = par[c], x = tok[c];
+        w.par[c] = pc;
+        w.tok[c] = x;
+        w.u[c] = p.greedy ? 0.0f : p.u[row0 + c];
+        float zq = NAN, zp = NAN;
+        if (mode == MODE_SAMPLED && c >= 1 && pc >= 0 && pc < c && x >= 0 && x < V) {
+            zq = logit_at<DT>(p.target, (row0 + pc) * (size_t)V + x);
+            zp = logit_at<DT>(p.draft, (row0 + pc) * (size_t)V + x);
+        }
+        w.zq[c] = zq;
+        w.zp[c] = zp;
+    }
     sv::grid_dependency_wait();  // kernel A's statistics
+    for (int i = tid; i < (M + 1) * 4; i += kWalkThreads)
+        w.st[i] = __ldcg(p.ws_stats + row0 * 4 + i);
+    if (mode == MODE_GREEDY)
+        for (int c = tid; c <= M; c += kWalkThreads)
+            w.amax[c] = __ldcg(&p.ws_tok[row0 + c]);
     __syncthreads();
     const int err = __ldcg(&p.ws_err[b]);
     if (err || mode == MODE_INVALID) {
@@ -1645,16 +1656,16 @@ __global__ void __launch_bounds__(kWalkThreads, 1) sv_tree_walk_kernel(const SvP
         if (tid == 0) {
             int n = 0;
             for (;;) {
-                const int an = __ldcg(&p.ws_tok[row0 + n]);
+                const int an = w.amax[n];
                 int next = -1;
                 for (int c = n + 1; c <= M && next < 0; ++c)
-                    if (par[c] == n && tok[c] == an)
+                    if (w.par[c] == n && w.tok[c] == an)
                         next = c;
                 if (next < 0) {
                     out[depth] = an;
                     break;
                 }
-                out[depth] = tok[next];
+                out[depth] = w.tok[next];
                 path[depth] = next;
                 ++depth;
                 n = next;
@@ -1662,12 +1673,12 @@ __global__ void __launch_bounds__(kWalkThreads, 1) sv_tree_walk_kernel(const SvP
         }
     } else {
         const float cf = w.cf;
-        const float u0 = p.u[row0];
+        const float u0 = w.u[0];
         uint32_t g = 0;
         int n = 0;
         for (;;) {
-            const float *st = p.ws_stats + (row0 + n) * 4;
-            const float mq = __ldcg(st + 0), Sq = __ldcg(st + 1), mp = __ldcg(st + 2), Sp = __ldcg(st + 3);
+            const float *st = w.st + n * 4;
+            const float mq = st[0], Sq = st[1], mp = st[2], Sp = st[3];
             const float isq = 1.0f / Sq;
             const uint4 *tsrc = static_cast<const uint4 *>(p.target) + (row0 + n) * (size_t)NV;
             const uint4 *dsrc = static_cast<const uint4 *>(p.draft) + (row0 + n) * (size_t)NV;
@@ -1676,7 +1687,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) sv_tree_walk_kernel(const SvP
                 int cnt = 0;
                 for (int c0 = n + 1; c0 <= M; c0 += 32) {
                     const int c = c0 + lane;
-                    const bool is = c <= M && par[c] == n;
+                    const bool is = c <= M && w.par[c] == n;
                     const unsigned m = __ballot_sync(0xffffffffu, is);
                     if (is)
                         w.kids[cnt + __popc(m & ((1u << lane) - 1u))] = c;
@@ -1688,44 +1699,49 @@ __global__ void __launch_bounds__(kWalkThreads, 1) sv_tree_walk_kernel(const SvP
             __syncthreads();
             const int nk = w.nkids;
             const float isp = nk ? 1.0f / Sp : 0.0f;
-            int k = 0, accepted = -1;
-            bool masses_ready = false;  // w.slice holds r_k's masses up to a factor
+            // After k rejections with a non-empty residual, r_k = (q - c p)+ / Z:
+            // r_0 = q (c = 0, Z = 1), and (r_k - p)+ = (q - (c + Z) p)+ / Z, so a
+            // rejection moves c to c + Z and Z to the new pass's total (both
+            // unchanged when that total is 0: r_k stays).
+            float c = 0.0f, Z = 1.0f;
+            int accepted = -1;
+            bool masses_ready = false;  // w.slice holds the masses of (q - c p)+
             for (int ci = 0; ci < nk; ++ci) {
-                const int c = w.kids[ci];
+                const int ch = w.kids[ci];
                 if (tid == 0) {
-                    const int x = tok[c];
-                    const float zq = logit_at<DT>(p.target, (row0 + n) * (size_t)V + x);
-                    const float zp = logit_at<DT>(p.draft, (row0 + n) * (size_t)V + x);
-                    const double uc = (double)p.u[row0 + c];
+                    const float zq = w.zq[ch], zp = w.zp[ch];  // at ch's token in n's rows
+                    const double uc = (double)w.u[ch];
                     bool acc;
-                    if (k == 0) {
+                    if (c == 0.0f) {
                         acc = first_child_test(zq, zp, mq, Sq, mp, Sp, T, uc);
                     } else {
-                        float rk, px;
-                        tree_elem(zq, zp, k, w.invR, mq, isq, mp, isp, cf, rk, px);
+                        const float qx = __fmul_rn(sv::ex2(__fmul_rn(__fsub_rn(zq, mq), cf)), isq);
+                        const float px = __fmul_rn(sv::ex2(__fmul_rn(__fsub_rn(zp, mp), cf)), isp);
+                        const float rk = __fdiv_rn(fmaxf(__fmaf_rn(px, -c, qx), 0.0f), Z);
                         acc = (zp == -INFINITY) || (px == 0.0f) || (uc < fmin(1.0, (double)rk / (double)px));
                     }
                     w.accept = acc ? 1 : 0;
                 }
                 __syncthreads();
                 if (w.accept) {
-                    accepted = c;
+                    accepted = ch;
                     break;
                 }
-                walk_mass_pass<DT>(w, ring, g, tsrc, dsrc, NV, /*diff=*/true, k, mq, isq, mp, isp, cf);
-                if (w.Rt > 0.0f) {
-                    if (tid == 0)
-                        w.invR[k] = __frcp_rn(w.Rt);
-                    ++k;
+                const float c1 = __fadd_rn(c, Z);
+                walk_mass_pass<DT>(w, ring, g, tsrc, dsrc, NV, mq, isq, mp, isp, c1, cf);
+                const float R = w.Rt;
+                if (R > 0.0f) {
+                    c = c1;
+                    Z = R;
                     masses_ready = true;
                 } else {
                     masses_ready = false;  // the residual is empty: r_k stays
                 }
-                __syncthreads();
+                __syncthreads();  // every thread has read w.Rt before the next pass rewrites it
             }
             if (accepted >= 0) {
                 if (tid == 0 && leader) {
-                    out[depth] = tok[accepted];
+                    out[depth] = w.tok[accepted];
                     path[depth] = accepted;
                 }
                 ++depth;
@@ -1733,17 +1749,11 @@ __global__ void __launch_bounds__(kWalkThreads, 1) sv_tree_walk_kernel(const SvP
                 __syncthreads();
                 continue;
             }
-            // the token: from r_k
-            bool diff = false;
-            int kk = k;
-            if (masses_ready) {
-                diff = true;  // the last pass: (r_{k-1} - p)+ = R_k r_k
-                kk = k - 1;
-            } else {
-                walk_mass_pass<DT>(w, ring, g, tsrc, nk ? dsrc : nullptr, NV, false, k, mq, isq, mp, isp, cf);
-            }
-            const int t = walk_pick<DT>(w, tsrc, (diff || kk > 0) ? dsrc : nullptr, NV, diff, kk, mq, isq, mp, isp,
-                                        cf, u0);
+            // the token: from r_k = (q - c p)+ / Z, by inverse CDF over its slice masses
+            const uint4 *dk = (c > 0.0f) ? dsrc : nullptr;
+            if (!masses_ready)
+                walk_mass_pass<DT>(w, ring, g, tsrc, dk, NV, mq, isq, mp, isp, c, cf);
+            const int t = walk_pick<DT>(w, tsrc, dk, NV, mq, isq, mp, isp, c, cf, u0);
             if (tid == 0 && leader)
                 out[depth] = t;
             break;

@@ -188,6 +188,14 @@ __device__ __forceinline__ unsigned long long add2(unsigned long long a, unsigne
     return r;
 }
 
+// a * b + c, one rounding per lane
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b, unsigned long long c)
+{
+    unsigned long long r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
 // max of two bf16x2 words, lane by lane; a NaN lane yields the other operand
 __device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b)
 {
