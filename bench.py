@@ -454,7 +454,7 @@ def run_ours(args):
     # then every timed call follows an L2 flush (a 256 MiB write, then a
     # 256 MiB read of another buffer, so no dirty lines are left to write
     # back) and the calls' own event intervals are summed.
-    flush = w.logit_bytes < 2 * L2_BYTES
+    flush = args.flush or w.logit_bytes < 2 * L2_BYTES
     if flush:
         fl_w = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
         fl_r = torch.ones(64 << 20, dtype=torch.float32, device=dev)
@@ -625,6 +625,7 @@ def main():
     ap.add_argument("--workload", default="headline")
     ap.add_argument("--batch", type=int, default=0, help="override B (profiling of a smaller case)")
     ap.add_argument("--cluster", type=int, default=0, help="cluster size override (0 = automatic)")
+    ap.add_argument("--flush", action="store_true", help="flush L2 before every timed call, whatever the input size")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-check", action="store_true")
