@@ -554,6 +554,8 @@ __global__ void __launch_bounds__(kThreads, 4) sv_rows_kernel(const SvParams p)
     constexpr int kStages = kStagesA;
     CtlA &ctl = *reinterpret_cast<CtlA *>(smem + ring_bytes(kStages));
 
+    if constexpr (TREE)
+        sv::grid_launch_dependents();  // the walk's clusters may start on SMs as this grid's CTAs retire
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t C = sv::cluster_nctarank();
     const uint32_t rank = sv::cluster_ctarank();

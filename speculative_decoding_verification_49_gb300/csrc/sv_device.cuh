@@ -98,6 +98,14 @@ __device__ __forceinline__ void grid_dependency_wait()
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// Lets the grid launched after this one with programmatic serialisation
+// schedule its CTAs as soon as every CTA of this grid has executed this (or
+// exited); their grid_dependency_wait still waits for this grid to complete.
+__device__ __forceinline__ void grid_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- thread-block cluster --------------------------------------------------
 __device__ __forceinline__ uint32_t cluster_ctarank()
 {
