@@ -1367,6 +1367,7 @@ struct CtlW {
     float u[kMaxTreeNodes];
     float zq[kMaxTreeNodes], zp[kMaxTreeNodes];  // logits at node c's token in its parent's rows
     float st[kMaxTreeNodes * 4];                // (mq, Sq, mp, Sp) of each node
+    int err;                                    // the sequence's error bits, read once
 };
 
 constexpr size_t kSmemW = ring_bytes(kStagesW) + sizeof(CtlW);
@@ -1635,8 +1636,16 @@ __global__ void __launch_bounds__(kWalkThreads, 1) sv_tree_walk_kernel(const SvP
     if (mode == MODE_GREEDY)
         for (int c = tid; c <= M; c += kWalkThreads)
             w.amax[c] = __ldcg(&p.ws_tok[row0 + c]);
+    if (tid == 0)
+        w.err = __ldcg(&p.ws_err[b]);
     __syncthreads();
-    const int err = __ldcg(&p.ws_err[b]);
+    const int err = w.err;
+    // The leader resets the error word for the next call: every CTA of the
+    // cluster has read it first, so all of them take the same branch below (a
+    // CTA that missed the error would wait for the exited leader at a pass's
+    // cluster barrier).
+    if (C > 1)
+        sv::cluster_sync();
     if (err || mode == MODE_INVALID) {
         if (tid == 0 && leader) {
             for (int q = 0; q <= M; ++q) {
