@@ -131,6 +131,36 @@ def test_tree_invalid_inputs():
     _check(synth.make_tree_workload("tree_small", seed=7, device="cuda", B=6), ctx=ctx)
 
 
+@pytest.mark.parametrize("B", [6, 64])
+def test_tree_invalid_trees_repeatedly_in_clustered_walks(B):
+    """Invalid trees (a NaN temperature, a bad token) beside valid ones, 25
+    calls in a row on one context, with the walk split over clusters of 4 CTAs
+    (B = 6) and of 2 (B = 64): every call returns -1 rows for the invalid trees
+    and the same tokens for the valid ones.  Every CTA of a walk cluster reads
+    the sequence's error word before the leader resets it for the next call."""
+    w = synth.make_tree_workload("tree_small", seed=11, device="cuda", B=B)
+    bad_t = list(range(0, B, 3))
+    bad_d = [b for b in range(1, B, 3)]
+    for b in bad_t:
+        w.temperature[b] = float("nan")
+    for b in bad_d:
+        w.tokens[b, 1] = w.V
+    bad = sorted(bad_t + bad_d)
+    good = [b for b in range(B) if b not in bad]
+    ctx = _ctx(w)
+    first = None
+    for _ in range(25):
+        gpu = parity.run_gpu_tree(ctx, w, stats=False)
+        assert (gpu["num_accepted"][bad] == -1).all() and (gpu["out_tokens"][bad] == -1).all()
+        assert (gpu["num_accepted"][good] >= 0).all()
+        assert ctx.status() != sv.SV_OK
+        if first is None:
+            first = gpu
+        else:
+            assert np.array_equal(gpu["out_tokens"], first["out_tokens"])
+            assert np.array_equal(gpu["path_nodes"], first["path_nodes"])
+
+
 def test_tree_root_only_and_ragged_vocabularies():
     for V, dtype in [(1000, "f32"), (4104, "bf16"), (16, "f32")]:
         w = synth.make_tree_workload("tree_small", seed=8, device="cuda", B=5, M=0, V=V, dtype=dtype)
