@@ -175,37 +175,6 @@ struct Online {
     float m, s;
 };
 
-template <int NE>
-__device__ __forceinline__ void online_add(Online &o, const float *z, float cf)
-{
-    float vmax = z[0];
-#pragma unroll
-    for (int k = 1; k < NE; ++k)
-        vmax = fmaxf(vmax, z[k]);
-    if (vmax > o.m) {
-        o.s *= sv::ex2((o.m - vmax) * cf);
-        o.m = vmax;
-    }
-    if (o.m != -INFINITY) {
-        float e[NE];
-#pragma unroll
-        for (int k = 0; k < NE; ++k)
-            e[k] = sv::ex2((z[k] - o.m) * cf);
-#pragma unroll
-        for (int w = 1; w < NE; w *= 2)
-#pragma unroll
-            for (int k = 0; k + w < NE; k += 2 * w)
-                e[k] += e[k + w];
-        o.s += e[0];
-    } else {
-        // only -inf (or NaN) seen so far: a NaN must still poison the sum
-#pragma unroll
-        for (int k = 0; k < NE; ++k)
-            if (z[k] != z[k])
-                o.s = NAN;
-    }
-}
-
 __device__ __forceinline__ Online online_merge(Online a, Online b, float cf)
 {
     const float m = fmaxf(a.m, b.m);
@@ -226,10 +195,12 @@ __device__ __forceinline__ Online warp_merge(Online o, float cf)
     return o;
 }
 
-// Packed form of online_add for one 16-byte vector: the max over the vector
-// is taken on bf16x2 words (exact), the exponent arguments (z - m) * c and the
-// sums run on f32x2 pairs, and the thread keeps two partial sums (s, s2).
-// The arguments are rounded exactly as in online_add.
+// One 16-byte vector of logits into a thread's running normaliser: the vector
+// max (on bf16x2 words for bf16, exact), then, when it exceeds m, the sums are
+// rescaled by exp2((m_old - m) c) and m moves; every element adds exp2((z - m) c),
+// the arguments and the sums computed on f32x2 pairs so that the thread keeps
+// two partial sums (even and odd elements).  While only -inf has been seen the
+// sums stay 0, and a NaN element makes them NaN.
 struct Online2 {
     float m;
     unsigned long long s;  // (even, odd) partial sums
@@ -302,32 +273,9 @@ struct ArgMax {
     int nan;
 };
 
-template <int NE>
-__device__ __forceinline__ void argmax_add(ArgMax &a, const float *z, int col0)
-{
-    float vmax = z[0];
-    int nan = z[0] != z[0];
-#pragma unroll
-    for (int k = 1; k < NE; ++k) {
-        vmax = fmaxf(vmax, z[k]);
-        nan |= z[k] != z[k];
-    }
-    a.nan |= nan;
-    if (vmax > a.v) {
-        // first element of this vector that holds the new max (ascending columns)
-        int best = NE - 1;
-#pragma unroll
-        for (int k = NE - 1; k >= 0; --k)
-            if (z[k] == vmax)
-                best = k;
-        a.v = vmax;
-        a.i = col0 + best;
-    }
-}
-
-// Packed form of argmax_add for one 16-byte vector: the vector max (and a
-// NaN test) on bf16x2 words / pairs of floats, the index only when the max
-// improves.
+// One 16-byte vector of logits into a thread's running argmax: the vector max
+// (and a NaN test) on bf16x2 words or pairs of floats, NaN never the max; when
+// it exceeds the running max, the lowest column of the vector holding it.
 template <int DT>
 __device__ __forceinline__ void argmax_add2(ArgMax &a, const uint4 v, int col0)
 {

@@ -147,13 +147,6 @@ __device__ __forceinline__ float ld_dsmem_f32(uint32_t a)
     return v;
 }
 
-__device__ __forceinline__ double ld_dsmem_f64(uint32_t a)
-{
-    double v;
-    asm volatile("ld.shared::cluster.f64 %0, [%1];" : "=d"(v) : "r"(a) : "memory");
-    return v;
-}
-
 __device__ __forceinline__ int ld_dsmem_s32(uint32_t a)
 {
     int v;
