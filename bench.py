@@ -509,9 +509,16 @@ def run_ours(args):
     rows_us = 1e3 * ms_rows / nprof
     sample_us = 1e3 * ms_sample / nprof
     rows_gbs = w.logit_bytes / (rows_us * 1e-6) / 1e9
+    # bytes kernel A actually reads: every verifier row, and the draft rows of
+    # sampled sequences only (greedy ones need no draft probabilities)
+    Tc = w.temperature.float().cpu()
+    n_sampled = 0 if w.greedy else int(((Tc > 0) & torch.isfinite(Tc)).sum())
+    bytes_read = w.B * (w.N + 1) * w.V * w.elt + n_sampled * w.N * w.V * w.elt
     kernels = {
         "sv_rows_kernel": {"us_per_launch": rows_us, "share": ms_rows / (ms_rows + ms_sample),
-                           "algorithmic_bytes": w.logit_bytes, "gbs": rows_gbs},
+                           "algorithmic_bytes": w.logit_bytes, "gbs": rows_gbs,
+                           "bytes_read": bytes_read, "gbs_read": bytes_read / (rows_us * 1e-6) / 1e9,
+                           "sampled_sequences": n_sampled},
         "sv_mass_kernel+sv_pick_kernel": {
             "us_per_launch": sample_us, "share": ms_sample / (ms_rows + ms_sample),
             "note": "residual sampling; re-reads the rejected row pair of each sampled sequence "
