@@ -2034,9 +2034,11 @@ int clamp_cluster(int C, int nv, const int *fits)
 
 // Kernel A: one CTA per position once there are at least two positions per
 // SM, else split the rows over a cluster for parallelism (about two waves of
-// four CTAs per SM).  Measured on GB300: 384 positions (mixed batch) 56.4 us
-// with one CTA per position against 59.5 us in clusters of 4; 1024 tree nodes
-// 166 us against 168 us in clusters of 2.
+// four CTAs per SM), down to 4 KiB of a row per CTA.  Measured on GB300: 384
+// positions (mixed batch) 56.4 us with one CTA per position against 59.5 us in
+// clusters of 4; 1024 tree nodes 137.5 us against 139.3 us in clusters of 2;
+// 5 positions of 4 KiB rows 17.7 us per call unsplit against 18.7 us in
+// clusters of 8.
 int cluster_a(const spec_verify_ctx *c, int B, int N, bool tree = false)
 {
     if (c->cluster_override > 0)
@@ -2047,7 +2049,12 @@ int cluster_a(const spec_verify_ctx *c, int B, int N, bool tree = false)
     if (units >= 2LL * c->num_sms)
         return clamp_cluster(1, nv, fits);
     const long long want = 8LL * c->num_sms;
-    const int C = (int)((want + units - 1) / (units > 0 ? units : 1));
+    int C = (int)((want + units - 1) / (units > 0 ? units : 1));
+    // a CTA's share of a row stays at least 4 KiB: shorter rows are not split
+    // (tiny rows gain nothing from a cluster but its launch and barriers)
+    const long long by_len = (long long)nv * 16 / 4096;
+    if (C > by_len)
+        C = by_len > 1 ? (int)by_len : 1;
     return clamp_cluster(C < 8 ? C : 8, nv, fits);
 }
 
