@@ -76,15 +76,23 @@ struct GemmCtl {
     int abort;
 };
 
-// Logits epilogue: each epilogue warp turns its 32 rows x 32 columns around in
-// shared memory (row stride 33: no bank conflicts) so that every store of the
-// warp writes 128 contiguous bytes of one row.
+// Logits epilogue, staged in shared memory 32 rows x 32 columns at a time.
+// With a tensor map of the output (V a multiple of 4): each epilogue warp
+// writes its block into one of two 4 KiB buffers in the 128-byte-swizzled
+// layout of the map and one lane stores it with a single TMA tensor store.
+// Otherwise the warp turns the block around (row stride 33: no bank
+// conflicts) so that every warp store writes 128 contiguous bytes of one row.
 constexpr int kEpiStride = 33;
-constexpr size_t kEpiBytes = 4 * 32 * kEpiStride * sizeof(float);
+constexpr int kEpiBuf = 32 * 32 * 4;                   // one staged block, bytes
+constexpr size_t kEpiBytes = 4 * 2 * (size_t)kEpiBuf;  // 4 warps x 2 buffers
+static_assert(4 * 32 * kEpiStride * 4 <= (int)kEpiBytes, "the transpose fits in the staging area");
+
+template <bool PAIR> __host__ __device__ constexpr size_t smem_ring() { return (size_t)GemmCfg<PAIR>::kStages * GemmCfg<PAIR>::kStage; }
+static_assert(smem_ring<true>() % 1024 == 0 && smem_ring<false>() % 1024 == 0, "the staging area stays 1024-aligned");
 
 template <bool PAIR> constexpr size_t smem_bytes()
 {
-    return 1024 + (size_t)GemmCfg<PAIR>::kStages * GemmCfg<PAIR>::kStage + sizeof(GemmCtl) + kEpiBytes;
+    return 1024 + smem_ring<PAIR>() + kEpiBytes + sizeof(GemmCtl);
 }
 static_assert(smem_bytes<true>() <= 232448 && smem_bytes<false>() <= 232448, "227 KiB of shared memory per CTA");
 
@@ -93,6 +101,7 @@ constexpr double kLog2e = 1.4426950408889634074;
 struct LmParams {
     int M, N, K;
     float *logits;  // [M, N] f32 (logits epilogue)
+    int tma_store;  // the logits go out through the output tensor map
     int *status;    // error bits, may be null
     svlm::StatsArgs st;  // statistics epilogue
 };
@@ -188,7 +197,8 @@ __device__ __forceinline__ void row_stats(uint32_t taddr, int n0, const LmParams
 
 template <bool STATS, bool PAIR>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    sv_lmhead_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, LmParams p)
+    sv_lmhead_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmC, LmParams p)
 {
     using Cfg = GemmCfg<PAIR>;
     constexpr int kStages = Cfg::kStages;
@@ -196,8 +206,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     extern __shared__ unsigned char smem_raw[];
     // 128-byte-swizzled tiles want 1024-byte alignment
     unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    GemmCtl &ctl = *reinterpret_cast<GemmCtl *>(smem + (size_t)kStages * Cfg::kStage);
-    float *epi = reinterpret_cast<float *>(smem + (size_t)kStages * Cfg::kStage + sizeof(GemmCtl));
+    unsigned char *epi_raw = smem + smem_ring<PAIR>();  // 1024-aligned staging area
+    float *epi = reinterpret_cast<float *>(epi_raw);
+    GemmCtl &ctl = *reinterpret_cast<GemmCtl *>(epi_raw + kEpiBytes);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = PAIR ? sv::cluster_ctarank() : 0u;
     const bool leader = rank == 0;  // the CTA whose thread issues the MMAs
@@ -320,6 +331,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     } else if (warp >= 4) {
         const int q = warp - 4;  // TMEM lanes 32q .. 32q+31
         int t = 0;
+        uint32_t nstore = 0;  // staged blocks so far (TMA-store epilogue): alternates the buffers
         for (int blk = unit; blk < nblock; blk += nunits, ++t) {
             const int buf = t & 1;
             const uint32_t use = (uint32_t)(t >> 1);
@@ -335,6 +347,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * kBN);
             if constexpr (STATS) {
                 row_stats(taddr, n0, p, row);
+            } else if (p.tma_store) {
+                const int r0 = m0 + 32 * q;  // the warp's first row
+                for (int c0 = 0; c0 < kBN; c0 += 32, ++nstore) {
+                    float v[32];
+                    sv::tmem_ld32(taddr + (uint32_t)c0, v);
+                    unsigned char *buf = epi_raw + (size_t)(q * 2 + (nstore & 1)) * kEpiBuf;
+                    if (lane == 0)
+                        sv::bulk_wait_read<1>();  // the store that last read this buffer is done with it
+                    __syncwarp();
+                    // row `lane`: 16-byte chunk j at chunk j ^ (row % 8) (128-byte swizzle)
+                    float4 *rowp = reinterpret_cast<float4 *>(buf + lane * 128);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        rowp[j ^ (lane & 7)] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                    sv::fence_async_shared();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (r0 < p.M && n0 + c0 < p.N)
+                            sv::tma_store_2d(&tmC, n0 + c0, r0, buf);
+                        sv::bulk_commit();  // one group per block, empty when nothing was stored
+                    }
+                }
             } else {
                 float *stg = epi + q * 32 * kEpiStride;
                 const int r0 = m0 + 32 * q;  // the warp's first row
@@ -362,6 +396,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     sv::mbar_arrive(&ctl.acc_empty[buf]);
             }
         }
+        if (lane == 0)
+            sv::bulk_wait_all();  // every tensor store has read its buffer and completed
+        __syncwarp();
     }
     sv::tc_fence_before();
     __syncthreads();
@@ -426,6 +463,23 @@ bool make_map(CUtensorMap *m, const void *base, int rows, int K, int box_rows)
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Row-major f32 logits [rows, cols] as a TMA map with 32 x 32 boxes in the
+// 128-byte-swizzled layout (the epilogue's tensor stores); cols * 4 must be a
+// multiple of 16 and base 16-byte aligned.
+bool make_map_out(CUtensorMap *m, const float *base, int rows, int cols)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc)
+        return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 4};
+    const cuuint32_t box[2] = {32, 32};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 std::once_flag g_attr_once;
 cudaError_t g_attr_err = cudaSuccess;
 
@@ -481,12 +535,20 @@ sv_status launch(const void *hidden, const void *weight, int M, int V, int K, co
     });
     if (g_attr_err != cudaSuccess)
         return SV_ERR_CUDA;
-    CUtensorMap ta, tb;
+    CUtensorMap ta, tb, tc;
+    // the logits go out by tensor stores when their rows are 16-byte multiples
+    LmParams q = p;
+    q.tma_store = 0;
+    if (!STATS && p.logits && V % 4 == 0 && (reinterpret_cast<uintptr_t>(p.logits) & 15u) == 0 &&
+        make_map_out(&tc, p.logits, M, V))
+        q.tma_store = 1;
     // CTA pairs (one 256-row MMA) when there are two row tiles to pair
     const bool pair = (M + kBM - 1) / kBM >= 2;
     const int P = pair ? 2 : 1;
     if (!make_map(&ta, hidden, M, K, kBM) || !make_map(&tb, weight, V, K, kBN / P))
         return SV_ERR_CUDA;
+    if (!q.tma_store)
+        tc = ta;  // not read
     const long long nblock = (long long)((M + kBM * P - 1) / (kBM * P)) * ((V + kBN - 1) / kBN);
     if (nblock > INT_MAX / P)
         return SV_ERR_INVALID_ARG;
@@ -509,8 +571,8 @@ sv_status launch(const void *hidden, const void *weight, int M, int V, int K, co
     const int fit = resident_units<STATS>(pair, dev, sms, cfg);
     const long long units = nblock < fit ? nblock : fit;
     cfg.gridDim = dim3((unsigned)(units * P));
-    const cudaError_t e = pair ? cudaLaunchKernelEx(&cfg, sv_lmhead_kernel<STATS, true>, ta, tb, p)
-                               : cudaLaunchKernelEx(&cfg, sv_lmhead_kernel<STATS, false>, ta, tb, p);
+    const cudaError_t e = pair ? cudaLaunchKernelEx(&cfg, sv_lmhead_kernel<STATS, true>, ta, tb, tc, q)
+                               : cudaLaunchKernelEx(&cfg, sv_lmhead_kernel<STATS, false>, ta, tb, tc, q);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return SV_ERR_CUDA;
