@@ -22,7 +22,8 @@
 // finished tile back (tcgen05.ld, one TMEM lane = one row per thread) while
 // the next tile accumulates into the other one.  A product with a single row
 // tile runs on single CTAs (M = 128, the whole weight tile, 4 stages).  The
-// epilogue either writes the logits as f32, or (the fused verify path) only
+// epilogue either writes the logits as f32 (32 x 32 blocks staged in shared
+// memory and written by TMA tensor stores), or (the fused verify path) only
 // each row's statistics over the tile -- max and sum of exp2((z - max) *
 // log2(e)/T), or max and argmax for greedy rows, and the logit at the row's
 // draft token -- so the logits never reach HBM.  The blocks of one
