@@ -49,3 +49,20 @@ def test_lm_head_logits_sampled_at_vocabulary_size():
     want = oracle.lm_head_logits(h[rows].cpu(), w.cpu())
     err = np.abs(got[rows.cuda()].cpu().double().numpy() - want)
     assert (err <= _bound(h[rows].cpu(), w.cpu())).all()
+
+
+def test_lm_head_logits_into_an_unaligned_output():
+    """An output buffer that starts 4 bytes past a 16-byte boundary (no tensor
+    map: the epilogue's warp stores) gives the same logits as an aligned one
+    (tensor stores), and neither writes outside its [M, V] block."""
+    M, V, K = 200, 2048, 128
+    h, w = _case(M, V, K, seed=11)
+    h, w = h.cuda(), w.cuda()
+    want = sv.lm_head_logits(h, w).cpu()
+    flat = torch.full((M * V + 8,), -7.0, dtype=torch.float32, device="cuda")
+    out = flat[1:1 + M * V].view(M, V)
+    assert out.data_ptr() % 16 == 4
+    got = sv.lm_head_logits(h, w, out=out)
+    torch.cuda.synchronize()
+    assert torch.equal(got.cpu(), want)
+    assert flat[0].item() == -7.0 and (flat[1 + M * V:] == -7.0).all()
