@@ -55,6 +55,28 @@ def test_parity_full_oracle(name, seed, overrides):
     _check(w)
 
 
+def _random_shapes(n=12, seed=2026):
+    """Seeded random shapes: dtype, V at every 16-byte alignment (a multiple of
+    8 bf16 or 4 f32 elements, up to 9600), N 0..7, B 1..40, one temperature or a
+    per-sequence mix that includes greedy sequences."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for k in range(n):
+        dtype = "bf16" if rng.random() < 0.5 else "f32"
+        V = int(rng.integers(1, 1201)) * (8 if dtype == "bf16" else 4)
+        N = int(rng.integers(0, 8))
+        B = int(rng.integers(1, 41))
+        T = (0.0, 0.5, 1.0, 1.7) if rng.random() < 0.5 else float(rng.choice([0.3, 0.8, 1.0, 2.0]))
+        out.append((k, dtype, V, N, B, T))
+    return out
+
+
+@pytest.mark.parametrize("k,dtype,V,N,B,T", _random_shapes())
+def test_parity_random_shapes(k, dtype, V, N, B, T):
+    w = synth.make_workload("small", seed=100 + k, device="cuda", B=B, N=N, V=V, dtype=dtype, T=T)
+    _check(w)
+
+
 @pytest.mark.parametrize("name,nsample", [("headline", 24), ("stress", 24)])
 def test_parity_full_size_sampled(name, nsample):
     """The full-size launch the benchmark times; the oracle checks a spread
