@@ -66,3 +66,18 @@ def test_lm_head_logits_into_an_unaligned_output():
     torch.cuda.synchronize()
     assert torch.equal(got.cpu(), want)
     assert flat[0].item() == -7.0 and (flat[1 + M * V:] == -7.0).all()
+
+
+def test_lm_head_logits_long_hidden_size():
+    """A 70B-class hidden size (K = 8192: 128 stages per tile, the ring wrapping
+    many times within each tile) for 512 rows of a 32768-entry head; 16 rows
+    checked against the float64 product within the accumulation bound."""
+    M, V, K = 512, 32768, 8192
+    g = torch.Generator(device="cuda").manual_seed(3)
+    h = (torch.randn((M, K), generator=g, device="cuda") * 0.5).to(torch.bfloat16)
+    w = (torch.randn((V, K), generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    got = sv.lm_head_logits(h, w)
+    rows = torch.tensor([0, 1, 31, 32, 127, 128, 255, 256, 300, 383, 384, 400, 450, 500, 510, 511])
+    want = oracle.lm_head_logits(h[rows].cpu(), w.cpu())
+    err = np.abs(got[rows.cuda()].cpu().double().numpy() - want)
+    assert (err <= _bound(h[rows].cpu(), w.cpu())).all()
