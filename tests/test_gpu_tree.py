@@ -161,6 +161,13 @@ def test_tree_invalid_trees_repeatedly_in_clustered_walks(B):
             assert np.array_equal(gpu["path_nodes"], first["path_nodes"])
 
 
+def test_tree_with_the_most_nodes():
+    """1024 nodes per tree (M = 1023, the largest tree the walk holds in shared
+    memory), random topologies, against the tree oracle."""
+    w = synth.make_tree_workload("tree_small", seed=21, device="cuda", B=3, M=1023, V=256)
+    _check(w)
+
+
 def test_tree_root_only_and_ragged_vocabularies():
     for V, dtype in [(1000, "f32"), (4104, "bf16"), (16, "f32")]:
         w = synth.make_tree_workload("tree_small", seed=8, device="cuda", B=5, M=0, V=V, dtype=dtype)
