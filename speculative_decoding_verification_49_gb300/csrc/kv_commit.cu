@@ -23,8 +23,9 @@
 // and most units are empty.  Measured alternatives that were no faster on
 // such a commit: a TMA-staged copy (bulk load into shared memory, bulk store
 // out; the stage must be sized for all N rows), a persistent grid, one CTA
-// per (sequence, split) striping all planes, larger or smaller units, and
-// deeper unrolling.
+// per (sequence, split) striping all planes, larger or smaller units, deeper
+// unrolling, and one warp serving the same unit of 2, 4 or 8 planes with all
+// their loads in flight (12.6-15.0 us against 12.55 us per commit).
 #include <climits>
 #include <cstddef>
 #include <cstdint>
