@@ -8,6 +8,7 @@ import numpy as np
 import torch
 
 import synth
+from synth.workloads import EAGLE16_PARENT
 
 
 def _arr(t):
@@ -72,3 +73,38 @@ def test_stress_forces_tokens_the_verifier_rules_out():
     b, i = np.meshgrid(np.arange(w.B), np.arange(w.N), indexing="ij")
     forced = zt[b, i, d] == -30.0
     assert 0.02 < forced.mean() < 0.09, forced.mean()
+
+
+def test_tree_topologies_and_greedy_children():
+    """Random trees: parent[n] in [max(0, n-3), n-1] and parent[0] = -1; the
+    bench tree is the fixed 16-node shape; a greedy tree's children all carry
+    the argmax of their parent's draft row."""
+    w = synth.make_tree_workload("tree_mixed", seed=6, B=24, V=2048)
+    par = w.parent.numpy()
+    n = np.arange(1, w.M + 1)
+    assert (par[:, 0] == -1).all()
+    assert ((par[:, 1:] >= np.maximum(0, n - 3)) & (par[:, 1:] <= n - 1)).all()
+    T = w.temperature.numpy()
+    assert (T == 0).any()
+    zd = _arr(w.draft)
+    tok = w.tokens.numpy()
+    for b in np.nonzero(T == 0)[0]:
+        for c in range(1, w.M + 1):
+            assert tok[b, c] == zd[b, par[b, c]].argmax()
+    fixed = synth.make_tree_workload("tree", seed=0, B=2, V=1024)
+    assert fixed.parent.numpy().tolist() == [EAGLE16_PARENT] * 2
+
+
+def test_fused_draft_model_reads_the_first_features():
+    """fused: the draft head is the verifier head's first Kd features scaled by
+    sqrt(Kt/Kd) (rounded to bf16); greedy drafts are the argmax of the draft
+    product."""
+    w = synth.make_fused_workload("fused_mixed", seed=7, B=6)
+    wt, wd = w.target_weight.float(), w.draft_weight.float()
+    want = (wt[:, :w.Kd] * (w.Kt / w.Kd) ** 0.5).to(torch.bfloat16).float()
+    assert torch.equal(wd, want)
+    T = w.temperature.numpy()
+    zd = (w.draft_hidden.float() @ wd.T).view(w.B, w.N, w.V).numpy()
+    d = w.draft_tokens.numpy()
+    for b in np.nonzero(T <= 0)[0]:
+        assert (d[b] == zd[b].argmax(axis=-1)).all()
