@@ -48,6 +48,31 @@ def test_fused_ragged_vocabulary_and_depth(V, Kt, Kd):
     _check(w)
 
 
+def _random_fused_shapes(n=6, seed=77):
+    """Seeded random shapes: V any multiple of 4 up to 12000 (the float32
+    context's rule; most leave a ragged last 32-column box for the tensor
+    stores), verifier and draft hidden sizes multiples of 8 (not of the 64-wide
+    stage; the draft's no larger than the verifier's), B 1-24, N 0-6, one
+    temperature or a per-sequence mix with greedy sequences."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for k in range(n):
+        V = int(rng.integers(1, 3001)) * 4
+        Kt = int(rng.integers(2, 129)) * 8
+        Kd = int(rng.integers(1, Kt // 8 + 1)) * 8  # the draft reads the first Kd hidden features
+        B = int(rng.integers(1, 25))
+        N = int(rng.integers(0, 7))
+        T = (0.0, 0.7, 1.0) if rng.random() < 0.5 else float(rng.choice([0.5, 1.0, 1.5]))
+        out.append((k, V, Kt, Kd, B, N, T))
+    return out
+
+
+@pytest.mark.parametrize("k,V,Kt,Kd,B,N,T", _random_fused_shapes())
+def test_fused_random_shapes(k, V, Kt, Kd, B, N, T):
+    w = synth.make_fused_workload("fused_small", seed=200 + k, device="cuda", V=V, Kt=Kt, Kd=Kd, B=B, N=N, T=T)
+    _check(w)
+
+
 def test_fused_all_greedy_without_draft_model():
     w = synth.make_fused_workload("fused_mixed", seed=1, device="cuda")
     rep, _ = _check(w, greedy=True)
