@@ -66,6 +66,26 @@ def test_kv_commit_matches_the_oracle(P, B, N, row, max_len):
     assert np.array_equal(got[0], want[0])
 
 
+def _random_layouts(n=10, seed=31):
+    """Seeded random layouts: planes 1-12, B 1-60, N 1-8, rows a multiple of
+    16 bytes up to 5 KiB (units that end inside a row and rows that span
+    units), cache lengths 1-40; invalid, bad and overflowing counts mixed in."""
+    rng = np.random.default_rng(seed)
+    return [(k, int(rng.integers(1, 13)), int(rng.integers(1, 61)), int(rng.integers(1, 9)),
+             int(rng.integers(1, 321)) * 16, int(rng.integers(1, 41))) for k in range(n)]
+
+
+@pytest.mark.parametrize("k,P,B,N,row,max_len", _random_layouts())
+def test_kv_commit_random_layouts(k, P, B, N, row, max_len):
+    rng = np.random.default_rng(900 + k)
+    case = _random_case(rng, P, B, N, row, max_len, invalid=True)
+    want = oracle.kv_commit(*case)
+    got = _gpu_commit(*case)
+    assert got[2] == want[2]
+    assert np.array_equal(got[1], want[1])
+    assert np.array_equal(got[0], want[0])
+
+
 def test_kv_commit_without_drafts_only_checks_lengths():
     rng = np.random.default_rng(5)
     cache = rng.integers(0, 256, (2, 4, 6, 16), dtype=np.uint8)
