@@ -161,6 +161,28 @@ def test_tree_invalid_trees_repeatedly_in_clustered_walks(B):
             assert np.array_equal(gpu["path_nodes"], first["path_nodes"])
 
 
+def _random_trees(n=6, seed=55):
+    """Seeded random tree batches: bf16 or f32, V at any 16-byte multiple up to
+    9600, 1-100 nodes below the root (random parents in the last three
+    nodes), B 1-30, one temperature or a per-sequence mix with greedy trees."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for k in range(n):
+        dtype = "bf16" if rng.random() < 0.5 else "f32"
+        V = int(rng.integers(1, 1201)) * (8 if dtype == "bf16" else 4)
+        M = int(rng.integers(1, 101))
+        B = int(rng.integers(1, 31))
+        T = (0.0, 0.7, 1.0) if rng.random() < 0.5 else float(rng.choice([0.5, 1.0, 1.5]))
+        out.append((k, dtype, V, M, B, T))
+    return out
+
+
+@pytest.mark.parametrize("k,dtype,V,M,B,T", _random_trees())
+def test_tree_random_shapes(k, dtype, V, M, B, T):
+    w = synth.make_tree_workload("tree_small", seed=300 + k, device="cuda", B=B, M=M, V=V, dtype=dtype, T=T)
+    _check(w)
+
+
 def test_tree_with_the_most_nodes():
     """1024 nodes per tree (M = 1023, the largest tree the walk holds in shared
     memory), random topologies, against the tree oracle."""
