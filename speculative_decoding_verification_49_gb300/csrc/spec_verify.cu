@@ -195,12 +195,16 @@ __device__ __forceinline__ Online warp_merge(Online o, float cf)
     return o;
 }
 
-// One 16-byte vector of logits into a thread's running normaliser: the vector
-// max (on bf16x2 words for bf16, exact), then, when it exceeds m, the sums are
-// rescaled by exp2((m_old - m) c) and m moves; every element adds exp2((z - m) c),
-// the arguments and the sums computed on f32x2 pairs so that the thread keeps
-// two partial sums (even and odd elements).  While only -inf has been seen the
-// sums stay 0, and a NaN element makes them NaN.
+// K 16-byte vectors of logits (one ring tile's share of a thread) into its
+// running normaliser, without branches: M = max(m, tile max) (the tile max on
+// bf16x2 words for bf16, exact; NaN never the max), the sums are scaled by
+// exp2((m - M) c) when the max moved (else by 1), and every element adds
+// exp2((z - M) c), the arguments and the sums on f32x2 pairs so that the
+// thread keeps two partial sums (even and odd elements).  For bf16 the
+// argument is z c - M c in one rounding (fma).  While only -inf has been seen
+// M is -inf and the arguments are taken against 0 instead, so the sums stay 0;
+// a NaN element makes them NaN.  Elements past the row's end are passed as
+// -inf.
 struct Online2 {
     float m;
     unsigned long long s;  // (even, odd) partial sums
@@ -209,54 +213,71 @@ struct Online2 {
 __device__ __forceinline__ float lo_bf16(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float hi_bf16(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-template <int DT>
-__device__ __forceinline__ void online_add2(Online2 &o, const uint4 v, float cf)
+template <int DT, int K>
+__device__ __forceinline__ void online_add_tile(Online2 &o, const uint4 (&v)[K], float cf)
 {
-    float vmax;
-    unsigned long long z[4];
     constexpr int NP = (DT == SV_BF16) ? 4 : 2;  // f32x2 pairs per vector
+    float vmax;
     if constexpr (DT == SV_BF16) {
-        const uint32_t mx = sv::bmax2(sv::bmax2(v.x, v.y), sv::bmax2(v.z, v.w));
+        uint32_t mx = sv::bmax2(sv::bmax2(v[0].x, v[0].y), sv::bmax2(v[0].z, v[0].w));
+#pragma unroll
+        for (int k = 1; k < K; ++k)
+            mx = sv::bmax2(mx, sv::bmax2(sv::bmax2(v[k].x, v[k].y), sv::bmax2(v[k].z, v[k].w)));
         vmax = fmaxf(lo_bf16(mx), hi_bf16(mx));
-        z[0] = sv::pack2(lo_bf16(v.x), hi_bf16(v.x));
-        z[1] = sv::pack2(lo_bf16(v.y), hi_bf16(v.y));
-        z[2] = sv::pack2(lo_bf16(v.z), hi_bf16(v.z));
-        z[3] = sv::pack2(lo_bf16(v.w), hi_bf16(v.w));
     } else {
-        const float x = __uint_as_float(v.x), y = __uint_as_float(v.y);
-        const float zz = __uint_as_float(v.z), w = __uint_as_float(v.w);
-        vmax = fmaxf(fmaxf(x, y), fmaxf(zz, w));
-        z[0] = sv::pack2(x, y);
-        z[1] = sv::pack2(zz, w);
-    }
-    if (vmax > o.m) {
-        const float r = sv::ex2((o.m - vmax) * cf);
-        o.s = sv::mul2(o.s, sv::pack2(r, r));
-        o.m = vmax;
-    }
-    if (o.m != -INFINITY) {
-        const unsigned long long M = sv::pack2(o.m, o.m), Cf = sv::pack2(cf, cf);
-        unsigned long long e[NP];
+        vmax = -INFINITY;
 #pragma unroll
-        for (int k = 0; k < NP; ++k) {
-            float a0, a1;
-            sv::unpack2(sv::mul2(sv::sub2(z[k], M), Cf), a0, a1);
-            e[k] = sv::pack2(sv::ex2(a0), sv::ex2(a1));
+        for (int k = 0; k < K; ++k)
+            vmax = fmaxf(vmax, fmaxf(fmaxf(__uint_as_float(v[k].x), __uint_as_float(v[k].y)),
+                                     fmaxf(__uint_as_float(v[k].z), __uint_as_float(v[k].w))));
+    }
+    const float M = fmaxf(o.m, vmax);
+    const float r = (vmax > o.m) ? sv::ex2((o.m - vmax) * cf) : 1.0f;
+    const float Ms = (M == -INFINITY) ? 0.0f : M;
+    const unsigned long long Cf = sv::pack2(cf, cf);
+    unsigned long long e[K * NP];
+    if constexpr (DT == SV_BF16) {
+        const float nmc = -(Ms * cf);
+        const unsigned long long Nmc = sv::pack2(nmc, nmc);
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float a0, a1;
+                sv::unpack2(sv::fma2(sv::pack2(lo_bf16(w[q]), hi_bf16(w[q])), Cf, Nmc), a0, a1);
+                e[k * NP + q] = sv::pack2(sv::ex2(a0), sv::ex2(a1));
+            }
         }
-        if constexpr (NP == 4)
-            o.s = sv::add2(o.s, sv::add2(sv::add2(e[0], e[1]), sv::add2(e[2], e[3])));
-        else
-            o.s = sv::add2(o.s, sv::add2(e[0], e[1]));
     } else {
-        // only -inf (or NaN) seen so far: a NaN must still poison the sum
+        const unsigned long long Mp = sv::pack2(Ms, Ms);
 #pragma unroll
-        for (int k = 0; k < NP; ++k) {
-            float a0, a1;
-            sv::unpack2(z[k], a0, a1);
-            if (a0 != a0 || a1 != a1)
-                o.s = sv::pack2(NAN, NAN);
+        for (int k = 0; k < K; ++k) {
+            const unsigned long long z[2] = {sv::pack2(__uint_as_float(v[k].x), __uint_as_float(v[k].y)),
+                                             sv::pack2(__uint_as_float(v[k].z), __uint_as_float(v[k].w))};
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                float a0, a1;
+                sv::unpack2(sv::mul2(sv::sub2(z[q], Mp), Cf), a0, a1);
+                e[k * NP + q] = sv::pack2(sv::ex2(a0), sv::ex2(a1));
+            }
         }
     }
+    // pairwise sum of the K * NP pairs
+#pragma unroll
+    for (int w = 1; w < K * NP; w *= 2)
+#pragma unroll
+        for (int q = 0; q + w < K * NP; q += 2 * w)
+            e[q] = sv::add2(e[q], e[q + w]);
+    o.s = sv::fma2(o.s, sv::pack2(r, r), e[0]);
+    o.m = M;
+}
+
+// Elements past a row's end: -inf in every lane of a vector.
+template <int DT> __device__ __forceinline__ uint4 neg_inf_vec()
+{
+    constexpr uint32_t w = (DT == SV_BF16) ? 0xff80ff80u : 0xff800000u;
+    return make_uint4(w, w, w, w);
 }
 
 __device__ __forceinline__ Online online_fold(const Online2 &o)
@@ -577,20 +598,27 @@ __global__ void __launch_bounds__(kThreads, 4) sv_rows_kernel(const SvParams p)
             for (int t = 0; t < ch.ntiles; ++t) {
                 if (consume_wait(ctl.ring, t)) {
                     const unsigned char *stage = ring + (t % kStages) * (2 * kTileBytes);
+                    if (mode == MODE_GREEDY) {
 #pragma unroll
-                    for (int k = 0; k < kVPT; ++k) {
-                        const int sv_ = k * kSliceVecs + tid;  // vector within the stage
-                        const int vec = t * kTileVecs + sv_;
-                        if (vec < ch.nvec) {
-                            const uint4 vt = reinterpret_cast<const uint4 *>(stage)[sv_];
-                            if (mode == MODE_GREEDY) {
-                                argmax_add2<DT>(ga, vt, (ch.v0 + vec) * VE);
-                            } else {
-                                online_add2<DT>(ot2, vt, cf);
-                                if (has_draft)
-                                    online_add2<DT>(od2, reinterpret_cast<const uint4 *>(stage + kTileBytes)[sv_], cf);
-                            }
+                        for (int k = 0; k < kVPT; ++k) {
+                            const int sv_ = k * kSliceVecs + tid;  // vector within the stage
+                            const int vec = t * kTileVecs + sv_;
+                            if (vec < ch.nvec)
+                                argmax_add2<DT>(ga, reinterpret_cast<const uint4 *>(stage)[sv_], (ch.v0 + vec) * VE);
                         }
+                    } else {
+                        uint4 vt[kVPT], vd[kVPT];
+#pragma unroll
+                        for (int k = 0; k < kVPT; ++k) {
+                            const int sv_ = k * kSliceVecs + tid;
+                            const bool in = t * kTileVecs + sv_ < ch.nvec;
+                            vt[k] = in ? reinterpret_cast<const uint4 *>(stage)[sv_] : neg_inf_vec<DT>();
+                            vd[k] = (in && has_draft) ? reinterpret_cast<const uint4 *>(stage + kTileBytes)[sv_]
+                                                      : neg_inf_vec<DT>();
+                        }
+                        online_add_tile<DT, kVPT>(ot2, vt, cf);
+                        if (has_draft)
+                            online_add_tile<DT, kVPT>(od2, vd, cf);
                     }
                 } else {
                     ctl.ring.abort = 1;
