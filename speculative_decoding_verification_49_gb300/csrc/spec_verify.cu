@@ -121,7 +121,8 @@ template <int S> struct Ring {
 // over DSMEM are written before a cluster barrier and not rewritten after it.
 struct CtlA {
     Ring<kStagesA> ring;
-    float cf;                      // log2(e) / T
+    double cfd;                    // log2(e) / T
+    float cf;                      // the same, rounded to float
     float pm_t, ps_t, pm_d, ps_d;  // sampled partials (target, draft)
     float gv;                      // greedy partial
     int gi, gnan;
@@ -507,6 +508,34 @@ __device__ __forceinline__ Chunk chunk_of(int NV, uint32_t rank, uint32_t C)
     return c;
 }
 
+// The accept test of a draft token x: u < min(1, q(x)/p(x)), evaluated in the
+// log domain.  cfd = log2(e)/T in double; with lq = (zq - mq) cfd and
+// lp = (zp - mp) cfd (both exact differences, one rounding each), the ratio is
+// 2^(lq - lp) * Sp/Sq: the integer part of lq - lp goes to the exponent and the
+// fractional part through ex2, so no double-precision exp or division is on
+// the common path.  Only when an argument nears double underflow are q(x) and
+// p(x) evaluated as the definition does.  p(x) == 0 accepts; q(x) == 0 rejects
+// (u < 0 never holds).
+__device__ __forceinline__ bool accept_test(float zq, float zp, float mq, float Sq, float mp, float Sp, double cfd,
+                                            double u)
+{
+    if (zp == -INFINITY)
+        return true;
+    if (zq == -INFINITY)
+        return false;
+    const double lq = ((double)zq - (double)mq) * cfd;
+    const double lp = ((double)zp - (double)mp) * cfd;
+    if (lq < -1000.0 || lp < -1000.0) {
+        const double qd = exp2(lq) / (double)Sq, pd = exp2(lp) / (double)Sp;
+        return (pd == 0.0) || (u < fmin(1.0, qd / pd));
+    }
+    const double L = lq - lp;
+    const double fl = floor(L);
+    const float frac = (float)(L - fl);
+    const double ratio = ldexp((double)(sv::ex2(frac) * (Sp / Sq)), (int)fl);
+    return u < fmin(1.0, ratio);
+}
+
 // =============================================================================
 // Kernel A: row normalisers and accept decisions, one cluster per position
 // =============================================================================
@@ -559,7 +588,9 @@ __global__ void __launch_bounds__(kThreads, 4) sv_rows_kernel(const SvParams p)
 
     if (tid == 0) {
         ring_init(ctl.ring);
-        ctl.cf = (mode == MODE_SAMPLED) ? (float)(kLog2e / (double)T) : 0.0f;  // log2(e)/T
+        const double cfd = (mode == MODE_SAMPLED) ? kLog2e / (double)T : 0.0;
+        ctl.cfd = cfd;
+        ctl.cf = (float)cfd;
     }
     if constexpr (TREE) {
         // a node's draft row is read only when the node has children
@@ -738,35 +769,14 @@ __global__ void __launch_bounds__(kThreads, 4) sv_rows_kernel(const SvParams p)
                 if (!valid) {
                     errb |= kErrBadValue;
                 } else if (!TREE && i < N && !bad_d) {
-                    // accept iff p(d) == 0 or u < min(1, q(d)/p(d)), with
-                    // q(d)/p(d) = 2^L * Sp/Sq, L = ((zq-mq) - (zp-mp)) log2(e)/T
                     const float zq = ctl.zq_d, zp = ctl.zp_d;
-                    const double ui = (double)ctl.u_i;
-                    const double invT = 1.0 / (double)T;
-                    const double xq = ((double)zq - (double)mq) * invT;
-                    const double xp = ((double)zp - (double)mp) * invT;
-                    bool accept;
-                    if (zp == -INFINITY) {
-                        accept = true;  // p(d) = 0
-                    } else if (zq == -INFINITY) {
-                        accept = false;  // q(d) = 0 and u < 0 never holds
-                    } else if (xq < -700.0 || xp < -700.0) {
-                        // near double underflow: evaluate q(d), p(d) as the definition does
-                        const double qd = exp(xq) / (double)Sq, pd = exp(xp) / (double)Sp;
-                        accept = (pd == 0.0) || (ui < fmin(1.0, qd / pd));
-                    } else {
-                        const double L = (xq - xp) * kLog2e;
-                        const double n = floor(L);
-                        const float frac = (float)(L - n);
-                        const double ratio = ldexp((double)(sv::ex2(frac) * (Sp / Sq)), (int)n);
-                        accept = ui < fmin(1.0, ratio);
-                    }
-                    if (!accept)
+                    const double cfd = ctl.cfd;
+                    if (!accept_test(zq, zp, mq, Sq, mp, Sp, cfd, (double)ctl.u_i))
                         atomicMin(&p.ws_first[b], i);
                     if (p.q_at)
-                        p.q_at[drow] = (float)(exp(xq) / (double)Sq);
+                        p.q_at[drow] = (float)(exp2(((double)zq - (double)mq) * cfd) / (double)Sq);
                     if (p.p_at)
-                        p.p_at[drow] = (float)(exp(xp) / (double)Sp);
+                        p.p_at[drow] = (float)(exp2(((double)zp - (double)mp) * cfd) / (double)Sp);
                 }
                 float *st = p.ws_stats + trow * 4;
                 st[0] = mq;
@@ -1337,12 +1347,14 @@ struct CtlW {
     int kids[kMaxTreeNodes];
     int nkids, accept, sstar;
     float Rt, x1, cf;
+    double cfd;                                 // log2(e) / T in double
     // the tree, fetched once: every decision of the walk reads shared memory
     int par[kMaxTreeNodes], tok[kMaxTreeNodes];
     int amax[kMaxTreeNodes];                    // greedy: the argmax of each node's verifier row
     float u[kMaxTreeNodes];
     float zq[kMaxTreeNodes], zp[kMaxTreeNodes];  // logits at node c's token in its parent's rows
     float st[kMaxTreeNodes * 4];                // (mq, Sq, mp, Sp) of each node
+    unsigned char acc0[kMaxTreeNodes];          // node c's test against q of its parent (no rejection yet)
     int err;                                    // the sequence's error bits, read once
 };
 
@@ -1389,29 +1401,6 @@ __device__ __forceinline__ void tree_vec(const uint4 vt, const uint4 vd, bool us
             sv::unpack2(x, r[2 * e], r[2 * e + 1]);
         }
     }
-}
-
-// Chain test at the first child: u < min(1, q(x)/p(x)) in the log domain, as
-// kernel A decides it.
-__device__ __forceinline__ bool first_child_test(float zq, float zp, float mq, float Sq, float mp, float Sp, float T,
-                                                 double u)
-{
-    if (zp == -INFINITY)
-        return true;  // p(x) = 0
-    if (zq == -INFINITY)
-        return false;  // q(x) = 0 and u < 0 never holds
-    const double invT = 1.0 / (double)T;
-    const double xq = ((double)zq - (double)mq) * invT;
-    const double xp = ((double)zp - (double)mp) * invT;
-    if (xq < -700.0 || xp < -700.0) {
-        const double qd = exp(xq) / (double)Sq, pd = exp(xp) / (double)Sp;
-        return (pd == 0.0) || (u < fmin(1.0, qd / pd));
-    }
-    const double L = (xq - xp) * kLog2e;
-    const double fl = floor(L);
-    const float frac = (float)(L - fl);
-    const double ratio = ldexp((double)(sv::ex2(frac) * (Sp / Sq)), (int)fl);
-    return u < fmin(1.0, ratio);
 }
 
 // Ring tile of the i-th tile this CTA streams in a pass: a cluster of C CTAs
@@ -1587,7 +1576,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1) sv_tree_walk_kernel(const SvP
     const int mode = sequence_mode(p, b, T);
     if (tid == 0) {
         ring_init(w.ring);
-        w.cf = (mode == MODE_SAMPLED) ? (float)(kLog2e / (double)T) : 0.0f;
+        w.cfd = (mode == MODE_SAMPLED) ? kLog2e / (double)T : 0.0;
+        w.cf = (float)w.cfd;
     }
     // The tree's inputs (kernel A does not write them, so before the wait):
     // topology, tokens, uniforms and, for sampled trees, the two logits each
@@ -1615,6 +1605,20 @@ __global__ void __launch_bounds__(kWalkThreads, 1) sv_tree_walk_kernel(const SvP
     if (tid == 0)
         w.err = __ldcg(&p.ws_err[b]);
     __syncthreads();
+    // Every child's test before any rejection at its parent (r_0 = q), in
+    // parallel and off the walk's serial path.
+    if (mode == MODE_SAMPLED) {
+        for (int c = 1 + tid; c <= M; c += kWalkThreads) {
+            const int pc = w.par[c];
+            bool a = false;
+            if (pc >= 0 && pc < c) {
+                const float *s = w.st + pc * 4;
+                a = accept_test(w.zq[c], w.zp[c], s[0], s[1], s[2], s[3], w.cfd, (double)w.u[c]);
+            }
+            w.acc0[c] = a ? 1 : 0;
+        }
+        __syncthreads();
+    }
     const int err = w.err;
     // The leader resets the error word for the next call: every CTA of the
     // cluster has read it first, so all of them take the same branch below (a
@@ -1700,12 +1704,13 @@ __global__ void __launch_bounds__(kWalkThreads, 1) sv_tree_walk_kernel(const SvP
                     const double uc = (double)w.u[ch];
                     bool acc;
                     if (c == 0.0f) {
-                        acc = first_child_test(zq, zp, mq, Sq, mp, Sp, T, uc);
+                        acc = w.acc0[ch] != 0;
                     } else {
                         const float qx = __fmul_rn(sv::ex2(__fmul_rn(__fsub_rn(zq, mq), cf)), isq);
                         const float px = __fmul_rn(sv::ex2(__fmul_rn(__fsub_rn(zp, mp), cf)), isp);
                         const float rk = __fdiv_rn(fmaxf(__fmaf_rn(px, -c, qx), 0.0f), Z);
-                        acc = (zp == -INFINITY) || (px == 0.0f) || (uc < fmin(1.0, (double)rk / (double)px));
+                        // u < min(1, rk/px) with px > 0, compared exactly: u px < rk
+                        acc = (zp == -INFINITY) || (px == 0.0f) || (uc < 1.0 && uc * (double)px < (double)rk);
                     }
                     w.accept = acc ? 1 : 0;
                 }
@@ -1823,7 +1828,8 @@ __global__ void __launch_bounds__(256) sv_fused_decide_kernel(const SvParams p, 
         return;
     }
     const bool sampled = mode == MODE_SAMPLED;
-    const float cf = sampled ? (float)(kLog2e / (double)T) : 0.0f;
+    const double cfd = sampled ? kLog2e / (double)T : 0.0;
+    const float cf = (float)cfd;
     const size_t trow = (size_t)b * (N + 1) + i, drow = (size_t)b * N + i;
     float mq, Sq, mp = -INFINITY, Sp = 0.0f;
     int aq, ap;
@@ -1848,7 +1854,7 @@ __global__ void __launch_bounds__(256) sv_fused_decide_kernel(const SvParams p, 
         }
     } else {
         if (!errb && i < N &&
-            !first_child_test(__ldcg(&f.zgat_t[trow]), __ldcg(&f.zgat_d[drow]), mq, Sq, mp, Sp, T, (double)p.u[trow]))
+            !accept_test(__ldcg(&f.zgat_t[trow]), __ldcg(&f.zgat_d[drow]), mq, Sq, mp, Sp, cfd, (double)p.u[trow]))
             atomicMin(&p.ws_first[b], i);
         float *st = p.ws_stats + trow * 4;
         st[0] = mq;
