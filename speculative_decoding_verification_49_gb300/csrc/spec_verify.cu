@@ -1149,50 +1149,51 @@ struct PickShared {
     float x1;
 };
 
-// Outputs of a sequence that is not sampled -- invalid (-1 everywhere, the
-// status bits) or greedy (the argmax at j) -- and the reset of its slots.
-// Thread 0.
-__device__ void emit_unsampled(const SvParams &p, int b, int j)
+// Outputs of sequence b, written by every thread of the block in parallel:
+// slot k < j the accepted draft, slot j `last`, the rest -1 (every slot -1
+// for an invalid sequence).  my_tok is this thread's draft token
+// (tokens[b][tid] for tid < N), loaded when the kernel started so that no
+// load is left on the way out.  Then thread 0 writes num_accepted, counts the
+// telemetry and returns the sequence's slots to idle (after the barrier: every
+// thread has read them).
+__device__ void emit_outputs(const SvParams &p, int b, int j, int last, bool invalid, int my_tok)
 {
-    const int N = p.N;
+    const int N = p.N, tid = threadIdx.x;
     int32_t *out = p.out + (size_t)b * (N + 1);
-    const int err = __ldcg(&p.ws_err[b]);
-    if (err) {
-        for (int k = 0; k <= N; ++k)
-            out[k] = -1;
-        p.nacc[b] = -1;
-        atomicOr(p.status, err);
-        if (p.hist)
-            atomicAdd(p.hist_invalid, 1ull);
-    } else {
-        for (int k = 0; k < j; ++k)
-            out[k] = p.tokens[(size_t)b * N + k];
-        out[j] = __ldcg(&p.ws_tok[(size_t)b * (N + 1) + j]);
-        for (int k = j + 1; k <= N; ++k)
-            out[k] = -1;
-        p.nacc[b] = j;
-        if (p.hist)
-            atomicAdd(&p.hist[j], 1ull);
+    for (int k = tid; k <= N; k += blockDim.x) {
+        int v = -1;
+        if (!invalid) {
+            if (k < j)
+                v = (k == tid) ? my_tok : p.tokens[(size_t)b * N + k];
+            else if (k == j)
+                v = last;
+        }
+        out[k] = v;
     }
-    p.ws_first[b] = kNoReject;
-    p.ws_err[b] = 0;
+    __syncthreads();
+    if (tid == 0) {
+        if (invalid) {
+            p.nacc[b] = -1;
+            atomicOr(p.status, __ldcg(&p.ws_err[b]));
+            if (p.hist)
+                atomicAdd(p.hist_invalid, 1ull);
+        } else {
+            p.nacc[b] = j;
+            if (p.hist)
+                atomicAdd(&p.hist[j], 1ull);
+        }
+        p.ws_first[b] = kNoReject;
+        p.ws_err[b] = 0;
+    }
 }
 
-// Outputs of a sampled sequence and the reset of its slots.  Thread 0.
-__device__ void emit_sampled(const SvParams &p, int b, int j, int token)
+// A sequence that is not sampled: invalid (its error bits go to the status
+// word) or greedy (the argmax at j).  Every thread of the block.
+__device__ void emit_unsampled(const SvParams &p, int b, int j, int my_tok)
 {
-    const int N = p.N;
-    int32_t *out = p.out + (size_t)b * (N + 1);
-    for (int k = 0; k < j; ++k)
-        out[k] = p.tokens[(size_t)b * N + k];
-    out[j] = token;
-    for (int k = j + 1; k <= N; ++k)
-        out[k] = -1;
-    p.nacc[b] = j;
-    if (p.hist)
-        atomicAdd(&p.hist[j], 1ull);
-    p.ws_first[b] = kNoReject;
-    p.ws_err[b] = 0;
+    const bool invalid = __ldcg(&p.ws_err[b]) != 0;
+    const int last = invalid ? -1 : __ldcg(&p.ws_tok[(size_t)b * (p.N + 1) + j]);
+    emit_outputs(p, b, j, last, invalid, my_tok);
 }
 
 // The token of a sampled sequence, from the slice masses of its residual in
@@ -1260,6 +1261,23 @@ __device__ int draw_token(PickShared &sh, SeqSample &sq, const uint4 *tsrc, cons
     return pick_in_slice<VE>(sh.ps, ss, part, r, sh.x1, NV);
 }
 
+// Slice sl's mass: its 8 warp shares (left by kernel B) added in warp order.
+__device__ __forceinline__ float slice_share_total(const float *shares, int sl)
+{
+    const float4 a = __ldcg(reinterpret_cast<const float4 *>(shares + (size_t)sl * kConsWarps));
+    const float4 c = __ldcg(reinterpret_cast<const float4 *>(shares + (size_t)sl * kConsWarps + 4));
+    float tot = 0.0f;
+    tot = __fadd_rn(tot, a.x);
+    tot = __fadd_rn(tot, a.y);
+    tot = __fadd_rn(tot, a.z);
+    tot = __fadd_rn(tot, a.w);
+    tot = __fadd_rn(tot, c.x);
+    tot = __fadd_rn(tot, c.y);
+    tot = __fadd_rn(tot, c.z);
+    tot = __fadd_rn(tot, c.w);
+    return tot;
+}
+
 template <int DT>
 __global__ void __launch_bounds__(kPickThreads) sv_pick_kernel(const SvParams p)
 {
@@ -1272,6 +1290,10 @@ __global__ void __launch_bounds__(kPickThreads) sv_pick_kernel(const SvParams p)
     const int S = (NV + kSliceVecs - 1) / kSliceVecs;
 
     sv::grid_dependency_wait();  // kernel B's slice masses
+    const int my_tok = (tid < N) ? p.tokens[(size_t)b * N + tid] : -1;  // for the outputs
+    // slice tid's mass, loaded alongside the sequence's statistics (used only if it is sampled)
+    const float *shares = p.ws_slice + (size_t)b * S * kConsWarps;
+    const float my_mass = (tid < S) ? slice_share_total(shares, tid) : 0.0f;
     SeqSample sq{};
     const bool sampled = sequence_sample(p, b, sq, /*with_cf=*/false);  // sq.cf holds T
     if (tid == 0)
@@ -1280,33 +1302,19 @@ __global__ void __launch_bounds__(kPickThreads) sv_pick_kernel(const SvParams p)
     sq.cf = sh.x1;
     const int j = sq.j;
     if (!sampled) {
-        if (tid == 0)
-            emit_unsampled(p, b, j);
+        emit_unsampled(p, b, j, my_tok);
         return;
     }
 
     const uint4 *tsrc = static_cast<const uint4 *>(p.target) + sample_trow(p, b, j) * (size_t)NV;
     const uint4 *dsrc = (j < N) ? static_cast<const uint4 *>(p.draft) + sample_drow(p, b, j) * (size_t)NV : nullptr;
-    const float *shares = p.ws_slice + (size_t)b * S * kConsWarps;
-    for (int sl = tid; sl < S; sl += kPickThreads) {
-        // a slice's mass: its 8 warp shares added in warp order
-        const float4 a = __ldcg(reinterpret_cast<const float4 *>(shares + (size_t)sl * kConsWarps));
-        const float4 c = __ldcg(reinterpret_cast<const float4 *>(shares + (size_t)sl * kConsWarps + 4));
-        float tot = 0.0f;
-        tot = __fadd_rn(tot, a.x);
-        tot = __fadd_rn(tot, a.y);
-        tot = __fadd_rn(tot, a.z);
-        tot = __fadd_rn(tot, a.w);
-        tot = __fadd_rn(tot, c.x);
-        tot = __fadd_rn(tot, c.y);
-        tot = __fadd_rn(tot, c.z);
-        tot = __fadd_rn(tot, c.w);
-        sh.slice[sl] = tot;
-    }
+    if (tid < S)
+        sh.slice[tid] = my_mass;
+    for (int sl = tid + kPickThreads; sl < S; sl += kPickThreads)
+        sh.slice[sl] = slice_share_total(shares, sl);
     __syncthreads();
     const int token = draw_token<DT>(sh, sq, tsrc, dsrc, NV, S);
-    if (tid == 0)
-        emit_sampled(p, b, j, token);
+    emit_outputs(p, b, j, token, false, my_tok);
 }
 
 // =============================================================================
