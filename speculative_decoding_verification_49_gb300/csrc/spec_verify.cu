@@ -407,6 +407,19 @@ __device__ __forceinline__ float warp_incl_scan(float x, int lane)
     return x;
 }
 
+// The warp's total of x, in every lane, by a xor butterfly.  Bit for bit the
+// value warp_incl_scan leaves in lane 31: at step o both add to lane 31's
+// partial the partial of lane 31 - o (= 31 xor o), which in both covers the
+// same o lanes summed by the same tree, so every addition has the same
+// operands in the same order.
+__device__ __forceinline__ float warp_total(float x)
+{
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1)
+        x = __fadd_rn(x, __shfl_xor_sync(0xffffffffu, x, o));
+    return x;
+}
+
 // ---- ring of shared-memory stages fed by TMA bulk copies --------------------
 // Issues ring tiles [t_begin, t_end) of the chunk into ring positions g, g+1,
 // ...  Runs on one lane of the producer warp.
@@ -837,7 +850,7 @@ constexpr int kTileBytesM = kTileVecsM * 16;
 constexpr int kRingBytesM = kStagesM * 2 * kTileBytesM;
 
 // Per-stage description of the tile the producer put there.
-struct TileMeta {
+struct alignas(16) TileMeta {
     int b;         // sequence, or -1: no more tiles
     int slice;     // first slice of the tile within the sequence's row
     int res_mode;
@@ -982,10 +995,10 @@ __global__ void __launch_bounds__(kThreads, 4) sv_mass_kernel(const SvParams p)
                     for (int e = 0; e < VE; ++e)
                         part = __fadd_rn(part, r[e]);
                 }
-                const float incl = warp_incl_scan(part, lane);
+                const float tot = warp_total(part);  // = the inclusive scan's lane 31
                 const int sl = m.slice + k;
                 if (lane == 31 && sl < S)
-                    p.ws_slice[((size_t)m.b * S + sl) * kConsWarps + warp] = incl;  // this warp's share
+                    p.ws_slice[((size_t)m.b * S + sl) * kConsWarps + warp] = tot;  // this warp's share
             }
             consume_release(ctl.ring, g, lane);
         }
@@ -1482,10 +1495,10 @@ __device__ void walk_mass_pass(CtlW &w, unsigned char *ring, uint32_t &g, const 
                         for (int e = 0; e < VE; ++e)
                             part = __fadd_rn(part, r[e]);
                     }
-                    const float incl = warp_incl_scan(part, lane);
+                    const float tot = warp_total(part);  // = the inclusive scan's lane 31
                     const int sl = t * kVPT + q;
                     if (lane == 31 && sl < S)
-                        w.shares[sl * kConsWarps + lw] = incl;
+                        w.shares[sl * kConsWarps + lw] = tot;
                 }
             } else {
                 w.ring.abort = 1;
