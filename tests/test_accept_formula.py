@@ -110,3 +110,32 @@ def test_underflow_branch_follows_the_float64_definition():
                 assert a == b
             else:
                 assert abs(a / b - 1.0) < 1e-3
+
+
+def test_sibling_test_is_exact():
+    """The walk tests a later sibling with u < 1 and u * p(x) < r_k(x), u, p and
+    r_k float32 promoted to double: the product of two float32 values is exact
+    in double, so the comparison equals u < min(1, r_k/p) in rational
+    arithmetic for every input with p > 0, ties included (no quotient is
+    rounded)."""
+    from fractions import Fraction
+    rng = np.random.default_rng(8)
+    cases = 0
+    for k in range(20000):
+        if k % 4 == 0:
+            # exact ties: short mantissas, so u * p is a float32 and r_k = u * p
+            u = np.float32(rng.integers(1, 256) / 256.0)
+            p = np.float32(rng.integers(1, 4096) * 2.0 ** -int(rng.integers(12, 60)))
+            r = np.float32(float(u) * float(p))
+            assert float(r) == float(u) * float(p)
+        else:
+            u = np.float32(rng.random())
+            p = np.float32(10.0 ** rng.uniform(-30, 0))
+            r = np.float32(float(u) * float(p) * (1.0 + rng.uniform(-1e-6, 1e-6)))
+        if p == 0 or not np.isfinite(r):
+            continue
+        exact = Fraction(float(u)) < min(Fraction(1), Fraction(float(r)) / Fraction(float(p)))
+        product = (float(u) < 1.0) and (float(u) * float(p) < float(r))
+        assert product == exact
+        cases += 1
+    assert cases > 19000
