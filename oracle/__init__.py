@@ -84,11 +84,11 @@ class Oracle:
         i = ctypes.c_int
         self.lib.orc_verify.restype = i
         self.lib.orc_verify.argtypes = [P, P, i, P, P, P, i, i, i, i, P, P,
-                                        P, P, P, P, P, P, P, i]
+                                        P, P, P, P, P, P, P, P, i]
         self.lib.orc_softmax_row.restype = i
         self.lib.orc_softmax_row.argtypes = [P, i, i, ctypes.c_double, P, P, P]
         self.lib.orc_tree_verify.restype = i
-        self.lib.orc_tree_verify.argtypes = [P, P, i, P, P, P, P, i, i, i, i, P, P, P, P, P, P, P, P, i]
+        self.lib.orc_tree_verify.argtypes = [P, P, i, P, P, P, P, i, i, i, i, P, P, P, P, P, P, P, P, P, i]
         self.lib.orc_kv_commit.restype = i
         self.lib.orc_kv_commit.argtypes = [P, P, P, P, i, i, i, i, ctypes.c_size_t]
 
@@ -103,7 +103,8 @@ class Oracle:
         Returns a dict of numpy arrays: out_tokens [B, N+1], num_accepted [B],
         seq_status [B] and, with diagnostics, q_at_d / p_at_d [B, N],
         tstats [B, N+1, 2], dstats [B, N, 2], accept_margin [B, N],
-        sample_margin [B].
+        sample_margin [B] and ratio_at_d [B, N] (q(d)/p(d) of every accept
+        test made, +inf where p(d) == 0, NaN where no test was made).
         """
         tgt = _as_logits(target, dtype)
         B, N1, V = tgt.shape
@@ -128,7 +129,8 @@ class Oracle:
             res.update(
                 q_at_d=np.full((B, N), np.nan), p_at_d=np.full((B, N), np.nan),
                 tstats=np.full((B, N + 1, 2), np.nan), dstats=np.full((B, N, 2), np.nan),
-                accept_margin=np.full((B, N), np.nan), sample_margin=np.full((B,), np.nan))
+                accept_margin=np.full((B, N), np.nan), sample_margin=np.full((B,), np.nan),
+                ratio_at_d=np.full((B, N), np.nan))
 
         def ptr(a):
             return None if a is None else a.ctypes.data
@@ -139,7 +141,7 @@ class Oracle:
             ptr(res.get("q_at_d")), ptr(res.get("p_at_d")),
             ptr(res.get("tstats")), ptr(res.get("dstats")),
             ptr(res.get("accept_margin")), ptr(res.get("sample_margin")),
-            ptr(st), int(threads))
+            ptr(st), ptr(res.get("ratio_at_d")), int(threads))
         if rc != 0:
             raise ValueError("oracle rejected its arguments")
         return res
@@ -170,7 +172,9 @@ class Oracle:
 
         Returns out_tokens, path_nodes [B, M+1], num_accepted, seq_status [B]
         and, with diagnostics, tstats / dstats [B, M+1, 2] (visited nodes),
-        accept_margin [B, M+1] (NaN = not tested), sample_margin [B]."""
+        accept_margin [B, M+1] (NaN = not tested), sample_margin [B] and
+        ratio_at [B, M+1] (r(x)/p(x) of each tested child, +inf where
+        p(x) == 0, NaN = not tested)."""
         tgt = _as_logits(target, dtype)
         B, M1, V = tgt.shape
         M = M1 - 1
@@ -188,7 +192,8 @@ class Oracle:
                "num_accepted": np.full((B,), -7, np.int32), "seq_status": np.zeros((B,), np.int32)}
         if diagnostics:
             res.update(tstats=np.full((B, M + 1, 2), np.nan), dstats=np.full((B, M + 1, 2), np.nan),
-                       accept_margin=np.full((B, M + 1), np.nan), sample_margin=np.full((B,), np.nan))
+                       accept_margin=np.full((B, M + 1), np.nan), sample_margin=np.full((B,), np.nan),
+                       ratio_at=np.full((B, M + 1), np.nan))
 
         def ptr(a):
             return None if a is None else a.ctypes.data
@@ -197,7 +202,7 @@ class Oracle:
             ptr(tgt), ptr(drf), DTYPES[dtype], ptr(par), ptr(tok), ptr(u), ptr(T), int(bool(greedy)),
             B, M, V, ptr(res["out_tokens"]), ptr(res["path_nodes"]), ptr(res["num_accepted"]),
             ptr(res.get("tstats")), ptr(res.get("dstats")), ptr(res.get("accept_margin")),
-            ptr(res.get("sample_margin")), ptr(res["seq_status"]), int(threads))
+            ptr(res.get("sample_margin")), ptr(res["seq_status"]), ptr(res.get("ratio_at")), int(threads))
         if rc != 0:
             raise ValueError("oracle rejected its arguments")
         return res

@@ -20,7 +20,8 @@
  *   no rejection (j = N):  sample the bonus token t from q_N
  *   emit d_0..d_{j-1}, t ;  num_accepted = j
  *
- * Readings taken where the pages are silent (each is listed in the design doc):
+ * Readings taken where the pages are silent (none of the four pages fixes
+ * these points; each is the plainest form the rest of the pages support):
  *   - softmax is evaluated in its max-subtracted form, with plain
  *     left-to-right summation in double;
  *   - temperature divides both the target and the draft logits;
@@ -42,10 +43,15 @@
  *     one.
  *
  * Decision margins (reported so that tests can tell rounding-sensitive
- * decisions apart): for an accept test with ratio < 1 the margin is
- * |u_i - ratio|, otherwise +inf; for the final sample it is the distance
- * from u[b,N] to the nearer edge of the chosen token's CDF interval,
- * min(|u - C_{t-1}/R|, |u - C_t/R|).  Greedy decisions have margin +inf.
+ * decisions apart): for an accept test the margin is |u_i - ratio|, the
+ * distance the ratio would have to move to change the decision (below 1 the
+ * threshold is the ratio itself; at or above 1 the threshold is 1 and the
+ * decision changes only once the ratio falls to u_i, which is ratio - u_i
+ * away); a zero draft probability accepts with margin +inf.  For the final
+ * sample it is the distance from u[b,N] to the nearer edge of the chosen
+ * token's CDF interval, min(|u - C_{t-1}/R|, |u - C_t/R|).  Greedy decisions
+ * have margin +inf.  The ratio q_i(d_i)/p_i(d_i) itself is reported too
+ * (+inf where p_i(d_i) == 0).
  */
 #include <float.h>
 #include <math.h>
@@ -187,6 +193,7 @@ typedef struct {
     double *accept_margin; /* [B, N]   NaN where not evaluated */
     double *sample_margin; /* [B] */
     int32_t *seq_status;   /* [B]  0, or ORC_SEQ_* bits */
+    double *ratio_at_d;    /* [B, N]   q_i(d_i)/p_i(d_i) of every test made, NaN elsewhere */
 } orc_args;
 
 static void orc_fill_invalid(const orc_args *a, int b)
@@ -206,6 +213,9 @@ static void orc_verify_sequence(const orc_args *a, int b, double *r)
     if (a->accept_margin)
         for (int i = 0; i < N; i++)
             a->accept_margin[drow0 + i] = NAN;
+    if (a->ratio_at_d)
+        for (int i = 0; i < N; i++)
+            a->ratio_at_d[drow0 + i] = NAN;
     if (a->sample_margin)
         a->sample_margin[b] = NAN;
 
@@ -308,18 +318,19 @@ static void orc_verify_sequence(const orc_args *a, int b, double *r)
         double pd = orc_prob(orc_logit(a->draft, a->dtype, (drow0 + i) * (size_t)V + d), mp[i], Sp[i], T);
         double ui = a->u[trow0 + i];
         int accept;
-        double margin = INFINITY;
+        double margin = INFINITY, ratio = INFINITY;
         if (pd == 0.0) {
             accept = 1;
         } else {
-            double ratio = qd / pd;
+            ratio = qd / pd;
             double thresh = ratio < 1.0 ? ratio : 1.0;
             accept = ui < thresh;
-            if (ratio < 1.0)
-                margin = fabs(ui - ratio);
+            margin = fabs(ui - ratio);
         }
         if (a->accept_margin)
             a->accept_margin[drow0 + i] = margin;
+        if (a->ratio_at_d)
+            a->ratio_at_d[drow0 + i] = ratio;
         if (!accept) {
             j = i;
             break;
@@ -383,7 +394,7 @@ int orc_verify(const void *target, const void *draft, int dtype,
                int32_t *out_tokens, int32_t *num_accepted,
                double *q_at_d, double *p_at_d, double *tstats, double *dstats,
                double *accept_margin, double *sample_margin,
-               int32_t *seq_status, int nthreads)
+               int32_t *seq_status, double *ratio_at_d, int nthreads)
 {
     if (B < 0 || N < 0 || V < 1 || !target || !out_tokens || !num_accepted || !u)
         return -1;
@@ -395,7 +406,7 @@ int orc_verify(const void *target, const void *draft, int dtype,
         return -1;
     orc_args a = {target, draft, dtype, draft_tokens, u, T, greedy, B, N, V,
                   out_tokens, num_accepted, q_at_d, p_at_d, tstats, dstats,
-                  accept_margin, sample_margin, seq_status};
+                  accept_margin, sample_margin, seq_status, ratio_at_d};
     if (nthreads <= 1 || B <= 1) {
         orc_range rg = {&a, 0, B};
         orc_worker(&rg);
@@ -529,6 +540,7 @@ typedef struct {
     int32_t *out_tokens, *path_nodes, *num_accepted;
     double *tstats, *dstats, *accept_margin, *sample_margin;
     int32_t *seq_status;
+    double *ratio_at; /* [B, M+1] r(x)/p_n(x) of every child tested, NaN elsewhere */
 } orc_tree_args;
 
 static void orc_tree_sequence(const orc_tree_args *a, int b, double *r, double *p)
@@ -545,6 +557,8 @@ static void orc_tree_sequence(const orc_tree_args *a, int b, double *r, double *
         path[n] = -1;
         if (a->accept_margin)
             a->accept_margin[row0 + n] = NAN;
+        if (a->ratio_at)
+            a->ratio_at[row0 + n] = NAN;
     }
     if (a->sample_margin)
         a->sample_margin[b] = NAN;
@@ -643,18 +657,19 @@ static void orc_tree_sequence(const orc_tree_args *a, int b, double *r, double *
                 continue;
             const int x = tok[c];
             int accept;
-            double margin = INFINITY;
+            double margin = INFINITY, ratio = INFINITY;
             if (p[x] == 0.0) {
                 accept = 1;
             } else {
-                double ratio = r[x] / p[x];
+                ratio = r[x] / p[x];
                 double thresh = ratio < 1.0 ? ratio : 1.0;
                 accept = a->u[row0 + c] < thresh;
-                if (ratio < 1.0)
-                    margin = fabs(a->u[row0 + c] - ratio);
+                margin = fabs(a->u[row0 + c] - ratio);
             }
             if (a->accept_margin)
                 a->accept_margin[row0 + c] = margin;
+            if (a->ratio_at)
+                a->ratio_at[row0 + c] = ratio;
             if (accept) {
                 next = c;
                 break;
@@ -707,7 +722,7 @@ int orc_tree_verify(const void *target, const void *draft, int dtype, const int3
                     int B, int M, int V, int32_t *out_tokens, int32_t *path_nodes,
                     int32_t *num_accepted, double *tstats, double *dstats,
                     double *accept_margin, double *sample_margin, int32_t *seq_status,
-                    int nthreads)
+                    double *ratio_at, int nthreads)
 {
     if (B < 0 || M < 0 || V < 1 || !target || !parent || !tokens || !u || !out_tokens ||
         !path_nodes || !num_accepted)
@@ -718,7 +733,7 @@ int orc_tree_verify(const void *target, const void *draft, int dtype, const int3
         return -1;
     orc_tree_args a = {target, draft, dtype, parent, tokens, u, T, greedy, B, M, V,
                        out_tokens, path_nodes, num_accepted, tstats, dstats,
-                       accept_margin, sample_margin, seq_status};
+                       accept_margin, sample_margin, seq_status, ratio_at};
     if (nthreads <= 1 || B <= 1) {
         orc_tree_range rg = {&a, 0, B};
         orc_tree_worker(&rg);

@@ -49,7 +49,7 @@ class BlackBox:
             self.zq.ctypes.data, self.zp.ctypes.data, 2, self.tok.ctypes.data,
             self.u.ctypes.data, self.T.ctypes.data, self.greedy, 1, self.N, self.V,
             self.out.ctypes.data, self.acc.ctypes.data, None, None, None, None,
-            None, None, self.st.ctypes.data, 1)
+            None, None, self.st.ctypes.data, None, 1)
         assert rc == 0
         self.calls += 1
         return self.out[0].copy(), int(self.acc[0])

@@ -290,6 +290,40 @@ def pin_inverse_cdf_edges(orc):
         assert r["out_tokens"][0, 1] == want, (uN, r["out_tokens"][0])
 
 
+def pin_accept_margin_is_the_distance_to_a_flip(orc):
+    """The margin of an accept test is how far the ratio q(d)/p(d) would have
+    to move for the decision u < min(1, ratio) to change: |u - ratio| below 1,
+    and ratio - u at or above 1 (the threshold is then 1, and the decision
+    changes only once the ratio has fallen to u).  Exact cases with dyadic
+    probabilities: ratio 1 (identical rows), ratio 2 and ratio 1/2."""
+    eps = 2.0 ** -24
+    zq = np.zeros((1, 2, 4))                              # q = 1/4 each
+    # identical rows: ratio exactly 1; u one float32 step below 1
+    for u0, want in [(1.0 - eps, eps), (0.5, 0.5), (0.0, 1.0)]:
+        r = orc.verify(zq, zq[:, :1].copy(), np.array([[2]], np.int32), np.array([[u0, 0.3]]), np.ones(1),
+                       dtype="f64")
+        assert r["num_accepted"][0] == 1
+        assert r["ratio_at_d"][0, 0] == 1.0
+        assert r["accept_margin"][0, 0] == want, (u0, r["accept_margin"][0, 0])
+    # q(d) = 1/2, p(d) = 1/4: ratio 2, always accepted, margin 2 - u
+    zq2 = np.array([[[0.0, 0.0, NEG_INF, NEG_INF]] * 2])
+    for u0 in (0.0, 0.25, 1.0 - eps):
+        r = orc.verify(zq2, np.zeros((1, 1, 4)), np.array([[0]], np.int32), np.array([[u0, 0.3]]), np.ones(1),
+                       dtype="f64")
+        assert r["num_accepted"][0] == 1 and r["ratio_at_d"][0, 0] == 2.0
+        assert r["accept_margin"][0, 0] == 2.0 - u0
+    # q(d) = 1/4, p(d) = 1/2: ratio 1/2, margin |u - 1/2| on both sides
+    zp = np.array([[[0.0, 0.0, NEG_INF, NEG_INF]]])
+    for u0, acc in [(0.1, 1), (0.75, 0)]:
+        r = orc.verify(zq, zp, np.array([[0]], np.int32), np.array([[u0, 0.3]]), np.ones(1), dtype="f64")
+        assert r["num_accepted"][0] == acc and r["ratio_at_d"][0, 0] == 0.5
+        assert r["accept_margin"][0, 0] == abs(u0 - 0.5)
+    # a zero draft probability: ratio +inf, accepted whatever u, margin +inf
+    zp0 = np.array([[[NEG_INF, 0.0, 0.0, 0.0]]])
+    r = orc.verify(zq, zp0, np.array([[0]], np.int32), np.array([[1.0 - eps, 0.3]]), np.ones(1), dtype="f64")
+    assert r["num_accepted"][0] == 1 and r["ratio_at_d"][0, 0] == np.inf and r["accept_margin"][0, 0] == np.inf
+
+
 def pin_zero_draft_probability_accepts(orc):
     """p_i(d_i) == 0 accepts whatever the uniform (ratio taken as +inf)."""
     zq = np.zeros((1, 2, 3))
@@ -667,8 +701,12 @@ def pin_tree_worked_siblings(orc):
         if toks == (0, 0) and u1 > 5.0 / 9.0:
             assert abs(r["accept_margin"][0][2] - 0.99) < 1e-15  # |u - 0|
             assert r["sample_margin"][0] > 0.3 - 1e-15  # the residual is all on token 1
+        assert abs(r["ratio_at"][0][1] - 5.0 / 9.0) < 1e-15
         if toks == (0, 1) and u1 > 5.0 / 9.0:
-            assert r["accept_margin"][0][2] == np.inf
+            # ratio r(1)/p(1) = 1/0.1 = 10: accepted, and the ratio would have
+            # to fall by 10 - 0.99 to change that
+            assert abs(r["ratio_at"][0][2] - 10.0) < 1e-12
+            assert abs(r["accept_margin"][0][2] - (10.0 - 0.99)) < 1e-12
     # a child whose token the draft gives probability 0 is accepted (ratio +inf),
     # as in the chain verify, whatever its uniform
     zp0 = np.array([[[0.0, -np.inf], [0.0, 0.0], [0.0, 0.0]]])
@@ -768,6 +806,7 @@ ALL_PINS = [
     pin_disjoint_one_hot,
     pin_strict_comparison,
     pin_inverse_cdf_edges,
+    pin_accept_margin_is_the_distance_to_a_flip,
     pin_zero_draft_probability_accepts,
     pin_zero_residual_samples_q,
     pin_accept_when_verifier_not_below,

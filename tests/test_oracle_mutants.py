@@ -14,7 +14,11 @@ import pins
 
 MUTANTS = [
     ("accept test not strict", "accept = ui < thresh;", "accept = ui <= thresh;"),
-    ("ratio inverted", "double ratio = qd / pd;", "double ratio = pd / qd;"),
+    ("accept margin ignores ratios at or above 1", "margin = fabs(ui - ratio);",
+     "margin = ratio < 1.0 ? fabs(ui - ratio) : INFINITY;"),
+    ("accept margin measured against the clamped threshold", "margin = fabs(ui - ratio);",
+     "margin = fabs(ui - thresh);"),
+    ("ratio inverted", "ratio = qd / pd;", "ratio = pd / qd;"),
     ("zero draft probability rejects",
      "if (pd == 0.0) {\n            accept = 1;", "if (pd == 0.0) {\n            accept = 0;"),
     ("residual sign flipped", "double diff = qk - pk;", "double diff = pk - qk;"),
@@ -71,6 +75,8 @@ MUTANTS = [
     ("tree: a node may be its own parent", "if (par[n] < 0 || par[n] >= n)", "if (par[n] < 0 || par[n] > n)"),
     ("tree: leaves' draft rows validated", "if (!greedy && has_child && !(status & ORC_SEQ_BAD_TREE) &&",
      "if (!greedy && !(status & ORC_SEQ_BAD_TREE) &&"),
+    ("tree: margin ignores ratios at or above 1", "margin = fabs(a->u[row0 + c] - ratio);",
+     "margin = ratio < 1.0 ? fabs(a->u[row0 + c] - ratio) : INFINITY;"),
     ("tree: zero draft probability rejects", "if (p[x] == 0.0) {\n                accept = 1;",
      "if (p[x] == 0.0) {\n                accept = 0;"),
     ("tree: greedy takes the last matching child",
