@@ -106,18 +106,25 @@ sv_status spec_verify_run(spec_verify_ctx *ctx, const void *target_logits, const
 /*
  * Same as spec_verify_run, and also writes, for every position, the
  * quantities the decisions were made from (any of these may be NULL):
- *   q_at_draft        float [B, N]: q_i(d_i)
- *   p_at_draft        float [B, N]: p_i(d_i)
+ *   q_at_draft        float [B, N]: q_i(d_i), evaluated in double from the
+ *                     row statistics (a check of the normalisers)
+ *   p_at_draft        float [B, N]: p_i(d_i), likewise
  *   target_row_stats  float [B, N+1, 2]: (max_k z, sum_k exp((z_k - max)/T))
  *   draft_row_stats   float [B, N, 2]:   the same for the draft rows
- * Greedy sequences report (max, NaN) and NaN probabilities.
+ *   ratio_at_draft    float [B, N]: the ratio q_i(d_i)/p_i(d_i) that the
+ *                     accept test of position i compared u[b,i] with (the
+ *                     test is u < min(1, ratio)), rounded to float; +inf
+ *                     where p_i(d_i) == 0
+ * Greedy and invalid sequences report (max, NaN) and NaN probabilities and
+ * ratios.
  */
 sv_status spec_verify_run_debug(spec_verify_ctx *ctx, const void *target_logits,
                                 const void *draft_logits, const int32_t *draft_tokens,
                                 const float *uniforms, const float *temperature, int greedy,
                                 int B, int N, int32_t *out_tokens, int32_t *num_accepted,
                                 void *stream, float *q_at_draft, float *p_at_draft,
-                                float *target_row_stats, float *draft_row_stats);
+                                float *target_row_stats, float *draft_row_stats,
+                                float *ratio_at_draft);
 
 /*
  * Synchronise the device, read and clear the sticky device status of this
@@ -159,6 +166,10 @@ sv_status spec_verify_get_status(spec_verify_ctx *ctx);
  *   num_accepted  int32 [B]       path length (-1 for an invalid sequence)
  *   target_row_stats, draft_row_stats  float [B, M+1, 2] (m, S) per node, or
  *                 NULL; written for every node (draft: nodes with children)
+ *   ratio_at_node float [B, M+1] or NULL: for every child the walk tested,
+ *                 the ratio r(x)/p(x) its uniform was compared with (r the
+ *                 verifier distribution or residual at that point, x its
+ *                 token; +inf where p(x) == 0), NaN for nodes not tested
  * Requires B <= max_B, M <= max_N of the context, M + 1 <= 1024 and
  * V*elt <= 2 MiB.  Invalid sequences (a bad token, a bad parent array, a row
  * with NaN/+inf or only -inf among those read, a bad temperature) emit -1
@@ -170,7 +181,7 @@ sv_status spec_verify_tree_run(spec_verify_ctx *ctx, const void *target_logits, 
                                const int32_t *parent, const int32_t *draft_tokens, const float *uniforms,
                                const float *temperature, int greedy, int B, int M, int32_t *out_tokens,
                                int32_t *path_nodes, int32_t *num_accepted, float *target_row_stats,
-                               float *draft_row_stats, void *stream);
+                               float *draft_row_stats, float *ratio_at_node, void *stream);
 
 /*
  * The LM-head product on the tensor cores: logits[r][v] = sum_k hidden[r][k] *
@@ -201,7 +212,9 @@ sv_status spec_verify_lm_head_logits(const void *hidden, const void *weight, int
  *   target_weight [V, Kt] bf16 (row v: vocabulary entry v)
  *   draft_hidden  [B*N, Kd] bf16, draft_weight [V, Kd] bf16 (NULL when greedy)
  *   the other arguments as spec_verify_run; target_row_stats [B, N+1, 2] and
- *   draft_row_stats [B, N, 2] (m, S) may be NULL.
+ *   draft_row_stats [B, N, 2] (m, S) and ratio_at_draft [B, N] (the ratio
+ *   each accept test compared its uniform with, as in spec_verify_run_debug)
+ *   may be NULL.
  * Requires a context created with SV_F32 (SV_ERR_DTYPE otherwise; its V is the
  * vocabulary size), Kt and Kd multiples of 8, 16-byte aligned inputs.  The
  * first call (and a call with larger Kt or Kd) allocates its scratch
@@ -214,7 +227,8 @@ sv_status spec_verify_run_fused(spec_verify_ctx *ctx, const void *target_hidden,
                                 int Kt, const void *draft_hidden, const void *draft_weight, int Kd,
                                 const int32_t *draft_tokens, const float *uniforms, const float *temperature,
                                 int greedy, int B, int N, int32_t *out_tokens, int32_t *num_accepted,
-                                float *target_row_stats, float *draft_row_stats, void *stream);
+                                float *target_row_stats, float *draft_row_stats, float *ratio_at_draft,
+                                void *stream);
 
 /*
  * Acceptance telemetry (how many drafts each verify accepted, the quantity
@@ -277,12 +291,15 @@ void spec_verify_destroy(spec_verify_ctx *ctx);
  * a plug-in whose host framework owns every allocation, or a decode loop that
  * cannot afford the implicit device synchronisation and possible failure of a
  * cudaMalloc.  This entry point needs no context and allocates nothing: its
- * scratch is a fixed array of about 848 KiB compiled into the library, which
+ * scratch is a fixed array of about 1.33 MiB compiled into the library, which
  * every GPU that loads the library holds until the process exits.
  *
  * Arguments are those of spec_verify_run, with the vocabulary size V and the
  * logit dtype given per call; it runs on the current device.  Limits: B <= 2048,
- * B*(N+1) <= 16384 and B*ceil(V*elt/4 KiB) <= 16384, else SV_ERR_TOO_LARGE and nothing is enqueued.
+ * B*(N+1) <= 16384 and B*ceil(V*elt/4 KiB) <= 32768 (so 256 sequences of
+ * N = 7 drafts over a 151936-token bf16 vocabulary fit, and 1024 sequences of
+ * 128256 float32 logits do not), else SV_ERR_TOO_LARGE and nothing is
+ * enqueued.
  * Invalid sequences are reported through out_tokens = -1 and
  * num_accepted = -1 only (there is no status word to query).
  *

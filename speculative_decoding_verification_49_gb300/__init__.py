@@ -37,7 +37,7 @@ _I = ctypes.c_int
 _SIGNATURES = [
     ("spec_verify_create", _I, [ctypes.POINTER(_P), _I, _I, _I, _I, _I]),
     ("spec_verify_run", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P]),
-    ("spec_verify_run_debug", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
+    ("spec_verify_run_debug", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P]),
     ("spec_verify_get_status", _I, [_P]),
     ("spec_verify_set_cluster_size", _I, [_P, _I]),
     ("spec_verify_cluster_size", _I, [_P, _I, _I]),
@@ -49,10 +49,10 @@ _SIGNATURES = [
     ("spec_verify_profile_read", _I, [_P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double),
                                       ctypes.POINTER(_I)]),
     ("spec_verify_kv_commit", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, ctypes.c_size_t, _P]),
-    ("spec_verify_tree_run", _I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
+    ("spec_verify_tree_run", _I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
     ("spec_verify_lm_head_logits", _I, [_P, _P, _I, _I, _I, _P, _P]),
     ("spec_verify_selftest_timeout", _I, [_I, ctypes.POINTER(_I), _P]),
-    ("spec_verify_run_fused", _I, [_P, _P, _P, _I, _P, _P, _I, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P]),
+    ("spec_verify_run_fused", _I, [_P, _P, _P, _I, _P, _P, _I, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
 ]
 
 SV_KV_OVERFLOW = 1
@@ -105,10 +105,11 @@ def spec_verify_run(ctx, target, draft, draft_tokens, uniforms, temperature, gre
 
 def spec_verify_run_debug(ctx, target, draft, draft_tokens, uniforms, temperature, greedy, B, N,
                           out_tokens, num_accepted, stream, q_at_draft, p_at_draft,
-                          target_row_stats, draft_row_stats) -> int:
+                          target_row_stats, draft_row_stats, ratio_at_draft=None) -> int:
     return load().spec_verify_run_debug(ctx, target, draft, draft_tokens, uniforms, temperature,
                                         int(greedy), B, N, out_tokens, num_accepted, stream,
-                                        q_at_draft, p_at_draft, target_row_stats, draft_row_stats)
+                                        q_at_draft, p_at_draft, target_row_stats, draft_row_stats,
+                                        ratio_at_draft)
 
 
 def spec_verify_get_status(ctx) -> int:
@@ -135,7 +136,7 @@ def spec_verify_run_noalloc(target, draft, draft_tokens, uniforms, temperature, 
                             out_tokens, num_accepted, stream) -> int:
     """Context-free variant that allocates nothing: scratch is a fixed array
     inside the library (B <= 2048, B*(N+1) <= 16384,
-    B*ceil(V*elt/4KiB) <= 16384), shared by every call on
+    B*ceil(V*elt/4KiB) <= 32768), shared by every call on
     the device, so calls must not overlap on the GPU."""
     return load().spec_verify_run_noalloc(target, draft, draft_tokens, uniforms, temperature,
                                           int(greedy), B, N, V, dtype, out_tokens, num_accepted, stream)
@@ -161,11 +162,12 @@ def spec_verify_profile_read(ctx):
 
 
 def spec_verify_tree_run(ctx, target, draft, parent, draft_tokens, uniforms, temperature, greedy, B, M,
-                         out_tokens, path_nodes, num_accepted, target_row_stats, draft_row_stats, stream) -> int:
+                         out_tokens, path_nodes, num_accepted, target_row_stats, draft_row_stats, ratio_at_node,
+                         stream) -> int:
     """Verify B candidate trees of M+1 nodes (device pointers; asynchronous)."""
     return load().spec_verify_tree_run(ctx, target, draft, parent, draft_tokens, uniforms, temperature,
                                        int(greedy), B, M, out_tokens, path_nodes, num_accepted,
-                                       target_row_stats, draft_row_stats, stream)
+                                       target_row_stats, draft_row_stats, ratio_at_node, stream)
 
 
 def spec_verify_kv_commit(scratch, cache, cache_len, num_accepted, status, planes, B, N, max_len, row_bytes,
@@ -273,7 +275,7 @@ class SpecVerify:
         else:
             st = spec_verify_run_debug(*args, _ptr(debug.get("q_at_draft")), _ptr(debug.get("p_at_draft")),
                                        _ptr(debug.get("target_row_stats")),
-                                       _ptr(debug.get("draft_row_stats")))
+                                       _ptr(debug.get("draft_row_stats")), _ptr(debug.get("ratio_at_draft")))
         if st != SV_OK:
             raise SpecVerifyError(st, "spec_verify_run")
         return out_tokens, num_accepted
@@ -282,7 +284,9 @@ class SpecVerify:
                  path_nodes=None, num_accepted=None, stream=None, stats=None):
         """Tree verification; returns (out_tokens [B, M+1], path_nodes [B, M+1],
         num_accepted [B]) without synchronising.  ``stats`` may hold
-        "target_row_stats" / "draft_row_stats" float32 [B, M+1, 2] tensors."""
+        "target_row_stats" / "draft_row_stats" float32 [B, M+1, 2] tensors and
+        "ratio_at_node" float32 [B, M+1] (the ratio each tested child's
+        uniform was compared with)."""
         import torch
         B, M1, V = target.shape
         M = M1 - 1
@@ -307,7 +311,8 @@ class SpecVerify:
         st = spec_verify_tree_run(self.ctx, _ptr(target), _ptr(draft), _ptr(parent), _ptr(tokens), _ptr(uniforms),
                                   _ptr(temperature), greedy, B, M, _ptr(out_tokens), _ptr(path_nodes),
                                   _ptr(num_accepted), _ptr(stats.get("target_row_stats")),
-                                  _ptr(stats.get("draft_row_stats")), s.cuda_stream)
+                                  _ptr(stats.get("draft_row_stats")), _ptr(stats.get("ratio_at_node")),
+                                  s.cuda_stream)
         if st != SV_OK:
             raise SpecVerifyError(st, "spec_verify_tree_run")
         return out_tokens, path_nodes, num_accepted
@@ -336,7 +341,7 @@ class SpecVerify:
             self.ctx, _ptr(target_hidden), _ptr(target_weight), Kt, _ptr(draft_hidden), _ptr(draft_weight), Kd,
             _ptr(draft_tokens), _ptr(uniforms), _ptr(temperature), int(bool(greedy)), B, N, _ptr(out_tokens),
             _ptr(num_accepted), _ptr(stats.get("target_row_stats")), _ptr(stats.get("draft_row_stats")),
-            s.cuda_stream)
+            _ptr(stats.get("ratio_at_draft")), s.cuda_stream)
         if st != SV_OK:
             raise SpecVerifyError(st, "spec_verify_run_fused")
         return out_tokens, num_accepted
@@ -348,6 +353,7 @@ class SpecVerify:
             "p_at_draft": torch.full((B, N), float("nan"), device=device),
             "target_row_stats": torch.full((B, N + 1, 2), float("nan"), device=device),
             "draft_row_stats": torch.full((B, N, 2), float("nan"), device=device),
+            "ratio_at_draft": torch.full((B, N), float("nan"), device=device),
         }
 
 

@@ -80,6 +80,7 @@ struct SvParams {
     float *p_at;
     float *tstats;
     float *dstats;
+    float *ratio_at;  // debug: the ratio each accept test compared u with (NaN where none)
     int *ws_first;    // [max_B] first rejected position, kNoReject if none
     int *ws_err;      // [max_B] error bits of the sequence
     int *ws_tok;      // [max_B*(max_N+1)] greedy argmax of each position
@@ -201,11 +202,18 @@ __device__ __forceinline__ Online warp_merge(Online o, float cf)
 // bf16x2 words for bf16, exact; NaN never the max), the sums are scaled by
 // exp2((m - M) c) when the max moved (else by 1), and every element adds
 // exp2((z - M) c), the arguments and the sums on f32x2 pairs so that the
-// thread keeps two partial sums (even and odd elements).  For bf16 the
-// argument is z c - M c in one rounding (fma).  While only -inf has been seen
-// M is -inf and the arguments are taken against 0 instead, so the sums stay 0;
-// a NaN element makes them NaN.  Elements past the row's end are passed as
-// -inf.
+// thread keeps two partial sums (even and odd elements).  While only -inf has
+// been seen M is -inf and the arguments are taken against 0 instead, so the
+// sums stay 0; a NaN element makes them NaN.  Elements past the row's end are
+// passed as -inf.
+//
+// For bf16 the argument is z c - K in one rounding (fma), K = fl(M c).  That
+// shifts every term by the same e = M c - K (the rounding error of M c, up to
+// half an ulp of M c: about 1e-6 in log2 units at |M c| = 50), so the sum is
+// 2^e times sum exp2((z - M) c).  The rescale when the max moves is
+// exp2(K_old - K_new), which keeps one common shift e of the final M in the
+// whole sum, and online_fold removes it: e = fma(M, c, -K) exactly, and the
+// sum is multiplied by 2^-e = 1 - e ln 2 (to within e^2).
 struct Online2 {
     float m;
     unsigned long long s;  // (even, odd) partial sums
@@ -233,12 +241,19 @@ __device__ __forceinline__ void online_add_tile(Online2 &o, const uint4 (&v)[K],
                                      fmaxf(__uint_as_float(v[k].z), __uint_as_float(v[k].w))));
     }
     const float M = fmaxf(o.m, vmax);
-    const float r = (vmax > o.m) ? sv::ex2((o.m - vmax) * cf) : 1.0f;
     const float Ms = (M == -INFINITY) ? 0.0f : M;
+    // the arguments' shift, new and so far (bf16; -inf before any finite max),
+    // each rounded once and never contracted
+    const float Kn = __fmul_rn(Ms, cf), Ko = __fmul_rn(o.m, cf);
+    float r;
+    if constexpr (DT == SV_BF16)
+        r = (vmax > o.m) ? sv::ex2(__fsub_rn(Ko, Kn)) : 1.0f;
+    else
+        r = (vmax > o.m) ? sv::ex2((o.m - vmax) * cf) : 1.0f;
     const unsigned long long Cf = sv::pack2(cf, cf);
     unsigned long long e[K * NP];
     if constexpr (DT == SV_BF16) {
-        const float nmc = -(Ms * cf);
+        const float nmc = -Kn;
         const unsigned long long Nmc = sv::pack2(nmc, nmc);
 #pragma unroll
         for (int k = 0; k < K; ++k) {
@@ -281,11 +296,21 @@ template <int DT> __device__ __forceinline__ uint4 neg_inf_vec()
     return make_uint4(w, w, w, w);
 }
 
-__device__ __forceinline__ Online online_fold(const Online2 &o)
+// A thread's (m, s) from its running state.  For bf16 the common shift
+// e = m c - fl(m c) of every term is taken out: s * 2^-e = s - s e ln 2.
+template <int DT>
+__device__ __forceinline__ Online online_fold(const Online2 &o, float cf)
 {
     float a, b;
     sv::unpack2(o.s, a, b);
-    return {o.m, a + b};
+    float s = a + b;
+    if constexpr (DT == SV_BF16) {
+        if (isfinite(o.m)) {
+            const float e = fmaf(o.m, cf, -__fmul_rn(o.m, cf));
+            s = fmaf(s, -(e * 0.6931471805599453f), s);
+        }
+    }
+    return {o.m, s};
 }
 
 // ---- greedy: max, lowest index of the max, NaN seen --------------------------
@@ -521,32 +546,44 @@ __device__ __forceinline__ Chunk chunk_of(int NV, uint32_t rank, uint32_t C)
     return c;
 }
 
-// The accept test of a draft token x: u < min(1, q(x)/p(x)), evaluated in the
+// The ratio q(x)/p(x) of the accept test of a draft token x, evaluated in the
 // log domain.  cfd = log2(e)/T in double; with lq = (zq - mq) cfd and
 // lp = (zp - mp) cfd (both exact differences, one rounding each), the ratio is
 // 2^(lq - lp) * Sp/Sq: the integer part of lq - lp goes to the exponent and the
 // fractional part through ex2, so no double-precision exp or division is on
 // the common path.  Only when an argument nears double underflow are q(x) and
-// p(x) evaluated as the definition does.  p(x) == 0 accepts; q(x) == 0 rejects
-// (u < 0 never holds).
-__device__ __forceinline__ bool accept_test(float zq, float zp, float mq, float Sq, float mp, float Sp, double cfd,
-                                            double u)
+// p(x) evaluated as the definition does.  p(x) == 0 gives +inf; q(x) == 0
+// gives 0.
+__device__ __forceinline__ double decision_ratio(float zq, float zp, float mq, float Sq, float mp, float Sp,
+                                                 double cfd)
 {
     if (zp == -INFINITY)
-        return true;
+        return INFINITY;
     if (zq == -INFINITY)
-        return false;
+        return 0.0;
     const double lq = ((double)zq - (double)mq) * cfd;
     const double lp = ((double)zp - (double)mp) * cfd;
     if (lq < -1000.0 || lp < -1000.0) {
         const double qd = exp2(lq) / (double)Sq, pd = exp2(lp) / (double)Sp;
-        return (pd == 0.0) || (u < fmin(1.0, qd / pd));
+        return (pd == 0.0) ? INFINITY : qd / pd;
     }
     const double L = lq - lp;
     const double fl = floor(L);
     const float frac = (float)(L - fl);
-    const double ratio = ldexp((double)(sv::ex2(frac) * (Sp / Sq)), (int)fl);
-    return u < fmin(1.0, ratio);
+    return ldexp((double)(sv::ex2(frac) * (Sp / Sq)), (int)fl);
+}
+
+// u < min(1, ratio); an infinite ratio (p(x) == 0) accepts whatever u is, and
+// a zero ratio (q(x) == 0) never does (u < 0 never holds).
+__device__ __forceinline__ bool accept_by_ratio(double ratio, double u)
+{
+    return ratio == INFINITY || u < fmin(1.0, ratio);
+}
+
+__device__ __forceinline__ bool accept_test(float zq, float zp, float mq, float Sq, float mp, float Sp, double cfd,
+                                            double u)
+{
+    return accept_by_ratio(decision_ratio(zq, zp, mq, Sq, mp, Sp, cfd), u);
 }
 
 // =============================================================================
@@ -679,7 +716,7 @@ __global__ void __launch_bounds__(kThreads, 4) sv_rows_kernel(const SvParams p)
     }
 
     // ---- CTA partial
-    Online ot = online_fold(ot2), od = online_fold(od2);
+    Online ot = online_fold<DT>(ot2, cf), od = online_fold<DT>(od2, cf);
     if (warp < kConsWarps) {
         if (mode == MODE_GREEDY) {
             ga = warp_argmax(ga);
@@ -755,6 +792,8 @@ __global__ void __launch_bounds__(kThreads, 4) sv_rows_kernel(const SvParams p)
                         p.q_at[drow] = NAN;
                     if (p.p_at)
                         p.p_at[drow] = NAN;
+                    if (p.ratio_at)
+                        p.ratio_at[drow] = NAN;
                     if (p.dstats) {
                         p.dstats[drow * 2 + 0] = NAN;
                         p.dstats[drow * 2 + 1] = NAN;
@@ -779,13 +818,18 @@ __global__ void __launch_bounds__(kThreads, 4) sv_rows_kernel(const SvParams p)
                 bool valid = isfinite(mq) && isfinite(Sq) && Sq > 0.0f;
                 if (has_draft)
                     valid = valid && isfinite(mp) && isfinite(Sp) && Sp > 0.0f;
+                if (!TREE && i < N && p.ratio_at)
+                    p.ratio_at[drow] = NAN;
                 if (!valid) {
                     errb |= kErrBadValue;
                 } else if (!TREE && i < N && !bad_d) {
                     const float zq = ctl.zq_d, zp = ctl.zp_d;
                     const double cfd = ctl.cfd;
-                    if (!accept_test(zq, zp, mq, Sq, mp, Sp, cfd, (double)ctl.u_i))
+                    const double ratio = decision_ratio(zq, zp, mq, Sq, mp, Sp, cfd);
+                    if (!accept_by_ratio(ratio, (double)ctl.u_i))
                         atomicMin(&p.ws_first[b], i);
+                    if (p.ratio_at)
+                        p.ratio_at[drow] = (float)ratio;
                     if (p.q_at)
                         p.q_at[drow] = (float)(exp2(((double)zq - (double)mq) * cfd) / (double)Sq);
                     if (p.p_at)
@@ -809,6 +853,8 @@ __global__ void __launch_bounds__(kThreads, 4) sv_rows_kernel(const SvParams p)
             }
         } else if (lane == 0) {
             atomicOr(&p.ws_err[b], kErrBadValue | (bad_d ? kErrBadToken : 0) | (bad_tree ? kErrBadTree : 0));
+            if (!TREE && i < N && p.ratio_at)
+                p.ratio_at[drow] = NAN;
         }
     }
     if (tid == 0 && ctl.ring.abort)
@@ -1036,32 +1082,71 @@ __device__ __forceinline__ float slice_thread_mass(const uint4 *tsrc, const uint
 constexpr int kMaxRowSlices = kMaxCluster * kMaxSlices;  // slices of the longest supported row
 
 // ---- inverse CDF over slice masses (kernel C and the tree walk) ---------------
+// The search above the slice level runs in double: slice masses are the
+// double sums of their eight float warp shares, their prefix and the target
+// x = u * R are double, so where a token falls is resolved to the float
+// precision of one warp's share of one slice, not of the running total (in
+// float, the cumulative mass near R/2 has a resolution of about 3e-8 R, wider
+// than many tail tokens of a 150 000-token vocabulary).
+__device__ __forceinline__ double warp_incl_scan_d(double x, int lane)
+{
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const double y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o)
+            x = __dadd_rn(x, y);
+    }
+    return x;
+}
+
+// Total of a slice: its eight warp shares (float, in warp order) added in double.
+__device__ __forceinline__ double slice_total_d(const float *w8)
+{
+    double t = 0.0;
+#pragma unroll
+    for (int q = 0; q < kConsWarps; ++q)
+        t = __dadd_rn(t, (double)w8[q]);
+    return t;
+}
+
+// Warp 0: the total of S slice masses, by warp-inclusive scans in slice order.
+__device__ __forceinline__ double warp_total_slices(const double *slice, int S, int lane)
+{
+    double carry = 0.0;
+    for (int c0 = 0; c0 < S; c0 += 32) {
+        const int c = c0 + lane;
+        const double m = (c < S) ? slice[c] : 0.0;
+        carry = __shfl_sync(0xffffffffu, __dadd_rn(warp_incl_scan_d(m, lane), carry), 31);
+    }
+    return carry;
+}
+
 // Warp-wide: the first slice whose cumulative mass exceeds x, and x1 = x minus
 // the mass before it; when rounding leaves x at or above the total, the last
 // slice with mass and x1 = INFINITY.  Cumulative sums are warp-inclusive scans
-// in slice order.
-__device__ __forceinline__ void warp_find_slice(const float *slice, int S, float x, int lane, int &cs, float &x1)
+// in slice order (the same additions as warp_total_slices).
+__device__ __forceinline__ void warp_find_slice(const double *slice, int S, double x, int lane, int &cs, double &x1)
 {
     cs = -1;
     x1 = INFINITY;
-    float run = 0.0f;
+    double run = 0.0;
     for (int c0 = 0; c0 < S && cs < 0; c0 += 32) {
         const int c = c0 + lane;
-        const float m = (c < S) ? slice[c] : 0.0f;
-        const float inc = __fadd_rn(warp_incl_scan(m, lane), run);
+        const double m = (c < S) ? slice[c] : 0.0;
+        const double inc = __dadd_rn(warp_incl_scan_d(m, lane), run);
         const unsigned hit = __ballot_sync(0xffffffffu, c < S && x < inc);
         if (hit) {
             const int l = __ffs(hit) - 1;
-            const float prev = __shfl_sync(0xffffffffu, inc, l > 0 ? l - 1 : 0);
+            const double prev = __shfl_sync(0xffffffffu, inc, l > 0 ? l - 1 : 0);
             cs = c0 + l;
-            x1 = __fsub_rn(x, l > 0 ? prev : run);
+            x1 = __dsub_rn(x, l > 0 ? prev : run);
         }
         run = __shfl_sync(0xffffffffu, inc, 31);
     }
     if (cs < 0) {  // rounding: the last slice that has mass
         for (int c0 = ((S - 1) / 32) * 32; c0 >= 0 && cs < 0; c0 -= 32) {
             const int c = c0 + lane;
-            const unsigned m = __ballot_sync(0xffffffffu, c < S && slice[c] > 0.0f);
+            const unsigned m = __ballot_sync(0xffffffffu, c < S && slice[c] > 0.0);
             if (m)
                 cs = c0 + 31 - __clz(m);
         }
@@ -1073,9 +1158,10 @@ __device__ __forceinline__ void warp_find_slice(const float *slice, int S, float
 
 // Element search inside slice ss, whose masses thread t holds for vector t
 // (r[VE] and their sum `part`; threads past the 256 of a slice pass zeros):
-// warp totals in warp order, then the lane, then the element where the
-// cumulative mass first exceeds x1; rounding falls back to the last element
-// with mass.  Every thread of the block calls it (it synchronises the block).
+// warp totals in warp order (a double running sum, as the slice total was
+// formed), then the lane, then the element where the cumulative mass first
+// exceeds x1; rounding falls back to the last element with mass.  Every thread
+// of the block calls it (it synchronises the block).
 struct PickState {
     float incl[kConsThreads];
     int sel, token;
@@ -1083,7 +1169,7 @@ struct PickState {
 };
 
 template <int VE>
-__device__ int pick_in_slice(PickState &ps, int ss, float part, const float *r, float x1, int NV)
+__device__ int pick_in_slice(PickState &ps, int ss, float part, const float *r, double x1, int NV)
 {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const float incl = warp_incl_scan(part, lane);
@@ -1095,11 +1181,11 @@ __device__ int pick_in_slice(PickState &ps, int ss, float part, const float *r, 
         float xl = 0.0f;
         if (x1 != INFINITY) {
             const float wt = (lane < kConsWarps) ? ps.incl[lane * 32 + 31] : 0.0f;
-            float wc = 0.0f, wprev = 0.0f;
+            double wc = 0.0, wprev = 0.0;
             int ws = -1;
             for (int w = 0; w < kConsWarps; ++w) {
-                const float wtw = __shfl_sync(0xffffffffu, wt, w);
-                const float next = __fadd_rn(wc, wtw);
+                const double wtw = (double)__shfl_sync(0xffffffffu, wt, w);
+                const double next = __dadd_rn(wc, wtw);
                 if (ws < 0 && x1 < next) {
                     ws = w;
                     wprev = wc;
@@ -1107,7 +1193,7 @@ __device__ int pick_in_slice(PickState &ps, int ss, float part, const float *r, 
                 wc = next;
             }
             if (ws >= 0) {
-                const float xw = __fsub_rn(x1, wprev);
+                const float xw = __double2float_rn(__dsub_rn(x1, wprev));
                 const float li = ps.incl[ws * 32 + lane];
                 const unsigned ml = __ballot_sync(0xffffffffu, xw < li);
                 if (ml) {
@@ -1155,11 +1241,12 @@ __device__ int pick_in_slice(PickState &ps, int ss, float part, const float *r, 
 }
 
 struct PickShared {
-    float slice[kMaxRowSlices];  // the sequence's slice masses
+    double slice[kMaxRowSlices];  // the sequence's slice masses
     float wtot[kConsWarps];
     PickState ps;
     int sstar, retry;
-    float x1;
+    double x1;
+    float cf;                     // log2(e)/T
 };
 
 // Outputs of sequence b, written by every thread of the block in parallel:
@@ -1231,28 +1318,18 @@ __device__ int draw_token(PickShared &sh, SeqSample &sq, const uint4 *tsrc, cons
                 if (lane == 31 && cons)
                     sh.wtot[warp] = incl;
                 __syncthreads();
-                if (tid == 0) {
-                    float tot = 0.0f;
-                    for (int w = 0; w < kConsWarps; ++w)
-                        tot = __fadd_rn(tot, sh.wtot[w]);
-                    sh.slice[sl] = tot;
-                }
+                if (tid == 0)
+                    sh.slice[sl] = slice_total_d(sh.wtot);
                 __syncthreads();
             }
         }
         if (warp == 0) {
-            float carry = 0.0f;
-            for (int c0 = 0; c0 < S; c0 += 32) {
-                const int c = c0 + lane;
-                const float m = (c < S) ? sh.slice[c] : 0.0f;
-                carry = __shfl_sync(0xffffffffu, __fadd_rn(warp_incl_scan(m, lane), carry), 31);
-            }
-            const float Rt = carry;
+            const double Rt = warp_total_slices(sh.slice, S, lane);
             int cs;
-            float x1;
-            warp_find_slice(sh.slice, S, __fmul_rn(sq.uN, Rt), lane, cs, x1);
+            double x1;
+            warp_find_slice(sh.slice, S, __dmul_rn((double)sq.uN, Rt), lane, cs, x1);
             if (lane == 0) {
-                sh.retry = (Rt == 0.0f && sq.res_mode == RES_DIFF) ? 1 : 0;
+                sh.retry = (Rt == 0.0 && sq.res_mode == RES_DIFF) ? 1 : 0;
                 sh.sstar = cs;
                 sh.x1 = x1;
             }
@@ -1274,21 +1351,13 @@ __device__ int draw_token(PickShared &sh, SeqSample &sq, const uint4 *tsrc, cons
     return pick_in_slice<VE>(sh.ps, ss, part, r, sh.x1, NV);
 }
 
-// Slice sl's mass: its 8 warp shares (left by kernel B) added in warp order.
-__device__ __forceinline__ float slice_share_total(const float *shares, int sl)
+// Slice sl's mass: its 8 warp shares (left by kernel B) added in warp order, in double.
+__device__ __forceinline__ double slice_share_total(const float *shares, int sl)
 {
     const float4 a = __ldcg(reinterpret_cast<const float4 *>(shares + (size_t)sl * kConsWarps));
     const float4 c = __ldcg(reinterpret_cast<const float4 *>(shares + (size_t)sl * kConsWarps + 4));
-    float tot = 0.0f;
-    tot = __fadd_rn(tot, a.x);
-    tot = __fadd_rn(tot, a.y);
-    tot = __fadd_rn(tot, a.z);
-    tot = __fadd_rn(tot, a.w);
-    tot = __fadd_rn(tot, c.x);
-    tot = __fadd_rn(tot, c.y);
-    tot = __fadd_rn(tot, c.z);
-    tot = __fadd_rn(tot, c.w);
-    return tot;
+    const float w8[kConsWarps] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+    return slice_total_d(w8);
 }
 
 template <int DT>
@@ -1306,13 +1375,13 @@ __global__ void __launch_bounds__(kPickThreads) sv_pick_kernel(const SvParams p)
     const int my_tok = (tid < N) ? p.tokens[(size_t)b * N + tid] : -1;  // for the outputs
     // slice tid's mass, loaded alongside the sequence's statistics (used only if it is sampled)
     const float *shares = p.ws_slice + (size_t)b * S * kConsWarps;
-    const float my_mass = (tid < S) ? slice_share_total(shares, tid) : 0.0f;
+    const double my_mass = (tid < S) ? slice_share_total(shares, tid) : 0.0;
     SeqSample sq{};
     const bool sampled = sequence_sample(p, b, sq, /*with_cf=*/false);  // sq.cf holds T
     if (tid == 0)
-        sh.x1 = sampled ? (float)(kLog2e / (double)sq.cf) : 0.0f;  // log2(e)/T, once
+        sh.cf = sampled ? (float)(kLog2e / (double)sq.cf) : 0.0f;  // log2(e)/T, once
     __syncthreads();
-    sq.cf = sh.x1;
+    sq.cf = sh.cf;
     const int j = sq.j;
     if (!sampled) {
         emit_unsampled(p, b, j, my_tok);
@@ -1351,8 +1420,9 @@ __global__ void __launch_bounds__(kPickThreads) sv_pick_kernel(const SvParams p)
 // group that consumes a tile maps thread t to vector t of each slice, exactly
 // as the recomputation does.
 
-constexpr int kStagesW = 8;                 // ring depth of the walk: 128 KiB of row pairs in flight
-constexpr int kWalkGroups = 3;              // consumer groups of 8 warps; group g takes ring tiles g, g+3, ...
+constexpr int kWalkGroups = 3;              // consumer groups of 8 warps; group g takes pass tiles g, g+3, ...
+constexpr int kStagesG = 3;                 // ring stages of one consumer group
+constexpr int kStagesW = kWalkGroups * kStagesG;  // 144 KiB of row pairs in flight
 constexpr int kWalkThreads = kWalkGroups * kConsThreads + 32;  // + the producer warp
 constexpr int kWalkProducerWarp = kWalkGroups * kConsWarps;
 static_assert(kWalkThreads <= 1024, "a CTA holds at most 1024 threads");
@@ -1360,14 +1430,25 @@ constexpr int kMaxTreeNodes = 1024;         // nodes per tree (root included)
 constexpr int kMaxWalkSlices = 512;         // slices of one row: V*elt <= 2 MiB
 constexpr int kMaxWalkCluster = 4;          // CTAs (SMs) that share one tree's passes
 
+// Each consumer group owns kStagesG stages of the ring (group g: stages
+// g*kStagesG .. g*kStagesG + kStagesG - 1), which it alone consumes and the
+// producer alone fills, in the order of the group's own tiles.  So every wait
+// of a group is on the next phase of a stage whose previous phase that group
+// consumed itself: an mbarrier parity wait cannot be satisfied by a phase two
+// steps back.  (With one ring shared by groups that each take every third
+// position, a group would wait on stages whose previous phase belonged to
+// another group and might not have completed yet; the parity of that wait
+// would then match the phase before it, and the wait would return early.)
 struct CtlW {
     Ring<kStagesW> ring;
+    uint32_t gcount[kWalkGroups];               // tiles each group has consumed in earlier passes
     float shares[kMaxWalkSlices * kConsWarps];  // warp shares of every slice of the current pass
-    float slice[kMaxWalkSlices];                // slice masses
+    double slice[kMaxWalkSlices];               // slice masses (double sums of their shares)
     PickState ps;
     int kids[kMaxTreeNodes];
     int nkids, accept, sstar;
-    float Rt, x1, cf;
+    double Rt, x1;                              // total of the pass's slice masses; the pick's remainder
+    float cf;
     double cfd;                                 // log2(e) / T in double
     // the tree, fetched once: every decision of the walk reads shared memory
     int par[kMaxTreeNodes], tok[kMaxTreeNodes];
@@ -1376,6 +1457,7 @@ struct CtlW {
     float zq[kMaxTreeNodes], zp[kMaxTreeNodes];  // logits at node c's token in its parent's rows
     float st[kMaxTreeNodes * 4];                // (mq, Sq, mp, Sp) of each node
     unsigned char acc0[kMaxTreeNodes];          // node c's test against q of its parent (no rejection yet)
+    float ratio0[kMaxTreeNodes];                // that test's ratio (kept for the debug output only)
     int err;                                    // the sequence's error bits, read once
 };
 
@@ -1439,8 +1521,13 @@ __device__ __forceinline__ int walk_tile(int i, uint32_t rank, uint32_t C)
 // barrier every CTA adds up every slice (reading the peers' shares over
 // distributed shared memory) in the same order, so all of them hold the same
 // slice masses and total.
+// Ring stage and phase parity of the k-th tile (counted over every pass) of
+// consumer group grp.
+__device__ __forceinline__ uint32_t walk_stage(int grp, uint32_t k) { return (uint32_t)grp * kStagesG + k % kStagesG; }
+__device__ __forceinline__ uint32_t walk_parity(uint32_t k) { return (k / kStagesG) & 1u; }
+
 template <int DT>
-__device__ void walk_mass_pass(CtlW &w, unsigned char *ring, uint32_t &g, const uint4 *tsrc, const uint4 *dsrc,
+__device__ void walk_mass_pass(CtlW &w, unsigned char *ring, const uint4 *tsrc, const uint4 *dsrc,
                                int NV, float mq, float isq, float mp, float isp, float c, float cf)
 {
     constexpr int VE = Elt<DT>::kPerVec;
@@ -1451,13 +1538,16 @@ __device__ void walk_mass_pass(CtlW &w, unsigned char *ring, uint32_t &g, const 
     int n_own = 0;  // tiles this CTA streams: a prefix i = 0 .. n_own-1 of its sequence
     while (walk_tile(n_own, rank, C) < NT)
         ++n_own;
+    // pass tile i belongs to group i % kWalkGroups, as that group's tile
+    // gcount[grp] + i / kWalkGroups
     if (warp == kWalkProducerWarp) {
         if (lane == 0) {
+            const uint32_t g0 = w.gcount[0], g1 = w.gcount[1], g2 = w.gcount[2];
             for (int i = 0; i < n_own; ++i) {
-                const uint32_t gi = g + (uint32_t)i;
-                const uint32_t st = gi % kStagesW;
-                if (!sv::mbar_wait_bounded(&w.ring.empty[st], ((gi / kStagesW) & 1u) ^ 1u, &w.ring.abort,
-                                           kWaitLimitNs)) {
+                const int grp = i % kWalkGroups;
+                const uint32_t k = (grp == 0 ? g0 : grp == 1 ? g1 : g2) + (uint32_t)(i / kWalkGroups);
+                const uint32_t st = walk_stage(grp, k);
+                if (!sv::mbar_wait_bounded(&w.ring.empty[st], walk_parity(k) ^ 1u, &w.ring.abort, kWaitLimitNs)) {
                     w.ring.abort = 1;
                     break;
                 }
@@ -1469,17 +1559,19 @@ __device__ void walk_mass_pass(CtlW &w, unsigned char *ring, uint32_t &g, const 
                 sv::bulk_g2s(stage, tsrc + (size_t)t * kTileVecs, bytes, &w.ring.full[st]);
                 if (dsrc)
                     sv::bulk_g2s(stage + kTileBytes, dsrc + (size_t)t * kTileVecs, bytes, &w.ring.full[st]);
-                w.ring.last_g[st] = static_cast<int>(gi);
+                w.ring.last_g[st] = static_cast<int>(k);
             }
         }
         __syncwarp();
     } else {
         const int grp = warp / kConsWarps, lt = tid - grp * kConsThreads, lw = warp - grp * kConsWarps;
+        const uint32_t gbase = w.gcount[grp];
         for (int i = grp; i < n_own; i += kWalkGroups) {
-            const uint32_t gt = g + (uint32_t)i;
+            const uint32_t k = gbase + (uint32_t)(i / kWalkGroups);
+            const uint32_t st = walk_stage(grp, k);
             const int t = walk_tile(i, rank, C);
-            if (consume_wait(w.ring, gt)) {
-                const unsigned char *stage = ring + (gt % kStagesW) * (2 * kTileBytes);
+            if (sv::mbar_wait_bounded(&w.ring.full[st], walk_parity(k), &w.ring.abort, kWaitLimitNs)) {
+                const unsigned char *stage = ring + st * (2 * kTileBytes);
 #pragma unroll
                 for (int q = 0; q < kVPT; ++q) {
                     const int sv_ = q * kSliceVecs + lt;
@@ -1503,37 +1595,34 @@ __device__ void walk_mass_pass(CtlW &w, unsigned char *ring, uint32_t &g, const 
             } else {
                 w.ring.abort = 1;
             }
-            consume_release(w.ring, gt, lane);
+            __syncwarp();
+            if (lane == 0)
+                sv::mbar_arrive(&w.ring.empty[st]);
         }
     }
-    g += (uint32_t)n_own;
     if (C > 1)
         sv::cluster_sync();  // every CTA's shares are visible cluster-wide
     else
         __syncthreads();
+    if (tid == 0)  // every thread read the counts before the barrier; the next pass reads them after the last one
+        for (int grp = 0; grp < kWalkGroups; ++grp)
+            w.gcount[grp] += (n_own > grp) ? (uint32_t)((n_own - grp + kWalkGroups - 1) / kWalkGroups) : 0u;
     for (int sl = tid; sl < S; sl += kWalkThreads) {
         const uint32_t owner = (uint32_t)((sl / kVPT) / kWalkGroups) % C;
-        float tot = 0.0f;
-        for (int q = 0; q < kConsWarps; ++q) {
-            const float v = (owner == rank) ? w.shares[sl * kConsWarps + q]
-                                            : sv::ld_dsmem_f32(sv::dsmem_addr(&w.shares[sl * kConsWarps + q], owner));
-            tot = __fadd_rn(tot, v);
-        }
-        w.slice[sl] = tot;
+        float w8[kConsWarps];
+        for (int q = 0; q < kConsWarps; ++q)
+            w8[q] = (owner == rank) ? w.shares[sl * kConsWarps + q]
+                                    : sv::ld_dsmem_f32(sv::dsmem_addr(&w.shares[sl * kConsWarps + q], owner));
+        w.slice[sl] = slice_total_d(w8);
     }
     if (C > 1)
         sv::cluster_sync();  // no peer reads these shares any more: the next pass may overwrite them
     else
         __syncthreads();
     if (warp == 0) {
-        float carry = 0.0f;
-        for (int c0 = 0; c0 < S; c0 += 32) {
-            const int c = c0 + lane;
-            const float m = (c < S) ? w.slice[c] : 0.0f;
-            carry = __shfl_sync(0xffffffffu, __fadd_rn(warp_incl_scan(m, lane), carry), 31);
-        }
+        const double tot = warp_total_slices(w.slice, S, lane);
         if (lane == 0)
-            w.Rt = carry;
+            w.Rt = tot;
     }
     __syncthreads();
 }
@@ -1551,8 +1640,8 @@ __device__ int walk_pick(CtlW &w, const uint4 *tsrc, const uint4 *dsrc, int NV, 
     const int S = (NV + kSliceVecs - 1) / kSliceVecs;
     if (warp == 0) {
         int cs;
-        float x1;
-        warp_find_slice(w.slice, S, __fmul_rn(u, w.Rt), lane, cs, x1);
+        double x1;
+        warp_find_slice(w.slice, S, __dmul_rn((double)u, w.Rt), lane, cs, x1);
         if (lane == 0) {
             w.sstar = cs;
             w.x1 = x1;
@@ -1597,6 +1686,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1) sv_tree_walk_kernel(const SvP
     const int mode = sequence_mode(p, b, T);
     if (tid == 0) {
         ring_init(w.ring);
+        for (int grp = 0; grp < kWalkGroups; ++grp)
+            w.gcount[grp] = 0;
         w.cfd = (mode == MODE_SAMPLED) ? kLog2e / (double)T : 0.0;
         w.cf = (float)w.cfd;
     }
@@ -1616,6 +1707,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1) sv_tree_walk_kernel(const SvP
         }
         w.zq[c] = zq;
         w.zp[c] = zp;
+        if (p.ratio_at && leader)
+            p.ratio_at[row0 + c] = NAN;  // nodes the walk does not test
     }
     sv::grid_dependency_wait();  // kernel A's statistics
     for (int i = tid; i < (M + 1) * 4; i += kWalkThreads)
@@ -1632,11 +1725,14 @@ __global__ void __launch_bounds__(kWalkThreads, 1) sv_tree_walk_kernel(const SvP
         for (int c = 1 + tid; c <= M; c += kWalkThreads) {
             const int pc = w.par[c];
             bool a = false;
+            double ratio = 0.0;
             if (pc >= 0 && pc < c) {
                 const float *s = w.st + pc * 4;
-                a = accept_test(w.zq[c], w.zp[c], s[0], s[1], s[2], s[3], w.cfd, (double)w.u[c]);
+                ratio = decision_ratio(w.zq[c], w.zp[c], s[0], s[1], s[2], s[3], w.cfd);
+                a = accept_by_ratio(ratio, (double)w.u[c]);
             }
             w.acc0[c] = a ? 1 : 0;
+            w.ratio0[c] = (float)ratio;
         }
         __syncthreads();
     }
@@ -1686,7 +1782,6 @@ __global__ void __launch_bounds__(kWalkThreads, 1) sv_tree_walk_kernel(const SvP
     } else {
         const float cf = w.cf;
         const float u0 = w.u[0];
-        uint32_t g = 0;
         int n = 0;
         for (;;) {
             const float *st = w.st + n * 4;
@@ -1724,16 +1819,21 @@ __global__ void __launch_bounds__(kWalkThreads, 1) sv_tree_walk_kernel(const SvP
                     const float zq = w.zq[ch], zp = w.zp[ch];  // at ch's token in n's rows
                     const double uc = (double)w.u[ch];
                     bool acc;
+                    double ratio;  // for the debug output only
                     if (c == 0.0f) {
                         acc = w.acc0[ch] != 0;
+                        ratio = w.ratio0[ch];
                     } else {
                         const float qx = __fmul_rn(sv::ex2(__fmul_rn(__fsub_rn(zq, mq), cf)), isq);
                         const float px = __fmul_rn(sv::ex2(__fmul_rn(__fsub_rn(zp, mp), cf)), isp);
                         const float rk = __fdiv_rn(fmaxf(__fmaf_rn(px, -c, qx), 0.0f), Z);
                         // u < min(1, rk/px) with px > 0, compared exactly: u px < rk
                         acc = (zp == -INFINITY) || (px == 0.0f) || (uc < 1.0 && uc * (double)px < (double)rk);
+                        ratio = (zp == -INFINITY || px == 0.0f) ? (double)INFINITY : (double)rk / (double)px;
                     }
                     w.accept = acc ? 1 : 0;
+                    if (p.ratio_at && leader)
+                        p.ratio_at[row0 + ch] = (float)ratio;
                 }
                 __syncthreads();
                 if (w.accept) {
@@ -1741,8 +1841,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1) sv_tree_walk_kernel(const SvP
                     break;
                 }
                 const float c1 = __fadd_rn(c, Z);
-                walk_mass_pass<DT>(w, ring, g, tsrc, dsrc, NV, mq, isq, mp, isp, c1, cf);
-                const float R = w.Rt;
+                walk_mass_pass<DT>(w, ring, tsrc, dsrc, NV, mq, isq, mp, isp, c1, cf);
+                const float R = (float)w.Rt;
                 if (R > 0.0f) {
                     c = c1;
                     Z = R;
@@ -1765,7 +1865,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) sv_tree_walk_kernel(const SvP
             // the token: from r_k = (q - c p)+ / Z, by inverse CDF over its slice masses
             const uint4 *dk = (c > 0.0f) ? dsrc : nullptr;
             if (!masses_ready)
-                walk_mass_pass<DT>(w, ring, g, tsrc, dk, NV, mq, isq, mp, isp, c, cf);
+                walk_mass_pass<DT>(w, ring, tsrc, dk, NV, mq, isq, mp, isp, c, cf);
             const int t = walk_pick<DT>(w, tsrc, dk, NV, mq, isq, mp, isp, c, cf, u0);
             if (tid == 0 && leader)
                 out[depth] = t;
@@ -1784,7 +1884,15 @@ __global__ void __launch_bounds__(kWalkThreads, 1) sv_tree_walk_kernel(const SvP
     }
     if (tid == 0 && w.ring.abort) {
         atomicOr(p.status, kErrTimeout);
-        ring_drain(w.ring);
+        // never leave with a bulk copy still writing into this CTA's shared
+        // memory: a bounded wait on the last tile issued into each stage
+        for (int st = 0; st < kStagesW; ++st) {
+            const int lk = w.ring.last_g[st];
+            if (lk >= 0) {
+                int never = 0;
+                sv::mbar_wait_bounded(&w.ring.full[st], walk_parity((uint32_t)lk), &never, kWaitLimitNs / 4);
+            }
+        }
     }
 }
 
@@ -1844,8 +1952,11 @@ __global__ void __launch_bounds__(256) sv_fused_decide_kernel(const SvParams p, 
     float T;
     const int mode = sequence_mode(p, b, T);
     if (mode == MODE_INVALID) {
-        if (lane == 0)
+        if (lane == 0) {
             atomicOr(&p.ws_err[b], kErrBadValue);
+            if (p.ratio_at && i < N)
+                p.ratio_at[(size_t)b * N + i] = NAN;
+        }
         return;
     }
     const bool sampled = mode == MODE_SAMPLED;
@@ -1865,6 +1976,8 @@ __global__ void __launch_bounds__(256) sv_fused_decide_kernel(const SvParams p, 
     if (!isfinite(mq) || (sampled && !(isfinite(Sq) && Sq > 0.0f)) ||
         (sampled && i < N && !(isfinite(mp) && isfinite(Sp) && Sp > 0.0f)))
         errb |= kErrBadValue;
+    if (p.ratio_at && i < N)
+        p.ratio_at[drow] = NAN;
     if (!sampled) {
         p.ws_tok[trow] = aq;
         if (i < N && d != aq)
@@ -1874,9 +1987,13 @@ __global__ void __launch_bounds__(256) sv_fused_decide_kernel(const SvParams p, 
             p.tstats[trow * 2 + 1] = NAN;
         }
     } else {
-        if (!errb && i < N &&
-            !accept_test(__ldcg(&f.zgat_t[trow]), __ldcg(&f.zgat_d[drow]), mq, Sq, mp, Sp, cfd, (double)p.u[trow]))
-            atomicMin(&p.ws_first[b], i);
+        if (!errb && i < N) {
+            const double ratio = decision_ratio(__ldcg(&f.zgat_t[trow]), __ldcg(&f.zgat_d[drow]), mq, Sq, mp, Sp, cfd);
+            if (!accept_by_ratio(ratio, (double)p.u[trow]))
+                atomicMin(&p.ws_first[b], i);
+            if (p.ratio_at)
+                p.ratio_at[drow] = (float)ratio;
+        }
         float *st = p.ws_stats + trow * 4;
         st[0] = mq;
         st[1] = Sq;
@@ -2115,7 +2232,8 @@ int cluster_a(const spec_verify_ctx *c, int B, int N, bool tree = false)
 
 sv_status run_impl(spec_verify_ctx *ctx, const void *target, const void *draft, const int32_t *tokens,
                    const float *u, const float *T, int greedy, int B, int N, int32_t *out,
-                   int32_t *nacc, void *stream, float *q_at, float *p_at, float *tstats, float *dstats)
+                   int32_t *nacc, void *stream, float *q_at, float *p_at, float *tstats, float *dstats,
+                   float *ratio_at)
 {
     if (!ctx)
         return SV_ERR_INVALID_ARG;
@@ -2159,6 +2277,7 @@ sv_status run_impl(spec_verify_ctx *ctx, const void *target, const void *draft, 
     prm.p_at = p_at;
     prm.tstats = tstats;
     prm.dstats = dstats;
+    prm.ratio_at = ratio_at;
     prm.ws_first = ctx->ws_first;
     prm.ws_err = ctx->ws_err;
     prm.ws_tok = ctx->ws_tok;
@@ -2224,7 +2343,8 @@ sv_status run_impl(spec_verify_ctx *ctx, const void *target, const void *draft, 
 
 sv_status tree_run_impl(spec_verify_ctx *ctx, const void *target, const void *draft, const int32_t *parent,
                         const int32_t *tokens, const float *u, const float *T, int greedy, int B, int M,
-                        int32_t *out, int32_t *path, int32_t *nacc, float *tstats, float *dstats, void *stream)
+                        int32_t *out, int32_t *path, int32_t *nacc, float *tstats, float *dstats, float *ratio_at,
+                        void *stream)
 {
     if (!ctx)
         return SV_ERR_INVALID_ARG;
@@ -2262,6 +2382,7 @@ sv_status tree_run_impl(spec_verify_ctx *ctx, const void *target, const void *dr
     prm.nacc = nacc;
     prm.tstats = tstats;
     prm.dstats = dstats;
+    prm.ratio_at = ratio_at;
     prm.ws_first = ctx->ws_first;
     prm.ws_err = ctx->ws_err;
     prm.ws_tok = ctx->ws_tok;
@@ -2351,7 +2472,7 @@ sv_status fused_scratch(spec_verify_ctx *ctx, int Kt, int Kd)
 
 sv_status fused_run_impl(spec_verify_ctx *ctx, const void *ht, const void *wt, int Kt, const void *hd, const void *wd,
                          int Kd, const int32_t *tokens, const float *u, const float *T, int greedy, int B, int N,
-                         int32_t *out, int32_t *nacc, float *tstats, float *dstats, void *stream)
+                         int32_t *out, int32_t *nacc, float *tstats, float *dstats, float *ratio_at, void *stream)
 {
     if (!ctx)
         return SV_ERR_INVALID_ARG;
@@ -2399,6 +2520,7 @@ sv_status fused_run_impl(spec_verify_ctx *ctx, const void *ht, const void *wt, i
     prm.nacc = nacc;
     prm.tstats = tstats;
     prm.dstats = dstats;
+    prm.ratio_at = ratio_at;
     prm.ws_first = ctx->ws_first;
     prm.ws_err = ctx->ws_err;
     prm.ws_tok = ctx->ws_tok;
@@ -2533,39 +2655,41 @@ sv_status spec_verify_run(spec_verify_ctx *ctx, const void *target_logits, const
                           int greedy, int B, int N, int32_t *out_tokens, int32_t *num_accepted, void *stream)
 {
     return run_impl(ctx, target_logits, draft_logits, draft_tokens, uniforms, temperature, greedy, B, N,
-                    out_tokens, num_accepted, stream, nullptr, nullptr, nullptr, nullptr);
+                    out_tokens, num_accepted, stream, nullptr, nullptr, nullptr, nullptr, nullptr);
 }
 
 sv_status spec_verify_run_debug(spec_verify_ctx *ctx, const void *target_logits, const void *draft_logits,
                                 const int32_t *draft_tokens, const float *uniforms, const float *temperature,
                                 int greedy, int B, int N, int32_t *out_tokens, int32_t *num_accepted,
                                 void *stream, float *q_at_draft, float *p_at_draft, float *target_row_stats,
-                                float *draft_row_stats)
+                                float *draft_row_stats, float *ratio_at_draft)
 {
     return run_impl(ctx, target_logits, draft_logits, draft_tokens, uniforms, temperature, greedy, B, N,
                     out_tokens, num_accepted, stream, q_at_draft, p_at_draft, target_row_stats,
-                    draft_row_stats);
+                    draft_row_stats, ratio_at_draft);
 }
 
 sv_status spec_verify_tree_run(spec_verify_ctx *ctx, const void *target_logits, const void *draft_logits,
                                const int32_t *parent, const int32_t *draft_tokens, const float *uniforms,
                                const float *temperature, int greedy, int B, int M, int32_t *out_tokens,
                                int32_t *path_nodes, int32_t *num_accepted, float *target_row_stats,
-                               float *draft_row_stats, void *stream)
+                               float *draft_row_stats, float *ratio_at_node, void *stream)
 {
     return tree_run_impl(ctx, target_logits, draft_logits, parent, draft_tokens, uniforms, temperature, greedy, B,
-                         M, out_tokens, path_nodes, num_accepted, target_row_stats, draft_row_stats, stream);
+                         M, out_tokens, path_nodes, num_accepted, target_row_stats, draft_row_stats, ratio_at_node,
+                         stream);
 }
 
 sv_status spec_verify_run_fused(spec_verify_ctx *ctx, const void *target_hidden, const void *target_weight,
                                 int Kt, const void *draft_hidden, const void *draft_weight, int Kd,
                                 const int32_t *draft_tokens, const float *uniforms, const float *temperature,
                                 int greedy, int B, int N, int32_t *out_tokens, int32_t *num_accepted,
-                                float *target_row_stats, float *draft_row_stats, void *stream)
+                                float *target_row_stats, float *draft_row_stats, float *ratio_at_draft,
+                                void *stream)
 {
     return fused_run_impl(ctx, target_hidden, target_weight, Kt, draft_hidden, draft_weight, Kd, draft_tokens,
                           uniforms, temperature, greedy, B, N, out_tokens, num_accepted, target_row_stats,
-                          draft_row_stats, stream);
+                          draft_row_stats, ratio_at_draft, stream);
 }
 
 sv_status spec_verify_selftest_timeout(int limit_us, int *gave_up, void *stream)
@@ -2678,7 +2802,7 @@ const char *spec_verify_error_string(sv_status s)
     case SV_ERR_BAD_TREE: return "SV_ERR_BAD_TREE: a parent array broke parent[0] = -1, 0 <= parent[n] < n";
     case SV_ERR_TOO_LARGE:
         return "SV_ERR_TOO_LARGE: batch exceeds the fixed scratch of spec_verify_run_noalloc "
-               "(B <= 2048, B*(N+1) <= 16384, B*ceil(V*elt/4KiB) <= 16384)";
+               "(B <= 2048, B*(N+1) <= 16384, B*ceil(V*elt/4KiB) <= 32768)";
     }
     return "unknown sv_status";
 }
@@ -2774,10 +2898,12 @@ void spec_verify_destroy(spec_verify_ctx *ctx)
 // entry point for callers that cannot allocate device memory
 // =============================================================================
 //
-// spec_verify_run_noalloc runs the same kernel as spec_verify_run, but its
-// scratch (per-sequence tickets, first-rejection slots, error flags, sampled
-// tokens and a status word) lives in the file-scope array below instead of a
-// context workspace.  The array is part of the module image: every GPU that
+// spec_verify_run_noalloc runs the same kernels as spec_verify_run, but its
+// scratch lives in the file-scope array below instead of a context
+// workspace: per sequence the first-rejection slot and the error bits, per
+// verified position the greedy argmax and the row statistics (mq, Sq, mp,
+// Sp), per 4 KiB slice of a sampled row pair the eight warp shares of its
+// residual mass, and one status word.  The array is part of the module image: every GPU that
 // loads this library holds it until the process exits, and nothing is ever
 // allocated for it.  Host code only sees a stand-in symbol for it, so the
 // device address is looked up once per device with cudaGetSymbolAddress.
@@ -2785,10 +2911,12 @@ void spec_verify_destroy(spec_verify_ctx *ctx)
 namespace {
 constexpr int kNoAllocMaxB = 2048;        // sequences per call
 constexpr int kNoAllocMaxUnits = 16384;   // B*(N+1) verified positions per call
-constexpr int kNoAllocMaxSlices = 16384;  // B*ceil(V*elt/4 KiB) residual slices per call
+constexpr int kNoAllocMaxSlices = 32768;  // B*ceil(V*elt/4 KiB) residual slices per call
 constexpr int kNoAllocSliceOff = 2 * kNoAllocMaxB + 5 * kNoAllocMaxUnits;  // a multiple of 64 ints
 static_assert(kNoAllocSliceOff % 64 == 0, "slice shares must start on a 256-byte boundary");
-constexpr int kNoAllocInts = kNoAllocSliceOff + 8 * kNoAllocMaxSlices + 1;  // about 848 KiB
+constexpr int kNoAllocInts = kNoAllocSliceOff + 8 * kNoAllocMaxSlices + 1;  // about 1.33 MiB
+// the 256-sequence Qwen-vocabulary batch (V = 151936 bf16: 75 slices a row) fits
+static_assert(256 * 75 <= kNoAllocMaxSlices, "the scratch holds a 256 x 151936 bf16 batch");
 constexpr int kNoAllocMaxDevices = 64;
 } // namespace
 
@@ -2903,5 +3031,5 @@ extern "C" sv_status spec_verify_run_noalloc(const void *target_logits, const vo
         return SV_ERR_CUDA;
     }
     return run_impl(&c, target_logits, draft_logits, draft_tokens, uniforms, temperature, greedy, B, N,
-                    out_tokens, num_accepted, stream, nullptr, nullptr, nullptr, nullptr);
+                    out_tokens, num_accepted, stream, nullptr, nullptr, nullptr, nullptr, nullptr);
 }

@@ -17,9 +17,10 @@ int use_every_entry_point(void *stream)
     double ms_rows = 0.0, ms_sample = 0.0;
     int runs = 0;
     st = spec_verify_run(ctx, cv, cv, i32, f32, f32, 0, 256, 7, i32, i32, stream);
-    st = spec_verify_run_debug(ctx, cv, cv, i32, f32, f32, 0, 256, 7, i32, i32, stream, f32, f32, f32, f32);
-    st = spec_verify_tree_run(ctx, cv, cv, i32, i32, f32, f32, 0, 64, 15, i32, i32, i32, f32, f32, stream);
-    st = spec_verify_run_fused(ctx, cv, cv, 3584, cv, cv, 896, i32, f32, f32, 0, 256, 7, i32, i32, f32, f32, stream);
+    st = spec_verify_run_debug(ctx, cv, cv, i32, f32, f32, 0, 256, 7, i32, i32, stream, f32, f32, f32, f32, f32);
+    st = spec_verify_tree_run(ctx, cv, cv, i32, i32, f32, f32, 0, 64, 15, i32, i32, i32, f32, f32, f32, stream);
+    st = spec_verify_run_fused(ctx, cv, cv, 3584, cv, cv, 896, i32, f32, f32, 0, 256, 7, i32, i32, f32, f32, f32,
+                               stream);
     st = spec_verify_lm_head_logits(cv, cv, 256, 151936, 3584, f32, stream);
     st = spec_verify_kv_commit(cv, (void *)f32, i32, i32, i32, 56, 256, 7, 2048, (size_t)1024, stream);
     st = spec_verify_acceptance_counts(ctx, counts, 9, 1);

@@ -68,13 +68,13 @@ def test_host_validation_without_gpu(lib):
 
 def test_tree_run_host_validation_without_gpu(lib):
     tr = sv.spec_verify_tree_run
-    args = (16, 16, 16, 16, 16, 16, 0, 2, 3, 16, 16, 16, None, None, None)
+    args = (16, 16, 16, 16, 16, 16, 0, 2, 3, 16, 16, 16, None, None, None, None)
     assert tr(None, *args) == sv.SV_ERR_INVALID_ARG  # no context: rejected before any CUDA call
 
 
 def test_fused_and_lm_head_host_validation_without_gpu(lib):
     fr = lib.spec_verify_run_fused
-    args = (16, 16, 64, 16, 16, 64, 16, 16, 16, 0, 2, 3, 16, 16, None, None, None)
+    args = (16, 16, 64, 16, 16, 64, 16, 16, 16, 0, 2, 3, 16, 16, None, None, None, None)
     assert fr(None, *args) == sv.SV_ERR_INVALID_ARG  # no context
     lm = lib.spec_verify_lm_head_logits
     assert lm(16, 16, 4, 8, 12, 16, None) == sv.SV_ERR_INVALID_ARG   # K not a multiple of 8

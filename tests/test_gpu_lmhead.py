@@ -4,6 +4,7 @@ import pytest
 import torch
 
 import oracle
+import parity
 import speculative_decoding_verification_49_gb300 as sv
 
 pytestmark = pytest.mark.gpu
@@ -24,8 +25,28 @@ def _case(M, V, K, seed):
 
 
 def _bound(h, w):
-    # f32 accumulation of K products: |error| <= K * 2^-23 * sum_k |h_k w_k| (generous)
-    return (h.abs().double() @ w.abs().double().T).numpy() * h.shape[1] * 2.0 ** -23 + 1e-30
+    """Bound on the float32 product's error: LOGIT_ERR_FACTOR (2) times the
+    size of a float32 sum of K products with random signs, sqrt(K) 2^-24
+    sum_k |h_k w_k| (every case below measures at most 0.31 of that size).
+    A product that dropped one term of its sum misses it by |h_k w_k|, far
+    above the bound (checked on each case)."""
+    return parity.LOGIT_ERR_FACTOR * parity.lm_head_error_scale(h, w) + 1e-30
+
+
+def _report(err, h, w):
+    """Largest error over the random-sign scale sqrt(K) 2^-24 sum_k |h_k w_k|."""
+    r = float((err / (parity.lm_head_error_scale(h, w) + 1e-300)).max())
+    print(f"lm-head error over sqrt(K) 2^-24 sum|hw|: {r:.3g} (K = {h.shape[1]})")
+    return r
+
+
+def _dropped_term_fails(want, h, w, bound):
+    """The float64 product without its middle term lies outside the bound for
+    most outputs (over 80 %): the bound can tell a missing product term apart."""
+    k = h.shape[1] // 2
+    term = np.outer(h[:, k].double().numpy(), w[:, k].double().numpy())
+    off = np.abs(term) > bound
+    assert off.mean() > 0.8, off.mean()
 
 
 @pytest.mark.parametrize("M,V,K", [(128, 256, 64), (300, 1000, 72), (1, 17, 8), (257, 2304, 896),
@@ -35,7 +56,10 @@ def test_lm_head_logits_match_the_definition(M, V, K):
     got = sv.lm_head_logits(h.cuda(), w.cuda()).cpu().double().numpy()
     want = oracle.lm_head_logits(h, w)
     err = np.abs(got - want)
-    assert (err <= _bound(h, w)).all(), float((err / _bound(h, w)).max())
+    _report(err, h, w)
+    bound = _bound(h, w)
+    assert (err <= bound).all(), float((err / bound).max())
+    _dropped_term_fails(want, h, w, bound)
 
 
 def test_lm_head_logits_sampled_at_vocabulary_size():
@@ -48,7 +72,10 @@ def test_lm_head_logits_sampled_at_vocabulary_size():
     rows = torch.tensor([0, 1, 63, 64, 127, 128, 200, 255, 5, 77, 99, 150, 180, 222, 240, 254])
     want = oracle.lm_head_logits(h[rows].cpu(), w.cpu())
     err = np.abs(got[rows.cuda()].cpu().double().numpy() - want)
-    assert (err <= _bound(h[rows].cpu(), w.cpu())).all()
+    _report(err, h[rows].cpu(), w.cpu())
+    bound = _bound(h[rows].cpu(), w.cpu())
+    assert (err <= bound).all()
+    _dropped_term_fails(want, h[rows].cpu(), w.cpu(), bound)
 
 
 def test_lm_head_logits_into_an_unaligned_output():
@@ -80,4 +107,7 @@ def test_lm_head_logits_long_hidden_size():
     rows = torch.tensor([0, 1, 31, 32, 127, 128, 255, 256, 300, 383, 384, 400, 450, 500, 510, 511])
     want = oracle.lm_head_logits(h[rows].cpu(), w.cpu())
     err = np.abs(got[rows.cuda()].cpu().double().numpy() - want)
-    assert (err <= _bound(h[rows].cpu(), w.cpu())).all()
+    _report(err, h[rows].cpu(), w.cpu())
+    bound = _bound(h[rows].cpu(), w.cpu())
+    assert (err <= bound).all()
+    _dropped_term_fails(want, h[rows].cpu(), w.cpu(), bound)

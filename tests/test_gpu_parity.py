@@ -1,8 +1,9 @@
 """CUDA path against the float64 oracle (needs a GB300).
 
 Every call goes through the C ABI (ctypes binding of libspecverify.so).  The
-five workloads run at full size; where the oracle would take too long, it
-checks a sample of the sequences of the full-size launch.
+five workloads run at full size, and the oracle checks every sequence of
+every launch, including the full headline and stress launches the benchmark
+times.
 """
 import os
 
@@ -36,7 +37,9 @@ def _check(w, seqs=None, ctx=None, greedy=None):
     orc = parity.run_oracle(w, seqs=seqs, threads=THREADS, greedy=greedy)
     rep = parity.compare(w, gpu, orc, check_probs=not (greedy or w.greedy))
     print(w.name, rep)
-    assert rep["band_decisions"] <= max(1, 1e-4 * rep["decisions"]) or rep["band_mismatch"] == 0
+    # sequences that differ (all inside the band): at most one a launch here;
+    # their rate over many launches is checked below
+    assert rep["band_mismatch"] <= max(1, 1e-4 * rep["decisions"])
     assert ctx.status() == sv.SV_OK
     return rep
 
@@ -77,15 +80,60 @@ def test_parity_random_shapes(k, dtype, V, N, B, T):
     _check(w)
 
 
-@pytest.mark.parametrize("name,nsample", [("headline", 24), ("stress", 24)])
-def test_parity_full_size_sampled(name, nsample):
-    """The full-size launch the benchmark times; the oracle checks a spread
-    of its sequences one by one."""
+@pytest.mark.parametrize("name", ["headline", "stress"])
+def test_parity_full_size_every_sequence(name):
+    """The full-size launch the benchmark times (headline: 256 sequences x 15
+    rows of 151936 bf16 logits; stress: 1024 x 7 rows of 128256 f32 logits),
+    every sequence checked against the oracle."""
     w = synth.make_workload(name, seed=0, device="cuda")
-    rng = np.random.default_rng(1)
-    seqs = np.sort(rng.choice(w.B, size=nsample, replace=False))
-    seqs[0], seqs[-1] = 0, w.B - 1
-    _check(w, seqs=seqs)
+    rep = _check(w)
+    assert rep["sequences"] == w.B
+
+
+def test_band_rate_over_fifty_headline_launches():
+    """Every sequence of 50 full-size headline launches (seeds 100-149, about
+    43 000 accept and sampling decisions) against the oracle.  Outside the
+    1e-6 margin band every token and count matches, and every decision ratio
+    lies within the band of the oracle's.  The sequences that differ (all
+    inside the band) must be fewer than 1e-4 of the decisions.  The share of
+    decisions inside the band is reported, split into accept tests and final
+    samples."""
+    ctx = sv.SpecVerify(256, 7, 151936, "bf16")
+    tot = {"decisions": 0, "band_decisions": 0, "band_mismatch": 0, "sequences": 0, "exact": 0}
+    acc_dec = acc_band = smp_dec = smp_band = 0
+    worst = 0.0
+    details = []
+    for seed in range(100, 150):
+        w = synth.make_workload("headline", seed=seed, device="cuda")
+        gpu = parity.run_gpu(ctx, w)
+        orc = parity.run_oracle(w, threads=THREADS)
+        rep = parity.compare(w, gpu, orc)
+        assert ctx.status() == sv.SV_OK
+        for k in tot:
+            tot[k] += rep[k]
+        am, sm = orc["accept_margin"], orc["sample_margin"]
+        acc_dec += int((~np.isnan(am)).sum())
+        acc_band += int((am < parity.BAND).sum())
+        smp_dec += int((~np.isnan(sm)).sum())
+        smp_band += int((sm < parity.BAND).sum())
+        worst = max(worst, rep["decision_ratio_err_max"])
+        diff = np.nonzero(((gpu["out_tokens"] != orc["out_tokens"]).any(axis=1))
+                          | (gpu["num_accepted"] != orc["num_accepted"]))[0]
+        for b in diff:
+            details.append((seed, int(b), int(orc["num_accepted"][b]), int(gpu["num_accepted"][b]),
+                            float(np.nanmin(am[b], initial=np.inf)), float(sm[b])))
+        del w, gpu, orc
+        torch.cuda.empty_cache()
+    print(f"50 headline launches: {tot}; accept tests {acc_dec} ({acc_band} in the band), "
+          f"samples {smp_dec} ({smp_band} in the band); band rate {tot['band_decisions'] / tot['decisions']:.3g}; "
+          f"differing sequences {tot['band_mismatch']} = {tot['band_mismatch'] / tot['decisions']:.3g} of decisions; "
+          f"decision ratio error max {worst:.3g}")
+    for d in details:
+        print("differs (seed, b, j oracle, j gpu, min accept margin, sample margin):", d)
+    assert tot["decisions"] >= 40000
+    assert worst <= parity.BAND
+    assert acc_band < 1e-4 * acc_dec
+    assert tot["band_mismatch"] < 1e-4 * tot["decisions"]
 
 
 def test_parity_all_greedy_without_draft_logits():
