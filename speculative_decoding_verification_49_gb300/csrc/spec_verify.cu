@@ -580,11 +580,6 @@ __device__ __forceinline__ bool accept_by_ratio(double ratio, double u)
     return ratio == INFINITY || u < fmin(1.0, ratio);
 }
 
-__device__ __forceinline__ bool accept_test(float zq, float zp, float mq, float Sq, float mp, float Sp, double cfd,
-                                            double u)
-{
-    return accept_by_ratio(decision_ratio(zq, zp, mq, Sq, mp, Sp, cfd), u);
-}
 
 // =============================================================================
 // Kernel A: row normalisers and accept decisions, one cluster per position
