@@ -377,13 +377,17 @@ __device__ __forceinline__ ArgMax warp_argmax(ArgMax a)
 
 // ---- residual mass of one 16-byte vector --------------------------------------
 // r_k = max(0, q_k - p_k) (RES_DIFF) or q_k (RES_Q), with
-// q_k = 2^((zq_k - mq) c) / Sq.  Adjacent elements k, k+1 travel as one f32x2
-// pair (they come out of one bf16x2 word, or two neighbouring floats).  Every
-// operation rounds to nearest and nothing is contracted, so the result is
-// bit-identical wherever it is recomputed (kernels B and C).
+// q_k = 2^((zq_k - mq) c) / Sq evaluated as 2^(zq_k c - Kq) * Iq: the argument
+// in one rounding against the shift Kq = fl(mq c), whose rounding error e is
+// folded into the row's scale, Iq = (1 - e ln 2) / Sq (residual_shift below),
+// and q_k - p_k = fma(2^(..) , Iq, -p_k) in one rounding.  Adjacent elements
+// k, k+1 travel as one f32x2 pair (they come out of one bf16x2 word, or two
+// neighbouring floats).  Every operation rounds to nearest and nothing is
+// contracted, so the result is bit-identical wherever it is recomputed
+// (kernels B and C).
 template <int DT>
-__device__ __forceinline__ void residual_vec(const uint4 vt, const uint4 vd, int res_mode, float mq,
-                                             float isq, float mp, float isp, float cf, float *r)
+__device__ __forceinline__ void residual_vec(const uint4 vt, const uint4 vd, int res_mode, float Kq,
+                                             float Iq_, float Kp, float Ip_, float cf, float *r)
 {
     constexpr int NE = Elt<DT>::kPerVec;
     constexpr int NP = NE / 2;
@@ -401,24 +405,33 @@ __device__ __forceinline__ void residual_vec(const uint4 vt, const uint4 vd, int
         }
     }
     const unsigned long long Cf = sv::pack2(cf, cf);
-    const unsigned long long Mq = sv::pack2(mq, mq), Iq = sv::pack2(isq, isq);
+    const unsigned long long NKq = sv::pack2(-Kq, -Kq), Iq = sv::pack2(Iq_, Iq_);
 #pragma unroll
     for (int k = 0; k < NP; ++k) {
         float a0, a1;
-        sv::unpack2(sv::mul2(sv::sub2(zt[k], Mq), Cf), a0, a1);
-        const unsigned long long q = sv::mul2(sv::pack2(sv::ex2(a0), sv::ex2(a1)), Iq);
+        sv::unpack2(sv::fma2(zt[k], Cf, NKq), a0, a1);
+        const unsigned long long eq = sv::pack2(sv::ex2(a0), sv::ex2(a1));
         if (res_mode == RES_DIFF) {
-            const unsigned long long Mp = sv::pack2(mp, mp), Ip = sv::pack2(isp, isp);
-            sv::unpack2(sv::mul2(sv::sub2(zd[k], Mp), Cf), a0, a1);
-            const unsigned long long pk = sv::mul2(sv::pack2(sv::ex2(a0), sv::ex2(a1)), Ip);
+            const unsigned long long NKp = sv::pack2(-Kp, -Kp), NIp = sv::pack2(-Ip_, -Ip_);
+            sv::unpack2(sv::fma2(zd[k], Cf, NKp), a0, a1);
+            const unsigned long long npk = sv::mul2(sv::pack2(sv::ex2(a0), sv::ex2(a1)), NIp);  // -p
             float d0, d1;
-            sv::unpack2(sv::sub2(q, pk), d0, d1);
+            sv::unpack2(sv::fma2(eq, Iq, npk), d0, d1);
             r[2 * k] = fmaxf(d0, 0.0f);
             r[2 * k + 1] = fmaxf(d1, 0.0f);
         } else {
-            sv::unpack2(q, r[2 * k], r[2 * k + 1]);
+            sv::unpack2(sv::mul2(eq, Iq), r[2 * k], r[2 * k + 1]);
         }
     }
+}
+
+// The shift and scale of a row for residual_vec from its statistics (m, S):
+// K = fl(m c), e = m c - K exactly (fma), I = (1 - e ln 2) / S.
+__device__ __forceinline__ void residual_shift(float m, float S, float cf, float &K, float &I)
+{
+    K = __fmul_rn(m, cf);
+    const float e = fmaf(m, cf, -K);
+    I = __fmul_rn(1.0f / S, fmaf(-e, 0.6931471805599453f, 1.0f));
 }
 
 __device__ __forceinline__ float warp_incl_scan(float x, int lane)
@@ -905,13 +918,25 @@ struct CtlM {
 
 constexpr size_t kSmemM = kRingBytesM + sizeof(CtlM);
 
-// Residual-mode parameters of sequence b, or false when b is not sampled.
+// Residual-mode parameters of sequence b, or false when b is not sampled:
+// (mq, isq, mp, isp) are residual_vec's shifts and scales (residual_shift).
 struct SeqSample {
     int j, res_mode;
     float mq, isq, mp, isp, cf, uN;
 };
 
-// cf (log2(e)/T, one double division) is left to the caller when with_cf is false.
+// The row statistics of position j as residual_vec's shifts and scales.
+__device__ __forceinline__ void sample_shifts(SeqSample &s, float cf)
+{
+    s.cf = cf;
+    residual_shift(s.mq, s.isq, cf, s.mq, s.isq);
+    if (s.res_mode == RES_DIFF)
+        residual_shift(s.mp, s.isp, cf, s.mp, s.isp);
+}
+
+// cf (log2(e)/T, one double division) and with it the shifts are left to the
+// caller (sample_shifts) when with_cf is false: then mq, isq, mp, isp hold the
+// raw statistics (m, S) and cf holds T.
 __device__ __forceinline__ bool sequence_sample(const SvParams &p, int b, SeqSample &s, bool with_cf = true)
 {
     float T;
@@ -925,11 +950,14 @@ __device__ __forceinline__ bool sequence_sample(const SvParams &p, int b, SeqSam
     const float *st = p.ws_stats + ((size_t)b * (p.N + 1) + j) * 4;
     s.res_mode = (j < p.N) ? RES_DIFF : RES_Q;
     s.mq = __ldcg(st + 0);
-    s.isq = 1.0f / __ldcg(st + 1);
+    s.isq = __ldcg(st + 1);
     s.mp = (j < p.N) ? __ldcg(st + 2) : 0.0f;
-    s.isp = (j < p.N) ? 1.0f / __ldcg(st + 3) : 0.0f;
-    s.cf = with_cf ? (float)(kLog2e / (double)T) : T;
+    s.isp = (j < p.N) ? __ldcg(st + 3) : 1.0f;
     s.uN = p.u[(size_t)b * (p.N + 1) + p.N];
+    if (with_cf)
+        sample_shifts(s, (float)(kLog2e / (double)T));
+    else
+        s.cf = T;
     return true;
 }
 
@@ -1376,7 +1404,8 @@ __global__ void __launch_bounds__(kPickThreads) sv_pick_kernel(const SvParams p)
     if (tid == 0)
         sh.cf = sampled ? (float)(kLog2e / (double)sq.cf) : 0.0f;  // log2(e)/T, once
     __syncthreads();
-    sq.cf = sh.cf;
+    if (sampled)
+        sample_shifts(sq, sh.cf);
     const int j = sq.j;
     if (!sampled) {
         emit_unsampled(p, b, j, my_tok);
