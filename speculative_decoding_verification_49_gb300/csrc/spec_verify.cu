@@ -1563,13 +1563,13 @@ __device__ void walk_mass_pass(CtlW &w, unsigned char *ring, const uint4 *tsrc, 
     while (walk_tile(n_own, rank, C) < NT)
         ++n_own;
     // pass tile i belongs to group i % kWalkGroups, as that group's tile
-    // gcount[grp] + i / kWalkGroups
+    // gcount[grp] + i / kWalkGroups; lane grp of the producer warp fills that
+    // group's stages, so a slower group never holds up the others' copies
     if (warp == kWalkProducerWarp) {
-        if (lane == 0) {
-            const uint32_t g0 = w.gcount[0], g1 = w.gcount[1], g2 = w.gcount[2];
-            for (int i = 0; i < n_own; ++i) {
-                const int grp = i % kWalkGroups;
-                const uint32_t k = (grp == 0 ? g0 : grp == 1 ? g1 : g2) + (uint32_t)(i / kWalkGroups);
+        if (lane < kWalkGroups) {
+            const int grp = lane;
+            for (int i = grp; i < n_own; i += kWalkGroups) {
+                const uint32_t k = w.gcount[grp] + (uint32_t)(i / kWalkGroups);
                 const uint32_t st = walk_stage(grp, k);
                 if (!sv::mbar_wait_bounded(&w.ring.empty[st], walk_parity(k) ^ 1u, &w.ring.abort, kWaitLimitNs)) {
                     w.ring.abort = 1;
