@@ -406,6 +406,19 @@ def measure_fused(sv, torch, dev, stream, rank, steps=20, warmup=3, batch=0):
             "launches_per_call": 8, "steps": steps}
 
 
+def measure_fused_sweep(sv, torch, dev, stream, rank, batches=(32, 64, 128, 512)):
+    """The fused path against the unfused pipeline at other batch sizes (the
+    256-sequence batch is measure_fused's): where, if anywhere, fusing pays."""
+    rows = []
+    for B in batches:
+        r = measure_fused(sv, torch, dev, stream, rank, steps=10, warmup=2, batch=B)
+        rows.append({"B": B, "fused_us": r["us_per_call"], "unfused_us": r["unfused_us_per_call"],
+                     "cublas_gemms_us": r["cublas_gemms_us"], "speedup_vs_unfused": r["speedup_vs_unfused"],
+                     "tflops_frac": r["roofline"]["frac"]})
+        torch.cuda.empty_cache()
+    return rows
+
+
 def run_ours(args):
     import torch
     world, rank, local, pg = dist_init(args)
@@ -429,19 +442,6 @@ def run_ours(args):
     def step():
         ctx.run(w.target, w.draft, w.draft_tokens, w.uniforms, w.temperature, out_tokens=out,
                 num_accepted=nacc, stream=stream)
-
-    # self-check against the oracle on a few sequences (rank 0, untimed)
-    check = None
-    if rank == 0 and not args.no_check:
-        sys.path.insert(0, os.path.join(ROOT, "tests"))
-        import numpy as np
-        import parity
-        seqs = np.array(sorted({b for b in (0, 1, w.B // 2, w.B - 1) if b < w.B}))
-        rep = parity.compare(w, parity.run_gpu(ctx, w, seqs=seqs),
-                             parity.run_oracle(w, seqs=seqs, threads=os.cpu_count() or 1))
-        check = {"sequences": rep["sequences"], "exact": rep["exact"],
-                 "band_sequences": rep["band_sequences"], "q_rel_max": rep.get("q_rel_max"),
-                 "S_rel_max": rep.get("S_rel_max")}
 
     for _ in range(args.warmup):
         step()
@@ -581,9 +581,23 @@ def run_ours(args):
     fused = None
     if not args.no_fused:
         fused = measure_fused(sv, torch, dev, stream, rank, batch=args.fused_batch)
+        if not args.no_fused_sweep:
+            fused["sweep"] = measure_fused_sweep(sv, torch, dev, stream, rank)
 
     cpu = None
+    check = None
     if rank == 0 and not args.no_cpu:
+        if not args.no_check:
+            # the CPU-baseline leg's oracle also checks every sequence of the
+            # launch timed above (same inputs; a debug call for the ratios)
+            sys.path.insert(0, os.path.join(ROOT, "tests"))
+            import parity
+            rep = parity.compare(w, parity.run_gpu(ctx, w), parity.run_oracle(w, threads=os.cpu_count() or 1))
+            check = {k: rep.get(k) for k in ("sequences", "exact", "decisions", "band_decisions",
+                                              "band_sequences", "band_mismatch", "q_rel_max", "S_rel_max",
+                                              "decision_ratio_err_max")}
+            check["band_rate"] = rep["band_decisions"] / max(1, rep["decisions"])
+            check["mismatch_rate"] = rep["band_mismatch"] / max(1, rep["decisions"])
         rate, n, dt = cpu_oracle_rate(w, args.cpu_budget, os.cpu_count() or 1)
         rate1, n1, dt1 = cpu_oracle_rate(w, args.cpu_budget / 2, 1)
         cpu = {"value": rate, "unit": UNIT, "cores": os.cpu_count() or 1, "kind": "oracle",
@@ -640,6 +654,7 @@ def main():
     ap.add_argument("--no-tree", action="store_true", help="skip the tree-verification measurement")
     ap.add_argument("--no-fused", action="store_true", help="skip the fused LM-head measurement")
     ap.add_argument("--fused-batch", type=int, default=0, help="override B of the fused LM-head measurement")
+    ap.add_argument("--no-fused-sweep", action="store_true", help="skip the fused-vs-unfused batch sweep")
     ap.add_argument("--kv-max-len", type=int, default=KV_MAX_LEN,
                     help="cache positions of the KV-commit measurement (the copy does not depend on it)")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
