@@ -84,6 +84,7 @@ struct SvParams {
     int *ws_first;    // [max_B] first rejected position, kNoReject if none
     int *ws_err;      // [max_B] error bits of the sequence
     int *ws_tok;      // [max_B*(max_N+1)] greedy argmax of each position
+    int *ws_ticket;   // [max_B*(max_N+1)] rows of the position normalised so far (one-row units), 0 between calls
     float *ws_stats;  // [max_B*(max_N+1)][4] (mq, Sq, mp, Sp) of each position
     float *ws_slice;  // [max_B*slices][8] residual mass of each warp's share of a slice
     int *status;      // sticky error bits of the context
@@ -871,6 +872,268 @@ __global__ void __launch_bounds__(kThreads, 4) sv_rows_kernel(const SvParams p)
         sv::cluster_sync();  // no peer reads this CTA's shared memory any more
     if (tid == 0 && ctl.ring.abort)
         ring_drain(ctl.ring);
+}
+
+// =============================================================================
+// Kernel A1: one logit row per CTA (batches with a CTA per position)
+// =============================================================================
+//
+// Where kernel A would run one CTA per position (no cluster), the units are
+// single rows instead: a sampled position's target and draft rows are two
+// CTAs, a greedy or bonus position's target row one.  Every unit then streams
+// the same number of bytes, so one-wave batches (a mixed batch whose greedy
+// positions read half as much) and the last wave of large ones do not end on
+// a tail of two-row units.  Each ring stage holds two consecutive 8 KiB tiles
+// of the one row (the same 16 KiB in flight per stage, the same 32 elements
+// per thread and stage).  A position's two rows meet through the workspace:
+// each CTA writes its row's statistics, takes a ticket, and the second one
+// decides with kernel A's arithmetic.  Units run position by position in
+// descending order (position 0 last, as in kernel A), a sequence's two rows
+// next to each other; a draft-row unit of a greedy sequence (or of a tree node
+// without children) reads nothing and leaves.
+template <int DT, bool TREE>
+__global__ void __launch_bounds__(kThreads, 4) sv_row_kernel(const SvParams p)
+{
+    constexpr int VE = Elt<DT>::kPerVec;
+    constexpr int kStageVecs = 2 * kTileVecs;  // vectors of the row per ring stage
+    extern __shared__ __align__(128) unsigned char smem[];
+    unsigned char *ring = smem;
+    constexpr int kStages = kStagesA;
+    CtlA &ctl = *reinterpret_cast<CtlA *>(smem + ring_bytes(kStages));
+
+    if constexpr (TREE)
+        sv::grid_launch_dependents();  // the walk's clusters may start on SMs as this grid's CTAs retire
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int N = p.N, V = p.V, B = p.B;
+    int i, b, is_draft;
+    {
+        const int u = blockIdx.x;
+        if (TREE) {  // every node may have a draft row
+            const int pos = u / (2 * B), w = u - pos * (2 * B);
+            i = N - pos;
+            b = w >> 1;
+            is_draft = w & 1;
+        } else if (u < B) {  // position N: target rows only
+            i = N;
+            b = u;
+            is_draft = 0;
+        } else {
+            const int v = u - B, pos = v / (2 * B), w = v - pos * (2 * B);
+            i = N - 1 - pos;
+            b = w >> 1;
+            is_draft = w & 1;
+        }
+    }
+
+    float T;
+    const int mode = sequence_mode(p, b, T);
+    const size_t trow = (size_t)b * (N + 1) + i;
+    const size_t drow = TREE ? trow : (size_t)b * N + i;
+    int d = 0;
+    bool bad_d = false, bad_tree = false;
+    if constexpr (TREE) {
+        if (i > 0) {
+            d = p.tokens[trow];
+            bad_d = d < 0 || d >= V;
+        }
+        const int par = p.parent[trow];
+        bad_tree = (i == 0) ? (par != -1) : (par < 0 || par >= i);
+    } else {
+        d = (i < N) ? p.tokens[(size_t)b * N + i] : 0;
+        bad_d = (i < N) && (d < 0 || d >= V);
+    }
+    if (tid == 0) {
+        ring_init(ctl.ring);
+        const double cfd = (mode == MODE_SAMPLED) ? kLog2e / (double)T : 0.0;
+        ctl.cfd = cfd;
+        ctl.cf = (float)cfd;
+        if (!TREE)
+            ctl.has_child = 1;  // (a tree node's is set by the producer warp below)
+    }
+    if constexpr (TREE) {
+        if (warp == kProducerWarp) {
+            bool any = false;
+            for (int c = i + 1 + lane; c <= N; c += 32)
+                any |= p.parent[(size_t)b * (N + 1) + c] == i;
+            any = __any_sync(0xffffffffu, any);
+            __syncwarp();
+            if (lane == 0)
+                ctl.has_child = any ? 1 : 0;
+        }
+    }
+    const bool decides = !TREE && mode == MODE_SAMPLED && i < N;  // a two-row position of the chain
+    const bool prefetcher = tid == 32 * kProducerWarp + 1;
+    float pre_zq = 0.0f, pre_zp = 0.0f, pre_u = 0.0f;
+    if (prefetcher && decides && !bad_d) {
+        pre_zq = logit_at<DT>(p.target, trow * (size_t)V + d);
+        pre_zp = logit_at<DT>(p.draft, drow * (size_t)V + d);
+        pre_u = p.u[trow];
+    }
+    __syncthreads();
+    if (is_draft && (mode != MODE_SAMPLED || !ctl.has_child))
+        return;  // no draft row is read (uniform over the CTA)
+    const float cf = ctl.cf;
+    const int NV = V / VE;
+    const uint4 *src = static_cast<const uint4 *>(is_draft ? p.draft : p.target) + (is_draft ? drow : trow) * (size_t)NV;
+    const int nst = (NV + kStageVecs - 1) / kStageVecs;
+
+    // ---- stream the row once
+    Online2 o2{-INFINITY, 0ull};
+    ArgMax ga{-INFINITY, INT_MAX, 0};
+    if (mode != MODE_INVALID) {
+        if (warp == kProducerWarp) {
+            if (lane == 0) {
+                for (int t = 0; t < nst; ++t) {
+                    const uint32_t s = (uint32_t)t % kStages;
+                    if (!sv::mbar_wait_bounded(&ctl.ring.empty[s], (((uint32_t)t / kStages) & 1u) ^ 1u, &ctl.ring.abort,
+                                               kWaitLimitNs)) {
+                        ctl.ring.abort = 1;
+                        break;
+                    }
+                    const int nvec = min(kStageVecs, NV - t * kStageVecs);
+                    const uint32_t bytes = static_cast<uint32_t>(nvec) * 16u;
+                    sv::mbar_arrive_expect_tx(&ctl.ring.full[s], bytes);
+                    sv::bulk_g2s(ring + s * (2 * kTileBytes), src + (size_t)t * kStageVecs, bytes, &ctl.ring.full[s]);
+                    ctl.ring.last_g[s] = t;
+                }
+            }
+            __syncwarp();
+        } else {
+            for (int t = 0; t < nst; ++t) {
+                if (consume_wait(ctl.ring, t)) {
+                    const uint4 *stage = reinterpret_cast<const uint4 *>(ring + (t % kStages) * (2 * kTileBytes));
+                    if (mode == MODE_GREEDY) {
+#pragma unroll
+                        for (int k = 0; k < 2 * kVPT; ++k) {
+                            const int sv_ = k * kSliceVecs + tid;
+                            const int vec = t * kStageVecs + sv_;
+                            if (vec < NV)
+                                argmax_add2<DT>(ga, stage[sv_], vec * VE);
+                        }
+                    } else {
+                        uint4 v[2 * kVPT];
+#pragma unroll
+                        for (int k = 0; k < 2 * kVPT; ++k) {
+                            const int sv_ = k * kSliceVecs + tid;
+                            v[k] = (t * kStageVecs + sv_ < NV) ? stage[sv_] : neg_inf_vec<DT>();
+                        }
+                        online_add_tile<DT, 2 * kVPT>(o2, v, cf);
+                    }
+                } else {
+                    ctl.ring.abort = 1;
+                }
+                consume_release(ctl.ring, t, lane);
+            }
+        }
+    }
+    if (prefetcher) {
+        ctl.zq_d = pre_zq;
+        ctl.zp_d = pre_zp;
+        ctl.u_i = pre_u;
+    }
+
+    // ---- the CTA's result
+    Online o = online_fold<DT>(o2, cf);
+    if (warp < kConsWarps) {
+        if (mode == MODE_GREEDY) {
+            ga = warp_argmax(ga);
+            if (lane == 0) {
+                ctl.red_m[warp] = ga.v;
+                ctl.red_i[warp] = ga.i;
+                ctl.red_n[warp] = ga.nan;
+            }
+        } else if (mode == MODE_SAMPLED) {
+            o = warp_merge(o, cf);
+            if (lane == 0) {
+                ctl.red_m[warp] = o.m;
+                ctl.red_s[warp] = o.s;
+            }
+        }
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int errb = (bad_d ? kErrBadToken : 0) | (bad_tree ? kErrBadTree : 0);
+        if (mode == MODE_GREEDY) {
+            ArgMax a{ctl.red_m[0], ctl.red_i[0], ctl.red_n[0]};
+            for (int w = 1; w < kConsWarps; ++w)
+                a = argmax_merge(a, ArgMax{ctl.red_m[w], ctl.red_i[w], ctl.red_n[w]});
+            if (a.nan || a.v == INFINITY || a.v == -INFINITY)
+                errb |= kErrBadValue;
+            p.ws_tok[trow] = a.i;
+            if (!TREE && i < N && d != a.i)
+                atomicMin(&p.ws_first[b], i);
+            if (p.tstats) {
+                p.tstats[trow * 2 + 0] = a.v;
+                p.tstats[trow * 2 + 1] = NAN;
+            }
+            if (!TREE && i < N) {
+                if (p.q_at)
+                    p.q_at[drow] = NAN;
+                if (p.p_at)
+                    p.p_at[drow] = NAN;
+                if (p.ratio_at)
+                    p.ratio_at[drow] = NAN;
+                if (p.dstats) {
+                    p.dstats[drow * 2 + 0] = NAN;
+                    p.dstats[drow * 2 + 1] = NAN;
+                }
+            }
+        } else if (mode == MODE_SAMPLED) {
+            Online a{ctl.red_m[0], ctl.red_s[0]};
+            for (int w = 1; w < kConsWarps; ++w)
+                a = online_merge(a, Online{ctl.red_m[w], ctl.red_s[w]}, cf);
+            if (!(isfinite(a.m) && isfinite(a.s) && a.s > 0.0f))
+                errb |= kErrBadValue;
+            float *st = p.ws_stats + trow * 4 + (is_draft ? 2 : 0);
+            st[0] = a.m;
+            st[1] = a.s;
+            if (!is_draft && p.tstats) {
+                p.tstats[trow * 2 + 0] = a.m;
+                p.tstats[trow * 2 + 1] = a.s;
+            }
+            if (is_draft && p.dstats) {
+                p.dstats[drow * 2 + 0] = a.m;
+                p.dstats[drow * 2 + 1] = a.s;
+            }
+            if (decides) {
+                // the second of the position's two rows decides it
+                __threadfence();
+                if (atomicAdd(&p.ws_ticket[trow], 1) == 1) {
+                    __threadfence();
+                    p.ws_ticket[trow] = 0;
+                    const float *sq = p.ws_stats + trow * 4;
+                    const float mq = __ldcg(sq + 0), Sq = __ldcg(sq + 1), mp = __ldcg(sq + 2), Sp = __ldcg(sq + 3);
+                    const bool valid = isfinite(mq) && isfinite(Sq) && Sq > 0.0f && isfinite(mp) && isfinite(Sp) &&
+                                       Sp > 0.0f;
+                    if (p.ratio_at)
+                        p.ratio_at[drow] = NAN;
+                    if (valid && !bad_d) {
+                        const float zq = ctl.zq_d, zp = ctl.zp_d;
+                        const double cfd = ctl.cfd;
+                        const double ratio = decision_ratio(zq, zp, mq, Sq, mp, Sp, cfd);
+                        if (!accept_by_ratio(ratio, (double)ctl.u_i))
+                            atomicMin(&p.ws_first[b], i);
+                        if (p.ratio_at)
+                            p.ratio_at[drow] = (float)ratio;
+                        if (p.q_at)
+                            p.q_at[drow] = (float)(exp2(((double)zq - (double)mq) * cfd) / (double)Sq);
+                        if (p.p_at)
+                            p.p_at[drow] = (float)(exp2(((double)zp - (double)mp) * cfd) / (double)Sp);
+                    }
+                }
+            }
+        } else if (!is_draft) {
+            errb |= kErrBadValue;
+            if (!TREE && i < N && p.ratio_at)
+                p.ratio_at[drow] = NAN;
+        }
+        if (ctl.ring.abort)
+            errb |= kErrTimeout;
+        if (errb)
+            atomicOr(&p.ws_err[b], errb);
+        if (ctl.ring.abort)
+            ring_drain(ctl.ring);
+    }
 }
 
 // =============================================================================
@@ -2093,7 +2356,7 @@ struct spec_verify_ctx {
     int clusters_tree[kMaxCluster + 1];  // the same for kernel A over tree nodes
     void *ws;
     int mass_ctas;                       // resident CTAs of the mass kernel (all SMs)
-    int *ws_first, *ws_err, *ws_tok, *status;
+    int *ws_first, *ws_err, *ws_tok, *ws_ticket, *status;
     float *ws_stats, *ws_slice;
     unsigned long long *hist;  // [max_N + 2]: accepted-draft histogram, then invalid
     // fused LM-head path: scratch allocated on its first call (and when K grows)
@@ -2138,6 +2401,10 @@ template <typename K> cudaError_t set_kernel_attrs(K kernel, size_t smem)
 template <int DT> cudaError_t set_attrs()
 {
     cudaError_t e = set_kernel_attrs(sv_rows_kernel<DT, false>, kSmemA);
+    if (e == cudaSuccess)
+        e = set_kernel_attrs(sv_row_kernel<DT, false>, kSmemA);
+    if (e == cudaSuccess)
+        e = set_kernel_attrs(sv_row_kernel<DT, true>, kSmemA);
     if (e == cudaSuccess)
         e = set_kernel_attrs(sv_rows_kernel<DT, true>, kSmemA);
     if (e == cudaSuccess)
@@ -2305,6 +2572,7 @@ sv_status run_impl(spec_verify_ctx *ctx, const void *target, const void *draft, 
     prm.ws_first = ctx->ws_first;
     prm.ws_err = ctx->ws_err;
     prm.ws_tok = ctx->ws_tok;
+    prm.ws_ticket = ctx->ws_ticket;
     prm.ws_stats = ctx->ws_stats;
     prm.ws_slice = ctx->ws_slice;
     prm.hist = ctx->hist;
@@ -2325,9 +2593,20 @@ sv_status run_impl(spec_verify_ctx *ctx, const void *target, const void *draft, 
     if (ev)
         cudaEventRecord(ev[0], st);
     cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = launch_config((unsigned)(units * CA), CA, kSmemA, st, attr);
-    cudaError_t e = (ctx->dtype == SV_BF16) ? cudaLaunchKernelEx(&cfg, sv_rows_kernel<SV_BF16, false>, prm)
-                                            : cudaLaunchKernelEx(&cfg, sv_rows_kernel<SV_F32, false>, prm);
+    cudaError_t e;
+    if (CA == 1 && units >= ctx->clusters_a[1]) {
+        // at least a wave of positions: one CTA per logit row (B target rows at
+        // position N, two rows at the others).  Measured on GB300: headline
+        // 212.3 -> 209.1 us per call, stress 682.3 -> 672.4 us; a one-wave mixed
+        // batch (384 positions) 58.8 -> 63.0 us, so it keeps a CTA per position.
+        cudaLaunchConfig_t cfg = launch_config((unsigned)(B * (2LL * N + 1)), 1, kSmemA, st, attr);
+        e = (ctx->dtype == SV_BF16) ? cudaLaunchKernelEx(&cfg, sv_row_kernel<SV_BF16, false>, prm)
+                                    : cudaLaunchKernelEx(&cfg, sv_row_kernel<SV_F32, false>, prm);
+    } else {
+        cudaLaunchConfig_t cfg = launch_config((unsigned)(units * CA), CA, kSmemA, st, attr);
+        e = (ctx->dtype == SV_BF16) ? cudaLaunchKernelEx(&cfg, sv_rows_kernel<SV_BF16, false>, prm)
+                                    : cudaLaunchKernelEx(&cfg, sv_rows_kernel<SV_F32, false>, prm);
+    }
     if (e == cudaSuccess) {
         if (ev)
             cudaEventRecord(ev[1], st);
@@ -2410,6 +2689,7 @@ sv_status tree_run_impl(spec_verify_ctx *ctx, const void *target, const void *dr
     prm.ws_first = ctx->ws_first;
     prm.ws_err = ctx->ws_err;
     prm.ws_tok = ctx->ws_tok;
+    prm.ws_ticket = ctx->ws_ticket;
     prm.ws_stats = ctx->ws_stats;
     prm.ws_slice = ctx->ws_slice;
     prm.hist = ctx->hist;
@@ -2424,9 +2704,18 @@ sv_status tree_run_impl(spec_verify_ctx *ctx, const void *target, const void *dr
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = launch_config((unsigned)(units * CA), CA, kSmemA, st, attr);
-    cudaError_t e = (ctx->dtype == SV_BF16) ? cudaLaunchKernelEx(&cfg, sv_rows_kernel<SV_BF16, true>, prm)
-                                            : cudaLaunchKernelEx(&cfg, sv_rows_kernel<SV_F32, true>, prm);
+    cudaError_t e;
+    if (CA == 1 && units >= ctx->clusters_tree[1]) {
+        // one CTA per logit row: each node's target row and, if it has
+        // children, its draft row (64-tree call 132.1 -> 125.4 us)
+        cudaLaunchConfig_t cfg = launch_config((unsigned)(2LL * units), 1, kSmemA, st, attr);
+        e = (ctx->dtype == SV_BF16) ? cudaLaunchKernelEx(&cfg, sv_row_kernel<SV_BF16, true>, prm)
+                                    : cudaLaunchKernelEx(&cfg, sv_row_kernel<SV_F32, true>, prm);
+    } else {
+        cudaLaunchConfig_t cfg = launch_config((unsigned)(units * CA), CA, kSmemA, st, attr);
+        e = (ctx->dtype == SV_BF16) ? cudaLaunchKernelEx(&cfg, sv_rows_kernel<SV_BF16, true>, prm)
+                                    : cudaLaunchKernelEx(&cfg, sv_rows_kernel<SV_F32, true>, prm);
+    }
     if (e == cudaSuccess) {
         cudaLaunchAttribute pdl[1];
         pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -2548,6 +2837,7 @@ sv_status fused_run_impl(spec_verify_ctx *ctx, const void *ht, const void *wt, i
     prm.ws_first = ctx->ws_first;
     prm.ws_err = ctx->ws_err;
     prm.ws_tok = ctx->ws_tok;
+    prm.ws_ticket = ctx->ws_ticket;
     prm.ws_stats = ctx->ws_stats;
     prm.ws_slice = ctx->ws_slice;
     prm.hist = ctx->hist;
@@ -2642,13 +2932,14 @@ sv_status spec_verify_create(spec_verify_ctx **out, int device, int max_B, int m
 
     c->mass_ctas = (dtype == SV_BF16) ? mass_ctas<SV_BF16>(c->num_sms) : mass_ctas<SV_F32>(c->num_sms);
 
-    // workspace: hist[max_N+2] (u64) | first[nb] err[nb] tok[ntok] stats[4*ntok] | slice[nb*S*8] status;
+    // workspace: hist[max_N+2] (u64) | first[nb] err[nb] tok[ntok] stats[4*ntok] ticket[ntok] |
+    // slice[nb*S*8] status;
     // the slice shares start on a 256-byte boundary (kernel C reads them as float4)
     const size_t nb = (size_t)(max_B > 0 ? max_B : 1);
     const size_t ntok = nb * (size_t)(max_N + 1);
     const size_t nslice = nb * (size_t)residual_slices(V, dtype) * kConsWarps;
     const size_t hist_ints = ((size_t)(max_N + 2) * 2 + 63) / 64 * 64;
-    const size_t slice_off = (hist_ints + 2 * nb + 5 * ntok + 63) / 64 * 64;
+    const size_t slice_off = (hist_ints + 2 * nb + 6 * ntok + 63) / 64 * 64;
     const size_t bytes = sizeof(int) * (slice_off + nslice + 1);
     if (cudaMalloc(&c->ws, bytes) != cudaSuccess) {
         cudaGetLastError();
@@ -2661,6 +2952,7 @@ sv_status spec_verify_create(spec_verify_ctx **out, int device, int max_B, int m
     c->ws_err = w + nb;
     c->ws_tok = w + 2 * nb;
     c->ws_stats = reinterpret_cast<float *>(w + 2 * nb + ntok);
+    c->ws_ticket = w + 2 * nb + 5 * ntok;
     c->ws_slice = reinterpret_cast<float *>(static_cast<int *>(c->ws) + slice_off);
     c->status = static_cast<int *>(c->ws) + slice_off + nslice;
     if (cudaMemset(c->ws, 0, bytes) != cudaSuccess || cudaMemset(c->ws_first, 0x7f, sizeof(int) * nb) != cudaSuccess ||
@@ -2936,9 +3228,9 @@ namespace {
 constexpr int kNoAllocMaxB = 2048;        // sequences per call
 constexpr int kNoAllocMaxUnits = 16384;   // B*(N+1) verified positions per call
 constexpr int kNoAllocMaxSlices = 32768;  // B*ceil(V*elt/4 KiB) residual slices per call
-constexpr int kNoAllocSliceOff = 2 * kNoAllocMaxB + 5 * kNoAllocMaxUnits;  // a multiple of 64 ints
+constexpr int kNoAllocSliceOff = 2 * kNoAllocMaxB + 6 * kNoAllocMaxUnits;  // a multiple of 64 ints
 static_assert(kNoAllocSliceOff % 64 == 0, "slice shares must start on a 256-byte boundary");
-constexpr int kNoAllocInts = kNoAllocSliceOff + 8 * kNoAllocMaxSlices + 1;  // about 1.33 MiB
+constexpr int kNoAllocInts = kNoAllocSliceOff + 8 * kNoAllocMaxSlices + 1;  // about 1.39 MiB
 // the 256-sequence Qwen-vocabulary batch (V = 151936 bf16: 75 slices a row) fits
 static_assert(256 * 75 <= kNoAllocMaxSlices, "the scratch holds a 256 x 151936 bf16 batch");
 constexpr int kNoAllocMaxDevices = 64;
@@ -3041,6 +3333,7 @@ extern "C" sv_status spec_verify_run_noalloc(const void *target_logits, const vo
     c.ws_err = w + kNoAllocMaxB;
     c.ws_tok = w + 2 * kNoAllocMaxB;
     c.ws_stats = reinterpret_cast<float *>(w + 2 * kNoAllocMaxB + kNoAllocMaxUnits);
+    c.ws_ticket = w + 2 * kNoAllocMaxB + 5 * kNoAllocMaxUnits;
     c.ws_slice = reinterpret_cast<float *>(w + kNoAllocSliceOff);
     c.status = w + kNoAllocSliceOff + 8 * kNoAllocMaxSlices;
 

@@ -80,6 +80,30 @@ def test_parity_random_shapes(k, dtype, V, N, B, T):
     _check(w)
 
 
+@pytest.mark.parametrize("dtype,T", [("bf16", (0.0, 0.7, 1.0)), ("f32", 0.9)])
+def test_parity_one_row_per_cta(dtype, T):
+    """More than a wave of positions (320 sequences x 4 positions) makes the
+    row kernel take one CTA per logit row and meet a position's two rows
+    through the workspace; every sequence against the oracle, with greedy
+    sequences (draft rows not read), a bad token and a NaN row among them."""
+    w = synth.make_workload("small", seed=31, device="cuda", B=320, N=3, V=4096 if dtype == "f32" else 8192,
+                            dtype=dtype, T=T)
+    w.draft_tokens[5, 1] = w.V + 3        # bad token
+    w.draft[7, 2, 11] = float("nan")      # NaN in a draft row
+    if dtype == "bf16":
+        w.temperature[7] = 1.0            # a sampled sequence, so that its draft rows are read
+    ctx = _ctx(w)
+    assert ctx.cluster_size(w.B, w.N) == 1
+    gpu = parity.run_gpu(ctx, w)
+    orc = parity.run_oracle(w, threads=THREADS)
+    rep = parity.compare(w, gpu, orc)
+    print(w.name, rep)
+    assert rep["sequences"] == w.B and rep["band_mismatch"] <= 1
+    assert gpu["num_accepted"][5] == -1 and gpu["num_accepted"][7] == -1
+    assert ctx.status() in (sv.SV_ERR_BAD_TOKEN, sv.SV_ERR_BAD_VALUE)
+    assert ctx.status() == sv.SV_OK
+
+
 @pytest.mark.parametrize("name", ["headline", "stress"])
 def test_parity_full_size_every_sequence(name):
     """The full-size launch the benchmark times (headline: 256 sequences x 15

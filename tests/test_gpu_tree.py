@@ -46,6 +46,8 @@ def _check(w, ctx=None, greedy=None, seqs=None):
     ("tree_small", 0, {}), ("tree_small", 1, {}), ("tree_small", 2, {"B": 40}),
     ("tree_mixed", 0, {}), ("tree_mixed", 1, {}),
     ("tree", 0, {"B": 6}),
+    # at least a wave of nodes (660 and 1260): kernel A runs one CTA per logit row
+    ("tree_small", 3, {"B": 60}), ("tree_mixed", 2, {"B": 60}),
 ])
 def test_tree_parity(name, seed, over):
     w = synth.make_tree_workload(name, seed=seed, device="cuda", **over)
