@@ -1368,83 +1368,116 @@ __device__ __forceinline__ float slice_thread_mass(const uint4 *tsrc, const uint
 constexpr int kMaxRowSlices = kMaxCluster * kMaxSlices;  // slices of the longest supported row
 
 // ---- inverse CDF over slice masses (kernel C and the tree walk) ---------------
-// The search above the slice level runs in double: slice masses are the
-// double sums of their eight float warp shares, their prefix and the target
-// x = u * R are double, so where a token falls is resolved to the float
-// precision of one warp's share of one slice, not of the running total (in
-// float, the cumulative mass near R/2 has a resolution of about 3e-8 R, wider
-// than many tail tokens of a 150 000-token vocabulary).
-__device__ __forceinline__ double warp_incl_scan_d(double x, int lane)
+// Above the slice level the search runs in 64-bit fixed point: every float
+// warp share x (a mass in [0, 1]) is the integer floor(x 2^62), exact for
+// x >= 2^-38, so slice masses, their prefix sums and the total R are exact
+// integer sums, and the target floor(u R) is one 64 x 64-bit high product.
+// Where a token falls is then resolved to the float precision of one warp's
+// share of one slice, not of the running total (in float the cumulative mass
+// near R/2 resolves only about 3e-8 R, coarser than many tail tokens of a
+// 150 000-token vocabulary), and with integer additions, not the narrow FP64
+// pipe.
+typedef unsigned long long fx_t;
+constexpr fx_t kFxNone = ~0ull;  // no remainder: rounding fell back to the last slice with mass
+
+__device__ __forceinline__ fx_t fx_of(float x)
+{
+    const uint32_t bits = __float_as_uint(x);
+    int e = (int)((bits >> 23) & 0xffu);
+    if ((bits >> 31) || e == 0)  // -0, or below 2^-126: nothing at this scale
+        return 0ull;
+    e = e > 127 ? 127 : e;       // masses stay below 2 (a share is at most R <= 1 plus rounding)
+    const fx_t m = (fx_t)((bits & 0x7fffffu) | 0x800000u);
+    const int sh = e - 88;       // x = m 2^(e - 150), so x 2^62 = m 2^(e - 88)
+    return sh >= 0 ? (m << sh) : (sh > -24 ? (m >> -sh) : 0ull);
+}
+
+__device__ __forceinline__ float fx_to_float(fx_t v) { return __ull2float_rn(v) * 0x1p-62f; }
+
+// floor(u R) for u in [0, 1): u as the exact integer u 2^64 (for u >= 2^-40),
+// times R, high 64 bits of the product.
+__device__ __forceinline__ fx_t fx_scale(float u, fx_t R)
+{
+    const uint32_t bits = __float_as_uint(u);
+    const int e = (int)((bits >> 23) & 0xffu);
+    if ((bits >> 31) || e == 0)
+        return 0ull;
+    const fx_t m = (fx_t)((bits & 0x7fffffu) | 0x800000u);
+    const int sh = e - 86;  // u 2^64 = m 2^(e - 86); e <= 126 since u < 1
+    const fx_t ux = sh >= 0 ? (m << (sh > 40 ? 40 : sh)) : (sh > -24 ? (m >> -sh) : 0ull);
+    return __umul64hi(ux, R);
+}
+
+__device__ __forceinline__ fx_t warp_incl_scan_fx(fx_t x, int lane)
 {
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const double y = __shfl_up_sync(0xffffffffu, x, o);
+        const fx_t y = __shfl_up_sync(0xffffffffu, x, o);
         if (lane >= o)
-            x = __dadd_rn(x, y);
+            x += y;
     }
     return x;
 }
 
-// Total of a slice: its eight warp shares (float, in warp order) added in double.
-__device__ __forceinline__ double slice_total_d(const float *w8)
+// Total of a slice: its eight warp shares, in fixed point.
+__device__ __forceinline__ fx_t slice_total_fx(const float *w8)
 {
-    double t = 0.0;
+    fx_t t = 0ull;
 #pragma unroll
     for (int q = 0; q < kConsWarps; ++q)
-        t = __dadd_rn(t, (double)w8[q]);
+        t += fx_of(w8[q]);
     return t;
 }
 
-// Warp 0: the total of S slice masses, by warp-inclusive scans in slice order.
-__device__ __forceinline__ double warp_total_slices(const double *slice, int S, int lane)
+// Warp 0: the total of S slice masses.
+__device__ __forceinline__ fx_t warp_total_slices(const fx_t *slice, int S, int lane)
 {
-    double carry = 0.0;
+    fx_t carry = 0ull;
     for (int c0 = 0; c0 < S; c0 += 32) {
         const int c = c0 + lane;
-        const double m = (c < S) ? slice[c] : 0.0;
-        carry = __shfl_sync(0xffffffffu, __dadd_rn(warp_incl_scan_d(m, lane), carry), 31);
+        const fx_t m = (c < S) ? slice[c] : 0ull;
+        carry = __shfl_sync(0xffffffffu, warp_incl_scan_fx(m, lane) + carry, 31);
     }
     return carry;
 }
 
 // Warp-wide: the first slice whose cumulative mass exceeds x, and x1 = x minus
-// the mass before it; when rounding leaves x at or above the total, the last
-// slice with mass and x1 = INFINITY.  Cumulative sums are warp-inclusive scans
-// in slice order (the same additions as warp_total_slices).
-__device__ __forceinline__ void warp_find_slice(const double *slice, int S, double x, int lane, int &cs, double &x1)
+// the mass before it.  x < R always (u < 1), so a slice is always found; the
+// fallback (the last slice with mass, x1 = kFxNone) guards only an empty total.
+__device__ __forceinline__ void warp_find_slice(const fx_t *slice, int S, fx_t x, int lane, int &cs, fx_t &x1)
 {
     cs = -1;
-    x1 = INFINITY;
-    double run = 0.0;
+    x1 = kFxNone;
+    fx_t run = 0ull;
     for (int c0 = 0; c0 < S && cs < 0; c0 += 32) {
         const int c = c0 + lane;
-        const double m = (c < S) ? slice[c] : 0.0;
-        const double inc = __dadd_rn(warp_incl_scan_d(m, lane), run);
+        const fx_t m = (c < S) ? slice[c] : 0ull;
+        const fx_t inc = warp_incl_scan_fx(m, lane) + run;
         const unsigned hit = __ballot_sync(0xffffffffu, c < S && x < inc);
         if (hit) {
             const int l = __ffs(hit) - 1;
-            const double prev = __shfl_sync(0xffffffffu, inc, l > 0 ? l - 1 : 0);
+            const fx_t prev = __shfl_sync(0xffffffffu, inc, l > 0 ? l - 1 : 0);
             cs = c0 + l;
-            x1 = __dsub_rn(x, l > 0 ? prev : run);
+            x1 = x - (l > 0 ? prev : run);
         }
         run = __shfl_sync(0xffffffffu, inc, 31);
     }
-    if (cs < 0) {  // rounding: the last slice that has mass
+    if (cs < 0) {  // no mass at all: the last slice that has mass, else the last
         for (int c0 = ((S - 1) / 32) * 32; c0 >= 0 && cs < 0; c0 -= 32) {
             const int c = c0 + lane;
-            const unsigned m = __ballot_sync(0xffffffffu, c < S && slice[c] > 0.0);
+            const unsigned m = __ballot_sync(0xffffffffu, c < S && slice[c] > 0ull);
             if (m)
                 cs = c0 + 31 - __clz(m);
         }
         if (cs < 0)
             cs = S - 1;
-        x1 = INFINITY;
+        x1 = kFxNone;
     }
 }
 
 // Element search inside slice ss, whose masses thread t holds for vector t
 // (r[VE] and their sum `part`; threads past the 256 of a slice pass zeros):
-// warp totals in warp order (a double running sum, as the slice total was
+// warp totals in warp order (a fixed-point running sum, as the slice total was
 // formed), then the lane, then the element where the cumulative mass first
 // exceeds x1; rounding falls back to the last element with mass.  Every thread
 // of the block calls it (it synchronises the block).
@@ -1455,7 +1488,7 @@ struct PickState {
 };
 
 template <int VE>
-__device__ int pick_in_slice(PickState &ps, int ss, float part, const float *r, double x1, int NV)
+__device__ int pick_in_slice(PickState &ps, int ss, float part, const float *r, fx_t x1, int NV)
 {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const float incl = warp_incl_scan(part, lane);
@@ -1465,13 +1498,12 @@ __device__ int pick_in_slice(PickState &ps, int ss, float part, const float *r, 
     if (warp == 0) {
         int sel = -1;
         float xl = 0.0f;
-        if (x1 != INFINITY) {
-            const float wt = (lane < kConsWarps) ? ps.incl[lane * 32 + 31] : 0.0f;
-            double wc = 0.0, wprev = 0.0;
+        if (x1 != kFxNone) {
+            const fx_t wt = (lane < kConsWarps) ? fx_of(ps.incl[lane * 32 + 31]) : 0ull;
+            fx_t wc = 0ull, wprev = 0ull;
             int ws = -1;
             for (int w = 0; w < kConsWarps; ++w) {
-                const double wtw = (double)__shfl_sync(0xffffffffu, wt, w);
-                const double next = __dadd_rn(wc, wtw);
+                const fx_t next = wc + __shfl_sync(0xffffffffu, wt, w);
                 if (ws < 0 && x1 < next) {
                     ws = w;
                     wprev = wc;
@@ -1479,7 +1511,7 @@ __device__ int pick_in_slice(PickState &ps, int ss, float part, const float *r, 
                 wc = next;
             }
             if (ws >= 0) {
-                const float xw = __double2float_rn(__dsub_rn(x1, wprev));
+                const float xw = fx_to_float(x1 - wprev);
                 const float li = ps.incl[ws * 32 + lane];
                 const unsigned ml = __ballot_sync(0xffffffffu, xw < li);
                 if (ml) {
@@ -1527,12 +1559,12 @@ __device__ int pick_in_slice(PickState &ps, int ss, float part, const float *r, 
 }
 
 struct PickShared {
-    double slice[kMaxRowSlices];  // the sequence's slice masses
+    fx_t slice[kMaxRowSlices];  // the sequence's slice masses
     float wtot[kConsWarps];
     PickState ps;
     int sstar, retry;
-    double x1;
-    float cf;                     // log2(e)/T
+    fx_t x1;
+    float cf;                   // log2(e)/T
 };
 
 // Outputs of sequence b, written by every thread of the block in parallel:
@@ -1605,17 +1637,17 @@ __device__ int draw_token(PickShared &sh, SeqSample &sq, const uint4 *tsrc, cons
                     sh.wtot[warp] = incl;
                 __syncthreads();
                 if (tid == 0)
-                    sh.slice[sl] = slice_total_d(sh.wtot);
+                    sh.slice[sl] = slice_total_fx(sh.wtot);
                 __syncthreads();
             }
         }
         if (warp == 0) {
-            const double Rt = warp_total_slices(sh.slice, S, lane);
+            const fx_t Rt = warp_total_slices(sh.slice, S, lane);
             int cs;
-            double x1;
-            warp_find_slice(sh.slice, S, __dmul_rn((double)sq.uN, Rt), lane, cs, x1);
+            fx_t x1;
+            warp_find_slice(sh.slice, S, fx_scale(sq.uN, Rt), lane, cs, x1);
             if (lane == 0) {
-                sh.retry = (Rt == 0.0 && sq.res_mode == RES_DIFF) ? 1 : 0;
+                sh.retry = (Rt == 0ull && sq.res_mode == RES_DIFF) ? 1 : 0;
                 sh.sstar = cs;
                 sh.x1 = x1;
             }
@@ -1637,13 +1669,13 @@ __device__ int draw_token(PickShared &sh, SeqSample &sq, const uint4 *tsrc, cons
     return pick_in_slice<VE>(sh.ps, ss, part, r, sh.x1, NV);
 }
 
-// Slice sl's mass: its 8 warp shares (left by kernel B) added in warp order, in double.
-__device__ __forceinline__ double slice_share_total(const float *shares, int sl)
+// Slice sl's mass: its 8 warp shares (left by kernel B), in fixed point.
+__device__ __forceinline__ fx_t slice_share_total(const float *shares, int sl)
 {
     const float4 a = __ldcg(reinterpret_cast<const float4 *>(shares + (size_t)sl * kConsWarps));
     const float4 c = __ldcg(reinterpret_cast<const float4 *>(shares + (size_t)sl * kConsWarps + 4));
     const float w8[kConsWarps] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
-    return slice_total_d(w8);
+    return slice_total_fx(w8);
 }
 
 template <int DT>
@@ -1661,7 +1693,7 @@ __global__ void __launch_bounds__(kPickThreads) sv_pick_kernel(const SvParams p)
     const int my_tok = (tid < N) ? p.tokens[(size_t)b * N + tid] : -1;  // for the outputs
     // slice tid's mass, loaded alongside the sequence's statistics (used only if it is sampled)
     const float *shares = p.ws_slice + (size_t)b * S * kConsWarps;
-    const double my_mass = (tid < S) ? slice_share_total(shares, tid) : 0.0;
+    const fx_t my_mass = (tid < S) ? slice_share_total(shares, tid) : 0ull;
     SeqSample sq{};
     const bool sampled = sequence_sample(p, b, sq, /*with_cf=*/false);  // sq.cf holds T
     if (tid == 0)
@@ -1730,11 +1762,11 @@ struct CtlW {
     Ring<kStagesW> ring;
     uint32_t gcount[kWalkGroups];               // tiles each group has consumed in earlier passes
     float shares[kMaxWalkSlices * kConsWarps];  // warp shares of every slice of the current pass
-    double slice[kMaxWalkSlices];               // slice masses (double sums of their shares)
+    fx_t slice[kMaxWalkSlices];                 // slice masses (fixed-point sums of their shares)
     PickState ps;
     int kids[kMaxTreeNodes];
     int nkids, accept, sstar;
-    double Rt, x1;                              // total of the pass's slice masses; the pick's remainder
+    fx_t Rt, x1;                                // total of the pass's slice masses; the pick's remainder
     float cf;
     double cfd;                                 // log2(e) / T in double
     // the tree, fetched once: every decision of the walk reads shared memory
@@ -1900,14 +1932,14 @@ __device__ void walk_mass_pass(CtlW &w, unsigned char *ring, const uint4 *tsrc, 
         for (int q = 0; q < kConsWarps; ++q)
             w8[q] = (owner == rank) ? w.shares[sl * kConsWarps + q]
                                     : sv::ld_dsmem_f32(sv::dsmem_addr(&w.shares[sl * kConsWarps + q], owner));
-        w.slice[sl] = slice_total_d(w8);
+        w.slice[sl] = slice_total_fx(w8);
     }
     if (C > 1)
         sv::cluster_sync();  // no peer reads these shares any more: the next pass may overwrite them
     else
         __syncthreads();
     if (warp == 0) {
-        const double tot = warp_total_slices(w.slice, S, lane);
+        const fx_t tot = warp_total_slices(w.slice, S, lane);
         if (lane == 0)
             w.Rt = tot;
     }
@@ -1927,8 +1959,8 @@ __device__ int walk_pick(CtlW &w, const uint4 *tsrc, const uint4 *dsrc, int NV, 
     const int S = (NV + kSliceVecs - 1) / kSliceVecs;
     if (warp == 0) {
         int cs;
-        double x1;
-        warp_find_slice(w.slice, S, __dmul_rn((double)u, w.Rt), lane, cs, x1);
+        fx_t x1;
+        warp_find_slice(w.slice, S, fx_scale(u, w.Rt), lane, cs, x1);
         if (lane == 0) {
             w.sstar = cs;
             w.x1 = x1;
@@ -2129,7 +2161,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) sv_tree_walk_kernel(const SvP
                 }
                 const float c1 = __fadd_rn(c, Z);
                 walk_mass_pass<DT>(w, ring, tsrc, dsrc, NV, mq, isq, mp, isp, c1, cf);
-                const float R = (float)w.Rt;
+                const float R = fx_to_float(w.Rt);
                 if (R > 0.0f) {
                     c = c1;
                     Z = R;
