@@ -1784,22 +1784,25 @@ constexpr size_t kSmemW = ring_bytes(kStagesW) + sizeof(CtlW);
 static_assert(kSmemW <= 232448, "227 KiB of shared memory per CTA");
 
 // (q - c p)+ (use_p) or q for the VE elements of one 16-byte vector, with
-// q = 2^((zq - mq) cf) / Sq and p = 2^((zp - mp) cf) / Sp, each rounded, then
-// q - c p = fma(p, -c, q) (one rounding: at c = 1 exactly kernel B's q - p, so
-// a chain-shaped tree samples as the chain does).  Pairs of adjacent elements
-// travel as one f32x2; every operation rounds to nearest, so the walk's passes
-// and the recomputation of the chosen slice agree bit for bit.
+// q = 2^(zq cf - Kq) * Iq and p = 2^(zp cf - Kp) * Ip in residual_vec's form
+// (shifts and scales from residual_shift), and q - c p = fma(2^(..), Iq,
+// 2^(..) * (-c Ip)) in one rounding: at c = 1, -c Ip = -Ip exactly and this is
+// kernel B's q - p bit for bit, so a chain-shaped tree samples as the chain
+// does.  Pairs of adjacent elements travel as one f32x2; every operation
+// rounds to nearest, so the walk's passes and the recomputation of the chosen
+// slice agree bit for bit.
 template <int DT>
-__device__ __forceinline__ void tree_vec(const uint4 vt, const uint4 vd, bool use_p, float mq, float isq, float mp,
-                                         float isp, float c, float cf, float *r)
+__device__ __forceinline__ void tree_vec(const uint4 vt, const uint4 vd, bool use_p, float Kq, float Iq_, float Kp,
+                                         float Ip_, float c, float cf, float *r)
 {
     constexpr int NE = Elt<DT>::kPerVec;
     constexpr int NP = NE / 2;
     const uint32_t wt[4] = {vt.x, vt.y, vt.z, vt.w};
     const uint32_t wd[4] = {vd.x, vd.y, vd.z, vd.w};
     const unsigned long long Cf = sv::pack2(cf, cf);
-    const unsigned long long Mq = sv::pack2(mq, mq), Iq = sv::pack2(isq, isq);
-    const unsigned long long Mp = sv::pack2(mp, mp), Ip = sv::pack2(isp, isp), Nc = sv::pack2(-c, -c);
+    const unsigned long long NKq = sv::pack2(-Kq, -Kq), Iq = sv::pack2(Iq_, Iq_);
+    const float ncp = -__fmul_rn(c, Ip_);  // -c / Sp' (exactly -Ip_ at c = 1)
+    const unsigned long long NKp = sv::pack2(-Kp, -Kp), NcIp = sv::pack2(ncp, ncp);
 #pragma unroll
     for (int e = 0; e < NP; ++e) {
         unsigned long long zt, zd;
@@ -1811,16 +1814,17 @@ __device__ __forceinline__ void tree_vec(const uint4 vt, const uint4 vd, bool us
             zd = sv::pack2(__uint_as_float(wd[2 * e]), __uint_as_float(wd[2 * e + 1]));
         }
         float a0, a1;
-        sv::unpack2(sv::mul2(sv::sub2(zt, Mq), Cf), a0, a1);
-        const unsigned long long x = sv::mul2(sv::pack2(sv::ex2(a0), sv::ex2(a1)), Iq);
+        sv::unpack2(sv::fma2(zt, Cf, NKq), a0, a1);
+        const unsigned long long eq = sv::pack2(sv::ex2(a0), sv::ex2(a1));
         if (use_p) {
-            sv::unpack2(sv::mul2(sv::sub2(zd, Mp), Cf), a0, a1);
+            sv::unpack2(sv::fma2(zd, Cf, NKp), a0, a1);
+            const unsigned long long ncp_k = sv::mul2(sv::pack2(sv::ex2(a0), sv::ex2(a1)), NcIp);  // -c p
             float d0, d1;
-            sv::unpack2(sv::fma2(sv::mul2(sv::pack2(sv::ex2(a0), sv::ex2(a1)), Ip), Nc, x), d0, d1);
+            sv::unpack2(sv::fma2(eq, Iq, ncp_k), d0, d1);
             r[2 * e] = fmaxf(d0, 0.0f);
             r[2 * e + 1] = fmaxf(d1, 0.0f);
         } else {
-            sv::unpack2(x, r[2 * e], r[2 * e + 1]);
+            sv::unpack2(sv::mul2(eq, Iq), r[2 * e], r[2 * e + 1]);
         }
     }
 }
@@ -1847,7 +1851,7 @@ __device__ __forceinline__ uint32_t walk_parity(uint32_t k) { return (k / kStage
 
 template <int DT>
 __device__ void walk_mass_pass(CtlW &w, unsigned char *ring, const uint4 *tsrc, const uint4 *dsrc,
-                               int NV, float mq, float isq, float mp, float isp, float c, float cf)
+                               int NV, float Kq, float Iq, float Kp, float Ip, float c, float cf)
 {
     constexpr int VE = Elt<DT>::kPerVec;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1900,8 +1904,8 @@ __device__ void walk_mass_pass(CtlW &w, unsigned char *ring, const uint4 *tsrc, 
                         float r[VE];
                         const uint4 vd = dsrc ? reinterpret_cast<const uint4 *>(stage + kTileBytes)[sv_]
                                               : make_uint4(0, 0, 0, 0);
-                        tree_vec<DT>(reinterpret_cast<const uint4 *>(stage)[sv_], vd, dsrc != nullptr, mq, isq, mp,
-                                     isp, c, cf, r);
+                        tree_vec<DT>(reinterpret_cast<const uint4 *>(stage)[sv_], vd, dsrc != nullptr, Kq, Iq, Kp,
+                                     Ip, c, cf, r);
 #pragma unroll
                         for (int e = 0; e < VE; ++e)
                             part = __fadd_rn(part, r[e]);
@@ -1951,8 +1955,8 @@ __device__ void walk_mass_pass(CtlW &w, unsigned char *ring, const uint4 *tsrc, 
 // dsrc is given, else q) the warp, lane and element.  Every thread calls it;
 // returns the token.
 template <int DT>
-__device__ int walk_pick(CtlW &w, const uint4 *tsrc, const uint4 *dsrc, int NV, float mq, float isq, float mp,
-                         float isp, float c, float cf, float u)
+__device__ int walk_pick(CtlW &w, const uint4 *tsrc, const uint4 *dsrc, int NV, float Kq, float Iq, float Kp,
+                         float Ip, float c, float cf, float u)
 {
     constexpr int VE = Elt<DT>::kPerVec;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1976,7 +1980,7 @@ __device__ int walk_pick(CtlW &w, const uint4 *tsrc, const uint4 *dsrc, int NV, 
     const int vec = ss * kSliceVecs + tid;
     if (tid < kConsThreads && vec < NV) {
         const uint4 vd = dsrc ? __ldcg(dsrc + vec) : make_uint4(0, 0, 0, 0);
-        tree_vec<DT>(__ldcg(tsrc + vec), vd, dsrc != nullptr, mq, isq, mp, isp, c, cf, r);
+        tree_vec<DT>(__ldcg(tsrc + vec), vd, dsrc != nullptr, Kq, Iq, Kp, Ip, c, cf, r);
 #pragma unroll
         for (int e = 0; e < VE; ++e)
             part = __fadd_rn(part, r[e]);
@@ -2106,6 +2110,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1) sv_tree_walk_kernel(const SvP
             const float *st = w.st + n * 4;
             const float mq = st[0], Sq = st[1], mp = st[2], Sp = st[3];
             const float isq = 1.0f / Sq;
+            float Kq, Iq, Kp = 0.0f, Ip = 0.0f;  // the passes' shifts and scales (residual_shift)
+            residual_shift(mq, Sq, cf, Kq, Iq);
             const uint4 *tsrc = static_cast<const uint4 *>(p.target) + (row0 + n) * (size_t)NV;
             const uint4 *dsrc = static_cast<const uint4 *>(p.draft) + (row0 + n) * (size_t)NV;
             // children of n, in index order
@@ -2125,6 +2131,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1) sv_tree_walk_kernel(const SvP
             __syncthreads();
             const int nk = w.nkids;
             const float isp = nk ? 1.0f / Sp : 0.0f;
+            if (nk)
+                residual_shift(mp, Sp, cf, Kp, Ip);
             // After k rejections with a non-empty residual, r_k = (q - c p)+ / Z:
             // r_0 = q (c = 0, Z = 1), and (r_k - p)+ = (q - (c + Z) p)+ / Z, so a
             // rejection moves c to c + Z and Z to the new pass's total (both
@@ -2160,7 +2168,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) sv_tree_walk_kernel(const SvP
                     break;
                 }
                 const float c1 = __fadd_rn(c, Z);
-                walk_mass_pass<DT>(w, ring, tsrc, dsrc, NV, mq, isq, mp, isp, c1, cf);
+                walk_mass_pass<DT>(w, ring, tsrc, dsrc, NV, Kq, Iq, Kp, Ip, c1, cf);
                 const float R = fx_to_float(w.Rt);
                 if (R > 0.0f) {
                     c = c1;
@@ -2184,8 +2192,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1) sv_tree_walk_kernel(const SvP
             // the token: from r_k = (q - c p)+ / Z, by inverse CDF over its slice masses
             const uint4 *dk = (c > 0.0f) ? dsrc : nullptr;
             if (!masses_ready)
-                walk_mass_pass<DT>(w, ring, tsrc, dk, NV, mq, isq, mp, isp, c, cf);
-            const int t = walk_pick<DT>(w, tsrc, dk, NV, mq, isq, mp, isp, c, cf, u0);
+                walk_mass_pass<DT>(w, ring, tsrc, dk, NV, Kq, Iq, Kp, Ip, c, cf);
+            const int t = walk_pick<DT>(w, tsrc, dk, NV, Kq, Iq, Kp, Ip, c, cf, u0);
             if (tid == 0 && leader)
                 out[depth] = t;
             break;
