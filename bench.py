@@ -34,9 +34,13 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "row_normaliser_traffic.txt")
 def dominant_kernel(w, num_sms: int) -> str:
     """The kernel that streams all B(2N+1) logit rows (row normalisers and
     accept tests): one CTA per logit row (sv_row_kernel) from a full wave of
-    positions (four CTAs per SM), else one CTA or cluster per position
-    (sv_rows_kernel)."""
-    return "sv_row_kernel" if w.B * (w.N + 1) >= 4 * num_sms else "sv_rows_kernel"
+    positions (four CTAs per SM), and from two CTAs per SM for batches of at
+    most 1024 sequences (the rows that are read packed at the front of the
+    grid), else one CTA or cluster per position (sv_rows_kernel)."""
+    units = w.B * (w.N + 1)
+    if units >= 4 * num_sms or (units >= 2 * num_sms and w.B <= 1024):
+        return "sv_row_kernel"
+    return "sv_rows_kernel"
 L2_BYTES = 129 * 10**6  # GB300 L2
 
 

@@ -54,6 +54,7 @@ constexpr int kStagesA = 3;                  // ring depth of the row kernel
 __host__ __device__ constexpr int ring_bytes(int stages) { return stages * 2 * kTileBytes; }
 constexpr int kMaxSlices = 128;              // slices per chunk (512 KiB of one row)
 constexpr int kMaxCluster = 16;
+constexpr int kPackMaxB = 1024;              // sequences whose sampled flags one warp holds (32 per lane)
 constexpr int kProfRuns = 4096;  // runs whose kernel times one profiling session keeps
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait, then give up
 
@@ -890,8 +891,10 @@ __global__ void __launch_bounds__(kThreads, 4) sv_rows_kernel(const SvParams p)
 // decides with kernel A's arithmetic.  Units run position by position in
 // descending order (position 0 last, as in kernel A), a sequence's two rows
 // next to each other; a draft-row unit of a greedy sequence (or of a tree node
-// without children) reads nothing and leaves.
-template <int DT, bool TREE>
+// without children) reads nothing and leaves.  PACKED (chains of at most
+// kPackMaxB sequences): the rows that are read take the front of the grid,
+// and no block is spent on a draft row that is not read.
+template <int DT, bool TREE, bool PACKED = false>
 __global__ void __launch_bounds__(kThreads, 4) sv_row_kernel(const SvParams p)
 {
     constexpr int VE = Elt<DT>::kPerVec;
@@ -917,6 +920,48 @@ __global__ void __launch_bounds__(kThreads, 4) sv_row_kernel(const SvParams p)
             i = N;
             b = u;
             is_draft = 0;
+        } else if (PACKED) {
+            // The B(N+1) target rows first (positions in descending order),
+            // then the draft rows of the nS sampled sequences at positions
+            // N-1 .. 0; blocks past the last of them leave.  A draft block's
+            // warps each read the sampled flags of all sequences (lane w holds
+            // those of sequences 32w .. 32w + 31) and map the block themselves.
+            if (u < B * (N + 1)) {
+                const int pos = u / B;
+                i = N - pos;
+                b = u - pos * B;
+                is_draft = 0;
+            } else {
+                uint32_t word = 0;
+                if (lane * 32 < B) {
+                    float Tb;
+#pragma unroll 8
+                    for (int k = 0; k < 32; ++k) {
+                        const int bb = lane * 32 + k;
+                        if (bb < B && sequence_mode(p, bb, Tb) == MODE_SAMPLED)
+                            word |= 1u << k;
+                    }
+                }
+                int cum = __popc(word);  // inclusive prefix over lanes
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const int o = __shfl_up_sync(0xffffffffu, cum, off);
+                    if (lane >= off)
+                        cum += o;
+                }
+                const int nS = __shfl_sync(0xffffffffu, cum, 31);
+                const int v = u - B * (N + 1);
+                if (v >= N * nS)
+                    return;  // uniform over the CTA
+                const int pos = v / nS, k = v - pos * nS;  // k-th sampled sequence
+                i = N - 1 - pos;
+                const int w = __ffs(__ballot_sync(0xffffffffu, cum > k)) - 1;  // its word
+                uint32_t m = __shfl_sync(0xffffffffu, word, w);
+                for (int rem = k - (__shfl_sync(0xffffffffu, cum, w) - __popc(m)); rem > 0; --rem)
+                    m &= m - 1;
+                b = w * 32 + __ffs(m) - 1;
+                is_draft = 1;
+            }
         } else {
             const int v = u - B, pos = v / (2 * B), w = v - pos * (2 * B);
             i = N - 1 - pos;
@@ -962,9 +1007,16 @@ __global__ void __launch_bounds__(kThreads, 4) sv_row_kernel(const SvParams p)
         }
     }
     const bool decides = !TREE && mode == MODE_SAMPLED && i < N;  // a two-row position of the chain
+    // The decision's inputs, loaded by an idle lane of the producer warp and
+    // parked in shared memory after the stream.  In a packed (one-wave) grid
+    // they are loaded while the row streams, so that no block starts its
+    // stream late; in larger grids a block's late start is covered by the
+    // others on its SM, and loading them before the stream measured 0.4 %
+    // faster (headline kernel A 173.1 -> 172.4 us).
     const bool prefetcher = tid == 32 * kProducerWarp + 1;
+    const bool prefetch = prefetcher && decides && !bad_d;
     float pre_zq = 0.0f, pre_zp = 0.0f, pre_u = 0.0f;
-    if (prefetcher && decides && !bad_d) {
+    if (prefetch && !PACKED) {
         pre_zq = logit_at<DT>(p.target, trow * (size_t)V + d);
         pre_zp = logit_at<DT>(p.draft, drow * (size_t)V + d);
         pre_u = p.u[trow];
@@ -972,6 +1024,11 @@ __global__ void __launch_bounds__(kThreads, 4) sv_row_kernel(const SvParams p)
     __syncthreads();
     if (is_draft && (mode != MODE_SAMPLED || !ctl.has_child))
         return;  // no draft row is read (uniform over the CTA)
+    if (prefetch && PACKED) {
+        pre_zq = logit_at<DT>(p.target, trow * (size_t)V + d);
+        pre_zp = logit_at<DT>(p.draft, drow * (size_t)V + d);
+        pre_u = p.u[trow];
+    }
     const float cf = ctl.cf;
     const int NV = V / VE;
     const uint4 *src = static_cast<const uint4 *>(is_draft ? p.draft : p.target) + (is_draft ? drow : trow) * (size_t)NV;
@@ -2444,6 +2501,8 @@ template <int DT> cudaError_t set_attrs()
     if (e == cudaSuccess)
         e = set_kernel_attrs(sv_row_kernel<DT, false>, kSmemA);
     if (e == cudaSuccess)
+        e = set_kernel_attrs(sv_row_kernel<DT, false, true>, kSmemA);
+    if (e == cudaSuccess)
         e = set_kernel_attrs(sv_row_kernel<DT, true>, kSmemA);
     if (e == cudaSuccess)
         e = set_kernel_attrs(sv_rows_kernel<DT, true>, kSmemA);
@@ -2596,7 +2655,7 @@ sv_status run_impl(spec_verify_ctx *ctx, const void *target, const void *draft, 
     if (!guard.ok)
         return SV_ERR_CUDA;
 
-    SvParams prm;
+    SvParams prm{};
     prm.target = target;
     prm.draft = greedy ? nullptr : draft;
     prm.tokens = tokens;
@@ -2634,14 +2693,23 @@ sv_status run_impl(spec_verify_ctx *ctx, const void *target, const void *draft, 
         cudaEventRecord(ev[0], st);
     cudaLaunchAttribute attr[2];
     cudaError_t e;
-    if (CA == 1 && units >= ctx->clusters_a[1]) {
-        // at least a wave of positions: one CTA per logit row (B target rows at
-        // position N, two rows at the others).  Measured on GB300: headline
-        // 212.3 -> 209.1 us per call, stress 682.3 -> 672.4 us; a one-wave mixed
-        // batch (384 positions) 58.8 -> 63.0 us, so it keeps a CTA per position.
+    const bool wave = CA == 1 && units >= ctx->clusters_a[1];
+    const bool packed = CA == 1 && !wave && units >= 2LL * ctx->num_sms && B <= kPackMaxB;
+    if (wave || packed) {
+        // One CTA per logit row (B target rows at position N, two rows at the
+        // others).  Measured on GB300: headline 212.3 -> 209.1 us per call,
+        // stress 682.3 -> 672.4 us.  Below a wave of positions the rows that
+        // are read are packed at the front of the grid, target rows first, so
+        // that they all start in the first wave and without a dependent load
+        // (mixed batch, 384 positions: 38.4 -> 35.5 us against kernel A's CTA
+        // per position; batches of tiny rows keep kernel A, 10.5 against 12.5 us).
         cudaLaunchConfig_t cfg = launch_config((unsigned)(B * (2LL * N + 1)), 1, kSmemA, st, attr);
-        e = (ctx->dtype == SV_BF16) ? cudaLaunchKernelEx(&cfg, sv_row_kernel<SV_BF16, false>, prm)
-                                    : cudaLaunchKernelEx(&cfg, sv_row_kernel<SV_F32, false>, prm);
+        if (packed)
+            e = (ctx->dtype == SV_BF16) ? cudaLaunchKernelEx(&cfg, sv_row_kernel<SV_BF16, false, true>, prm)
+                                        : cudaLaunchKernelEx(&cfg, sv_row_kernel<SV_F32, false, true>, prm);
+        else
+            e = (ctx->dtype == SV_BF16) ? cudaLaunchKernelEx(&cfg, sv_row_kernel<SV_BF16, false>, prm)
+                                        : cudaLaunchKernelEx(&cfg, sv_row_kernel<SV_F32, false>, prm);
     } else {
         cudaLaunchConfig_t cfg = launch_config((unsigned)(units * CA), CA, kSmemA, st, attr);
         e = (ctx->dtype == SV_BF16) ? cudaLaunchKernelEx(&cfg, sv_rows_kernel<SV_BF16, false>, prm)
@@ -2714,7 +2782,7 @@ sv_status tree_run_impl(spec_verify_ctx *ctx, const void *target, const void *dr
     if (!guard.ok)
         return SV_ERR_CUDA;
 
-    SvParams prm;
+    SvParams prm{};
     memset(&prm, 0, sizeof prm);
     prm.target = target;
     prm.draft = greedy ? nullptr : draft;
@@ -2862,7 +2930,7 @@ sv_status fused_run_impl(spec_verify_ctx *ctx, const void *ht, const void *wt, i
             return r;
     }
 
-    SvParams prm;
+    SvParams prm{};
     memset(&prm, 0, sizeof prm);
     prm.target = ctx->fz_lt;
     prm.draft = ctx->fz_ld;

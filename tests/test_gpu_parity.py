@@ -104,6 +104,40 @@ def test_parity_one_row_per_cta(dtype, T):
     assert ctx.status() == sv.SV_OK
 
 
+@pytest.mark.parametrize("dtype,T,greedy", [("bf16", (0.0, 0.7, 1.0), False), ("f32", 0.9, False),
+                                             ("bf16", 1.0, True)])
+def test_parity_packed_rows(dtype, T, greedy):
+    """Between two CTAs per SM and a wave of positions (64 sequences x 6
+    positions on 152 SMs) the row kernel takes one CTA per row and packs the
+    rows it reads at the front of its grid: every target row, then the draft
+    rows of the sampled sequences only.  Every sequence against the oracle:
+    greedy and sampled sequences side by side with an invalid temperature, a
+    bad token and a NaN among them; all sampled in float32 (more rows than a
+    wave); and the greedy flag with no draft logits (no draft rows at all)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    w = synth.make_workload("mixed", seed=41, device="cuda", B=64, N=5, V=8192 if dtype == "bf16" else 4096,
+                            dtype=dtype, T=T)
+    assert 2 * sms <= w.B * (w.N + 1) < 4 * sms
+    ctx = _ctx(w)
+    assert ctx.cluster_size(w.B, w.N) == 1
+    if greedy:
+        rep = _check(w, ctx=ctx, greedy=True)
+        assert rep["exact"] == rep["sequences"] == w.B
+        return
+    w.draft_tokens[5, 1] = w.V + 3        # bad token
+    w.draft[9, 2, 11] = float("nan")      # NaN in a draft row
+    w.temperature[9] = 1.0                # a sampled sequence, so that its draft rows are read
+    w.temperature[12] = float("nan")      # invalid temperature
+    gpu = parity.run_gpu(ctx, w)
+    orc = parity.run_oracle(w, threads=THREADS)
+    rep = parity.compare(w, gpu, orc)
+    print(w.name, dtype, rep)
+    assert rep["sequences"] == w.B and rep["band_mismatch"] <= 1
+    assert gpu["num_accepted"][5] == -1 and gpu["num_accepted"][9] == -1 and gpu["num_accepted"][12] == -1
+    assert ctx.status() in (sv.SV_ERR_BAD_TOKEN, sv.SV_ERR_BAD_VALUE)
+    assert ctx.status() == sv.SV_OK
+
+
 @pytest.mark.parametrize("name", ["headline", "stress"])
 def test_parity_full_size_every_sequence(name):
     """The full-size launch the benchmark times (headline: 256 sequences x 15
