@@ -1817,13 +1817,15 @@ constexpr int kMaxWalkCluster = 4;          // CTAs (SMs) that share one tree's 
 // would then match the phase before it, and the wait would return early.)
 struct CtlW {
     Ring<kStagesW> ring;
-    uint32_t gcount[kWalkGroups];               // tiles each group has consumed in earlier passes
     float shares[kMaxWalkSlices * kConsWarps];  // warp shares of every slice of the current pass
-    fx_t slice[kMaxWalkSlices];                 // slice masses (fixed-point sums of their shares)
+    fx_t slice[kMaxWalkSlices];                 // slice masses (fixed-point sums of their shares): this
+                                                // CTA's slices after a pass, every slice in the pick
+    fx_t rsum[3];                               // a pass's total, added up by every CTA of the
+                                                // cluster into each CTA's copy; slot = pass % 3
     PickState ps;
     int kids[kMaxTreeNodes];
     int nkids, accept, sstar;
-    fx_t Rt, x1;                                // total of the pass's slice masses; the pick's remainder
+    fx_t x1;                                    // the pick's remainder
     float cf;
     double cfd;                                 // log2(e) / T in double
     // the tree, fetched once: every decision of the walk reads shared memory
@@ -1893,22 +1895,35 @@ __device__ __forceinline__ int walk_tile(int i, uint32_t rank, uint32_t C)
     return (int)(((uint32_t)(i / kWalkGroups) * C + rank) * kWalkGroups) + i % kWalkGroups;
 }
 
+// gcount[grp] without indexing a register array by a run-time value.
+__device__ __forceinline__ uint32_t group_count(const uint32_t (&gcount)[kWalkGroups], int grp)
+{
+    static_assert(kWalkGroups == 3, "one select per group");
+    return grp == 0 ? gcount[0] : (grp == 1 ? gcount[1] : gcount[2]);
+}
+
+// The CTA of the cluster that streams slice sl (in tile sl / kVPT).
+__device__ __forceinline__ uint32_t walk_slice_owner(int sl, uint32_t C)
+{
+    return (uint32_t)((sl / kVPT) / kWalkGroups) % C;
+}
+
 // One pass over the row pair of a node: the slice masses of (q - c p)+
-// (use_p) or q into w.slice, their total into w.Rt.  Every thread
-// of every CTA of the cluster calls it; g is this CTA's ring position,
-// advanced by the pass.  Each CTA streams its share of the tiles, writes the
-// warp shares of those slices into its own shared memory, and after a cluster
-// barrier every CTA adds up every slice (reading the peers' shares over
-// distributed shared memory) in the same order, so all of them hold the same
-// slice masses and total.
+// (use_p) or q; returns their total.  Every thread of every CTA of the
+// cluster calls it.  Each CTA streams its share of the tiles, writes the warp
+// shares of those slices into its own shared memory, totals its own slices
+// into w.slice (fixed point) and their sum into w.rpart; after a cluster
+// barrier every CTA adds up the C partials, so all of them return the same
+// total (the pick gathers the peers' slices once, at the end).
 // Ring stage and phase parity of the k-th tile (counted over every pass) of
 // consumer group grp.
 __device__ __forceinline__ uint32_t walk_stage(int grp, uint32_t k) { return (uint32_t)grp * kStagesG + k % kStagesG; }
 __device__ __forceinline__ uint32_t walk_parity(uint32_t k) { return (k / kStagesG) & 1u; }
 
 template <int DT>
-__device__ void walk_mass_pass(CtlW &w, unsigned char *ring, const uint4 *tsrc, const uint4 *dsrc,
-                               int NV, float Kq, float Iq, float Kp, float Ip, float c, float cf)
+__device__ fx_t walk_mass_pass(CtlW &w, unsigned char *ring, const uint4 *tsrc, const uint4 *dsrc, int NV,
+                               float Kq, float Iq, float Kp, float Ip, float c, float cf,
+                               uint32_t (&gcount)[kWalkGroups], int &npass)
 {
     constexpr int VE = Elt<DT>::kPerVec;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1918,6 +1933,11 @@ __device__ void walk_mass_pass(CtlW &w, unsigned char *ring, const uint4 *tsrc, 
     int n_own = 0;  // tiles this CTA streams: a prefix i = 0 .. n_own-1 of its sequence
     while (walk_tile(n_own, rank, C) < NT)
         ++n_own;
+    // The pass's total goes to slot npass % 3 of every CTA's rsum; the slot
+    // of the pass after next, read two barriers ago, is cleared here for it.
+    const int slot = npass % 3;
+    if (tid == 0)
+        w.rsum[(npass + 1) % 3] = 0ull;
     // pass tile i belongs to group i % kWalkGroups, as that group's tile
     // gcount[grp] + i / kWalkGroups; lane grp of the producer warp fills that
     // group's stages, so a slower group never holds up the others' copies
@@ -1925,7 +1945,7 @@ __device__ void walk_mass_pass(CtlW &w, unsigned char *ring, const uint4 *tsrc, 
         if (lane < kWalkGroups) {
             const int grp = lane;
             for (int i = grp; i < n_own; i += kWalkGroups) {
-                const uint32_t k = w.gcount[grp] + (uint32_t)(i / kWalkGroups);
+                const uint32_t k = group_count(gcount, grp) + (uint32_t)(i / kWalkGroups);
                 const uint32_t st = walk_stage(grp, k);
                 if (!sv::mbar_wait_bounded(&w.ring.empty[st], walk_parity(k) ^ 1u, &w.ring.abort, kWaitLimitNs)) {
                     w.ring.abort = 1;
@@ -1945,7 +1965,7 @@ __device__ void walk_mass_pass(CtlW &w, unsigned char *ring, const uint4 *tsrc, 
         __syncwarp();
     } else {
         const int grp = warp / kConsWarps, lt = tid - grp * kConsThreads, lw = warp - grp * kConsWarps;
-        const uint32_t gbase = w.gcount[grp];
+        const uint32_t gbase = group_count(gcount, grp);
         for (int i = grp; i < n_own; i += kWalkGroups) {
             const uint32_t k = gbase + (uint32_t)(i / kWalkGroups);
             const uint32_t st = walk_stage(grp, k);
@@ -1979,32 +1999,37 @@ __device__ void walk_mass_pass(CtlW &w, unsigned char *ring, const uint4 *tsrc, 
             if (lane == 0)
                 sv::mbar_arrive(&w.ring.empty[st]);
         }
+        // The warp's shares of this pass in fixed point, one per lane (the
+        // j-th share the warp wrote: tile j / kVPT of its group, slot j %
+        // kVPT).  Fixed-point sums are exact: whatever the order of these
+        // additions, every CTA ends with the same total, the sum of all
+        // slice masses.
+        __syncwarp();
+        fx_t acc = 0ull;
+        for (int j = lane; j < ((n_own - grp + kWalkGroups - 1) / kWalkGroups) * kVPT; j += 32) {
+            const int sl = walk_tile(grp + (j / kVPT) * kWalkGroups, rank, C) * kVPT + j % kVPT;
+            if (sl < S)
+                acc += fx_of(w.shares[sl * kConsWarps + lw]);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (lane == 0 && acc != 0ull) {
+            if (C > 1)
+                for (uint32_t r = 0; r < C; ++r)
+                    sv::red_add_dsmem_u64(sv::dsmem_addr(&w.rsum[slot], r), acc);
+            else
+                atomicAdd(&w.rsum[slot], acc);
+        }
     }
+    for (int grp = 0; grp < kWalkGroups; ++grp)  // every thread keeps the counts
+        gcount[grp] += (n_own > grp) ? (uint32_t)((n_own - grp + kWalkGroups - 1) / kWalkGroups) : 0u;
     if (C > 1)
-        sv::cluster_sync();  // every CTA's shares are visible cluster-wide
+        sv::cluster_sync();  // the additions into every CTA's slot are complete and visible
     else
         __syncthreads();
-    if (tid == 0)  // every thread read the counts before the barrier; the next pass reads them after the last one
-        for (int grp = 0; grp < kWalkGroups; ++grp)
-            w.gcount[grp] += (n_own > grp) ? (uint32_t)((n_own - grp + kWalkGroups - 1) / kWalkGroups) : 0u;
-    for (int sl = tid; sl < S; sl += kWalkThreads) {
-        const uint32_t owner = (uint32_t)((sl / kVPT) / kWalkGroups) % C;
-        float w8[kConsWarps];
-        for (int q = 0; q < kConsWarps; ++q)
-            w8[q] = (owner == rank) ? w.shares[sl * kConsWarps + q]
-                                    : sv::ld_dsmem_f32(sv::dsmem_addr(&w.shares[sl * kConsWarps + q], owner));
-        w.slice[sl] = slice_total_fx(w8);
-    }
-    if (C > 1)
-        sv::cluster_sync();  // no peer reads these shares any more: the next pass may overwrite them
-    else
-        __syncthreads();
-    if (warp == 0) {
-        const fx_t tot = warp_total_slices(w.slice, S, lane);
-        if (lane == 0)
-            w.Rt = tot;
-    }
-    __syncthreads();
+    ++npass;
+    return w.rsum[slot];
 }
 
 // Inverse CDF over the slice masses in w.slice (total w.Rt) at u: the slice,
@@ -2013,15 +2038,33 @@ __device__ void walk_mass_pass(CtlW &w, unsigned char *ring, const uint4 *tsrc, 
 // returns the token.
 template <int DT>
 __device__ int walk_pick(CtlW &w, const uint4 *tsrc, const uint4 *dsrc, int NV, float Kq, float Iq, float Kp,
-                         float Ip, float c, float cf, float u)
+                         float Ip, float c, float cf, float u, fx_t Rt)
 {
     constexpr int VE = Elt<DT>::kPerVec;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t C = sv::cluster_nctarank(), rank = sv::cluster_ctarank();
     const int S = (NV + kSliceVecs - 1) / kSliceVecs;
+    // The slice masses of the last pass: each CTA totals its own slices from
+    // its warp shares, then reads the peers' (after the barrier that makes
+    // them visible; after the second no CTA reads another's memory).
+    for (int sl = tid; sl < S; sl += kWalkThreads)
+        if (walk_slice_owner(sl, C) == rank)
+            w.slice[sl] = slice_total_fx(&w.shares[sl * kConsWarps]);
+    if (C > 1) {
+        sv::cluster_sync();
+        for (int sl = tid; sl < S; sl += kWalkThreads) {
+            const uint32_t owner = walk_slice_owner(sl, C);
+            if (owner != rank)
+                w.slice[sl] = sv::ld_dsmem_u64(sv::dsmem_addr(&w.slice[sl], owner));
+        }
+        sv::cluster_sync();
+    } else {
+        __syncthreads();
+    }
     if (warp == 0) {
         int cs;
         fx_t x1;
-        warp_find_slice(w.slice, S, fx_scale(u, w.Rt), lane, cs, x1);
+        warp_find_slice(w.slice, S, fx_scale(u, Rt), lane, cs, x1);
         if (lane == 0) {
             w.sstar = cs;
             w.x1 = x1;
@@ -2066,8 +2109,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1) sv_tree_walk_kernel(const SvP
     const int mode = sequence_mode(p, b, T);
     if (tid == 0) {
         ring_init(w.ring);
-        for (int grp = 0; grp < kWalkGroups; ++grp)
-            w.gcount[grp] = 0;
+        for (int k = 0; k < 3; ++k)
+            w.rsum[k] = 0ull;
         w.cfd = (mode == MODE_SAMPLED) ? kLog2e / (double)T : 0.0;
         w.cf = (float)w.cfd;
     }
@@ -2162,7 +2205,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1) sv_tree_walk_kernel(const SvP
     } else {
         const float cf = w.cf;
         const float u0 = w.u[0];
-        int n = 0;
+        int n = 0, npass = 0;                      // node; passes so far
+        uint32_t gcount[kWalkGroups] = {0u, 0u, 0u};  // tiles each consumer group has consumed
         for (;;) {
             const float *st = w.st + n * 4;
             const float mq = st[0], Sq = st[1], mp = st[2], Sp = st[3];
@@ -2196,7 +2240,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1) sv_tree_walk_kernel(const SvP
             // unchanged when that total is 0: r_k stays).
             float c = 0.0f, Z = 1.0f;
             int accepted = -1;
-            bool masses_ready = false;  // w.slice holds the masses of (q - c p)+
+            bool masses_ready = false;  // w.slice holds the masses of (q - c p)+, Rlast their total
+            fx_t Rlast = 0ull;
             for (int ci = 0; ci < nk; ++ci) {
                 const int ch = w.kids[ci];
                 if (tid == 0) {
@@ -2225,16 +2270,16 @@ __global__ void __launch_bounds__(kWalkThreads, 1) sv_tree_walk_kernel(const SvP
                     break;
                 }
                 const float c1 = __fadd_rn(c, Z);
-                walk_mass_pass<DT>(w, ring, tsrc, dsrc, NV, Kq, Iq, Kp, Ip, c1, cf);
-                const float R = fx_to_float(w.Rt);
+                const fx_t Rt = walk_mass_pass<DT>(w, ring, tsrc, dsrc, NV, Kq, Iq, Kp, Ip, c1, cf, gcount, npass);
+                const float R = fx_to_float(Rt);
                 if (R > 0.0f) {
+                    Rlast = Rt;
                     c = c1;
                     Z = R;
                     masses_ready = true;
                 } else {
                     masses_ready = false;  // the residual is empty: r_k stays
                 }
-                __syncthreads();  // every thread has read w.Rt before the next pass rewrites it
             }
             if (accepted >= 0) {
                 if (tid == 0 && leader) {
@@ -2249,8 +2294,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1) sv_tree_walk_kernel(const SvP
             // the token: from r_k = (q - c p)+ / Z, by inverse CDF over its slice masses
             const uint4 *dk = (c > 0.0f) ? dsrc : nullptr;
             if (!masses_ready)
-                walk_mass_pass<DT>(w, ring, tsrc, dk, NV, Kq, Iq, Kp, Ip, c, cf);
-            const int t = walk_pick<DT>(w, tsrc, dk, NV, Kq, Iq, Kp, Ip, c, cf, u0);
+                Rlast = walk_mass_pass<DT>(w, ring, tsrc, dk, NV, Kq, Iq, Kp, Ip, c, cf, gcount, npass);
+            const int t = walk_pick<DT>(w, tsrc, dk, NV, Kq, Iq, Kp, Ip, c, cf, u0, Rlast);
             if (tid == 0 && leader)
                 out[depth] = t;
             break;

@@ -154,6 +154,20 @@ __device__ __forceinline__ int ld_dsmem_s32(uint32_t a)
     return v;
 }
 
+// Adds v to the 64-bit word at cluster shared address a (this CTA's or a
+// peer's); a later cluster barrier makes the sum visible to its owner.
+__device__ __forceinline__ void red_add_dsmem_u64(uint32_t a, unsigned long long v)
+{
+    asm volatile("red.relaxed.cluster.shared::cluster.add.u64 [%0], %1;" ::"r"(a), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long ld_dsmem_u64(uint32_t a)
+{
+    unsigned long long v;
+    asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(a) : "memory");
+    return v;
+}
+
 // ---- arithmetic --------------------------------------------------------------
 // Packed pairs: two floats in one 64-bit register pair, and bf16x2 words.
 __device__ __forceinline__ unsigned long long pack2(float lo, float hi)
