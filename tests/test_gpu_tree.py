@@ -78,6 +78,31 @@ def test_tree_wide_siblings_exercise_many_residual_steps():
     assert rep["sibling_tests"] >= 24
 
 
+@pytest.mark.parametrize("name,over,seqs", [
+    # one CTA per tree (80 trees), 18 ring tiles a row
+    ("tree_small", {"B": 80, "M": 12, "V": 36864}, None),
+    # the benchmark's rows, two CTAs per tree (64 trees), 19-20 ring tiles a CTA
+    ("tree", {"M": 12, "topology": "random"}, [0, 5, 9, 21, 33, 40, 52, 63]),
+])
+def test_tree_wide_siblings_at_long_rows(name, over, seqs):
+    """Stars of 12 children with a draft far from the verifier, at row
+    lengths where every consumer group of the walk streams six or more ring
+    tiles per pass: several rejections in a row at one node, each a full
+    pass over its row pair through the same ring stages."""
+    w = synth.make_tree_workload(name, seed=13, device="cuda", sigma_q=3.0, **over)
+    w.parent[:] = 0
+    w.parent[:, 0] = -1
+    g = torch.Generator(device="cuda").manual_seed(13)
+    z = w.draft[:, 0].float()
+    for n in range(1, w.M + 1):
+        gum = -torch.log(torch.empty_like(z).exponential_(generator=g))
+        w.tokens[:, n] = torch.argmax(z + gum, dim=-1).to(torch.int32)
+    rep, gpu = _check(w, seqs=None if seqs is None else np.array(seqs))
+    print(name, rep)
+    assert rep["k_max"] >= 3  # three or more rejections at one node
+    assert rep["sibling_tests"] >= rep["sequences"]
+
+
 def test_tree_all_greedy_without_draft_logits():
     w = synth.make_tree_workload("tree_mixed", seed=2, device="cuda")
     rep, _ = _check(w, greedy=True)
