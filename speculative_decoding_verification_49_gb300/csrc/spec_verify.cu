@@ -3370,9 +3370,10 @@ void spec_verify_destroy(spec_verify_ctx *ctx)
 // spec_verify_run_noalloc runs the same kernels as spec_verify_run, but its
 // scratch lives in the file-scope array below instead of a context
 // workspace: per sequence the first-rejection slot and the error bits, per
-// verified position the greedy argmax and the row statistics (mq, Sq, mp,
-// Sp), per 4 KiB slice of a sampled row pair the eight warp shares of its
-// residual mass, and one status word.  The array is part of the module image: every GPU that
+// verified position the greedy argmax, the row statistics (mq, Sq, mp, Sp)
+// and the ticket that pairs the position's two row CTAs, per 4 KiB slice of
+// a sampled row pair the eight warp shares of its residual mass, and one
+// status word.  The array is part of the module image: every GPU that
 // loads this library holds it until the process exits, and nothing is ever
 // allocated for it.  Host code only sees a stand-in symbol for it, so the
 // device address is looked up once per device with cudaGetSymbolAddress.
