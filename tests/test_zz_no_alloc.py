@@ -6,9 +6,9 @@ whose host framework owns every allocation.  spec_verify_run_noalloc serves
 them with a fixed scratch array built into the library instead of a context
 workspace.  Here it must give the same tokens and accept counts as the
 context entry point, call after call on the one shared scratch (batches of
-different sizes and dtypes in a row, the full 256-sequence headline batch,
-and a batch exactly at the scratch's slice limit), and agree with the float64
-oracle outside its margin band.  The file name makes pytest collect it last.
+different sizes and dtypes in a row, the full 256-sequence headline batch, the
+mixed greedy/sampled batch, and a batch exactly at the scratch's slice limit),
+and agree with the float64 oracle outside its margin band.  The file name makes pytest collect it last.
 """
 import os
 
@@ -56,9 +56,10 @@ def test_noalloc_matches_the_context_entry_point_call_after_call():
     stream = torch.cuda.current_stream()
     # calls in a row on the same scratch: a larger batch, then a smaller one,
     # then float32 logits, then the full 256-sequence headline batch
-    # (256 x 75 residual slices), then the first batch again
+    # (256 x 75 residual slices), then the mixed greedy/sampled batch (one
+    # CTA per row, the rows read packed into one wave), then the first again
     cases = [("headline", 21, {"B": 24}), ("headline", 22, {"B": 9}), ("stress", 23, {"B": 40}),
-             ("headline", 24, {}), ("headline", 21, {"B": 24})]
+             ("headline", 24, {}), ("mixed", 26, {}), ("headline", 21, {"B": 24})]
     for name, seed, over in cases:
         w = synth.make_workload(name, seed=seed, device="cuda", **over)
         ctx = sv.SpecVerify(w.B, w.N, w.V, w.dtype)
