@@ -1056,30 +1056,38 @@ __global__ void __launch_bounds__(kThreads, 4) sv_row_kernel(const SvParams p)
             }
             __syncwarp();
         } else {
+            // Each thread takes its vectors of the stage into registers and the
+            // stage is released before the arithmetic, so that the next copy
+            // into it overlaps the arithmetic on this one (headline kernel A1
+            // 175.1 -> 174.6 us with the unchecked loads of full stages).
             for (int t = 0; t < nst; ++t) {
-                if (consume_wait(ctl.ring, t)) {
-                    const uint4 *stage = reinterpret_cast<const uint4 *>(ring + (t % kStages) * (2 * kTileBytes));
-                    if (mode == MODE_GREEDY) {
+                const bool ok = consume_wait(ctl.ring, t);
+                const uint4 *stage = reinterpret_cast<const uint4 *>(ring + (t % kStages) * (2 * kTileBytes));
+                uint4 v[2 * kVPT];
+                if (ok && (t + 1) * kStageVecs <= NV) {  // a full stage
 #pragma unroll
-                        for (int k = 0; k < 2 * kVPT; ++k) {
-                            const int sv_ = k * kSliceVecs + tid;
-                            const int vec = t * kStageVecs + sv_;
-                            if (vec < NV)
-                                argmax_add2<DT>(ga, stage[sv_], vec * VE);
-                        }
-                    } else {
-                        uint4 v[2 * kVPT];
-#pragma unroll
-                        for (int k = 0; k < 2 * kVPT; ++k) {
-                            const int sv_ = k * kSliceVecs + tid;
-                            v[k] = (t * kStageVecs + sv_ < NV) ? stage[sv_] : neg_inf_vec<DT>();
-                        }
-                        online_add_tile<DT, 2 * kVPT>(o2, v, cf);
-                    }
+                    for (int k = 0; k < 2 * kVPT; ++k)
+                        v[k] = stage[k * kSliceVecs + tid];
                 } else {
-                    ctl.ring.abort = 1;
+#pragma unroll
+                    for (int k = 0; k < 2 * kVPT; ++k) {
+                        const int sv_ = k * kSliceVecs + tid;
+                        v[k] = (ok && t * kStageVecs + sv_ < NV) ? stage[sv_] : neg_inf_vec<DT>();
+                    }
                 }
                 consume_release(ctl.ring, t, lane);
+                if (!ok) {
+                    ctl.ring.abort = 1;
+                } else if (mode == MODE_GREEDY) {
+#pragma unroll
+                    for (int k = 0; k < 2 * kVPT; ++k) {
+                        const int vec = t * kStageVecs + k * kSliceVecs + tid;
+                        if (vec < NV)
+                            argmax_add2<DT>(ga, v[k], vec * VE);
+                    }
+                } else {
+                    online_add_tile<DT, 2 * kVPT>(o2, v, cf);
+                }
             }
         }
     }
