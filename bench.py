@@ -363,11 +363,15 @@ def measure_fused(sv, torch, dev, stream, rank, steps=20, warmup=3, batch=0):
     """Times spec_verify_run_fused on the 256-sequence, 7-draft batch with
     Qwen-sized heads (V = 151936; verifier K = 3584, draft K = 896) against
     the unfused pipeline: cuBLAS (torch.matmul) writes bf16 logits, then
-    spec_verify_run verifies them.  The hidden states and weights (1.4 GB)
-    exceed L2; calls run back to back between two CUDA events."""
+    spec_verify_run verifies them.  The fused path runs both ways: keeping
+    the verifier rows' float32 logits (the default) and recomputing the
+    sampled verifier rows too (no logits in HBM).  The hidden states and weights (1.4 GB) exceed L2;
+    calls run back to back between two CUDA events."""
     import synth
     w = synth.make_fused_workload("fused", seed=rank, device=dev, **({"B": batch} if batch else {}))
     ctx = sv.SpecVerify(w.B, w.N, w.V, "f32", device=dev.index or 0)
+    ctx_r = sv.SpecVerify(w.B, w.N, w.V, "f32", device=dev.index or 0)
+    ctx_r.set_fused_logits(False)
     ctx_b = sv.SpecVerify(w.B, w.N, w.V, "bf16", device=dev.index or 0)
     out = torch.empty((w.B, w.N + 1), dtype=torch.int32, device=dev)
     nacc = torch.empty((w.B,), dtype=torch.int32, device=dev)
@@ -377,6 +381,10 @@ def measure_fused(sv, torch, dev, stream, rank, steps=20, warmup=3, batch=0):
     def fused():
         ctx.run_fused(w.target_hidden, w.target_weight, w.draft_hidden, w.draft_weight, w.draft_tokens, w.uniforms,
                       w.temperature, out_tokens=out, num_accepted=nacc, stream=stream)
+
+    def fused_recompute():
+        ctx_r.run_fused(w.target_hidden, w.target_weight, w.draft_hidden, w.draft_weight, w.draft_tokens,
+                        w.uniforms, w.temperature, out_tokens=out, num_accepted=nacc, stream=stream)
 
     def unfused():
         torch.matmul(w.target_hidden, w.target_weight.T, out=zt)
@@ -389,7 +397,8 @@ def measure_fused(sv, torch, dev, stream, rank, steps=20, warmup=3, batch=0):
         torch.matmul(w.draft_hidden, w.draft_weight.T, out=zd)
 
     res = {}
-    for name, fn in (("fused", fused), ("cublas_then_verify", unfused), ("cublas_gemms_alone", gemm_only)):
+    for name, fn in (("fused", fused), ("fused_recompute", fused_recompute), ("cublas_then_verify", unfused),
+                     ("cublas_gemms_alone", gemm_only)):
         for _ in range(warmup):
             fn()
         torch.cuda.synchronize(dev)
@@ -400,21 +409,26 @@ def measure_fused(sv, torch, dev, stream, rank, steps=20, warmup=3, batch=0):
         e1.record(stream)
         torch.cuda.synchronize(dev)
         res[name] = 1e3 * e0.elapsed_time(e1) / steps
-    if ctx.status() != sv.SV_OK or ctx_b.status() != sv.SV_OK:
+    if ctx.status() != sv.SV_OK or ctx_r.status() != sv.SV_OK or ctx_b.status() != sv.SV_OK:
         raise RuntimeError("device status set during the fused measurement")
     tc_peak, tc_kind = tensor_peak()
     tflops = w.flops / (res["fused"] * 1e-6) / 1e12
     ctx.close()
+    ctx_r.close()
     ctx_b.close()
     return {"workload": f"fused: B={w.B} N={w.N} V={w.V}, verifier K={w.Kt}, draft K={w.Kd}, bf16 hidden states and "
                         f"heads, T=0.8",
             "us_per_call": res["fused"], "verified_rows_per_s": w.B * (w.N + 1) / (res["fused"] * 1e-6),
             "unfused_us_per_call": res["cublas_then_verify"], "cublas_gemms_us": res["cublas_gemms_alone"],
             "speedup_vs_unfused": res["cublas_then_verify"] / res["fused"],
+            "logits": "every verifier row's float32 logits written by its statistics epilogue and the sampled rows "
+                      "read back; the sampled draft rows recomputed",
+            "recompute_us_per_call": res["fused_recompute"],
+            "recompute_speedup_vs_unfused": res["cublas_then_verify"] / res["fused_recompute"],
             "roofline": {"bound": "tensor", "achieved": tflops, "peak": tc_peak, "unit": "TFLOP/s",
                          "frac": tflops / tc_peak, "flops_per_call": w.flops,
                          "peak_kind": tc_kind},
-            "launches_per_call": 8, "steps": steps}
+            "launches_per_call": 7, "recompute_launches_per_call": 8, "steps": steps}
 
 
 def measure_fused_sweep(sv, torch, dev, stream, rank, batches=(32, 64, 128, 512)):
@@ -425,6 +439,8 @@ def measure_fused_sweep(sv, torch, dev, stream, rank, batches=(32, 64, 128, 512)
         r = measure_fused(sv, torch, dev, stream, rank, steps=10, warmup=2, batch=B)
         rows.append({"B": B, "fused_us": r["us_per_call"], "unfused_us": r["unfused_us_per_call"],
                      "cublas_gemms_us": r["cublas_gemms_us"], "speedup_vs_unfused": r["speedup_vs_unfused"],
+                     "recompute_us": r["recompute_us_per_call"],
+                     "recompute_speedup_vs_unfused": r["recompute_speedup_vs_unfused"],
                      "tflops_frac": r["roofline"]["frac"]})
         torch.cuda.empty_cache()
     return rows

@@ -204,10 +204,15 @@ sv_status spec_verify_lm_head_logits(const void *hidden, const void *weight, int
  * decoding -- draft, verify, repeat", section "Core algorithm").  The logits
  * are computed on the tensor cores and reduced in the product's epilogue to
  * the row statistics the method needs (max, sum of exp((z - max)/T), or the
- * argmax for greedy sequences, and the logit at each draft token), so they
- * never reach HBM; only the row pair at each sampled sequence's first
- * rejection is recomputed, as float32 logits, to draw the token.  The result
- * equals spec_verify_run on the float32 logits hidden @ weight^T.
+ * argmax for greedy sequences, and the logit at each draft token), so no pass
+ * over the logits reads them back.  To draw the token, the row pair at each
+ * sampled sequence's first rejection is needed: by default the verifier
+ * product's epilogue also writes every verifier row's float32 logits into the
+ * context's scratch, the draw reads back only the rows it needs, and the
+ * draft row is recomputed on the tensor cores (a second read of the draft
+ * head); with spec_verify_set_fused_logits(ctx, 0) no logits reach HBM and
+ * both rows are recomputed (a second read of both heads).  The result equals
+ * spec_verify_run on the float32 logits hidden @ weight^T.
  *
  *   target_hidden [B*(N+1), Kt] bf16, row b*(N+1)+i for position i
  *   target_weight [V, Kt] bf16 (row v: vocabulary entry v)
@@ -218,11 +223,15 @@ sv_status spec_verify_lm_head_logits(const void *hidden, const void *weight, int
  *   may be NULL.
  * Requires a context created with SV_F32 (SV_ERR_DTYPE otherwise; its V is the
  * vocabulary size), Kt and Kd multiples of 8, 16-byte aligned inputs.  The
- * first call (and a call with larger Kt or Kd) allocates its scratch
- * (cudaMalloc, about 8*(2*max_N+1)*max_B*ceil(V/256) + 8*max_B*V +
- * 2*max_B*(Kt+Kd) bytes) and therefore synchronises; later calls enqueue eight
- * launches on `stream` (six when greedy: no draft products) and allocate
- * nothing.
+ * first call (and a call with larger Kt or Kd, or after the mode changed)
+ * allocates its scratch and therefore synchronises: about
+ * 8*(2*max_N+1)*max_B*ceil(V/256) bytes of tile statistics, 4*max_B*V +
+ * 2*max_B*Kd bytes for the draft rows' recomputation, plus
+ * 4*(max_N+1)*max_B*V bytes of kept verifier logits, or 4*max_B*V +
+ * 2*max_B*Kt bytes when the verifier rows are recomputed too.  Later calls
+ * enqueue seven launches on `stream` when the verifier logits are kept (four
+ * when greedy: no draft product), eight when they are recomputed (six when
+ * greedy), and allocate nothing.
  */
 sv_status spec_verify_run_fused(spec_verify_ctx *ctx, const void *target_hidden, const void *target_weight,
                                 int Kt, const void *draft_hidden, const void *draft_weight, int Kd,
@@ -230,6 +239,16 @@ sv_status spec_verify_run_fused(spec_verify_ctx *ctx, const void *target_hidden,
                                 int greedy, int B, int N, int32_t *out_tokens, int32_t *num_accepted,
                                 float *target_row_stats, float *draft_row_stats, float *ratio_at_draft,
                                 void *stream);
+
+/*
+ * The fused path's handling of the verifier logits (spec_verify_run_fused):
+ * keep != 0 (the default) writes every verifier row's float32 logits from the
+ * statistics epilogue and reads back the rows it samples from; keep == 0
+ * keeps them out of HBM and recomputes the sampled rows (the draft rows are
+ * recomputed either way).  Takes effect at the next fused call, which then
+ * reallocates the scratch.  SV_ERR_INVALID_ARG for a null context.
+ */
+sv_status spec_verify_set_fused_logits(spec_verify_ctx *ctx, int keep);
 
 /*
  * Acceptance telemetry (how many drafts each verify accepted, the quantity

@@ -41,6 +41,7 @@ _SIGNATURES = [
     ("spec_verify_get_status", _I, [_P]),
     ("spec_verify_set_cluster_size", _I, [_P, _I]),
     ("spec_verify_cluster_size", _I, [_P, _I, _I]),
+    ("spec_verify_set_fused_logits", _I, [_P, _I]),
     ("spec_verify_error_string", ctypes.c_char_p, [_I]),
     ("spec_verify_destroy", None, [_P]),
     ("spec_verify_run_noalloc", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
@@ -122,6 +123,10 @@ def spec_verify_set_cluster_size(ctx, cluster_size: int) -> int:
 
 def spec_verify_cluster_size(ctx, B: int, N: int) -> int:
     return load().spec_verify_cluster_size(ctx, B, N)
+
+
+def spec_verify_set_fused_logits(ctx, keep: bool) -> int:
+    return load().spec_verify_set_fused_logits(ctx, int(bool(keep)))
 
 
 def spec_verify_error_string(status: int) -> str:
@@ -215,6 +220,15 @@ class SpecVerify:
 
     def cluster_size(self, B: int, N: int) -> int:
         return spec_verify_cluster_size(self.ctx, B, N)
+
+    def set_fused_logits(self, keep: bool):
+        """run_fused: write every verifier row's float32 logits from the
+        statistics epilogue and read back the sampled rows (keep=True, the
+        default), or keep them out of HBM and recompute the sampled verifier
+        rows; the sampled draft rows are recomputed either way."""
+        st = spec_verify_set_fused_logits(self.ctx, keep)
+        if st != SV_OK:
+            raise SpecVerifyError(st, "spec_verify_set_fused_logits")
 
     def status(self) -> int:
         return spec_verify_get_status(self.ctx)

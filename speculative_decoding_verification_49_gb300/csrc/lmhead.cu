@@ -23,10 +23,12 @@
 // the next tile accumulates into the other one.  A product with a single row
 // tile runs on single CTAs (M = 128, the whole weight tile, 4 stages).  The
 // epilogue either writes the logits as f32 (32 x 32 blocks staged in shared
-// memory and written by TMA tensor stores), or (the fused verify path) only
-// each row's statistics over the tile -- max and sum of exp2((z - max) *
+// memory and written by TMA tensor stores), or (the fused verify path) each
+// row's statistics over the tile -- max and sum of exp2((z - max) *
 // log2(e)/T), or max and argmax for greedy rows, and the logit at the row's
-// draft token -- so the logits never reach HBM.  The blocks of one
+// draft token -- and, when given a buffer, the f32 logits as well (the verify
+// then reads back only the rows it samples from; without one the logits never
+// reach HBM).  The blocks of one
 // 256-column weight slab come next to each other so that the units working at
 // the same time share that slab through L2.
 // Every mbarrier wait is bounded (2 s); a CTA that gives up sets the status
@@ -196,6 +198,35 @@ __device__ __forceinline__ void row_stats(uint32_t taddr, int n0, const LmParams
     }
 }
 
+// One epilogue warp's 32 rows of a finished tile (row r0 + lane for lane) out
+// as f32 logits: 32-column blocks through one of the warp's two staging
+// buffers in the 128-byte-swizzled layout of the output map, each written by
+// one TMA tensor store (blocks past M or N are clipped by the map).
+__device__ __forceinline__ void store_tile(uint32_t taddr, unsigned char *epi_raw, int q, int lane, int r0, int n0,
+                                           uint32_t &nstore, const CUtensorMap *tmC, const LmParams &p)
+{
+    for (int c0 = 0; c0 < kBN; c0 += 32, ++nstore) {
+        float v[32];
+        sv::tmem_ld32(taddr + (uint32_t)c0, v);
+        unsigned char *buf = epi_raw + (size_t)(q * 2 + (nstore & 1)) * kEpiBuf;
+        if (lane == 0)
+            sv::bulk_wait_read<1>();  // the store that last read this buffer is done with it
+        __syncwarp();
+        // row `lane`: 16-byte chunk j at chunk j ^ (row % 8) (128-byte swizzle)
+        float4 *rowp = reinterpret_cast<float4 *>(buf + lane * 128);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            rowp[j ^ (lane & 7)] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        sv::fence_async_shared();
+        __syncwarp();
+        if (lane == 0) {
+            if (r0 < p.M && n0 + c0 < p.N)
+                sv::tma_store_2d(tmC, n0 + c0, r0, buf);
+            sv::bulk_commit();  // one group per block, empty when nothing was stored
+        }
+    }
+}
+
 template <bool STATS, bool PAIR>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     sv_lmhead_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -348,28 +379,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * kBN);
             if constexpr (STATS) {
                 row_stats(taddr, n0, p, row);
+                if (p.tma_store)  // the logits too, from the same accumulator
+                    store_tile(taddr, epi_raw, q, lane, m0 + 32 * q, n0, nstore, &tmC, p);
             } else if (p.tma_store) {
-                const int r0 = m0 + 32 * q;  // the warp's first row
-                for (int c0 = 0; c0 < kBN; c0 += 32, ++nstore) {
-                    float v[32];
-                    sv::tmem_ld32(taddr + (uint32_t)c0, v);
-                    unsigned char *buf = epi_raw + (size_t)(q * 2 + (nstore & 1)) * kEpiBuf;
-                    if (lane == 0)
-                        sv::bulk_wait_read<1>();  // the store that last read this buffer is done with it
-                    __syncwarp();
-                    // row `lane`: 16-byte chunk j at chunk j ^ (row % 8) (128-byte swizzle)
-                    float4 *rowp = reinterpret_cast<float4 *>(buf + lane * 128);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        rowp[j ^ (lane & 7)] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-                    sv::fence_async_shared();
-                    __syncwarp();
-                    if (lane == 0) {
-                        if (r0 < p.M && n0 + c0 < p.N)
-                            sv::tma_store_2d(&tmC, n0 + c0, r0, buf);
-                        sv::bulk_commit();  // one group per block, empty when nothing was stored
-                    }
-                }
+                store_tile(taddr, epi_raw, q, lane, m0 + 32 * q, n0, nstore, &tmC, p);
             } else {
                 float *stg = epi + q * 32 * kEpiStride;
                 const int r0 = m0 + 32 * q;  // the warp's first row
@@ -538,11 +551,14 @@ sv_status launch(const void *hidden, const void *weight, int M, int V, int K, co
         return SV_ERR_CUDA;
     CUtensorMap ta, tb, tc;
     // the logits go out by tensor stores when their rows are 16-byte multiples
+    // (the statistics epilogue writes them only that way)
     LmParams q = p;
     q.tma_store = 0;
-    if (!STATS && p.logits && V % 4 == 0 && (reinterpret_cast<uintptr_t>(p.logits) & 15u) == 0 &&
+    if (p.logits && V % 4 == 0 && (reinterpret_cast<uintptr_t>(p.logits) & 15u) == 0 &&
         make_map_out(&tc, p.logits, M, V))
         q.tma_store = 1;
+    if (STATS && p.logits && !q.tma_store)
+        return SV_ERR_INVALID_ARG;
     // CTA pairs (one 256-row MMA) when there are two row tiles to pair
     const bool pair = (M + kBM - 1) / kBM >= 2;
     const int P = pair ? 2 : 1;
@@ -599,7 +615,7 @@ sv_status launch_logits(const void *hidden, const void *weight, int M, int V, in
 }
 
 sv_status launch_stats(const void *hidden, const void *weight, int M, int V, int K, const StatsArgs &a,
-                       cudaStream_t stream)
+                       cudaStream_t stream, float *logits)
 {
     if (M > 0 && V > 0 && (!a.part || !a.zgat || a.rows_per_seq < 1 || (a.N > 0 && !a.tokens)))
         return SV_ERR_INVALID_ARG;
@@ -607,6 +623,7 @@ sv_status launch_stats(const void *hidden, const void *weight, int M, int V, int
     p.M = M;
     p.N = V;
     p.K = K;
+    p.logits = logits;
     p.st = a;
     return launch<true>(hidden, weight, M, V, K, p, stream);
 }

@@ -34,8 +34,10 @@ inline int tiles(int V) { return (V + kTileN - 1) / kTileN; }
 // logits [M, V] f32
 sv_status launch_logits(const void *hidden, const void *weight, int M, int V, int K, float *logits,
                         cudaStream_t stream);
-// statistics only: the logits never leave tensor memory
+// statistics; with `logits` ([M, V] f32, 16-byte aligned, V % 4 == 0) the
+// logits as well, from the same accumulators; without it they never leave
+// tensor memory
 sv_status launch_stats(const void *hidden, const void *weight, int M, int V, int K, const StatsArgs &a,
-                       cudaStream_t stream);
+                       cudaStream_t stream, float *logits = nullptr);
 
 } // namespace svlm

@@ -94,21 +94,22 @@ struct SvParams {
     // tree verification (N is then the node count M; rows are per node)
     const int32_t *parent;  // [B][M+1]
     int32_t *path;          // [B][M+1] accepted node ids
-    // fused LM-head path: the sampling kernels read row b of compact
-    // [B, V] buffers instead of the verify inputs' rows (b, j)
-    int sample_compact;
+    // fused LM-head path: the sampling kernels read row b of a compact
+    // [B, V] buffer instead of the rows (b, j) of the full logits (target
+    // and draft rows separately)
+    int compact_t, compact_d;
     int B, N, V, greedy;
 };
 
 // Rows the sampling kernels read for sequence b stopping at position j.
 __device__ __forceinline__ size_t sample_trow(const SvParams &p, int b, int j)
 {
-    return p.sample_compact ? (size_t)b : (size_t)b * (p.N + 1) + j;
+    return p.compact_t ? (size_t)b : (size_t)b * (p.N + 1) + j;
 }
 
 __device__ __forceinline__ size_t sample_drow(const SvParams &p, int b, int j)
 {
-    return p.sample_compact ? (size_t)b : (size_t)b * p.N + j;
+    return p.compact_d ? (size_t)b : (size_t)b * p.N + j;
 }
 
 // Producer/consumer ring state in shared memory.
@@ -2449,17 +2450,21 @@ __global__ void __launch_bounds__(256) sv_fused_decide_kernel(const SvParams p, 
         atomicOr(&p.ws_err[b], errb);
 }
 
-// Hidden states of row pair j of every sequence into the compact buffers.
+// Hidden states of the rows at the first rejection j of every sequence into
+// the compact buffers: the draft row, and the verifier row when its logits
+// were not kept.
 __global__ void __launch_bounds__(256) sv_fused_gather_kernel(const SvParams p, const FusedArgs f)
 {
     sv::grid_dependency_wait();
     const int b = blockIdx.x, N = p.N;
     int j = __ldcg(&p.ws_first[b]);
     j = j > N ? N : j;
-    const uint4 *src = reinterpret_cast<const uint4 *>(f.hid_t + ((size_t)b * (N + 1) + j) * f.row_bytes_t);
-    uint4 *dst = reinterpret_cast<uint4 *>(f.hc_t + (size_t)b * f.row_bytes_t);
-    for (int v = threadIdx.x; v < f.row_bytes_t / 16; v += blockDim.x)
-        dst[v] = __ldg(src + v);
+    if (f.hid_t) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(f.hid_t + ((size_t)b * (N + 1) + j) * f.row_bytes_t);
+        uint4 *dst = reinterpret_cast<uint4 *>(f.hc_t + (size_t)b * f.row_bytes_t);
+        for (int v = threadIdx.x; v < f.row_bytes_t / 16; v += blockDim.x)
+            dst[v] = __ldg(src + v);
+    }
     if (j < N && f.hid_d) {
         const uint4 *sd = reinterpret_cast<const uint4 *>(f.hid_d + ((size_t)b * N + j) * f.row_bytes_d);
         uint4 *dd = reinterpret_cast<uint4 *>(f.hc_d + (size_t)b * f.row_bytes_d);
@@ -2512,6 +2517,8 @@ struct spec_verify_ctx {
     // fused LM-head path: scratch allocated on its first call (and when K grows)
     void *fz;
     int fz_Kt, fz_Kd;
+    int fz_keep;        // the statistics products also write every row's logits (else the rejected rows are recomputed)
+    int fz_keep_alloc;  // the mode the scratch was allocated for
     float *fz_part_t, *fz_part_d, *fz_zgat_t, *fz_zgat_d, *fz_lt, *fz_ld;
     unsigned char *fz_hc_t, *fz_hc_d;
     // profiling: events before kernel A, between the kernels and after kernel B
@@ -2732,7 +2739,8 @@ sv_status run_impl(spec_verify_ctx *ctx, const void *target, const void *draft, 
     prm.status = ctx->status;
     prm.parent = nullptr;
     prm.path = nullptr;
-    prm.sample_compact = 0;
+    prm.compact_t = 0;
+    prm.compact_d = 0;
     prm.B = B;
     prm.N = N;
     prm.V = ctx->V;
@@ -2909,19 +2917,26 @@ sv_status tree_run_impl(spec_verify_ctx *ctx, const void *target, const void *dr
 
 // Scratch of the fused path, sized for the context's limits and the widest
 // hidden states seen so far.
+// Scratch of the fused path: tile statistics and draft-token logits of every
+// row; the logits of every verifier row (kept) or, for the recomputation, of
+// one verifier row per sequence and its hidden state; the logits and hidden
+// state of one draft row per sequence (always recomputed).
 sv_status fused_scratch(spec_verify_ctx *ctx, int Kt, int Kd)
 {
-    if (ctx->fz && Kt <= ctx->fz_Kt && Kd <= ctx->fz_Kd)
+    if (ctx->fz && Kt <= ctx->fz_Kt && Kd <= ctx->fz_Kd && ctx->fz_keep == ctx->fz_keep_alloc)
         return SV_OK;
     Kt = Kt > ctx->fz_Kt ? Kt : ctx->fz_Kt;
     Kd = Kd > ctx->fz_Kd ? Kd : ctx->fz_Kd;
+    const bool keep = ctx->fz_keep != 0;
     const size_t nb = (size_t)(ctx->max_B > 0 ? ctx->max_B : 1);
     const size_t rows_t = nb * (size_t)(ctx->max_N + 1), rows_d = nb * (size_t)(ctx->max_N > 0 ? ctx->max_N : 1);
     const size_t tiles = (size_t)svlm::tiles(ctx->V);
     auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    const size_t lt_rows = keep ? rows_t : nb;
     const size_t o_pt = 0, o_pd = o_pt + up(rows_t * tiles * 8), o_zt = o_pd + up(rows_d * tiles * 8);
-    const size_t o_zd = o_zt + up(rows_t * 4), o_lt = o_zd + up(rows_d * 4), o_ld = o_lt + up(nb * ctx->V * 4);
-    const size_t o_ht = o_ld + up(nb * ctx->V * 4), o_hd = o_ht + up(nb * (size_t)Kt * 2);
+    const size_t o_zd = o_zt + up(rows_t * 4), o_lt = o_zd + up(rows_d * 4), o_ld = o_lt + up(lt_rows * ctx->V * 4);
+    const size_t o_ht = o_ld + up(nb * ctx->V * 4);
+    const size_t o_hd = o_ht + (keep ? 0 : up(nb * (size_t)Kt * 2));
     const size_t bytes = o_hd + up(nb * (size_t)(Kd > 0 ? Kd : 8) * 2);
     cudaFree(ctx->fz);
     ctx->fz = nullptr;
@@ -2937,10 +2952,11 @@ sv_status fused_scratch(spec_verify_ctx *ctx, int Kt, int Kd)
     ctx->fz_zgat_d = reinterpret_cast<float *>(z + o_zd);
     ctx->fz_lt = reinterpret_cast<float *>(z + o_lt);
     ctx->fz_ld = reinterpret_cast<float *>(z + o_ld);
-    ctx->fz_hc_t = z + o_ht;
+    ctx->fz_hc_t = keep ? nullptr : z + o_ht;
     ctx->fz_hc_d = z + o_hd;
     ctx->fz_Kt = Kt;
     ctx->fz_Kd = Kd;
+    ctx->fz_keep_alloc = ctx->fz_keep;
     return SV_OK;
 }
 
@@ -2971,11 +2987,14 @@ sv_status fused_run_impl(spec_verify_ctx *ctx, const void *ht, const void *wt, i
     if (r != SV_OK)
         return r;
     const int V = ctx->V;
+    const bool keep = ctx->fz_keep != 0;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
-    // 1. tile statistics of every verifier row and every draft row
+    // 1. tile statistics of every verifier row and every draft row (and, when
+    //    kept, the verifier rows' logits: that product is bound by its MMAs,
+    //    while the draft's, at its short K, would be bound by the stores)
     svlm::StatsArgs a{tokens, greedy ? nullptr : T, greedy ? 1 : 0, N, N + 1, ctx->fz_part_t, ctx->fz_zgat_t};
-    if ((r = svlm::launch_stats(ht, wt, B * (N + 1), V, Kt, a, st)) != SV_OK)
+    if ((r = svlm::launch_stats(ht, wt, B * (N + 1), V, Kt, a, st, keep ? ctx->fz_lt : nullptr)) != SV_OK)
         return r;
     if (need_draft) {
         svlm::StatsArgs ad{tokens, T, 0, N, N, ctx->fz_part_d, ctx->fz_zgat_d};
@@ -3004,7 +3023,8 @@ sv_status fused_run_impl(spec_verify_ctx *ctx, const void *ht, const void *wt, i
     prm.hist = ctx->hist;
     prm.hist_invalid = ctx->hist ? ctx->hist + ctx->max_N + 1 : nullptr;
     prm.status = ctx->status;
-    prm.sample_compact = 1;
+    prm.compact_t = keep ? 0 : 1;  // kept: the rows (b, j) of the full verifier logits
+    prm.compact_d = 1;
     prm.B = B;
     prm.N = N;
     prm.V = V;
@@ -3015,21 +3035,26 @@ sv_status fused_run_impl(spec_verify_ctx *ctx, const void *ht, const void *wt, i
     f.zgat_t = ctx->fz_zgat_t;
     f.zgat_d = ctx->fz_zgat_d;
     f.tiles = svlm::tiles(V);
-    f.hid_t = static_cast<const unsigned char *>(ht);
+    f.hid_t = keep ? nullptr : static_cast<const unsigned char *>(ht);
     f.hid_d = need_draft ? static_cast<const unsigned char *>(hd) : nullptr;
     f.hc_t = ctx->fz_hc_t;
     f.hc_d = ctx->fz_hc_d;
     f.row_bytes_t = Kt * 2;
     f.row_bytes_d = need_draft ? Kd * 2 : 0;
 
-    // 2. decisions; 3. the hidden rows at the first rejection
+    // 2. decisions
     const long long units = (long long)B * (N + 1);
     sv_fused_decide_kernel<<<(unsigned)((units + 7) / 8), 256, 0, st>>>(prm, f);
-    sv_fused_gather_kernel<<<(unsigned)B, 256, 0, st>>>(prm, f);
     if (cudaGetLastError() != cudaSuccess)
         return SV_ERR_CUDA;
-    // 4. their logits, recomputed on the tensor cores
-    if ((r = svlm::launch_logits(ctx->fz_hc_t, wt, B, V, Kt, ctx->fz_lt, st)) != SV_OK)
+    // 3. the hidden rows at the first rejection; 4. their logits, recomputed
+    //    (the draft row always, the verifier row when not kept)
+    if (!keep || need_draft) {
+        sv_fused_gather_kernel<<<(unsigned)B, 256, 0, st>>>(prm, f);
+        if (cudaGetLastError() != cudaSuccess)
+            return SV_ERR_CUDA;
+    }
+    if (!keep && (r = svlm::launch_logits(ctx->fz_hc_t, wt, B, V, Kt, ctx->fz_lt, st)) != SV_OK)
         return r;
     if (need_draft && (r = svlm::launch_logits(ctx->fz_hc_d, wd, B, V, Kd, ctx->fz_ld, st)) != SV_OK)
         return r;
@@ -3092,6 +3117,7 @@ sv_status spec_verify_create(spec_verify_ctx **out, int device, int max_B, int m
     }
 
     c->mass_ctas = (dtype == SV_BF16) ? mass_ctas<SV_BF16>(c->num_sms) : mass_ctas<SV_F32>(c->num_sms);
+    c->fz_keep = 1;  // the fused path keeps every row's logits unless told otherwise
 
     // workspace: hist[max_N+2] (u64) | first[nb] err[nb] tok[ntok] stats[4*ntok] ticket[ntok] |
     // slice[nb*S*8] status;
@@ -3254,6 +3280,14 @@ sv_status spec_verify_set_cluster_size(spec_verify_ctx *ctx, int cluster_size)
     if (cluster_size > nv)
         return SV_ERR_INVALID_ARG;
     ctx->cluster_override = cluster_size;
+    return SV_OK;
+}
+
+sv_status spec_verify_set_fused_logits(spec_verify_ctx *ctx, int keep)
+{
+    if (!ctx)
+        return SV_ERR_INVALID_ARG;
+    ctx->fz_keep = keep ? 1 : 0;
     return SV_OK;
 }
 

@@ -27,6 +27,7 @@ int use_every_entry_point(void *stream)
     st = spec_verify_get_status(ctx);
     st = spec_verify_set_cluster_size(ctx, 0);
     st = (sv_status)spec_verify_cluster_size(ctx, 256, 7);
+    st = spec_verify_set_fused_logits(ctx, 1);
     st = spec_verify_profile(ctx, 1);
     st = spec_verify_profile_read(ctx, &ms_rows, &ms_sample, &runs);
     st = spec_verify_run_noalloc(cv, cv, i32, f32, f32, 0, 256, 7, 151936, SV_BF16, i32, i32, stream);

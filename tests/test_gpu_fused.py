@@ -23,8 +23,9 @@ def _built():
     assert torch.cuda.is_available()
 
 
-def _check(w, greedy=None, seqs=None, ctx=None):
+def _check(w, greedy=None, seqs=None, ctx=None, keep=True):
     ctx = ctx or sv.SpecVerify(w.B, w.N, w.V, "f32")
+    ctx.set_fused_logits(keep)
     gpu = parity.run_gpu_fused(ctx, w, greedy=greedy, seqs=seqs)
     orc = parity.run_oracle_fused(w, seqs=seqs, threads=THREADS, greedy=greedy)
     rep = parity.compare_fused(w, gpu, orc, greedy=bool(greedy))
@@ -34,18 +35,20 @@ def _check(w, greedy=None, seqs=None, ctx=None):
     return rep, gpu
 
 
+@pytest.mark.parametrize("keep", [True, False], ids=["kept_logits", "recomputed_rows"])
 @pytest.mark.parametrize("name,seed", [("fused_small", 0), ("fused_small", 1), ("fused_mixed", 0)])
-def test_fused_parity(name, seed):
+def test_fused_parity(name, seed, keep):
     w = synth.make_fused_workload(name, seed=seed, device="cuda")
-    _check(w)
+    _check(w, keep=keep)
 
 
+@pytest.mark.parametrize("keep", [True, False], ids=["kept_logits", "recomputed_rows"])
 @pytest.mark.parametrize("V,Kt,Kd", [(4104, 200, 72), (1000, 64, 8), (20, 520, 136)])
-def test_fused_ragged_vocabulary_and_depth(V, Kt, Kd):
+def test_fused_ragged_vocabulary_and_depth(V, Kt, Kd, keep):
     """A last vocabulary tile shorter than 256 columns, and K not a multiple of
     the 64-wide stage (the tensor maps fill the missing columns with zeros)."""
     w = synth.make_fused_workload("fused_small", seed=V, device="cuda", V=V, Kt=Kt, Kd=Kd)
-    _check(w)
+    _check(w, keep=keep)
 
 
 def _random_fused_shapes(n=6, seed=77):
@@ -112,11 +115,35 @@ def test_fused_greedy_ties_take_the_lowest_column(c1, c2):
     assert ctx.status() == sv.SV_OK
 
 
-def test_fused_full_size_sampled():
+@pytest.mark.parametrize("keep", [True, False], ids=["kept_logits", "recomputed_rows"])
+def test_fused_full_size_sampled(keep):
     """The 256-sequence batch the benchmark times (Qwen-sized heads: V = 151936,
     Kt = 3584, Kd = 896); the oracle checks a spread of sequences."""
     w = synth.make_fused_workload("fused", seed=0, device="cuda")
-    _check(w, seqs=np.array([0, 1, 100, 255]))
+    _check(w, seqs=np.array([0, 1, 100, 255]), keep=keep)
+
+
+def test_fused_kept_and_recomputed_rows_agree_on_one_context():
+    """One context switched between the two ways of getting the sampled rows
+    (its scratch is reallocated at each switch): the same tokens outside the
+    band, call after call."""
+    w = synth.make_fused_workload("fused_mixed", seed=3, device="cuda")
+    ctx = sv.SpecVerify(w.B, w.N, w.V, "f32")
+    orc = parity.run_oracle_fused(w, threads=THREADS)
+    in_band = (np.nan_to_num(orc["accept_margin"], nan=np.inf) < parity.FUSED_BAND).any(axis=1) | \
+        (np.nan_to_num(orc["sample_margin"], nan=np.inf) < parity.FUSED_BAND)
+    runs = []
+    for keep in (True, False, True):
+        ctx.set_fused_logits(keep)
+        out, nacc = ctx.run_fused(w.target_hidden, w.target_weight, w.draft_hidden, w.draft_weight,
+                                  w.draft_tokens, w.uniforms, w.temperature)
+        torch.cuda.synchronize()
+        assert ctx.status() == sv.SV_OK
+        runs.append((out.cpu().numpy(), nacc.cpu().numpy()))
+    for out, nacc in runs[1:]:
+        same = (out == runs[0][0]).all(axis=1) & (nacc == runs[0][1])
+        assert (same | in_band).all()
+    assert np.array_equal(runs[0][0], runs[2][0]) and np.array_equal(runs[0][1], runs[2][1])
 
 
 def test_fused_matches_the_logit_path():
