@@ -62,10 +62,10 @@ typedef enum { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
 /*
  * Create a context on `device` for batches of up to max_B sequences with up
  * to max_N draft tokens over a vocabulary of V tokens stored as `dtype`.
- * Allocates a workspace of about 8*(max_N+2) + 8*max_B + 24*max_B*(max_N+1) +
+ * Allocates a workspace of about 8*(max_N+2) + 8*max_B + 28*max_B*(max_N+1) +
  * 32*max_B*ceil(V*elt/4 KiB) bytes (per-sequence first-rejection slots and
- * error flags; per-position argmax, row statistics and the ticket that pairs
- * a position's two rows; per-slice residual masses, the acceptance counters)
+ * error flags; per-position argmax, row statistics and the 64-bit cell that
+ * pairs a position's two rows; per-slice residual masses, the acceptance counters)
  * and one status word.  spec_verify_run and
  * spec_verify_tree_run allocate nothing later; spec_verify_run_fused adds its
  * own scratch on its first call.
@@ -311,7 +311,7 @@ void spec_verify_destroy(spec_verify_ctx *ctx);
  * a plug-in whose host framework owns every allocation, or a decode loop that
  * cannot afford the implicit device synchronisation and possible failure of a
  * cudaMalloc.  This entry point needs no context and allocates nothing: its
- * scratch is a fixed array of about 1.39 MiB compiled into the library, which
+ * scratch is a fixed array of about 1.45 MiB compiled into the library, which
  * every GPU that loads the library holds until the process exits.
  *
  * Arguments are those of spec_verify_run, with the vocabulary size V and the

@@ -85,7 +85,7 @@ struct SvParams {
     int *ws_first;    // [max_B] first rejected position, kNoReject if none
     int *ws_err;      // [max_B] error bits of the sequence
     int *ws_tok;      // [max_B*(max_N+1)] greedy argmax of each position
-    int *ws_ticket;   // [max_B*(max_N+1)] rows of the position normalised so far (one-row units), 0 between calls
+    unsigned long long *ws_xc;  // [max_B*(max_N+1)] (m, S) of a position's first normalised row (one-row units), 0 between calls
     float *ws_stats;  // [max_B*(max_N+1)][4] (mq, Sq, mp, Sp) of each position
     float *ws_slice;  // [max_B*slices][8] residual mass of each warp's share of a slice
     int *status;      // sticky error bits of the context
@@ -1162,13 +1162,26 @@ __global__ void __launch_bounds__(kThreads, 4) sv_row_kernel(const SvParams p)
                 p.dstats[drow * 2 + 1] = a.s;
             }
             if (decides) {
-                // the second of the position's two rows decides it
-                __threadfence();
-                if (atomicAdd(&p.ws_ticket[trow], 1) == 1) {
-                    __threadfence();
-                    p.ws_ticket[trow] = 0;
-                    const float *sq = p.ws_stats + trow * 4;
-                    const float mq = __ldcg(sq + 0), Sq = __ldcg(sq + 1), mp = __ldcg(sq + 2), Sp = __ldcg(sq + 3);
+                // The position's two rows meet in one 64-bit exchange: each
+                // swaps its (m, S) into the position's cell, and the row that
+                // finds the other's pair there is the second and decides.  The
+                // pair travels in the atomic, so no fence and no reload.
+                unsigned long long mine =
+                    ((unsigned long long)__float_as_uint(a.s) << 32) | (unsigned long long)__float_as_uint(a.m);
+                if (mine == 0ull)
+                    mine = 0x7fffffff7fffffffull;  // (0, 0) is not a valid pair either; 0 marks an empty cell
+                const unsigned long long other = atomicExch(&p.ws_xc[trow], mine);
+                if (other != 0ull) {
+                    p.ws_xc[trow] = 0ull;
+                    const float om = __uint_as_float((unsigned)(other & 0xffffffffull));
+                    const float os = __uint_as_float((unsigned)(other >> 32));
+                    const float mq = is_draft ? om : a.m, Sq = is_draft ? os : a.s;
+                    const float mp = is_draft ? a.m : om, Sp = is_draft ? a.s : os;
+                    float *sq = p.ws_stats + trow * 4;  // both rows' statistics, for the residual pass
+                    sq[0] = mq;
+                    sq[1] = Sq;
+                    sq[2] = mp;
+                    sq[3] = Sp;
                     const bool valid = isfinite(mq) && isfinite(Sq) && Sq > 0.0f && isfinite(mp) && isfinite(Sp) &&
                                        Sp > 0.0f;
                     if (p.ratio_at)
@@ -2511,7 +2524,8 @@ struct spec_verify_ctx {
     int clusters_tree[kMaxCluster + 1];  // the same for kernel A over tree nodes
     void *ws;
     int mass_ctas;                       // resident CTAs of the mass kernel (all SMs)
-    int *ws_first, *ws_err, *ws_tok, *ws_ticket, *status;
+    int *ws_first, *ws_err, *ws_tok, *status;
+    unsigned long long *ws_xc;
     float *ws_stats, *ws_slice;
     unsigned long long *hist;  // [max_N + 2]: accepted-draft histogram, then invalid
     // fused LM-head path: scratch allocated on its first call (and when K grows)
@@ -2731,7 +2745,7 @@ sv_status run_impl(spec_verify_ctx *ctx, const void *target, const void *draft, 
     prm.ws_first = ctx->ws_first;
     prm.ws_err = ctx->ws_err;
     prm.ws_tok = ctx->ws_tok;
-    prm.ws_ticket = ctx->ws_ticket;
+    prm.ws_xc = ctx->ws_xc;
     prm.ws_stats = ctx->ws_stats;
     prm.ws_slice = ctx->ws_slice;
     prm.hist = ctx->hist;
@@ -2858,7 +2872,7 @@ sv_status tree_run_impl(spec_verify_ctx *ctx, const void *target, const void *dr
     prm.ws_first = ctx->ws_first;
     prm.ws_err = ctx->ws_err;
     prm.ws_tok = ctx->ws_tok;
-    prm.ws_ticket = ctx->ws_ticket;
+    prm.ws_xc = ctx->ws_xc;
     prm.ws_stats = ctx->ws_stats;
     prm.ws_slice = ctx->ws_slice;
     prm.hist = ctx->hist;
@@ -3017,7 +3031,7 @@ sv_status fused_run_impl(spec_verify_ctx *ctx, const void *ht, const void *wt, i
     prm.ws_first = ctx->ws_first;
     prm.ws_err = ctx->ws_err;
     prm.ws_tok = ctx->ws_tok;
-    prm.ws_ticket = ctx->ws_ticket;
+    prm.ws_xc = ctx->ws_xc;
     prm.ws_stats = ctx->ws_stats;
     prm.ws_slice = ctx->ws_slice;
     prm.hist = ctx->hist;
@@ -3119,14 +3133,15 @@ sv_status spec_verify_create(spec_verify_ctx **out, int device, int max_B, int m
     c->mass_ctas = (dtype == SV_BF16) ? mass_ctas<SV_BF16>(c->num_sms) : mass_ctas<SV_F32>(c->num_sms);
     c->fz_keep = 1;  // the fused path keeps every row's logits unless told otherwise
 
-    // workspace: hist[max_N+2] (u64) | first[nb] err[nb] tok[ntok] stats[4*ntok] ticket[ntok] |
+    // workspace: hist[max_N+2] (u64) | first[nb] err[nb] tok[ntok] stats[4*ntok] | xc[ntok] (u64) |
     // slice[nb*S*8] status;
     // the slice shares start on a 256-byte boundary (kernel C reads them as float4)
     const size_t nb = (size_t)(max_B > 0 ? max_B : 1);
     const size_t ntok = nb * (size_t)(max_N + 1);
     const size_t nslice = nb * (size_t)residual_slices(V, dtype) * kConsWarps;
     const size_t hist_ints = ((size_t)(max_N + 2) * 2 + 63) / 64 * 64;
-    const size_t slice_off = (hist_ints + 2 * nb + 6 * ntok + 63) / 64 * 64;
+    const size_t xc_off = (hist_ints + 2 * nb + 5 * ntok + 1) / 2 * 2;  // 8-byte aligned
+    const size_t slice_off = (xc_off + 2 * ntok + 63) / 64 * 64;
     const size_t bytes = sizeof(int) * (slice_off + nslice + 1);
     if (cudaMalloc(&c->ws, bytes) != cudaSuccess) {
         cudaGetLastError();
@@ -3139,7 +3154,7 @@ sv_status spec_verify_create(spec_verify_ctx **out, int device, int max_B, int m
     c->ws_err = w + nb;
     c->ws_tok = w + 2 * nb;
     c->ws_stats = reinterpret_cast<float *>(w + 2 * nb + ntok);
-    c->ws_ticket = w + 2 * nb + 5 * ntok;
+    c->ws_xc = reinterpret_cast<unsigned long long *>(static_cast<int *>(c->ws) + xc_off);
     c->ws_slice = reinterpret_cast<float *>(static_cast<int *>(c->ws) + slice_off);
     c->status = static_cast<int *>(c->ws) + slice_off + nslice;
     if (cudaMemset(c->ws, 0, bytes) != cudaSuccess || cudaMemset(c->ws_first, 0x7f, sizeof(int) * nb) != cudaSuccess ||
@@ -3424,9 +3439,10 @@ namespace {
 constexpr int kNoAllocMaxB = 2048;        // sequences per call
 constexpr int kNoAllocMaxUnits = 16384;   // B*(N+1) verified positions per call
 constexpr int kNoAllocMaxSlices = 32768;  // B*ceil(V*elt/4 KiB) residual slices per call
-constexpr int kNoAllocSliceOff = 2 * kNoAllocMaxB + 6 * kNoAllocMaxUnits;  // a multiple of 64 ints
+constexpr int kNoAllocXcOff = 2 * kNoAllocMaxB + 5 * kNoAllocMaxUnits;  // even: 8-byte aligned
+constexpr int kNoAllocSliceOff = kNoAllocXcOff + 2 * kNoAllocMaxUnits;  // a multiple of 64 ints
 static_assert(kNoAllocSliceOff % 64 == 0, "slice shares must start on a 256-byte boundary");
-constexpr int kNoAllocInts = kNoAllocSliceOff + 8 * kNoAllocMaxSlices + 1;  // about 1.39 MiB
+constexpr int kNoAllocInts = kNoAllocSliceOff + 8 * kNoAllocMaxSlices + 1;  // about 1.45 MiB
 // the 256-sequence Qwen-vocabulary batch (V = 151936 bf16: 75 slices a row) fits
 static_assert(256 * 75 <= kNoAllocMaxSlices, "the scratch holds a 256 x 151936 bf16 batch");
 constexpr int kNoAllocMaxDevices = 64;
@@ -3529,7 +3545,7 @@ extern "C" sv_status spec_verify_run_noalloc(const void *target_logits, const vo
     c.ws_err = w + kNoAllocMaxB;
     c.ws_tok = w + 2 * kNoAllocMaxB;
     c.ws_stats = reinterpret_cast<float *>(w + 2 * kNoAllocMaxB + kNoAllocMaxUnits);
-    c.ws_ticket = w + 2 * kNoAllocMaxB + 5 * kNoAllocMaxUnits;
+    c.ws_xc = reinterpret_cast<unsigned long long *>(w + kNoAllocXcOff);
     c.ws_slice = reinterpret_cast<float *>(w + kNoAllocSliceOff);
     c.status = w + kNoAllocSliceOff + 8 * kNoAllocMaxSlices;
 
