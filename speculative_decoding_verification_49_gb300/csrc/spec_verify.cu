@@ -1276,10 +1276,9 @@ __device__ __forceinline__ void sample_shifts(SeqSample &s, float cf)
         residual_shift(s.mp, s.isp, cf, s.mp, s.isp);
 }
 
-// cf (log2(e)/T, one double division) and with it the shifts are left to the
-// caller (sample_shifts) when with_cf is false: then mq, isq, mp, isp hold the
-// raw statistics (m, S) and cf holds T.
-__device__ __forceinline__ bool sequence_sample(const SvParams &p, int b, SeqSample &s, bool with_cf = true)
+// The first half of sequence_sample: j, the residual mode and whether b is
+// sampled (T in s.cf).  The rows to read are known from here on.
+__device__ __forceinline__ bool sequence_head(const SvParams &p, int b, SeqSample &s)
 {
     float T;
     const int mode = sequence_mode(p, b, T);
@@ -1287,20 +1286,27 @@ __device__ __forceinline__ bool sequence_sample(const SvParams &p, int b, SeqSam
     j = j > p.N ? p.N : j;
     const int err = __ldcg(&p.ws_err[b]);
     s.j = j;
-    if (err || mode != MODE_SAMPLED)
-        return false;
-    const float *st = p.ws_stats + ((size_t)b * (p.N + 1) + j) * 4;
+    s.cf = T;
     s.res_mode = (j < p.N) ? RES_DIFF : RES_Q;
+    return !err && mode == MODE_SAMPLED;
+}
+
+// The second half: position j's raw statistics (m, S) ...
+__device__ __forceinline__ void sequence_stats(const SvParams &p, int b, SeqSample &s)
+{
+    const int j = s.j;
+    const float *st = p.ws_stats + ((size_t)b * (p.N + 1) + j) * 4;
     s.mq = __ldcg(st + 0);
     s.isq = __ldcg(st + 1);
     s.mp = (j < p.N) ? __ldcg(st + 2) : 0.0f;
     s.isp = (j < p.N) ? __ldcg(st + 3) : 1.0f;
-    s.uN = p.u[(size_t)b * (p.N + 1) + p.N];
-    if (with_cf)
-        sample_shifts(s, (float)(kLog2e / (double)T));
-    else
-        s.cf = T;
-    return true;
+}
+
+// ... and as residual_vec's shifts and scales (T in s.cf on entry).
+__device__ __forceinline__ void sequence_tail(const SvParams &p, int b, SeqSample &s)
+{
+    sequence_stats(p, b, s);
+    sample_shifts(s, (float)(kLog2e / (double)s.cf));
 }
 
 template <int DT>
@@ -1329,14 +1335,15 @@ __global__ void __launch_bounds__(kThreads, 4) sv_mass_kernel(const SvParams p)
         if (lane == 0) {
             uint32_t g = 0;
             int cur_b = -1;
-            bool cur_ok = false;
+            bool cur_ok = false, have_stats = false;
             SeqSample sq{};
             for (long long tt = t_begin; tt < t_end && !ctl.ring.abort; ++tt) {
                 const int b = (int)(tt / T);
                 const int t = (int)(tt - (long long)b * T);
                 if (b != cur_b) {
                     cur_b = b;
-                    cur_ok = sequence_sample(p, b, sq);
+                    cur_ok = sequence_head(p, b, sq);
+                    have_stats = false;
                 }
                 if (!cur_ok)
                     continue;
@@ -1345,6 +1352,25 @@ __global__ void __launch_bounds__(kThreads, 4) sv_mass_kernel(const SvParams p)
                                            kWaitLimitNs)) {
                     ctl.ring.abort = 1;
                     break;
+                }
+                // the copies first (the rows are known from j), then the
+                // statistics they are summed with, loaded while the copies fly,
+                // then the producer's arrival
+                const uint4 *tsrc = static_cast<const uint4 *>(p.target) + sample_trow(p, b, sq.j) * (size_t)NV;
+                const uint4 *dsrc = (sq.res_mode == RES_DIFF)
+                                        ? static_cast<const uint4 *>(p.draft) + sample_drow(p, b, sq.j) * (size_t)NV
+                                        : nullptr;
+                const int nvec = min(kTileVecsM, NV - t * kTileVecsM);
+                const uint32_t bytes = static_cast<uint32_t>(nvec) * 16u;
+                sv::mbar_expect_tx(&ctl.ring.full[s], dsrc ? 2u * bytes : bytes);
+                unsigned char *stage = ring + s * (2 * kTileBytesM);
+                sv::bulk_g2s(stage, tsrc + (size_t)t * kTileVecsM, bytes, &ctl.ring.full[s]);
+                if (dsrc)
+                    sv::bulk_g2s(stage + kTileBytesM, dsrc + (size_t)t * kTileVecsM, bytes, &ctl.ring.full[s]);
+                ctl.ring.last_g[s] = static_cast<int>(g);
+                if (!have_stats) {
+                    sequence_tail(p, b, sq);
+                    have_stats = true;
                 }
                 TileMeta &m = ctl.meta[s];
                 m.b = b;
@@ -1355,18 +1381,7 @@ __global__ void __launch_bounds__(kThreads, 4) sv_mass_kernel(const SvParams p)
                 m.mp = sq.mp;
                 m.isp = sq.isp;
                 m.cf = sq.cf;
-                const uint4 *tsrc = static_cast<const uint4 *>(p.target) + sample_trow(p, b, sq.j) * (size_t)NV;
-                const uint4 *dsrc = (sq.res_mode == RES_DIFF)
-                                        ? static_cast<const uint4 *>(p.draft) + sample_drow(p, b, sq.j) * (size_t)NV
-                                        : nullptr;
-                const int nvec = min(kTileVecsM, NV - t * kTileVecsM);
-                const uint32_t bytes = static_cast<uint32_t>(nvec) * 16u;
-                sv::mbar_arrive_expect_tx(&ctl.ring.full[s], dsrc ? 2u * bytes : bytes);
-                unsigned char *stage = ring + s * (2 * kTileBytesM);
-                sv::bulk_g2s(stage, tsrc + (size_t)t * kTileVecsM, bytes, &ctl.ring.full[s]);
-                if (dsrc)
-                    sv::bulk_g2s(stage + kTileBytesM, dsrc + (size_t)t * kTileVecsM, bytes, &ctl.ring.full[s]);
-                ctl.ring.last_g[s] = static_cast<int>(g);
+                sv::mbar_arrive(&ctl.ring.full[s]);
                 ++g;
             }
             // end marker (no bytes): consumers stop at it
@@ -1706,8 +1721,11 @@ __device__ int draw_token(PickShared &sh, SeqSample &sq, const uint4 *tsrc, cons
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool cons = tid < kConsThreads;
     float r[VE];
+    bool shifted = false;  // sq holds the raw statistics until the first residual needs them
     for (int attempt = 0; attempt < 2; ++attempt) {
         if (attempt == 1) {
+            sample_shifts(sq, sh.cf);
+            shifted = true;
             sq.res_mode = RES_Q;
             for (int sl = 0; sl < S; ++sl) {
                 const float part = cons ? slice_thread_mass<DT>(tsrc, nullptr, sl, NV, tid, sq, r) : 0.0f;
@@ -1737,9 +1755,23 @@ __device__ int draw_token(PickShared &sh, SeqSample &sq, const uint4 *tsrc, cons
         __syncthreads();
     }
     const int ss = sh.sstar;
+    // the chosen slice's vectors are loaded before the statistics are first used
+    const int vec = ss * kSliceVecs + tid;
+    const bool in = cons && vec < NV;
+    uint4 vt = make_uint4(0, 0, 0, 0), vd = make_uint4(0, 0, 0, 0);
+    if (in) {
+        vt = __ldcg(tsrc + vec);
+        if (sq.res_mode == RES_DIFF)
+            vd = __ldcg(dsrc + vec);
+    }
+    if (!shifted)
+        sample_shifts(sq, sh.cf);
     float part = 0.0f;
-    if (cons) {
-        part = slice_thread_mass<DT>(tsrc, sq.res_mode == RES_DIFF ? dsrc : nullptr, ss, NV, tid, sq, r);
+    if (in) {
+        residual_vec<DT>(vt, vd, sq.res_mode, sq.mq, sq.isq, sq.mp, sq.isp, sq.cf, r);
+#pragma unroll
+        for (int e = 0; e < VE; ++e)
+            part = __fadd_rn(part, r[e]);
     } else {
 #pragma unroll
         for (int e = 0; e < VE; ++e)
@@ -1774,12 +1806,14 @@ __global__ void __launch_bounds__(kPickThreads) sv_pick_kernel(const SvParams p)
     const float *shares = p.ws_slice + (size_t)b * S * kConsWarps;
     const fx_t my_mass = (tid < S) ? slice_share_total(shares, tid) : 0ull;
     SeqSample sq{};
-    const bool sampled = sequence_sample(p, b, sq, /*with_cf=*/false);  // sq.cf holds T
+    // u is read only where it is required ([B, N+1] unless the whole call is greedy)
+    sq.uN = (!p.greedy && p.u) ? p.u[(size_t)b * (N + 1) + N] : 0.0f;
+    const bool sampled = sequence_head(p, b, sq);  // sq.cf holds T
     if (tid == 0)
         sh.cf = sampled ? (float)(kLog2e / (double)sq.cf) : 0.0f;  // log2(e)/T, once
-    __syncthreads();
     if (sampled)
-        sample_shifts(sq, sh.cf);
+        sequence_stats(p, b, sq);  // in flight until the chosen slice's vectors are loaded (draw_token)
+    __syncthreads();
     const int j = sq.j;
     if (!sampled) {
         emit_unsampled(p, b, j, my_tok);
