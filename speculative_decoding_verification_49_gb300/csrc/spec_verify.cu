@@ -887,9 +887,9 @@ __global__ void __launch_bounds__(kThreads, 4) sv_rows_kernel(const SvParams p)
 // positions read half as much) and the last wave of large ones do not end on
 // a tail of two-row units.  Each ring stage holds two consecutive 8 KiB tiles
 // of the one row (the same 16 KiB in flight per stage, the same 32 elements
-// per thread and stage).  A position's two rows meet through the workspace:
-// each CTA writes its row's statistics, takes a ticket, and the second one
-// decides with kernel A's arithmetic.  Units run position by position in
+// per thread and stage).  A position's two rows meet in one 64-bit workspace
+// cell: each CTA swaps its row's (m, S) in, and the one that finds the other
+// row's pair there decides with kernel A's arithmetic.  Units run position by position in
 // descending order (position 0 last, as in kernel A), a sequence's two rows
 // next to each other; a draft-row unit of a greedy sequence (or of a tree node
 // without children) reads nothing and leaves.  PACKED (chains of at most
@@ -3462,7 +3462,7 @@ void spec_verify_destroy(spec_verify_ctx *ctx)
 // scratch lives in the file-scope array below instead of a context
 // workspace: per sequence the first-rejection slot and the error bits, per
 // verified position the greedy argmax, the row statistics (mq, Sq, mp, Sp)
-// and the ticket that pairs the position's two row CTAs, per 4 KiB slice of
+// and the 64-bit cell that pairs the position's two row CTAs, per 4 KiB slice of
 // a sampled row pair the eight warp shares of its residual mass, and one
 // status word.  The array is part of the module image: every GPU that
 // loads this library holds it until the process exits, and nothing is ever

@@ -28,3 +28,17 @@ def test_reference_arm_prints_one_contract_line():
     assert e["value"] == d["value"] and e["unit"] == d["unit"]
     assert e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0
     assert "workload" in d["config"]
+
+
+def test_kernel_digest_ignores_comments_only():
+    """The digest that vouches for the committed DRAM counters changes with
+    the code, not with its comments or layout."""
+    sys.path.insert(0, ROOT)
+    import bench
+    base = 'int f(int x) { // twice\n  return 2 * x; /* doubled */ }\nconst char *s = "a // b /* c */";\n'
+    assert bench._code_only(base) == bench._code_only(base.replace("// twice", "// two times"))
+    assert bench._code_only(base) == bench._code_only(base.replace("/* doubled */", "").replace("  ", "    "))
+    assert bench._code_only(base) != bench._code_only(base.replace("2 * x", "3 * x"))
+    assert '"a // b /* c */"' in bench._code_only(base)  # literals are code
+    assert bench._code_only("char c = '\"'; int y; // z") == "char c = '\"'; int y;"
+    assert len(bench.kernel_digest()) == 16
