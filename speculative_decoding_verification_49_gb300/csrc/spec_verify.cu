@@ -1263,8 +1263,9 @@ struct CtlM {
 
 constexpr size_t kSmemM = kRingBytesM + sizeof(CtlM);
 
-// Residual-mode parameters of sequence b, or false when b is not sampled:
-// (mq, isq, mp, isp) are residual_vec's shifts and scales (residual_shift).
+// Residual-mode parameters of a sampled sequence: j, the residual mode, and
+// (mq, isq, mp, isp) as the raw statistics (m, S) of position j's rows until
+// sample_shifts turns them into residual_vec's shifts and scales.
 struct SeqSample {
     int j, res_mode;
     float mq, isq, mp, isp, cf, uN;
@@ -1279,8 +1280,8 @@ __device__ __forceinline__ void sample_shifts(SeqSample &s, float cf)
         residual_shift(s.mp, s.isp, cf, s.mp, s.isp);
 }
 
-// The first half of sequence_sample: j, the residual mode and whether b is
-// sampled (T in s.cf).  The rows to read are known from here on.
+// Sequence b's first rejection j, its residual mode and whether it is sampled
+// (T in s.cf); the rows to read are known from here on.
 __device__ __forceinline__ bool sequence_head(const SvParams &p, int b, SeqSample &s)
 {
     float T;
